@@ -1,0 +1,393 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test checks one oracle function against what the mathematics or the
+IEEE-754 definitions fix: brute force in plain Python on tiny inputs (with
+``struct`` doing the fp32 / fp16 roundings, independently of numpy), exact
+closed forms, a lossless special case in which the int8 layer must reproduce
+the exact product, and error bounds.  A planted mistake in the oracle (a
+dropped term, a wrong scale, a transposed operand) fails at least one of them.
+"""
+import math
+import struct
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+
+
+# ---------------------------------------------------------------------------
+# plain-Python IEEE helpers (independent of numpy)
+# ---------------------------------------------------------------------------
+
+def f32(x: float) -> float:
+    """Round a Python float (binary64) to binary32, nearest-even."""
+    return struct.unpack("<f", struct.pack("<f", x))[0]
+
+
+def f16(x: float) -> float:
+    """Round a Python float to binary16, nearest-even (struct 'e')."""
+    try:
+        return struct.unpack("<e", struct.pack("<e", x))[0]
+    except OverflowError:
+        return math.copysign(math.inf, x)
+
+
+def py_codes(row, absmax):
+    """round_half_even(fp32(x) * fp32(127 / absmax)); fp32 division and
+    multiply each done exactly in binary64 and rounded once (binary64 has
+    more than 2*24+2 bits, so this equals the fp32 operation)."""
+    if absmax == 0.0:
+        return [0] * len(row)
+    s = f32(127.0 / absmax)
+    return [max(-127, min(127, round(f32(x * s)))) for x in row]   # round(): half-even
+
+
+# ---------------------------------------------------------------------------
+# casts
+# ---------------------------------------------------------------------------
+
+def test_f16_cast_roundtrip_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    h = bits.view(np.float16)
+    fin = np.isfinite(h)
+    back = O.cast_f16(h.astype(np.float32)[fin], O.F32)
+    assert np.array_equal(back.view(np.uint16), bits[fin])
+
+
+def test_f16_cast_midpoints_round_to_even():
+    pos = np.arange(0, 0x7BFF, dtype=np.uint16).view(np.float16).astype(np.float64)
+    a, b = pos[:-1], pos[1:]
+    mid = (a + b) / 2                           # exact in binary64 and binary32
+    got = O.cast_f16(mid.astype(np.float32), O.F32).view(np.uint16).astype(np.int64)
+    lo = np.arange(0, 0x7BFE, dtype=np.int64)
+    want = np.where(lo % 2 == 0, lo, lo + 1)    # the even neighbour
+    assert np.array_equal(got, want)
+    # and a hair either side of the midpoint goes to the nearer neighbour
+    eps = (b - a) / 8
+    assert np.array_equal(O.cast_f16((mid - eps).astype(np.float32), O.F32).view(np.uint16), lo.astype(np.uint16))
+    assert np.array_equal(O.cast_f16((mid + eps).astype(np.float32), O.F32).view(np.uint16), (lo + 1).astype(np.uint16))
+
+
+def test_f16_cast_edges():
+    vals = np.array([65504.0, 65519.99, 65520.0, 1e9, -65520.0, 2.0 ** -24,
+                     2.0 ** -25, 1.5 * 2.0 ** -25, -0.0], dtype=np.float32)
+    got = O.cast_f16(vals, O.F32).astype(np.float64)
+    want = [65504.0, 65504.0, math.inf, math.inf, -math.inf, 2.0 ** -24, 0.0,
+            2.0 ** -24, 0.0]
+    assert list(got) == want
+    assert np.signbit(got[-1])
+
+
+def test_f16_cast_matches_struct_on_random():
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 12, 20000))).astype(np.float32)
+    got = O.cast_f16(x, O.F32).astype(np.float64)
+    want = [f16(float(v)) for v in x]
+    assert list(got) == want
+
+
+def _all_bf16_pos():
+    b = np.arange(0, 0x7F80, dtype=np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def test_bf16_rounding_bruteforce():
+    grid = _all_bf16_pos()
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal(4000) * np.exp(rng.uniform(-90, 88, 4000))
+    # add exact midpoints between neighbours (ties) and values near the top
+    i = rng.integers(1, len(grid) - 2, 500)
+    x = np.concatenate([x, (grid[i] + grid[i + 1]) / 2, -(grid[i] + grid[i + 1]) / 2,
+                        [3.3895313892515355e38, 3.39e38, 3.4e38, 2.0 ** -133, 2.0 ** -134, 0.0]])
+    got = O.widen(O.round_to(x, O.BF16), O.BF16)
+    for v, g in zip(x, got):
+        a = abs(v)
+        j = np.searchsorted(grid, a)            # grid[j-1] < a <= grid[j]
+        if j >= len(grid):
+            top = grid[-1]
+            half_up = top + (top - grid[-2]) / 2
+            want = math.inf if a >= half_up else top
+        elif grid[j] == a:
+            want = a
+        else:
+            lo, hi = grid[j - 1], grid[j]
+            if a - lo < hi - a:
+                want = lo
+            elif hi - a < a - lo:
+                want = hi
+            else:
+                want = lo if (j - 1) % 2 == 0 else hi
+        assert g == math.copysign(want, v), (v, g, want)
+
+
+def test_bf16_widen_is_exact():
+    bits = np.arange(0, 65536, dtype=np.uint32).astype(np.uint16)
+    v = O.widen(bits, O.BF16)
+    fin = np.isfinite(v)
+    assert np.array_equal(O.round_to(v[fin], O.BF16), bits[fin])
+
+
+# ---------------------------------------------------------------------------
+# outlier columns
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("thr", [6.0, 0.5, 2.75])
+def test_outlier_columns_bruteforce(thr):
+    rng = np.random.default_rng(3)
+    A = (rng.standard_normal((7, 11)) * 3).astype(np.float16)
+    A[2, 4] = thr            # equal to the threshold: not an outlier by itself
+    A[5, 9] = -np.float16(thr) * 2
+    got = O.outlier_columns(A, thr)
+    want = [k for k in range(11) if any(abs(float(A[m, k])) > thr for m in range(7))]
+    assert got.tolist() == want
+    assert 9 in want
+
+
+def test_outlier_columns_disabled():
+    A = (np.ones((3, 4)) * 100).astype(np.float16)
+    for thr in (math.inf, 0.0, -1.0, math.nan):
+        assert O.outlier_columns(A, thr).size == 0
+    assert O.outlier_columns(A[:0], 6.0).size == 0
+
+
+def test_outlier_columns_contain_heavy():
+    spec = W.WORKLOADS["linear_4096"].layers[0]
+    spec = W.LayerSpec(256, 512, 8, torch.float16, 0.02, 0.01, 0.01, 20.0, 6.0)
+    A = W.activation(spec, 0).numpy()
+    heavy = W.heavy_columns(512, 0.01, 0 + W.OFF_HEAVY).numpy()
+    idx = O.outlier_columns(A, 6.0)
+    assert set(heavy.tolist()) <= set(idx.tolist())
+    assert np.all(np.diff(idx) > 0)
+
+
+# ---------------------------------------------------------------------------
+# row quantization
+# ---------------------------------------------------------------------------
+
+def test_quantize_rows_bruteforce():
+    rng = np.random.default_rng(4)
+    A = (rng.standard_normal((8, 9)) * 2).astype(np.float16)
+    A[3, :] = 0                    # zero row
+    A[6, :] = 0
+    A[6, 2] = 50                   # only an outlier value: scale 0 after removal
+    idx = np.array([2, 7], dtype=np.int32)
+    SCA, Aq, subA = O.quantize_rows(A, idx)
+    for m in range(8):
+        row = [0.0 if k in (2, 7) else float(A[m, k]) for k in range(9)]
+        am = max(abs(v) for v in row)
+        assert SCA[m] == am
+        assert Aq[m].tolist() == py_codes(row, am)
+        assert subA[m].tolist() == [float(A[m, 2]), float(A[m, 7])]
+
+
+def test_quantize_ties_round_half_even():
+    # absmax = 127 * 2^-4 -> s = 16 exactly; x * s lands on .5 ties
+    u = 2.0 ** -4
+    row = np.array([[127 * u, 2.5 * u, 3.5 * u, -2.5 * u, 0.5 * u, -1.5 * u, 126.5 * u]],
+                   dtype=np.float16)
+    SCA, Aq, _ = O.quantize_rows(row, np.zeros(0, np.int32))
+    assert SCA[0] == np.float32(127 * u)
+    assert Aq[0].tolist() == [127, 2, 4, -2, 0, -2, 126]
+
+
+def test_quantize_rows_invariants():
+    spec = W.LayerSpec(64, 300, 8, torch.float16, 0.02, 0.01, 0.01, 20.0, 6.0)
+    A16 = O.cast_f16(W.activation(spec, 5).numpy(), O.F16)
+    idx = O.outlier_columns(A16, 6.0)
+    SCA, Aq, subA = O.quantize_rows(A16, idx)
+    assert Aq.dtype == np.int8 and Aq.min() >= -127 and Aq.max() <= 127
+    assert np.all(Aq[:, idx] == 0)
+    X = A16.astype(np.float64)
+    X[:, idx] = 0
+    am = np.argmax(np.abs(X), axis=1)
+    assert np.all(np.abs(Aq[np.arange(64), am]) == 127)
+    err = np.abs(X - Aq.astype(np.float64) * SCA[:, None].astype(np.float64) / 127)
+    assert np.all(err <= SCA[:, None] / 254 * (1 + 2.0 ** -20))
+    assert np.array_equal(subA, A16[:, idx])
+
+
+# ---------------------------------------------------------------------------
+# weights
+# ---------------------------------------------------------------------------
+
+def test_quantize_weight_bruteforce_fp32_input():
+    rng = np.random.default_rng(6)
+    Wf = (rng.standard_normal((5, 7)) * 0.02).astype(np.float32)
+    Wf[4] = 0.0
+    CB, SCB = O.quantize_weight(Wf, O.F32)
+    for n in range(5):
+        row = [f16(float(v)) for v in Wf[n]]          # cast to fp16 first
+        am = max(abs(v) for v in row)
+        assert SCB[n] == am
+        assert CB[n].tolist() == py_codes(row, am)
+
+
+def test_dequant_weight_closed_forms():
+    # fp32(1/127) = 2^-7 (1 + 2^-7 + 2^-14 + 2^-21) and 127 * fp32(1/127) = 1 - 2^-28
+    assert float(np.float32(1 / 127)) == 2.0 ** -7 * (1 + 2.0 ** -7 + 2.0 ** -14 + 2.0 ** -21)
+    CB = np.array([[127, 1, -127, 0]], dtype=np.int8)
+    SCB = np.array([127.0], dtype=np.float32)       # f = fp32(1 - 2^-28) = 1
+    assert O.dequant_weight(CB, SCB).astype(np.float64).tolist() == [[127.0, 1.0, -127.0, 0.0]]
+    SCB = np.array([0.5], dtype=np.float32)
+    # f = 2^-8 (1 + 2^-7 + 2^-14 + 2^-21); 127 f = 0.5 (1 - 2^-28) -> fp32 0.5
+    assert O.dequant_weight(CB, SCB)[0, 0] == np.float16(0.5)
+
+
+def test_dequant_weight_bruteforce():
+    rng = np.random.default_rng(7)
+    CB = rng.integers(-127, 128, (6, 9)).astype(np.int8)
+    SCB = (np.abs(rng.standard_normal(6)) * 0.05 + 1e-3).astype(np.float32)
+    got = O.dequant_weight(CB, SCB).astype(np.float64)
+    c = f32(1.0 / 127.0)
+    for n in range(6):
+        f = f32(float(SCB[n]) * c)
+        for k in range(9):
+            assert got[n, k] == f16(f32(float(CB[n, k]) * f))
+
+
+# ---------------------------------------------------------------------------
+# integer GEMM
+# ---------------------------------------------------------------------------
+
+def test_int_gemm_bruteforce_and_int64():
+    rng = np.random.default_rng(8)
+    a = rng.integers(-127, 128, (5, 13)).astype(np.int8)
+    b = rng.integers(-127, 128, (4, 13)).astype(np.int8)
+    C = O.int_gemm(a, b)
+    for m in range(5):
+        for n in range(4):
+            assert C[m, n] == sum(int(a[m, k]) * int(b[n, k]) for k in range(13))
+    a = rng.integers(-127, 128, (40, 3000)).astype(np.int8)
+    b = rng.integers(-127, 128, (30, 3000)).astype(np.int8)
+    assert np.array_equal(O.int_gemm(a, b), a.astype(np.int64) @ b.astype(np.int64).T)
+    # the extreme: every product 127*127 -> K * 16129, still exact
+    a = np.full((2, 4096), 127, np.int8)
+    b = np.full((2, 4096), -127, np.int8)
+    assert np.all(O.int_gemm(a, b) == -4096 * 16129)
+
+
+# ---------------------------------------------------------------------------
+# whole forward: the lossless special case (exact pin)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("outliers", [(), (3,), (0, 17, 40)])
+@pytest.mark.parametrize("dtype", [O.F16, O.BF16])
+def test_forward_lossless_exact(outliers, dtype):
+    M, K, N = 24, 48, 20
+    case = W.lossless_case(M, K, N, seed=11, outlier_cols=outliers, threshold=6.0)
+    A64 = case["A"].double().numpy()
+    W64 = case["W"].double().numpy()
+    bias = (np.arange(N) / 64.0 - 0.1).astype(np.float16)
+    CB, SCB = O.quantize_weight(case["W"].numpy(), O.F16)
+    assert np.array_equal(CB, case["qw"].numpy().astype(np.int8))
+    A_in = O.round_to(A64, dtype)              # exact: on the grid of both dtypes
+    r = O.forward(A_in, dtype, CB, SCB, bias, O.F16, threshold=6.0)
+    assert r["idx"].tolist() == sorted(outliers)
+    exact = A64 @ W64.T + bias.astype(np.float64)[None, :]
+    assert np.array_equal(r["out64"], exact)
+    assert np.array_equal(r["out"], O.round_to(exact, dtype))
+    if not outliers:
+        assert np.array_equal(r["Aq"], case["qa"].numpy().astype(np.int8))
+
+
+def test_forward_residual_is_added_once():
+    M, K, N = 8, 32, 8
+    case = W.lossless_case(M, K, N, seed=12)
+    CB, SCB = O.quantize_weight(case["W"].numpy(), O.F16)
+    res = (np.arange(M * N).reshape(M, N) / 32.0).astype(np.float16)
+    r0 = O.forward(case["A"].numpy(), O.F16, CB, SCB, threshold=math.inf)
+    r1 = O.forward(case["A"].numpy(), O.F16, CB, SCB, threshold=math.inf, residual=res)
+    assert np.array_equal(r1["out64"], r0["out64"] + res.astype(np.float64))
+
+
+def test_forward_reconstruction_bound():
+    """Generic inputs: the int8 part plus the outlier part reconstruct
+    A16 @ Wdq^T within the quantization error of the int8 part."""
+    spec = W.LayerSpec(32, 256, 24, torch.float16, 0.02, 0.01, 0.02, 20.0, 6.0)
+    A = W.activation(spec, 13).numpy()
+    Wf, b, _ = W.layer_tensors(W.Workload("t", "", (spec,), w_dtype=torch.float16), 0, 13)
+    b = b.numpy()
+    CB, SCB = O.quantize_weight(Wf.numpy(), O.F16)
+    r = O.forward(A, O.F16, CB, SCB, b, O.F16, threshold=6.0)
+    assert len(r["idx"]) >= 5
+    A16 = A.astype(np.float64)
+    Wq = CB.astype(np.float64) * SCB.astype(np.float64)[:, None] / 127      # exact dequant
+    Wdq = O.dequant_weight(CB, SCB).astype(np.float64)
+    target = A16 @ Wdq.T + b.astype(np.float64)[None, :]
+    mask = np.ones(256, bool)
+    mask[r["idx"]] = False
+    bound = ((r["SCA"].astype(np.float64)[:, None] / 254) * np.abs(Wq[:, mask]).sum(1)[None, :]
+             + np.abs(A16[:, mask]) @ np.abs(Wq[:, mask] - Wdq[:, mask]).T)
+    err = np.abs(r["out64"] - target)
+    assert np.all(err <= bound * (1 + 1e-9) + 1e-12)
+    # a dropped outlier term would not fit the bound by orders of magnitude
+    drop = r["out64"] - r["subA"].astype(np.float64) @ r["subB"].astype(np.float64).T
+    assert np.abs(drop - target).max() > 10 * bound.max()
+
+
+def test_forward_rows_matches_full():
+    spec = W.LayerSpec(40, 128, 16, torch.float16, 0.02, 0.01, 0.02, 20.0, 6.0)
+    A = W.activation(spec, 14).numpy()
+    Wf, b, _ = W.layer_tensors(W.Workload("t", "", (spec,), w_dtype=torch.float16), 0, 14)
+    CB, SCB = O.quantize_weight(Wf.numpy(), O.F16)
+    full = O.forward(A, O.F16, CB, SCB, b.numpy(), O.F16, threshold=6.0)
+    rows = np.array([0, 7, 39])
+    part = O.forward_rows(A, O.F16, CB, SCB, rows, b.numpy(), O.F16, threshold=6.0)
+    for k in ("SCA", "Aq", "subA", "Cacc", "out"):
+        assert np.array_equal(part[k], full[k][rows])
+
+
+# ---------------------------------------------------------------------------
+# backward
+# ---------------------------------------------------------------------------
+
+def test_backward_bruteforce():
+    rng = np.random.default_rng(15)
+    M, N, K = 4, 6, 5
+    G = rng.standard_normal((M, N)).astype(np.float32)
+    CB = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    SCB = (np.abs(rng.standard_normal(N)) * 0.05 + 1e-3).astype(np.float32)
+    r = O.backward_input(G, O.F32, CB, SCB)
+    Wdq = O.dequant_weight(CB, SCB).astype(np.float64)
+    for m in range(M):
+        for k in range(K):
+            s = math.fsum(f16(float(G[m, n])) * float(Wdq[n, k]) for n in range(N))
+            assert r["grad_A"][m, k] == f32(s)
+    gb = O.grad_bias(G, O.F32, O.F32)
+    for n in range(N):
+        assert gb[n] == f32(math.fsum(float(G[m, n]) for m in range(M)))
+
+
+def test_backward_lossless_exact():
+    M, K, N = 16, 40, 24
+    case = W.lossless_case(M, K, N, seed=16)
+    CB, SCB = O.quantize_weight(case["W"].numpy(), O.F16)
+    G = (np.random.default_rng(16).integers(-64, 64, (M, N)) / 16.0).astype(np.float16)
+    r = O.backward_input(G, O.F16, CB, SCB)
+    exact = G.astype(np.float64) @ case["W"].double().numpy()    # Wdq == W here
+    assert np.array_equal(r["grad64"], exact)
+    add = (np.arange(M * K).reshape(M, K) / 128.0).astype(np.float16)
+    r2 = O.backward_input(G, O.F16, CB, SCB, addend=add)
+    assert np.array_equal(r2["grad64"], exact + add.astype(np.float64))
+
+
+def test_grad_bias_closed_form():
+    G = np.ones((1000, 3), dtype=np.float16)
+    assert O.grad_bias(G, O.F16, O.F32).tolist() == [1000.0] * 3
+    # uncast: fp32 values that fp16 would flush/round still count in full
+    G = np.full((4, 2), 1e-8, dtype=np.float32)
+    assert O.grad_bias(G, O.F32, O.F32).tolist() == [f32(4e-8)] * 2
+
+
+def test_silu_closed_forms():
+    h = np.array([0.0, 1.0, -1.0, 20.0], dtype=np.float32)
+    s = O.silu(h, O.F32).astype(np.float64)
+    assert s[0] == 0.0 and s[3] == pytest.approx(20.0, rel=1e-8)
+    assert s[1] == f32(1 / (1 + math.exp(-1)))
+    g = O.silu_backward(np.ones(4, np.float32), h, O.F32).astype(np.float64)
+    assert g[0] == 0.5                                  # silu'(0) = 1/2
+    sg = 1 / (1 + math.exp(-1))
+    assert g[1] == f32(sg * (1 + 1 * (1 - sg)))
