@@ -1,0 +1,494 @@
+"""Benchmark of the int8 quantized linear layer on GB300: forward + backward
+to the input (and bias) of every layer of a workload, throughput in TOPS.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step = every layer of the workload: quantize the activations (outlier
+detection, row quantization, outlier weight columns), the int8 GEMM with its
+fused dequant/outlier/bias epilogue, the grad_output prepass (grad_bias) and
+the dequantizing backward GEMM.  Inputs are resident in HBM and larger than
+L2 (so no flush is needed between steps).  Under torchrun every rank runs its
+own replica of the workload (no collective on the data path): weak scaling.
+
+``--impl reference`` times the CPU oracle on the host cores instead, on a
+bounded row sample of the same workload, and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "Int8 linear fwd+bwd TOPS on one GB300, % of int8/fp16 tensor-core peak"
+DEFAULT_WORKLOAD = "proj_8192x28672"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: timing only, no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, device) -> float:
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, device) -> float:
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class Layer:
+    """Device-resident tensors of one layer of the workload."""
+
+    def __init__(self, wl, li, seed, device):
+        import int8_quantized_linear_i8lt_gb300 as I
+        spec = wl.layers[li]
+        self.spec = spec
+        gen_dev = device                      # draw on the GPU: same recipe, fast
+        torch.manual_seed(seed * 1000 + li)
+        A = torch.randn(spec.M, spec.K, device=gen_dev, dtype=torch.float32)
+        heavy = W.heavy_columns(spec.K, spec.heavy_frac, seed + li * W.OFF_LAYER2 + W.OFF_HEAVY).to(device)
+        if len(heavy):
+            A[:, heavy] *= spec.heavy_factor
+        self.A = A.to(spec.dtype)
+        del A
+        wdt = wl.w_dtype or spec.dtype
+        Wf = (torch.randn(spec.N, spec.K, device=gen_dev) * spec.w_std).to(wdt)
+        self.CB, self.SCB = I.quantize_weight(Wf)
+        del Wf
+        self.bias = (torch.randn(spec.N, device=gen_dev) * (spec.bias_std or 0.0)).to(wdt)
+        self.G = torch.randn(spec.M, spec.N, device=gen_dev).to(spec.dtype)
+        cap = I.default_max_outliers(spec.K)
+        self.cap = cap
+        self.out = torch.empty(spec.M, spec.N, dtype=spec.dtype, device=device)
+        self.ws_f = I.functional.forward_workspace(spec.M, spec.K, spec.N, cap, device)
+        self.ws_b = I.functional.backward_workspace(spec.M, spec.N, spec.dtype, device)
+        self.grad_A = torch.empty(spec.M, spec.K, dtype=spec.dtype, device=device)
+        self.grad_bias = torch.empty(spec.N, dtype=wdt, device=device)
+
+    def ops(self):
+        s = self.spec
+        return 4.0 * s.M * s.N * s.K        # 2MNK forward + 2MNK backward-to-input
+
+
+def _launch_layer(L, stream_ptr, ev=None):
+    """One layer through the C ABI: forward, then backward to the input and
+    the bias.  ``ev``: optional dict of CUDA event pairs around the GEMMs."""
+    from int8_quantized_linear_i8lt_gb300 import _lib
+    from int8_quantized_linear_i8lt_gb300.functional import DTYPE_CODE
+    s = L.spec
+    dt = DTYPE_CODE[s.dtype]
+    bt = DTYPE_CODE[L.bias.dtype]
+    st = _lib.i8lt_forward(L.A.data_ptr(), dt, s.M, s.K, L.CB.data_ptr(), L.SCB.data_ptr(), s.N,
+                           L.bias.data_ptr(), bt, s.threshold, None, L.out.data_ptr(), L.ws_f.data_ptr(),
+                           L.ws_f.numel(), L.cap, stream=stream_ptr)
+    assert st == 0, _lib.i8lt_status_string(st)
+    st = _lib.i8lt_backward_input(L.G.data_ptr(), dt, s.M, s.N, L.CB.data_ptr(), L.SCB.data_ptr(), s.K, None,
+                                  L.grad_A.data_ptr(), L.grad_bias.data_ptr(), bt, L.ws_b.data_ptr(),
+                                  L.ws_b.numel(), stream_ptr)
+    assert st == 0, _lib.i8lt_status_string(st)
+
+
+def kernel_flops(L, name):
+    """Algorithmic work of one launch of a GEMM kernel: 2*M*N*K."""
+    s = L.spec
+    return 2.0 * s.M * s.N * s.K if name in ("fwd_gemm", "bwd_gemm") else 0.0
+
+
+def kernel_bytes(L, name):
+    """Algorithmic HBM bytes of one launch of a memory-bound kernel."""
+    s = L.spec
+    a = {torch.float16: 2, torch.bfloat16: 2, torch.float32: 4}[s.dtype]
+    cnt = getattr(L, "found", 0)
+    cap_pad = (min(cnt, s.K) + 63) // 64 * 64
+    kp = (s.K + 15) // 16 * 16
+    return {
+        "colmax": s.M * s.K * a + s.K * 4,
+        "row_quantize": s.M * s.K * a + s.M * kp * 2 + s.M * 4 + s.M * cap_pad * 2,
+        "gradout_prepass": s.M * s.N * a,
+        "build_subB": s.N * cap_pad * 3,
+    }.get(name, 0.0)
+
+
+def run_ours(args):
+    import int8_quantized_linear_i8lt_gb300 as I  # noqa: F401  (fails loudly without the library)
+    from int8_quantized_linear_i8lt_gb300 import _lib
+    _lib.load()
+    ws, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    wl = W.WORKLOADS[args.workload]
+    layers = [Layer(wl, li, 1234 + rank, device) for li in range(len(wl.layers))]
+    stream = torch.cuda.current_stream(device)
+    sp = stream.cuda_stream
+    for _ in range(args.warmup):
+        for L in layers:
+            _launch_layer(L, sp)
+    torch.cuda.synchronize()
+    for L in layers:
+        st, found = I.device_status(L.ws_f)
+        assert st == 0, _lib.i8lt_status_string(st)
+        L.found = found
+    # --- timed region: K steps, every kernel launch bracketed by CUDA events
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _lib.i8lt_profile_start(1 << 20)
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            for L in layers:
+                _launch_layer(L, sp)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    pst, recs, n_launches = _lib.i8lt_profile_stop(1 << 20)
+    assert pst == 0
+    barrier()
+    ms_total = reduce_max(ev0.elapsed_time(ev1), device)
+    ops_step = sum(L.ops() for L in layers)
+    ms_step = ms_total / args.steps
+    units = reduce_sum(ops_step * args.steps, device)
+    value = units / (ms_total * 1e-3) / 1e12
+
+    # --- per-kernel totals from the records (launch order repeats per step)
+    per_step = len(recs) // args.steps
+    kern = {}
+    for i, (name, ms) in enumerate(recs):
+        L = layers[_layer_of(i % per_step, layers)]
+        d = kern.setdefault(name, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
+        d["launches"] += 1
+        d["ms"] += ms
+        d["flops"] += kernel_flops(L, name)
+        d["bytes"] += kernel_bytes(L, name)
+    total_k_ms = sum(d["ms"] for d in kern.values())
+    dom = max(kern, key=lambda k: kern[k]["ms"])
+    peaks, peak_src = load_peaks()
+    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak_b = float(peaks.get("hbm_gbs"))
+    d = kern[dom]
+    if d["flops"] > 0:
+        achieved = d["flops"] / (d["ms"] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak_t,
+                "unit": "TFLOP/s", "frac": round(achieved / peak_t, 4),
+                "peak_source": f"{peak_src} bf16 sustained (fp16 runs at the bf16 rate)"}
+    else:
+        achieved = d["bytes"] / (d["ms"] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak_b, "unit": "GB/s",
+                "frac": round(achieved / peak_b, 4), "peak_source": f"{peak_src} hbm copy"}
+    roof["launch_ms"] = round(d["ms"] / d["launches"], 4)
+    roof["traffic"] = None
+    kernels = {}
+    for k, v in sorted(kern.items(), key=lambda kv: -kv[1]["ms"]):
+        e = {"launches": v["launches"], "ms_per_launch": round(v["ms"] / v["launches"], 4),
+             "share": round(v["ms"] / total_k_ms, 4)}
+        if v["flops"]:
+            t = v["flops"] / (v["ms"] * 1e-3) / 1e12
+            e.update(tflops=round(t, 1), frac_tensor=round(t / peak_t, 4))
+        elif v["bytes"]:
+            g = v["bytes"] / (v["ms"] * 1e-3) / 1e9
+            e.update(gbs=round(g, 1), frac_hbm=round(g / peak_b, 4))
+        kernels[k] = e
+    # --- end to end through host buffers (pinned), inputs and results copied each step
+    e2e = run_e2e(layers, stream, max(1, min(args.steps, 3)), device)
+
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 codes (exact fp16 on tcgen05 kind::f16, int32 sums) + f16",
+        "data": "synthetic (seeded N(0,1) activations with heavy outlier columns, N(0,std) weights)",
+        "config": {"workload": wl.name, "layers": [[s.M, s.K, s.N, str(s.dtype).replace("torch.", "")]
+                                                   for s in wl.layers],
+                   "threshold": wl.layers[0].threshold, "outlier_columns": [L.found for L in layers],
+                   "l2": "inputs larger than L2 (126 MB); no flush", "parallelism": f"replicas x{ws}"},
+        "roofline": roof,
+        "kernels": kernels,
+        "e2e": e2e,
+        "gpu_launches": n_launches,
+        "clocks": clocks,
+        "wall_s": round(t_wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _layer_of(i, layers):
+    """Index of the layer that launch ``i`` (within one step) belongs to."""
+    n = 0
+    for li, L in enumerate(layers):
+        n += launches_per_layer(L)
+        if i < n:
+            return li
+    return len(layers) - 1
+
+
+def launches_per_layer(L) -> int:
+    """Our kernels per layer and step: colmax, outlier index, row quantize,
+    subB (outliers on), forward GEMM; grad_output prepass, grad_bias
+    finalize, backward GEMM."""
+    import math
+    fwd = 5 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 2
+    return fwd + 3
+
+
+def run_e2e(layers, stream, steps, device):
+    """The metric through the public C ABI with host buffers: every step copies
+    A and grad_output from pinned host memory and reads out, grad_A and
+    grad_bias back, inside the timed region."""
+    host_in = [(torch.empty_like(L.A, device="cpu").pin_memory(), torch.empty_like(L.G, device="cpu").pin_memory())
+               for L in layers]
+    host_out = [(torch.empty_like(L.out, device="cpu").pin_memory(),
+                 torch.empty_like(L.grad_A, device="cpu").pin_memory(),
+                 torch.empty_like(L.grad_bias, device="cpu").pin_memory()) for L in layers]
+    for (hA, hG), L in zip(host_in, layers):
+        hA.copy_(L.A)
+        hG.copy_(L.G)
+    sp = stream.cuda_stream
+    h2d = sum(hA.numel() * hA.element_size() + hG.numel() * hG.element_size() for hA, hG in host_in)
+    d2h = sum(sum(t.numel() * t.element_size() for t in ho) for ho in host_out)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        for (hA, hG), (ho, hga, hgb), L in zip(host_in, host_out, layers):
+            L.A.copy_(hA, non_blocking=True)
+            L.G.copy_(hG, non_blocking=True)
+            _launch_layer(L, sp)
+            ho.copy_(L.out, non_blocking=True)
+            hga.copy_(L.grad_A, non_blocking=True)
+            hgb.copy_(L.grad_bias, non_blocking=True)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(ev0.elapsed_time(ev1), device)
+    ops = reduce_sum(sum(L.ops() for L in layers) * steps, device)
+    return {"value": round(ops / (ms * 1e-3) / 1e12, 2), "unit": "TOPS", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms / steps, 3)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def oracle_sample_step(wl, rows_per_layer, seed=0):
+    """One bounded oracle step: for every layer, the forward and the backward
+    to the input on ``rows_per_layer`` rows (the outlier columns taken over
+    those rows), with the weight quantized beforehand (off the step path).
+    Returns (seconds, ops done)."""
+    import oracle as O
+    ops, secs = 0.0, 0.0
+    for li, spec in enumerate(wl.layers):
+        rows = np.arange(min(rows_per_layer, spec.M))
+        sub = W.LayerSpec(len(rows), spec.K, spec.N, spec.dtype, spec.w_std, spec.bias_std, spec.heavy_frac,
+                          spec.heavy_factor, spec.threshold)
+        A = W.activation(sub, seed + li * W.OFF_LAYER2)
+        g = torch.Generator().manual_seed(seed + li)
+        wdt = wl.w_dtype or spec.dtype
+        Wf = (torch.randn(spec.N, spec.K, generator=g) * spec.w_std).to(wdt)
+        b = (torch.randn(spec.N, generator=g) * (spec.bias_std or 0.0)).to(wdt)
+        G = torch.randn(len(rows), spec.N, generator=g).to(spec.dtype)
+        odt = {torch.float16: O.F16, torch.bfloat16: O.BF16, torch.float32: O.F32}
+
+        def np_(t):
+            t = t.contiguous()
+            return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+        CB, SCB = O.quantize_weight(np_(Wf), odt[wdt])
+        A_np, b_np, G_np = np_(A), np_(b), np_(G)
+        t0 = time.perf_counter()
+        O.forward(A_np, odt[spec.dtype], CB, SCB, b_np, odt[wdt], spec.threshold)
+        O.backward_input(G_np, odt[spec.dtype], CB, SCB)
+        O.grad_bias(G_np, odt[spec.dtype], odt[wdt])
+        secs += time.perf_counter() - t0
+        ops += 4.0 * len(rows) * spec.N * spec.K
+    return secs, ops
+
+
+def cpu_baseline(wl, budget_s=20.0):
+    rows = 16
+    secs, ops = oracle_sample_step(wl, rows)
+    # grow the sample towards the budget (rows scale the GEMM work linearly)
+    if secs < budget_s / 4:
+        rows = int(min(max(wl.layers[0].M, 16), rows * max(1.0, (budget_s / 2) / max(secs, 1e-3))))
+        rows = max(16, min(rows, 512))
+        secs, ops = oracle_sample_step(wl, rows)
+    return {"value": round(ops / secs / 1e12, 6), "unit": "TOPS", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{rows} rows of every layer of {wl.name}: forward + backward to the input + grad_bias, "
+                      f"weights pre-quantized; {secs:.1f} s of CPU time"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    wl = W.WORKLOADS[args.workload]
+    rows = max(16, min(256, int(args.ref_rows)))
+    for _ in range(args.warmup):
+        oracle_sample_step(wl, 16)
+    secs_total, ops_total = 0.0, 0.0
+    for k in range(args.steps):
+        s, o = oracle_sample_step(wl, rows, seed=k)
+        secs_total += s
+        ops_total += o
+    value = ops_total / secs_total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs_total / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic", "config": {"workload": wl.name, "sample_rows_per_layer": rows},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": _blas_threads(), "kind": "oracle",
+                         "sample": f"{rows} rows of every layer per step"},
+        "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--ref-rows", type=int, default=64)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

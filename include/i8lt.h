@@ -1,0 +1,201 @@
+/*
+ * i8lt.h -- C ABI of the GB300 (sm_103a) int8 quantized linear layer.
+ *
+ * The layer is the memory-efficient Linear8bitLt of bitsandbytes PR #33
+ * "Memory efficient backward":
+ *   - weights live as row-major int8 codes CB [N, K] with one fp32 absmax per
+ *     output row SCB [N] (PR description, "Stores int8 weights in row-major
+ *     format");
+ *   - the forward casts A to fp16, quantizes it row-wise (vector-wise absmax),
+ *     takes columns with an element above the outlier threshold out as subA and
+ *     multiplies them in fp16 against the matching weight columns subB
+ *     (review thread, "4. Mixed-precision decomposition matmul"), dequantizes,
+ *     adds the bias and casts back to A's dtype (PR description, "Cast inputs
+ *     and outputs of the 8bit layer to fp16 and back");
+ *   - the backward rebuilds fp16 weights CB * (SCB * (1/127)) inside the GEMM
+ *     and never stores them (PR description, backward bullet; review thread on
+ *     ".mul(1/127.0)"), and sums grad_bias from the uncast grad_output (PR
+ *     conversation, "grad_bias is now computed on natural grad_output").
+ *
+ * Conventions for every entry point:
+ *   - Matrices are row-major and contiguous.  Device pointers unless stated.
+ *     Base pointers of matrices must be 16-byte aligned.
+ *   - The caller owns every buffer, including the workspace.  The library
+ *     allocates no device memory.
+ *   - `stream` is a cudaStream_t passed as void*.  Work is asynchronous on it;
+ *     nothing synchronizes except i8lt_read_device_status.
+ *   - Errors found on the host are returned before anything is launched.
+ *     Errors found on the device (outlier capacity exceeded, a pipeline wait
+ *     that timed out) are written to the status word at the start of the
+ *     workspace; the outputs of that call are then unspecified.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef I8LT_H_
+#define I8LT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  I8LT_OK = 0,
+  I8LT_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad shape */
+  I8LT_ERR_UNSUPPORTED_DTYPE = 2, /* dtype not in i8lt_dtype */
+  I8LT_ERR_MISALIGNED = 3,        /* a matrix base pointer is not 16-byte aligned */
+  I8LT_ERR_WORKSPACE = 4,         /* workspace null or smaller than required */
+  I8LT_ERR_K_TOO_LARGE = 5,       /* int32 accumulator could overflow */
+  I8LT_ERR_OUTLIER_CAPACITY = 6,  /* device: more outlier columns than max_outliers */
+  I8LT_ERR_TIMEOUT = 7,           /* device: a pipeline wait ran out of time */
+  I8LT_ERR_CUDA = 8,              /* a CUDA runtime / driver call failed */
+  I8LT_ERR_DEVICE = 9             /* the current device is not sm_103 */
+} i8lt_status;
+
+typedef enum { I8LT_F16 = 0, I8LT_BF16 = 1, I8LT_F32 = 2 } i8lt_dtype;
+
+/* Largest in_features for which K * 127 * 127 < 2^31 (exact int32 sums). */
+#define I8LT_MAX_K 133144
+
+/* Version of this ABI; bumped on any incompatible change. */
+int i8lt_abi_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* i8lt_status_string(int status);
+
+/* Leading dimension (elements) of the int8 weight CB for in_features K:
+ * K rounded up to a multiple of 16, so that every row starts on 16 bytes. */
+int64_t i8lt_weight_ld(int64_t K);
+
+/*
+ * Weight quantization (once per weight; "memory_efficient_backward" keeps
+ * only CB and SCB, the fp16 weight is not kept).
+ *   W    [N, K] in dtype `wt` (read only)
+ *   CB   [N, i8lt_weight_ld(K)] int8 (written; columns >= K are set to 0)
+ *   SCB  [N] fp32 (written)
+ * W16 = fp16_rn(W); SCB[n] = max_k |W16[n,k]|;
+ * CB[n,k] = round_half_even(fp32(W16[n,k]) * (127 / SCB[n])) in IEEE fp32,
+ * 0 for a row whose absmax is 0.
+ */
+int i8lt_quantize_weight(const void* W, int wt, int64_t N, int64_t K,
+                         int8_t* CB, float* SCB, void* stream);
+
+/* Workspace of i8lt_forward, in bytes.  max_outliers is the capacity for
+ * outlier columns (0 when the threshold disables the decomposition). */
+size_t i8lt_forward_workspace_size(int64_t M, int64_t K, int64_t N,
+                                   int64_t max_outliers);
+
+/* Byte offsets of the regions of the forward workspace (for tests and
+ * debugging; every region is 256-byte aligned):
+ *   status  int32[4]: {status, outlier count found, count used, spare}
+ *   colmax  uint32[K]: per column, fp16 bits of max_m |A16[m,k]|
+ *   mask    uint32[ceil(K/32)]: bit k set when column k is an outlier
+ *   idx     int32[cap_pad]: ascending outlier column indices
+ *   SCA     fp32[M]: row absmax of A16 outside the outlier columns
+ *   Aq      fp16[M, K_pad]: the int8 codes of A, stored as exact fp16 integers
+ *                           (the form the fp16 tensor cores read)
+ *   subA    fp16[M, cap_pad]: A16[:, idx], zero past the count
+ *   subB    fp16[N, cap_pad]: dequantized weight columns W_dq[:, idx]
+ * cap = min(max_outliers, K); cap_pad = cap rounded up to a multiple of 64. */
+typedef struct {
+  size_t status, colmax, mask, idx, sca, aq, suba, subb, total;
+  int64_t k_pad, cap_pad;
+} i8lt_fwd_layout;
+int i8lt_forward_workspace_layout(int64_t M, int64_t K, int64_t N,
+                                  int64_t max_outliers, i8lt_fwd_layout* out);
+
+/* Optional extra outputs of the forward for parity checks.  Any field may be
+ * NULL.  acc_i32 [M, N] receives the exact int32 accumulator
+ * sum_k Aq[m,k] * CB[n,k] of the int8 part. */
+typedef struct {
+  int32_t* acc_i32;
+} i8lt_fwd_debug;
+
+/*
+ * Forward: out = to_dtype(at)( Cacc[m,n] * SCA[m] * SCB[n] / 127^2
+ *                             + sum_j subA[m,j] * subB[n,j]
+ *                             + bias[n] + residual[m,n] )
+ *   A        [M, K] dtype `at` in {f16, bf16, f32}; cast to fp16 first
+ *   CB, SCB  from i8lt_quantize_weight (CB leading dimension i8lt_weight_ld(K))
+ *   bias     [N] dtype `bt`, or NULL
+ *   residual [M, N] dtype `at`, or NULL (added before the single rounding)
+ *   threshold outlier threshold: column k is an outlier when some row has
+ *            |A16[m,k]| > threshold; a value that is not a positive finite
+ *            number disables the decomposition
+ *   out      [M, N] dtype `at`
+ *   ws       workspace of at least i8lt_forward_workspace_size bytes,
+ *            256-byte aligned
+ *   max_outliers capacity for outlier columns; more columns than this sets
+ *            I8LT_ERR_OUTLIER_CAPACITY in the device status word
+ *   dbg      optional debug outputs, or NULL
+ * Returns I8LT_ERR_K_TOO_LARGE for K > I8LT_MAX_K.
+ */
+int i8lt_forward(const void* A, int at, int64_t M, int64_t K,
+                 const int8_t* CB, const float* SCB, int64_t N,
+                 const void* bias, int bt, float threshold,
+                 const void* residual, void* out,
+                 void* ws, size_t ws_bytes, int64_t max_outliers,
+                 const i8lt_fwd_debug* dbg, void* stream);
+
+/* Workspace of i8lt_backward_input, in bytes (space for the fp16 copy of
+ * grad_output when it is not already fp16 with N a multiple of 8). */
+size_t i8lt_backward_workspace_size(int64_t M, int64_t N, int gt);
+
+/*
+ * Memory-efficient backward to the input (no weight gradient: the weight is
+ * frozen in this mode).
+ *   G         [M, N] grad_output, dtype `gt` (the layer's output dtype)
+ *   CB, SCB   the quantized weight, CB leading dimension i8lt_weight_ld(K)
+ *   addend    [M, K] dtype `gt`, or NULL: added to grad_A before rounding
+ *   grad_A    [M, K] dtype `gt`, or NULL to skip:
+ *             grad_A = to_dtype( fp16(G) @ W_dq ),
+ *             W_dq[n,k] = fp16_rn(fp32(CB[n,k]) * (SCB[n] * fp32(1/127)))
+ *             built in shared memory inside the GEMM, never stored
+ *   grad_bias [N] dtype `bt`, or NULL to skip: sum over rows of the uncast G
+ *   ws        workspace of at least i8lt_backward_workspace_size bytes
+ */
+int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N,
+                        const int8_t* CB, const float* SCB, int64_t K,
+                        const void* addend, void* grad_A,
+                        void* grad_bias, int bt,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/* SiLU between the two layers of an MLP: out = h * sigmoid(h), and its
+ * backward out = g * silu'(h).  n elements of dtype dt. */
+int i8lt_silu_forward(const void* h, int dt, int64_t n, void* out, void* stream);
+int i8lt_silu_backward(const void* g, const void* h, int dt, int64_t n,
+                       void* out, void* stream);
+
+/* Kernel-level timing.  Between i8lt_profile_start and i8lt_profile_stop
+ * the library records a CUDA event before and after every kernel it
+ * launches, on the launch stream (no synchronization while recording).
+ * i8lt_profile_stop waits for the recorded events, writes up to `cap`
+ * {kernel id, milliseconds} records in launch order, sets *n_records to the
+ * number written and *n_launches to the number of kernel launches made while
+ * recording, and stops recording.  Host-side state only; at most
+ * `max_launches` launches are timed (later ones are counted, not timed). */
+typedef enum {
+  I8LT_K_QUANTIZE_WEIGHT = 0, I8LT_K_COLMAX = 1, I8LT_K_OUTLIER_INDEX = 2, I8LT_K_ROW_QUANTIZE = 3,
+  I8LT_K_SUBB = 4, I8LT_K_FWD_GEMM = 5, I8LT_K_GRADOUT_PREPASS = 6, I8LT_K_GRAD_BIAS_FINALIZE = 7,
+  I8LT_K_BWD_GEMM = 8, I8LT_K_SILU = 9, I8LT_K_SILU_BACKWARD = 10, I8LT_K_COUNT = 11
+} i8lt_kernel_id;
+typedef struct {
+  int kernel;
+  float ms;
+} i8lt_kernel_time;
+int i8lt_profile_start(int max_launches);
+int i8lt_profile_stop(i8lt_kernel_time* out, int cap, int* n_records, int* n_launches);
+const char* i8lt_kernel_name(int kernel);
+
+/* Synchronizes `stream`, then reads the status word of a forward or backward
+ * workspace (status and the number of outlier columns found; either output
+ * pointer may be NULL), and clears it.  Returns I8LT_OK or the status the
+ * device recorded. */
+int i8lt_read_device_status(void* ws, int32_t* status, int32_t* outliers,
+                            void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* I8LT_H_ */

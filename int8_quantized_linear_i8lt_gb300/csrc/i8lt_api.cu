@@ -1,0 +1,417 @@
+// C ABI of libi8lt: argument checks, workspace layout, TMA descriptors and
+// the launch sequence of the forward and backward of the int8 quantized
+// linear layer (bitsandbytes PR #33 "Memory efficient backward").
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "i8lt.h"
+#include "i8lt_internal.h"
+
+using namespace i8lt;
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool valid_dt(int dt) { return dt == DT_F16 || dt == DT_BF16 || dt == DT_F32; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool threshold_enabled(float t) { return std::isfinite(t) && t > 0.0f; }
+
+int64_t cap_pad_of(int64_t cap) { return cap > 0 ? round_up(cap, 64) : 0; }
+
+// Device check: the kernels are built for sm_103a only.
+int check_device() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return I8LT_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return I8LT_ERR_DEVICE;
+  int c = cached[dev].load();
+  if (c == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return I8LT_ERR_CUDA;
+    c = (major == 10 && minor == 3) ? 1 : 2;
+    cached[dev].store(c);
+  }
+  return c == 1 ? I8LT_OK : I8LT_ERR_DEVICE;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor (inner x outer elements, row pitch in bytes) with a
+// box of box_inner x box_outer elements.
+bool make_tmap(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t pitch, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? I8LT_OK : I8LT_ERR_CUDA; }
+
+i8lt_fwd_layout fwd_layout(int64_t M, int64_t K, int64_t N, int64_t cap) {
+  i8lt_fwd_layout L;
+  std::memset(&L, 0, sizeof(L));
+  L.k_pad = round_up(K, 16);
+  L.cap_pad = cap_pad_of(cap < K ? cap : K);
+  size_t off = 0;
+  L.status = off;
+  off += kAlign;
+  L.colmax = off;
+  off += align_up(static_cast<size_t>(K) * 4);
+  L.mask = off;
+  off += align_up(static_cast<size_t>(ceil_div(K, 32)) * 4);
+  L.idx = off;
+  off += align_up(static_cast<size_t>(L.cap_pad) * 4);
+  L.sca = off;
+  off += align_up(static_cast<size_t>(M) * 4);
+  L.aq = off;
+  off += align_up(static_cast<size_t>(M) * L.k_pad * 2);
+  L.suba = off;
+  off += align_up(static_cast<size_t>(M) * L.cap_pad * 2);
+  L.subb = off;
+  off += align_up(static_cast<size_t>(N) * L.cap_pad * 2);
+  L.total = off;
+  return L;
+}
+
+bool needs_g16(int64_t N, int gt) { return gt != DT_F16 || (N % 8) != 0; }
+
+struct BwdLayout {
+  size_t status, partial, g16, total;
+  int64_t n_pad, chunks;
+};
+
+BwdLayout bwd_layout(int64_t M, int64_t N, int gt) {
+  BwdLayout L;
+  L.n_pad = round_up(N, 8);
+  L.chunks = gradout_partial_chunks(M);
+  size_t off = 0;
+  L.status = off;
+  off += kAlign;
+  L.partial = off;
+  off += align_up(static_cast<size_t>(L.chunks) * N * 4);
+  L.g16 = off;
+  if (needs_g16(N, gt)) off += align_up(static_cast<size_t>(M) * L.n_pad * 2);
+  L.total = off;
+  return L;
+}
+
+// ---- kernel timing --------------------------------------------------------
+struct ProfRec {
+  int id;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+int g_prof_max = 0;
+int g_prof_count = 0;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_ev_pool;
+int g_ev_next = 0;
+
+cudaEvent_t pool_event() {
+  if (g_ev_next == static_cast<int>(g_ev_pool.size())) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_ev_pool.push_back(e);
+  }
+  return g_ev_pool[g_ev_next++];
+}
+
+}  // namespace
+
+namespace i8lt {
+void prof_begin(int id, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) return;
+  ++g_prof_count;
+  if (static_cast<int>(g_prof.size()) >= g_prof_max) return;
+  ProfRec r{id, pool_event(), pool_event()};
+  if (r.a == nullptr || r.b == nullptr) return;
+  cudaEventRecord(r.a, s);
+  g_prof.push_back(r);
+}
+void prof_end(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on || g_prof.empty()) return;
+  cudaEventRecord(g_prof.back().b, s);
+}
+}  // namespace i8lt
+
+extern "C" {
+
+int i8lt_abi_version(void) { return kAbiVersion; }
+
+const char* i8lt_status_string(int s) {
+  switch (s) {
+    case I8LT_OK: return "ok";
+    case I8LT_ERR_INVALID_ARG: return "invalid argument";
+    case I8LT_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case I8LT_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case I8LT_ERR_WORKSPACE: return "workspace missing or too small";
+    case I8LT_ERR_K_TOO_LARGE: return "in_features too large for exact int32 accumulation";
+    case I8LT_ERR_OUTLIER_CAPACITY: return "more outlier columns than max_outliers";
+    case I8LT_ERR_TIMEOUT: return "a device pipeline wait timed out";
+    case I8LT_ERR_CUDA: return "CUDA error";
+    case I8LT_ERR_DEVICE: return "device is not sm_103 (GB300)";
+    default: return "unknown status";
+  }
+}
+
+int64_t i8lt_weight_ld(int64_t K) { return K < 0 ? -1 : round_up(K, 16); }
+
+int i8lt_quantize_weight(const void* W, int wt, int64_t N, int64_t K, int8_t* CB, float* SCB, void* stream) {
+  if (!valid_dt(wt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (N < 0 || K <= 0) return I8LT_ERR_INVALID_ARG;
+  if (N == 0) return I8LT_OK;
+  if (W == nullptr || CB == nullptr || SCB == nullptr) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(CB)) return I8LT_ERR_MISALIGNED;
+  if (int d = check_device()) return d;
+  const bool vec = (K % 8) == 0;
+  return cuda_status(launch_quantize_weight(W, wt, N, K, round_up(K, 16), vec, CB, SCB,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+size_t i8lt_forward_workspace_size(int64_t M, int64_t K, int64_t N, int64_t max_outliers) {
+  if (M < 0 || K < 0 || N < 0 || max_outliers < 0) return 0;
+  return fwd_layout(M, K, N, max_outliers).total;
+}
+
+int i8lt_forward_workspace_layout(int64_t M, int64_t K, int64_t N, int64_t max_outliers, i8lt_fwd_layout* out) {
+  if (out == nullptr || M < 0 || K < 0 || N < 0 || max_outliers < 0) return I8LT_ERR_INVALID_ARG;
+  *out = fwd_layout(M, K, N, max_outliers);
+  return I8LT_OK;
+}
+
+int i8lt_forward(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, const float* SCB, int64_t N,
+                 const void* bias, int bt, float threshold, const void* residual, void* out, void* ws,
+                 size_t ws_bytes, int64_t max_outliers, const i8lt_fwd_debug* dbg, void* stream) {
+  if (!valid_dt(at) || (bias != nullptr && !valid_dt(bt))) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (M < 0 || N <= 0 || K <= 0 || max_outliers < 0) return I8LT_ERR_INVALID_ARG;
+  if (K > I8LT_MAX_K) return I8LT_ERR_K_TOO_LARGE;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
+  if (CB == nullptr || SCB == nullptr || ws == nullptr) return I8LT_ERR_INVALID_ARG;
+  if (M > 0 && (A == nullptr || out == nullptr)) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(CB) || !aligned16(out) || !aligned16(residual)) return I8LT_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
+  const i8lt_fwd_layout L = fwd_layout(M, K, N, max_outliers);
+  if (ws_bytes < L.total) return I8LT_ERR_WORKSPACE;
+  if (dbg != nullptr && dbg->acc_i32 != nullptr && !aligned16(dbg->acc_i32)) return I8LT_ERR_MISALIGNED;
+  if (int d = check_device()) return d;
+  if (M == 0) return I8LT_OK;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  DevStatus* st = reinterpret_cast<DevStatus*>(w + L.status);
+  uint32_t* colmax = reinterpret_cast<uint32_t*>(w + L.colmax);
+  uint32_t* mask = reinterpret_cast<uint32_t*>(w + L.mask);
+  int* idx = reinterpret_cast<int*>(w + L.idx);
+  float* SCA = reinterpret_cast<float*>(w + L.sca);
+  __half* Aq = reinterpret_cast<__half*>(w + L.aq);
+  __half* subA = reinterpret_cast<__half*>(w + L.suba);
+  __half* subB = reinterpret_cast<__half*>(w + L.subb);
+  const bool enabled = threshold_enabled(threshold);
+  const bool vec = (K % 8) == 0;
+  cudaError_t e = cudaSuccess;
+
+  if (enabled) {
+    if ((e = cudaMemsetAsync(colmax, 0, static_cast<size_t>(K) * 4, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+    if ((e = launch_colmax(A, at, M, K, vec, colmax, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+    if ((e = launch_outlier_index(colmax, K, threshold, max_outliers, idx, mask, st, s)) != cudaSuccess)
+      return I8LT_ERR_CUDA;
+  } else {
+    if ((e = cudaMemsetAsync(&st->found, 0, 2 * sizeof(int), s)) != cudaSuccess) return I8LT_ERR_CUDA;
+  }
+  if ((e = launch_row_quantize(A, at, M, K, L.k_pad, vec, enabled ? mask : nullptr, idx, st, L.cap_pad, SCA, Aq,
+                               enabled ? subA : nullptr, s)) != cudaSuccess)
+    return I8LT_ERR_CUDA;
+  const bool with_outliers = enabled && L.cap_pad > 0;
+  if (with_outliers) {
+    if ((e = launch_build_subB(CB, L.k_pad, SCB, N, idx, st, L.cap_pad, subB, s)) != cudaSuccess)
+      return I8LT_ERR_CUDA;
+  }
+
+  FwdGemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  if (!make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Aq, L.k_pad, M, L.k_pad * 2, kBK, kFwdBM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, CB, L.k_pad, N, L.k_pad, kBK, kFwdBN,
+                 CU_TENSOR_MAP_SWIZZLE_NONE))
+    return I8LT_ERR_CUDA;
+  if (with_outliers) {
+    if (!make_tmap(&g.tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subA, L.cap_pad, M, L.cap_pad * 2, kBK, kFwdBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap(&g.tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subB, L.cap_pad, N, L.cap_pad * 2, kBK, kFwdBN,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return I8LT_ERR_CUDA;
+  }
+  FwdEpiArgs ea;
+  ea.M = static_cast<int>(M);
+  ea.N = static_cast<int>(N);
+  ea.K_pad = static_cast<int>(L.k_pad);
+  ea.use_outliers = with_outliers ? 1 : 0;
+  ea.SCA = SCA;
+  ea.SCB = SCB;
+  ea.bias = bias;
+  ea.bias_dt = bt;
+  ea.residual = residual;
+  ea.out = out;
+  ea.out_dt = at;
+  ea.acc_i32 = dbg != nullptr ? dbg->acc_i32 : nullptr;
+  ea.st = st;
+  return cuda_status(launch_fwd_gemm(g, ea, s));
+}
+
+size_t i8lt_backward_workspace_size(int64_t M, int64_t N, int gt) {
+  if (M < 0 || N < 0 || !valid_dt(gt)) return 0;
+  return bwd_layout(M, N, gt).total;
+}
+
+int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_t* CB, const float* SCB, int64_t K,
+                        const void* addend, void* grad_A, void* grad_bias, int bt, void* ws, size_t ws_bytes,
+                        void* stream) {
+  if (!valid_dt(gt) || (grad_bias != nullptr && !valid_dt(bt))) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (M < 0 || N <= 0 || K <= 0) return I8LT_ERR_INVALID_ARG;
+  if (K > I8LT_MAX_K) return I8LT_ERR_K_TOO_LARGE;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
+  if (ws == nullptr) return I8LT_ERR_WORKSPACE;
+  if (grad_A != nullptr && (CB == nullptr || SCB == nullptr)) return I8LT_ERR_INVALID_ARG;
+  if (M > 0 && G == nullptr) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(G) || !aligned16(CB) || !aligned16(grad_A) || !aligned16(addend)) return I8LT_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
+  const BwdLayout L = bwd_layout(M, N, gt);
+  if (ws_bytes < L.total) return I8LT_ERR_WORKSPACE;
+  if (int d = check_device()) return d;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  DevStatus* st = reinterpret_cast<DevStatus*>(w + L.status);
+  float* partial = reinterpret_cast<float*>(w + L.partial);
+  const bool g16_needed = grad_A != nullptr && M > 0 && needs_g16(N, gt);
+  __half* G16 = g16_needed ? reinterpret_cast<__half*>(w + L.g16) : nullptr;
+  const bool vec = (N % 8) == 0;
+
+  if (grad_bias != nullptr || G16 != nullptr) {
+    if (launch_gradout_prepass(G, gt, M, N, vec, G16, L.n_pad, grad_bias, bt, partial, L.chunks, s) != cudaSuccess)
+      return I8LT_ERR_CUDA;
+  }
+  if (grad_A == nullptr || M == 0) return I8LT_OK;
+
+  const int64_t k_pad = round_up(K, 16);
+  BwdGemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  const void* gsrc = G16 != nullptr ? static_cast<const void*>(G16) : G;
+  const int64_t gpitch = G16 != nullptr ? L.n_pad : N;
+  if (!make_tmap(&g.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, CB, k_pad, N, k_pad, kBwdBM, kBK,
+                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_tmap(&g.tmG, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, gsrc, gpitch, M, gpitch * 2, kBK, kBwdBN,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return I8LT_ERR_CUDA;
+  BwdEpiArgs ea;
+  ea.M = static_cast<int>(M);
+  ea.N = static_cast<int>(N);
+  ea.K = static_cast<int>(K);
+  ea.SCB = SCB;
+  ea.addend = addend;
+  ea.grad_A = grad_A;
+  ea.dt = gt;
+  ea.st = st;
+  return cuda_status(launch_bwd_gemm(g, ea, s));
+}
+
+int i8lt_silu_forward(const void* h, int dt, int64_t n, void* out, void* stream) {
+  if (!valid_dt(dt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (n < 0 || (n > 0 && (h == nullptr || out == nullptr))) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(out)) return I8LT_ERR_MISALIGNED;
+  if (int d = check_device()) return d;
+  return cuda_status(launch_silu(h, dt, n, true, out, static_cast<cudaStream_t>(stream)));
+}
+
+int i8lt_silu_backward(const void* g, const void* h, int dt, int64_t n, void* out, void* stream) {
+  if (!valid_dt(dt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (n < 0 || (n > 0 && (g == nullptr || h == nullptr || out == nullptr))) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(g) || !aligned16(h) || !aligned16(out)) return I8LT_ERR_MISALIGNED;
+  if (int d = check_device()) return d;
+  return cuda_status(launch_silu_backward(g, h, dt, n, true, out, static_cast<cudaStream_t>(stream)));
+}
+
+int i8lt_profile_start(int max_launches) {
+  if (max_launches < 0) return I8LT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof.clear();
+  g_ev_next = 0;
+  g_prof_count = 0;
+  g_prof_max = max_launches;
+  g_prof_on = true;
+  return I8LT_OK;
+}
+
+int i8lt_profile_stop(i8lt_kernel_time* out, int cap, int* n_records, int* n_launches) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = false;
+  int st = I8LT_OK;
+  int k = 0;
+  for (const ProfRec& r : g_prof) {
+    float ms = -1.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+      st = I8LT_ERR_CUDA;
+      ms = -1.f;
+    }
+    if (out != nullptr && k < cap) out[k++] = i8lt_kernel_time{r.id, ms};
+  }
+  if (n_records != nullptr) *n_records = k;
+  if (n_launches != nullptr) *n_launches = g_prof_count;
+  g_prof.clear();
+  g_ev_next = 0;
+  return st;
+}
+
+const char* i8lt_kernel_name(int k) {
+  static const char* names[] = {"quantize_weight", "colmax",          "outlier_index",      "row_quantize",
+                                "build_subB",      "fwd_gemm",        "gradout_prepass",    "grad_bias_finalize",
+                                "bwd_gemm",        "silu",            "silu_backward"};
+  return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
+}
+
+int i8lt_read_device_status(void* ws, int32_t* status, int32_t* outliers, void* stream) {
+  if (ws == nullptr) return I8LT_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus h;
+  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return I8LT_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return I8LT_ERR_CUDA;
+  if (h.status != 0 && cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return I8LT_ERR_CUDA;
+  if (status != nullptr) *status = h.status;
+  if (outliers != nullptr) *outliers = h.found;
+  return h.status;
+}
+
+}  // extern "C"

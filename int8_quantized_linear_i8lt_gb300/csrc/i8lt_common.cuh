@@ -1,0 +1,352 @@
+// Shared device helpers: dtypes, status codes, and inline-PTX wrappers for
+// mbarrier, TMA (cp.async.bulk.tensor) and the 5th-generation tensor cores
+// (tcgen05: TMEM allocation, MMA, commit, TMEM load/store).  sm_103a only.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace i8lt {
+
+enum Dtype { DT_F16 = 0, DT_BF16 = 1, DT_F32 = 2 };
+
+enum Status {
+  ST_OK = 0,
+  ST_INVALID_ARG = 1,
+  ST_UNSUPPORTED_DTYPE = 2,
+  ST_MISALIGNED = 3,
+  ST_WORKSPACE = 4,
+  ST_K_TOO_LARGE = 5,
+  ST_OUTLIER_CAPACITY = 6,
+  ST_TIMEOUT = 7,
+  ST_CUDA = 8,
+  ST_DEVICE = 9,
+};
+
+// Layout of the status word at the start of every workspace.
+struct DevStatus {
+  int status;      // first device-side error, 0 if none
+  int found;       // outlier columns found by the last forward
+  int used;        // outlier columns used (min(found, capacity))
+  int where;       // which wait timed out (role id), for diagnosis
+};
+
+// A pipeline wait that has not completed after this long (wall clock, ns)
+// is treated as a failure: the kernel records ST_TIMEOUT and winds down.
+constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
+
+// ---------------------------------------------------------------------------
+// element conversions
+// ---------------------------------------------------------------------------
+
+template <int DT> struct Elem;
+template <> struct Elem<DT_F16> { using T = __half; };
+template <> struct Elem<DT_BF16> { using T = __nv_bfloat16; };
+template <> struct Elem<DT_F32> { using T = float; };
+
+// Round-to-nearest-even cast of one stored element to fp16.
+__device__ __forceinline__ __half to_half(__half x) { return x; }
+__device__ __forceinline__ __half to_half(__nv_bfloat16 x) {
+  return __float2half_rn(__bfloat162float(x));
+}
+__device__ __forceinline__ __half to_half(float x) { return __float2half_rn(x); }
+
+__device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_float(float x) { return x; }
+
+template <typename T> __device__ __forceinline__ T from_float(float x);
+template <> __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+template <> __device__ __forceinline__ float from_float<float>(float x) { return x; }
+
+// Load 8 consecutive elements (as fp16-rounded values).  `vec` says the
+// 8-element group is complete and 16-byte aligned.
+template <typename T>
+__device__ __forceinline__ void load8_half(const T* p, int64_t valid, bool vec, __half (&h)[8]);
+
+template <>
+__device__ __forceinline__ void load8_half<__half>(const __half* p, int64_t valid, bool vec, __half (&h)[8]) {
+  if (vec) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const __half* q = reinterpret_cast<const __half*>(&u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = q[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = (i < valid) ? p[i] : __float2half_rn(0.f);
+  }
+}
+template <>
+__device__ __forceinline__ void load8_half<__nv_bfloat16>(const __nv_bfloat16* p, int64_t valid, bool vec,
+                                                          __half (&h)[8]) {
+  if (vec) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = to_half(q[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = (i < valid) ? to_half(p[i]) : __float2half_rn(0.f);
+  }
+}
+template <>
+__device__ __forceinline__ void load8_half<float>(const float* p, int64_t valid, bool vec, __half (&h)[8]) {
+  if (vec) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    h[0] = to_half(a.x); h[1] = to_half(a.y); h[2] = to_half(a.z); h[3] = to_half(a.w);
+    h[4] = to_half(b.x); h[5] = to_half(b.y); h[6] = to_half(b.z); h[7] = to_half(b.w);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = (i < valid) ? to_half(p[i]) : __float2half_rn(0.f);
+  }
+}
+
+// Load 8 consecutive elements widened to fp32 (exact).
+template <typename T>
+__device__ __forceinline__ void load8_float(const T* p, int64_t valid, bool vec, float (&f)[8]) {
+  if (vec) {
+    if constexpr (sizeof(T) == 4) {
+      float4 a = __ldg(reinterpret_cast<const float4*>(p));
+      float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+      f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+      f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    } else {
+      uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+      const T* q = reinterpret_cast<const T*>(&u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = to_float(q[i]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = (i < valid) ? to_float(p[i]) : 0.f;
+  }
+}
+
+// Store 8 consecutive elements rounded from fp32.
+template <typename T>
+__device__ __forceinline__ void store8(T* p, int64_t valid, bool vec, const float (&f)[8]) {
+  if (vec) {
+    if constexpr (sizeof(T) == 4) {
+      reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+      reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+    } else {
+      uint4 u;
+      T* q = reinterpret_cast<T*>(&u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = from_float<T>(f[i]);
+      *reinterpret_cast<uint4*>(p) = u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < valid) p[i] = from_float<T>(f[i]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// status word
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void set_status(DevStatus* st, int code, int where = 0) {
+  if (st == nullptr) return;
+  if (atomicCAS(&st->status, 0, code) == 0) st->where = where;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// shared memory, mbarrier
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on the phase with the given parity.  Returns false when the
+// CTA is aborting (another role timed out) or when this wait timed out; in
+// the latter case it raises the CTA's abort flag and records ST_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          DevStatus* st, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        set_status(st, ST_TIMEOUT, where);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+// 2-D tiled load of the box at element coordinates (x = inner, y = outer).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (TMEM + MMA)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, fp16 inputs, fp32 accumulation.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (16-byte units), fixed version bits 46-48 = 0b001,
+// base offset 0 (atoms are 1024-byte aligned), swizzle mode in bits 61-63.
+constexpr uint32_t kSwizzle128B = 2;
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(swz & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with fp16 A and B and fp32 D.
+// a_mn / b_mn: operand stored MN-major (transposed) instead of K-major.
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                                   // D format: f32
+         | (0u << 7) | (0u << 10)                    // A, B format: f16
+         | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16)
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// 32 lanes x 32 columns of 32-bit TMEM -> registers (then waits).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// registers -> 32 lanes x 32 columns of TMEM (then waits).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+      "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier over `nthreads` threads that also returns the AND of `pred`
+// over them: every participant leaves with the same answer.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+}  // namespace i8lt

@@ -1,0 +1,115 @@
+// Host-side launchers shared between the translation units of libi8lt.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "i8lt_common.cuh"
+
+namespace i8lt {
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+inline int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
+
+// ---- kernel timing (i8lt_api.cu): no-ops unless i8lt_profile_start ran ----
+void prof_begin(int kernel_id, cudaStream_t s);
+void prof_end(cudaStream_t s);
+
+struct ProfScope {
+  cudaStream_t s;
+  ProfScope(int id, cudaStream_t st) : s(st) { prof_begin(id, st); }
+  ~ProfScope() { prof_end(s); }
+};
+
+// ---- memory-bound kernels (i8lt_quant.cu) --------------------------------
+
+// K1: W [N,K] (dtype wt) -> CB int8 [N, ld] (zero pad), SCB fp32 [N].
+cudaError_t launch_quantize_weight(const void* W, int wt, int64_t N, int64_t K, int64_t ld, bool vec,
+                                   int8_t* CB, float* SCB, cudaStream_t s);
+
+// K2: colmax[k] = fp16 bits of max_m |fp16(A[m,k])| (atomic max; colmax must
+// be zeroed first).
+cudaError_t launch_colmax(const void* A, int at, int64_t M, int64_t K, bool vec, uint32_t* colmax,
+                          cudaStream_t s);
+
+// Outlier set from colmax: mask bits, ascending idx[], found/used counts.
+cudaError_t launch_outlier_index(const uint32_t* colmax, int64_t K, float thr, int64_t cap, int* idx,
+                                 uint32_t* mask, DevStatus* st, cudaStream_t s);
+
+// K3: SCA[m], Aq [M, K_pad] (codes as exact fp16), subA [M, cap_pad].
+cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int64_t K_pad, bool vec,
+                                const uint32_t* mask, const int* idx, const DevStatus* st, int64_t cap_pad,
+                                float* SCA, __half* Aq, __half* subA, cudaStream_t s);
+
+// K4: subB[n, j] = fp16(fp32(CB[n, idx[j]]) * SCB[n] * fp32(1/127)).
+cudaError_t launch_build_subB(const int8_t* CB, int64_t ld, const float* SCB, int64_t N, const int* idx,
+                              const DevStatus* st, int64_t cap_pad, __half* subB, cudaStream_t s);
+
+// K7: grad_bias partial sums of the uncast G and (optionally) G16 = fp16(G)
+// with N padded to N_pad.
+cudaError_t launch_gradout_prepass(const void* G, int gt, int64_t M, int64_t N, bool vec, __half* G16,
+                                   int64_t N_pad, void* grad_bias, int bt, float* partial,
+                                   int64_t max_chunks, cudaStream_t s);
+int64_t gradout_partial_chunks(int64_t M);
+
+cudaError_t launch_silu(const void* h, int dt, int64_t n, bool vec, void* out, cudaStream_t s);
+cudaError_t launch_silu_backward(const void* g, const void* h, int dt, int64_t n, bool vec, void* out,
+                                 cudaStream_t s);
+
+// ---- tensor-core GEMMs (i8lt_gemm.cu) -------------------------------------
+
+struct FwdGemmArgs {
+  CUtensorMap tmA;    // Aq fp16 [M, K_pad], box 64 x 128, 128B swizzle
+  CUtensorMap tmB;    // CB int8 [N, K_pad], box 64 x 256, no swizzle
+  CUtensorMap tmSA;   // subA fp16 [M, cap_pad], box 64 x 128, 128B swizzle
+  CUtensorMap tmSB;   // subB fp16 [N, cap_pad], box 64 x 256, 128B swizzle
+};
+
+struct FwdEpiArgs {
+  int M, N, K_pad;
+  int use_outliers;       // 0: decomposition disabled
+  const float* SCA;
+  const float* SCB;
+  const void* bias;
+  int bias_dt;
+  const void* residual;
+  void* out;
+  int out_dt;
+  int32_t* acc_i32;       // optional raw accumulator
+  DevStatus* st;
+};
+
+cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s);
+
+struct BwdGemmArgs {
+  CUtensorMap tmW;    // CB int8 [N, K_pad] viewed as (inner K_pad, outer N), box 128 x 64
+  CUtensorMap tmG;    // G16 fp16 [M, N_pad], box 64 x 256, 128B swizzle
+};
+
+struct BwdEpiArgs {
+  int M, N, K;
+  const float* SCB;
+  const void* addend;
+  void* grad_A;
+  int dt;
+  DevStatus* st;
+};
+
+cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaStream_t s);
+
+// Kernel ids of the timing records (match i8lt_kernel_id in i8lt.h).
+enum KernelId {
+  K_QUANTIZE_WEIGHT = 0, K_COLMAX, K_OUTLIER_INDEX, K_ROW_QUANTIZE, K_SUBB, K_FWD_GEMM, K_GRADOUT_PREPASS,
+  K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_COUNT
+};
+
+// Tile sizes shared with the host code that builds the tensor maps.
+constexpr int kFwdBM = 128;   // rows of A (tokens) per tile
+constexpr int kFwdBN = 256;   // rows of CB (output features) per tile
+constexpr int kBwdBM = 128;   // output features of grad_A (k) per tile
+constexpr int kBwdBN = 256;   // tokens per tile
+constexpr int kBK = 64;       // reduction elements per pipeline stage
+
+}  // namespace i8lt

@@ -1,0 +1,456 @@
+// Memory-bound kernels of the int8 quantized linear layer (sm_103a):
+//   K1 weight quantization, K2 outlier-column detection, the outlier index
+//   build, K3 row-wise (vector-wise) activation quantization, K4 the fp16
+//   outlier weight columns, K7 the grad_output prepass (grad_bias + fp16 cast)
+//   and the SiLU between MLP layers.
+//
+// Method: bitsandbytes PR #33 "Memory efficient backward" (PR description and
+// the review threads on bitsandbytes/autograd/_functions.py).  All loads and
+// stores move 16 bytes per thread when rows are 16-byte aligned.
+#include <algorithm>
+#include <type_traits>
+
+#include "i8lt_internal.h"
+
+namespace i8lt {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float r = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0.f;
+  if (w == 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, o));
+    if (l == 0) red[0] = r;
+  }
+  __syncthreads();
+  r = red[0];
+  __syncthreads();
+  return r;
+}
+
+// q = round_half_even(x * s) in IEEE fp32 (s = 127 / absmax), |q| <= 127.
+__device__ __forceinline__ int quant_code(float x, float s) {
+  int q = __float2int_rn(__fmul_rn(x, s));
+  return max(-127, min(127, q));
+}
+
+// ---------------------------------------------------------------------------
+// K1 (weights) and K3 (activations): row-wise absmax quantization.
+// One block per row (grid-stride).  Pass 1: absmax of the fp16-cast row
+// outside the outlier columns.  Pass 2: codes, zero for outlier columns and
+// for the padding up to ld.  Activations also gather their outlier columns.
+// ---------------------------------------------------------------------------
+template <typename T, typename OutT>
+__global__ void __launch_bounds__(kThreads) row_quantize_kernel(
+    const T* __restrict__ A, int64_t M, int64_t K, int64_t ld, int vec, const uint32_t* __restrict__ mask,
+    const int* __restrict__ idx, const DevStatus* __restrict__ st, int64_t cap_pad, float* __restrict__ scale,
+    OutT* __restrict__ codes, __half* __restrict__ sub) {
+  __shared__ float red[32];
+  const int used = (mask != nullptr) ? st->used : 0;
+  const int used_pad = (used + 63) / 64 * 64;
+  for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+    const T* row = A + m * K;
+    float amax = 0.f;
+    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < K; c += kThreads * 8) {
+      __half h[8];
+      load8_half(row + c, K - c, vec != 0 && c + 8 <= K, h);
+      const uint32_t bits = (mask != nullptr) ? ((mask[c >> 5] >> (c & 31)) & 0xFFu) : 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (!((bits >> i) & 1u)) amax = fmaxf(amax, fabsf(__half2float(h[i])));
+    }
+    amax = block_max(amax, red);
+    const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
+    OutT* out = codes + m * ld;
+    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < ld; c += kThreads * 8) {
+      __half h[8];
+      if (c < K) {
+        load8_half(row + c, K - c, vec != 0 && c + 8 <= K, h);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = __float2half_rn(0.f);
+      }
+      const uint32_t bits = (mask != nullptr && c < K) ? ((mask[c >> 5] >> (c & 31)) & 0xFFu) : 0u;
+      int q[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        q[i] = (amax > 0.f && !((bits >> i) & 1u)) ? quant_code(__half2float(h[i]), s) : 0;
+      if constexpr (sizeof(OutT) == 1) {
+        uint2 u;
+        u.x = (q[0] & 0xFF) | ((q[1] & 0xFF) << 8) | ((q[2] & 0xFF) << 16) | ((q[3] & 0xFF) << 24);
+        u.y = (q[4] & 0xFF) | ((q[5] & 0xFF) << 8) | ((q[6] & 0xFF) << 16) | ((q[7] & 0xFF) << 24);
+        *reinterpret_cast<uint2*>(out + c) = u;   // ld % 16 == 0, c % 8 == 0
+      } else {
+        uint4 u;
+        __half* o = reinterpret_cast<__half*>(&u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = __int2half_rn(q[i]);   // exact: |q| <= 127
+        *reinterpret_cast<uint4*>(out + c) = u;
+      }
+    }
+    if (sub != nullptr) {
+      for (int j = threadIdx.x; j < used_pad; j += kThreads)
+        sub[m * cap_pad + j] = (j < used) ? to_half(row[idx[j]]) : __float2half_rn(0.f);
+    }
+    if (threadIdx.x == 0) scale[m] = amax;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K2: per-column max of |fp16(A)|.  Block = 32 column groups of 8 x 8 row
+// lanes; each block covers 256 columns x kColRows rows, then one atomicMax
+// per column.  fp16 magnitudes compare as unsigned integers.
+// ---------------------------------------------------------------------------
+constexpr int kColRows = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) colmax_kernel(const T* __restrict__ A, int64_t M, int64_t K, int vec,
+                                                          uint32_t* __restrict__ colmax) {
+  __shared__ uint16_t red[8][256 + 8];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 32 + tx) * 8;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColRows;
+  const int64_t r1 = min(M, r0 + kColRows);
+  uint32_t mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = 0;
+  if (c0 < K) {
+    for (int64_t r = r0 + ty; r < r1; r += 8) {
+      __half h[8];
+      load8_half(A + r * K + c0, K - c0, vec != 0 && c0 + 8 <= K, h);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = max(mx[i], static_cast<uint32_t>(__half_as_ushort(h[i]) & 0x7FFFu));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[ty][tx * 8 + i] = static_cast<uint16_t>(mx[i]);
+  __syncthreads();
+  // 256 threads reduce 256 columns over the 8 row lanes
+  const int col = threadIdx.x;
+  uint32_t v = 0;
+#pragma unroll
+  for (int y = 0; y < 8; ++y) v = max(v, static_cast<uint32_t>(red[y][col]));
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * 256 + col;
+  if (k < K && v != 0) atomicMax(colmax + k, v);
+}
+
+// ---------------------------------------------------------------------------
+// Outlier index build (one block of 1024 threads): mask bit k set when
+// fp16(colmax[k]) > thr; ascending idx[] by a block-wide exclusive scan.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) outlier_index_kernel(const uint32_t* __restrict__ colmax, int64_t K,
+                                                             float thr, int64_t cap, int* __restrict__ idx,
+                                                             uint32_t* __restrict__ mask, DevStatus* st) {
+  __shared__ int wsum[32];
+  const int t = threadIdx.x;
+  const int64_t nwords = (K + 31) / 32;
+  const int64_t wpt = (nwords + 1023) / 1024;
+  const int64_t w0 = t * wpt, w1 = min(nwords, w0 + wpt);
+  int count = 0;
+  for (int64_t w = w0; w < w1; ++w) {
+    uint32_t bits = 0;
+    for (int b = 0; b < 32; ++b) {
+      const int64_t k = w * 32 + b;
+      if (k < K && __half2float(__ushort_as_half(static_cast<unsigned short>(colmax[k]))) > thr) bits |= 1u << b;
+    }
+    mask[w] = bits;
+    count += __popc(bits);
+  }
+  // exclusive scan of count over the block
+  int incl = count;
+  const int lane = t & 31, w = t >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int v = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    wsum[lane] = v;   // inclusive over warps
+  }
+  __syncthreads();
+  const int offset = incl - count + (w > 0 ? wsum[w - 1] : 0);
+  int j = offset;
+  for (int64_t ww = w0; ww < w1; ++ww) {
+    uint32_t bits = mask[ww];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (j < cap) idx[j] = static_cast<int>(ww * 32 + b);
+      ++j;
+    }
+  }
+  if (t == 1023) {
+    const int total = wsum[31];
+    st->found = total;
+    st->used = static_cast<int>(min(static_cast<int64_t>(total), cap));
+    if (total > cap) set_status(st, ST_OUTLIER_CAPACITY, 0);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K4: subB[n, j] = fp16_rn(fp32(CB[n, idx[j]]) * (SCB[n] * fp32(1/127))),
+// zero for used <= j < used_pad.  One warp per row.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) build_subB_kernel(const int8_t* __restrict__ CB, int64_t ld,
+                                                              const float* __restrict__ SCB, int64_t N,
+                                                              const int* __restrict__ idx,
+                                                              const DevStatus* __restrict__ st, int64_t cap_pad,
+                                                              __half* __restrict__ subB) {
+  const int used = st->used;
+  const int used_pad = (used + 63) / 64 * 64;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int64_t n = warp; n < N; n += nwarps) {
+    const float f = __fmul_rn(SCB[n], 1.0f / 127.0f);
+    for (int j = lane; j < used_pad; j += 32)
+      subB[n * cap_pad + j] =
+          (j < used) ? __float2half_rn(__fmul_rn(static_cast<float>(CB[n * ld + idx[j]]), f)) : __float2half_rn(0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K7: grad_output prepass.  Column sums of the uncast G in fp32 per chunk of
+// kSumRows rows (deterministic order), optional G16 = fp16_rn(G) padded to
+// N_pad columns.  Then a finalize kernel sums the chunks in order.
+// ---------------------------------------------------------------------------
+constexpr int kSumRows = 512;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) gradout_prepass_kernel(const T* __restrict__ G, int64_t M, int64_t N,
+                                                                   int vec, __half* __restrict__ G16,
+                                                                   int64_t N_pad, float* __restrict__ partial) {
+  __shared__ float red[8][256 + 4];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 32 + tx) * 8;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kSumRows;
+  const int64_t r1 = min(M, r0 + kSumRows);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  const int64_t width = (G16 != nullptr) ? N_pad : N;
+  if (c0 < width) {
+    for (int64_t r = r0 + ty; r < r1; r += 8) {
+      float f[8];
+      if (c0 < N) {
+        load8_float(G + r * N + c0, N - c0, vec != 0 && c0 + 8 <= N, f);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+      if (G16 != nullptr) {
+        uint4 u;
+        __half* o = reinterpret_cast<__half*>(&u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = __float2half_rn(f[i]);
+        *reinterpret_cast<uint4*>(G16 + r * N_pad + c0) = u;   // N_pad % 8 == 0
+      }
+    }
+  }
+  if (partial == nullptr) return;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[ty][tx * 8 + i] = acc[i];
+  __syncthreads();
+  const int col = threadIdx.x;
+  float s = 0.f;
+#pragma unroll
+  for (int y = 0; y < 8; ++y) s += red[y][col];
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * 256 + col;
+  if (n < N) partial[static_cast<int64_t>(blockIdx.y) * N + n] = s;
+}
+
+template <typename BT>
+__global__ void __launch_bounds__(kThreads) grad_bias_finalize_kernel(const float* __restrict__ partial,
+                                                                      int64_t chunks, int64_t N,
+                                                                      BT* __restrict__ grad_bias) {
+  for (int64_t n = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; n < N;
+       n += static_cast<int64_t>(gridDim.x) * kThreads) {
+    float s = 0.f;
+    for (int64_t c = 0; c < chunks; ++c) s += partial[c * N + n];
+    grad_bias[n] = from_float<BT>(s);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// SiLU between MLP layers: y = h * sigmoid(h); dh = g * s * (1 + h (1 - s)).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) silu_kernel(const T* __restrict__ h, int64_t n, int vec,
+                                                        T* __restrict__ out) {
+  for (int64_t c = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * 8; c < n;
+       c += static_cast<int64_t>(gridDim.x) * kThreads * 8) {
+    float x[8], y[8];
+    const bool v = vec != 0 && c + 8 <= n;
+    load8_float(h + c, n - c, v, x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = x[i] * sigmoidf_(x[i]);
+    store8(out + c, n - c, v, y);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) silu_backward_kernel(const T* __restrict__ g, const T* __restrict__ h,
+                                                                 int64_t n, int vec, T* __restrict__ out) {
+  for (int64_t c = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * 8; c < n;
+       c += static_cast<int64_t>(gridDim.x) * kThreads * 8) {
+    float x[8], gg[8], y[8];
+    const bool v = vec != 0 && c + 8 <= n;
+    load8_float(h + c, n - c, v, x);
+    load8_float(g + c, n - c, v, gg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float s = sigmoidf_(x[i]);
+      y[i] = gg[i] * (s * (1.0f + x[i] * (1.0f - s)));
+    }
+    store8(out + c, n - c, v, y);
+  }
+}
+
+int grid_rows(int64_t rows) {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  return static_cast<int>(rows < cap ? (rows > 0 ? rows : 1) : cap);
+}
+
+template <typename F>
+cudaError_t dispatch_dt(int dt, F&& f) {
+  switch (dt) {
+    case DT_F16: return f(static_cast<__half*>(nullptr));
+    case DT_BF16: return f(static_cast<__nv_bfloat16*>(nullptr));
+    case DT_F32: return f(static_cast<float*>(nullptr));
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_weight(const void* W, int wt, int64_t N, int64_t K, int64_t ld, bool vec, int8_t* CB,
+                                   float* SCB, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  return dispatch_dt(wt, [&](auto* tag) {
+    using T = std::remove_pointer_t<decltype(tag)>;
+    ProfScope ps(K_QUANTIZE_WEIGHT, s);
+    row_quantize_kernel<T, int8_t><<<grid_rows(N), kThreads, 0, s>>>(
+        static_cast<const T*>(W), N, K, ld, vec ? 1 : 0, nullptr, nullptr, nullptr, 0, SCB, CB, nullptr);
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_colmax(const void* A, int at, int64_t M, int64_t K, bool vec, uint32_t* colmax,
+                          cudaStream_t s) {
+  if (M == 0 || K == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(ceil_div(K, 256)), static_cast<unsigned>(ceil_div(M, kColRows)));
+  return dispatch_dt(at, [&](auto* tag) {
+    using T = std::remove_pointer_t<decltype(tag)>;
+    ProfScope ps(K_COLMAX, s);
+    colmax_kernel<T><<<grid, kThreads, 0, s>>>(static_cast<const T*>(A), M, K, vec ? 1 : 0, colmax);
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_outlier_index(const uint32_t* colmax, int64_t K, float thr, int64_t cap, int* idx,
+                                 uint32_t* mask, DevStatus* st, cudaStream_t s) {
+  ProfScope ps(K_OUTLIER_INDEX, s);
+  outlier_index_kernel<<<1, 1024, 0, s>>>(colmax, K, thr, cap, idx, mask, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int64_t K_pad, bool vec,
+                                const uint32_t* mask, const int* idx, const DevStatus* st, int64_t cap_pad,
+                                float* SCA, __half* Aq, __half* subA, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  return dispatch_dt(at, [&](auto* tag) {
+    using T = std::remove_pointer_t<decltype(tag)>;
+    ProfScope ps(K_ROW_QUANTIZE, s);
+    row_quantize_kernel<T, __half><<<grid_rows(M), kThreads, 0, s>>>(
+        static_cast<const T*>(A), M, K, K_pad, vec ? 1 : 0, mask, idx, st, cap_pad, SCA, Aq, subA);
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_build_subB(const int8_t* CB, int64_t ld, const float* SCB, int64_t N, const int* idx,
+                              const DevStatus* st, int64_t cap_pad, __half* subB, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(N, kThreads / 32), 152 * 8));
+  ProfScope ps(K_SUBB, s);
+  build_subB_kernel<<<blocks, kThreads, 0, s>>>(CB, ld, SCB, N, idx, st, cap_pad, subB);
+  return cudaGetLastError();
+}
+
+int64_t gradout_partial_chunks(int64_t M) { return ceil_div(M > 0 ? M : 1, kSumRows); }
+
+cudaError_t launch_gradout_prepass(const void* G, int gt, int64_t M, int64_t N, bool vec, __half* G16,
+                                   int64_t N_pad, void* grad_bias, int bt, float* partial, int64_t max_chunks,
+                                   cudaStream_t s) {
+  const int64_t chunks = gradout_partial_chunks(M);
+  if (chunks > max_chunks) return cudaErrorInvalidValue;
+  const int64_t width = (G16 != nullptr) ? N_pad : N;
+  if (M > 0 && width > 0) {
+    const dim3 grid(static_cast<unsigned>(ceil_div(width, 256)), static_cast<unsigned>(chunks));
+    cudaError_t e = dispatch_dt(gt, [&](auto* tag) {
+      using T = std::remove_pointer_t<decltype(tag)>;
+      ProfScope ps(K_GRADOUT_PREPASS, s);
+      gradout_prepass_kernel<T><<<grid, kThreads, 0, s>>>(static_cast<const T*>(G), M, N, vec ? 1 : 0, G16, N_pad,
+                                                          grad_bias != nullptr ? partial : nullptr);
+      return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return e;
+  }
+  if (grad_bias == nullptr || N == 0) return cudaSuccess;
+  if (M == 0) return cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(N) * (bt == DT_F32 ? 4 : 2), s);
+  const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(N, kThreads), 152 * 4));
+  return dispatch_dt(bt, [&](auto* tag) {
+    using BT = std::remove_pointer_t<decltype(tag)>;
+    ProfScope ps(K_GRAD_BIAS_FINALIZE, s);
+    grad_bias_finalize_kernel<BT><<<blocks, kThreads, 0, s>>>(partial, chunks, N, static_cast<BT*>(grad_bias));
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_silu(const void* h, int dt, int64_t n, bool vec, void* out, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(n, kThreads * 8), 152 * 8));
+  return dispatch_dt(dt, [&](auto* tag) {
+    using T = std::remove_pointer_t<decltype(tag)>;
+    ProfScope ps(K_SILU, s);
+    silu_kernel<T><<<blocks, kThreads, 0, s>>>(static_cast<const T*>(h), n, vec ? 1 : 0, static_cast<T*>(out));
+    return cudaGetLastError();
+  });
+}
+
+cudaError_t launch_silu_backward(const void* g, const void* h, int dt, int64_t n, bool vec, void* out,
+                                 cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(n, kThreads * 8), 152 * 8));
+  return dispatch_dt(dt, [&](auto* tag) {
+    using T = std::remove_pointer_t<decltype(tag)>;
+    ProfScope ps(K_SILU_BACKWARD, s);
+    silu_backward_kernel<T><<<blocks, kThreads, 0, s>>>(static_cast<const T*>(g), static_cast<const T*>(h), n,
+                                                        vec ? 1 : 0, static_cast<T*>(out));
+    return cudaGetLastError();
+  });
+}
+
+}  // namespace i8lt

@@ -1,0 +1,246 @@
+"""Torch-facing calls of the int8 quantized linear layer.
+
+PyTorch supplies device memory (the caching allocator), the current stream
+and autograd; every arithmetic step runs in libi8lt's CUDA kernels.  The
+calls fail loudly when the library is missing or the device is not sm_103.
+
+Method: the memory-efficient Linear8bitLt of bitsandbytes PR #33 "Memory
+efficient backward" (see include/i8lt.h for the formulas).
+"""
+from __future__ import annotations
+
+import math
+import warnings
+
+import torch
+
+from . import _lib
+
+DTYPE_CODE = {torch.float16: _lib.I8LT_F16, torch.bfloat16: _lib.I8LT_BF16, torch.float32: _lib.I8LT_F32}
+
+
+class I8LTError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str):
+    if status != _lib.I8LT_OK:
+        raise I8LTError(f"{what}: {_lib.i8lt_status_string(status)} (status {status})")
+
+
+def _code(dtype: torch.dtype) -> int:
+    try:
+        return DTYPE_CODE[dtype]
+    except KeyError:
+        raise I8LTError(f"unsupported dtype {dtype}") from None
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise I8LTError("libi8lt runs on CUDA tensors only (no CPU path)")
+
+
+def default_max_outliers(K: int) -> int:
+    """Capacity for outlier columns: 1/16 of the features, at least 256."""
+    return min(K, max(256, K // 16))
+
+
+def weight_ld(K: int) -> int:
+    return _lib.i8lt_weight_ld(K)
+
+
+def quantize_weight(W: torch.Tensor):
+    """W [N, K] (f16 / bf16 / f32, CUDA) -> (CB int8 [N, ld], SCB fp32 [N])."""
+    _require_cuda(W)
+    W = W.contiguous()
+    N, K = W.shape
+    CB = torch.empty(N, weight_ld(K), dtype=torch.int8, device=W.device)
+    SCB = torch.empty(N, dtype=torch.float32, device=W.device)
+    _check(_lib.i8lt_quantize_weight(W.data_ptr(), _code(W.dtype), N, K, CB.data_ptr(), SCB.data_ptr(),
+                                     _stream(W)), "i8lt_quantize_weight")
+    return CB, SCB
+
+
+def forward_workspace(M: int, K: int, N: int, max_outliers: int, device) -> torch.Tensor:
+    n = _lib.i8lt_forward_workspace_size(M, K, N, max_outliers)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def backward_workspace(M: int, N: int, dtype: torch.dtype, device) -> torch.Tensor:
+    n = _lib.i8lt_backward_workspace_size(M, N, _code(dtype))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def forward(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, bias: torch.Tensor | None = None,
+            threshold: float = 6.0, residual: torch.Tensor | None = None, max_outliers: int | None = None,
+            out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+            acc_i32: torch.Tensor | None = None):
+    """out [M, N] = int8 linear of A [M, K] (see i8lt_forward).  Returns
+    (out, ws); ``ws`` holds the quantized activations and the outlier set."""
+    _require_cuda(A, CB, SCB, bias, residual)
+    A = A.contiguous()
+    M = A.shape[0]
+    if A.shape[1] != K:
+        raise I8LTError(f"A has {A.shape[1]} features, the weight {K}")
+    N = CB.shape[0]
+    cap = default_max_outliers(K) if max_outliers is None else int(max_outliers)
+    if not (math.isfinite(threshold) and threshold > 0):
+        cap = 0
+    if out is None:
+        out = torch.empty(M, N, dtype=A.dtype, device=A.device)
+    if ws is None:
+        ws = forward_workspace(M, K, N, cap, A.device)
+    if residual is not None:
+        residual = residual.contiguous()
+    bias_c = None if bias is None else bias.contiguous()
+    _check(_lib.i8lt_forward(A.data_ptr(), _code(A.dtype), M, K, CB.data_ptr(), SCB.data_ptr(), N,
+                             _ptr(bias_c), _code(bias_c.dtype) if bias_c is not None else 0, float(threshold),
+                             _ptr(residual), out.data_ptr(), ws.data_ptr(), ws.numel(), cap,
+                             acc_i32=_ptr(acc_i32), stream=_stream(A)), "i8lt_forward")
+    return out, ws
+
+
+def backward_input(G: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, need_grad_A: bool = True,
+                   bias_dtype: torch.dtype | None = None, addend: torch.Tensor | None = None,
+                   ws: torch.Tensor | None = None):
+    """(grad_A [M, K] or None, grad_bias [N] or None) from grad_output G [M, N]."""
+    _require_cuda(G, CB, SCB, addend)
+    G = G.contiguous()
+    M, N = G.shape
+    grad_A = torch.empty(M, K, dtype=G.dtype, device=G.device) if need_grad_A else None
+    grad_bias = torch.empty(N, dtype=bias_dtype, device=G.device) if bias_dtype is not None else None
+    if ws is None:
+        ws = backward_workspace(M, N, G.dtype, G.device)
+    if addend is not None:
+        addend = addend.contiguous()
+    _check(_lib.i8lt_backward_input(G.data_ptr(), _code(G.dtype), M, N, CB.data_ptr(), SCB.data_ptr(), K,
+                                    _ptr(addend), _ptr(grad_A), _ptr(grad_bias),
+                                    _code(bias_dtype) if bias_dtype is not None else 0,
+                                    ws.data_ptr(), ws.numel(), _stream(G)), "i8lt_backward_input")
+    return grad_A, grad_bias
+
+
+def silu(h: torch.Tensor) -> torch.Tensor:
+    _require_cuda(h)
+    h = h.contiguous()
+    out = torch.empty_like(h)
+    _check(_lib.i8lt_silu_forward(h.data_ptr(), _code(h.dtype), h.numel(), out.data_ptr(), _stream(h)),
+           "i8lt_silu_forward")
+    return out
+
+
+def silu_backward(g: torch.Tensor, h: torch.Tensor) -> torch.Tensor:
+    _require_cuda(g, h)
+    g, h = g.contiguous(), h.contiguous()
+    out = torch.empty_like(h)
+    _check(_lib.i8lt_silu_backward(g.data_ptr(), h.data_ptr(), _code(h.dtype), h.numel(), out.data_ptr(),
+                                   _stream(h)), "i8lt_silu_backward")
+    return out
+
+
+def device_status(ws: torch.Tensor):
+    """(status code, outlier columns found) of the last call that used ``ws``
+    (synchronizes the current stream; clears a recorded error)."""
+    r, st, found = _lib.i8lt_read_device_status(ws.data_ptr(), _stream(ws))
+    return st, found
+
+
+# ---------------------------------------------------------------------------
+# autograd
+# ---------------------------------------------------------------------------
+
+_warned_cast = False
+
+
+def _warn_cast(dtype):
+    global _warned_cast
+    if dtype != torch.float16 and not _warned_cast:
+        _warned_cast = True
+        warnings.warn(f"Linear8bitLt: input of dtype {dtype} is cast to float16 for the int8 "
+                      "quantization; the output is cast back to the input's dtype.")
+
+
+class Int8LinearFunction(torch.autograd.Function):
+    """y = int8 linear(x); the weight is frozen (memory-efficient backward:
+    grad to the input and the bias only)."""
+
+    @staticmethod
+    def forward(ctx, x, CB, SCB, bias, threshold, max_outliers):
+        _warn_cast(x.dtype)
+        shape = x.shape
+        K = shape[-1]
+        x2 = x.reshape(-1, K)
+        out, _ = forward(x2, CB, SCB, K, bias, threshold, max_outliers=max_outliers)
+        ctx.save_for_backward(CB, SCB)
+        ctx.K = K
+        ctx.x_shape = shape
+        ctx.bias_dtype = None if bias is None else bias.dtype
+        return out.reshape(*shape[:-1], CB.shape[0])
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        CB, SCB = ctx.saved_tensors
+        need_x = ctx.needs_input_grad[0]
+        need_b = ctx.needs_input_grad[3] and ctx.bias_dtype is not None
+        G = grad_out.reshape(-1, grad_out.shape[-1])
+        gA, gb = backward_input(G, CB, SCB, ctx.K, need_grad_A=need_x,
+                                bias_dtype=ctx.bias_dtype if need_b else None)
+        if gA is not None:
+            gA = gA.reshape(ctx.x_shape)
+        return gA, None, None, gb, None, None
+
+
+class SiLUFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, h):
+        ctx.save_for_backward(h)
+        return silu(h)
+
+    @staticmethod
+    def backward(ctx, g):
+        (h,) = ctx.saved_tensors
+        return silu_backward(g, h)
+
+
+class Int8MLPFunction(torch.autograd.Function):
+    """y = fc2(silu(fc1(x))) (+ x): the two int8 layers, the SiLU and the
+    residual add (fused into fc2's epilogue forward, and into fc1's backward
+    as an addend) all in libi8lt kernels."""
+
+    @staticmethod
+    def forward(ctx, x, CB1, SCB1, b1, CB2, SCB2, b2, threshold, residual, max_outliers):
+        _warn_cast(x.dtype)
+        shape = x.shape
+        K = shape[-1]
+        x2 = x.reshape(-1, K)
+        h, _ = forward(x2, CB1, SCB1, K, b1, threshold, max_outliers=max_outliers)
+        a = silu(h)
+        y, _ = forward(a, CB2, SCB2, a.shape[1], b2, threshold, residual=x2 if residual else None,
+                       max_outliers=max_outliers)
+        ctx.save_for_backward(CB1, SCB1, CB2, SCB2, h)
+        ctx.K = K
+        ctx.H = CB1.shape[0]
+        ctx.shape = shape
+        ctx.residual = residual
+        ctx.b1_dtype = None if b1 is None else b1.dtype
+        ctx.b2_dtype = None if b2 is None else b2.dtype
+        return y.reshape(*shape[:-1], CB2.shape[0])
+
+    @staticmethod
+    def backward(ctx, g):
+        CB1, SCB1, CB2, SCB2, h = ctx.saved_tensors
+        G = g.reshape(-1, g.shape[-1])
+        ga, gb2 = backward_input(G, CB2, SCB2, ctx.H, bias_dtype=ctx.b2_dtype if ctx.needs_input_grad[6] else None)
+        gh = silu_backward(ga, h)
+        gx, gb1 = backward_input(gh, CB1, SCB1, ctx.K, addend=G if ctx.residual else None,
+                                 bias_dtype=ctx.b1_dtype if ctx.needs_input_grad[3] else None)
+        return gx.reshape(ctx.shape), None, None, gb1, None, None, gb2, None, None, None

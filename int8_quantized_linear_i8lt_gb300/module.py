@@ -1,0 +1,68 @@
+"""nn.Module front ends: Linear8bitLt and the two-layer SiLU MLP.
+
+The int8 weight is never drawn at random (``normal_`` has no int8 kernel, as
+the lit-gpt QLoRA PR notes for bnb.int8 training): a layer is built from a
+float weight with ``from_float``, or loaded with its CB / SCB buffers.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import functional as F
+
+
+class Linear8bitLt(torch.nn.Module):
+    """Memory-efficient int8 linear layer (bitsandbytes PR #33): int8
+    row-major weight CB with per-row scales SCB, fp16 outlier decomposition
+    above ``threshold``, input cast to fp16 and output cast back, backward
+    to the input through fp16 weights rebuilt on the fly.  The weight takes
+    no gradient; the bias does."""
+
+    def __init__(self, in_features: int, out_features: int, bias: bool = True, threshold: float = 6.0,
+                 device=None, bias_dtype: torch.dtype = torch.float16, max_outliers: int | None = None):
+        super().__init__()
+        self.in_features = in_features
+        self.out_features = out_features
+        self.threshold = float(threshold)
+        self.max_outliers = max_outliers
+        ld = F.weight_ld(in_features)
+        self.register_buffer("CB", torch.zeros(out_features, ld, dtype=torch.int8, device=device))
+        self.register_buffer("SCB", torch.zeros(out_features, dtype=torch.float32, device=device))
+        if bias:
+            self.bias = torch.nn.Parameter(torch.zeros(out_features, dtype=bias_dtype, device=device))
+        else:
+            self.register_parameter("bias", None)
+
+    @classmethod
+    def from_float(cls, weight: torch.Tensor, bias: torch.Tensor | None = None, threshold: float = 6.0,
+                   max_outliers: int | None = None) -> "Linear8bitLt":
+        """Quantize a float weight [out, in] on its CUDA device."""
+        N, K = weight.shape
+        layer = cls(K, N, bias=bias is not None, threshold=threshold, device=weight.device,
+                    bias_dtype=bias.dtype if bias is not None else torch.float16, max_outliers=max_outliers)
+        CB, SCB = F.quantize_weight(weight)
+        layer.CB.copy_(CB)
+        layer.SCB.copy_(SCB)
+        if bias is not None:
+            with torch.no_grad():
+                layer.bias.copy_(bias)
+        return layer
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return F.Int8LinearFunction.apply(x, self.CB, self.SCB, self.bias, self.threshold, self.max_outliers)
+
+    def extra_repr(self) -> str:
+        return (f"in_features={self.in_features}, out_features={self.out_features}, "
+                f"bias={self.bias is not None}, threshold={self.threshold}")
+
+
+class Int8MLP(torch.nn.Module):
+    """y = fc2(silu(fc1(x))) (+ x when ``residual``), both layers int8."""
+
+    def __init__(self, fc1: Linear8bitLt, fc2: Linear8bitLt, residual: bool = False):
+        super().__init__()
+        self.fc1, self.fc2, self.residual = fc1, fc2, residual
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return F.Int8MLPFunction.apply(x, self.fc1.CB, self.fc1.SCB, self.fc1.bias, self.fc2.CB, self.fc2.SCB,
+                                       self.fc2.bias, self.fc1.threshold, self.residual, self.fc1.max_outliers)

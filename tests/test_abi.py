@@ -1,0 +1,132 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library builds for sm_103a, loads, exports every function that
+include/i8lt.h declares, and rejects bad arguments with a status code before
+it touches the device.  The pointers passed here are never dereferenced:
+every call returns at its argument checks.
+"""
+import ctypes
+import math
+
+import pytest
+
+from int8_quantized_linear_i8lt_gb300 import _lib
+from int8_quantized_linear_i8lt_gb300.build import build
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return _lib.load()
+
+
+def test_exports_every_declared_function(L):
+    names = _lib.header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_version_and_strings(L):
+    assert _lib.i8lt_abi_version() == 1
+    for code in range(10):
+        assert _lib.i8lt_status_string(code) != "unknown status"
+    assert _lib.i8lt_status_string(42) == "unknown status"
+
+
+@pytest.mark.parametrize("K,ld", [(1, 16), (4, 16), (16, 16), (17, 32), (4096, 4096), (11008, 11008), (-1, -1)])
+def test_weight_ld(L, K, ld):
+    assert _lib.i8lt_weight_ld(K) == ld
+
+
+def test_forward_layout(L):
+    M, K, N, cap = 600, 4, 16, 0
+    lay = _lib.i8lt_forward_workspace_layout(M, K, N, cap)
+    assert lay.k_pad == 16 and lay.cap_pad == 0
+    M, K, N, cap = 2048, 4096, 4096, 256
+    lay = _lib.i8lt_forward_workspace_layout(M, K, N, cap)
+    offs = [lay.status, lay.colmax, lay.mask, lay.idx, lay.sca, lay.aq, lay.suba, lay.subb, lay.total]
+    assert offs == sorted(offs)
+    assert all(o % 256 == 0 for o in offs)
+    assert lay.aq - lay.sca >= M * 4
+    assert lay.suba - lay.aq >= M * lay.k_pad * 2
+    assert lay.subb - lay.suba >= M * lay.cap_pad * 2
+    assert lay.total - lay.subb >= N * lay.cap_pad * 2
+    assert _lib.i8lt_forward_workspace_size(M, K, N, cap) == lay.total
+    # capacity is clamped to K and padded to 64
+    assert _lib.i8lt_forward_workspace_layout(8, 40, 8, 1000).cap_pad == 64
+
+
+FAKE = 1 << 20          # 16-byte aligned, never dereferenced
+
+
+def fwd(**kw):
+    a = dict(A=FAKE, at=0, M=64, K=64, CB=FAKE, SCB=FAKE, N=64, bias=None, bt=0, threshold=6.0, residual=None,
+             out=FAKE, ws=FAKE, ws_bytes=1 << 40, max_outliers=16)
+    a.update(kw)
+    return _lib.i8lt_forward(a["A"], a["at"], a["M"], a["K"], a["CB"], a["SCB"], a["N"], a["bias"], a["bt"],
+                             a["threshold"], a["residual"], a["out"], a["ws"], a["ws_bytes"], a["max_outliers"])
+
+
+def test_forward_argument_errors(L):
+    assert fwd(at=3) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert fwd(bias=FAKE, bt=-1) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert fwd(K=0) == _lib.I8LT_ERR_INVALID_ARG
+    assert fwd(N=0) == _lib.I8LT_ERR_INVALID_ARG
+    assert fwd(M=-1) == _lib.I8LT_ERR_INVALID_ARG
+    assert fwd(max_outliers=-1) == _lib.I8LT_ERR_INVALID_ARG
+    assert fwd(K=_lib.I8LT_MAX_K + 1) == _lib.I8LT_ERR_K_TOO_LARGE
+    assert fwd(CB=None) == _lib.I8LT_ERR_INVALID_ARG
+    assert fwd(ws=None) == _lib.I8LT_ERR_INVALID_ARG
+    assert fwd(A=None) == _lib.I8LT_ERR_INVALID_ARG
+    assert fwd(A=FAKE + 8) == _lib.I8LT_ERR_MISALIGNED
+    assert fwd(residual=FAKE + 2) == _lib.I8LT_ERR_MISALIGNED
+    assert fwd(ws=FAKE + 16) == _lib.I8LT_ERR_MISALIGNED       # workspace wants 256 bytes
+    need = _lib.i8lt_forward_workspace_size(64, 64, 64, 16)
+    assert fwd(ws_bytes=need - 1) == _lib.I8LT_ERR_WORKSPACE
+
+
+def bwd(**kw):
+    a = dict(G=FAKE, gt=0, M=64, N=64, CB=FAKE, SCB=FAKE, K=64, addend=None, grad_A=FAKE, grad_bias=None, bt=0,
+             ws=FAKE, ws_bytes=1 << 40)
+    a.update(kw)
+    return _lib.i8lt_backward_input(a["G"], a["gt"], a["M"], a["N"], a["CB"], a["SCB"], a["K"], a["addend"],
+                                    a["grad_A"], a["grad_bias"], a["bt"], a["ws"], a["ws_bytes"])
+
+
+def test_backward_argument_errors(L):
+    assert bwd(gt=9) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert bwd(grad_bias=FAKE, bt=5) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert bwd(K=0) == _lib.I8LT_ERR_INVALID_ARG
+    assert bwd(K=_lib.I8LT_MAX_K + 1) == _lib.I8LT_ERR_K_TOO_LARGE
+    assert bwd(ws=None) == _lib.I8LT_ERR_WORKSPACE
+    assert bwd(G=FAKE + 4) == _lib.I8LT_ERR_MISALIGNED
+    assert bwd(grad_A=FAKE, CB=None) == _lib.I8LT_ERR_INVALID_ARG
+    need = _lib.i8lt_backward_workspace_size(64, 64, 0)
+    assert bwd(ws_bytes=need - 1) == _lib.I8LT_ERR_WORKSPACE
+    # bf16 grad_output needs room for its fp16 copy
+    assert _lib.i8lt_backward_workspace_size(64, 64, 1) >= need + 64 * 64 * 2
+
+
+def test_other_entry_points_argument_errors(L):
+    assert _lib.i8lt_quantize_weight(FAKE, 7, 4, 4, FAKE, FAKE, None) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert _lib.i8lt_quantize_weight(FAKE, 0, 4, 0, FAKE, FAKE, None) == _lib.I8LT_ERR_INVALID_ARG
+    assert _lib.i8lt_quantize_weight(FAKE + 1, 0, 4, 4, FAKE, FAKE, None) == _lib.I8LT_ERR_MISALIGNED
+    assert _lib.i8lt_silu_forward(FAKE, 4, 8, FAKE) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert _lib.i8lt_silu_backward(None, FAKE, 0, 8, FAKE) == _lib.I8LT_ERR_INVALID_ARG
+    r, _, _ = _lib.i8lt_read_device_status(None)
+    assert r == _lib.I8LT_ERR_INVALID_ARG
+
+
+def test_valid_call_without_gpu_reports_error_not_crash(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = fwd(ws_bytes=_lib.i8lt_forward_workspace_size(64, 64, 64, 16))
+    assert st in (_lib.I8LT_ERR_CUDA, _lib.I8LT_ERR_DEVICE)
+
+
+def test_max_k_is_the_int32_bound():
+    assert _lib.I8LT_MAX_K * 127 * 127 < 2 ** 31 <= (_lib.I8LT_MAX_K + 1) * 127 * 127
+    assert math.floor((2 ** 31 - 1) / 16129) == _lib.I8LT_MAX_K

@@ -1,0 +1,307 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Integer stages are compared bit for bit: the weight codes CB and scales SCB,
+the outlier count and indices, the row scales SCA, the activation codes, the
+gathered outlier columns subA / subB and the int32 accumulator.  The
+dequantized output and the gradients are compared with the tolerance rule in
+``_helpers.assert_tol``.  Small cases run the oracle on every element and
+span several tiles, several exact-accumulation chunks and ragged tails; the
+full-size workloads check sampled rows.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+import int8_quantized_linear_i8lt_gb300 as I
+from int8_quantized_linear_i8lt_gb300 import _lib
+from int8_quantized_linear_i8lt_gb300.build import build
+
+from _helpers import ODT, assert_tol, check_forward_stages, check_weight, gpu_forward, to_np, widen
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+    torch.cuda.init()
+
+
+def _layer(spec, seed, w_dtype=None):
+    wl = W.Workload("case", "", (spec,), w_dtype=w_dtype or spec.dtype)
+    A = W.activation(spec, seed)
+    Wf, b, G = W.layer_tensors(wl, 0, seed)
+    return A, Wf, b, G
+
+
+def run_layer_case(spec, seed=0, rows=None, w_dtype=None, max_outliers=None):
+    A, Wf, b, G = _layer(spec, seed, w_dtype)
+    K = spec.K
+    CB, SCB = I.quantize_weight(Wf.to(DEV))
+    CB_ref, SCB_ref = check_weight(CB, SCB, Wf, K)
+    g = gpu_forward(A.to(DEV), CB, SCB, K, b.to(DEV), spec.threshold, max_outliers=max_outliers)
+    A_np = to_np(A)
+    if rows is None:
+        ref = O.forward(A_np, ODT[A.dtype], CB_ref, SCB_ref, to_np(b), ODT[b.dtype], spec.threshold)
+    else:
+        ref = O.forward_rows(A_np, ODT[A.dtype], CB_ref, SCB_ref, rows, to_np(b), ODT[b.dtype], spec.threshold)
+    rep = check_forward_stages(g, ref, rows)
+    if len(ref["idx"]):
+        subB = to_np(g["subB"])[:, :len(ref["idx"])]
+        subB_ref = O.dequant_weight(CB_ref, SCB_ref)[:, ref["idx"]]
+        assert np.array_equal(subB.view(np.uint16), subB_ref.view(np.uint16))
+    # backward to the input and the bias
+    gA, gb = I.backward_input(G.to(DEV), CB, SCB, K, bias_dtype=b.dtype)
+    rb = O.backward_input(to_np(G), ODT[G.dtype], CB_ref, SCB_ref, rows=rows)
+    gA_sel = gA if rows is None else gA[torch.as_tensor(rows, device=DEV)]
+    assert_tol(widen(gA_sel), rb["grad64"], "grad_A")
+    gsum = np.zeros(spec.N)
+    Gn = to_np(G)
+    for r in range(0, spec.M, 2048):
+        gsum += O.widen(Gn[r:r + 2048], ODT[G.dtype]).sum(0)
+    assert_tol(widen(gb), gsum, "grad_bias")
+    return g, ref, rep
+
+
+SMALL = [
+    # M, K, N, dtype, heavy fraction, heavy factor, threshold
+    (300, 1100, 520, torch.float16, 0.01, 20.0, 6.0),      # 2 exact chunks, 3 x 3 tiles, ragged
+    (129, 2112, 257, torch.bfloat16, 0.005, 10.0, 6.0),   # 3 chunks, ragged by one row / column
+    (77, 72, 40, torch.float32, 0.0, 1.0, math.inf),      # fp32 input, no outliers
+    (256, 4096, 512, torch.float16, 0.002, 15.0, 6.0),    # 4 full chunks, full tiles
+    (5, 24, 12, torch.float16, 0.1, 20.0, 6.0),           # tiny, K not a multiple of 16
+    (19, 13, 9, torch.float32, 0.0, 1.0, 6.0),            # K, N not multiples of 8 (scalar paths)
+    (140, 200, 300, torch.bfloat16, 0.05, 10.0, 6.0),     # many outliers (4 outlier blocks)
+    (600, 16, 4, torch.float32, 0.0, 1.0, math.inf),      # the tiny MLP's second layer shape
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-{str(c[3])[6:]}")
+def test_layer_small(case):
+    M, K, N, dt, hf, hx, thr = case
+    spec = W.LayerSpec(M, K, N, dt, 0.02, 0.01, hf, hx, thr)
+    run_layer_case(spec, seed=7)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_layer_small_seeds(seed):
+    """The pages ran every test 10 times for stability; different seeds
+    here (ten in the slow run below)."""
+    spec = W.LayerSpec(384, 1536, 768, torch.float16, 0.02, 0.01, 0.004, 20.0, 6.0)
+    run_layer_case(spec, seed=100 + seed)
+
+
+def test_exact_int32_beyond_fp32_range():
+    """Constant rows make every product +-127^2: |Cacc| = K * 16129 far above
+    2^24, where a single fp32 accumulator would round."""
+    M, K, N = 130, 3000, 260
+    A = torch.ones(M, K, dtype=torch.float16)
+    A[1::2] *= -1.0
+    A[7, :1500] = -1.0
+    Wf = torch.full((N, K), 0.5, dtype=torch.float16)
+    Wf[::3] *= -1.0
+    g = torch.Generator().manual_seed(3)
+    Wf[200:] = torch.where(torch.rand(N - 200, K, generator=g) < 0.5, -0.5, 0.5).half()
+    CB, SCB = I.quantize_weight(Wf.to(DEV))
+    CB_ref, SCB_ref = check_weight(CB, SCB, Wf, K)
+    res = gpu_forward(A.to(DEV), CB, SCB, K, None, math.inf)
+    ref = O.forward(to_np(A), O.F16, CB_ref, SCB_ref, threshold=math.inf)
+    assert np.abs(ref["Cacc"]).max() == K * 16129 > 2 ** 24
+    check_forward_stages(res, ref)
+
+
+def test_max_k_accumulator():
+    """K at the int32 bound: every product +127^2, |Cacc| = 2147479576."""
+    M, K, N = 128, _lib.I8LT_MAX_K, 256
+    A = torch.ones(M, K, dtype=torch.float16, device=DEV)
+    Wf = torch.ones(N, K, dtype=torch.float16, device=DEV)
+    Wf[1::2] = -1
+    CB, SCB = I.quantize_weight(Wf)
+    acc = torch.empty(M, N, dtype=torch.int32, device=DEV)
+    out, ws = I.forward(A, CB, SCB, K, None, math.inf, acc_i32=acc)
+    st, _ = I.device_status(ws)
+    assert st == 0
+    want = torch.full((N,), K * 16129, dtype=torch.int64)
+    want[1::2] *= -1
+    assert torch.equal(acc.cpu().long(), want.expand(M, N))
+    # out = Cacc * 1 * 1 / 127^2 = +-K
+    assert torch.allclose(out.float().cpu(), want.float().expand(M, N) / 16129, rtol=1e-3)
+
+
+def test_empty_batch():
+    K, N = 64, 32
+    Wf = torch.randn(N, K, dtype=torch.float16, device=DEV)
+    CB, SCB = I.quantize_weight(Wf)
+    out, ws = I.forward(torch.empty(0, K, dtype=torch.float16, device=DEV), CB, SCB, K, None, 6.0)
+    assert out.shape == (0, N)
+    gA, gb = I.backward_input(torch.empty(0, N, dtype=torch.float16, device=DEV), CB, SCB, K,
+                              bias_dtype=torch.float16)
+    assert gA.shape == (0, K)
+    assert torch.count_nonzero(gb).item() == 0
+
+
+def test_outlier_capacity_reported():
+    M, K, N = 64, 256, 64
+    A = torch.randn(M, K, dtype=torch.float16, device=DEV) * 10        # nearly every column > 1
+    Wf = torch.randn(N, K, dtype=torch.float16, device=DEV)
+    CB, SCB = I.quantize_weight(Wf)
+    out, ws = I.forward(A, CB, SCB, K, None, 1.0, max_outliers=8)
+    st, found = I.device_status(ws)
+    assert st == _lib.I8LT_ERR_OUTLIER_CAPACITY and found > 8
+    st2, _ = I.device_status(ws)          # reading clears it
+    assert st2 == 0
+    out, ws = I.forward(A, CB, SCB, K, None, 1.0, max_outliers=K, ws=ws) if False else I.forward(
+        A, CB, SCB, K, None, 1.0, max_outliers=K)
+    assert I.device_status(ws)[0] == 0
+
+
+def test_residual_and_addend():
+    """The fused residual (forward) and addend (backward) equal the oracle's
+    single-rounding definitions."""
+    M, K, N = 200, 320, 160
+    spec = W.LayerSpec(M, K, N, torch.float16, 0.02, 0.01, 0.01, 20.0, 6.0)
+    A, Wf, b, G = _layer(spec, 21)
+    R = W.normal((M, N), 1.0, 99, torch.float16)
+    D = W.normal((M, K), 1.0, 98, torch.float16)
+    CB, SCB = I.quantize_weight(Wf.to(DEV))
+    CB_ref, SCB_ref = check_weight(CB, SCB, Wf, K)
+    g = gpu_forward(A.to(DEV), CB, SCB, K, b.to(DEV), 6.0, residual=R.to(DEV))
+    ref = O.forward(to_np(A), O.F16, CB_ref, SCB_ref, to_np(b), O.F16, 6.0, residual=to_np(R))
+    check_forward_stages(g, ref)
+    gA, _ = I.backward_input(G.to(DEV), CB, SCB, K, addend=D.to(DEV))
+    rb = O.backward_input(to_np(G), O.F16, CB_ref, SCB_ref, addend=to_np(D))
+    assert_tol(widen(gA), rb["grad64"], "grad_A + addend")
+
+
+def test_repeat_calls_identical():
+    """Same inputs twice (reused workspace): identical bits (no state leaks
+    between calls, deterministic reductions)."""
+    spec = W.LayerSpec(300, 1100, 520, torch.float16, 0.02, 0.01, 0.01, 20.0, 6.0)
+    A, Wf, b, G = _layer(spec, 5)
+    A, b, G = A.to(DEV), b.to(DEV), G.to(DEV)
+    CB, SCB = I.quantize_weight(Wf.to(DEV))
+    o1, ws = I.forward(A, CB, SCB, spec.K, b, 6.0)
+    o1 = o1.clone()
+    o2, _ = I.forward(A, CB, SCB, spec.K, b, 6.0, ws=ws)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    g1, b1 = I.backward_input(G, CB, SCB, spec.K, bias_dtype=b.dtype)
+    g2, b2 = I.backward_input(G, CB, SCB, spec.K, bias_dtype=b.dtype)
+    assert torch.equal(g1.view(torch.int16), g2.view(torch.int16))
+    assert torch.equal(b1.view(torch.int16), b2.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# the workloads
+# ---------------------------------------------------------------------------
+
+def _rows(M, n=40, seed=0):
+    g = np.random.default_rng(seed)
+    r = set(g.choice(M, size=min(n, M), replace=False).tolist())
+    r |= {0, min(1, M - 1), min(127, M - 1), min(128, M - 1), M - 1}
+    return np.array(sorted(r))
+
+
+@pytest.mark.parametrize("name", ["linear_4096", "linear_bf16_4096x11008", "proj_8192x28672"])
+def test_workload_layers(name):
+    wl = W.WORKLOADS[name]
+    for li, spec in enumerate(wl.layers):
+        seed = li * W.OFF_LAYER2
+        A = W.activation(spec, seed)
+        Wf, b, G = W.layer_tensors(wl, li, 0)
+        K = spec.K
+        CB, SCB = I.quantize_weight(Wf.to(DEV))
+        CB_ref, SCB_ref = check_weight(CB, SCB, Wf, K)
+        del Wf
+        g = gpu_forward(A.to(DEV), CB, SCB, K, b.to(DEV), spec.threshold)
+        rows = _rows(spec.M, seed=li)
+        ref = O.forward_rows(to_np(A), ODT[A.dtype], CB_ref, SCB_ref, rows, to_np(b), ODT[b.dtype],
+                             spec.threshold)
+        heavy = W.heavy_columns(K, spec.heavy_frac, seed + W.OFF_HEAVY).numpy()
+        assert set(heavy.tolist()) <= set(ref["idx"].tolist())
+        check_forward_stages(g, ref, rows)
+        del g
+        gA, gb = I.backward_input(G.to(DEV), CB, SCB, K, bias_dtype=b.dtype)
+        rb = O.backward_input(to_np(G), ODT[G.dtype], CB_ref, SCB_ref, rows=rows)
+        assert_tol(widen(gA[torch.as_tensor(rows, device=DEV)]), rb["grad64"], f"{name} L{li} grad_A")
+        Gn = to_np(G)
+        gsum = np.zeros(spec.N)
+        for r in range(0, spec.M, 2048):
+            gsum += O.widen(Gn[r:r + 2048], ODT[G.dtype]).sum(0)
+        assert_tol(widen(gb), gsum, f"{name} L{li} grad_bias")
+        del gA, gb, CB, SCB
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["tiny_mlp", "mlp_7b"])
+def test_workload_mlp(name):
+    """The chained MLPs: every layer checked against the oracle fed with the
+    same input the GPU layer saw (so integer stages stay bit-exact); the
+    whole chain against the oracle chain within the tolerance."""
+    wl = W.WORKLOADS[name]
+    s1, s2 = wl.layers
+    x = W.layer_input(wl, 0, 0)
+    W1, b1, _ = W.layer_tensors(wl, 0, 0)
+    W2, b2, G = W.layer_tensors(wl, 1, 0)
+    dt = ODT[x.dtype]
+    thr = s1.threshold
+    CB1, SCB1 = I.quantize_weight(W1.to(DEV))
+    CB2, SCB2 = I.quantize_weight(W2.to(DEV))
+    CB1r, SCB1r = check_weight(CB1, SCB1, W1, s1.K)
+    CB2r, SCB2r = check_weight(CB2, SCB2, W2, s2.K)
+    full = s1.M <= 4096
+    rows = None if full else _rows(s1.M, seed=3)
+    rsel = (lambda t: t) if full else (lambda t: t[torch.as_tensor(rows, device=DEV)])
+    fwd = O.forward if full else (lambda *a, **k: O.forward_rows(a[0], a[1], a[2], a[3], rows, *a[4:], **k))
+    xd = x.to(DEV)
+    # layer 1
+    g1 = gpu_forward(xd, CB1, SCB1, s1.K, b1.to(DEV), thr)
+    r1 = fwd(to_np(x), dt, CB1r, SCB1r, to_np(b1), ODT[b1.dtype], thr)
+    check_forward_stages(g1, r1, rows)
+    h = g1["out"]
+    a = I.silu(h)
+    assert_tol(widen(rsel(a)), O.widen(O.silu(to_np(rsel(h)), dt), dt), "silu")
+    # layer 2 (+ residual x for the tiny MLP)
+    res = xd if wl.residual else None
+    g2 = gpu_forward(a, CB2, SCB2, s2.K, b2.to(DEV), thr, residual=res)
+    r2 = fwd(to_np(a), dt, CB2r, SCB2r, to_np(b2), ODT[b2.dtype], thr,
+             residual=to_np(x) if wl.residual else None) if full else O.forward_rows(
+        to_np(a), dt, CB2r, SCB2r, rows, to_np(b2), ODT[b2.dtype], thr,
+        residual=to_np(x)[rows] if wl.residual else None)
+    check_forward_stages(g2, r2, rows)
+    # backward chain
+    Gd = G.to(DEV)
+    ga, gb2 = I.backward_input(Gd, CB2, SCB2, s2.K, bias_dtype=b2.dtype)
+    rb2 = O.backward_input(to_np(G), dt, CB2r, SCB2r, rows=rows)
+    assert_tol(widen(rsel(ga)), rb2["grad64"], "grad a")
+    gh = I.silu_backward(ga, h)
+    assert_tol(widen(rsel(gh)), O.widen(O.silu_backward(to_np(rsel(ga)), to_np(rsel(h)), dt), dt), "grad h")
+    gx, gb1 = I.backward_input(gh, CB1, SCB1, s1.K, bias_dtype=b1.dtype, addend=Gd if wl.residual else None)
+    rb1 = O.backward_input(to_np(gh), dt, CB1r, SCB1r, addend=to_np(G) if wl.residual else None, rows=rows)
+    assert_tol(widen(rsel(gx)), rb1["grad64"], "grad x")
+    if full:
+        # end to end: the oracle chain fed with x only
+        e1 = O.forward(to_np(x), dt, CB1r, SCB1r, to_np(b1), ODT[b1.dtype], thr)
+        ea = O.silu(e1["out"], dt)
+        e2 = O.forward(ea, dt, CB2r, SCB2r, to_np(b2), ODT[b2.dtype], thr,
+                       residual=to_np(x) if wl.residual else None)
+        assert_tol(widen(g2["out"]), e2["out64"], "mlp out end to end")
+        # the autograd module path runs the same kernels: identical bits
+        fc1 = I.Linear8bitLt(s1.K, s1.N, threshold=thr, device=DEV, bias_dtype=b1.dtype)
+        fc2 = I.Linear8bitLt(s2.K, s2.N, threshold=thr, device=DEV, bias_dtype=b2.dtype)
+        for fc, CB, SCB, bb in ((fc1, CB1, SCB1, b1), (fc2, CB2, SCB2, b2)):
+            fc.CB.copy_(CB)
+            fc.SCB.copy_(SCB)
+            with torch.no_grad():
+                fc.bias.copy_(bb.to(DEV))
+        mlp = I.Int8MLP(fc1, fc2, residual=wl.residual)
+        xr = xd.clone().requires_grad_(True)
+        y = mlp(xr)
+        y.backward(Gd)
+        assert torch.equal(y.detach(), g2["out"])
+        assert torch.equal(xr.grad, gx)
+        assert torch.equal(fc1.bias.grad, gb1) and torch.equal(fc2.bias.grad, gb2)
