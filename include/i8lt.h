@@ -27,7 +27,8 @@
  *   - Errors found on the host are returned before anything is launched.
  *     Errors found on the device (outlier capacity exceeded, a pipeline wait
  *     that timed out) are written to the status word at the start of the
- *     workspace; the outputs of that call are then unspecified.
+ *     workspace, which every forward / backward call clears when it starts;
+ *     the outputs of that call are then unspecified.
  *   - No C++ exception crosses this boundary.
  */
 #ifndef I8LT_H_
@@ -189,9 +190,9 @@ int i8lt_profile_stop(i8lt_kernel_time* out, int cap, int* n_records, int* n_lau
 const char* i8lt_kernel_name(int kernel);
 
 /* Synchronizes `stream`, then reads the status word of a forward or backward
- * workspace (status and the number of outlier columns found; either output
- * pointer may be NULL), and clears it.  Returns I8LT_OK or the status the
- * device recorded. */
+ * workspace, i.e. of the last call that used it (status and the number of
+ * outlier columns found; either output pointer may be NULL), and clears the
+ * status.  Returns I8LT_OK or the status the device recorded. */
 int i8lt_read_device_status(void* ws, int32_t* status, int32_t* outliers,
                             void* stream);
 

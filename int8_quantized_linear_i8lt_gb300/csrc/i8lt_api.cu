@@ -243,13 +243,13 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, 
   const bool vec = (K % 8) == 0;
   cudaError_t e = cudaSuccess;
 
+  // one memset clears the status word of this call and the column maxima
+  const size_t clear = enabled ? L.colmax + static_cast<size_t>(K) * 4 : sizeof(DevStatus);
+  if ((e = cudaMemsetAsync(w, 0, clear, s)) != cudaSuccess) return I8LT_ERR_CUDA;
   if (enabled) {
-    if ((e = cudaMemsetAsync(colmax, 0, static_cast<size_t>(K) * 4, s)) != cudaSuccess) return I8LT_ERR_CUDA;
     if ((e = launch_colmax(A, at, M, K, vec, colmax, s)) != cudaSuccess) return I8LT_ERR_CUDA;
     if ((e = launch_outlier_index(colmax, K, threshold, max_outliers, idx, mask, st, s)) != cudaSuccess)
       return I8LT_ERR_CUDA;
-  } else {
-    if ((e = cudaMemsetAsync(&st->found, 0, 2 * sizeof(int), s)) != cudaSuccess) return I8LT_ERR_CUDA;
   }
   if ((e = launch_row_quantize(A, at, M, K, L.k_pad, vec, enabled ? mask : nullptr, idx, st, L.cap_pad, SCA, Aq,
                                enabled ? subA : nullptr, s)) != cudaSuccess)
@@ -319,6 +319,7 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_
   const bool g16_needed = grad_A != nullptr && M > 0 && needs_g16(N, gt);
   __half* G16 = g16_needed ? reinterpret_cast<__half*>(w + L.g16) : nullptr;
   const bool vec = (N % 8) == 0;
+  if (cudaMemsetAsync(st, 0, sizeof(DevStatus), s) != cudaSuccess) return I8LT_ERR_CUDA;
 
   if (grad_bias != nullptr || G16 != nullptr) {
     if (launch_gradout_prepass(G, gt, M, N, vec, G16, L.n_pad, grad_bias, bt, partial, L.chunks, s) != cudaSuccess)
