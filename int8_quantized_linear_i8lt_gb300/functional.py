@@ -50,10 +50,11 @@ def _require_cuda(*ts):
 
 
 def default_max_outliers(K: int) -> int:
-    """Capacity for outlier columns: a quarter of the features, at least 256
-    (the input of a second MLP layer can hold hundreds of sporadic outlier
-    columns, see the 7B-style MLP workload)."""
-    return min(K, max(256, K // 4))
+    """Capacity for outlier columns: all K columns, so the capacity can never
+    be exceeded (the input of a second MLP layer can hold thousands of
+    sporadic outlier columns).  Pass a smaller ``max_outliers`` to shrink the
+    workspace (subA and subB are M x cap and N x cap fp16)."""
+    return K
 
 
 def weight_ld(K: int) -> int:
