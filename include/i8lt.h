@@ -51,7 +51,9 @@ typedef enum {
   I8LT_ERR_OUTLIER_CAPACITY = 6,  /* device: more outlier columns than max_outliers */
   I8LT_ERR_TIMEOUT = 7,           /* device: a pipeline wait ran out of time */
   I8LT_ERR_CUDA = 8,              /* a CUDA runtime / driver call failed */
-  I8LT_ERR_DEVICE = 9             /* the current device is not sm_103 */
+  I8LT_ERR_DEVICE = 9,            /* the current device is not sm_103 */
+  I8LT_ERR_SCRATCH_LIMIT = 10     /* the problem needs more scratch than the
+                                     static buffer of the no-alloc entry point */
 } i8lt_status;
 
 typedef enum { I8LT_F16 = 0, I8LT_BF16 = 1, I8LT_F32 = 2 } i8lt_dtype;
@@ -161,6 +163,40 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N,
                         const void* addend, void* grad_A,
                         void* grad_bias, int bt,
                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * i8lt_backward_input_noalloc -- the same computation as i8lt_backward_input,
+ * for callers that cannot allocate device memory: a host framework that has
+ * reserved the GPU's memory for its own pool at start-up (so a cudaMalloc
+ * would fail or fragment it), code that runs inside another library's
+ * allocator or memory-pressure callback, or a latency-critical loop that must
+ * not enter the driver's allocator.  No counterpart on the pages: it is an
+ * interface addition, not part of the method.
+ *
+ * The scratch (status word, grad_bias partial sums, fp16 copy of G) lives in
+ * one static device array of I8LT_NOALLOC_SCRATCH_BYTES that every GPU which
+ * loads this library holds until the process exits.  The caller still passes
+ * every input and output.  A problem whose scratch
+ * (i8lt_backward_workspace_size(M, N, gt)) exceeds that size is rejected with
+ * I8LT_ERR_SCRATCH_LIMIT before anything is launched.  The call allocates no
+ * device memory (no cudaMalloc / cudaFree, no allocating library routine);
+ * with kernel timing switched on (i8lt_profile_start) the library creates
+ * CUDA events, so such callers should leave timing off.
+ *
+ * The first call on each device looks up the device address of the array
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  Every call shares the one array, which keeps the last
+ * call's contents (each call clears the status word it needs): calls whose
+ * work overlaps on the GPU (other streams, other threads) race on it and
+ * must be serialised by the caller.  The status word of this scratch is not
+ * visible to the caller: device-side errors of this entry point go
+ * unreported (host-side errors are returned as usual).
+ */
+#define I8LT_NOALLOC_SCRATCH_BYTES (32u << 20)
+int i8lt_backward_input_noalloc(const void* G, int gt, int64_t M, int64_t N,
+                                const int8_t* CB, const float* SCB, int64_t K,
+                                const void* addend, void* grad_A,
+                                void* grad_bias, int bt, void* stream);
 
 /* SiLU between the two layers of an MLP: out = h * sigmoid(h), and its
  * backward out = g * silu'(h).  n elements of dtype dt. */

@@ -26,6 +26,8 @@ I8LT_ERR_OUTLIER_CAPACITY = 6
 I8LT_ERR_TIMEOUT = 7
 I8LT_ERR_CUDA = 8
 I8LT_ERR_DEVICE = 9
+I8LT_ERR_SCRATCH_LIMIT = 10
+I8LT_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 I8LT_F16, I8LT_BF16, I8LT_F32 = 0, 1, 2
 I8LT_MAX_K = 133144
@@ -63,6 +65,8 @@ SIGNATURES = {
     "i8lt_backward_workspace_size": (c_size_t, [c_int64, c_int64, c_int]),
     "i8lt_backward_input": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
                                     c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
+    "i8lt_backward_input_noalloc": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
+                                            c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
     "i8lt_silu_forward": (c_int, [c_void_p, c_int, c_int64, c_void_p, c_void_p]),
     "i8lt_silu_backward": (c_int, [c_void_p, c_void_p, c_int, c_int64, c_void_p, c_void_p]),
     "i8lt_profile_start": (c_int, [c_int]),
@@ -147,6 +151,11 @@ def i8lt_backward_input(G, gt, M, N, CB, SCB, K, addend, grad_A, grad_bias, bt, 
                         stream=None) -> int:
     return load().i8lt_backward_input(_p(G), gt, M, N, _p(CB), _p(SCB), K, _p(addend), _p(grad_A),
                                       _p(grad_bias), bt, _p(ws), ws_bytes, _p(stream))
+
+
+def i8lt_backward_input_noalloc(G, gt, M, N, CB, SCB, K, addend, grad_A, grad_bias, bt, stream=None) -> int:
+    return load().i8lt_backward_input_noalloc(_p(G), gt, M, N, _p(CB), _p(SCB), K, _p(addend), _p(grad_A),
+                                              _p(grad_bias), bt, _p(stream))
 
 
 def i8lt_silu_forward(h, dt, n, out, stream=None) -> int:

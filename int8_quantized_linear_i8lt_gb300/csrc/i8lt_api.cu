@@ -183,6 +183,7 @@ const char* i8lt_status_string(int s) {
     case I8LT_ERR_TIMEOUT: return "a device pipeline wait timed out";
     case I8LT_ERR_CUDA: return "CUDA error";
     case I8LT_ERR_DEVICE: return "device is not sm_103 (GB300)";
+    case I8LT_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the no-alloc buffer holds";
     default: return "unknown status";
   }
 }
