@@ -318,6 +318,8 @@ def run_ours(args):
         "kernels": kernels,
         "e2e": e2e,
         "gpu_launches": n_launches,
+        "gemm_launch": {k: dict(zip(("status", "ctas", "threads", "smem"), _lib.i8lt_gemm_launch_info(k)))
+                        for k in ("fwd_gemm", "bwd_gemm")},
         "clocks": clocks,
         "wall_s": round(t_wall, 3),
     }

@@ -222,6 +222,11 @@ typedef struct {
   float ms;
 } i8lt_kernel_time;
 int i8lt_profile_start(int max_launches);
+/* Launch shape the library uses for the persistent GEMM kernels
+ * (kernel = I8LT_K_FWD_GEMM or I8LT_K_BWD_GEMM): CTAs (pairs x 2), threads
+ * per CTA and dynamic shared memory per CTA on the current device.  Any
+ * output pointer may be NULL. */
+int i8lt_gemm_launch_info(int kernel, int* ctas, int* threads, int* smem_bytes);
 int i8lt_profile_stop(i8lt_kernel_time* out, int cap, int* n_records, int* n_launches);
 const char* i8lt_kernel_name(int kernel);
 

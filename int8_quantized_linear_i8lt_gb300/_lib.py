@@ -72,6 +72,7 @@ SIGNATURES = {
     "i8lt_profile_start": (c_int, [c_int]),
     "i8lt_profile_stop": (c_int, [POINTER(i8lt_kernel_time), c_int, POINTER(c_int), POINTER(c_int)]),
     "i8lt_kernel_name": (c_char_p, [c_int]),
+    "i8lt_gemm_launch_info": (c_int, [c_int, POINTER(c_int), POINTER(c_int), POINTER(c_int)]),
     "i8lt_read_device_status": (c_int, [c_void_p, POINTER(c_int32), POINTER(c_int32), c_void_p]),
 }
 
@@ -187,3 +188,11 @@ def i8lt_profile_stop(cap: int = 65536):
 
 def i8lt_kernel_name(kernel: int) -> str:
     return load().i8lt_kernel_name(int(kernel)).decode()
+
+
+def i8lt_gemm_launch_info(kernel: str):
+    """(status, CTAs, threads per CTA, dynamic shared memory) of 'fwd_gemm' / 'bwd_gemm'."""
+    k = KERNELS.index(kernel)
+    c, t, m = c_int(0), c_int(0), c_int(0)
+    st = load().i8lt_gemm_launch_info(k, ctypes.byref(c), ctypes.byref(t), ctypes.byref(m))
+    return st, c.value, t.value, m.value

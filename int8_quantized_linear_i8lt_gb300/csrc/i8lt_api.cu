@@ -263,15 +263,15 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, 
 
   FwdGemmArgs g;
   std::memset(&g, 0, sizeof(g));
-  if (!make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Aq, L.k_pad, M, L.k_pad * 2, kBK, kFwdBM,
+  if (!make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Aq, L.k_pad, M, L.k_pad * 2, kBK, kBoxRows,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, CB, L.k_pad, N, L.k_pad, kBK, kFwdBN,
+      !make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, CB, L.k_pad, N, L.k_pad, kBK, kBoxRows,
                  CU_TENSOR_MAP_SWIZZLE_NONE))
     return I8LT_ERR_CUDA;
   if (with_outliers) {
-    if (!make_tmap(&g.tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subA, L.cap_pad, M, L.cap_pad * 2, kBK, kFwdBM,
+    if (!make_tmap(&g.tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subA, L.cap_pad, M, L.cap_pad * 2, kBK, kBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap(&g.tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subB, L.cap_pad, N, L.cap_pad * 2, kBK, kFwdBN,
+        !make_tmap(&g.tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subB, L.cap_pad, N, L.cap_pad * 2, kBK, kBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return I8LT_ERR_CUDA;
   }
@@ -333,9 +333,9 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_
   std::memset(&g, 0, sizeof(g));
   const void* gsrc = G16 != nullptr ? static_cast<const void*>(G16) : G;
   const int64_t gpitch = G16 != nullptr ? L.n_pad : N;
-  if (!make_tmap(&g.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, CB, k_pad, N, k_pad, kBwdBM, kBK,
+  if (!make_tmap(&g.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, CB, k_pad, N, k_pad, kBoxK, kBK,
                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_tmap(&g.tmG, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, gsrc, gpitch, M, gpitch * 2, kBK, kBwdBN,
+      !make_tmap(&g.tmG, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, gsrc, gpitch, M, gpitch * 2, kBK, kBoxRows,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return I8LT_ERR_CUDA;
   BwdEpiArgs ea;
@@ -395,6 +395,12 @@ int i8lt_profile_stop(i8lt_kernel_time* out, int cap, int* n_records, int* n_lau
   g_prof.clear();
   g_ev_next = 0;
   return st;
+}
+
+int i8lt_gemm_launch_info(int kernel, int* ctas, int* threads, int* smem_bytes) {
+  if (kernel != I8LT_K_FWD_GEMM && kernel != I8LT_K_BWD_GEMM) return I8LT_ERR_INVALID_ARG;
+  if (int d = check_device()) return d;
+  return cuda_status(gemm_launch_shape(kernel, ctas, threads, smem_bytes));
 }
 
 const char* i8lt_kernel_name(int k) {

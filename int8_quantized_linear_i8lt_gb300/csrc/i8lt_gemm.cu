@@ -1,32 +1,42 @@
-// Tensor-core GEMMs of the int8 quantized linear layer (sm_103a, tcgen05).
+// Tensor-core GEMMs of the int8 quantized linear layer (sm_103a, tcgen05,
+// CTA pairs).
 //
 // Forward (K5): out[m,n] = Cacc[m,n] * SCA[m] * SCB[n] / 127^2
 //                          + sum_j subA[m,j] subB[n,j] + bias[n] (+ residual)
 //   Cacc = sum_k Aq[m,k] CB[n,k] is the exact integer product of the int8
-//   codes (bitsandbytes PR #33 "Memory efficient backward", the int8 matmul of
-//   the forward and the "Mixed-precision decomposition matmul" review thread).
-//   sm_103a has no int8 MMA (ptxas rejects tcgen05.mma .kind::i8 for this
-//   target), so the codes enter the fp16 tensor cores as exact fp16 integers
-//   and accumulate in fp32 TMEM.  Every partial sum of at most 1024 products
-//   is an integer of magnitude <= 1024 * 127^2 < 2^24, hence exact in fp32;
-//   every 1024-deep chunk is drained from TMEM into an int32 running sum held
-//   in TMEM, so Cacc is exact for any K <= 133144.
-//   Tile 128 (tokens) x 256 (features) x 64 per stage.  A = Aq via TMA
-//   (128B swizzle); B = CB int8 via TMA, widened to fp16 in shared memory by
-//   four converter warps (in place, 128B-swizzled K-major).  The outlier
-//   sub-GEMM subA x subB^T runs as one more fp32 accumulation unit.
+//   codes (bitsandbytes PR #33 "Memory efficient backward": the int8 matmul
+//   of the forward, and the "Mixed-precision decomposition matmul" review
+//   thread for the outlier part).  sm_103a has no int8 MMA (ptxas rejects
+//   tcgen05.mma .kind::i8 for this target), so the codes enter the fp16
+//   tensor cores as exact fp16 integers and accumulate in fp32 TMEM.  Every
+//   partial sum of at most 1024 products is an integer of magnitude
+//   <= 1024 * 127^2 < 2^24, hence exact in fp32; every 1024-deep chunk is
+//   drained from TMEM into an int32 running sum held in TMEM, so Cacc is exact
+//   for any K <= 133144.  The outlier sub-GEMM subA x subB^T runs as one more
+//   fp32 accumulation unit after the int8 chunks.
 //
 // Backward (K6): grad_A[m,k] = sum_n fp16(G)[m,n] * Wdq[n,k],
 //   Wdq[n,k] = fp16_rn(fp32(CB[n,k]) * (SCB[n] * fp32(1/127))), rebuilt per
-//   tile in shared memory and never stored (PR description, backward bullet;
+//   stage in shared memory and never stored (PR description, backward bullet;
 //   review thread on ".mul(1/127.0)").  Computed transposed,
-//   D[k, m] = Wdq^T G16^T, so the converted operand is the 128-row A side
-//   (half the conversion work of a 256-row B side).  A = Wdq^T stored
-//   MN-major (k contiguous, as CB's rows are), B = G16 via TMA, K-major.
+//   D[k, m] = Wdq^T G16^T, so the converted operand is the A side, stored
+//   MN-major (k contiguous, as CB's rows are); B = G16 via TMA, K-major.
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-5 int8 -> fp16 converters, warps 6-9 epilogue (warp w reads
-// TMEM lanes 32 * (w % 4) ...).  Every wait is bounded (see mbar_wait).
+// Both kernels run on CTA pairs (a cluster of 2, tcgen05 cta_group::2): the
+// pair computes a 256 x 256 tile with M = 256 MMAs issued by the even CTA;
+// each CTA stages its own 128 rows of A and its own 128 rows of B, so the
+// per-SM shared-memory traffic and the int8 -> fp16 widening work are half of
+// a single-CTA 128 x 256 tile.  Five 40 KB stages per CTA: the fp16 A and B
+// operands (16 KB each) and the int8 tile the converters widen (8 KB).
+// Persistent: each pair walks tiles cluster_id, cluster_id + #clusters, ...
+// in a grouped raster.
+//
+// Warp roles (448 threads per CTA): warp 0 TMA producer; warp 1 TMEM owner
+// and, in the even CTA, the MMA issuer; warps 2-5 converters in two groups
+// that take alternate stages (int8 -> fp16, then each warp tells the even CTA
+// its part of the stage is ready); warps 6-13 epilogue (warp w reads TMEM
+// lanes 32 * (w % 4); warps 6-9 take columns 0-127, warps 10-13 columns
+// 128-255).  Every wait is bounded (mbar_wait).
 #include <algorithm>
 
 #include "i8lt_internal.h"
@@ -35,43 +45,48 @@ namespace i8lt {
 
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kStages = 4;
+constexpr int kThreads = 448;
+constexpr int kStages = 5;
 constexpr int kChunkKB = 16;   // K-blocks of 64 per exact fp32 chunk: 1024 products
 
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMMA = 1;
 constexpr int kWarpCvt0 = 2;   // 2..5
-constexpr int kWarpEpi0 = 6;   // 6..9
-constexpr int kCvtThreads = 128;
-constexpr int kEpiThreads = 128;
+constexpr int kWarpEpi0 = 6;   // 6..13
+constexpr int kCvtWarps = 4;
+constexpr int kCvtGroupWarps = 2;   // converter warps per group; the two groups take alternate stages
+constexpr int kEpiWarps = 8;
+constexpr int kCvtThreads = kCvtWarps * 32;
+constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kBarCvt = 1;     // named barrier ids
 constexpr int kBarEpi = 2;
+
+constexpr int kPairM = 256;    // rows of the pair tile (MMA M)
+constexpr int kPairN = 256;    // columns of the pair tile (MMA N)
+constexpr int kCtaRows = 128;  // rows of A and of B that each CTA stages
 
 // roles reported in the status word when a wait times out
 enum { kWhereProducer = 1, kWhereCvt = 2, kWhereMMA = 3, kWhereEpi = 4, kWhereTeardown = 5 };
 
 struct __align__(8) Barriers {
-  uint64_t tma_full[kStages];
-  uint64_t cvt_full[kStages];
-  uint64_t empty[kStages];
-  uint64_t acc_full;
-  uint64_t acc_empty;
-  uint64_t teardown;
+  uint64_t tma_full[kStages];   // this CTA's copies of stage s landed
+  uint64_t ready[kStages];      // even CTA: both CTAs' operands of stage s are in place
+  uint64_t empty[kStages];      // the pair's MMAs finished reading stage s
+  uint64_t acc_full[2];         // an accumulator unit / buffer is complete
+  uint64_t acc_empty[2];        // even CTA: both CTAs' epilogues released it
+  uint64_t teardown;            // even CTA: every MMA finished
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// --- shared memory plan (identical for both GEMMs) --------------------------
-// stage s: [A tile 16 KB][B tile 32 KB]; forward: A = Aq (TMA), B = CB int8
-// (TMA into the first 16 KB, widened in place to 32 KB fp16); backward:
-// A = Wdq^T (int8 TMA into the first 8 KB, widened in place to 16 KB),
-// B = G16 (TMA).
-constexpr int kATileBytes = 128 * kBK * 2;   // 16 KB
-constexpr int kBTileBytes = 256 * kBK * 2;   // 32 KB
-constexpr int kStageBytes = kATileBytes + kBTileBytes;
+// stage s of each CTA: [A operand 16 KB][B operand 16 KB] fp16, 128B-swizzled,
+// then the 8 KB int8 tile that the converters widen into one of them.
+constexpr int kOpBytes = kCtaRows * kBK * 2;   // 16 KB
+constexpr int kI8Bytes = kCtaRows * kBK;       // 8 KB
+constexpr int kStageBytes = 2 * kOpBytes + kI8Bytes;
 constexpr int kSmemTiles = kStages * kStageBytes;
-constexpr int kSmemBytes = 1024 /*align slack*/ + kSmemTiles + 2 * 256 * 4 /*epilogue vectors*/ + sizeof(Barriers);
+constexpr int kSmemBytes = 1024 /*align slack*/ + kSmemTiles + 2 * kPairN * 4 /*epilogue vectors*/ +
+                           static_cast<int>(sizeof(Barriers));
 
 __device__ __forceinline__ uint32_t f2i_rn(uint32_t fbits) {
   return static_cast<uint32_t>(__float2int_rn(__uint_as_float(fbits)));
@@ -129,8 +144,8 @@ __device__ __forceinline__ float load_any(const void* p, int dt, int64_t i) {
   }
 }
 
-// Grouped raster: consecutive CTAs walk `group` M-tiles of one N-tile, so a
-// wave shares its A rows and B rows through L2.
+// Grouped raster: consecutive tiles walk `group` M-tiles of one N-tile, so
+// the pairs working at the same time share their A rows and B rows in L2.
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group, int& tm, int& tn) {
   const int per_group = group * num_n;
   const int g = t / per_group;
@@ -141,15 +156,30 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
   tn = local / gm;
 }
 
+__device__ __forceinline__ void init_barriers(Barriers* bars) {
+  for (int s = 0; s < kStages; ++s) {
+    mbar_init(&bars->tma_full[s], 1);
+    mbar_init(&bars->ready[s], 2 * kCvtGroupWarps);
+    mbar_init(&bars->empty[s], 1);
+  }
+  for (int b = 0; b < 2; ++b) {
+    mbar_init(&bars->acc_full[b], 1);
+    mbar_init(&bars->acc_empty[b], 2 * kEpiWarps);
+  }
+  mbar_init(&bars->teardown, 1);
+  bars->abort_flag = 0;
+  fence_mbar_init();
+}
+
 // ---------------------------------------------------------------------------
 // Forward GEMM
 // ---------------------------------------------------------------------------
 template <typename OutT>
-__device__ __forceinline__ void fwd_store_row(const FwdEpiArgs& e, int64_t m, int n_base, const float (&v)[32],
-                                              bool vec) {
+__device__ __forceinline__ void fwd_store16(const FwdEpiArgs& e, int64_t m, int n_base, const float (&v)[16],
+                                            bool vec) {
   OutT* out = static_cast<OutT*>(e.out) + m * static_cast<int64_t>(e.N) + n_base;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 2; ++q) {
     const int n = n_base + q * 8;
     if (n >= e.N) break;
     float f[8];
@@ -160,59 +190,45 @@ __device__ __forceinline__ void fwd_store_row(const FwdEpiArgs& e, int64_t m, in
 }
 
 template <typename OutT>
-__device__ __forceinline__ void fwd_load_residual(const FwdEpiArgs& e, int64_t m, int n_base, float (&v)[32],
-                                                  bool vec) {
+__device__ __forceinline__ void fwd_add_residual16(const FwdEpiArgs& e, int64_t m, int n_base, float (&v)[16],
+                                                   bool vec) {
   const OutT* res = static_cast<const OutT*>(e.residual) + m * static_cast<int64_t>(e.N) + n_base;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 2; ++q) {
     const int n = n_base + q * 8;
+    if (n >= e.N) break;
     float f[8];
-    if (n < e.N) {
-      load8_float(res + q * 8, e.N - n, vec && n + 8 <= e.N, f);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) f[i] = 0.f;
-    }
+    load8_float(res + q * 8, e.N - n, vec && n + 8 <= e.N, f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[q * 8 + i] += f[i];
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fwd_gemm_kernel(const __grid_constant__ FwdGemmArgs g, const FwdEpiArgs e, int num_m, int num_n, int group) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* scb_s = reinterpret_cast<float*>(smem + kSmemTiles);
-  float* bias_s = scb_s + 256;
-  Barriers* bars = reinterpret_cast<Barriers*>(bias_s + 256);
+  float* bias_s = scb_s + kPairN;
+  Barriers* bars = reinterpret_cast<Barriers*>(bias_s + kPairN);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int tm, tn;
-  tile_coords(blockIdx.x, num_m, num_n, group, tm, tn);
-  const int m0 = tm * kFwdBM, n0 = tn * kFwdBN;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = static_cast<int>(cluster_id_x()), ncl = static_cast<int>(num_clusters_x());
+  const int num_tiles = num_m * num_n;
 
   const int KB = (e.K_pad + kBK - 1) / kBK;
   const int nchunks = (KB + kChunkKB - 1) / kChunkKB;
   const int used = e.use_outliers ? e.st->used : 0;
   const int OB = (used + kBK - 1) / kBK;
-  const int total_blocks = KB + OB;
+  const int blocks = KB + OB;                      // pipeline stages per tile
+  const int units = nchunks + (OB > 0 ? 1 : 0);    // accumulation units per tile
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->tma_full[s], 1);
-      mbar_init(&bars->cvt_full[s], kCvtThreads);
-      mbar_init(&bars->empty[s], 1);
-    }
-    mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, kEpiThreads / 32);
-    mbar_init(&bars->teardown, 1);
-    bars->abort_flag = 0;
-    fence_mbar_init();
-  }
+  if (threadIdx.x == 0) init_barriers(bars);
   if (warp == kWarpMMA) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(&bars->tmem_base, 512);
+    tmem_relinquish_pair();
   }
   if (warp == kWarpProducer && lane == 0) {
     tma_prefetch_desc(&g.tmA);
@@ -223,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const uint32_t tmem_R = tmem;          // int32 running sum, columns [0, 256)
@@ -231,188 +247,230 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpProducer) {
     if (lane == 0) {
-      int issued = 0;
-      for (int it = 0; it < total_blocks; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) break;
-        uint8_t* sa = smem + s * kStageBytes;
-        uint8_t* sb = sa + kATileBytes;
-        if (it < KB) {
-          mbar_arrive_expect_tx(&bars->tma_full[s], kATileBytes + kFwdBN * kBK);
-          tma_load_2d(sa, &g.tmA, it * kBK, m0, &bars->tma_full[s]);
-          tma_load_2d(sb, &g.tmB, it * kBK, n0, &bars->tma_full[s]);
-        } else {
-          const int ob = it - KB;
-          mbar_arrive_expect_tx(&bars->tma_full[s], kATileBytes + kBTileBytes);
-          tma_load_2d(sa, &g.tmSA, ob * kBK, m0, &bars->tma_full[s]);
-          tma_load_2d(sb, &g.tmSB, ob * kBK, n0, &bars->tma_full[s]);
-        }
-        issued = it + 1;
-      }
-      // teardown: every issued copy must have landed before the CTA exits
-      for (int it = max(0, issued - kStages); it < issued; ++it)
-        mbar_wait_teardown(&bars->tma_full[it % kStages], (it / kStages) & 1, e.st);
-    }
-  } else if (warp == kWarpMMA) {
-    if (lane == 0) {
-      const uint32_t idesc = make_idesc_f16(kFwdBM, kFwdBN, false, false);
-      const int units = nchunks + (OB > 0 ? 1 : 0);
+      int it = 0;
       bool ok = true;
-      for (int u = 0; u < units && ok; ++u) {
-        if (u >= 1 && !mbar_wait(&bars->acc_empty, (u - 1) & 1, abort_flag, e.st, kWhereMMA)) break;
-        tc_fence_after();
-        const bool is_int = u < nchunks;
-        const int b0 = is_int ? u * kChunkKB : KB;
-        const int b1 = is_int ? min(KB, b0 + kChunkKB) : total_blocks;
-        for (int it = b0; it < b1; ++it) {
+      for (int t = cid; t < num_tiles && ok; t += ncl) {
+        int tm, tn;
+        tile_coords(t, num_m, num_n, group, tm, tn);
+        const int m_cta = tm * kPairM + static_cast<int>(rank) * kCtaRows;
+        const int n_cta = tn * kPairN + static_cast<int>(rank) * kCtaRows;
+        for (int b = 0; b < blocks; ++b, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
-          if (!mbar_wait(&bars->tma_full[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
-          if (is_int && !mbar_wait(&bars->cvt_full[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + s * kStageBytes);
-          const uint32_t b_base = a_base + kATileBytes;
-#pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = make_sdesc(a_base + k * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bd = make_sdesc(b_base + k * 32, 16, 1024, kSwizzle128B);
-            umma_f16(tmem_X, ad, bd, idesc, (it > b0 || k > 0) ? 1u : 0u);
+          if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
+          uint8_t* sa = smem + s * kStageBytes;
+          uint8_t* sb = sa + kOpBytes;
+          if (b < KB) {
+            mbar_arrive_expect_tx(&bars->tma_full[s], kOpBytes + kI8Bytes);
+            tma_load_2d(sa, &g.tmA, b * kBK, m_cta, &bars->tma_full[s]);
+            tma_load_2d(sb + kOpBytes, &g.tmB, b * kBK, n_cta, &bars->tma_full[s]);   // int8 staging
+          } else {
+            mbar_arrive_expect_tx(&bars->tma_full[s], 2 * kOpBytes);
+            tma_load_2d(sa, &g.tmSA, (b - KB) * kBK, m_cta, &bars->tma_full[s]);
+            tma_load_2d(sb, &g.tmSB, (b - KB) * kBK, n_cta, &bars->tma_full[s]);
           }
-          umma_commit(&bars->empty[s]);
         }
-        if (ok) umma_commit(&bars->acc_full);
       }
-      umma_commit(&bars->teardown);
+      // teardown: every issued copy must have landed before the CTA exits
+      for (int j = max(0, it - kStages); j < it; ++j)
+        mbar_wait_teardown(&bars->tma_full[j % kStages], (j / kStages) & 1, e.st);
+    }
+  } else if (warp == kWarpMMA) {
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc = make_idesc_f16(kPairM, kPairN, false, false);
+      int it = 0, u = 0;
+      bool ok = true;
+      for (int t = cid; t < num_tiles && ok; t += ncl) {
+        for (int uu = 0; uu < units && ok; ++uu, ++u) {
+          // the epilogues of both CTAs released the accumulator of unit u-1
+          if (u > 0 && !mbar_wait_cluster(&bars->acc_empty[0], (u - 1) & 1, abort_flag, e.st, kWhereMMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const bool is_int = uu < nchunks;
+          const int b0 = is_int ? uu * kChunkKB : KB;
+          const int b1 = is_int ? min(KB, b0 + kChunkKB) : blocks;
+          for (int b = b0; b < b1; ++b, ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (it / kStages) & 1;
+            if (!mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(smem + s * kStageBytes);
+            const uint32_t b_base = a_base + kOpBytes;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t ad = make_sdesc(a_base + k * 32, 16, 1024, kSwizzle128B);
+              const uint64_t bd = make_sdesc(b_base + k * 32, 16, 1024, kSwizzle128B);
+              umma_f16_pair(tmem_X, ad, bd, idesc, (b > b0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit_pair_mc(&bars->empty[s], 0x3);
+          }
+          if (ok) umma_commit_pair_mc(&bars->acc_full[0], 0x3);
+        }
+      }
+      umma_commit_pair(&bars->teardown);
       mbar_wait_teardown(&bars->teardown, 0, e.st);
     }
   } else if (warp < kWarpEpi0) {
-    // ---- converters: CB int8 [256 rows][64] -> fp16 128B-swizzled K-major
-    const int ct = threadIdx.x - kWarpCvt0 * 32;
-    for (int it = 0; it < KB; ++it) {
-      const int s = it % kStages;
-      const uint32_t ph = (it / kStages) & 1;
-      const bool ok = mbar_wait(&bars->tma_full[s], ph, abort_flag, e.st, kWhereCvt);
-      uint8_t* sb = smem + s * kStageBytes + kATileBytes;
-      uint4 v[8];
-      if (ok) {
+    // ---- converters: this CTA's 128 CB rows, int8 [128][64] -> fp16 128B-swizzled K-major.
+    // Group cg takes the stages with it % 2 == cg; its two warps take 64 rows each.
+    const int cw = warp - kWarpCvt0;
+    const int cg = cw / kCvtGroupWarps;
+    const int gt = (cw % kCvtGroupWarps) * 32 + lane;   // thread index within the group
+    const uint32_t ready0 = mapa_shared(&bars->ready[0], 0);
+    int it = 0;
+    bool go = true;
+    for (int t = cid; t < num_tiles && go; t += ncl) {
+      for (int b = 0; b < blocks; ++b, ++it) {
+        if ((it & 1) != cg) continue;
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->tma_full[s], ph, abort_flag, e.st, kWhereCvt))) {
+          go = false;
+          break;
+        }
+        if (b < KB) {
+          uint8_t* sb = smem + s * kStageBytes + kOpBytes;
+          const uint4* src = reinterpret_cast<const uint4*>(sb + kOpBytes);
+          uint4 v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = reinterpret_cast<const uint4*>(sb)[ct + kCvtThreads * j];
-      }
-      // all int8 read before the in-place widening; all converters agree to go on
-      if (!named_bar_and(kBarCvt, kCvtThreads, ok)) break;
+          for (int j = 0; j < 8; ++j) v[j] = src[gt + 64 * j];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int item = ct + kCvtThreads * j;   // row = item / 4, 16-byte quarter q = item % 4
-        const int row = item >> 2, q = item & 3;
-        uint4 o0, o1;
-        i8x4_to_h4(v[j].x, o0.x, o0.y);
-        i8x4_to_h4(v[j].y, o0.z, o0.w);
-        i8x4_to_h4(v[j].z, o1.x, o1.y);
-        i8x4_to_h4(v[j].w, o1.z, o1.w);
-        uint8_t* rowp = sb + row * 128;
-        *reinterpret_cast<uint4*>(rowp + (((2 * q) ^ (row & 7)) << 4)) = o0;
-        *reinterpret_cast<uint4*>(rowp + (((2 * q + 1) ^ (row & 7)) << 4)) = o1;
+          for (int j = 0; j < 8; ++j) {
+            const int item = gt + 64 * j;   // row = item / 4, 16-byte quarter q = item % 4
+            const int row = item >> 2, q = item & 3;
+            uint4 o0, o1;
+            i8x4_to_h4(v[j].x, o0.x, o0.y);
+            i8x4_to_h4(v[j].y, o0.z, o0.w);
+            i8x4_to_h4(v[j].z, o1.x, o1.y);
+            i8x4_to_h4(v[j].w, o1.z, o1.w);
+            uint8_t* rowp = sb + row * 128;
+            *reinterpret_cast<uint4*>(rowp + (((2 * q) ^ (row & 7)) << 4)) = o0;
+            *reinterpret_cast<uint4*>(rowp + (((2 * q + 1) ^ (row & 7)) << 4)) = o1;
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive(&bars->ready[s]);
+          else mbar_arrive_remote(ready0 + static_cast<uint32_t>(s) * 8u);
+        }
       }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->cvt_full[s]);
     }
   } else {
-    // ---- epilogue
+    // ---- epilogue: 8 warps; lanes = this CTA's 128 rows, two column halves
     const int et = threadIdx.x - kWarpEpi0 * 32;
     const int quad = warp & 3;
-    for (int i = et; i < 256; i += kEpiThreads) {
-      const int n = n0 + i;
-      scb_s[i] = (n < e.N) ? e.SCB[n] : 0.f;
-      bias_s[i] = (n < e.N && e.bias != nullptr) ? load_any(e.bias, e.bias_dt, n) : 0.f;
-    }
-    named_bar_sync(kBarEpi, kEpiThreads);
+    const int col0 = ((warp - kWarpEpi0) >> 2) * 128;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t acc_empty0 = mapa_shared(&bars->acc_empty[0], 0);
+    const bool vec = (e.N % 8) == 0;
+    int u = 0;
     bool ok = true;
-    for (int u = 0; u < nchunks; ++u) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full, u & 1, abort_flag, e.st, kWhereEpi))) {
-        ok = false;
-        break;
+    for (int t = cid; t < num_tiles && ok; t += ncl) {
+      int tm, tn;
+      tile_coords(t, num_m, num_n, group, tm, tn);
+      const int n0 = tn * kPairN;
+      named_bar_sync(kBarEpi, kEpiThreads);   // the previous tile no longer reads the vectors
+      {
+        const int n = n0 + et;
+        scb_s[et] = (n < e.N) ? e.SCB[n] : 0.f;
+        bias_s[et] = (n < e.N && e.bias != nullptr) ? load_any(e.bias, e.bias_dt, n) : 0.f;
       }
-      tc_fence_after();
-#pragma unroll 1
-      for (int gcol = 0; gcol < 8; ++gcol) {
-        uint32_t x[32], r[32];
-        tmem_ld32(tmem_X + lane_off + gcol * 32, x);
-        if (u > 0) {
-          tmem_ld32(tmem_R + lane_off + gcol * 32, r);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] += f2i_rn(x[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = f2i_rn(x[j]);
-        }
-        tmem_st32(tmem_R + lane_off + gcol * 32, r);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->acc_empty);
-    }
-    const bool has_o = OB > 0;
-    if (ok && has_o && !__all_sync(0xffffffffu, mbar_wait(&bars->acc_full, nchunks & 1, abort_flag, e.st, kWhereEpi)))
-      ok = false;
-    if (ok) {
-      tc_fence_after();
-      const int64_t m = m0 + quad * 32 + lane;
+      named_bar_sync(kBarEpi, kEpiThreads);
+      const int64_t m = static_cast<int64_t>(tm) * kPairM + static_cast<int64_t>(rank) * kCtaRows + quad * 32 + lane;
       const bool row_ok = m < e.M;
-      const float rs = row_ok ? __fmul_rn(e.SCA[m], 1.0f / 16129.0f) : 0.f;
-      const bool vec = (e.N % 8) == 0;
+      for (int uu = 0; uu < units; ++uu, ++u) {
+        // all 256 epilogue threads agree, so none is left at a named barrier
+        if (!named_bar_and(kBarEpi, kEpiThreads, mbar_wait(&bars->acc_full[0], u & 1, abort_flag, e.st, kWhereEpi))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (uu < units - 1) {
+          // an int8 chunk followed by more units: X -> R (exact int32)
 #pragma unroll 1
-      for (int gcol = 0; gcol < 8; ++gcol) {
-        uint32_t r[32], o[32];
-        if (nchunks > 0) {
-          tmem_ld32(tmem_R + lane_off + gcol * 32, r);
+          for (int gc = 0; gc < 128; gc += 32) {
+            uint32_t x[32], r[32];
+            tmem_ld32_nowait(tmem_X + lane_off + col0 + gc, x);
+            if (uu > 0) tmem_ld32_nowait(tmem_R + lane_off + col0 + gc, r);
+            tmem_ld_wait_tie(x, r);
+            if (uu > 0) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] += f2i_rn(x[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = f2i_rn(x[j]);
+            }
+            tmem_st32_nowait(tmem_R + lane_off + col0 + gc, r);
+          }
+          tmem_st_wait();
         } else {
+          // last unit of the tile: the output
+          const bool has_o = OB > 0;
+          const bool r_live = has_o ? (nchunks > 0) : (nchunks > 1);
+          const float rs = row_ok ? __fmul_rn(e.SCA[m], 1.0f / 16129.0f) : 0.f;
+#pragma unroll 1
+          for (int gc = 0; gc < 128; gc += 16) {
+            uint32_t r[16], x[16];
+            tmem_ld16_nowait(tmem_X + lane_off + col0 + gc, x);
+            if (r_live) tmem_ld16_nowait(tmem_R + lane_off + col0 + gc, r);
+            tmem_ld_wait_tie16(x, r);
+            if (!r_live) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = 0;
-        }
-        if (has_o) {
-          tmem_ld32(tmem_X + lane_off + gcol * 32, o);
-        } else {
+              for (int j = 0; j < 16; ++j) r[j] = 0;
+            }
+            if (!has_o) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = 0;
-        }
-        const int nb = n0 + gcol * 32;
-        if (!row_ok || nb >= e.N) continue;
-        float v[32];
+              for (int j = 0; j < 16; ++j) {
+                r[j] += f2i_rn(x[j]);
+                x[j] = 0u;   // no outlier term
+              }
+            }
+            const int nb = n0 + col0 + gc;
+            if (row_ok && nb < e.N) {
+              float v[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float sc = __fmul_rn(rs, scb_s[gcol * 32 + j]);
-          v[j] = __fadd_rn(__fmaf_rn(static_cast<float>(static_cast<int32_t>(r[j])), sc, __uint_as_float(o[j])),
-                           bias_s[gcol * 32 + j]);
-        }
-        if (e.residual != nullptr) {
-          switch (e.out_dt) {
-            case DT_F16: fwd_load_residual<__half>(e, m, nb, v, vec); break;
-            case DT_BF16: fwd_load_residual<__nv_bfloat16>(e, m, nb, v, vec); break;
-            default: fwd_load_residual<float>(e, m, nb, v, vec); break;
+              for (int j = 0; j < 16; ++j) {
+                const float sc = __fmul_rn(rs, scb_s[col0 + gc + j]);
+                v[j] = __fadd_rn(__fmaf_rn(static_cast<float>(static_cast<int32_t>(r[j])), sc, __uint_as_float(x[j])),
+                                 bias_s[col0 + gc + j]);
+              }
+              if (e.residual != nullptr) {
+                switch (e.out_dt) {
+                  case DT_F16: fwd_add_residual16<__half>(e, m, nb, v, vec); break;
+                  case DT_BF16: fwd_add_residual16<__nv_bfloat16>(e, m, nb, v, vec); break;
+                  default: fwd_add_residual16<float>(e, m, nb, v, vec); break;
+                }
+              }
+              switch (e.out_dt) {
+                case DT_F16: fwd_store16<__half>(e, m, nb, v, vec); break;
+                case DT_BF16: fwd_store16<__nv_bfloat16>(e, m, nb, v, vec); break;
+                default: fwd_store16<float>(e, m, nb, v, vec); break;
+              }
+              if (e.acc_i32 != nullptr) {
+                int32_t* dst = e.acc_i32 + m * static_cast<int64_t>(e.N);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (nb + j < e.N) dst[nb + j] = static_cast<int32_t>(r[j]);
+              }
+            }
+            __syncwarp();
           }
         }
-        switch (e.out_dt) {
-          case DT_F16: fwd_store_row<__half>(e, m, nb, v, vec); break;
-          case DT_BF16: fwd_store_row<__nv_bfloat16>(e, m, nb, v, vec); break;
-          default: fwd_store_row<float>(e, m, nb, v, vec); break;
-        }
-        if (e.acc_i32 != nullptr) {
-          int32_t* dst = e.acc_i32 + m * static_cast<int64_t>(e.N);
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (nb + j < e.N) dst[nb + j] = static_cast<int32_t>(r[j]);
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(acc_empty0);
       }
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == kWarpMMA) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -420,11 +478,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Backward GEMM (transposed): D[k, m] = sum_n Wdq[n, k] * G16[m, n]
 // ---------------------------------------------------------------------------
 template <typename OutT>
-__device__ __forceinline__ void bwd_store(const BwdEpiArgs& e, int64_t kk, int m_base, const uint32_t (&x)[32]) {
+__device__ __forceinline__ void bwd_store16(const BwdEpiArgs& e, int64_t kk, int m_base, const uint32_t (&x)[16]) {
   OutT* out = static_cast<OutT*>(e.grad_A);
   const OutT* add = static_cast<const OutT*>(e.addend);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < 16; ++j) {
     const int64_t mm = m_base + j;
     if (mm < e.M) {
       float v = __uint_as_float(x[j]);
@@ -434,189 +492,255 @@ __device__ __forceinline__ void bwd_store(const BwdEpiArgs& e, int64_t kk, int m
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bwd_gemm_kernel(const __grid_constant__ BwdGemmArgs g, const BwdEpiArgs e, int num_k, int num_m, int group) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + kSmemTiles + 2 * 256 * 4);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + kSmemTiles + 2 * kPairN * 4);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int tk, tm;
-  tile_coords(blockIdx.x, num_m, num_k, group, tm, tk);
-  const int k0 = tk * kBwdBM, m0 = tm * kBwdBN;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = static_cast<int>(cluster_id_x()), ncl = static_cast<int>(num_clusters_x());
+  const int num_tiles = num_k * num_m;
   const int NB = (e.N + kBK - 1) / kBK;   // reduction blocks over n
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->tma_full[s], 1);
-      mbar_init(&bars->cvt_full[s], kCvtThreads);
-      mbar_init(&bars->empty[s], 1);
-    }
-    mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, kEpiThreads / 32);
-    mbar_init(&bars->teardown, 1);
-    bars->abort_flag = 0;
-    fence_mbar_init();
-  }
+  if (threadIdx.x == 0) init_barriers(bars);
   if (warp == kWarpMMA) {
-    tmem_alloc(&bars->tmem_base, 256);
-    tmem_relinquish();
+    tmem_alloc_pair(&bars->tmem_base, 512);
+    tmem_relinquish_pair();
   }
   if (warp == kWarpProducer && lane == 0) {
     tma_prefetch_desc(&g.tmW);
     tma_prefetch_desc(&g.tmG);
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
+  const uint32_t tmem = bars->tmem_base;   // two 256-column accumulators
 
   if (warp == kWarpProducer) {
     if (lane == 0) {
-      int issued = 0;
-      for (int it = 0; it < NB; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) break;
-        uint8_t* sa = smem + s * kStageBytes;
-        uint8_t* sb = sa + kATileBytes;
-        mbar_arrive_expect_tx(&bars->tma_full[s], kBK * kBwdBM + kBTileBytes);
-        tma_load_2d(sa, &g.tmW, k0, it * kBK, &bars->tma_full[s]);   // CB[n0:+64][k0:+128] int8
-        tma_load_2d(sb, &g.tmG, it * kBK, m0, &bars->tma_full[s]);   // G16[m0:+256][n0:+64]
-        issued = it + 1;
+      int it = 0;
+      bool ok = true;
+      for (int t = cid; t < num_tiles && ok; t += ncl) {
+        int tm, tk;
+        tile_coords(t, num_m, num_k, group, tm, tk);
+        const int k_cta = tk * kPairM + static_cast<int>(rank) * kCtaRows;
+        const int m_cta = tm * kPairN + static_cast<int>(rank) * kCtaRows;
+        for (int b = 0; b < NB; ++b, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
+          uint8_t* sa = smem + s * kStageBytes;
+          uint8_t* sb = sa + kOpBytes;
+          mbar_arrive_expect_tx(&bars->tma_full[s], kI8Bytes + kOpBytes);
+          tma_load_2d(sa + 2 * kOpBytes, &g.tmW, k_cta, b * kBK, &bars->tma_full[s]);   // CB[n:+64][k:+128] int8
+          tma_load_2d(sb, &g.tmG, b * kBK, m_cta, &bars->tma_full[s]);   // G16[m:+128][n:+64]
+        }
       }
-      for (int it = max(0, issued - kStages); it < issued; ++it)
-        mbar_wait_teardown(&bars->tma_full[it % kStages], (it / kStages) & 1, e.st);
+      for (int j = max(0, it - kStages); j < it; ++j)
+        mbar_wait_teardown(&bars->tma_full[j % kStages], (j / kStages) & 1, e.st);
     }
   } else if (warp == kWarpMMA) {
-    if (lane == 0) {
+    if (rank == 0 && lane == 0) {
       // A: MN-major, 128B swizzle; MN atoms (64 k) 1024 B apart, K atoms (8 n) 2048 B apart.
-      const uint32_t idesc = make_idesc_f16(kBwdBM, kBwdBN, true, false);
+      const uint32_t idesc = make_idesc_f16(kPairM, kPairN, true, false);
+      int it = 0, tl = 0;
       bool ok = true;
-      for (int it = 0; it < NB; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        if (!mbar_wait(&bars->tma_full[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
-        if (!mbar_wait(&bars->cvt_full[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t a_base = smem_u32(smem + s * kStageBytes);
-        const uint32_t b_base = a_base + kATileBytes;
-#pragma unroll
-        for (int k = 0; k < kBK / 16; ++k) {
-          const uint64_t ad = make_sdesc(a_base + k * 4096, 1024, 2048, kSwizzle128B);
-          const uint64_t bd = make_sdesc(b_base + k * 32, 16, 1024, kSwizzle128B);
-          umma_f16(tmem, ad, bd, idesc, (it > 0 || k > 0) ? 1u : 0u);
+      for (int t = cid; t < num_tiles && ok; t += ncl, ++tl) {
+        const int buf = tl & 1;
+        const int use = tl >> 1;
+        if (use > 0 && !mbar_wait_cluster(&bars->acc_empty[buf], (use - 1) & 1, abort_flag, e.st, kWhereMMA)) {
+          ok = false;
+          break;
         }
-        umma_commit(&bars->empty[s]);
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf) * 256u;
+        for (int b = 0; b < NB; ++b, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + s * kStageBytes);
+          const uint32_t b_base = a_base + kOpBytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = make_sdesc(a_base + k * 4096, 1024, 2048, kSwizzle128B);
+            const uint64_t bd = make_sdesc(b_base + k * 32, 16, 1024, kSwizzle128B);
+            umma_f16_pair(d, ad, bd, idesc, (b > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit_pair_mc(&bars->empty[s], 0x3);
+        }
+        if (ok) umma_commit_pair_mc(&bars->acc_full[buf], 0x3);
       }
-      if (ok && NB > 0) umma_commit(&bars->acc_full);
-      umma_commit(&bars->teardown);
+      umma_commit_pair(&bars->teardown);
       mbar_wait_teardown(&bars->teardown, 0, e.st);
     }
   } else if (warp < kWarpEpi0) {
-    // ---- converters: CB int8 [64 n][128 k] -> Wdq^T fp16, MN-major 128B-swizzled
-    const int ct = threadIdx.x - kWarpCvt0 * 32;
-    for (int it = 0; it < NB; ++it) {
-      const int s = it % kStages;
-      const uint32_t ph = (it / kStages) & 1;
-      const bool ok = mbar_wait(&bars->tma_full[s], ph, abort_flag, e.st, kWhereCvt);
-      uint8_t* sa = smem + s * kStageBytes;
-      uint4 v[4];
-      float f[4];
+    // ---- converters: CB int8 [64 n][128 k] -> Wdq^T fp16, MN-major 128B-swizzled.
+    // Group cg takes the stages with it % 2 == cg; its two warps take 32 n-rows each.
+    const int cw = warp - kWarpCvt0;
+    const int cg = cw / kCvtGroupWarps;
+    const int gt = (cw % kCvtGroupWarps) * 32 + lane;
+    const uint32_t ready0 = mapa_shared(&bars->ready[0], 0);
+    int it = 0;
+    bool go = true;
+    for (int t = cid; t < num_tiles && go; t += ncl) {
+      for (int b = 0; b < NB; ++b, ++it) {
+        if ((it & 1) != cg) continue;
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->tma_full[s], ph, abort_flag, e.st, kWhereCvt))) {
+          go = false;
+          break;
+        }
+        uint8_t* sa = smem + s * kStageBytes;
+        const uint4* src = reinterpret_cast<const uint4*>(sa + 2 * kOpBytes);
+        uint4 v[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int item = ct + kCvtThreads * j;   // n_local = item / 8, 16-byte group q = item % 8
-        if (ok) v[j] = reinterpret_cast<const uint4*>(sa)[item];
-        const int n = it * kBK + (item >> 3);
-        f[j] = (n < e.N) ? __fmul_rn(__ldg(e.SCB + n), 1.0f / 127.0f) : 0.f;
-      }
-      if (!named_bar_and(kBarCvt, kCvtThreads, ok)) break;
+        for (int j = 0; j < 8; ++j) v[j] = src[gt + 64 * j];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int item = ct + kCvtThreads * j;
-        const int nl = item >> 3, q = item & 7;
-        const int r = nl & 7, i = nl >> 3;       // row in atom, K atom
-        const int ja = q >> 2;                   // MN atom (64 k)
-        const int c0 = (q & 3) * 2;              // 16-byte chunk in the 128-byte row
-        uint4 o0, o1;
-        i8x4_scale_to_h4(v[j].x, f[j], o0.x, o0.y);
-        i8x4_scale_to_h4(v[j].y, f[j], o0.z, o0.w);
-        i8x4_scale_to_h4(v[j].z, f[j], o1.x, o1.y);
-        i8x4_scale_to_h4(v[j].w, f[j], o1.z, o1.w);
-        uint8_t* rowp = sa + i * 2048 + ja * 1024 + r * 128;
-        *reinterpret_cast<uint4*>(rowp + ((c0 ^ r) << 4)) = o0;
-        *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ r) << 4)) = o1;
+        for (int j = 0; j < 8; ++j) {
+          const int item = gt + 64 * j;            // n_local = item / 8, 16-byte group q = item % 8
+          const int nl = item >> 3, q = item & 7;
+          const int n = b * kBK + nl;
+          const float f = (n < e.N) ? __fmul_rn(__ldg(e.SCB + n), 1.0f / 127.0f) : 0.f;
+          const int r = nl & 7, i = nl >> 3;       // row in atom, K atom
+          const int ja = q >> 2;                   // MN atom (64 k)
+          const int c0 = (q & 3) * 2;              // 16-byte chunk in the 128-byte row
+          uint4 o0, o1;
+          i8x4_scale_to_h4(v[j].x, f, o0.x, o0.y);
+          i8x4_scale_to_h4(v[j].y, f, o0.z, o0.w);
+          i8x4_scale_to_h4(v[j].z, f, o1.x, o1.y);
+          i8x4_scale_to_h4(v[j].w, f, o1.z, o1.w);
+          uint8_t* rowp = sa + i * 2048 + ja * 1024 + r * 128;
+          *reinterpret_cast<uint4*>(rowp + ((c0 ^ r) << 4)) = o0;
+          *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ r) << 4)) = o1;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive(&bars->ready[s]);
+          else mbar_arrive_remote(ready0 + static_cast<uint32_t>(s) * 8u);
+        }
       }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->cvt_full[s]);
     }
   } else {
-    // ---- epilogue: lane = output feature k, columns = tokens m
+    // ---- epilogue: lanes = this CTA's 128 output features k, columns = 256 tokens
     const int quad = warp & 3;
+    const int col0 = ((warp - kWarpEpi0) >> 2) * 128;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    bool ok = NB > 0 && __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, abort_flag, e.st, kWhereEpi));
-    if (ok) tc_fence_after();
-    const int64_t kk = k0 + quad * 32 + lane;
+    const uint32_t acc_empty_pair[2] = {mapa_shared(&bars->acc_empty[0], 0), mapa_shared(&bars->acc_empty[1], 0)};
+    int tl = 0;
+    for (int t = cid; t < num_tiles; t += ncl, ++tl) {
+      int tm, tk;
+      tile_coords(t, num_m, num_k, group, tm, tk);
+      const int buf = tl & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full[buf], (tl >> 1) & 1, abort_flag, e.st, kWhereEpi)))
+        break;
+      tc_fence_after();
+      const int64_t kk = static_cast<int64_t>(tk) * kPairM + static_cast<int64_t>(rank) * kCtaRows + quad * 32 + lane;
+      const uint32_t d = tmem + static_cast<uint32_t>(buf) * 256u + lane_off;
 #pragma unroll 1
-    for (int gcol = 0; gcol < 8; ++gcol) {
-      uint32_t x[32];
-      if (ok) {
-        tmem_ld32(tmem + lane_off + gcol * 32, x);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = 0;
+      for (int gc = 0; gc < 128; gc += 16) {
+        uint32_t x[16];
+        tmem_ld16(d + col0 + gc, x);
+        if (kk < e.K) {
+          const int mb = tm * kPairN + col0 + gc;
+          switch (e.dt) {
+            case DT_F16: bwd_store16<__half>(e, kk, mb, x); break;
+            case DT_BF16: bwd_store16<__nv_bfloat16>(e, kk, mb, x); break;
+            default: bwd_store16<float>(e, kk, mb, x); break;
+          }
+        }
+        __syncwarp();
       }
-      if (NB > 0 && !ok) break;
-      if (kk >= e.K) continue;
-      const int mb = m0 + gcol * 32;
-      switch (e.dt) {
-        case DT_F16: bwd_store<__half>(e, kk, mb, x); break;
-        case DT_BF16: bwd_store<__nv_bfloat16>(e, kk, mb, x); break;
-        default: bwd_store<float>(e, kk, mb, x); break;
-      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(acc_empty_pair[buf]);
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == kWarpMMA) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc_pair(tmem, 512);
   }
+}
+
+// Number of CTA pairs that fit on the device at once (each CTA needs most
+// of an SM's shared memory), so that a persistent grid never has a second
+// wave of pairs.
+int resident_pairs(const void* fn) {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int sms = 152;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  n = std::max(1, std::min(n, sms / 2));
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+bool set_smem_attr(const void* fn, bool& done) {
+  if (done) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) return false;
+  done = true;
+  return true;
 }
 
 }  // namespace
 
+cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_bytes) {
+  const void* fn = nullptr;
+  if (kernel_id == K_FWD_GEMM) fn = reinterpret_cast<const void*>(fwd_gemm_kernel);
+  else if (kernel_id == K_BWD_GEMM) fn = reinterpret_cast<const void*>(bwd_gemm_kernel);
+  else return cudaErrorInvalidValue;
+  static bool attr_fwd = false, attr_bwd = false;
+  if (!set_smem_attr(fn, kernel_id == K_FWD_GEMM ? attr_fwd : attr_bwd)) return cudaGetLastError();
+  if (ctas != nullptr) *ctas = 2 * resident_pairs(fn);
+  if (threads != nullptr) *threads = kThreads;
+  if (smem_bytes != nullptr) *smem_bytes = kSmemBytes;
+  return cudaSuccess;
+}
+
 cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s) {
-  const int num_m = static_cast<int>(ceil_div(e.M, kFwdBM));
-  const int num_n = static_cast<int>(ceil_div(e.N, kFwdBN));
+  const int num_m = static_cast<int>(ceil_div(e.M, kPairM));
+  const int num_n = static_cast<int>(ceil_div(e.N, kPairN));
   if (num_m == 0 || num_n == 0) return cudaSuccess;
   static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(fwd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (err != cudaSuccess) return err;
-    attr_set = true;
-  }
-  const int group = std::min(num_m, 16);
+  if (!set_smem_attr(reinterpret_cast<const void*>(fwd_gemm_kernel), attr_set)) return cudaGetLastError();
+  const int tiles = num_m * num_n;
+  const int clusters = std::min(tiles, resident_pairs(reinterpret_cast<const void*>(fwd_gemm_kernel)));
+  const int group = std::min(num_m, 8);
   ProfScope ps(K_FWD_GEMM, s);
-  fwd_gemm_kernel<<<num_m * num_n, kThreads, kSmemBytes, s>>>(g, e, num_m, num_n, group);
+  fwd_gemm_kernel<<<2 * clusters, kThreads, kSmemBytes, s>>>(g, e, num_m, num_n, group);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaStream_t s) {
-  const int num_k = static_cast<int>(ceil_div(e.K, kBwdBM));
-  const int num_m = static_cast<int>(ceil_div(e.M, kBwdBN));
+  const int num_k = static_cast<int>(ceil_div(e.K, kPairM));
+  const int num_m = static_cast<int>(ceil_div(e.M, kPairN));
   if (num_k == 0 || num_m == 0) return cudaSuccess;
   static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(bwd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (err != cudaSuccess) return err;
-    attr_set = true;
-  }
+  if (!set_smem_attr(reinterpret_cast<const void*>(bwd_gemm_kernel), attr_set)) return cudaGetLastError();
+  const int tiles = num_k * num_m;
+  const int clusters = std::min(tiles, resident_pairs(reinterpret_cast<const void*>(bwd_gemm_kernel)));
   const int group = std::min(num_m, 8);
   ProfScope ps(K_BWD_GEMM, s);
-  bwd_gemm_kernel<<<num_k * num_m, kThreads, kSmemBytes, s>>>(g, e, num_k, num_m, group);
+  bwd_gemm_kernel<<<2 * clusters, kThreads, kSmemBytes, s>>>(g, e, num_k, num_m, group);
   return cudaGetLastError();
 }
 

@@ -62,9 +62,9 @@ cudaError_t launch_silu_backward(const void* g, const void* h, int dt, int64_t n
 
 struct FwdGemmArgs {
   CUtensorMap tmA;    // Aq fp16 [M, K_pad], box 64 x 128, 128B swizzle
-  CUtensorMap tmB;    // CB int8 [N, K_pad], box 64 x 256, no swizzle
+  CUtensorMap tmB;    // CB int8 [N, K_pad], box 64 x 128, no swizzle
   CUtensorMap tmSA;   // subA fp16 [M, cap_pad], box 64 x 128, 128B swizzle
-  CUtensorMap tmSB;   // subB fp16 [N, cap_pad], box 64 x 256, 128B swizzle
+  CUtensorMap tmSB;   // subB fp16 [N, cap_pad], box 64 x 128, 128B swizzle
 };
 
 struct FwdEpiArgs {
@@ -85,7 +85,7 @@ cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStrea
 
 struct BwdGemmArgs {
   CUtensorMap tmW;    // CB int8 [N, K_pad] viewed as (inner K_pad, outer N), box 128 x 64
-  CUtensorMap tmG;    // G16 fp16 [M, N_pad], box 64 x 256, 128B swizzle
+  CUtensorMap tmG;    // G16 fp16 [M, N_pad], box 64 x 128, 128B swizzle
 };
 
 struct BwdEpiArgs {
@@ -99,17 +99,19 @@ struct BwdEpiArgs {
 
 cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaStream_t s);
 
+// Persistent launch shape of a GEMM kernel (K_FWD_GEMM / K_BWD_GEMM).
+cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_bytes);
+
 // Kernel ids of the timing records (match i8lt_kernel_id in i8lt.h).
 enum KernelId {
   K_QUANTIZE_WEIGHT = 0, K_COLMAX, K_OUTLIER_INDEX, K_ROW_QUANTIZE, K_SUBB, K_FWD_GEMM, K_GRADOUT_PREPASS,
   K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_COUNT
 };
 
-// Tile sizes shared with the host code that builds the tensor maps.
-constexpr int kFwdBM = 128;   // rows of A (tokens) per tile
-constexpr int kFwdBN = 256;   // rows of CB (output features) per tile
-constexpr int kBwdBM = 128;   // output features of grad_A (k) per tile
-constexpr int kBwdBN = 256;   // tokens per tile
-constexpr int kBK = 64;       // reduction elements per pipeline stage
+// Box sizes of the tensor maps (each CTA of a pair stages 128 rows of each
+// operand per 64-deep stage).
+constexpr int kBoxRows = 128;  // rows of A / CB / subA / subB / G16 boxes
+constexpr int kBK = 64;        // reduction elements per pipeline stage
+constexpr int kBoxK = 128;     // backward: output features per CB box row
 
 }  // namespace i8lt
