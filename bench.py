@@ -215,6 +215,7 @@ def kernel_bytes(L, name):
         "row_quantize": s.M * s.K * a + s.M * kp * 2 + s.M * 4 + s.M * cap_pad * 2,
         "gradout_prepass": s.M * s.N * a,
         "build_subB": s.N * cap_pad * 3,
+        "widen_codes": s.N * kp * 3,
     }.get(name, 0.0)
 
 
@@ -344,10 +345,10 @@ def _layer_of(i, layers):
 
 def launches_per_layer(L) -> int:
     """Our kernels per layer and step: colmax, outlier index, row quantize,
-    subB (outliers on), forward GEMM; grad_output prepass, grad_bias
-    finalize, backward GEMM."""
+    subB (outliers on), weight-code widening, forward GEMM; grad_output
+    prepass, grad_bias finalize, backward GEMM."""
     import math
-    fwd = 5 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 2
+    fwd = 6 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 3
     return fwd + 3
 
 

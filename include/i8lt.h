@@ -96,13 +96,19 @@ size_t i8lt_forward_workspace_size(int64_t M, int64_t K, int64_t N,
  *   mask    uint32[ceil(K/32)]: bit k set when column k is an outlier
  *   idx     int32[cap_pad]: ascending outlier column indices
  *   SCA     fp32[M]: row absmax of A16 outside the outlier columns
+ *   rowsmall uint8[M]: 1 when every 1024-column chunk of the row's int8 codes
+ *                      has sum |code| <= 33026, i.e. every chunk of the
+ *                      row's int32 accumulator is below 2^22 in magnitude
  *   Aq      fp16[M, K_pad]: the int8 codes of A, stored as exact fp16 integers
  *                           (the form the fp16 tensor cores read)
  *   subA    fp16[M, cap_pad]: A16[:, idx], zero past the count
  *   subB    fp16[N, cap_pad]: dequantized weight columns W_dq[:, idx]
+ *   CBh     fp16[N, K_pad]: the weight's int8 codes as exact fp16 values,
+ *                           rebuilt on every call (the operand form the
+ *                           tensor-core pipeline loads)
  * cap = min(max_outliers, K); cap_pad = cap rounded up to a multiple of 64. */
 typedef struct {
-  size_t status, colmax, mask, idx, sca, aq, suba, subb, total;
+  size_t status, colmax, mask, idx, sca, rowsmall, aq, suba, subb, cbh, total;
   int64_t k_pad, cap_pad;
 } i8lt_fwd_layout;
 int i8lt_forward_workspace_layout(int64_t M, int64_t K, int64_t N,
@@ -215,7 +221,7 @@ int i8lt_silu_backward(const void* g, const void* h, int dt, int64_t n,
 typedef enum {
   I8LT_K_QUANTIZE_WEIGHT = 0, I8LT_K_COLMAX = 1, I8LT_K_OUTLIER_INDEX = 2, I8LT_K_ROW_QUANTIZE = 3,
   I8LT_K_SUBB = 4, I8LT_K_FWD_GEMM = 5, I8LT_K_GRADOUT_PREPASS = 6, I8LT_K_GRAD_BIAS_FINALIZE = 7,
-  I8LT_K_BWD_GEMM = 8, I8LT_K_SILU = 9, I8LT_K_SILU_BACKWARD = 10, I8LT_K_COUNT = 11
+  I8LT_K_BWD_GEMM = 8, I8LT_K_SILU = 9, I8LT_K_SILU_BACKWARD = 10, I8LT_K_WIDEN_CODES = 11, I8LT_K_COUNT = 12
 } i8lt_kernel_id;
 typedef struct {
   int kernel;

@@ -35,8 +35,8 @@ I8LT_MAX_K = 133144
 
 class i8lt_fwd_layout(Structure):
     _fields_ = [("status", c_size_t), ("colmax", c_size_t), ("mask", c_size_t), ("idx", c_size_t),
-                ("sca", c_size_t), ("aq", c_size_t), ("suba", c_size_t), ("subb", c_size_t),
-                ("total", c_size_t), ("k_pad", c_int64), ("cap_pad", c_int64)]
+                ("sca", c_size_t), ("rowsmall", c_size_t), ("aq", c_size_t), ("suba", c_size_t), ("subb", c_size_t),
+                ("cbh", c_size_t), ("total", c_size_t), ("k_pad", c_int64), ("cap_pad", c_int64)]
 
 
 class i8lt_fwd_debug(Structure):
@@ -48,7 +48,7 @@ class i8lt_kernel_time(Structure):
 
 
 KERNELS = ("quantize_weight", "colmax", "outlier_index", "row_quantize", "build_subB", "fwd_gemm",
-           "gradout_prepass", "grad_bias_finalize", "bwd_gemm", "silu", "silu_backward")
+           "gradout_prepass", "grad_bias_finalize", "bwd_gemm", "silu", "silu_backward", "widen_codes")
 
 
 # name -> (restype, argtypes); the same names and order as include/i8lt.h

@@ -93,12 +93,16 @@ i8lt_fwd_layout fwd_layout(int64_t M, int64_t K, int64_t N, int64_t cap) {
   off += align_up(static_cast<size_t>(L.cap_pad) * 4);
   L.sca = off;
   off += align_up(static_cast<size_t>(M) * 4);
+  L.rowsmall = off;
+  off += align_up(static_cast<size_t>(M));
   L.aq = off;
   off += align_up(static_cast<size_t>(M) * L.k_pad * 2);
   L.suba = off;
   off += align_up(static_cast<size_t>(M) * L.cap_pad * 2);
   L.subb = off;
   off += align_up(static_cast<size_t>(N) * L.cap_pad * 2);
+  L.cbh = off;
+  off += align_up(static_cast<size_t>(N) * L.k_pad * 2);
   L.total = off;
   return L;
 }
@@ -237,9 +241,11 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, 
   uint32_t* mask = reinterpret_cast<uint32_t*>(w + L.mask);
   int* idx = reinterpret_cast<int*>(w + L.idx);
   float* SCA = reinterpret_cast<float*>(w + L.sca);
+  uint8_t* rowsmall = w + L.rowsmall;
   __half* Aq = reinterpret_cast<__half*>(w + L.aq);
   __half* subA = reinterpret_cast<__half*>(w + L.suba);
   __half* subB = reinterpret_cast<__half*>(w + L.subb);
+  __half* CBh = reinterpret_cast<__half*>(w + L.cbh);
   const bool enabled = threshold_enabled(threshold);
   const bool vec = (K % 8) == 0;
   cudaError_t e = cudaSuccess;
@@ -253,7 +259,7 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, 
       return I8LT_ERR_CUDA;
   }
   if ((e = launch_row_quantize(A, at, M, K, L.k_pad, vec, enabled ? mask : nullptr, idx, st, L.cap_pad, SCA, Aq,
-                               enabled ? subA : nullptr, s)) != cudaSuccess)
+                               enabled ? subA : nullptr, rowsmall, s)) != cudaSuccess)
     return I8LT_ERR_CUDA;
   const bool with_outliers = enabled && L.cap_pad > 0;
   if (with_outliers) {
@@ -261,12 +267,14 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, 
       return I8LT_ERR_CUDA;
   }
 
+  if ((e = launch_widen_codes(CB, CBh, N * L.k_pad, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+
   FwdGemmArgs g;
   std::memset(&g, 0, sizeof(g));
   if (!make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Aq, L.k_pad, M, L.k_pad * 2, kBK, kBoxRows,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, CB, L.k_pad, N, L.k_pad, kBK, kBoxRows,
-                 CU_TENSOR_MAP_SWIZZLE_NONE))
+      !make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CBh, L.k_pad, N, L.k_pad * 2, kBK, kBoxRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
     return I8LT_ERR_CUDA;
   if (with_outliers) {
     if (!make_tmap(&g.tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subA, L.cap_pad, M, L.cap_pad * 2, kBK, kBoxRows,
@@ -281,6 +289,7 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, 
   ea.K_pad = static_cast<int>(L.k_pad);
   ea.use_outliers = with_outliers ? 1 : 0;
   ea.SCA = SCA;
+  ea.rowsmall = rowsmall;
   ea.SCB = SCB;
   ea.bias = bias;
   ea.bias_dt = bt;
@@ -406,7 +415,7 @@ int i8lt_gemm_launch_info(int kernel, int* ctas, int* threads, int* smem_bytes) 
 const char* i8lt_kernel_name(int k) {
   static const char* names[] = {"quantize_weight", "colmax",          "outlier_index",      "row_quantize",
                                 "build_subB",      "fwd_gemm",        "gradout_prepass",    "grad_bias_finalize",
-                                "bwd_gemm",        "silu",            "silu_backward"};
+                                "bwd_gemm",        "silu",            "silu_backward",      "widen_codes"};
   return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
 }
 

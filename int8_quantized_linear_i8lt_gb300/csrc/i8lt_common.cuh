@@ -235,6 +235,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
       : "memory");
 }
 
+// 2-D tiled load into this CTA's shared memory whose completion is counted
+// on an mbarrier of the pair's even CTA (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* tm, int x, int y, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -365,13 +375,18 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
-// Arrive on an mbarrier of another CTA of the cluster (default release
-// semantics at CTA scope: a cluster-scope release costs ~0.6 us per arrive on
-// GB300, which starves the MMA pipeline).  Operand data written to shared
-// memory before this arrive is ordered for the tensor cores by a preceding
-// fence.proxy.async.shared::cta of every writing thread.
+// Arrive on an mbarrier of another CTA of the cluster with CTA-scope release
+// semantics.  Enough where nothing written before it is read by the other
+// CTA (a TMEM region whose loads have completed, a stage whose readers are
+// done); not for handing over data.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Arrive with cluster-scope release: everything that happened before it in
+// this CTA (shared-memory operand tiles included) is visible to the other
+// CTA once it observes the phase.  Costs ~1 us per arrive on GB300.
+__device__ __forceinline__ void mbar_arrive_remote_release_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;

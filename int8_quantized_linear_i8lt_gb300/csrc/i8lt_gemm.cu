@@ -25,18 +25,27 @@
 // Both kernels run on CTA pairs (a cluster of 2, tcgen05 cta_group::2): the
 // pair computes a 256 x 256 tile with M = 256 MMAs issued by the even CTA;
 // each CTA stages its own 128 rows of A and its own 128 rows of B, so the
-// per-SM shared-memory traffic and the int8 -> fp16 widening work are half of
-// a single-CTA 128 x 256 tile.  Five 40 KB stages per CTA: the fp16 A and B
-// operands (16 KB each) and the int8 tile the converters widen (8 KB).
+// per-SM shared-memory traffic is half of a single-CTA 128 x 256 tile.
 // Persistent: each pair walks tiles cluster_id, cluster_id + #clusters, ...
 // in a grouped raster.
 //
-// Warp roles (448 threads per CTA): warp 0 TMA producer; warp 1 TMEM owner
-// and, in the even CTA, the MMA issuer; warps 2-5 converters in two groups
-// that take alternate stages (int8 -> fp16, then each warp tells the even CTA
-// its part of the stage is ready); warps 6-13 epilogue (warp w reads TMEM
-// lanes 32 * (w % 4); warps 6-9 take columns 0-127, warps 10-13 columns
-// 128-255).  Every wait is bounded (mbar_wait).
+// Operand hand-over between the CTAs of a pair.  The even CTA's MMA reads
+// both CTAs' shared memory, so every operand tile of the odd CTA must be
+// visible to it.  Forward: every operand arrives by TMA and both CTAs' copies
+// complete on the even CTA's barrier (cta_group::2 loads): ordered by the
+// hardware.  The weight codes are widened to fp16 once per call by a
+// memory-bound prepass (the page's forward also re-lays the weight out on
+// every call).  Backward: the fp16 weights are rebuilt per stage by converter
+// warps and never stored; the odd CTA's converters arrive on a local barrier
+// and three relay warps forward each stage to the even CTA with a
+// cluster-scope release arrive (~1 us each, so three in flight).
+//
+// Warp roles (512 threads per CTA): warp 0 TMA producer; warp 1 TMEM owner
+// and, in the even CTA, the MMA issuer (a relay in the odd CTA); warps 2-5
+// converters in two groups that take alternate stages (backward); warps 6-13
+// epilogue (warp w reads TMEM lanes 32 * (w % 4); warps 6-9 take columns
+// 0-127, warps 10-13 columns 128-255); warps 14-15 relays (backward, odd CTA).
+// Every wait is bounded (mbar_wait).
 #include <algorithm>
 
 #include "i8lt_internal.h"
@@ -45,14 +54,18 @@ namespace i8lt {
 
 namespace {
 
-constexpr int kThreads = 448;
-constexpr int kStages = 5;
+constexpr int kThreads = 512;
+constexpr int kFwdStages = 6;   // 32 KB stages: fp16 A and B tiles
+constexpr int kBwdStages = 5;   // 40 KB stages: fp16 A and B tiles and the int8 weight tile
+constexpr int kMaxStages = 6;
 constexpr int kChunkKB = 16;   // K-blocks of 64 per exact fp32 chunk: 1024 products
 
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMMA = 1;
 constexpr int kWarpCvt0 = 2;   // 2..5
 constexpr int kWarpEpi0 = 6;   // 6..13
+constexpr int kWarpRelay0 = 14; // 14..15 (and warp 1 in the odd CTA)
+constexpr int kRelays = 3;
 constexpr int kCvtWarps = 4;
 constexpr int kCvtGroupWarps = 2;   // converter warps per group; the two groups take alternate stages
 constexpr int kEpiWarps = 8;
@@ -69,9 +82,11 @@ constexpr int kCtaRows = 128;  // rows of A and of B that each CTA stages
 enum { kWhereProducer = 1, kWhereCvt = 2, kWhereMMA = 3, kWhereEpi = 4, kWhereTeardown = 5 };
 
 struct __align__(8) Barriers {
-  uint64_t tma_full[kStages];   // this CTA's copies of stage s landed
-  uint64_t ready[kStages];      // even CTA: both CTAs' operands of stage s are in place
-  uint64_t empty[kStages];      // the pair's MMAs finished reading stage s
+  uint64_t full[kMaxStages];      // forward: both CTAs' copies of stage s landed (even CTA);
+                                  // backward: this CTA's copies of stage s landed
+  uint64_t ready[kMaxStages];     // backward, even CTA: both CTAs' operands of stage s in place
+  uint64_t cvt_done[kMaxStages];  // backward, odd CTA: its converters finished stage s
+  uint64_t empty[kMaxStages];     // the pair's MMAs finished reading stage s
   uint64_t acc_full[2];         // an accumulator unit / buffer is complete
   uint64_t acc_empty[2];        // even CTA: both CTAs' epilogues released it
   uint64_t teardown;            // even CTA: every MMA finished
@@ -79,17 +94,43 @@ struct __align__(8) Barriers {
   int abort_flag;
 };
 
-// stage s of each CTA: [A operand 16 KB][B operand 16 KB] fp16, 128B-swizzled,
-// then the 8 KB int8 tile that the converters widen into one of them.
+// stage s of each CTA: [A operand 16 KB][B operand 16 KB] fp16, 128B-swizzled;
+// the backward adds the 8 KB int8 weight tile that its converters widen.
 constexpr int kOpBytes = kCtaRows * kBK * 2;   // 16 KB
 constexpr int kI8Bytes = kCtaRows * kBK;       // 8 KB
-constexpr int kStageBytes = 2 * kOpBytes + kI8Bytes;
-constexpr int kSmemTiles = kStages * kStageBytes;
+constexpr int kFwdStageBytes = 2 * kOpBytes;
+constexpr int kBwdStageBytes = 2 * kOpBytes + kI8Bytes;
+constexpr int kSmemTiles = kFwdStages * kFwdStageBytes > kBwdStages * kBwdStageBytes
+                               ? kFwdStages * kFwdStageBytes : kBwdStages * kBwdStageBytes;
 constexpr int kSmemBytes = 1024 /*align slack*/ + kSmemTiles + 2 * kPairN * 4 /*epilogue vectors*/ +
                            static_cast<int>(sizeof(Barriers));
 
 __device__ __forceinline__ uint32_t f2i_rn(uint32_t fbits) {
   return static_cast<uint32_t>(__float2int_rn(__uint_as_float(fbits)));
+}
+
+// Exact int32 of 32 integer-valued fp32 chunk sums, added to r (or written
+// when `first`).  `small`: every |x| < 2^22, so x + 1.5 * 2^23 lies in
+// [2^23, 2^24) where fp32 steps by 1 and bits(x + 1.5 * 2^23) = 0x4B400000 + x
+// exactly: one packed fp32 add and one integer add per element.  Otherwise
+// the conversion instruction (1/8 of the fp32 rate on this SM).
+template <int N>
+__device__ __forceinline__ void chunk_to_int(const uint32_t (&x)[N], uint32_t (&r)[N], bool first, bool small) {
+  if (small) {
+#pragma unroll
+    for (int j = 0; j < N; j += 2) {
+      uint32_t t0, t1;
+      asm("{\n .reg .b64 a, b;\n mov.b64 a, {%2, %3};\n"
+          " add.rn.f32x2 b, a, %4;\n mov.b64 {%0, %1}, b;\n}"
+          : "=r"(t0), "=r"(t1)
+          : "r"(x[j]), "r"(x[j + 1]), "l"(0x4B4000004B400000ull));
+      r[j] = (first ? 0u : r[j]) + t0 - 0x4B400000u;
+      r[j + 1] = (first ? 0u : r[j + 1]) + t1 - 0x4B400000u;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) r[j] = (first ? 0u : r[j]) + f2i_rn(x[j]);
+  }
 }
 
 // 4 signed int8 in a word -> 4 fp16 (exact): bytes biased to unsigned, placed
@@ -106,18 +147,32 @@ __device__ __forceinline__ void i8x4_to_h4(uint32_t w, uint32_t& lo, uint32_t& h
 }
 
 // 4 signed int8 -> fp16_rn(fp32(q) * f) for each byte.  fp32(q) is built
-// exactly as (2^23 + q + 128) - (2^23 + 128).
-__device__ __forceinline__ void i8x4_scale_to_h4(uint32_t w, float f, uint32_t& lo, uint32_t& hi) {
+// exactly as (2^23 + q + 128) - (2^23 + 128); the subtraction and the
+// multiply by f run as packed IEEE fp32 pairs (add/mul.rn.f32x2, the same
+// rounding per element as the scalar operations), then cvt.rn.f16x2.f32.
+__device__ __forceinline__ uint32_t i8x2_scale_to_h2(uint32_t x0, uint32_t x1, uint64_t negc2, uint64_t f2) {
+  uint32_t out;
+  asm("{\n .reg .b64 x, q, p;\n .reg .b32 plo, phi;\n"
+      " mov.b64 x, {%1, %2};\n"
+      " add.rn.f32x2 q, x, %3;\n"
+      " mul.rn.f32x2 p, q, %4;\n"
+      " mov.b64 {plo, phi}, p;\n"
+      " cvt.rn.f16x2.f32 %0, phi, plo;\n}"
+      : "=r"(out)
+      : "r"(x0), "r"(x1), "l"(negc2), "l"(f2));
+  return out;
+}
+
+__device__ __forceinline__ uint64_t f32x2_splat(float f) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "r"(__float_as_uint(f)));
+  return r;
+}
+
+__device__ __forceinline__ void i8x4_scale_to_h4(uint32_t w, uint64_t negc2, uint64_t f2, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;
-  const float c = 8388736.0f;   // 2^23 + 128
-  const float q0 = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)), c);
-  const float q1 = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)), c);
-  const float q2 = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)), c);
-  const float q3 = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)), c);
-  __half2 a = __floats2half2_rn(__fmul_rn(q0, f), __fmul_rn(q1, f));
-  __half2 b = __floats2half2_rn(__fmul_rn(q2, f), __fmul_rn(q3, f));
-  lo = *reinterpret_cast<uint32_t*>(&a);
-  hi = *reinterpret_cast<uint32_t*>(&b);
+  lo = i8x2_scale_to_h2(__byte_perm(u, 0x4B000000u, 0x7540), __byte_perm(u, 0x4B000000u, 0x7541), negc2, f2);
+  hi = i8x2_scale_to_h2(__byte_perm(u, 0x4B000000u, 0x7542), __byte_perm(u, 0x4B000000u, 0x7543), negc2, f2);
 }
 
 // Wait used in teardown only: bounded, ignores the abort flag.
@@ -157,9 +212,10 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
 }
 
 __device__ __forceinline__ void init_barriers(Barriers* bars) {
-  for (int s = 0; s < kStages; ++s) {
-    mbar_init(&bars->tma_full[s], 1);
-    mbar_init(&bars->ready[s], 2 * kCvtGroupWarps);
+  for (int s = 0; s < kMaxStages; ++s) {
+    mbar_init(&bars->full[s], 1);
+    mbar_init(&bars->ready[s], kCvtGroupWarps + 1);   // the even CTA's group + one relay arrival
+    mbar_init(&bars->cvt_done[s], kCvtGroupWarps);
     mbar_init(&bars->empty[s], 1);
   }
   for (int b = 0; b < 2; ++b) {
@@ -247,6 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpProducer) {
     if (lane == 0) {
+      const uint32_t full0 = mapa_shared(&bars->full[0], 0);   // the even CTA's barriers
       int it = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl) {
@@ -255,25 +312,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int m_cta = tm * kPairM + static_cast<int>(rank) * kCtaRows;
         const int n_cta = tn * kPairN + static_cast<int>(rank) * kCtaRows;
         for (int b = 0; b < blocks; ++b, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
+          const int s = it % kFwdStages;
+          const uint32_t ph = (it / kFwdStages) & 1;
           if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
-          uint8_t* sa = smem + s * kStageBytes;
+          uint8_t* sa = smem + s * kFwdStageBytes;
           uint8_t* sb = sa + kOpBytes;
+          const uint32_t full_s = full0 + static_cast<uint32_t>(s) * 8u;
+          // the even CTA expects the bytes of both CTAs' copies
+          if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], 2 * 2 * kOpBytes);
           if (b < KB) {
-            mbar_arrive_expect_tx(&bars->tma_full[s], kOpBytes + kI8Bytes);
-            tma_load_2d(sa, &g.tmA, b * kBK, m_cta, &bars->tma_full[s]);
-            tma_load_2d(sb + kOpBytes, &g.tmB, b * kBK, n_cta, &bars->tma_full[s]);   // int8 staging
+            tma_load_2d_pair(sa, &g.tmA, b * kBK, m_cta, full_s);
+            tma_load_2d_pair(sb, &g.tmB, b * kBK, n_cta, full_s);   // fp16 weight codes
           } else {
-            mbar_arrive_expect_tx(&bars->tma_full[s], 2 * kOpBytes);
-            tma_load_2d(sa, &g.tmSA, (b - KB) * kBK, m_cta, &bars->tma_full[s]);
-            tma_load_2d(sb, &g.tmSB, (b - KB) * kBK, n_cta, &bars->tma_full[s]);
+            tma_load_2d_pair(sa, &g.tmSA, (b - KB) * kBK, m_cta, full_s);
+            tma_load_2d_pair(sb, &g.tmSB, (b - KB) * kBK, n_cta, full_s);
           }
         }
       }
-      // teardown: every issued copy must have landed before the CTA exits
-      for (int j = max(0, it - kStages); j < it; ++j)
-        mbar_wait_teardown(&bars->tma_full[j % kStages], (j / kStages) & 1, e.st);
+      // teardown: every issued copy (of both CTAs) must have landed before the
+      // pair passes its final cluster barrier
+      if (rank == 0)
+        for (int j = max(0, it - kFwdStages); j < it; ++j)
+          mbar_wait_teardown(&bars->full[j % kFwdStages], (j / kFwdStages) & 1, e.st);
     }
   } else if (warp == kWarpMMA) {
     if (rank == 0 && lane == 0) {
@@ -292,11 +352,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int b0 = is_int ? uu * kChunkKB : KB;
           const int b1 = is_int ? min(KB, b0 + kChunkKB) : blocks;
           for (int b = b0; b < b1; ++b, ++it) {
-            const int s = it % kStages;
-            const uint32_t ph = (it / kStages) & 1;
-            if (!mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
+            const int s = it % kFwdStages;
+            const uint32_t ph = (it / kFwdStages) & 1;
+            if (!mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(smem + s * kStageBytes);
+            const uint32_t a_base = smem_u32(smem + s * kFwdStageBytes);
             const uint32_t b_base = a_base + kOpBytes;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
@@ -312,53 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       umma_commit_pair(&bars->teardown);
       mbar_wait_teardown(&bars->teardown, 0, e.st);
     }
-  } else if (warp < kWarpEpi0) {
-    // ---- converters: this CTA's 128 CB rows, int8 [128][64] -> fp16 128B-swizzled K-major.
-    // Group cg takes the stages with it % 2 == cg; its two warps take 64 rows each.
-    const int cw = warp - kWarpCvt0;
-    const int cg = cw / kCvtGroupWarps;
-    const int gt = (cw % kCvtGroupWarps) * 32 + lane;   // thread index within the group
-    const uint32_t ready0 = mapa_shared(&bars->ready[0], 0);
-    int it = 0;
-    bool go = true;
-    for (int t = cid; t < num_tiles && go; t += ncl) {
-      for (int b = 0; b < blocks; ++b, ++it) {
-        if ((it & 1) != cg) continue;
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->tma_full[s], ph, abort_flag, e.st, kWhereCvt))) {
-          go = false;
-          break;
-        }
-        if (b < KB) {
-          uint8_t* sb = smem + s * kStageBytes + kOpBytes;
-          const uint4* src = reinterpret_cast<const uint4*>(sb + kOpBytes);
-          uint4 v[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = src[gt + 64 * j];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int item = gt + 64 * j;   // row = item / 4, 16-byte quarter q = item % 4
-            const int row = item >> 2, q = item & 3;
-            uint4 o0, o1;
-            i8x4_to_h4(v[j].x, o0.x, o0.y);
-            i8x4_to_h4(v[j].y, o0.z, o0.w);
-            i8x4_to_h4(v[j].z, o1.x, o1.y);
-            i8x4_to_h4(v[j].w, o1.z, o1.w);
-            uint8_t* rowp = sb + row * 128;
-            *reinterpret_cast<uint4*>(rowp + (((2 * q) ^ (row & 7)) << 4)) = o0;
-            *reinterpret_cast<uint4*>(rowp + (((2 * q + 1) ^ (row & 7)) << 4)) = o1;
-          }
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) {
-          if (rank == 0) mbar_arrive(&bars->ready[s]);
-          else mbar_arrive_remote(ready0 + static_cast<uint32_t>(s) * 8u);
-        }
-      }
-    }
-  } else {
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
     // ---- epilogue: 8 warps; lanes = this CTA's 128 rows, two column halves
     const int et = threadIdx.x - kWarpEpi0 * 32;
     const int quad = warp & 3;
@@ -381,6 +395,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       named_bar_sync(kBarEpi, kEpiThreads);
       const int64_t m = static_cast<int64_t>(tm) * kPairM + static_cast<int64_t>(rank) * kCtaRows + quad * 32 + lane;
       const bool row_ok = m < e.M;
+      const bool small = !row_ok || e.rowsmall[m] != 0;
       for (int uu = 0; uu < units; ++uu, ++u) {
         // all 256 epilogue threads agree, so none is left at a named barrier
         if (!named_bar_and(kBarEpi, kEpiThreads, mbar_wait(&bars->acc_full[0], u & 1, abort_flag, e.st, kWhereEpi))) {
@@ -396,13 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld32_nowait(tmem_X + lane_off + col0 + gc, x);
             if (uu > 0) tmem_ld32_nowait(tmem_R + lane_off + col0 + gc, r);
             tmem_ld_wait_tie(x, r);
-            if (uu > 0) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] += f2i_rn(x[j]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = f2i_rn(x[j]);
-            }
+            chunk_to_int(x, r, uu == 0, small);
             tmem_st32_nowait(tmem_R + lane_off + col0 + gc, r);
           }
           tmem_st_wait();
@@ -417,16 +426,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld16_nowait(tmem_X + lane_off + col0 + gc, x);
             if (r_live) tmem_ld16_nowait(tmem_R + lane_off + col0 + gc, r);
             tmem_ld_wait_tie16(x, r);
-            if (!r_live) {
+            if (!has_o) {
+              chunk_to_int(x, r, !r_live, small);   // the last int8 chunk is still in X
+#pragma unroll
+              for (int j = 0; j < 16; ++j) x[j] = 0u;   // no outlier term
+            } else if (!r_live) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) r[j] = 0;
-            }
-            if (!has_o) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                r[j] += f2i_rn(x[j]);
-                x[j] = 0u;   // no outlier term
-              }
             }
             const int nb = n0 + col0 + gc;
             if (row_ok && nb < e.N) {
@@ -471,6 +477,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == kWarpMMA) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+// Odd CTA of a backward pair: forward "stage s converted" to the even CTA's
+// ready[s] with a cluster-scope release, so that the converted tiles (written
+// by this CTA's threads) are visible to the even CTA's MMA.  Relay r takes
+// the stages it % kRelays == r.
+__device__ __noinline__ void relay_loop(Barriers* bars, int cid, int ncl, int num_tiles, int NB, int r,
+                                        volatile int* abort_flag, DevStatus* st) {
+  const uint32_t ready0 = mapa_shared(&bars->ready[0], 0);
+  int it = 0;
+  for (int t = cid; t < num_tiles; t += ncl) {
+    for (int b = 0; b < NB; ++b, ++it) {
+      if (it % kRelays != r) continue;
+      const int s = it % kBwdStages;
+      if (!mbar_wait(&bars->cvt_done[s], (it / kBwdStages) & 1, abort_flag, st, kWhereCvt)) return;
+      mbar_arrive_remote_release_cluster(ready0 + static_cast<uint32_t>(s) * 8u);
+    }
   }
 }
 
@@ -529,18 +553,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int k_cta = tk * kPairM + static_cast<int>(rank) * kCtaRows;
         const int m_cta = tm * kPairN + static_cast<int>(rank) * kCtaRows;
         for (int b = 0; b < NB; ++b, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
+          const int s = it % kBwdStages;
+          const uint32_t ph = (it / kBwdStages) & 1;
           if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
-          uint8_t* sa = smem + s * kStageBytes;
+          uint8_t* sa = smem + s * kBwdStageBytes;
           uint8_t* sb = sa + kOpBytes;
-          mbar_arrive_expect_tx(&bars->tma_full[s], kI8Bytes + kOpBytes);
-          tma_load_2d(sa + 2 * kOpBytes, &g.tmW, k_cta, b * kBK, &bars->tma_full[s]);   // CB[n:+64][k:+128] int8
-          tma_load_2d(sb, &g.tmG, b * kBK, m_cta, &bars->tma_full[s]);   // G16[m:+128][n:+64]
+          mbar_arrive_expect_tx(&bars->full[s], kI8Bytes + kOpBytes);
+          tma_load_2d(sa + 2 * kOpBytes, &g.tmW, k_cta, b * kBK, &bars->full[s]);   // CB[n:+64][k:+128] int8
+          tma_load_2d(sb, &g.tmG, b * kBK, m_cta, &bars->full[s]);   // G16[m:+128][n:+64]
         }
       }
-      for (int j = max(0, it - kStages); j < it; ++j)
-        mbar_wait_teardown(&bars->tma_full[j % kStages], (j / kStages) & 1, e.st);
+      for (int j = max(0, it - kBwdStages); j < it; ++j)
+        mbar_wait_teardown(&bars->full[j % kBwdStages], (j / kBwdStages) & 1, e.st);
     }
   } else if (warp == kWarpMMA) {
     if (rank == 0 && lane == 0) {
@@ -558,11 +582,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(buf) * 256u;
         for (int b = 0; b < NB; ++b, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
+          const int s = it % kBwdStages;
+          const uint32_t ph = (it / kBwdStages) & 1;
           if (!mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + s * kStageBytes);
+          const uint32_t a_base = smem_u32(smem + s * kBwdStageBytes);
           const uint32_t b_base = a_base + kOpBytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
@@ -576,26 +600,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       umma_commit_pair(&bars->teardown);
       mbar_wait_teardown(&bars->teardown, 0, e.st);
+    } else if (rank == 1 && lane == 0) {
+      relay_loop(bars, cid, ncl, num_tiles, NB, 0, abort_flag, e.st);
     }
+  } else if (warp >= kWarpRelay0) {
+    if (rank == 1 && lane == 0)
+      relay_loop(bars, cid, ncl, num_tiles, NB, 1 + (warp - kWarpRelay0), abort_flag, e.st);
   } else if (warp < kWarpEpi0) {
     // ---- converters: CB int8 [64 n][128 k] -> Wdq^T fp16, MN-major 128B-swizzled.
     // Group cg takes the stages with it % 2 == cg; its two warps take 32 n-rows each.
     const int cw = warp - kWarpCvt0;
     const int cg = cw / kCvtGroupWarps;
     const int gt = (cw % kCvtGroupWarps) * 32 + lane;
-    const uint32_t ready0 = mapa_shared(&bars->ready[0], 0);
+    const uint64_t negc2 = f32x2_splat(-8388736.0f);   // -(2^23 + 128)
     int it = 0;
     bool go = true;
     for (int t = cid; t < num_tiles && go; t += ncl) {
       for (int b = 0; b < NB; ++b, ++it) {
         if ((it & 1) != cg) continue;
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->tma_full[s], ph, abort_flag, e.st, kWhereCvt))) {
+        const int s = it % kBwdStages;
+        const uint32_t ph = (it / kBwdStages) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereCvt))) {
           go = false;
           break;
         }
-        uint8_t* sa = smem + s * kStageBytes;
+        uint8_t* sa = smem + s * kBwdStageBytes;
         const uint4* src = reinterpret_cast<const uint4*>(sa + 2 * kOpBytes);
         uint4 v[8];
 #pragma unroll
@@ -605,25 +634,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int item = gt + 64 * j;            // n_local = item / 8, 16-byte group q = item % 8
           const int nl = item >> 3, q = item & 7;
           const int n = b * kBK + nl;
-          const float f = (n < e.N) ? __fmul_rn(__ldg(e.SCB + n), 1.0f / 127.0f) : 0.f;
+          const uint64_t f2 = f32x2_splat((n < e.N) ? __fmul_rn(__ldg(e.SCB + n), 1.0f / 127.0f) : 0.f);
           const int r = nl & 7, i = nl >> 3;       // row in atom, K atom
           const int ja = q >> 2;                   // MN atom (64 k)
           const int c0 = (q & 3) * 2;              // 16-byte chunk in the 128-byte row
           uint4 o0, o1;
-          i8x4_scale_to_h4(v[j].x, f, o0.x, o0.y);
-          i8x4_scale_to_h4(v[j].y, f, o0.z, o0.w);
-          i8x4_scale_to_h4(v[j].z, f, o1.x, o1.y);
-          i8x4_scale_to_h4(v[j].w, f, o1.z, o1.w);
+          i8x4_scale_to_h4(v[j].x, negc2, f2, o0.x, o0.y);
+          i8x4_scale_to_h4(v[j].y, negc2, f2, o0.z, o0.w);
+          i8x4_scale_to_h4(v[j].z, negc2, f2, o1.x, o1.y);
+          i8x4_scale_to_h4(v[j].w, negc2, f2, o1.z, o1.w);
           uint8_t* rowp = sa + i * 2048 + ja * 1024 + r * 128;
           *reinterpret_cast<uint4*>(rowp + ((c0 ^ r) << 4)) = o0;
           *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ r) << 4)) = o1;
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          if (rank == 0) mbar_arrive(&bars->ready[s]);
-          else mbar_arrive_remote(ready0 + static_cast<uint32_t>(s) * 8u);
-        }
+        // the even CTA's MMA thread reads this CTA's tiles: local arrive there,
+        // a relay (cluster-scope release) from the odd CTA
+        if (lane == 0) mbar_arrive(rank == 0 ? &bars->ready[s] : &bars->cvt_done[s]);
       }
     }
   } else {
@@ -667,6 +695,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == kWarpMMA) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+// Forward prepass: CB int8 codes -> the same values as fp16 (exact), 16
+// codes per thread and iteration, 16-byte loads and stores.
+__global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restrict__ CB, __half* __restrict__ CBh,
+                                                          int64_t n16) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(CB) + i);
+    uint4 o0, o1;
+    i8x4_to_h4(v.x, o0.x, o0.y);
+    i8x4_to_h4(v.y, o0.z, o0.w);
+    i8x4_to_h4(v.z, o1.x, o1.y);
+    i8x4_to_h4(v.w, o1.z, o1.w);
+    uint4* dst = reinterpret_cast<uint4*>(CBh) + 2 * i;
+    dst[0] = o0;
+    dst[1] = o1;
   }
 }
 
@@ -714,6 +760,18 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
   if (threads != nullptr) *threads = kThreads;
   if (smem_bytes != nullptr) *smem_bytes = kSmemBytes;
   return cudaSuccess;
+}
+
+cudaError_t launch_widen_codes(const int8_t* CB, __half* CBh, int64_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t n16 = n / 16;   // n is a multiple of 16 (rows padded to 16)
+  const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(n16, 256), static_cast<int64_t>(sms) * 8));
+  ProfScope ps(K_WIDEN_CODES, s);
+  widen_codes_kernel<<<blocks, 256, 0, s>>>(CB, CBh, n16);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s) {

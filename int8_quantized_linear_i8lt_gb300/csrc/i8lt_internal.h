@@ -38,10 +38,13 @@ cudaError_t launch_colmax(const void* A, int at, int64_t M, int64_t K, bool vec,
 cudaError_t launch_outlier_index(const uint32_t* colmax, int64_t K, float thr, int64_t cap, int* idx,
                                  uint32_t* mask, DevStatus* st, cudaStream_t s);
 
-// K3: SCA[m], Aq [M, K_pad] (codes as exact fp16), subA [M, cap_pad].
+// K3: SCA[m], Aq [M, K_pad] (codes as exact fp16), subA [M, cap_pad], and
+// rowsmall[m] = 1 when every 1024-column chunk of row m has sum |code| <=
+// kSmallChunkL1 (its int32 accumulator chunks then stay below 2^22).
+constexpr int kSmallChunkL1 = 33026;   // 33026 * 127 < 2^22
 cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int64_t K_pad, bool vec,
                                 const uint32_t* mask, const int* idx, const DevStatus* st, int64_t cap_pad,
-                                float* SCA, __half* Aq, __half* subA, cudaStream_t s);
+                                float* SCA, __half* Aq, __half* subA, uint8_t* rowsmall, cudaStream_t s);
 
 // K4: subB[n, j] = fp16(fp32(CB[n, idx[j]]) * SCB[n] * fp32(1/127)).
 cudaError_t launch_build_subB(const int8_t* CB, int64_t ld, const float* SCB, int64_t N, const int* idx,
@@ -62,7 +65,7 @@ cudaError_t launch_silu_backward(const void* g, const void* h, int dt, int64_t n
 
 struct FwdGemmArgs {
   CUtensorMap tmA;    // Aq fp16 [M, K_pad], box 64 x 128, 128B swizzle
-  CUtensorMap tmB;    // CB int8 [N, K_pad], box 64 x 128, no swizzle
+  CUtensorMap tmB;    // CBh fp16 [N, K_pad] (widened codes), box 64 x 128, 128B swizzle
   CUtensorMap tmSA;   // subA fp16 [M, cap_pad], box 64 x 128, 128B swizzle
   CUtensorMap tmSB;   // subB fp16 [N, cap_pad], box 64 x 128, 128B swizzle
 };
@@ -71,6 +74,7 @@ struct FwdEpiArgs {
   int M, N, K_pad;
   int use_outliers;       // 0: decomposition disabled
   const float* SCA;
+  const uint8_t* rowsmall;  // per row: chunk sums below 2^22 (fast exact conversion)
   const float* SCB;
   const void* bias;
   int bias_dt;
@@ -82,6 +86,9 @@ struct FwdEpiArgs {
 };
 
 cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s);
+
+// Forward prepass: CBh[i] = fp16(CB[i]) (exact) for n (multiple of 16) codes.
+cudaError_t launch_widen_codes(const int8_t* CB, __half* CBh, int64_t n, cudaStream_t s);
 
 struct BwdGemmArgs {
   CUtensorMap tmW;    // CB int8 [N, K_pad] viewed as (inner K_pad, outer N), box 128 x 64
@@ -105,7 +112,7 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
 // Kernel ids of the timing records (match i8lt_kernel_id in i8lt.h).
 enum KernelId {
   K_QUANTIZE_WEIGHT = 0, K_COLMAX, K_OUTLIER_INDEX, K_ROW_QUANTIZE, K_SUBB, K_FWD_GEMM, K_GRADOUT_PREPASS,
-  K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_COUNT
+  K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_WIDEN_CODES, K_COUNT
 };
 
 // Box sizes of the tensor maps (each CTA of a pair stages 128 rows of each

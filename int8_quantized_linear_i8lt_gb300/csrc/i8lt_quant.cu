@@ -52,8 +52,9 @@ template <typename T, typename OutT>
 __global__ void __launch_bounds__(kThreads) row_quantize_kernel(
     const T* __restrict__ A, int64_t M, int64_t K, int64_t ld, int vec, const uint32_t* __restrict__ mask,
     const int* __restrict__ idx, const DevStatus* __restrict__ st, int64_t cap_pad, float* __restrict__ scale,
-    OutT* __restrict__ codes, __half* __restrict__ sub) {
+    OutT* __restrict__ codes, __half* __restrict__ sub, uint8_t* __restrict__ rowsmall) {
   __shared__ float red[32];
+  __shared__ int chunk_l1[2];   // sum |code| of the two 1024-column chunks of one pass-2 step
   const int used = (mask != nullptr) ? st->used : 0;
   const int used_pad = (used + 63) / 64 * 64;
   for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
@@ -70,7 +71,13 @@ __global__ void __launch_bounds__(kThreads) row_quantize_kernel(
     amax = block_max(amax, red);
     const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
     OutT* out = codes + m * ld;
-    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < ld; c += kThreads * 8) {
+    bool small = true;   // block-uniform
+    for (int64_t c0 = 0; c0 < ld; c0 += kThreads * 8) {
+      const int64_t c = c0 + static_cast<int64_t>(threadIdx.x) * 8;
+      if (rowsmall != nullptr && threadIdx.x < 2) chunk_l1[threadIdx.x] = 0;
+      if (rowsmall != nullptr) __syncthreads();
+      int l1 = 0;
+      if (c < ld) {
       __half h[8];
       if (c < K) {
         load8_half(row + c, K - c, vec != 0 && c + 8 <= K, h);
@@ -81,8 +88,10 @@ __global__ void __launch_bounds__(kThreads) row_quantize_kernel(
       const uint32_t bits = (mask != nullptr && c < K) ? ((mask[c >> 5] >> (c & 31)) & 0xFFu) : 0u;
       int q[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i) {
         q[i] = (amax > 0.f && !((bits >> i) & 1u)) ? quant_code(__half2float(h[i]), s) : 0;
+        l1 += abs(q[i]);
+      }
       if constexpr (sizeof(OutT) == 1) {
         uint2 u;
         u.x = (q[0] & 0xFF) | ((q[1] & 0xFF) << 8) | ((q[2] & 0xFF) << 16) | ((q[3] & 0xFF) << 24);
@@ -95,7 +104,18 @@ __global__ void __launch_bounds__(kThreads) row_quantize_kernel(
         for (int i = 0; i < 8; ++i) o[i] = __int2half_rn(q[i]);   // exact: |q| <= 127
         *reinterpret_cast<uint4*>(out + c) = u;
       }
+      }
+      if (rowsmall != nullptr) {
+        // threads 0-127 cover columns c0 .. c0+1023, threads 128-255 the next 1024
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        if ((threadIdx.x & 31) == 0 && l1 != 0) atomicAdd(&chunk_l1[threadIdx.x >> 7], l1);
+        __syncthreads();
+        small = small && chunk_l1[0] <= kSmallChunkL1 && chunk_l1[1] <= kSmallChunkL1;
+        __syncthreads();
+      }
     }
+    if (rowsmall != nullptr && threadIdx.x == 0) rowsmall[m] = small ? 1 : 0;
     if (sub != nullptr) {
       for (int j = threadIdx.x; j < used_pad; j += kThreads)
         sub[m * cap_pad + j] = (j < used) ? to_half(row[idx[j]]) : __float2half_rn(0.f);
@@ -353,7 +373,7 @@ cudaError_t launch_quantize_weight(const void* W, int wt, int64_t N, int64_t K, 
     using T = std::remove_pointer_t<decltype(tag)>;
     ProfScope ps(K_QUANTIZE_WEIGHT, s);
     row_quantize_kernel<T, int8_t><<<grid_rows(N), kThreads, 0, s>>>(
-        static_cast<const T*>(W), N, K, ld, vec ? 1 : 0, nullptr, nullptr, nullptr, 0, SCB, CB, nullptr);
+        static_cast<const T*>(W), N, K, ld, vec ? 1 : 0, nullptr, nullptr, nullptr, 0, SCB, CB, nullptr, nullptr);
     return cudaGetLastError();
   });
 }
@@ -379,13 +399,13 @@ cudaError_t launch_outlier_index(const uint32_t* colmax, int64_t K, float thr, i
 
 cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int64_t K_pad, bool vec,
                                 const uint32_t* mask, const int* idx, const DevStatus* st, int64_t cap_pad,
-                                float* SCA, __half* Aq, __half* subA, cudaStream_t s) {
+                                float* SCA, __half* Aq, __half* subA, uint8_t* rowsmall, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
   return dispatch_dt(at, [&](auto* tag) {
     using T = std::remove_pointer_t<decltype(tag)>;
     ProfScope ps(K_ROW_QUANTIZE, s);
     row_quantize_kernel<T, __half><<<grid_rows(M), kThreads, 0, s>>>(
-        static_cast<const T*>(A), M, K, K_pad, vec ? 1 : 0, mask, idx, st, cap_pad, SCA, Aq, subA);
+        static_cast<const T*>(A), M, K, K_pad, vec ? 1 : 0, mask, idx, st, cap_pad, SCA, Aq, subA, rowsmall);
     return cudaGetLastError();
   });
 }

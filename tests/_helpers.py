@@ -70,6 +70,7 @@ def gpu_forward(A, CB, SCB, K, bias=None, threshold=6.0, residual=None, max_outl
     used = int(status[2]) if cap > 0 else 0
     res = dict(out=out, acc=acc, status=st, found=found, used=used, ws=ws,
                SCA=region(lay.sca, M * 4, torch.float32, (M,)),
+               rowsmall=region(lay.rowsmall, M, torch.uint8, (M,)),
                Aq=region(lay.aq, M * lay.k_pad * 2, torch.float16, (M, lay.k_pad)),
                k_pad=lay.k_pad, cap_pad=lay.cap_pad)
     if cap > 0:

@@ -46,13 +46,16 @@ def test_forward_layout(L):
     assert lay.k_pad == 16 and lay.cap_pad == 0
     M, K, N, cap = 2048, 4096, 4096, 256
     lay = _lib.i8lt_forward_workspace_layout(M, K, N, cap)
-    offs = [lay.status, lay.colmax, lay.mask, lay.idx, lay.sca, lay.aq, lay.suba, lay.subb, lay.total]
+    offs = [lay.status, lay.colmax, lay.mask, lay.idx, lay.sca, lay.rowsmall, lay.aq, lay.suba, lay.subb, lay.cbh,
+            lay.total]
     assert offs == sorted(offs)
     assert all(o % 256 == 0 for o in offs)
-    assert lay.aq - lay.sca >= M * 4
+    assert lay.rowsmall - lay.sca >= M * 4
+    assert lay.aq - lay.rowsmall >= M
     assert lay.suba - lay.aq >= M * lay.k_pad * 2
     assert lay.subb - lay.suba >= M * lay.cap_pad * 2
-    assert lay.total - lay.subb >= N * lay.cap_pad * 2
+    assert lay.cbh - lay.subb >= N * lay.cap_pad * 2
+    assert lay.total - lay.cbh >= N * lay.k_pad * 2
     assert _lib.i8lt_forward_workspace_size(M, K, N, cap) == lay.total
     # capacity is clamped to K and padded to 64
     assert _lib.i8lt_forward_workspace_layout(8, 40, 8, 1000).cap_pad == 64

@@ -115,6 +115,31 @@ def test_exact_int32_beyond_fp32_range():
     check_forward_stages(res, ref)
 
 
+def test_mixed_row_magnitudes_in_one_tile():
+    """Rows whose 1024-deep chunk sums stay below 2^22 use the fast exact
+    conversion, the others the conversion instruction; both kinds share
+    tiles here.  The per-row flag equals its definition on the oracle's
+    codes and the int32 accumulator is exact for every row."""
+    M, K, N = 200, 2100, 300
+    g = torch.Generator().manual_seed(17)
+    A = torch.randn(M, K, generator=g).half()
+    A[::3] = 1.0                      # constant rows: every code 127, chunk sums ~ 1024 * 127^2
+    A[1::7] = -0.5
+    Wf = (torch.randn(N, K, generator=g) * 0.02).half()
+    Wf[:40] = 0.25                    # constant weight rows: sums of the constant A rows hit K * 127^2
+    CB, SCB = I.quantize_weight(Wf.to(DEV))
+    CB_ref, SCB_ref = check_weight(CB, SCB, Wf, K)
+    res = gpu_forward(A.to(DEV), CB, SCB, K, None, math.inf)
+    ref = O.forward(to_np(A), O.F16, CB_ref, SCB_ref, threshold=math.inf)
+    check_forward_stages(res, ref)
+    aq = np.abs(ref["Aq"].astype(np.int64))
+    chunks = [aq[:, c:c + 1024].sum(1) for c in range(0, K, 1024)]
+    want = np.all(np.stack(chunks, 1) <= 33026, axis=1)
+    got = to_np(res["rowsmall"]).astype(bool)
+    assert np.array_equal(got, want)
+    assert want.any() and (~want).any()
+
+
 def test_max_k_accumulator():
     """K at the int32 bound: every product +127^2, |Cacc| = 2147479576."""
     M, K, N = 128, _lib.I8LT_MAX_K, 256
