@@ -62,13 +62,18 @@ constexpr int kChunkKB = 16;   // K-blocks of 64 per exact fp32 chunk: 1024 prod
 
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMMA = 1;
-constexpr int kWarpCvt0 = 2;   // 2..5
-constexpr int kWarpEpi0 = 6;   // 6..13
+constexpr int kWarpCvt0 = 2;   // backward: 2..9
+constexpr int kWarpEpi0 = 6;   // forward: 6..13
+constexpr int kBwdWarpEpi0 = 10; // backward: 10..13
 constexpr int kWarpRelay0 = 14; // 14..15 (and warp 1 in the odd CTA)
 constexpr int kRelays = 3;
-constexpr int kCvtWarps = 4;
-constexpr int kCvtGroupWarps = 2;   // converter warps per group; the two groups take alternate stages
-constexpr int kEpiWarps = 8;
+// The epilogue waits for a whole accumulation unit (microseconds): it polls
+// with a back-off so that the converter warps on the same schedulers keep
+// their issue slots.
+constexpr unsigned kEpiSleepNs = 256;
+constexpr int kCvtWarps = 8;       // backward: every converter warp works on every stage
+constexpr int kEpiWarps = 8;      // forward
+constexpr int kBwdEpiWarps = 4;   // backward
 constexpr int kCvtThreads = kCvtWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kBarCvt = 1;     // named barrier ids
@@ -211,16 +216,16 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
   tn = local / gm;
 }
 
-__device__ __forceinline__ void init_barriers(Barriers* bars) {
+__device__ __forceinline__ void init_barriers(Barriers* bars, int epi_warps) {
   for (int s = 0; s < kMaxStages; ++s) {
     mbar_init(&bars->full[s], 1);
-    mbar_init(&bars->ready[s], kCvtGroupWarps + 1);   // the even CTA's group + one relay arrival
-    mbar_init(&bars->cvt_done[s], kCvtGroupWarps);
+    mbar_init(&bars->ready[s], kCvtWarps + 1);   // the even CTA's converters + one relay arrival
+    mbar_init(&bars->cvt_done[s], kCvtWarps);
     mbar_init(&bars->empty[s], 1);
   }
   for (int b = 0; b < 2; ++b) {
     mbar_init(&bars->acc_full[b], 1);
-    mbar_init(&bars->acc_empty[b], 2 * kEpiWarps);
+    mbar_init(&bars->acc_empty[b], 2 * epi_warps);
   }
   mbar_init(&bars->teardown, 1);
   bars->abort_flag = 0;
@@ -281,7 +286,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int blocks = KB + OB;                      // pipeline stages per tile
   const int units = nchunks + (OB > 0 ? 1 : 0);    // accumulation units per tile
 
-  if (threadIdx.x == 0) init_barriers(bars);
+  if (threadIdx.x == 0) init_barriers(bars, kEpiWarps);
   if (warp == kWarpMMA) {
     tmem_alloc_pair(&bars->tmem_base, 512);
     tmem_relinquish_pair();
@@ -398,7 +403,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool small = !row_ok || e.rowsmall[m] != 0;
       for (int uu = 0; uu < units; ++uu, ++u) {
         // all 256 epilogue threads agree, so none is left at a named barrier
-        if (!named_bar_and(kBarEpi, kEpiThreads, mbar_wait(&bars->acc_full[0], u & 1, abort_flag, e.st, kWhereEpi))) {
+        if (!named_bar_and(kBarEpi, kEpiThreads,
+                           mbar_wait(&bars->acc_full[0], u & 1, abort_flag, e.st, kWhereEpi, kEpiSleepNs))) {
           ok = false;
           break;
         }
@@ -529,7 +535,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int num_tiles = num_k * num_m;
   const int NB = (e.N + kBK - 1) / kBK;   // reduction blocks over n
 
-  if (threadIdx.x == 0) init_barriers(bars);
+  if (threadIdx.x == 0) init_barriers(bars, kBwdEpiWarps);
   if (warp == kWarpMMA) {
     tmem_alloc_pair(&bars->tmem_base, 512);
     tmem_relinquish_pair();
@@ -606,18 +612,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp >= kWarpRelay0) {
     if (rank == 1 && lane == 0)
       relay_loop(bars, cid, ncl, num_tiles, NB, 1 + (warp - kWarpRelay0), abort_flag, e.st);
-  } else if (warp < kWarpEpi0) {
+  } else if (warp < kBwdWarpEpi0) {
     // ---- converters: CB int8 [64 n][128 k] -> Wdq^T fp16, MN-major 128B-swizzled.
-    // Group cg takes the stages with it % 2 == cg; its two warps take 32 n-rows each.
-    const int cw = warp - kWarpCvt0;
-    const int cg = cw / kCvtGroupWarps;
-    const int gt = (cw % kCvtGroupWarps) * 32 + lane;
+    // All eight warps work on every stage (two 16-byte items per thread), so
+    // that a stage is ready soon after its copy lands.
+    const int gt = threadIdx.x - kWarpCvt0 * 32;   // 0..255
     const uint64_t negc2 = f32x2_splat(-8388736.0f);   // -(2^23 + 128)
     int it = 0;
     bool go = true;
     for (int t = cid; t < num_tiles && go; t += ncl) {
       for (int b = 0; b < NB; ++b, ++it) {
-        if ((it & 1) != cg) continue;
         const int s = it % kBwdStages;
         const uint32_t ph = (it / kBwdStages) & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereCvt))) {
@@ -626,12 +630,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         uint8_t* sa = smem + s * kBwdStageBytes;
         const uint4* src = reinterpret_cast<const uint4*>(sa + 2 * kOpBytes);
-        uint4 v[8];
+        uint4 v[2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = src[gt + 64 * j];
+        for (int j = 0; j < 2; ++j) v[j] = src[gt + kCvtThreads * j];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int item = gt + 64 * j;            // n_local = item / 8, 16-byte group q = item % 8
+        for (int j = 0; j < 2; ++j) {
+          const int item = gt + kCvtThreads * j;   // n_local = item / 8, 16-byte group q = item % 8
           const int nl = item >> 3, q = item & 7;
           const int n = b * kBK + nl;
           const uint64_t f2 = f32x2_splat((n < e.N) ? __fmul_rn(__ldg(e.SCB + n), 1.0f / 127.0f) : 0.f);
@@ -657,7 +661,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ---- epilogue: lanes = this CTA's 128 output features k, columns = 256 tokens
     const int quad = warp & 3;
-    const int col0 = ((warp - kWarpEpi0) >> 2) * 128;
+    const int col0 = 0;   // four warps: each takes all 256 columns of its lanes
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t acc_empty_pair[2] = {mapa_shared(&bars->acc_empty[0], 0), mapa_shared(&bars->acc_empty[1], 0)};
     int tl = 0;
@@ -665,13 +669,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int tm, tk;
       tile_coords(t, num_m, num_k, group, tm, tk);
       const int buf = tl & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full[buf], (tl >> 1) & 1, abort_flag, e.st, kWhereEpi)))
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&bars->acc_full[buf], (tl >> 1) & 1, abort_flag, e.st, kWhereEpi, kEpiSleepNs)))
         break;
       tc_fence_after();
       const int64_t kk = static_cast<int64_t>(tk) * kPairM + static_cast<int64_t>(rank) * kCtaRows + quad * 32 + lane;
       const uint32_t d = tmem + static_cast<uint32_t>(buf) * 256u + lane_off;
 #pragma unroll 1
-      for (int gc = 0; gc < 128; gc += 16) {
+      for (int gc = 0; gc < 256; gc += 16) {
         uint32_t x[16];
         tmem_ld16(d + col0 + gc, x);
         if (kk < e.K) {
