@@ -343,7 +343,7 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_
   const void* gsrc = G16 != nullptr ? static_cast<const void*>(G16) : G;
   const int64_t gpitch = G16 != nullptr ? L.n_pad : N;
   if (!make_tmap(&g.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, CB, k_pad, N, k_pad, kBoxK, kBK,
-                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap(&g.tmG, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, gsrc, gpitch, M, gpitch * 2, kBK, kBoxRows,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return I8LT_ERR_CUDA;

@@ -201,11 +201,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on the phase with the given parity.  Returns false when the
 // CTA is aborting (another role timed out) or when this wait timed out; in
 // the latter case it raises the CTA's abort flag and records ST_TIMEOUT.
+// `sleep_ns` > 0 backs off between polls (for waiters that are not on the
+// critical path, so that they leave issue slots to the warps that are).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          DevStatus* st, int where) {
+                                          DevStatus* st, int where, unsigned sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
+    if (sleep_ns) __nanosleep(sleep_ns);
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 0) {
       if (*abort_flag) return false;
@@ -224,6 +227,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+// Fetch the box at (x, y) into L2 ahead of a later tiled load of it (a hint:
+// no shared memory, no barrier; boxes outside the tensor fetch nothing).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 // 2-D tiled load of the box at element coordinates (x = inner, y = outer).

@@ -37,15 +37,18 @@
 // memory-bound prepass (the page's forward also re-lays the weight out on
 // every call).  Backward: the fp16 weights are rebuilt per stage by converter
 // warps and never stored; the odd CTA's converters arrive on a local barrier
-// and three relay warps forward each stage to the even CTA with a
-// cluster-scope release arrive (~1 us each, so three in flight).
+// and four relay warps forward each stage to the even CTA with a
+// cluster-scope release arrive (~1 us each, so four in flight).  The int8
+// weight tiles have a ring of their own, so their copies run ahead of the
+// operand stages they are converted into.
 //
-// Warp roles (512 threads per CTA): warp 0 TMA producer; warp 1 TMEM owner
-// and, in the even CTA, the MMA issuer (a relay in the odd CTA); warps 2-5
-// converters in two groups that take alternate stages (backward); warps 6-13
-// epilogue (warp w reads TMEM lanes 32 * (w % 4); warps 6-9 take columns
-// 0-127, warps 10-13 columns 128-255); warps 14-15 relays (backward, odd CTA).
-// Every wait is bounded (mbar_wait).
+// Warp roles.  Forward (512 threads per CTA): warp 0 TMA producer; warp 1
+// TMEM owner and, in the even CTA, the MMA issuer; warps 6-13 epilogue (warp
+// w reads TMEM lanes 32 * (w % 4); warps 6-9 take columns 0-127, warps 10-13
+// columns 128-255).  Backward (576 threads): warp 0 G16 producer; warp 1
+// TMEM owner and MMA issuer (even CTA) or relay (odd CTA); warps 2-9
+// converters; warps 10-13 epilogue (all 256 columns); warp 16 int8 producer;
+// warps 14, 15, 17 relays (odd CTA).  Every wait is bounded (mbar_wait).
 #include <algorithm>
 
 #include "i8lt_internal.h"
@@ -54,9 +57,12 @@ namespace i8lt {
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kFwdStages = 6;   // 32 KB stages: fp16 A and B tiles
-constexpr int kBwdStages = 5;   // 40 KB stages: fp16 A and B tiles and the int8 weight tile
+constexpr int kThreads = 512;      // forward
+constexpr int kBwdThreads = 576;   // backward: two more warps (int8 producer, fourth relay)
+constexpr int kFwdStages = 6;      // 32 KB stages: fp16 A and B tiles
+constexpr int kBwdStages = 6;      // 32 KB stages: converted weight tile (A) and G16 tile (B)
+constexpr int kI8Stages = 3;       // 8 KB stages: int8 weight tiles on their way to the converters
+constexpr int kI8PrefetchAhead = 8;   // int8 weight tiles are fetched into L2 this many stages early
 constexpr int kMaxStages = 6;
 constexpr int kChunkKB = 16;   // K-blocks of 64 per exact fp32 chunk: 1024 products
 
@@ -65,8 +71,10 @@ constexpr int kWarpMMA = 1;
 constexpr int kWarpCvt0 = 2;   // backward: 2..9
 constexpr int kWarpEpi0 = 6;   // forward: 6..13
 constexpr int kBwdWarpEpi0 = 10; // backward: 10..13
-constexpr int kWarpRelay0 = 14; // 14..15 (and warp 1 in the odd CTA)
-constexpr int kRelays = 3;
+constexpr int kWarpRelay0 = 14; // backward, odd CTA: 14, 15, 17 and warp 1
+constexpr int kWarpI8Producer = 16;   // backward: TMA of the int8 weight tiles
+constexpr int kWarpRelayLast = 17;
+constexpr int kRelays = 4;
 // The epilogue waits for a whole accumulation unit (microseconds): it polls
 // with a back-off so that the converter warps on the same schedulers keep
 // their issue slots.
@@ -76,8 +84,7 @@ constexpr int kEpiWarps = 8;      // forward
 constexpr int kBwdEpiWarps = 4;   // backward
 constexpr int kCvtThreads = kCvtWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kBarCvt = 1;     // named barrier ids
-constexpr int kBarEpi = 2;
+constexpr int kBarEpi = 2;     // named barrier id
 
 constexpr int kPairM = 256;    // rows of the pair tile (MMA M)
 constexpr int kPairN = 256;    // columns of the pair tile (MMA N)
@@ -92,6 +99,8 @@ struct __align__(8) Barriers {
   uint64_t ready[kMaxStages];     // backward, even CTA: both CTAs' operands of stage s in place
   uint64_t cvt_done[kMaxStages];  // backward, odd CTA: its converters finished stage s
   uint64_t empty[kMaxStages];     // the pair's MMAs finished reading stage s
+  uint64_t i8_full[kI8Stages];    // backward: this CTA's int8 weight tile j landed
+  uint64_t i8_empty[kI8Stages];   // backward: this CTA's converters read int8 tile j
   uint64_t acc_full[2];         // an accumulator unit / buffer is complete
   uint64_t acc_empty[2];        // even CTA: both CTAs' epilogues released it
   uint64_t teardown;            // even CTA: every MMA finished
@@ -99,14 +108,18 @@ struct __align__(8) Barriers {
   int abort_flag;
 };
 
-// stage s of each CTA: [A operand 16 KB][B operand 16 KB] fp16, 128B-swizzled;
-// the backward adds the 8 KB int8 weight tile that its converters widen.
+// stage s of each CTA: [A operand 16 KB][B operand 16 KB] fp16, 128B-swizzled.
+// The backward keeps a separate ring of 8 KB int8 weight tiles after its
+// operand stages: a weight tile is loaded while the operand stage it will be
+// converted into is still being read by the tensor cores, so the copy latency
+// and the conversion and hand-over latency overlap instead of adding up.
 constexpr int kOpBytes = kCtaRows * kBK * 2;   // 16 KB
 constexpr int kI8Bytes = kCtaRows * kBK;       // 8 KB
 constexpr int kFwdStageBytes = 2 * kOpBytes;
-constexpr int kBwdStageBytes = 2 * kOpBytes + kI8Bytes;
-constexpr int kSmemTiles = kFwdStages * kFwdStageBytes > kBwdStages * kBwdStageBytes
-                               ? kFwdStages * kFwdStageBytes : kBwdStages * kBwdStageBytes;
+constexpr int kBwdStageBytes = 2 * kOpBytes;
+constexpr int kBwdI8Offset = kBwdStages * kBwdStageBytes;
+constexpr int kBwdSmemTiles = kBwdI8Offset + kI8Stages * kI8Bytes;
+constexpr int kSmemTiles = kFwdStages * kFwdStageBytes > kBwdSmemTiles ? kFwdStages * kFwdStageBytes : kBwdSmemTiles;
 constexpr int kSmemBytes = 1024 /*align slack*/ + kSmemTiles + 2 * kPairN * 4 /*epilogue vectors*/ +
                            static_cast<int>(sizeof(Barriers));
 
@@ -222,6 +235,10 @@ __device__ __forceinline__ void init_barriers(Barriers* bars, int epi_warps) {
     mbar_init(&bars->ready[s], kCvtWarps + 1);   // the even CTA's converters + one relay arrival
     mbar_init(&bars->cvt_done[s], kCvtWarps);
     mbar_init(&bars->empty[s], 1);
+  }
+  for (int j = 0; j < kI8Stages; ++j) {
+    mbar_init(&bars->i8_full[j], 1);
+    mbar_init(&bars->i8_empty[j], kCvtWarps);
   }
   for (int b = 0; b < 2; ++b) {
     mbar_init(&bars->acc_full[b], 1);
@@ -522,12 +539,13 @@ __device__ __forceinline__ void bwd_store16(const BwdEpiArgs& e, int64_t kk, int
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     bwd_gemm_kernel(const __grid_constant__ BwdGemmArgs g, const BwdEpiArgs e, int num_k, int num_m, int group) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Barriers* bars = reinterpret_cast<Barriers*>(smem + kSmemTiles + 2 * kPairN * 4);
   volatile int* abort_flag = &bars->abort_flag;
+  uint8_t* i8_ring = smem + kBwdI8Offset;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -540,16 +558,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc_pair(&bars->tmem_base, 512);
     tmem_relinquish_pair();
   }
-  if (warp == kWarpProducer && lane == 0) {
-    tma_prefetch_desc(&g.tmW);
-    tma_prefetch_desc(&g.tmG);
-  }
+  if (warp == kWarpProducer && lane == 0) tma_prefetch_desc(&g.tmG);
+  if (warp == kWarpI8Producer && lane == 0) tma_prefetch_desc(&g.tmW);
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;   // two 256-column accumulators
 
   if (warp == kWarpProducer) {
+    // ---- G16 tiles: both CTAs' copies complete on the even CTA's barrier
+    if (lane == 0) {
+      const uint32_t full0 = mapa_shared(&bars->full[0], 0);
+      int it = 0;
+      bool ok = true;
+      for (int t = cid; t < num_tiles && ok; t += ncl) {
+        int tm, tk;
+        tile_coords(t, num_m, num_k, group, tm, tk);
+        const int m_cta = tm * kPairN + static_cast<int>(rank) * kCtaRows;
+        for (int b = 0; b < NB; ++b, ++it) {
+          const int s = it % kBwdStages;
+          const uint32_t ph = (it / kBwdStages) & 1;
+          if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
+          if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], 2 * kOpBytes);
+          tma_load_2d_pair(smem + s * kBwdStageBytes + kOpBytes, &g.tmG, b * kBK, m_cta,
+                           full0 + static_cast<uint32_t>(s) * 8u);   // G16[m:+128][n:+64]
+        }
+      }
+      if (rank == 0)
+        for (int j = max(0, it - kBwdStages); j < it; ++j)
+          mbar_wait_teardown(&bars->full[j % kBwdStages], (j / kBwdStages) & 1, e.st);
+    }
+  } else if (warp == kWarpI8Producer) {
+    // ---- int8 weight tiles CB[n:+64][k:+128], this CTA's own ring
     if (lane == 0) {
       int it = 0;
       bool ok = true;
@@ -557,20 +597,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int tm, tk;
         tile_coords(t, num_m, num_k, group, tm, tk);
         const int k_cta = tk * kPairM + static_cast<int>(rank) * kCtaRows;
-        const int m_cta = tm * kPairN + static_cast<int>(rank) * kCtaRows;
         for (int b = 0; b < NB; ++b, ++it) {
-          const int s = it % kBwdStages;
-          const uint32_t ph = (it / kBwdStages) & 1;
-          if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
-          uint8_t* sa = smem + s * kBwdStageBytes;
-          uint8_t* sb = sa + kOpBytes;
-          mbar_arrive_expect_tx(&bars->full[s], kI8Bytes + kOpBytes);
-          tma_load_2d(sa + 2 * kOpBytes, &g.tmW, k_cta, b * kBK, &bars->full[s]);   // CB[n:+64][k:+128] int8
-          tma_load_2d(sb, &g.tmG, b * kBK, m_cta, &bars->full[s]);   // G16[m:+128][n:+64]
+          const int j = it % kI8Stages;
+          const uint32_t ph = (it / kI8Stages) & 1;
+          if (!mbar_wait(&bars->i8_empty[j], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->i8_full[j], kI8Bytes);
+          tma_load_2d(i8_ring + j * kI8Bytes, &g.tmW, k_cta, b * kBK, &bars->i8_full[j]);
+          // the copy above waits on DRAM for about a microsecond; a tile a few
+          // stages ahead is pulled into L2 now, so its own copy finds it there
+          int bp = b + kI8PrefetchAhead, tp = t;
+          while (bp >= NB && tp < num_tiles) {
+            bp -= NB;
+            tp += ncl;
+          }
+          if (tp < num_tiles) {
+            int tmp, tkp;
+            tile_coords(tp, num_m, num_k, group, tmp, tkp);
+            tma_prefetch_l2_2d(&g.tmW, tkp * kPairM + static_cast<int>(rank) * kCtaRows, bp * kBK);
+          }
         }
       }
-      for (int j = max(0, it - kBwdStages); j < it; ++j)
-        mbar_wait_teardown(&bars->full[j % kBwdStages], (j / kBwdStages) & 1, e.st);
+      for (int j = max(0, it - kI8Stages); j < it; ++j)
+        mbar_wait_teardown(&bars->i8_full[j % kI8Stages], (j / kI8Stages) & 1, e.st);
     }
   } else if (warp == kWarpMMA) {
     if (rank == 0 && lane == 0) {
@@ -590,7 +638,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int b = 0; b < NB; ++b, ++it) {
           const int s = it % kBwdStages;
           const uint32_t ph = (it / kBwdStages) & 1;
-          if (!mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
+          if (!mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereMMA) ||
+              !mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + s * kBwdStageBytes);
           const uint32_t b_base = a_base + kOpBytes;
@@ -611,35 +663,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kWarpRelay0) {
     if (rank == 1 && lane == 0)
-      relay_loop(bars, cid, ncl, num_tiles, NB, 1 + (warp - kWarpRelay0), abort_flag, e.st);
+      relay_loop(bars, cid, ncl, num_tiles, NB, warp == kWarpRelayLast ? 3 : 1 + (warp - kWarpRelay0), abort_flag,
+                 e.st);
   } else if (warp < kBwdWarpEpi0) {
-    // ---- converters: CB int8 [64 n][128 k] -> Wdq^T fp16, MN-major 128B-swizzled.
-    // All eight warps work on every stage (two 16-byte items per thread), so
-    // that a stage is ready soon after its copy lands.
+    // ---- converters: CB int8 [64 n][128 k] (128B-swizzled rows) -> Wdq^T
+    // fp16, MN-major 128B-swizzled.  All eight warps work on every stage: a
+    // thread takes the 16-byte chunk q of rows nl0 and nl0 + 32 (16 k x 1 n
+    // each).  The 8 lanes of a quarter warp take 8 consecutive rows of one
+    // chunk column, so that with both tiles swizzled their 16-byte loads and
+    // stores fall in 8 different bank groups.  The two row scales of a stage
+    // are loaded one stage ahead, so that their L2 latency overlaps the wait
+    // for the next tile.
     const int gt = threadIdx.x - kWarpCvt0 * 32;   // 0..255
     const uint64_t negc2 = f32x2_splat(-8388736.0f);   // -(2^23 + 128)
+    const int r = gt & 7;                          // row within an 8-row atom
+    const int q = (gt >> 3) & 7;                   // 16-byte chunk of the 128-byte int8 row
+    const int nl0 = r + 8 * (gt >> 6);             // rows nl0 and nl0 + 32 of every int8 tile
+    auto load_scb = [&](int b, float (&f)[2]) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int n = b * kBK + nl0 + 32 * j;
+        f[j] = n < e.N ? __ldg(e.SCB + n) : 0.f;
+      }
+    };
+    float scb_next[2];
+    load_scb(0, scb_next);
     int it = 0;
     bool go = true;
     for (int t = cid; t < num_tiles && go; t += ncl) {
       for (int b = 0; b < NB; ++b, ++it) {
+        const float scb_cur[2] = {scb_next[0], scb_next[1]};
+        load_scb(b + 1 < NB ? b + 1 : 0, scb_next);
         const int s = it % kBwdStages;
         const uint32_t ph = (it / kBwdStages) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereCvt))) {
+        const int j8 = it % kI8Stages;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&bars->i8_full[j8], (it / kI8Stages) & 1, abort_flag, e.st, kWhereCvt))) {
+          go = false;
+          break;
+        }
+        const uint8_t* src = i8_ring + j8 * kI8Bytes;
+        uint4 v[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) v[j] = *reinterpret_cast<const uint4*>(src + (nl0 + 32 * j) * 128 + ((q ^ r) << 4));
+        // the operand slot is free once the pair's MMAs of its previous use completed
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereCvt))) {
           go = false;
           break;
         }
         uint8_t* sa = smem + s * kBwdStageBytes;
-        const uint4* src = reinterpret_cast<const uint4*>(sa + 2 * kOpBytes);
-        uint4 v[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) v[j] = src[gt + kCvtThreads * j];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const int item = gt + kCvtThreads * j;   // n_local = item / 8, 16-byte group q = item % 8
-          const int nl = item >> 3, q = item & 7;
-          const int n = b * kBK + nl;
-          const uint64_t f2 = f32x2_splat((n < e.N) ? __fmul_rn(__ldg(e.SCB + n), 1.0f / 127.0f) : 0.f);
-          const int r = nl & 7, i = nl >> 3;       // row in atom, K atom
+          const uint64_t f2 = f32x2_splat(__fmul_rn(scb_cur[j], 1.0f / 127.0f));
+          const int i = (nl0 >> 3) + 4 * j;        // K atom (8 n) of row nl0 + 32 j
           const int ja = q >> 2;                   // MN atom (64 k)
           const int c0 = (q & 3) * 2;              // 16-byte chunk in the 128-byte row
           uint4 o0, o1;
@@ -653,9 +729,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        // the even CTA's MMA thread reads this CTA's tiles: local arrive there,
-        // a relay (cluster-scope release) from the odd CTA
-        if (lane == 0) mbar_arrive(rank == 0 ? &bars->ready[s] : &bars->cvt_done[s]);
+        if (lane == 0) {
+          mbar_arrive(&bars->i8_empty[j8]);
+          // the even CTA's MMA thread reads this CTA's tiles: local arrive there,
+          // a relay (cluster-scope release) from the odd CTA
+          mbar_arrive(rank == 0 ? &bars->ready[s] : &bars->cvt_done[s]);
+        }
       }
     }
   } else {
@@ -721,11 +800,13 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
   }
 }
 
+int g_pairs_fwd[64] = {};   // resident pairs per device, per kernel
+int g_pairs_bwd[64] = {};
+
 // Number of CTA pairs that fit on the device at once (each CTA needs most
 // of an SM's shared memory), so that a persistent grid never has a second
 // wave of pairs.
-int resident_pairs(const void* fn) {
-  static int cached[64] = {};
+int resident_pairs(const void* fn, int threads, int (&cached)[64]) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
@@ -733,7 +814,7 @@ int resident_pairs(const void* fn) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n <= 0) {
@@ -761,8 +842,9 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
   else return cudaErrorInvalidValue;
   static bool attr_fwd = false, attr_bwd = false;
   if (!set_smem_attr(fn, kernel_id == K_FWD_GEMM ? attr_fwd : attr_bwd)) return cudaGetLastError();
-  if (ctas != nullptr) *ctas = 2 * resident_pairs(fn);
-  if (threads != nullptr) *threads = kThreads;
+  const int nthreads = kernel_id == K_FWD_GEMM ? kThreads : kBwdThreads;
+  if (ctas != nullptr) *ctas = 2 * resident_pairs(fn, nthreads, kernel_id == K_FWD_GEMM ? g_pairs_fwd : g_pairs_bwd);
+  if (threads != nullptr) *threads = nthreads;
   if (smem_bytes != nullptr) *smem_bytes = kSmemBytes;
   return cudaSuccess;
 }
@@ -786,7 +868,7 @@ cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStrea
   static bool attr_set = false;
   if (!set_smem_attr(reinterpret_cast<const void*>(fwd_gemm_kernel), attr_set)) return cudaGetLastError();
   const int tiles = num_m * num_n;
-  const int clusters = std::min(tiles, resident_pairs(reinterpret_cast<const void*>(fwd_gemm_kernel)));
+  const int clusters = std::min(tiles, resident_pairs(reinterpret_cast<const void*>(fwd_gemm_kernel), kThreads, g_pairs_fwd));
   const int group = std::min(num_m, 8);
   ProfScope ps(K_FWD_GEMM, s);
   fwd_gemm_kernel<<<2 * clusters, kThreads, kSmemBytes, s>>>(g, e, num_m, num_n, group);
@@ -800,10 +882,11 @@ cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaStrea
   static bool attr_set = false;
   if (!set_smem_attr(reinterpret_cast<const void*>(bwd_gemm_kernel), attr_set)) return cudaGetLastError();
   const int tiles = num_k * num_m;
-  const int clusters = std::min(tiles, resident_pairs(reinterpret_cast<const void*>(bwd_gemm_kernel)));
+  const int clusters =
+      std::min(tiles, resident_pairs(reinterpret_cast<const void*>(bwd_gemm_kernel), kBwdThreads, g_pairs_bwd));
   const int group = std::min(num_m, 8);
   ProfScope ps(K_BWD_GEMM, s);
-  bwd_gemm_kernel<<<2 * clusters, kThreads, kSmemBytes, s>>>(g, e, num_k, num_m, group);
+  bwd_gemm_kernel<<<2 * clusters, kBwdThreads, kSmemBytes, s>>>(g, e, num_k, num_m, group);
   return cudaGetLastError();
 }
 
