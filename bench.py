@@ -170,7 +170,8 @@ class Layer:
         self.cap = cap
         self.out = torch.empty(spec.M, spec.N, dtype=spec.dtype, device=device)
         self.ws_f = I.functional.forward_workspace(spec.M, spec.K, spec.N, cap, device)
-        self.ws_b = I.functional.backward_workspace(spec.M, spec.N, spec.dtype, device)
+        # room for the materialized dequantized weight: the faster backward schedule
+        self.ws_b = I.functional.backward_workspace(spec.M, spec.N, spec.dtype, device, K=spec.K)
         self.grad_A = torch.empty(spec.M, spec.K, dtype=spec.dtype, device=device)
         self.grad_bias = torch.empty(spec.N, dtype=wdt, device=device)
 
@@ -216,6 +217,7 @@ def kernel_bytes(L, name):
         "gradout_prepass": s.M * s.N * a,
         "build_subB": s.N * cap_pad * 3,
         "widen_codes": s.N * kp * 3,
+        "dequant_weight": s.N * kp + kp * ((s.N + 7) // 8 * 8) * 2 + s.N * 4,
     }.get(name, 0.0)
 
 
@@ -346,10 +348,10 @@ def _layer_of(i, layers):
 def launches_per_layer(L) -> int:
     """Our kernels per layer and step: colmax, outlier index, row quantize,
     subB (outliers on), weight-code widening, forward GEMM; grad_output
-    prepass, grad_bias finalize, backward GEMM."""
+    prepass, grad_bias finalize, weight dequantization, backward GEMM."""
     import math
     fwd = 6 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 3
-    return fwd + 3
+    return fwd + 4
 
 
 def run_e2e(layers, stream, steps, device):

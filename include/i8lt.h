@@ -147,9 +147,15 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K,
                  void* ws, size_t ws_bytes, int64_t max_outliers,
                  const i8lt_fwd_debug* dbg, void* stream);
 
-/* Workspace of i8lt_backward_input, in bytes (space for the fp16 copy of
- * grad_output when it is not already fp16 with N a multiple of 8). */
+/* Workspace of i8lt_backward_input, in bytes.
+ * i8lt_backward_workspace_size: the minimum, for the fused schedule (status
+ * word, grad_bias partial sums, and the fp16 copy of grad_output when it is
+ * not already fp16 with N a multiple of 8).
+ * i8lt_backward_workspace_size_dq: the minimum plus the transient
+ * dequantized weight of the materialized schedule, K_pad x N_pad fp16
+ * (K_pad = i8lt_weight_ld(K), N_pad = N rounded up to 8). */
 size_t i8lt_backward_workspace_size(int64_t M, int64_t N, int gt);
+size_t i8lt_backward_workspace_size_dq(int64_t M, int64_t N, int64_t K, int gt);
 
 /*
  * Memory-efficient backward to the input (no weight gradient: the weight is
@@ -160,9 +166,17 @@ size_t i8lt_backward_workspace_size(int64_t M, int64_t N, int gt);
  *   grad_A    [M, K] dtype `gt`, or NULL to skip:
  *             grad_A = to_dtype( fp16(G) @ W_dq ),
  *             W_dq[n,k] = fp16_rn(fp32(CB[n,k]) * (SCB[n] * fp32(1/127)))
- *             built in shared memory inside the GEMM, never stored
+ *             (bitsandbytes PR #33, "Memory efficient backward": the int8
+ *             weight is dequantized to fp16 for the backward matmul on every
+ *             call and the fp16 weight is not kept between calls)
  *   grad_bias [N] dtype `bt`, or NULL to skip: sum over rows of the uncast G
- *   ws        workspace of at least i8lt_backward_workspace_size bytes
+ *   ws        workspace of at least i8lt_backward_workspace_size bytes.  The
+ *             size picks the schedule (same results either way):
+ *             ws_bytes >= i8lt_backward_workspace_size_dq: materialized --
+ *               a memory-bound prepass writes W_dq transposed into the
+ *               workspace, then a plain fp16 GEMM reads it (the faster one);
+ *             otherwise fused -- W_dq is rebuilt tile by tile in shared
+ *               memory inside the GEMM and never stored (no N x K buffer).
  */
 int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N,
                         const int8_t* CB, const float* SCB, int64_t K,
@@ -221,7 +235,8 @@ int i8lt_silu_backward(const void* g, const void* h, int dt, int64_t n,
 typedef enum {
   I8LT_K_QUANTIZE_WEIGHT = 0, I8LT_K_COLMAX = 1, I8LT_K_OUTLIER_INDEX = 2, I8LT_K_ROW_QUANTIZE = 3,
   I8LT_K_SUBB = 4, I8LT_K_FWD_GEMM = 5, I8LT_K_GRADOUT_PREPASS = 6, I8LT_K_GRAD_BIAS_FINALIZE = 7,
-  I8LT_K_BWD_GEMM = 8, I8LT_K_SILU = 9, I8LT_K_SILU_BACKWARD = 10, I8LT_K_WIDEN_CODES = 11, I8LT_K_COUNT = 12
+  I8LT_K_BWD_GEMM = 8, I8LT_K_SILU = 9, I8LT_K_SILU_BACKWARD = 10, I8LT_K_WIDEN_CODES = 11,
+  I8LT_K_DEQUANT_WEIGHT = 12, I8LT_K_COUNT = 13
 } i8lt_kernel_id;
 typedef struct {
   int kernel;

@@ -48,7 +48,8 @@ class i8lt_kernel_time(Structure):
 
 
 KERNELS = ("quantize_weight", "colmax", "outlier_index", "row_quantize", "build_subB", "fwd_gemm",
-           "gradout_prepass", "grad_bias_finalize", "bwd_gemm", "silu", "silu_backward", "widen_codes")
+           "gradout_prepass", "grad_bias_finalize", "bwd_gemm", "silu", "silu_backward", "widen_codes",
+           "dequant_weight")
 
 
 # name -> (restype, argtypes); the same names and order as include/i8lt.h
@@ -63,6 +64,7 @@ SIGNATURES = {
                              c_void_p, c_int, c_float, c_void_p, c_void_p,
                              c_void_p, c_size_t, c_int64, POINTER(i8lt_fwd_debug), c_void_p]),
     "i8lt_backward_workspace_size": (c_size_t, [c_int64, c_int64, c_int]),
+    "i8lt_backward_workspace_size_dq": (c_size_t, [c_int64, c_int64, c_int64, c_int]),
     "i8lt_backward_input": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
                                     c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
     "i8lt_backward_input_noalloc": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
@@ -146,6 +148,10 @@ def i8lt_forward(A, at, M, K, CB, SCB, N, bias, bt, threshold, residual, out, ws
 
 def i8lt_backward_workspace_size(M, N, gt) -> int:
     return load().i8lt_backward_workspace_size(M, N, gt)
+
+
+def i8lt_backward_workspace_size_dq(M, N, K, gt) -> int:
+    return load().i8lt_backward_workspace_size_dq(M, N, K, gt)
 
 
 def i8lt_backward_input(G, gt, M, N, CB, SCB, K, addend, grad_A, grad_bias, bt, ws, ws_bytes,

@@ -109,12 +109,15 @@ i8lt_fwd_layout fwd_layout(int64_t M, int64_t K, int64_t N, int64_t cap) {
 
 bool needs_g16(int64_t N, int gt) { return gt != DT_F16 || (N % 8) != 0; }
 
+// Backward workspace: [status][grad_bias partial sums][G16 when needed]
+// = the fused schedule's minimum (`total`), then [WdqT, K_pad x N_pad fp16]
+// for the materialized schedule (`total_dq`).
 struct BwdLayout {
-  size_t status, partial, g16, total;
+  size_t status, partial, g16, total, wdq, total_dq;
   int64_t n_pad, chunks;
 };
 
-BwdLayout bwd_layout(int64_t M, int64_t N, int gt) {
+BwdLayout bwd_layout(int64_t M, int64_t N, int64_t K, int gt) {
   BwdLayout L;
   L.n_pad = round_up(N, 8);
   L.chunks = gradout_partial_chunks(M);
@@ -126,6 +129,9 @@ BwdLayout bwd_layout(int64_t M, int64_t N, int gt) {
   L.g16 = off;
   if (needs_g16(N, gt)) off += align_up(static_cast<size_t>(M) * L.n_pad * 2);
   L.total = off;
+  L.wdq = off;
+  off += align_up(static_cast<size_t>(round_up(K, 16)) * L.n_pad * 2);
+  L.total_dq = off;
   return L;
 }
 
@@ -303,7 +309,12 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, 
 
 size_t i8lt_backward_workspace_size(int64_t M, int64_t N, int gt) {
   if (M < 0 || N < 0 || !valid_dt(gt)) return 0;
-  return bwd_layout(M, N, gt).total;
+  return bwd_layout(M, N, 0, gt).total;
+}
+
+size_t i8lt_backward_workspace_size_dq(int64_t M, int64_t N, int64_t K, int gt) {
+  if (M < 0 || N < 0 || K < 0 || K > I8LT_MAX_K || !valid_dt(gt)) return 0;
+  return bwd_layout(M, N, K, gt).total_dq;
 }
 
 int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_t* CB, const float* SCB, int64_t K,
@@ -318,8 +329,9 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_
   if (M > 0 && G == nullptr) return I8LT_ERR_INVALID_ARG;
   if (!aligned16(G) || !aligned16(CB) || !aligned16(grad_A) || !aligned16(addend)) return I8LT_ERR_MISALIGNED;
   if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
-  const BwdLayout L = bwd_layout(M, N, gt);
+  const BwdLayout L = bwd_layout(M, N, K, gt);
   if (ws_bytes < L.total) return I8LT_ERR_WORKSPACE;
+  const bool materialize = ws_bytes >= L.total_dq;   // else the fused schedule
   if (int d = check_device()) return d;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -342,11 +354,19 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_
   std::memset(&g, 0, sizeof(g));
   const void* gsrc = G16 != nullptr ? static_cast<const void*>(G16) : G;
   const int64_t gpitch = G16 != nullptr ? L.n_pad : N;
-  if (!make_tmap(&g.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, CB, k_pad, N, k_pad, kBoxK, kBK,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&g.tmG, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, gsrc, gpitch, M, gpitch * 2, kBK, kBoxRows,
+  if (!make_tmap(&g.tmG, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, gsrc, gpitch, M, gpitch * 2, kBK, kBoxRows,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return I8LT_ERR_CUDA;
+  if (materialize) {
+    __half* WdqT = reinterpret_cast<__half*>(w + L.wdq);
+    if (!make_tmap(&g.tmWT, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, WdqT, L.n_pad, k_pad, L.n_pad * 2, kBK, kBoxRows,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return I8LT_ERR_CUDA;
+    if (launch_dequant_weight(CB, SCB, N, k_pad, WdqT, L.n_pad, s) != cudaSuccess) return I8LT_ERR_CUDA;
+  } else if (!make_tmap(&g.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, CB, k_pad, N, k_pad, kBoxK, kBK,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) {
+    return I8LT_ERR_CUDA;
+  }
   BwdEpiArgs ea;
   ea.M = static_cast<int>(M);
   ea.N = static_cast<int>(N);
@@ -356,7 +376,7 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_
   ea.grad_A = grad_A;
   ea.dt = gt;
   ea.st = st;
-  return cuda_status(launch_bwd_gemm(g, ea, s));
+  return cuda_status(launch_bwd_gemm(g, ea, !materialize, s));
 }
 
 int i8lt_silu_forward(const void* h, int dt, int64_t n, void* out, void* stream) {
@@ -415,7 +435,8 @@ int i8lt_gemm_launch_info(int kernel, int* ctas, int* threads, int* smem_bytes) 
 const char* i8lt_kernel_name(int k) {
   static const char* names[] = {"quantize_weight", "colmax",          "outlier_index",      "row_quantize",
                                 "build_subB",      "fwd_gemm",        "gradout_prepass",    "grad_bias_finalize",
-                                "bwd_gemm",        "silu",            "silu_backward",      "widen_codes"};
+                                "bwd_gemm",        "silu",            "silu_backward",      "widen_codes",
+                                "dequant_weight"};
   return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
 }
 

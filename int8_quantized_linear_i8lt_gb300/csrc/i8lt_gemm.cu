@@ -82,7 +82,6 @@ constexpr unsigned kEpiSleepNs = 256;
 constexpr int kCvtWarps = 8;       // backward: every converter warp works on every stage
 constexpr int kEpiWarps = 8;      // forward
 constexpr int kBwdEpiWarps = 4;   // backward
-constexpr int kCvtThreads = kCvtWarps * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kBarEpi = 2;     // named barrier id
 
@@ -539,6 +538,11 @@ __device__ __forceinline__ void bwd_store16(const BwdEpiArgs& e, int64_t kk, int
   }
 }
 
+// kFused: the A operand (Wdq^T) is rebuilt per stage from the int8 weight
+// tiles by the converter warps; otherwise it is loaded by TMA from the
+// materialized WdqT (K-major, like G16) and the converter, int8-producer and
+// relay warps stay idle.
+template <bool kFused>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     bwd_gemm_kernel(const __grid_constant__ BwdGemmArgs g, const BwdEpiArgs e, int num_k, int num_m, int group) {
   extern __shared__ uint8_t smem_raw[];
@@ -558,15 +562,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     tmem_alloc_pair(&bars->tmem_base, 512);
     tmem_relinquish_pair();
   }
-  if (warp == kWarpProducer && lane == 0) tma_prefetch_desc(&g.tmG);
-  if (warp == kWarpI8Producer && lane == 0) tma_prefetch_desc(&g.tmW);
+  if (warp == kWarpProducer && lane == 0) {
+    tma_prefetch_desc(&g.tmG);
+    if (!kFused) tma_prefetch_desc(&g.tmWT);
+  }
+  if (kFused && warp == kWarpI8Producer && lane == 0) tma_prefetch_desc(&g.tmW);
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;   // two 256-column accumulators
 
   if (warp == kWarpProducer) {
-    // ---- G16 tiles: both CTAs' copies complete on the even CTA's barrier
+    // ---- G16 tiles (and WdqT tiles when materialized): both CTAs' copies
+    // complete on the even CTA's barrier
     if (lane == 0) {
       const uint32_t full0 = mapa_shared(&bars->full[0], 0);
       int it = 0;
@@ -575,13 +583,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
         int tm, tk;
         tile_coords(t, num_m, num_k, group, tm, tk);
         const int m_cta = tm * kPairN + static_cast<int>(rank) * kCtaRows;
+        const int k_cta = tk * kPairM + static_cast<int>(rank) * kCtaRows;
         for (int b = 0; b < NB; ++b, ++it) {
           const int s = it % kBwdStages;
           const uint32_t ph = (it / kBwdStages) & 1;
           if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
-          if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], 2 * kOpBytes);
-          tma_load_2d_pair(smem + s * kBwdStageBytes + kOpBytes, &g.tmG, b * kBK, m_cta,
-                           full0 + static_cast<uint32_t>(s) * 8u);   // G16[m:+128][n:+64]
+          if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], (kFused ? 2 : 4) * kOpBytes);
+          const uint32_t full_s = full0 + static_cast<uint32_t>(s) * 8u;
+          if (!kFused)
+            tma_load_2d_pair(smem + s * kBwdStageBytes, &g.tmWT, b * kBK, k_cta, full_s);   // WdqT[k:+128][n:+64]
+          tma_load_2d_pair(smem + s * kBwdStageBytes + kOpBytes, &g.tmG, b * kBK, m_cta, full_s);   // G16[m:+128][n:+64]
         }
       }
       if (rank == 0)
@@ -590,7 +601,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpI8Producer) {
     // ---- int8 weight tiles CB[n:+64][k:+128], this CTA's own ring
-    if (lane == 0) {
+    if (kFused && lane == 0) {
       int it = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl) {
@@ -622,8 +633,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpMMA) {
     if (rank == 0 && lane == 0) {
-      // A: MN-major, 128B swizzle; MN atoms (64 k) 1024 B apart, K atoms (8 n) 2048 B apart.
-      const uint32_t idesc = make_idesc_f16(kPairM, kPairN, true, false);
+      // A, fused: MN-major, 128B swizzle; MN atoms (64 k) 1024 B apart, K atoms
+      // (8 n) 2048 B apart.  Materialized: K-major like B.
+      const uint32_t idesc = make_idesc_f16(kPairM, kPairN, kFused, false);
       int it = 0, tl = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl, ++tl) {
@@ -639,7 +651,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
           const int s = it % kBwdStages;
           const uint32_t ph = (it / kBwdStages) & 1;
           if (!mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereMMA) ||
-              !mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA)) {
+              (kFused && !mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA))) {
             ok = false;
             break;
           }
@@ -648,7 +660,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
           const uint32_t b_base = a_base + kOpBytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = make_sdesc(a_base + k * 4096, 1024, 2048, kSwizzle128B);
+            const uint64_t ad = kFused ? make_sdesc(a_base + k * 4096, 1024, 2048, kSwizzle128B)
+                                       : make_sdesc(a_base + k * 32, 16, 1024, kSwizzle128B);
             const uint64_t bd = make_sdesc(b_base + k * 32, 16, 1024, kSwizzle128B);
             umma_f16_pair(d, ad, bd, idesc, (b > 0 || k > 0) ? 1u : 0u);
           }
@@ -658,82 +671,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       }
       umma_commit_pair(&bars->teardown);
       mbar_wait_teardown(&bars->teardown, 0, e.st);
-    } else if (rank == 1 && lane == 0) {
+    } else if (kFused && rank == 1 && lane == 0) {
       relay_loop(bars, cid, ncl, num_tiles, NB, 0, abort_flag, e.st);
     }
   } else if (warp >= kWarpRelay0) {
-    if (rank == 1 && lane == 0)
+    if (kFused && rank == 1 && lane == 0)
       relay_loop(bars, cid, ncl, num_tiles, NB, warp == kWarpRelayLast ? 3 : 1 + (warp - kWarpRelay0), abort_flag,
                  e.st);
   } else if (warp < kBwdWarpEpi0) {
-    // ---- converters: CB int8 [64 n][128 k] (128B-swizzled rows) -> Wdq^T
-    // fp16, MN-major 128B-swizzled.  All eight warps work on every stage: a
-    // thread takes the 16-byte chunk q of rows nl0 and nl0 + 32 (16 k x 1 n
-    // each).  The 8 lanes of a quarter warp take 8 consecutive rows of one
-    // chunk column, so that with both tiles swizzled their 16-byte loads and
-    // stores fall in 8 different bank groups.  The two row scales of a stage
-    // are loaded one stage ahead, so that their L2 latency overlaps the wait
-    // for the next tile.
-    const int gt = threadIdx.x - kWarpCvt0 * 32;   // 0..255
-    const uint64_t negc2 = f32x2_splat(-8388736.0f);   // -(2^23 + 128)
-    const int r = gt & 7;                          // row within an 8-row atom
-    const int q = (gt >> 3) & 7;                   // 16-byte chunk of the 128-byte int8 row
-    const int nl0 = r + 8 * (gt >> 6);             // rows nl0 and nl0 + 32 of every int8 tile
-    auto load_scb = [&](int b, float (&f)[2]) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int n = b * kBK + nl0 + 32 * j;
-        f[j] = n < e.N ? __ldg(e.SCB + n) : 0.f;
-      }
-    };
-    float scb_next[2];
-    load_scb(0, scb_next);
-    int it = 0;
-    bool go = true;
-    for (int t = cid; t < num_tiles && go; t += ncl) {
-      for (int b = 0; b < NB; ++b, ++it) {
-        const float scb_cur[2] = {scb_next[0], scb_next[1]};
-        load_scb(b + 1 < NB ? b + 1 : 0, scb_next);
-        const int s = it % kBwdStages;
-        const uint32_t ph = (it / kBwdStages) & 1;
-        const int j8 = it % kI8Stages;
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&bars->i8_full[j8], (it / kI8Stages) & 1, abort_flag, e.st, kWhereCvt))) {
-          go = false;
-          break;
-        }
-        const uint8_t* src = i8_ring + j8 * kI8Bytes;
-        uint4 v[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) v[j] = *reinterpret_cast<const uint4*>(src + (nl0 + 32 * j) * 128 + ((q ^ r) << 4));
-        // the operand slot is free once the pair's MMAs of its previous use completed
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereCvt))) {
-          go = false;
-          break;
-        }
-        uint8_t* sa = smem + s * kBwdStageBytes;
+    if constexpr (kFused) {
+      // ---- converters: CB int8 [64 n][128 k] (128B-swizzled rows) -> Wdq^T
+      // fp16, MN-major 128B-swizzled.  All eight warps work on every stage: a
+      // thread takes the 16-byte chunk q of rows nl0 and nl0 + 32 (16 k x 1 n
+      // each).  The 8 lanes of a quarter warp take 8 consecutive rows of one
+      // chunk column, so that with both tiles swizzled their 16-byte loads and
+      // stores fall in 8 different bank groups.  The two row scales of a stage
+      // are loaded one stage ahead, so that their L2 latency overlaps the wait
+      // for the next tile.
+      const int gt = threadIdx.x - kWarpCvt0 * 32;   // 0..255
+      const uint64_t negc2 = f32x2_splat(-8388736.0f);   // -(2^23 + 128)
+      const int r = gt & 7;                          // row within an 8-row atom
+      const int q = (gt >> 3) & 7;                   // 16-byte chunk of the 128-byte int8 row
+      const int nl0 = r + 8 * (gt >> 6);             // rows nl0 and nl0 + 32 of every int8 tile
+      auto load_scb = [&](int b, float (&f)[2]) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const uint64_t f2 = f32x2_splat(__fmul_rn(scb_cur[j], 1.0f / 127.0f));
-          const int i = (nl0 >> 3) + 4 * j;        // K atom (8 n) of row nl0 + 32 j
-          const int ja = q >> 2;                   // MN atom (64 k)
-          const int c0 = (q & 3) * 2;              // 16-byte chunk in the 128-byte row
-          uint4 o0, o1;
-          i8x4_scale_to_h4(v[j].x, negc2, f2, o0.x, o0.y);
-          i8x4_scale_to_h4(v[j].y, negc2, f2, o0.z, o0.w);
-          i8x4_scale_to_h4(v[j].z, negc2, f2, o1.x, o1.y);
-          i8x4_scale_to_h4(v[j].w, negc2, f2, o1.z, o1.w);
-          uint8_t* rowp = sa + i * 2048 + ja * 1024 + r * 128;
-          *reinterpret_cast<uint4*>(rowp + ((c0 ^ r) << 4)) = o0;
-          *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ r) << 4)) = o1;
+          const int n = b * kBK + nl0 + 32 * j;
+          f[j] = n < e.N ? __ldg(e.SCB + n) : 0.f;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars->i8_empty[j8]);
-          // the even CTA's MMA thread reads this CTA's tiles: local arrive there,
-          // a relay (cluster-scope release) from the odd CTA
-          mbar_arrive(rank == 0 ? &bars->ready[s] : &bars->cvt_done[s]);
+      };
+      float scb_next[2];
+      load_scb(0, scb_next);
+      int it = 0;
+      bool go = true;
+      for (int t = cid; t < num_tiles && go; t += ncl) {
+        for (int b = 0; b < NB; ++b, ++it) {
+          const float scb_cur[2] = {scb_next[0], scb_next[1]};
+          load_scb(b + 1 < NB ? b + 1 : 0, scb_next);
+          const int s = it % kBwdStages;
+          const uint32_t ph = (it / kBwdStages) & 1;
+          const int j8 = it % kI8Stages;
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(&bars->i8_full[j8], (it / kI8Stages) & 1, abort_flag, e.st, kWhereCvt))) {
+            go = false;
+            break;
+          }
+          const uint8_t* src = i8_ring + j8 * kI8Bytes;
+          uint4 v[2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) v[j] = *reinterpret_cast<const uint4*>(src + (nl0 + 32 * j) * 128 + ((q ^ r) << 4));
+          // the operand slot is free once the pair's MMAs of its previous use completed
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereCvt))) {
+            go = false;
+            break;
+          }
+          uint8_t* sa = smem + s * kBwdStageBytes;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint64_t f2 = f32x2_splat(__fmul_rn(scb_cur[j], 1.0f / 127.0f));
+            const int i = (nl0 >> 3) + 4 * j;        // K atom (8 n) of row nl0 + 32 j
+            const int ja = q >> 2;                   // MN atom (64 k)
+            const int c0 = (q & 3) * 2;              // 16-byte chunk in the 128-byte row
+            uint4 o0, o1;
+            i8x4_scale_to_h4(v[j].x, negc2, f2, o0.x, o0.y);
+            i8x4_scale_to_h4(v[j].y, negc2, f2, o0.z, o0.w);
+            i8x4_scale_to_h4(v[j].z, negc2, f2, o1.x, o1.y);
+            i8x4_scale_to_h4(v[j].w, negc2, f2, o1.z, o1.w);
+            uint8_t* rowp = sa + i * 2048 + ja * 1024 + r * 128;
+            *reinterpret_cast<uint4*>(rowp + ((c0 ^ r) << 4)) = o0;
+            *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ r) << 4)) = o1;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars->i8_empty[j8]);
+            // the even CTA's MMA thread reads this CTA's tiles: local arrive there,
+            // a relay (cluster-scope release) from the odd CTA
+            mbar_arrive(rank == 0 ? &bars->ready[s] : &bars->cvt_done[s]);
+          }
         }
       }
     }
@@ -803,6 +818,54 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
 int g_pairs_fwd[64] = {};   // resident pairs per device, per kernel
 int g_pairs_bwd[64] = {};
 
+// Backward prepass of the materialized schedule: WdqT[k][n] =
+// fp16_rn(fp32(CB[n][k]) * (SCB[n] * fp32(1/127))) -- the page's per-call
+// dequantization of the int8 weight for the fp16 backward matmul --
+// transposed so that the reduction index n is contiguous (a K-major GEMM
+// operand).  One CTA per 64 (n) x 128 (k) tile: coalesced 16-byte loads of
+// the int8 rows into shared memory, then each thread converts 8 consecutive
+// n of one k and writes them with one 16-byte store.
+constexpr int kDqN = 64, kDqK = 128, kDqPitch = kDqK + 4;   // shared rows padded by one word
+__global__ void __launch_bounds__(256) dequant_weight_kernel(const int8_t* __restrict__ CB,
+                                                             const float* __restrict__ SCB, int N, int k_pad,
+                                                             __half* __restrict__ WdqT, int n_pad) {
+  __shared__ __align__(16) uint8_t tile[kDqN * kDqPitch];
+  __shared__ float f_s[kDqN];
+  const int n0 = blockIdx.x * kDqN;
+  const int k0 = blockIdx.y * kDqK;
+  for (int c = threadIdx.x; c < kDqN * 8; c += 256) {
+    const int nl = c >> 3, q = c & 7;
+    const int n = n0 + nl, k = k0 + q * 16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < N && k < k_pad) v = __ldg(reinterpret_cast<const uint4*>(CB + static_cast<int64_t>(n) * k_pad + k));
+    uint32_t* dst = reinterpret_cast<uint32_t*>(tile + nl * kDqPitch + q * 16);
+    dst[0] = v.x;
+    dst[1] = v.y;
+    dst[2] = v.z;
+    dst[3] = v.w;
+  }
+  if (threadIdx.x < kDqN) {
+    const int n = n0 + static_cast<int>(threadIdx.x);
+    f_s[threadIdx.x] = n < N ? __fmul_rn(SCB[n], 1.0f / 127.0f) : 0.f;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < kDqK * 8; c += 256) {
+    const int g8 = c & 7, kl = c >> 3;
+    const int k = k0 + kl, n = n0 + g8 * 8;
+    if (k >= k_pad || n >= n_pad) continue;
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int a = g8 * 8 + 2 * i;
+      const float x0 = __fmul_rn(static_cast<float>(static_cast<int8_t>(tile[a * kDqPitch + kl])), f_s[a]);
+      const float x1 = __fmul_rn(static_cast<float>(static_cast<int8_t>(tile[(a + 1) * kDqPitch + kl])), f_s[a + 1]);
+      const __half2 p = __halves2half2(__float2half_rn(x0), __float2half_rn(x1));
+      h[i] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    *reinterpret_cast<uint4*>(WdqT + static_cast<int64_t>(k) * n_pad + n) = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
 // Number of CTA pairs that fit on the device at once (each CTA needs most
 // of an SM's shared memory), so that a persistent grid never has a second
 // wave of pairs.
@@ -835,13 +898,14 @@ bool set_smem_attr(const void* fn, bool& done) {
 
 }  // namespace
 
+bool g_attr_fwd = false, g_attr_bwd_fused = false, g_attr_bwd_dq = false;
+
 cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_bytes) {
   const void* fn = nullptr;
   if (kernel_id == K_FWD_GEMM) fn = reinterpret_cast<const void*>(fwd_gemm_kernel);
-  else if (kernel_id == K_BWD_GEMM) fn = reinterpret_cast<const void*>(bwd_gemm_kernel);
+  else if (kernel_id == K_BWD_GEMM) fn = reinterpret_cast<const void*>(bwd_gemm_kernel<false>);
   else return cudaErrorInvalidValue;
-  static bool attr_fwd = false, attr_bwd = false;
-  if (!set_smem_attr(fn, kernel_id == K_FWD_GEMM ? attr_fwd : attr_bwd)) return cudaGetLastError();
+  if (!set_smem_attr(fn, kernel_id == K_FWD_GEMM ? g_attr_fwd : g_attr_bwd_dq)) return cudaGetLastError();
   const int nthreads = kernel_id == K_FWD_GEMM ? kThreads : kBwdThreads;
   if (ctas != nullptr) *ctas = 2 * resident_pairs(fn, nthreads, kernel_id == K_FWD_GEMM ? g_pairs_fwd : g_pairs_bwd);
   if (threads != nullptr) *threads = nthreads;
@@ -865,8 +929,7 @@ cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStrea
   const int num_m = static_cast<int>(ceil_div(e.M, kPairM));
   const int num_n = static_cast<int>(ceil_div(e.N, kPairN));
   if (num_m == 0 || num_n == 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!set_smem_attr(reinterpret_cast<const void*>(fwd_gemm_kernel), attr_set)) return cudaGetLastError();
+  if (!set_smem_attr(reinterpret_cast<const void*>(fwd_gemm_kernel), g_attr_fwd)) return cudaGetLastError();
   const int tiles = num_m * num_n;
   const int clusters = std::min(tiles, resident_pairs(reinterpret_cast<const void*>(fwd_gemm_kernel), kThreads, g_pairs_fwd));
   const int group = std::min(num_m, 8);
@@ -875,18 +938,31 @@ cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStrea
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaStream_t s) {
+cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool fused, cudaStream_t s) {
   const int num_k = static_cast<int>(ceil_div(e.K, kPairM));
   const int num_m = static_cast<int>(ceil_div(e.M, kPairN));
   if (num_k == 0 || num_m == 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!set_smem_attr(reinterpret_cast<const void*>(bwd_gemm_kernel), attr_set)) return cudaGetLastError();
+  const void* fn = fused ? reinterpret_cast<const void*>(bwd_gemm_kernel<true>)
+                         : reinterpret_cast<const void*>(bwd_gemm_kernel<false>);
+  if (!set_smem_attr(fn, fused ? g_attr_bwd_fused : g_attr_bwd_dq)) return cudaGetLastError();
   const int tiles = num_k * num_m;
-  const int clusters =
-      std::min(tiles, resident_pairs(reinterpret_cast<const void*>(bwd_gemm_kernel), kBwdThreads, g_pairs_bwd));
+  const int clusters = std::min(tiles, resident_pairs(fn, kBwdThreads, g_pairs_bwd));
   const int group = std::min(num_m, 8);
   ProfScope ps(K_BWD_GEMM, s);
-  bwd_gemm_kernel<<<2 * clusters, kBwdThreads, kSmemBytes, s>>>(g, e, num_k, num_m, group);
+  if (fused)
+    bwd_gemm_kernel<true><<<2 * clusters, kBwdThreads, kSmemBytes, s>>>(g, e, num_k, num_m, group);
+  else
+    bwd_gemm_kernel<false><<<2 * clusters, kBwdThreads, kSmemBytes, s>>>(g, e, num_k, num_m, group);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_weight(const int8_t* CB, const float* SCB, int64_t N, int64_t k_pad, __half* WdqT,
+                                  int64_t n_pad, cudaStream_t s) {
+  if (N == 0 || k_pad == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(ceil_div(n_pad, kDqN)), static_cast<unsigned>(ceil_div(k_pad, kDqK)));
+  ProfScope ps(K_DEQUANT_WEIGHT, s);
+  dequant_weight_kernel<<<grid, 256, 0, s>>>(CB, SCB, static_cast<int>(N), static_cast<int>(k_pad), WdqT,
+                                             static_cast<int>(n_pad));
   return cudaGetLastError();
 }
 

@@ -91,7 +91,8 @@ cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStrea
 cudaError_t launch_widen_codes(const int8_t* CB, __half* CBh, int64_t n, cudaStream_t s);
 
 struct BwdGemmArgs {
-  CUtensorMap tmW;    // CB int8 [N, K_pad] viewed as (inner K_pad, outer N), box 128 x 64
+  CUtensorMap tmW;    // fused schedule: CB int8 [N, K_pad] (inner K_pad, outer N), box 128 x 64, 128B swizzle
+  CUtensorMap tmWT;   // materialized schedule: WdqT fp16 [K_pad, N_pad], box 64 x 128, 128B swizzle
   CUtensorMap tmG;    // G16 fp16 [M, N_pad], box 64 x 128, 128B swizzle
 };
 
@@ -104,7 +105,15 @@ struct BwdEpiArgs {
   DevStatus* st;
 };
 
-cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaStream_t s);
+// fused: the dequantized weight is rebuilt in shared memory from CB (tmW);
+// otherwise it is read from WdqT (tmWT), written by launch_dequant_weight.
+cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool fused, cudaStream_t s);
+
+// Backward prepass of the materialized schedule: WdqT[k, n] =
+// fp16_rn(fp32(CB[n, k]) * (SCB[n] * fp32(1/127))) for k < k_pad, n < N, and
+// 0 for N <= n < n_pad (n_pad a multiple of 8, k_pad of 16).
+cudaError_t launch_dequant_weight(const int8_t* CB, const float* SCB, int64_t N, int64_t k_pad, __half* WdqT,
+                                  int64_t n_pad, cudaStream_t s);
 
 // Persistent launch shape of a GEMM kernel (K_FWD_GEMM / K_BWD_GEMM).
 cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_bytes);
@@ -112,7 +121,7 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
 // Kernel ids of the timing records (match i8lt_kernel_id in i8lt.h).
 enum KernelId {
   K_QUANTIZE_WEIGHT = 0, K_COLMAX, K_OUTLIER_INDEX, K_ROW_QUANTIZE, K_SUBB, K_FWD_GEMM, K_GRADOUT_PREPASS,
-  K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_WIDEN_CODES, K_COUNT
+  K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_WIDEN_CODES, K_DEQUANT_WEIGHT, K_COUNT
 };
 
 // Box sizes of the tensor maps (each CTA of a pair stages 128 rows of each

@@ -78,8 +78,14 @@ def forward_workspace(M: int, K: int, N: int, max_outliers: int, device) -> torc
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
-def backward_workspace(M: int, N: int, dtype: torch.dtype, device) -> torch.Tensor:
-    n = _lib.i8lt_backward_workspace_size(M, N, _code(dtype))
+def backward_workspace(M: int, N: int, dtype: torch.dtype, device, K: int | None = None) -> torch.Tensor:
+    """Workspace of i8lt_backward_input.  With ``K`` it has room for the
+    materialized dequantized weight (K_pad x N_pad fp16), which selects the
+    faster schedule; without, the fused schedule (no N x K buffer)."""
+    if K is None:
+        n = _lib.i8lt_backward_workspace_size(M, N, _code(dtype))
+    else:
+        n = _lib.i8lt_backward_workspace_size_dq(M, N, K, _code(dtype))
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
@@ -114,15 +120,18 @@ def forward(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, bias: 
 
 def backward_input(G: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, need_grad_A: bool = True,
                    bias_dtype: torch.dtype | None = None, addend: torch.Tensor | None = None,
-                   ws: torch.Tensor | None = None):
-    """(grad_A [M, K] or None, grad_bias [N] or None) from grad_output G [M, N]."""
+                   ws: torch.Tensor | None = None, fused: bool = False):
+    """(grad_A [M, K] or None, grad_bias [N] or None) from grad_output G [M, N].
+    ``fused``: rebuild the dequantized weight tile by tile inside the GEMM
+    instead of materializing it in the workspace (less memory, slower).  A
+    caller-supplied ``ws`` decides by its size instead."""
     _require_cuda(G, CB, SCB, addend)
     G = G.contiguous()
     M, N = G.shape
     grad_A = torch.empty(M, K, dtype=G.dtype, device=G.device) if need_grad_A else None
     grad_bias = torch.empty(N, dtype=bias_dtype, device=G.device) if bias_dtype is not None else None
     if ws is None:
-        ws = backward_workspace(M, N, G.dtype, G.device)
+        ws = backward_workspace(M, N, G.dtype, G.device, K=None if (fused or not need_grad_A) else K)
     if addend is not None:
         addend = addend.contiguous()
     _check(_lib.i8lt_backward_input(G.data_ptr(), _code(G.dtype), M, N, CB.data_ptr(), SCB.data_ptr(), K,

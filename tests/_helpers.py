@@ -102,6 +102,26 @@ def check_forward_stages(g, ref, rows=None, K=None):
     return assert_tol(out, ref["out64"], "out")
 
 
+def check_wdq(ws, M, N, K, dtype, CB_ref, SCB_ref, max_rows=4096):
+    """The materialized schedule's dequantized weight, read back from the
+    backward workspace (it follows the first i8lt_backward_workspace_size
+    bytes): WdqT [K_pad, N_pad] fp16 must equal the oracle's Wdq transposed,
+    bit for bit, with zero padding.  At most ``max_rows`` rows k are checked
+    (evenly spaced, first and last included)."""
+    from int8_quantized_linear_i8lt_gb300.functional import DTYPE_CODE
+    off = _lib.i8lt_backward_workspace_size(M, N, DTYPE_CODE[dtype])
+    kp, npad = (K + 15) // 16 * 16, (N + 7) // 8 * 8
+    assert ws.numel() >= off + kp * npad * 2
+    wdqT = ws[off:off + kp * npad * 2].view(torch.float16).reshape(kp, npad)
+    ks = np.unique(np.linspace(0, kp - 1, min(kp, max_rows)).round().astype(np.int64))
+    got = wdqT[torch.as_tensor(ks, device=ws.device)].cpu().numpy()
+    ref = O.dequant_weight(CB_ref, SCB_ref)          # [N, K] fp16
+    inside = ks < K
+    assert np.array_equal(got[inside, :N].view(np.uint16), ref[:, ks[inside]].T.view(np.uint16)), "WdqT differs"
+    assert not np.any(got[~inside].astype(np.float32)), "WdqT padding rows not zero"
+    assert not np.any(got[:, N:].astype(np.float32)), "WdqT padding columns not zero"
+
+
 def check_weight(CB_gpu, SCB_gpu, W, K):
     CB_ref, SCB_ref = O.quantize_weight(to_np(W), ODT[W.dtype])
     cb = to_np(CB_gpu)

@@ -112,6 +112,19 @@ def test_backward_argument_errors(L):
     assert _lib.i8lt_backward_workspace_size(64, 64, 1) >= need + 64 * 64 * 2
 
 
+def test_backward_workspace_of_the_materialized_schedule(L):
+    # the transient dequantized weight (K_pad x N_pad fp16) follows the fused
+    # schedule's workspace
+    for M, N, K, gt in [(64, 64, 64, 0), (300, 520, 1100, 1), (7, 13, 5, 2), (0, 8, 8, 0)]:
+        lean = _lib.i8lt_backward_workspace_size(M, N, gt)
+        dq = _lib.i8lt_backward_workspace_size_dq(M, N, K, gt)
+        kp, npad = (K + 15) // 16 * 16, (N + 7) // 8 * 8
+        assert dq >= lean + kp * npad * 2
+        assert dq - lean < kp * npad * 2 + 256
+    assert _lib.i8lt_backward_workspace_size_dq(64, 64, _lib.I8LT_MAX_K + 1, 0) == 0
+    assert _lib.i8lt_backward_workspace_size_dq(64, 64, 64, 9) == 0
+
+
 def test_other_entry_points_argument_errors(L):
     assert _lib.i8lt_quantize_weight(FAKE, 7, 4, 4, FAKE, FAKE, None) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
     assert _lib.i8lt_quantize_weight(FAKE, 0, 4, 0, FAKE, FAKE, None) == _lib.I8LT_ERR_INVALID_ARG

@@ -20,7 +20,7 @@ import int8_quantized_linear_i8lt_gb300 as I
 from int8_quantized_linear_i8lt_gb300 import _lib
 from int8_quantized_linear_i8lt_gb300.build import build
 
-from _helpers import ODT, assert_tol, check_forward_stages, check_weight, gpu_forward, to_np, widen
+from _helpers import ODT, assert_tol, check_forward_stages, check_wdq, check_weight, gpu_forward, to_np, widen
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -55,8 +55,18 @@ def run_layer_case(spec, seed=0, rows=None, w_dtype=None, max_outliers=None):
         subB = to_np(g["subB"])[:, :len(ref["idx"])]
         subB_ref = O.dequant_weight(CB_ref, SCB_ref)[:, ref["idx"]]
         assert np.array_equal(subB.view(np.uint16), subB_ref.view(np.uint16))
-    # backward to the input and the bias
-    gA, gb = I.backward_input(G.to(DEV), CB, SCB, K, bias_dtype=b.dtype)
+    # backward to the input and the bias: the materialized schedule (its
+    # dequantized weight checked bit for bit), then the fused one, which must
+    # give the same bits
+    Gd = G.to(DEV)
+    ws_dq = I.functional.backward_workspace(spec.M, spec.N, G.dtype, DEV, K=K)
+    gA, gb = I.backward_input(Gd, CB, SCB, K, bias_dtype=b.dtype, ws=ws_dq)
+    if spec.M > 0:
+        check_wdq(ws_dq, spec.M, spec.N, K, G.dtype, CB_ref, SCB_ref)
+    del ws_dq
+    gA_fused, _ = I.backward_input(Gd, CB, SCB, K, fused=True)
+    assert torch.equal(gA_fused.view(torch.uint8), gA.view(torch.uint8)), "fused and materialized grad_A differ"
+    del gA_fused, Gd
     rb = O.backward_input(to_np(G), ODT[G.dtype], CB_ref, SCB_ref, rows=rows)
     gA_sel = gA if rows is None else gA[torch.as_tensor(rows, device=DEV)]
     assert_tol(widen(gA_sel), rb["grad64"], "grad_A")
