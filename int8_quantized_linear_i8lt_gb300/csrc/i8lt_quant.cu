@@ -125,6 +125,105 @@ __global__ void __launch_bounds__(kThreads) row_quantize_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// K3 for rows that fit in shared memory (K_pad <= kStagedMaxLd): the same
+// quantization as row_quantize_kernel<T, __half>, with the fp16-cast row
+// staged in shared memory so that A is read from HBM once.  The codes are
+// rounded with an IEEE fp32 add of 1.5 * 2^23 (round to nearest even, exact
+// for |x * s| < 2^22; here |x * s| <= 127 + 2^-16), the same rounding as
+// __float2int_rn, and stored two at a time with one fp32x2 -> fp16x2
+// conversion (exact: integers of magnitude <= 127).  The per-1024-column
+// absolute code sums that decide rowsmall are reduced once per row.
+// ---------------------------------------------------------------------------
+constexpr int kStagedMaxLd = 49152;   // 96 KB of fp16 per row
+constexpr int kStagedMaxChunks = kStagedMaxLd / 1024;
+
+__device__ __forceinline__ float rint_small(float y) {
+  return __fsub_rn(__fadd_rn(y, 12582912.0f), 12582912.0f);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) act_quantize_staged_kernel(
+    const T* __restrict__ A, int64_t M, int64_t K, int64_t ld, int vec, const uint32_t* __restrict__ mask,
+    const int* __restrict__ idx, const DevStatus* __restrict__ st, int64_t cap_pad, float* __restrict__ scale,
+    __half* __restrict__ codes, __half* __restrict__ sub, uint8_t* __restrict__ rowsmall) {
+  extern __shared__ uint4 srow4[];   // ld fp16 values of the current row
+  __shared__ float red[32];
+  __shared__ int chunk_l1[kStagedMaxChunks];
+  const __half* srow = reinterpret_cast<const __half*>(srow4);
+  const int used = (mask != nullptr) ? st->used : 0;
+  const int used_pad = (used + 63) / 64 * 64;
+  const int nchunks = static_cast<int>((ld + 1023) / 1024);
+  for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+    const T* row = A + m * K;
+    float amax = 0.f;
+    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < ld; c += kThreads * 8) {
+      __half h[8];
+      if (c < K) {
+        load8_half(row + c, K - c, vec != 0 && c + 8 <= K, h);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = __float2half_rn(0.f);
+      }
+      srow4[c >> 3] = *reinterpret_cast<const uint4*>(h);
+      const uint32_t bits = (mask != nullptr && c < K) ? ((mask[c >> 5] >> (c & 31)) & 0xFFu) : 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (!((bits >> i) & 1u)) amax = fmaxf(amax, fabsf(__half2float(h[i])));
+    }
+    if (rowsmall != nullptr)
+      for (int i = threadIdx.x; i < nchunks; i += kThreads) chunk_l1[i] = 0;
+    amax = block_max(amax, red);   // its barriers also publish the staged row and the cleared sums
+    const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
+    __half* out = codes + m * ld;
+    // every thread runs every iteration (the shuffles below need all 32 lanes)
+    for (int64_t c0 = 0; c0 < ld; c0 += kThreads * 8) {
+      const int64_t c = c0 + static_cast<int64_t>(threadIdx.x) * 8;
+      float l1 = 0.f;
+      if (c < ld) {
+        const uint4 u = srow4[c >> 3];
+        const __half* h = reinterpret_cast<const __half*>(&u);
+        const uint32_t bits = (mask != nullptr && c < K) ? ((mask[c >> 5] >> (c & 31)) & 0xFFu) : 0u;
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float r = rint_small(__fmul_rn(__half2float(h[i]), s));
+          q[i] = ((bits >> i) & 1u) ? 0.f : fminf(127.f, fmaxf(-127.f, r));
+          l1 += fabsf(q[i]);
+        }
+        uint4 o;
+        __half2* o2 = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o2[i] = __floats2half2_rn(q[2 * i], q[2 * i + 1]);
+        *reinterpret_cast<uint4*>(out + c) = o;
+      }
+      if (rowsmall != nullptr) {
+        // a warp's 256 columns lie in one 1024-column chunk; a warp past the
+        // end of the row sums to 0 and adds nothing
+        int v = static_cast<int>(l1);
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1) v += __shfl_xor_sync(0xffffffffu, v, k);
+        const int64_t cw = c0 + static_cast<int64_t>(threadIdx.x & ~31) * 8;
+        if ((threadIdx.x & 31) == 0 && v != 0) atomicAdd(&chunk_l1[cw >> 10], v);
+      }
+    }
+    if (sub != nullptr) {
+      for (int j = threadIdx.x; j < used_pad; j += kThreads)
+        sub[m * cap_pad + j] = (j < used) ? srow[idx[j]] : __float2half_rn(0.f);
+    }
+    bool small = true;
+    if (rowsmall != nullptr) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < nchunks; i += kThreads) small = small && chunk_l1[i] <= kSmallChunkL1;
+    }
+    small = __syncthreads_and(small) != 0;   // also: the staged row is no longer read
+    if (threadIdx.x == 0) {
+      if (rowsmall != nullptr) rowsmall[m] = small ? 1 : 0;
+      scale[m] = amax;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // K2: per-column max of |fp16(A)|.  Block = 32 column groups of 8 x 8 row
 // lanes; each block covers 256 columns x kColRows rows, then one atomicMax
 // per column.  fp16 magnitudes compare as unsigned integers.
@@ -403,6 +502,31 @@ cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int
   if (M == 0) return cudaSuccess;
   return dispatch_dt(at, [&](auto* tag) {
     using T = std::remove_pointer_t<decltype(tag)>;
+    if (K_pad <= kStagedMaxLd) {
+      const int smem = static_cast<int>(K_pad * 2);
+      static bool attr[3] = {false, false, false};
+      bool& done = attr[std::is_same_v<T, __half> ? 0 : (std::is_same_v<T, __nv_bfloat16> ? 1 : 2)];
+      if (!done) {
+        if (cudaFuncSetAttribute(act_quantize_staged_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kStagedMaxLd * 2) != cudaSuccess)
+          return cudaGetLastError();
+        done = true;
+      }
+      int dev = 0, sms = 152, per_sm = 1;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, act_quantize_staged_kernel<T>, kThreads, smem) !=
+              cudaSuccess ||
+          per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
+      }
+      const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(sms) * per_sm));
+      ProfScope ps(K_ROW_QUANTIZE, s);
+      act_quantize_staged_kernel<T><<<grid, kThreads, smem, s>>>(static_cast<const T*>(A), M, K, K_pad, vec ? 1 : 0,
+                                                                  mask, idx, st, cap_pad, SCA, Aq, subA, rowsmall);
+      return cudaGetLastError();
+    }
     ProfScope ps(K_ROW_QUANTIZE, s);
     row_quantize_kernel<T, __half><<<grid_rows(M), kThreads, 0, s>>>(
         static_cast<const T*>(A), M, K, K_pad, vec ? 1 : 0, mask, idx, st, cap_pad, SCA, Aq, subA, rowsmall);
