@@ -170,8 +170,10 @@ class Layer:
         self.cap = cap
         self.out = torch.empty(spec.M, spec.N, dtype=spec.dtype, device=device)
         self.ws_f = I.functional.forward_workspace(spec.M, spec.K, spec.N, cap, device)
-        # room for the materialized dequantized weight: the faster backward schedule
-        self.ws_b = I.functional.backward_workspace(spec.M, spec.N, spec.dtype, device, K=spec.K)
+        # fused backward schedule (the fp16 weight rebuilt inside the GEMM, never
+        # stored); the larger workspace selects the materialized schedule
+        self.ws_b = I.functional.backward_workspace(spec.M, spec.N, spec.dtype, device)
+        self.ws_b_dq = I.functional.backward_workspace(spec.M, spec.N, spec.dtype, device, K=spec.K)
         self.grad_A = torch.empty(spec.M, spec.K, dtype=spec.dtype, device=device)
         self.grad_bias = torch.empty(spec.N, dtype=wdt, device=device)
 
@@ -180,9 +182,9 @@ class Layer:
         return 4.0 * s.M * s.N * s.K        # 2MNK forward + 2MNK backward-to-input
 
 
-def _launch_layer(L, stream_ptr, ev=None):
+def _launch_layer(L, stream_ptr, materialized=False):
     """One layer through the C ABI: forward, then backward to the input and
-    the bias.  ``ev``: optional dict of CUDA event pairs around the GEMMs."""
+    the bias (fused backward schedule unless ``materialized``)."""
     from int8_quantized_linear_i8lt_gb300 import _lib
     from int8_quantized_linear_i8lt_gb300.functional import DTYPE_CODE
     s = L.spec
@@ -192,9 +194,10 @@ def _launch_layer(L, stream_ptr, ev=None):
                            L.bias.data_ptr(), bt, s.threshold, None, L.out.data_ptr(), L.ws_f.data_ptr(),
                            L.ws_f.numel(), L.cap, stream=stream_ptr)
     assert st == 0, _lib.i8lt_status_string(st)
+    wsb = L.ws_b_dq if materialized else L.ws_b
     st = _lib.i8lt_backward_input(L.G.data_ptr(), dt, s.M, s.N, L.CB.data_ptr(), L.SCB.data_ptr(), s.K, None,
-                                  L.grad_A.data_ptr(), L.grad_bias.data_ptr(), bt, L.ws_b.data_ptr(),
-                                  L.ws_b.numel(), stream_ptr)
+                                  L.grad_A.data_ptr(), L.grad_bias.data_ptr(), bt, wsb.data_ptr(),
+                                  wsb.numel(), stream_ptr)
     assert st == 0, _lib.i8lt_status_string(st)
 
 
@@ -306,6 +309,8 @@ def run_ours(args):
         kernels[k] = e
     # --- end to end through host buffers (pinned), inputs and results copied each step
     e2e = run_e2e(layers, stream, max(2, min(args.steps, 10)), device)
+    # --- the same step with the materialized backward schedule (context, not the headline)
+    alt = time_materialized(layers, stream, max(2, min(args.steps, 10)), device)
 
     clocks = clk.summary()
     line = {
@@ -320,6 +325,7 @@ def run_ours(args):
         "roofline": roof,
         "kernels": kernels,
         "e2e": e2e,
+        "bwd_materialized": alt,
         "gpu_launches": n_launches,
         "gemm_launch": {k: dict(zip(("status", "ctas", "threads", "smem"), _lib.i8lt_gemm_launch_info(k)))
                         for k in ("fwd_gemm", "bwd_gemm")},
@@ -348,10 +354,38 @@ def _layer_of(i, layers):
 def launches_per_layer(L) -> int:
     """Our kernels per layer and step: colmax, outlier index, row quantize,
     subB (outliers on), weight-code widening, forward GEMM; grad_output
-    prepass, grad_bias finalize, weight dequantization, backward GEMM."""
+    prepass, grad_bias finalize, backward GEMM (fused schedule)."""
     import math
     fwd = 6 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 3
-    return fwd + 4
+    return fwd + 3
+
+
+def time_materialized(layers, stream, steps, device):
+    """The step with the materialized backward schedule: a prepass writes the
+    dequantized weight (K x N fp16) to the workspace, then a TMA-fed fp16 GEMM
+    reads it.  Same results as the fused schedule; reported as context."""
+    from int8_quantized_linear_i8lt_gb300 import _lib
+    sp = stream.cuda_stream
+    for L in layers:
+        _launch_layer(L, sp, materialized=True)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _lib.i8lt_profile_start(1 << 16)
+    ev0.record(stream)
+    for _ in range(steps):
+        for L in layers:
+            _launch_layer(L, sp, materialized=True)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    pst, recs, _ = _lib.i8lt_profile_stop(1 << 16)
+    ms = reduce_max(ev0.elapsed_time(ev1), device)
+    ops = reduce_sum(sum(L.ops() for L in layers) * steps, device)
+    bwd_ms = sum(t for n, t in recs if n == "bwd_gemm")
+    dq_ms = sum(t for n, t in recs if n == "dequant_weight")
+    bwd_flops = sum(2.0 * L.spec.M * L.spec.N * L.spec.K for L in layers) * steps
+    return {"value": round(ops / (ms * 1e-3) / 1e12, 2), "unit": "TOPS", "ms_per_step": round(ms / steps, 3),
+            "steps": steps, "bwd_gemm_tflops": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 1) if bwd_ms else None,
+            "dequant_weight_ms_per_step": round(dq_ms / steps, 4)}
 
 
 def run_e2e(layers, stream, steps, device):

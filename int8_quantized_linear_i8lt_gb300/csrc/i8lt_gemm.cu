@@ -58,10 +58,9 @@ namespace i8lt {
 namespace {
 
 constexpr int kThreads = 512;      // forward
-constexpr int kBwdThreads = 576;   // backward: two more warps (int8 producer, fourth relay)
+constexpr int kBwdThreads = 704;   // backward: 22 warps
 constexpr int kFwdStages = 6;      // 32 KB stages: fp16 A and B tiles
-constexpr int kBwdStages = 6;      // 32 KB stages: converted weight tile (A) and G16 tile (B)
-constexpr int kI8Stages = 3;       // 8 KB stages: int8 weight tiles on their way to the converters
+constexpr int kI8Stages = 4;       // backward, fused: 8 KB int8 weight tiles on their way to the converters
 constexpr int kI8PrefetchAhead = 8;   // int8 weight tiles are fetched into L2 this many stages early
 constexpr int kMaxStages = 6;
 constexpr int kChunkKB = 16;   // K-blocks of 64 per exact fp32 chunk: 1024 products
@@ -70,7 +69,8 @@ constexpr int kWarpProducer = 0;
 constexpr int kWarpMMA = 1;
 constexpr int kWarpCvt0 = 2;   // backward: 2..9
 constexpr int kWarpEpi0 = 6;   // forward: 6..13
-constexpr int kBwdWarpEpi0 = 10; // backward: 10..13
+constexpr int kBwdWarpEpi0 = 10; // backward: 10..13 and 18..21
+constexpr int kBwdWarpEpi1 = 18;
 constexpr int kWarpRelay0 = 14; // backward, odd CTA: 14, 15, 17 and warp 1
 constexpr int kWarpI8Producer = 16;   // backward: TMA of the int8 weight tiles
 constexpr int kWarpRelayLast = 17;
@@ -81,7 +81,7 @@ constexpr int kRelays = 4;
 constexpr unsigned kEpiSleepNs = 256;
 constexpr int kCvtWarps = 8;       // backward: every converter warp works on every stage
 constexpr int kEpiWarps = 8;      // forward
-constexpr int kBwdEpiWarps = 4;   // backward
+constexpr int kBwdEpiWarps = 8;   // backward: two per TMEM lane quadrant, each half of the columns
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kBarEpi = 2;     // named barrier id
 
@@ -107,20 +107,40 @@ struct __align__(8) Barriers {
   int abort_flag;
 };
 
-// stage s of each CTA: [A operand 16 KB][B operand 16 KB] fp16, 128B-swizzled.
-// The backward keeps a separate ring of 8 KB int8 weight tiles after its
-// operand stages: a weight tile is loaded while the operand stage it will be
-// converted into is still being read by the tensor cores, so the copy latency
-// and the conversion and hand-over latency overlap instead of adding up.
+// stage s of each CTA: [A operand 16 KB][B operand(s) 16 KB each] fp16,
+// 128B-swizzled.
 constexpr int kOpBytes = kCtaRows * kBK * 2;   // 16 KB
 constexpr int kI8Bytes = kCtaRows * kBK;       // 8 KB
 constexpr int kFwdStageBytes = 2 * kOpBytes;
-constexpr int kBwdStageBytes = 2 * kOpBytes;
-constexpr int kBwdI8Offset = kBwdStages * kBwdStageBytes;
-constexpr int kBwdSmemTiles = kBwdI8Offset + kI8Stages * kI8Bytes;
-constexpr int kSmemTiles = kFwdStages * kFwdStageBytes > kBwdSmemTiles ? kFwdStages * kFwdStageBytes : kBwdSmemTiles;
-constexpr int kSmemBytes = 1024 /*align slack*/ + kSmemTiles + 2 * kPairN * 4 /*epilogue vectors*/ +
-                           static_cast<int>(sizeof(Barriers));
+constexpr int kFwdSmemBytes = 1024 /*align slack*/ + kFwdStages * kFwdStageBytes + 2 * kPairN * 4 /*epilogue vectors*/ +
+                              static_cast<int>(sizeof(Barriers));
+
+// Backward geometry.  Materialized schedule: 256 (k) x 256 (tokens) pair
+// tiles, 6 stages of [WdqT 16 KB][G16 16 KB], two 256-column accumulators so
+// that the epilogue of one tile overlaps the next tile's main loop.  Fused
+// schedule: 256 (k) x 512 (tokens) pair tiles -- every converted weight tile
+// feeds two N = 256 MMAs, which halves the conversion and hand-over work per
+// flop -- with 4 stages of [Wdq^T 16 KB][G16 2 x 16 KB], the 512 TMEM
+// columns as one accumulator, and a separate ring of 4 int8 weight tiles
+// after the operand stages: a weight tile is loaded while the operand stage
+// it will be converted into is still being read by the tensor cores, so the
+// copy latency and the conversion and hand-over latency overlap instead of
+// adding up.
+template <bool kFused>
+struct BwdGeom {
+  static constexpr int kSub = kFused ? 2 : 1;                  // N = 256 MMAs per k step
+  static constexpr int kTileTokens = kSub * kPairN;            // tokens per pair tile
+  static constexpr int kStages = kFused ? 4 : 6;
+  static constexpr int kStageBytes = (1 + kSub) * kOpBytes;
+  static constexpr int kI8Offset = kStages * kStageBytes;
+  static constexpr int kTiles = kI8Offset + (kFused ? kI8Stages * kI8Bytes : 0);
+  static constexpr int kAccBufs = kFused ? 1 : 2;
+  static constexpr int kSmemBytes = 1024 /*align slack*/ + kTiles + static_cast<int>(sizeof(Barriers));
+};
+static_assert(BwdGeom<true>::kSmemBytes <= 232448 && BwdGeom<false>::kSmemBytes <= 232448 &&
+                  kFwdSmemBytes <= 232448,
+              "shared memory per CTA");
+static_assert(BwdGeom<true>::kStages <= kMaxStages && BwdGeom<false>::kStages <= kMaxStages, "barrier arrays");
 
 __device__ __forceinline__ uint32_t f2i_rn(uint32_t fbits) {
   return static_cast<uint32_t>(__float2int_rn(__uint_as_float(fbits)));
@@ -285,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fwd_gemm_kernel(const __grid_constant__ FwdGemmArgs g, const FwdEpiArgs e, int num_m, int num_n, int group) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* scb_s = reinterpret_cast<float*>(smem + kSmemTiles);
+  float* scb_s = reinterpret_cast<float*>(smem + kFwdStages * kFwdStageBytes);
   float* bias_s = scb_s + kPairN;
   Barriers* bars = reinterpret_cast<Barriers*>(bias_s + kPairN);
   volatile int* abort_flag = &bars->abort_flag;
@@ -506,15 +526,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // ready[s] with a cluster-scope release, so that the converted tiles (written
 // by this CTA's threads) are visible to the even CTA's MMA.  Relay r takes
 // the stages it % kRelays == r.
-__device__ __noinline__ void relay_loop(Barriers* bars, int cid, int ncl, int num_tiles, int NB, int r,
+__device__ __noinline__ void relay_loop(Barriers* bars, int cid, int ncl, int num_tiles, int NB, int r, int stages,
                                         volatile int* abort_flag, DevStatus* st) {
   const uint32_t ready0 = mapa_shared(&bars->ready[0], 0);
   int it = 0;
   for (int t = cid; t < num_tiles; t += ncl) {
     for (int b = 0; b < NB; ++b, ++it) {
       if (it % kRelays != r) continue;
-      const int s = it % kBwdStages;
-      if (!mbar_wait(&bars->cvt_done[s], (it / kBwdStages) & 1, abort_flag, st, kWhereCvt)) return;
+      const int s = it % stages;
+      if (!mbar_wait(&bars->cvt_done[s], (it / stages) & 1, abort_flag, st, kWhereCvt)) return;
       mbar_arrive_remote_release_cluster(ready0 + static_cast<uint32_t>(s) * 8u);
     }
   }
@@ -545,11 +565,12 @@ __device__ __forceinline__ void bwd_store16(const BwdEpiArgs& e, int64_t kk, int
 template <bool kFused>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     bwd_gemm_kernel(const __grid_constant__ BwdGemmArgs g, const BwdEpiArgs e, int num_k, int num_m, int group) {
+  using Geo = BwdGeom<kFused>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + kSmemTiles + 2 * kPairN * 4);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + Geo::kTiles);
   volatile int* abort_flag = &bars->abort_flag;
-  uint8_t* i8_ring = smem + kBwdI8Offset;
+  uint8_t* i8_ring = smem + Geo::kI8Offset;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -570,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;   // two 256-column accumulators
+  const uint32_t tmem = bars->tmem_base;   // 512 columns: two 256-column accumulators, or one 512-column one
 
   if (warp == kWarpProducer) {
     // ---- G16 tiles (and WdqT tiles when materialized): both CTAs' copies
@@ -582,22 +603,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       for (int t = cid; t < num_tiles && ok; t += ncl) {
         int tm, tk;
         tile_coords(t, num_m, num_k, group, tm, tk);
-        const int m_cta = tm * kPairN + static_cast<int>(rank) * kCtaRows;
+        const int m_cta = tm * Geo::kTileTokens + static_cast<int>(rank) * kCtaRows;
         const int k_cta = tk * kPairM + static_cast<int>(rank) * kCtaRows;
         for (int b = 0; b < NB; ++b, ++it) {
-          const int s = it % kBwdStages;
-          const uint32_t ph = (it / kBwdStages) & 1;
+          const int s = it % Geo::kStages;
+          const uint32_t ph = (it / Geo::kStages) & 1;
           if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
-          if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], (kFused ? 2 : 4) * kOpBytes);
+          // the even CTA expects both CTAs' bytes of this stage
+          if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], 2 * (kFused ? Geo::kSub : 2) * kOpBytes);
           const uint32_t full_s = full0 + static_cast<uint32_t>(s) * 8u;
-          if (!kFused)
-            tma_load_2d_pair(smem + s * kBwdStageBytes, &g.tmWT, b * kBK, k_cta, full_s);   // WdqT[k:+128][n:+64]
-          tma_load_2d_pair(smem + s * kBwdStageBytes + kOpBytes, &g.tmG, b * kBK, m_cta, full_s);   // G16[m:+128][n:+64]
+          uint8_t* st_base = smem + s * Geo::kStageBytes;
+          if (!kFused) tma_load_2d_pair(st_base, &g.tmWT, b * kBK, k_cta, full_s);   // WdqT[k:+128][n:+64]
+#pragma unroll
+          for (int u = 0; u < Geo::kSub; ++u)   // G16[m:+128][n:+64] of token sub-tile u
+            tma_load_2d_pair(st_base + (1 + u) * kOpBytes, &g.tmG, b * kBK, m_cta + u * kPairN, full_s);
         }
       }
       if (rank == 0)
-        for (int j = max(0, it - kBwdStages); j < it; ++j)
-          mbar_wait_teardown(&bars->full[j % kBwdStages], (j / kBwdStages) & 1, e.st);
+        for (int j = max(0, it - Geo::kStages); j < it; ++j)
+          mbar_wait_teardown(&bars->full[j % Geo::kStages], (j / Geo::kStages) & 1, e.st);
     }
   } else if (warp == kWarpI8Producer) {
     // ---- int8 weight tiles CB[n:+64][k:+128], this CTA's own ring
@@ -639,8 +663,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       int it = 0, tl = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl, ++tl) {
-        const int buf = tl & 1;
-        const int use = tl >> 1;
+        const int buf = tl % Geo::kAccBufs;
+        const int use = tl / Geo::kAccBufs;
         if (use > 0 && !mbar_wait_cluster(&bars->acc_empty[buf], (use - 1) & 1, abort_flag, e.st, kWhereMMA)) {
           ok = false;
           break;
@@ -648,22 +672,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(buf) * 256u;
         for (int b = 0; b < NB; ++b, ++it) {
-          const int s = it % kBwdStages;
-          const uint32_t ph = (it / kBwdStages) & 1;
+          const int s = it % Geo::kStages;
+          const uint32_t ph = (it / Geo::kStages) & 1;
           if (!mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereMMA) ||
               (kFused && !mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + s * kBwdStageBytes);
-          const uint32_t b_base = a_base + kOpBytes;
+          const uint32_t a_base = smem_u32(smem + s * Geo::kStageBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t ad = kFused ? make_sdesc(a_base + k * 4096, 1024, 2048, kSwizzle128B)
                                        : make_sdesc(a_base + k * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bd = make_sdesc(b_base + k * 32, 16, 1024, kSwizzle128B);
-            umma_f16_pair(d, ad, bd, idesc, (b > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+            for (int u = 0; u < Geo::kSub; ++u) {   // token sub-tile u -> accumulator columns [256 u, 256 u + 256)
+              const uint64_t bd = make_sdesc(a_base + (1 + u) * kOpBytes + k * 32, 16, 1024, kSwizzle128B);
+              umma_f16_pair(d + static_cast<uint32_t>(u) * 256u, ad, bd, idesc, (b > 0 || k > 0) ? 1u : 0u);
+            }
           }
           umma_commit_pair_mc(&bars->empty[s], 0x3);
         }
@@ -672,12 +698,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       umma_commit_pair(&bars->teardown);
       mbar_wait_teardown(&bars->teardown, 0, e.st);
     } else if (kFused && rank == 1 && lane == 0) {
-      relay_loop(bars, cid, ncl, num_tiles, NB, 0, abort_flag, e.st);
+      relay_loop(bars, cid, ncl, num_tiles, NB, 0, Geo::kStages, abort_flag, e.st);
     }
-  } else if (warp >= kWarpRelay0) {
+  } else if (warp == kWarpRelay0 || warp == kWarpRelay0 + 1 || warp == kWarpRelayLast) {
     if (kFused && rank == 1 && lane == 0)
-      relay_loop(bars, cid, ncl, num_tiles, NB, warp == kWarpRelayLast ? 3 : 1 + (warp - kWarpRelay0), abort_flag,
-                 e.st);
+      relay_loop(bars, cid, ncl, num_tiles, NB, warp == kWarpRelayLast ? 3 : 1 + (warp - kWarpRelay0), Geo::kStages,
+                 abort_flag, e.st);
   } else if (warp < kBwdWarpEpi0) {
     if constexpr (kFused) {
       // ---- converters: CB int8 [64 n][128 k] (128B-swizzled rows) -> Wdq^T
@@ -708,8 +734,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
         for (int b = 0; b < NB; ++b, ++it) {
           const float scb_cur[2] = {scb_next[0], scb_next[1]};
           load_scb(b + 1 < NB ? b + 1 : 0, scb_next);
-          const int s = it % kBwdStages;
-          const uint32_t ph = (it / kBwdStages) & 1;
+          const int s = it % Geo::kStages;
+          const uint32_t ph = (it / Geo::kStages) & 1;
           const int j8 = it % kI8Stages;
           if (!__all_sync(0xffffffffu,
                           mbar_wait(&bars->i8_full[j8], (it / kI8Stages) & 1, abort_flag, e.st, kWhereCvt))) {
@@ -725,7 +751,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
             go = false;
             break;
           }
-          uint8_t* sa = smem + s * kBwdStageBytes;
+          uint8_t* sa = smem + s * Geo::kStageBytes;
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const uint64_t f2 = f32x2_splat(__fmul_rn(scb_cur[j], 1.0f / 127.0f));
@@ -753,34 +779,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else {
-    // ---- epilogue: lanes = this CTA's 128 output features k, columns = 256 tokens
+    // ---- epilogue: lanes = this CTA's 128 output features k, columns = the
+    // tile's tokens (column c of the accumulator is token tm * kTileTokens + c).
+    // Warps 10-13 take the first half of the columns, warps 18-21 the second.
     const int quad = warp & 3;
-    const int col0 = 0;   // four warps: each takes all 256 columns of its lanes
+    constexpr int kHalf = Geo::kTileTokens / 2;
+    const int col0 = warp >= kBwdWarpEpi1 ? kHalf : 0;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t acc_empty_pair[2] = {mapa_shared(&bars->acc_empty[0], 0), mapa_shared(&bars->acc_empty[1], 0)};
     int tl = 0;
     for (int t = cid; t < num_tiles; t += ncl, ++tl) {
       int tm, tk;
       tile_coords(t, num_m, num_k, group, tm, tk);
-      const int buf = tl & 1;
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(&bars->acc_full[buf], (tl >> 1) & 1, abort_flag, e.st, kWhereEpi, kEpiSleepNs)))
+      const int buf = tl % Geo::kAccBufs;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full[buf], (tl / Geo::kAccBufs) & 1, abort_flag, e.st,
+                                             kWhereEpi, kEpiSleepNs)))
         break;
       tc_fence_after();
       const int64_t kk = static_cast<int64_t>(tk) * kPairM + static_cast<int64_t>(rank) * kCtaRows + quad * 32 + lane;
-      const uint32_t d = tmem + static_cast<uint32_t>(buf) * 256u + lane_off;
-#pragma unroll 1
-      for (int gc = 0; gc < 256; gc += 16) {
-        uint32_t x[16];
-        tmem_ld16(d + col0 + gc, x);
+      const uint32_t d = tmem + static_cast<uint32_t>(buf) * 256u + lane_off + static_cast<uint32_t>(col0);
+      const int m0 = tm * Geo::kTileTokens + col0;
+      auto store = [&](const uint32_t(&x)[16], int gc) {
         if (kk < e.K) {
-          const int mb = tm * kPairN + col0 + gc;
           switch (e.dt) {
-            case DT_F16: bwd_store16<__half>(e, kk, mb, x); break;
-            case DT_BF16: bwd_store16<__nv_bfloat16>(e, kk, mb, x); break;
-            default: bwd_store16<float>(e, kk, mb, x); break;
+            case DT_F16: bwd_store16<__half>(e, kk, m0 + gc, x); break;
+            case DT_BF16: bwd_store16<__nv_bfloat16>(e, kk, m0 + gc, x); break;
+            default: bwd_store16<float>(e, kk, m0 + gc, x); break;
           }
         }
+      };
+      // two register buffers: the stores of one overlap the TMEM load of the other
+      uint32_t xa[16], xb[16];
+      tmem_ld16_nowait(d, xa);
+      tmem_ld_wait_tie16(xa, xb);
+#pragma unroll 1
+      for (int gc = 0; gc < kHalf; gc += 32) {
+        tmem_ld16_nowait(d + gc + 16, xb);
+        store(xa, gc);
+        tmem_ld_wait_tie16(xa, xb);
+        if (gc + 32 < kHalf) tmem_ld16_nowait(d + gc + 32, xa);
+        store(xb, gc + 16);
+        tmem_ld_wait_tie16(xa, xb);
         __syncwarp();
       }
       tc_fence_before();
@@ -816,7 +855,8 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
 }
 
 int g_pairs_fwd[64] = {};   // resident pairs per device, per kernel
-int g_pairs_bwd[64] = {};
+int g_pairs_bwd_fused[64] = {};
+int g_pairs_bwd_dq[64] = {};
 
 // Backward prepass of the materialized schedule: WdqT[k][n] =
 // fp16_rn(fp32(CB[n][k]) * (SCB[n] * fp32(1/127))) -- the page's per-call
@@ -869,7 +909,7 @@ __global__ void __launch_bounds__(256) dequant_weight_kernel(const int8_t* __res
 // Number of CTA pairs that fit on the device at once (each CTA needs most
 // of an SM's shared memory), so that a persistent grid never has a second
 // wave of pairs.
-int resident_pairs(const void* fn, int threads, int (&cached)[64]) {
+int resident_pairs(const void* fn, int threads, int smem_bytes, int* cached /* [64] */) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
@@ -878,7 +918,7 @@ int resident_pairs(const void* fn, int threads, int (&cached)[64]) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
@@ -889,9 +929,9 @@ int resident_pairs(const void* fn, int threads, int (&cached)[64]) {
   return n;
 }
 
-bool set_smem_attr(const void* fn, bool& done) {
+bool set_smem_attr(const void* fn, int smem_bytes, bool& done) {
   if (done) return true;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) return false;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess) return false;
   done = true;
   return true;
 }
@@ -901,15 +941,30 @@ bool set_smem_attr(const void* fn, bool& done) {
 bool g_attr_fwd = false, g_attr_bwd_fused = false, g_attr_bwd_dq = false;
 
 cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_bytes) {
+  // the backward reports the schedule the workspace-sized default picks: fused
   const void* fn = nullptr;
-  if (kernel_id == K_FWD_GEMM) fn = reinterpret_cast<const void*>(fwd_gemm_kernel);
-  else if (kernel_id == K_BWD_GEMM) fn = reinterpret_cast<const void*>(bwd_gemm_kernel<false>);
-  else return cudaErrorInvalidValue;
-  if (!set_smem_attr(fn, kernel_id == K_FWD_GEMM ? g_attr_fwd : g_attr_bwd_dq)) return cudaGetLastError();
-  const int nthreads = kernel_id == K_FWD_GEMM ? kThreads : kBwdThreads;
-  if (ctas != nullptr) *ctas = 2 * resident_pairs(fn, nthreads, kernel_id == K_FWD_GEMM ? g_pairs_fwd : g_pairs_bwd);
+  int nthreads = 0, smem = 0;
+  bool* done = nullptr;
+  int* cache = nullptr;
+  if (kernel_id == K_FWD_GEMM) {
+    fn = reinterpret_cast<const void*>(fwd_gemm_kernel);
+    nthreads = kThreads;
+    smem = kFwdSmemBytes;
+    done = &g_attr_fwd;
+    cache = g_pairs_fwd;
+  } else if (kernel_id == K_BWD_GEMM) {
+    fn = reinterpret_cast<const void*>(bwd_gemm_kernel<true>);
+    nthreads = kBwdThreads;
+    smem = BwdGeom<true>::kSmemBytes;
+    done = &g_attr_bwd_fused;
+    cache = g_pairs_bwd_fused;
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  if (!set_smem_attr(fn, smem, *done)) return cudaGetLastError();
+  if (ctas != nullptr) *ctas = 2 * resident_pairs(fn, nthreads, smem, cache);
   if (threads != nullptr) *threads = nthreads;
-  if (smem_bytes != nullptr) *smem_bytes = kSmemBytes;
+  if (smem_bytes != nullptr) *smem_bytes = smem;
   return cudaSuccess;
 }
 
@@ -929,31 +984,36 @@ cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStrea
   const int num_m = static_cast<int>(ceil_div(e.M, kPairM));
   const int num_n = static_cast<int>(ceil_div(e.N, kPairN));
   if (num_m == 0 || num_n == 0) return cudaSuccess;
-  if (!set_smem_attr(reinterpret_cast<const void*>(fwd_gemm_kernel), g_attr_fwd)) return cudaGetLastError();
+  if (!set_smem_attr(reinterpret_cast<const void*>(fwd_gemm_kernel), kFwdSmemBytes, g_attr_fwd))
+    return cudaGetLastError();
   const int tiles = num_m * num_n;
-  const int clusters = std::min(tiles, resident_pairs(reinterpret_cast<const void*>(fwd_gemm_kernel), kThreads, g_pairs_fwd));
+  const int clusters = std::min(
+      tiles, resident_pairs(reinterpret_cast<const void*>(fwd_gemm_kernel), kThreads, kFwdSmemBytes, g_pairs_fwd));
   const int group = std::min(num_m, 8);
   ProfScope ps(K_FWD_GEMM, s);
-  fwd_gemm_kernel<<<2 * clusters, kThreads, kSmemBytes, s>>>(g, e, num_m, num_n, group);
+  fwd_gemm_kernel<<<2 * clusters, kThreads, kFwdSmemBytes, s>>>(g, e, num_m, num_n, group);
+  return cudaGetLastError();
+}
+
+template <bool kFused>
+cudaError_t launch_bwd_schedule(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaStream_t s) {
+  using Geo = BwdGeom<kFused>;
+  const int num_k = static_cast<int>(ceil_div(e.K, kPairM));
+  const int num_m = static_cast<int>(ceil_div(e.M, Geo::kTileTokens));
+  if (num_k == 0 || num_m == 0) return cudaSuccess;
+  const void* fn = reinterpret_cast<const void*>(bwd_gemm_kernel<kFused>);
+  if (!set_smem_attr(fn, Geo::kSmemBytes, kFused ? g_attr_bwd_fused : g_attr_bwd_dq)) return cudaGetLastError();
+  const int tiles = num_k * num_m;
+  const int clusters =
+      std::min(tiles, resident_pairs(fn, kBwdThreads, Geo::kSmemBytes, kFused ? g_pairs_bwd_fused : g_pairs_bwd_dq));
+  const int group = std::min(num_m, 8);
+  ProfScope ps(K_BWD_GEMM, s);
+  bwd_gemm_kernel<kFused><<<2 * clusters, kBwdThreads, Geo::kSmemBytes, s>>>(g, e, num_k, num_m, group);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool fused, cudaStream_t s) {
-  const int num_k = static_cast<int>(ceil_div(e.K, kPairM));
-  const int num_m = static_cast<int>(ceil_div(e.M, kPairN));
-  if (num_k == 0 || num_m == 0) return cudaSuccess;
-  const void* fn = fused ? reinterpret_cast<const void*>(bwd_gemm_kernel<true>)
-                         : reinterpret_cast<const void*>(bwd_gemm_kernel<false>);
-  if (!set_smem_attr(fn, fused ? g_attr_bwd_fused : g_attr_bwd_dq)) return cudaGetLastError();
-  const int tiles = num_k * num_m;
-  const int clusters = std::min(tiles, resident_pairs(fn, kBwdThreads, g_pairs_bwd));
-  const int group = std::min(num_m, 8);
-  ProfScope ps(K_BWD_GEMM, s);
-  if (fused)
-    bwd_gemm_kernel<true><<<2 * clusters, kBwdThreads, kSmemBytes, s>>>(g, e, num_k, num_m, group);
-  else
-    bwd_gemm_kernel<false><<<2 * clusters, kBwdThreads, kSmemBytes, s>>>(g, e, num_k, num_m, group);
-  return cudaGetLastError();
+  return fused ? launch_bwd_schedule<true>(g, e, s) : launch_bwd_schedule<false>(g, e, s);
 }
 
 cudaError_t launch_dequant_weight(const int8_t* CB, const float* SCB, int64_t N, int64_t k_pad, __half* WdqT,

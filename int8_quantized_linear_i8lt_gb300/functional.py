@@ -79,9 +79,10 @@ def forward_workspace(M: int, K: int, N: int, max_outliers: int, device) -> torc
 
 
 def backward_workspace(M: int, N: int, dtype: torch.dtype, device, K: int | None = None) -> torch.Tensor:
-    """Workspace of i8lt_backward_input.  With ``K`` it has room for the
-    materialized dequantized weight (K_pad x N_pad fp16), which selects the
-    faster schedule; without, the fused schedule (no N x K buffer)."""
+    """Workspace of i8lt_backward_input.  Without ``K``: the fused schedule
+    (the fp16 weight is rebuilt tile by tile inside the GEMM, no N x K
+    buffer).  With ``K`` it has room for the materialized dequantized weight
+    (K_pad x N_pad fp16), which selects the materialized schedule."""
     if K is None:
         n = _lib.i8lt_backward_workspace_size(M, N, _code(dtype))
     else:
@@ -120,11 +121,13 @@ def forward(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, bias: 
 
 def backward_input(G: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, need_grad_A: bool = True,
                    bias_dtype: torch.dtype | None = None, addend: torch.Tensor | None = None,
-                   ws: torch.Tensor | None = None, fused: bool = False):
+                   ws: torch.Tensor | None = None, fused: bool = True):
     """(grad_A [M, K] or None, grad_bias [N] or None) from grad_output G [M, N].
-    ``fused``: rebuild the dequantized weight tile by tile inside the GEMM
-    instead of materializing it in the workspace (less memory, slower).  A
-    caller-supplied ``ws`` decides by its size instead."""
+    ``fused`` (default): the dequantized weight is rebuilt tile by tile inside
+    the GEMM and never stored.  ``fused=False``: it is first written to the
+    workspace (K x N fp16) by a memory-bound prepass, then read by a plain
+    fp16 GEMM -- more memory, a little faster.  A caller-supplied ``ws``
+    decides by its size instead.  Both give the same bits."""
     _require_cuda(G, CB, SCB, addend)
     G = G.contiguous()
     M, N = G.shape
