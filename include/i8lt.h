@@ -147,6 +147,36 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K,
                  void* ws, size_t ws_bytes, int64_t max_outliers,
                  const i8lt_fwd_debug* dbg, void* stream);
 
+/*
+ * Token-sharded forward (one batch whose rows are split over several ranks,
+ * each with its own workspace).  The outlier columns are a property of the
+ * whole batch (a column is an outlier when some row of the batch exceeds the
+ * threshold), so the ranks exchange one K-sized vector before quantizing:
+ *   1. i8lt_forward_colmax: clears the workspace's status word and column
+ *      maxima, then writes the column maxima of |fp16(A)| over this rank's M
+ *      rows (M may be 0) into the colmax region of `ws`
+ *      (i8lt_fwd_layout.colmax: K uint32 values, the fp16 bit pattern of
+ *      each magnitude; integer order = magnitude order).  Arguments as in
+ *      i8lt_forward (N and max_outliers size the workspace).
+ *   2. the caller combines the K values of all ranks with an element-wise
+ *      maximum (e.g. an all-reduce MAX over the region viewed as int32) and
+ *      writes the result back into every rank's region;
+ *   3. i8lt_forward_from_colmax: i8lt_forward on this rank's rows, taking the
+ *      colmax region as given instead of computing it.
+ * The rows of all ranks together then equal i8lt_forward on the whole batch,
+ * bit for bit.  With a disabled threshold the exchange changes nothing.
+ * No counterpart on the pages (their layer runs on one device); it is the
+ * exchange step a token-sharded version of the method needs.
+ */
+int i8lt_forward_colmax(const void* A, int at, int64_t M, int64_t K, int64_t N,
+                        void* ws, size_t ws_bytes, int64_t max_outliers, void* stream);
+int i8lt_forward_from_colmax(const void* A, int at, int64_t M, int64_t K,
+                             const int8_t* CB, const float* SCB, int64_t N,
+                             const void* bias, int bt, float threshold,
+                             const void* residual, void* out,
+                             void* ws, size_t ws_bytes, int64_t max_outliers,
+                             const i8lt_fwd_debug* dbg, void* stream);
+
 /* Workspace of i8lt_backward_input, in bytes.
  * i8lt_backward_workspace_size: the minimum, for the fused schedule (status
  * word, grad_bias partial sums, and the fp16 copy of grad_output when it is

@@ -63,6 +63,11 @@ SIGNATURES = {
     "i8lt_forward": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
                              c_void_p, c_int, c_float, c_void_p, c_void_p,
                              c_void_p, c_size_t, c_int64, POINTER(i8lt_fwd_debug), c_void_p]),
+    "i8lt_forward_colmax": (c_int, [c_void_p, c_int, c_int64, c_int64, c_int64, c_void_p, c_size_t, c_int64,
+                                    c_void_p]),
+    "i8lt_forward_from_colmax": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
+                                         c_void_p, c_int, c_float, c_void_p, c_void_p,
+                                         c_void_p, c_size_t, c_int64, POINTER(i8lt_fwd_debug), c_void_p]),
     "i8lt_backward_workspace_size": (c_size_t, [c_int64, c_int64, c_int]),
     "i8lt_backward_workspace_size_dq": (c_size_t, [c_int64, c_int64, c_int64, c_int]),
     "i8lt_backward_input": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
@@ -144,6 +149,17 @@ def i8lt_forward(A, at, M, K, CB, SCB, N, bias, bt, threshold, residual, out, ws
     dbg = ctypes.byref(i8lt_fwd_debug(_p(acc_i32))) if acc_i32 else None
     return load().i8lt_forward(_p(A), at, M, K, _p(CB), _p(SCB), N, _p(bias), bt, c_float(threshold),
                                _p(residual), _p(out), _p(ws), ws_bytes, max_outliers, dbg, _p(stream))
+
+
+def i8lt_forward_colmax(A, at, M, K, N, ws, ws_bytes, max_outliers, stream=None) -> int:
+    return load().i8lt_forward_colmax(_p(A), at, M, K, N, _p(ws), ws_bytes, max_outliers, _p(stream))
+
+
+def i8lt_forward_from_colmax(A, at, M, K, CB, SCB, N, bias, bt, threshold, residual, out, ws, ws_bytes,
+                             max_outliers, acc_i32=None, stream=None) -> int:
+    dbg = ctypes.byref(i8lt_fwd_debug(_p(acc_i32))) if acc_i32 else None
+    return load().i8lt_forward_from_colmax(_p(A), at, M, K, _p(CB), _p(SCB), N, _p(bias), bt, c_float(threshold),
+                                           _p(residual), _p(out), _p(ws), ws_bytes, max_outliers, dbg, _p(stream))
 
 
 def i8lt_backward_workspace_size(M, N, gt) -> int:

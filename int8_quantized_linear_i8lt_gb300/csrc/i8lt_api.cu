@@ -177,6 +177,105 @@ void prof_end(cudaStream_t s) {
 }
 }  // namespace i8lt
 
+namespace {
+
+// The three forms of the forward: the whole call; only the column maxima of
+// this call's rows (first half of a token-sharded forward); everything after
+// the column maxima, which the caller has merged across the shards.
+enum FwdMode { kFwdFull = 0, kFwdColmaxOnly = 1, kFwdFromColmax = 2 };
+
+int forward_impl(FwdMode mode, const void* A, int at, int64_t M, int64_t K, const int8_t* CB, const float* SCB,
+                 int64_t N, const void* bias, int bt, float threshold, const void* residual, void* out, void* ws,
+                 size_t ws_bytes, int64_t max_outliers, const i8lt_fwd_debug* dbg, void* stream) {
+  const bool colmax_only = mode == kFwdColmaxOnly;
+  if (!valid_dt(at) || (!colmax_only && bias != nullptr && !valid_dt(bt))) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (M < 0 || N <= 0 || K <= 0 || max_outliers < 0) return I8LT_ERR_INVALID_ARG;
+  if (K > I8LT_MAX_K) return I8LT_ERR_K_TOO_LARGE;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
+  if (ws == nullptr || (!colmax_only && (CB == nullptr || SCB == nullptr))) return I8LT_ERR_INVALID_ARG;
+  if (M > 0 && (A == nullptr || (!colmax_only && out == nullptr))) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(CB) || !aligned16(out) || !aligned16(residual)) return I8LT_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
+  const i8lt_fwd_layout L = fwd_layout(M, K, N, max_outliers);
+  if (ws_bytes < L.total) return I8LT_ERR_WORKSPACE;
+  if (dbg != nullptr && dbg->acc_i32 != nullptr && !aligned16(dbg->acc_i32)) return I8LT_ERR_MISALIGNED;
+  if (int d = check_device()) return d;
+  if (M == 0 && !colmax_only) return I8LT_OK;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  DevStatus* st = reinterpret_cast<DevStatus*>(w + L.status);
+  uint32_t* colmax = reinterpret_cast<uint32_t*>(w + L.colmax);
+  uint32_t* mask = reinterpret_cast<uint32_t*>(w + L.mask);
+  int* idx = reinterpret_cast<int*>(w + L.idx);
+  float* SCA = reinterpret_cast<float*>(w + L.sca);
+  uint8_t* rowsmall = w + L.rowsmall;
+  __half* Aq = reinterpret_cast<__half*>(w + L.aq);
+  __half* subA = reinterpret_cast<__half*>(w + L.suba);
+  __half* subB = reinterpret_cast<__half*>(w + L.subb);
+  __half* CBh = reinterpret_cast<__half*>(w + L.cbh);
+  const bool enabled = threshold_enabled(threshold);
+  const bool vec = (K % 8) == 0;
+  cudaError_t e = cudaSuccess;
+
+  // one memset clears the status word of this call and (unless they are
+  // given) the column maxima
+  const bool own_colmax = enabled && mode != kFwdFromColmax;
+  const size_t clear = own_colmax ? L.colmax + static_cast<size_t>(K) * 4 : sizeof(DevStatus);
+  if ((e = cudaMemsetAsync(w, 0, clear, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+  if (own_colmax && M > 0) {
+    if ((e = launch_colmax(A, at, M, K, vec, colmax, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+  }
+  if (colmax_only) return I8LT_OK;
+  if (enabled) {
+    if ((e = launch_outlier_index(colmax, K, threshold, max_outliers, idx, mask, st, s)) != cudaSuccess)
+      return I8LT_ERR_CUDA;
+  }
+  if ((e = launch_row_quantize(A, at, M, K, L.k_pad, vec, enabled ? mask : nullptr, idx, st, L.cap_pad, SCA, Aq,
+                               enabled ? subA : nullptr, rowsmall, s)) != cudaSuccess)
+    return I8LT_ERR_CUDA;
+  const bool with_outliers = enabled && L.cap_pad > 0;
+  if (with_outliers) {
+    if ((e = launch_build_subB(CB, L.k_pad, SCB, N, idx, st, L.cap_pad, subB, s)) != cudaSuccess)
+      return I8LT_ERR_CUDA;
+  }
+
+  if ((e = launch_widen_codes(CB, CBh, N * L.k_pad, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+
+  FwdGemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  if (!make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Aq, L.k_pad, M, L.k_pad * 2, kBK, kBoxRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CBh, L.k_pad, N, L.k_pad * 2, kBK, kBoxRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return I8LT_ERR_CUDA;
+  if (with_outliers) {
+    if (!make_tmap(&g.tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subA, L.cap_pad, M, L.cap_pad * 2, kBK, kBoxRows,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap(&g.tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subB, L.cap_pad, N, L.cap_pad * 2, kBK, kBoxRows,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return I8LT_ERR_CUDA;
+  }
+  FwdEpiArgs ea;
+  ea.M = static_cast<int>(M);
+  ea.N = static_cast<int>(N);
+  ea.K_pad = static_cast<int>(L.k_pad);
+  ea.use_outliers = with_outliers ? 1 : 0;
+  ea.SCA = SCA;
+  ea.rowsmall = rowsmall;
+  ea.SCB = SCB;
+  ea.bias = bias;
+  ea.bias_dt = bt;
+  ea.residual = residual;
+  ea.out = out;
+  ea.out_dt = at;
+  ea.acc_i32 = dbg != nullptr ? dbg->acc_i32 : nullptr;
+  ea.st = st;
+  return cuda_status(launch_fwd_gemm(g, ea, s));
+}
+
+}  // namespace
+
 extern "C" {
 
 int i8lt_abi_version(void) { return kAbiVersion; }
@@ -223,88 +322,26 @@ int i8lt_forward_workspace_layout(int64_t M, int64_t K, int64_t N, int64_t max_o
   return I8LT_OK;
 }
 
+
 int i8lt_forward(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, const float* SCB, int64_t N,
                  const void* bias, int bt, float threshold, const void* residual, void* out, void* ws,
                  size_t ws_bytes, int64_t max_outliers, const i8lt_fwd_debug* dbg, void* stream) {
-  if (!valid_dt(at) || (bias != nullptr && !valid_dt(bt))) return I8LT_ERR_UNSUPPORTED_DTYPE;
-  if (M < 0 || N <= 0 || K <= 0 || max_outliers < 0) return I8LT_ERR_INVALID_ARG;
-  if (K > I8LT_MAX_K) return I8LT_ERR_K_TOO_LARGE;
-  if (M > INT32_MAX / 2 || N > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
-  if (CB == nullptr || SCB == nullptr || ws == nullptr) return I8LT_ERR_INVALID_ARG;
-  if (M > 0 && (A == nullptr || out == nullptr)) return I8LT_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(CB) || !aligned16(out) || !aligned16(residual)) return I8LT_ERR_MISALIGNED;
-  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
-  const i8lt_fwd_layout L = fwd_layout(M, K, N, max_outliers);
-  if (ws_bytes < L.total) return I8LT_ERR_WORKSPACE;
-  if (dbg != nullptr && dbg->acc_i32 != nullptr && !aligned16(dbg->acc_i32)) return I8LT_ERR_MISALIGNED;
-  if (int d = check_device()) return d;
-  if (M == 0) return I8LT_OK;
+  return forward_impl(kFwdFull, A, at, M, K, CB, SCB, N, bias, bt, threshold, residual, out, ws, ws_bytes,
+                      max_outliers, dbg, stream);
+}
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  DevStatus* st = reinterpret_cast<DevStatus*>(w + L.status);
-  uint32_t* colmax = reinterpret_cast<uint32_t*>(w + L.colmax);
-  uint32_t* mask = reinterpret_cast<uint32_t*>(w + L.mask);
-  int* idx = reinterpret_cast<int*>(w + L.idx);
-  float* SCA = reinterpret_cast<float*>(w + L.sca);
-  uint8_t* rowsmall = w + L.rowsmall;
-  __half* Aq = reinterpret_cast<__half*>(w + L.aq);
-  __half* subA = reinterpret_cast<__half*>(w + L.suba);
-  __half* subB = reinterpret_cast<__half*>(w + L.subb);
-  __half* CBh = reinterpret_cast<__half*>(w + L.cbh);
-  const bool enabled = threshold_enabled(threshold);
-  const bool vec = (K % 8) == 0;
-  cudaError_t e = cudaSuccess;
+int i8lt_forward_colmax(const void* A, int at, int64_t M, int64_t K, int64_t N, void* ws, size_t ws_bytes,
+                        int64_t max_outliers, void* stream) {
+  return forward_impl(kFwdColmaxOnly, A, at, M, K, nullptr, nullptr, N, nullptr, 0, 1.0f, nullptr, nullptr, ws,
+                      ws_bytes, max_outliers, nullptr, stream);
+}
 
-  // one memset clears the status word of this call and the column maxima
-  const size_t clear = enabled ? L.colmax + static_cast<size_t>(K) * 4 : sizeof(DevStatus);
-  if ((e = cudaMemsetAsync(w, 0, clear, s)) != cudaSuccess) return I8LT_ERR_CUDA;
-  if (enabled) {
-    if ((e = launch_colmax(A, at, M, K, vec, colmax, s)) != cudaSuccess) return I8LT_ERR_CUDA;
-    if ((e = launch_outlier_index(colmax, K, threshold, max_outliers, idx, mask, st, s)) != cudaSuccess)
-      return I8LT_ERR_CUDA;
-  }
-  if ((e = launch_row_quantize(A, at, M, K, L.k_pad, vec, enabled ? mask : nullptr, idx, st, L.cap_pad, SCA, Aq,
-                               enabled ? subA : nullptr, rowsmall, s)) != cudaSuccess)
-    return I8LT_ERR_CUDA;
-  const bool with_outliers = enabled && L.cap_pad > 0;
-  if (with_outliers) {
-    if ((e = launch_build_subB(CB, L.k_pad, SCB, N, idx, st, L.cap_pad, subB, s)) != cudaSuccess)
-      return I8LT_ERR_CUDA;
-  }
-
-  if ((e = launch_widen_codes(CB, CBh, N * L.k_pad, s)) != cudaSuccess) return I8LT_ERR_CUDA;
-
-  FwdGemmArgs g;
-  std::memset(&g, 0, sizeof(g));
-  if (!make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Aq, L.k_pad, M, L.k_pad * 2, kBK, kBoxRows,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CBh, L.k_pad, N, L.k_pad * 2, kBK, kBoxRows,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-    return I8LT_ERR_CUDA;
-  if (with_outliers) {
-    if (!make_tmap(&g.tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subA, L.cap_pad, M, L.cap_pad * 2, kBK, kBoxRows,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap(&g.tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, subB, L.cap_pad, N, L.cap_pad * 2, kBK, kBoxRows,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
-      return I8LT_ERR_CUDA;
-  }
-  FwdEpiArgs ea;
-  ea.M = static_cast<int>(M);
-  ea.N = static_cast<int>(N);
-  ea.K_pad = static_cast<int>(L.k_pad);
-  ea.use_outliers = with_outliers ? 1 : 0;
-  ea.SCA = SCA;
-  ea.rowsmall = rowsmall;
-  ea.SCB = SCB;
-  ea.bias = bias;
-  ea.bias_dt = bt;
-  ea.residual = residual;
-  ea.out = out;
-  ea.out_dt = at;
-  ea.acc_i32 = dbg != nullptr ? dbg->acc_i32 : nullptr;
-  ea.st = st;
-  return cuda_status(launch_fwd_gemm(g, ea, s));
+int i8lt_forward_from_colmax(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, const float* SCB,
+                             int64_t N, const void* bias, int bt, float threshold, const void* residual, void* out,
+                             void* ws, size_t ws_bytes, int64_t max_outliers, const i8lt_fwd_debug* dbg,
+                             void* stream) {
+  return forward_impl(kFwdFromColmax, A, at, M, K, CB, SCB, N, bias, bt, threshold, residual, out, ws, ws_bytes,
+                      max_outliers, dbg, stream);
 }
 
 size_t i8lt_backward_workspace_size(int64_t M, int64_t N, int gt) {

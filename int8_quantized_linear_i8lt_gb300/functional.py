@@ -93,9 +93,15 @@ def backward_workspace(M: int, N: int, dtype: torch.dtype, device, K: int | None
 def forward(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, bias: torch.Tensor | None = None,
             threshold: float = 6.0, residual: torch.Tensor | None = None, max_outliers: int | None = None,
             out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
-            acc_i32: torch.Tensor | None = None):
+            acc_i32: torch.Tensor | None = None, merge_colmax=None):
     """out [M, N] = int8 linear of A [M, K] (see i8lt_forward).  Returns
-    (out, ws); ``ws`` holds the quantized activations and the outlier set."""
+    (out, ws); ``ws`` holds the quantized activations and the outlier set.
+
+    ``merge_colmax``: for a token-sharded batch, a callable that receives the
+    K column maxima of this call's rows (an int32 view into ``ws``, ordered
+    like the magnitudes) and replaces them in place with the maxima over
+    all shards, e.g. an all-reduce MAX; the outlier set is then the whole
+    batch's (i8lt_forward_colmax / i8lt_forward_from_colmax)."""
     _require_cuda(A, CB, SCB, bias, residual)
     A = A.contiguous()
     M = A.shape[0]
@@ -112,11 +118,30 @@ def forward(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, bias: 
     if residual is not None:
         residual = residual.contiguous()
     bias_c = None if bias is None else bias.contiguous()
-    _check(_lib.i8lt_forward(A.data_ptr(), _code(A.dtype), M, K, CB.data_ptr(), SCB.data_ptr(), N,
-                             _ptr(bias_c), _code(bias_c.dtype) if bias_c is not None else 0, float(threshold),
-                             _ptr(residual), out.data_ptr(), ws.data_ptr(), ws.numel(), cap,
-                             acc_i32=_ptr(acc_i32), stream=_stream(A)), "i8lt_forward")
+    args = (_ptr(bias_c), _code(bias_c.dtype) if bias_c is not None else 0, float(threshold),
+            _ptr(residual), out.data_ptr(), ws.data_ptr(), ws.numel(), cap)
+    if merge_colmax is None:
+        _check(_lib.i8lt_forward(A.data_ptr(), _code(A.dtype), M, K, CB.data_ptr(), SCB.data_ptr(), N, *args,
+                                 acc_i32=_ptr(acc_i32), stream=_stream(A)), "i8lt_forward")
+        return out, ws
+    _check(_lib.i8lt_forward_colmax(A.data_ptr(), _code(A.dtype), M, K, N, ws.data_ptr(), ws.numel(), cap,
+                                    stream=_stream(A)), "i8lt_forward_colmax")
+    lay = _lib.i8lt_forward_workspace_layout(M, K, N, cap)
+    merge_colmax(ws[lay.colmax:lay.colmax + 4 * K].view(torch.int32))
+    _check(_lib.i8lt_forward_from_colmax(A.data_ptr(), _code(A.dtype), M, K, CB.data_ptr(), SCB.data_ptr(), N,
+                                         *args, acc_i32=_ptr(acc_i32), stream=_stream(A)),
+           "i8lt_forward_from_colmax")
     return out, ws
+
+
+def allreduce_colmax(group=None):
+    """``merge_colmax`` for torch.distributed: an all-reduce MAX of the column
+    maxima over ``group`` (one K-sized int32 exchange per forward)."""
+    import torch.distributed as dist
+
+    def merge(t: torch.Tensor):
+        dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return merge
 
 
 def backward_input(G: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, need_grad_A: bool = True,

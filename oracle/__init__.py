@@ -144,16 +144,30 @@ def threshold_enabled(threshold: float) -> bool:
     return math.isfinite(t) and t > 0.0
 
 
+def column_absmax(A16: np.ndarray) -> np.ndarray:
+    """The reduction of step a2: max over the rows of |A16[m, k]| per column
+    (float64, exact: the values are fp16; 0 for no rows)."""
+    colmax = np.zeros(A16.shape[1], dtype=np.float64)
+    for r in range(0, A16.shape[0], 2048):          # row blocks: bounded memory
+        colmax = np.maximum(colmax, np.abs(A16[r:r + 2048].astype(np.float64)).max(axis=0))
+    return colmax
+
+
+def outlier_columns_from_absmax(colmax: np.ndarray, threshold: float) -> np.ndarray:
+    """The selection of step a2: ascending indices of the columns whose
+    absolute maximum exceeds the threshold (taken as an fp32 value)."""
+    if not threshold_enabled(threshold):
+        return np.zeros(0, dtype=np.int32)
+    thr = float(np.float32(threshold))
+    return np.nonzero(np.asarray(colmax, dtype=np.float64) > thr)[0].astype(np.int32)
+
+
 def outlier_columns(A16: np.ndarray, threshold: float) -> np.ndarray:
     """Step a2: ascending unique indices of the columns of A16 holding at least
     one element with |a| > threshold (the threshold taken as an fp32 value)."""
     if not threshold_enabled(threshold) or A16.shape[0] == 0:
         return np.zeros(0, dtype=np.int32)
-    thr = float(np.float32(threshold))
-    colmax = np.zeros(A16.shape[1], dtype=np.float64)
-    for r in range(0, A16.shape[0], 2048):          # row blocks: bounded memory
-        colmax = np.maximum(colmax, np.abs(A16[r:r + 2048].astype(np.float64)).max(axis=0))
-    return np.nonzero(colmax > thr)[0].astype(np.int32)
+    return outlier_columns_from_absmax(column_absmax(A16), threshold)
 
 
 def quantize_rows(A16: np.ndarray, idx: np.ndarray):
@@ -224,17 +238,23 @@ def int_gemm(Aq: np.ndarray, CB: np.ndarray) -> np.ndarray:
 
 
 def forward(A, dtype, CB, SCB, bias=None, bias_dtype=None, threshold=0.0,
-            residual=None):
+            residual=None, col_absmax=None):
     """Steps a1-a7: the whole quantized forward.
 
     ``A`` [M, K] in ``dtype`` storage; ``CB`` int8 [N, K]; ``SCB`` fp32 [N];
     ``bias`` [N] in ``bias_dtype`` storage or None; ``residual`` [M, N] in
     ``dtype`` storage or None (added before the single rounding).
+    ``col_absmax``: the column maxima of a larger batch that ``A`` is a row
+    shard of (token-sharded forward: the outlier set is the whole batch's);
+    None takes them over ``A``.
 
     out = round_to( Cacc * SCA * SCB / 127**2 + subA @ subB^T + bias + residual )
     """
     A16 = cast_f16(A, dtype)
-    idx = outlier_columns(A16, threshold)
+    if col_absmax is None:
+        idx = outlier_columns(A16, threshold)
+    else:
+        idx = outlier_columns_from_absmax(col_absmax, threshold)
     SCA, Aq, subA = quantize_rows(A16, idx)
     Wdq = dequant_weight(CB, SCB)
     subB = Wdq[:, idx]

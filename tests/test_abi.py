@@ -90,6 +90,20 @@ def test_forward_argument_errors(L):
     assert fwd(ws_bytes=need - 1) == _lib.I8LT_ERR_WORKSPACE
 
 
+def test_sharded_forward_argument_errors(L):
+    # step 1 needs no weight; both steps check the workspace like i8lt_forward
+    need = _lib.i8lt_forward_workspace_size(64, 64, 64, 16)
+    assert _lib.i8lt_forward_colmax(FAKE, 3, 64, 64, 64, FAKE, need, 16) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert _lib.i8lt_forward_colmax(FAKE, 0, 64, 0, 64, FAKE, need, 16) == _lib.I8LT_ERR_INVALID_ARG
+    assert _lib.i8lt_forward_colmax(FAKE, 0, 64, 64, 64, FAKE, need - 1, 16) == _lib.I8LT_ERR_WORKSPACE
+    assert _lib.i8lt_forward_colmax(FAKE, 0, 64, 64, 64, None, need, 16) == _lib.I8LT_ERR_INVALID_ARG
+    assert _lib.i8lt_forward_colmax(FAKE + 4, 0, 64, 64, 64, FAKE, need, 16) == _lib.I8LT_ERR_MISALIGNED
+    assert _lib.i8lt_forward_from_colmax(FAKE, 0, 64, 64, None, FAKE, 64, None, 0, 6.0, None, FAKE, FAKE, need,
+                                         16) == _lib.I8LT_ERR_INVALID_ARG
+    assert _lib.i8lt_forward_from_colmax(FAKE, 0, 64, _lib.I8LT_MAX_K + 1, FAKE, FAKE, 64, None, 0, 6.0, None, FAKE,
+                                         FAKE, 1 << 40, 16) == _lib.I8LT_ERR_K_TOO_LARGE
+
+
 def bwd(**kw):
     a = dict(G=FAKE, gt=0, M=64, N=64, CB=FAKE, SCB=FAKE, K=64, addend=None, grad_A=FAKE, grad_bias=None, bt=0,
              ws=FAKE, ws_bytes=1 << 40)
