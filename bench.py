@@ -238,9 +238,10 @@ def run_ours(args):
     layers = [Layer(wl, li, 1234 + rank, device) for li in range(len(wl.layers))]
     stream = torch.cuda.current_stream(device)
     sp = stream.cuda_stream
+    mat = args.bwd_schedule == "materialized"
     for _ in range(args.warmup):
         for L in layers:
-            _launch_layer(L, sp)
+            _launch_layer(L, sp, mat)
     torch.cuda.synchronize()
     for L in layers:
         st, found = I.device_status(L.ws_f)
@@ -256,7 +257,7 @@ def run_ours(args):
         ev0.record(stream)
         for _ in range(args.steps):
             for L in layers:
-                _launch_layer(L, sp)
+                _launch_layer(L, sp, mat)
         ev1.record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
@@ -273,7 +274,7 @@ def run_ours(args):
     per_step = len(recs) // args.steps
     kern = {}
     for i, (name, ms) in enumerate(recs):
-        L = layers[_layer_of(i % per_step, layers)]
+        L = layers[_layer_of(i % per_step, layers, mat)]
         d = kern.setdefault(name, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
         d["launches"] += 1
         d["ms"] += ms
@@ -309,8 +310,8 @@ def run_ours(args):
         kernels[k] = e
     # --- end to end through host buffers (pinned), inputs and results copied each step
     e2e = run_e2e(layers, stream, max(2, min(args.steps, 10)), device)
-    # --- the same step with the materialized backward schedule (context, not the headline)
-    alt = time_materialized(layers, stream, max(2, min(args.steps, 10)), device)
+    # --- the same step with the other backward schedule (context, not the headline)
+    alt = time_schedule(layers, stream, max(2, min(args.steps, 10)), device, not mat)
 
     clocks = clk.summary()
     line = {
@@ -325,7 +326,8 @@ def run_ours(args):
         "roofline": roof,
         "kernels": kernels,
         "e2e": e2e,
-        "bwd_materialized": alt,
+        "bwd_schedule": args.bwd_schedule,
+        ("bwd_fused" if mat else "bwd_materialized"): alt,
         "gpu_launches": n_launches,
         "gemm_launch": {k: dict(zip(("status", "ctas", "threads", "smem"), _lib.i8lt_gemm_launch_info(k)))
                         for k in ("fwd_gemm", "bwd_gemm")},
@@ -341,40 +343,43 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _layer_of(i, layers):
+def _layer_of(i, layers, materialized=False):
     """Index of the layer that launch ``i`` (within one step) belongs to."""
     n = 0
     for li, L in enumerate(layers):
-        n += launches_per_layer(L)
+        n += launches_per_layer(L, materialized)
         if i < n:
             return li
     return len(layers) - 1
 
 
-def launches_per_layer(L) -> int:
+def launches_per_layer(L, materialized=False) -> int:
     """Our kernels per layer and step: colmax, outlier index, row quantize,
     subB (outliers on), weight-code widening, forward GEMM; grad_output
-    prepass, grad_bias finalize, backward GEMM (fused schedule)."""
+    prepass, grad_bias finalize, (weight dequantization when materialized,)
+    backward GEMM."""
     import math
     fwd = 6 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 3
-    return fwd + 3
+    return fwd + (4 if materialized else 3)
 
 
-def time_materialized(layers, stream, steps, device):
-    """The step with the materialized backward schedule: a prepass writes the
-    dequantized weight (K x N fp16) to the workspace, then a TMA-fed fp16 GEMM
-    reads it.  Same results as the fused schedule; reported as context."""
+def time_schedule(layers, stream, steps, device, materialized):
+    """The step with the given backward schedule.  Materialized: a prepass
+    writes the dequantized weight (K x N fp16) to the workspace, then a
+    TMA-fed fp16 GEMM reads it; fused: the weight is rebuilt inside the GEMM.
+    Same results either way; the one not timed as the headline is reported
+    as context."""
     from int8_quantized_linear_i8lt_gb300 import _lib
     sp = stream.cuda_stream
     for L in layers:
-        _launch_layer(L, sp, materialized=True)
+        _launch_layer(L, sp, materialized)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _lib.i8lt_profile_start(1 << 16)
     ev0.record(stream)
     for _ in range(steps):
         for L in layers:
-            _launch_layer(L, sp, materialized=True)
+            _launch_layer(L, sp, materialized)
     ev1.record(stream)
     torch.cuda.synchronize()
     pst, recs, _ = _lib.i8lt_profile_stop(1 << 16)
@@ -558,6 +563,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--bwd-schedule", default="fused", choices=["fused", "materialized"],
+                    help="backward schedule of the timed steps (the other one is timed beside it)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
