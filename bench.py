@@ -327,6 +327,8 @@ def run_ours(args):
         "kernels": kernels,
         "e2e": e2e,
         "bwd_schedule": args.bwd_schedule,
+        **({"mlp_chain": time_mlp_chain(wl, layers, stream, max(2, min(args.steps, 10)), device)}
+           if wl.kind == "mlp" and len(layers) == 2 else {}),
         ("bwd_fused" if mat else "bwd_materialized"): alt,
         "gpu_launches": n_launches,
         "gemm_launch": {k: dict(zip(("status", "ctas", "threads", "smem"), _lib.i8lt_gemm_launch_info(k)))
@@ -361,6 +363,57 @@ def launches_per_layer(L, materialized=False) -> int:
     import math
     fwd = 6 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 3
     return fwd + (4 if materialized else 3)
+
+
+def time_mlp_chain(wl, layers, stream, steps, device):
+    """An MLP workload run as one block (fc1 -> SiLU -> fc2, then the
+    backward of both), fused -- fc1's epilogue applies the SiLU and writes
+    fc2's column maxima -- and unfused (separate SiLU kernel and column-maxima
+    pass).  Same results bit for bit; both timed with CUDA events."""
+    import int8_quantized_linear_i8lt_gb300 as I
+    F = I.functional
+    L1, L2 = layers
+    s1, s2 = L1.spec, L2.spec
+    thr = s1.threshold
+    x, G = L1.A, L2.G
+    M, K, H, N2 = s1.M, s1.K, s1.N, s2.N
+    cap2 = F._capacity(H, thr, None)
+    ws2 = F.forward_workspace(M, H, N2, cap2, device)
+    colmax = F.colmax_region(ws2, M, H, N2, thr)
+
+    def block(fused):
+        if fused:
+            h, a, _ = F.forward_silu(x, L1.CB, L1.SCB, K, L1.bias, thr, act_colmax=colmax)
+            y, _ = I.forward(a, L2.CB, L2.SCB, H, L2.bias, thr, ws=ws2, colmax_ready=True)
+        else:
+            h, _ = I.forward(x, L1.CB, L1.SCB, K, L1.bias, thr)
+            a = F.silu(h)
+            y, _ = I.forward(a, L2.CB, L2.SCB, H, L2.bias, thr, ws=ws2)
+        ga, _ = I.backward_input(G, L2.CB, L2.SCB, H, bias_dtype=L2.bias.dtype)
+        gh = F.silu_backward(ga, h)
+        gx, _ = I.backward_input(gh, L1.CB, L1.SCB, K, bias_dtype=L1.bias.dtype)
+        return y, gx
+
+    out = {}
+    for fused in (True, False):
+        block(fused)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            block(fused)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = reduce_max(ev0.elapsed_time(ev1), device) / steps
+        ops = 4.0 * M * K * H + 4.0 * M * H * N2
+        out["fused" if fused else "unfused"] = {"ms_per_step": round(ms, 4),
+                                                "value": round(ops / (ms * 1e-3) / 1e12, 2), "unit": "TOPS"}
+    y1, g1 = block(True)
+    y2, g2 = block(False)
+    out["bit_identical"] = bool(torch.equal(y1.view(torch.uint8), y2.view(torch.uint8))
+                                and torch.equal(g1.view(torch.uint8), g2.view(torch.uint8)))
+    out["steps"] = steps
+    return out
 
 
 def time_schedule(layers, stream, steps, device, materialized):

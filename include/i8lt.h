@@ -148,6 +148,30 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K,
                  const i8lt_fwd_debug* dbg, void* stream);
 
 /*
+ * i8lt_forward_silu -- i8lt_forward for the hidden layer of an MLP (Dense ->
+ * SiLU -> Dense), with the SiLU and the next layer's outlier detection fused
+ * into the GEMM epilogue:
+ *   out        [M, N] dtype `at`: the layer's output h, as i8lt_forward
+ *   act        [M, N] dtype `at`: silu(h) computed from the stored h with
+ *              the same arithmetic as i8lt_silu_forward (bit-identical)
+ *   act_colmax [N] uint32, device: cleared by the call, then set to the
+ *              per-column maxima of |fp16(act)| as fp16 bit patterns -- the
+ *              column maxima step of the next layer's forward.  Pass the
+ *              colmax region of the next layer's workspace
+ *              (i8lt_fwd_layout.colmax) and run that layer with
+ *              i8lt_forward_from_colmax: the pass of the standalone SiLU
+ *              kernel and the next layer's column-maxima pass are saved.
+ * Other arguments and errors as i8lt_forward; act 16-byte aligned,
+ * act_colmax 4-byte aligned, neither may be NULL.
+ */
+int i8lt_forward_silu(const void* A, int at, int64_t M, int64_t K,
+                      const int8_t* CB, const float* SCB, int64_t N,
+                      const void* bias, int bt, float threshold,
+                      const void* residual, void* out, void* act, uint32_t* act_colmax,
+                      void* ws, size_t ws_bytes, int64_t max_outliers,
+                      const i8lt_fwd_debug* dbg, void* stream);
+
+/*
  * Token-sharded forward (one batch whose rows are split over several ranks,
  * each with its own workspace).  The outlier columns are a property of the
  * whole batch (a column is an outlier when some row of the batch exceeds the

@@ -63,6 +63,9 @@ SIGNATURES = {
     "i8lt_forward": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
                              c_void_p, c_int, c_float, c_void_p, c_void_p,
                              c_void_p, c_size_t, c_int64, POINTER(i8lt_fwd_debug), c_void_p]),
+    "i8lt_forward_silu": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
+                                  c_void_p, c_int, c_float, c_void_p, c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_size_t, c_int64, POINTER(i8lt_fwd_debug), c_void_p]),
     "i8lt_forward_colmax": (c_int, [c_void_p, c_int, c_int64, c_int64, c_int64, c_void_p, c_size_t, c_int64,
                                     c_void_p]),
     "i8lt_forward_from_colmax": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
@@ -149,6 +152,14 @@ def i8lt_forward(A, at, M, K, CB, SCB, N, bias, bt, threshold, residual, out, ws
     dbg = ctypes.byref(i8lt_fwd_debug(_p(acc_i32))) if acc_i32 else None
     return load().i8lt_forward(_p(A), at, M, K, _p(CB), _p(SCB), N, _p(bias), bt, c_float(threshold),
                                _p(residual), _p(out), _p(ws), ws_bytes, max_outliers, dbg, _p(stream))
+
+
+def i8lt_forward_silu(A, at, M, K, CB, SCB, N, bias, bt, threshold, residual, out, act, act_colmax, ws, ws_bytes,
+                      max_outliers, acc_i32=None, stream=None) -> int:
+    dbg = ctypes.byref(i8lt_fwd_debug(_p(acc_i32))) if acc_i32 else None
+    return load().i8lt_forward_silu(_p(A), at, M, K, _p(CB), _p(SCB), N, _p(bias), bt, c_float(threshold),
+                                    _p(residual), _p(out), _p(act), _p(act_colmax), _p(ws), ws_bytes, max_outliers,
+                                    dbg, _p(stream))
 
 
 def i8lt_forward_colmax(A, at, M, K, N, ws, ws_bytes, max_outliers, stream=None) -> int:

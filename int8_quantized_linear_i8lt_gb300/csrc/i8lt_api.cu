@@ -186,7 +186,8 @@ enum FwdMode { kFwdFull = 0, kFwdColmaxOnly = 1, kFwdFromColmax = 2 };
 
 int forward_impl(FwdMode mode, const void* A, int at, int64_t M, int64_t K, const int8_t* CB, const float* SCB,
                  int64_t N, const void* bias, int bt, float threshold, const void* residual, void* out, void* ws,
-                 size_t ws_bytes, int64_t max_outliers, const i8lt_fwd_debug* dbg, void* stream) {
+                 size_t ws_bytes, int64_t max_outliers, const i8lt_fwd_debug* dbg, void* stream,
+                 void* act = nullptr, uint32_t* act_colmax = nullptr) {
   const bool colmax_only = mode == kFwdColmaxOnly;
   if (!valid_dt(at) || (!colmax_only && bias != nullptr && !valid_dt(bt))) return I8LT_ERR_UNSUPPORTED_DTYPE;
   if (M < 0 || N <= 0 || K <= 0 || max_outliers < 0) return I8LT_ERR_INVALID_ARG;
@@ -199,7 +200,12 @@ int forward_impl(FwdMode mode, const void* A, int at, int64_t M, int64_t K, cons
   const i8lt_fwd_layout L = fwd_layout(M, K, N, max_outliers);
   if (ws_bytes < L.total) return I8LT_ERR_WORKSPACE;
   if (dbg != nullptr && dbg->acc_i32 != nullptr && !aligned16(dbg->acc_i32)) return I8LT_ERR_MISALIGNED;
+  if ((act == nullptr) != (act_colmax == nullptr)) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(act) || (reinterpret_cast<uintptr_t>(act_colmax) & 3u) != 0) return I8LT_ERR_MISALIGNED;
   if (int d = check_device()) return d;
+  if (act_colmax != nullptr &&
+      cudaMemsetAsync(act_colmax, 0, static_cast<size_t>(N) * 4, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return I8LT_ERR_CUDA;
   if (M == 0 && !colmax_only) return I8LT_OK;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -270,6 +276,8 @@ int forward_impl(FwdMode mode, const void* A, int at, int64_t M, int64_t K, cons
   ea.out = out;
   ea.out_dt = at;
   ea.acc_i32 = dbg != nullptr ? dbg->acc_i32 : nullptr;
+  ea.act = act;
+  ea.act_colmax = act_colmax;
   ea.st = st;
   return cuda_status(launch_fwd_gemm(g, ea, s));
 }
@@ -328,6 +336,15 @@ int i8lt_forward(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, 
                  size_t ws_bytes, int64_t max_outliers, const i8lt_fwd_debug* dbg, void* stream) {
   return forward_impl(kFwdFull, A, at, M, K, CB, SCB, N, bias, bt, threshold, residual, out, ws, ws_bytes,
                       max_outliers, dbg, stream);
+}
+
+int i8lt_forward_silu(const void* A, int at, int64_t M, int64_t K, const int8_t* CB, const float* SCB, int64_t N,
+                      const void* bias, int bt, float threshold, const void* residual, void* out, void* act,
+                      uint32_t* act_colmax, void* ws, size_t ws_bytes, int64_t max_outliers,
+                      const i8lt_fwd_debug* dbg, void* stream) {
+  if (act == nullptr || act_colmax == nullptr) return I8LT_ERR_INVALID_ARG;
+  return forward_impl(kFwdFull, A, at, M, K, CB, SCB, N, bias, bt, threshold, residual, out, ws, ws_bytes,
+                      max_outliers, dbg, stream, act, act_colmax);
 }
 
 int i8lt_forward_colmax(const void* A, int at, int64_t M, int64_t K, int64_t N, void* ws, size_t ws_bytes,

@@ -58,6 +58,14 @@ __device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
 __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_float(float x) { return x; }
 
+// SiLU between MLP layers, one definition for every kernel that applies it
+// (the standalone kernel and the fused GEMM epilogue must agree bit for bit):
+// sigmoid(x) = 1 / (1 + e^-x) with the hardware exponential and the fast
+// division (a few ulp of fp32; the result is then rounded to fp16/bf16),
+// silu(x) = x * sigmoid(x).  Large negative x give e^-x = inf and sigmoid 0.
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, __fadd_rn(1.0f, __expf(-x))); }
+__device__ __forceinline__ float silu_f(float x) { return __fmul_rn(x, sigmoid_f(x)); }
+
 template <typename T> __device__ __forceinline__ T from_float(float x);
 template <> __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
 template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
@@ -521,6 +529,14 @@ __device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t 
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
       "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }

@@ -112,7 +112,7 @@ struct __align__(8) Barriers {
 constexpr int kOpBytes = kCtaRows * kBK * 2;   // 16 KB
 constexpr int kI8Bytes = kCtaRows * kBK;       // 8 KB
 constexpr int kFwdStageBytes = 2 * kOpBytes;
-constexpr int kFwdSmemBytes = 1024 /*align slack*/ + kFwdStages * kFwdStageBytes + 2 * kPairN * 4 /*epilogue vectors*/ +
+constexpr int kFwdSmemBytes = 1024 /*align slack*/ + kFwdStages * kFwdStageBytes + 3 * kPairN * 4 /*epilogue vectors*/ +
                               static_cast<int>(sizeof(Barriers));
 
 // Backward geometry.  Materialized schedule: 256 (k) x 256 (tokens) pair
@@ -272,18 +272,68 @@ __device__ __forceinline__ void init_barriers(Barriers* bars, int epi_warps) {
 // Forward GEMM
 // ---------------------------------------------------------------------------
 template <typename OutT>
-__device__ __forceinline__ void fwd_store16(const FwdEpiArgs& e, int64_t m, int n_base, const float (&v)[16],
-                                            bool vec) {
-  OutT* out = static_cast<OutT*>(e.out) + m * static_cast<int64_t>(e.N) + n_base;
+__device__ __forceinline__ void store16_to(void* base, int N, int64_t m, int n_base, const float (&v)[16], bool vec) {
+  OutT* out = static_cast<OutT*>(base) + m * static_cast<int64_t>(N) + n_base;
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     const int n = n_base + q * 8;
-    if (n >= e.N) break;
+    if (n >= N) break;
     float f[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) f[i] = v[q * 8 + i];
-    store8(out + q * 8, e.N - n, vec && n + 8 <= e.N, f);
+    store8(out + q * 8, N - n, vec && n + 8 <= N, f);
   }
+}
+
+// One halving step of a column-wise max over the lanes of a warp: c[0, 2H)
+// holds this lane's values of 2H columns; partners `lane ^ off` split them, the
+// lane with the `off` bit set keeping the upper H.
+template <int H>
+__device__ __forceinline__ void colmax_halve(uint32_t (&c)[16], int lane, int off) {
+  const bool upper = (lane & off) != 0;
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    const uint32_t lo = c[i], hi = c[i + H];
+    const uint32_t give = upper ? lo : hi;
+    const uint32_t keep = upper ? hi : lo;
+    c[i] = max(keep, __shfl_xor_sync(0xffffffffu, give, off));
+  }
+}
+
+// MLP hidden layer: act = silu(out) as the standalone SiLU kernel computes it
+// from the stored out, and the per-column maxima of |fp16(act)| over this
+// warp's 32 rows raised in the tile's shared column maxima (cmax_s, the 16
+// columns of this group), which go to act_colmax (the next layer's outlier
+// detection) once per tile.
+template <typename OutT>
+__device__ __forceinline__ void silu_epilogue16(const FwdEpiArgs& e, int64_t m, int n_base, bool row_ok,
+                                                const float (&v)[16], bool vec, int lane, uint32_t* cmax_s) {
+  float a[16];
+  uint32_t mag[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    a[j] = silu_f(to_float(from_float<OutT>(v[j])));
+    const float ar = to_float(from_float<OutT>(a[j]));
+    mag[j] = row_ok ? (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(ar))) & 0x7FFFu) : 0u;
+  }
+  if (row_ok) store16_to<OutT>(e.act, e.N, m, n_base, a, vec);
+  // max over the 32 lanes (rows) of each of the 16 columns by a halving
+  // exchange: each step a lane hands the partner the half of its columns it
+  // gives up and keeps the maxima of the other half; after four steps lane
+  // pairs (l, l ^ 1) hold column 8 b4 + 4 b3 + 2 b2 + b1 of their lane bits
+  colmax_halve<8>(mag, lane, 16);
+  colmax_halve<4>(mag, lane, 8);
+  colmax_halve<2>(mag, lane, 4);
+  colmax_halve<1>(mag, lane, 2);
+  const uint32_t mx = max(mag[0], __shfl_xor_sync(0xffffffffu, mag[0], 1));
+  const int j = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+  if ((lane & 1) == 0 && mx != 0u) atomicMax(cmax_s + j, mx);
+}
+
+template <typename OutT>
+__device__ __forceinline__ void fwd_store16(const FwdEpiArgs& e, int64_t m, int n_base, const float (&v)[16],
+                                            bool vec) {
+  store16_to<OutT>(e.out, e.N, m, n_base, v, vec);
 }
 
 template <typename OutT>
@@ -301,13 +351,17 @@ __device__ __forceinline__ void fwd_add_residual16(const FwdEpiArgs& e, int64_t 
   }
 }
 
+// kSilu: the MLP hidden-layer epilogue (also writes silu(out) and raises the
+// per-column maxima of |fp16(silu(out))|).
+template <bool kSilu>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fwd_gemm_kernel(const __grid_constant__ FwdGemmArgs g, const FwdEpiArgs e, int num_m, int num_n, int group) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* scb_s = reinterpret_cast<float*>(smem + kFwdStages * kFwdStageBytes);
   float* bias_s = scb_s + kPairN;
-  Barriers* bars = reinterpret_cast<Barriers*>(bias_s + kPairN);
+  uint32_t* colmax_s = reinterpret_cast<uint32_t*>(bias_s + kPairN);   // fused SiLU: the tile's column maxima
+  Barriers* bars = reinterpret_cast<Barriers*>(colmax_s + kPairN);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -423,11 +477,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool vec = (e.N % 8) == 0;
     int u = 0;
     bool ok = true;
+    int prev_n0 = -1;
+    // fused SiLU: the column maxima of a tile, gathered in shared memory by
+    // every epilogue warp, go out with one global atomic per column
+    auto flush_colmax = [&]() {
+      if constexpr (kSilu) {
+        if (prev_n0 >= 0) {
+          const int n = prev_n0 + et;
+          const uint32_t v = colmax_s[et];
+          if (n < e.N && v != 0u) atomicMax(e.act_colmax + n, v);
+        }
+        colmax_s[et] = 0u;
+      }
+    };
     for (int t = cid; t < num_tiles && ok; t += ncl) {
       int tm, tn;
       tile_coords(t, num_m, num_n, group, tm, tn);
       const int n0 = tn * kPairN;
       named_bar_sync(kBarEpi, kEpiThreads);   // the previous tile no longer reads the vectors
+      flush_colmax();
+      prev_n0 = n0;
       {
         const int n = n0 + et;
         scb_s[et] = (n < e.N) ? e.SCB[n] : 0.f;
@@ -458,7 +527,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tmem_st_wait();
         } else {
-          // last unit of the tile: the output
+          // last unit of the tile, phase 1: the fp32 output values before the
+          // residual, written over the running sum in R, so that X can be
+          // handed back to the MMA before the slower stores of phase 2
           const bool has_o = OB > 0;
           const bool r_live = has_o ? (nchunks > 0) : (nchunks > 1);
           const float rs = row_ok ? __fmul_rn(e.SCA[m], 1.0f / 16129.0f) : 0.f;
@@ -477,14 +548,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               for (int j = 0; j < 16; ++j) r[j] = 0;
             }
             const int nb = n0 + col0 + gc;
-            if (row_ok && nb < e.N) {
-              float v[16];
+            if (e.acc_i32 != nullptr && row_ok && nb < e.N) {
+              int32_t* dst = e.acc_i32 + m * static_cast<int64_t>(e.N);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float sc = __fmul_rn(rs, scb_s[col0 + gc + j]);
-                v[j] = __fadd_rn(__fmaf_rn(static_cast<float>(static_cast<int32_t>(r[j])), sc, __uint_as_float(x[j])),
-                                 bias_s[col0 + gc + j]);
-              }
+              for (int j = 0; j < 16; ++j)
+                if (nb + j < e.N) dst[nb + j] = static_cast<int32_t>(r[j]);
+            }
+            uint32_t vb[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float sc = __fmul_rn(rs, scb_s[col0 + gc + j]);
+              vb[j] = __float_as_uint(__fadd_rn(
+                  __fmaf_rn(static_cast<float>(static_cast<int32_t>(r[j])), sc, __uint_as_float(x[j])),
+                  bias_s[col0 + gc + j]));
+            }
+            tmem_st16_nowait(tmem_R + lane_off + col0 + gc, vb);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(acc_empty0);
+        if (uu == units - 1) {
+          // phase 2, while the MMA starts the next tile: residual, rounding,
+          // stores (and the fused SiLU) from the values in R
+#pragma unroll 1
+          for (int gc = 0; gc < 128; gc += 16) {
+            uint32_t vb[16];
+            tmem_ld16(tmem_R + lane_off + col0 + gc, vb);
+            const int nb = n0 + col0 + gc;
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = row_ok ? __uint_as_float(vb[j]) : 0.f;
+            if (row_ok && nb < e.N) {
               if (e.residual != nullptr) {
                 switch (e.out_dt) {
                   case DT_F16: fwd_add_residual16<__half>(e, m, nb, v, vec); break;
@@ -497,20 +593,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 case DT_BF16: fwd_store16<__nv_bfloat16>(e, m, nb, v, vec); break;
                 default: fwd_store16<float>(e, m, nb, v, vec); break;
               }
-              if (e.acc_i32 != nullptr) {
-                int32_t* dst = e.acc_i32 + m * static_cast<int64_t>(e.N);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  if (nb + j < e.N) dst[nb + j] = static_cast<int32_t>(r[j]);
+            }
+            if constexpr (kSilu) {
+              if (nb < e.N) {   // warp-uniform: every lane takes part in the column reduction
+                switch (e.out_dt) {
+                  case DT_F16: silu_epilogue16<__half>(e, m, nb, row_ok, v, vec, lane, colmax_s + col0 + gc); break;
+                  case DT_BF16:
+                    silu_epilogue16<__nv_bfloat16>(e, m, nb, row_ok, v, vec, lane, colmax_s + col0 + gc);
+                    break;
+                  default: silu_epilogue16<float>(e, m, nb, row_ok, v, vec, lane, colmax_s + col0 + gc); break;
+                }
               }
             }
             __syncwarp();
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(acc_empty0);
       }
+    }
+    if constexpr (kSilu) {
+      named_bar_sync(kBarEpi, kEpiThreads);   // every warp added the last tile's maxima
+      flush_colmax();
     }
   }
 
@@ -855,6 +957,7 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
 }
 
 int g_pairs_fwd[64] = {};   // resident pairs per device, per kernel
+int g_pairs_fwd_silu[64] = {};
 int g_pairs_bwd_fused[64] = {};
 int g_pairs_bwd_dq[64] = {};
 
@@ -938,7 +1041,7 @@ bool set_smem_attr(const void* fn, int smem_bytes, bool& done) {
 
 }  // namespace
 
-bool g_attr_fwd = false, g_attr_bwd_fused = false, g_attr_bwd_dq = false;
+bool g_attr_fwd = false, g_attr_fwd_silu = false, g_attr_bwd_fused = false, g_attr_bwd_dq = false;
 
 cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_bytes) {
   // the backward reports the schedule the workspace-sized default picks: fused
@@ -947,7 +1050,7 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
   bool* done = nullptr;
   int* cache = nullptr;
   if (kernel_id == K_FWD_GEMM) {
-    fn = reinterpret_cast<const void*>(fwd_gemm_kernel);
+    fn = reinterpret_cast<const void*>(fwd_gemm_kernel<false>);
     nthreads = kThreads;
     smem = kFwdSmemBytes;
     done = &g_attr_fwd;
@@ -980,19 +1083,23 @@ cudaError_t launch_widen_codes(const int8_t* CB, __half* CBh, int64_t n, cudaStr
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s) {
+template <bool kSilu>
+cudaError_t launch_fwd_variant(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s) {
   const int num_m = static_cast<int>(ceil_div(e.M, kPairM));
   const int num_n = static_cast<int>(ceil_div(e.N, kPairN));
   if (num_m == 0 || num_n == 0) return cudaSuccess;
-  if (!set_smem_attr(reinterpret_cast<const void*>(fwd_gemm_kernel), kFwdSmemBytes, g_attr_fwd))
-    return cudaGetLastError();
+  const void* fn = reinterpret_cast<const void*>(fwd_gemm_kernel<kSilu>);
+  if (!set_smem_attr(fn, kFwdSmemBytes, kSilu ? g_attr_fwd_silu : g_attr_fwd)) return cudaGetLastError();
   const int tiles = num_m * num_n;
-  const int clusters = std::min(
-      tiles, resident_pairs(reinterpret_cast<const void*>(fwd_gemm_kernel), kThreads, kFwdSmemBytes, g_pairs_fwd));
+  const int clusters = std::min(tiles, resident_pairs(fn, kThreads, kFwdSmemBytes, kSilu ? g_pairs_fwd_silu : g_pairs_fwd));
   const int group = std::min(num_m, 8);
   ProfScope ps(K_FWD_GEMM, s);
-  fwd_gemm_kernel<<<2 * clusters, kThreads, kFwdSmemBytes, s>>>(g, e, num_m, num_n, group);
+  fwd_gemm_kernel<kSilu><<<2 * clusters, kThreads, kFwdSmemBytes, s>>>(g, e, num_m, num_n, group);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s) {
+  return e.act != nullptr ? launch_fwd_variant<true>(g, e, s) : launch_fwd_variant<false>(g, e, s);
 }
 
 template <bool kFused>

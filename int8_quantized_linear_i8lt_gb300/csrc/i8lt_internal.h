@@ -82,6 +82,8 @@ struct FwdEpiArgs {
   void* out;
   int out_dt;
   int32_t* acc_i32;       // optional raw accumulator
+  void* act;              // optional: silu(out) [M, N] in out_dt (MLP hidden layer)
+  uint32_t* act_colmax;   // with act: per column max of |fp16(act)| bits, atomically raised
   DevStatus* st;
 };
 

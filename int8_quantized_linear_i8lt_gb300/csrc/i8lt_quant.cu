@@ -411,7 +411,6 @@ __global__ void __launch_bounds__(kThreads) grad_bias_finalize_kernel(const floa
 // ---------------------------------------------------------------------------
 // SiLU between MLP layers: y = h * sigmoid(h); dh = g * s * (1 + h (1 - s)).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) silu_kernel(const T* __restrict__ h, int64_t n, int vec,
@@ -422,7 +421,7 @@ __global__ void __launch_bounds__(kThreads) silu_kernel(const T* __restrict__ h,
     const bool v = vec != 0 && c + 8 <= n;
     load8_float(h + c, n - c, v, x);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = x[i] * sigmoidf_(x[i]);
+    for (int i = 0; i < 8; ++i) y[i] = silu_f(x[i]);
     store8(out + c, n - c, v, y);
   }
 }
@@ -438,7 +437,7 @@ __global__ void __launch_bounds__(kThreads) silu_backward_kernel(const T* __rest
     load8_float(g + c, n - c, v, gg);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float s = sigmoidf_(x[i]);
+      const float s = sigmoid_f(x[i]);
       y[i] = gg[i] * (s * (1.0f + x[i] * (1.0f - s)));
     }
     store8(out + c, n - c, v, y);

@@ -93,7 +93,7 @@ def backward_workspace(M: int, N: int, dtype: torch.dtype, device, K: int | None
 def forward(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, bias: torch.Tensor | None = None,
             threshold: float = 6.0, residual: torch.Tensor | None = None, max_outliers: int | None = None,
             out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
-            acc_i32: torch.Tensor | None = None, merge_colmax=None):
+            acc_i32: torch.Tensor | None = None, merge_colmax=None, colmax_ready: bool = False):
     """out [M, N] = int8 linear of A [M, K] (see i8lt_forward).  Returns
     (out, ws); ``ws`` holds the quantized activations and the outlier set.
 
@@ -101,37 +101,79 @@ def forward(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, bias: 
     K column maxima of this call's rows (an int32 view into ``ws``, ordered
     like the magnitudes) and replaces them in place with the maxima over
     all shards, e.g. an all-reduce MAX; the outlier set is then the whole
-    batch's (i8lt_forward_colmax / i8lt_forward_from_colmax)."""
+    batch's (i8lt_forward_colmax / i8lt_forward_from_colmax).
+    ``colmax_ready``: the column maxima of A are already in ``ws`` (written
+    by the previous layer's forward_silu); only the rest of the forward runs."""
     _require_cuda(A, CB, SCB, bias, residual)
     A = A.contiguous()
     M = A.shape[0]
     if A.shape[1] != K:
         raise I8LTError(f"A has {A.shape[1]} features, the weight {K}")
     N = CB.shape[0]
-    cap = default_max_outliers(K) if max_outliers is None else int(max_outliers)
-    if not (math.isfinite(threshold) and threshold > 0):
-        cap = 0
+    cap = _capacity(K, threshold, max_outliers)
     if out is None:
         out = torch.empty(M, N, dtype=A.dtype, device=A.device)
     if ws is None:
+        if colmax_ready:
+            raise I8LTError("colmax_ready needs the workspace that holds the column maxima")
         ws = forward_workspace(M, K, N, cap, A.device)
     if residual is not None:
         residual = residual.contiguous()
     bias_c = None if bias is None else bias.contiguous()
     args = (_ptr(bias_c), _code(bias_c.dtype) if bias_c is not None else 0, float(threshold),
             _ptr(residual), out.data_ptr(), ws.data_ptr(), ws.numel(), cap)
-    if merge_colmax is None:
+    if merge_colmax is None and not colmax_ready:
         _check(_lib.i8lt_forward(A.data_ptr(), _code(A.dtype), M, K, CB.data_ptr(), SCB.data_ptr(), N, *args,
                                  acc_i32=_ptr(acc_i32), stream=_stream(A)), "i8lt_forward")
         return out, ws
-    _check(_lib.i8lt_forward_colmax(A.data_ptr(), _code(A.dtype), M, K, N, ws.data_ptr(), ws.numel(), cap,
-                                    stream=_stream(A)), "i8lt_forward_colmax")
-    lay = _lib.i8lt_forward_workspace_layout(M, K, N, cap)
-    merge_colmax(ws[lay.colmax:lay.colmax + 4 * K].view(torch.int32))
+    if not colmax_ready:
+        _check(_lib.i8lt_forward_colmax(A.data_ptr(), _code(A.dtype), M, K, N, ws.data_ptr(), ws.numel(), cap,
+                                        stream=_stream(A)), "i8lt_forward_colmax")
+    if merge_colmax is not None:
+        lay = _lib.i8lt_forward_workspace_layout(M, K, N, cap)
+        merge_colmax(ws[lay.colmax:lay.colmax + 4 * K].view(torch.int32))
     _check(_lib.i8lt_forward_from_colmax(A.data_ptr(), _code(A.dtype), M, K, CB.data_ptr(), SCB.data_ptr(), N,
                                          *args, acc_i32=_ptr(acc_i32), stream=_stream(A)),
            "i8lt_forward_from_colmax")
     return out, ws
+
+
+def _capacity(K: int, threshold: float, max_outliers: int | None) -> int:
+    if not (math.isfinite(threshold) and threshold > 0):
+        return 0
+    return default_max_outliers(K) if max_outliers is None else int(max_outliers)
+
+
+def colmax_region(ws: torch.Tensor, M: int, K: int, N: int, threshold: float,
+                  max_outliers: int | None = None) -> torch.Tensor:
+    """The K column maxima of a forward workspace (int32 view)."""
+    lay = _lib.i8lt_forward_workspace_layout(M, K, N, _capacity(K, threshold, max_outliers))
+    return ws[lay.colmax:lay.colmax + 4 * K].view(torch.int32)
+
+
+def forward_silu(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor, K: int, bias: torch.Tensor | None = None,
+                 threshold: float = 6.0, max_outliers: int | None = None, act_colmax: torch.Tensor | None = None):
+    """MLP hidden layer (i8lt_forward_silu): returns (h, silu(h), ws).
+    ``act_colmax`` (int32 [N], e.g. ``colmax_region`` of the next layer's
+    workspace) receives the column maxima of |fp16(silu(h))|."""
+    _require_cuda(A, CB, SCB, bias)
+    A = A.contiguous()
+    M = A.shape[0]
+    if A.shape[1] != K:
+        raise I8LTError(f"A has {A.shape[1]} features, the weight {K}")
+    N = CB.shape[0]
+    cap = _capacity(K, threshold, max_outliers)
+    h = torch.empty(M, N, dtype=A.dtype, device=A.device)
+    a = torch.empty_like(h)
+    if act_colmax is None:
+        act_colmax = torch.empty(N, dtype=torch.int32, device=A.device)
+    ws = forward_workspace(M, K, N, cap, A.device)
+    bias_c = None if bias is None else bias.contiguous()
+    _check(_lib.i8lt_forward_silu(A.data_ptr(), _code(A.dtype), M, K, CB.data_ptr(), SCB.data_ptr(), N,
+                                  _ptr(bias_c), _code(bias_c.dtype) if bias_c is not None else 0, float(threshold),
+                                  None, h.data_ptr(), a.data_ptr(), act_colmax.data_ptr(), ws.data_ptr(), ws.numel(),
+                                  cap, stream=_stream(A)), "i8lt_forward_silu")
+    return h, a, ws
 
 
 def allreduce_colmax(group=None):
@@ -251,6 +293,15 @@ class SiLUFunction(torch.autograd.Function):
         return silu_backward(g, h)
 
 
+# MLP hidden layer: run the SiLU and fc2's column maxima inside fc1's GEMM
+# epilogue (i8lt_forward_silu) instead of as separate passes.  Same bits
+# either way.  Off by default: on GB300 the longer epilogue delays the
+# GEMM's next tile about as much as the two memory-bound passes it saves
+# cost (mlp_7b fc1 alone: 0.765 ms fused against 0.714 ms + 0.03 ms; the
+# whole block forward + backward: 2.857 ms against 2.866 ms).
+FUSED_SILU = False
+
+
 class Int8MLPFunction(torch.autograd.Function):
     """y = fc2(silu(fc1(x))) (+ x): the two int8 layers, the SiLU and the
     residual add (fused into fc2's epilogue forward, and into fc1's backward
@@ -262,10 +313,21 @@ class Int8MLPFunction(torch.autograd.Function):
         shape = x.shape
         K = shape[-1]
         x2 = x.reshape(-1, K)
-        h, _ = forward(x2, CB1, SCB1, K, b1, threshold, max_outliers=max_outliers)
-        a = silu(h)
-        y, _ = forward(a, CB2, SCB2, a.shape[1], b2, threshold, residual=x2 if residual else None,
-                       max_outliers=max_outliers)
+        H, N2 = CB1.shape[0], CB2.shape[0]
+        M = x2.shape[0]
+        res = x2 if residual else None
+        if FUSED_SILU:
+            # fc1's epilogue applies the SiLU and writes fc2's column maxima
+            # into fc2's workspace, so fc2 starts at its outlier index
+            ws2 = forward_workspace(M, H, N2, _capacity(H, threshold, max_outliers), x.device)
+            h, a, _ = forward_silu(x2, CB1, SCB1, K, b1, threshold, max_outliers=max_outliers,
+                                   act_colmax=colmax_region(ws2, M, H, N2, threshold, max_outliers))
+            y, _ = forward(a, CB2, SCB2, H, b2, threshold, residual=res, max_outliers=max_outliers, ws=ws2,
+                           colmax_ready=True)
+        else:
+            h, _ = forward(x2, CB1, SCB1, K, b1, threshold, max_outliers=max_outliers)
+            a = silu(h)
+            y, _ = forward(a, CB2, SCB2, H, b2, threshold, residual=res, max_outliers=max_outliers)
         ctx.save_for_backward(CB1, SCB1, CB2, SCB2, h)
         ctx.K = K
         ctx.H = CB1.shape[0]

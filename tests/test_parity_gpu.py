@@ -333,9 +333,49 @@ def test_workload_mlp(name):
             with torch.no_grad():
                 fc.bias.copy_(bb.to(DEV))
         mlp = I.Int8MLP(fc1, fc2, residual=wl.residual)
-        xr = xd.clone().requires_grad_(True)
-        y = mlp(xr)
-        y.backward(Gd)
-        assert torch.equal(y.detach(), g2["out"])
-        assert torch.equal(xr.grad, gx)
-        assert torch.equal(fc1.bias.grad, gb1) and torch.equal(fc2.bias.grad, gb2)
+        for fused in (False, True):          # SiLU as its own pass, or in fc1's epilogue
+            I.functional.FUSED_SILU = fused
+            try:
+                xr = xd.clone().requires_grad_(True)
+                fc1.bias.grad = fc2.bias.grad = None
+                y = mlp(xr)
+                y.backward(Gd)
+            finally:
+                I.functional.FUSED_SILU = False
+            assert torch.equal(y.detach(), g2["out"])
+            assert torch.equal(xr.grad, gx)
+            assert torch.equal(fc1.bias.grad, gb1) and torch.equal(fc2.bias.grad, gb2)
+
+
+@pytest.mark.parametrize("M,K,H,N2,dtype,thr", [(300, 256, 1100, 256, torch.float16, 6.0),
+                                                (129, 512, 640, 200, torch.bfloat16, 6.0),
+                                                (600, 4, 16, 4, torch.float32, math.inf)])
+def test_fused_silu_epilogue_matches_the_unfused_chain(M, K, H, N2, dtype, thr):
+    """MLP hidden layer: i8lt_forward_silu's h and silu(h) equal i8lt_forward
+    followed by i8lt_silu_forward bit for bit, its column maxima equal
+    i8lt_forward_colmax on silu(h), and the next layer run from them equals
+    the next layer run on its own."""
+    s1 = W.LayerSpec(M, K, H, dtype, 0.05, 0.01, 0.01, 12.0, thr)
+    s2 = W.LayerSpec(M, H, N2, dtype, 0.05, 0.01, 0.0, 1.0, thr)
+    wl = W.Workload("mlp", "", (s1, s2), kind="mlp", w_dtype=dtype)
+    x = W.activation(s1, 21).to(DEV)
+    W1, b1, _ = W.layer_tensors(wl, 0, 21)
+    W2, b2, _ = W.layer_tensors(wl, 1, 21)
+    CB1, SCB1 = I.quantize_weight(W1.to(DEV))
+    CB2, SCB2 = I.quantize_weight(W2.to(DEV))
+    b1, b2 = b1.to(DEV), b2.to(DEV)
+    F = I.functional
+    h_ref, _ = I.forward(x, CB1, SCB1, K, b1, thr)
+    a_ref = F.silu(h_ref)
+    y_ref, _ = I.forward(a_ref, CB2, SCB2, H, b2, thr)
+    ws2 = F.forward_workspace(M, H, N2, F._capacity(H, thr, None), x.device)
+    colmax = F.colmax_region(ws2, M, H, N2, thr)
+    h, a, _ = F.forward_silu(x, CB1, SCB1, K, b1, thr, act_colmax=colmax)
+    assert torch.equal(h.view(torch.uint8), h_ref.view(torch.uint8))
+    assert torch.equal(a.view(torch.uint8), a_ref.view(torch.uint8))
+    ws_chk = F.forward_workspace(M, H, N2, F._capacity(H, thr, None), x.device)
+    assert _lib.i8lt_forward_colmax(a.data_ptr(), F.DTYPE_CODE[dtype], M, H, N2, ws_chk.data_ptr(), ws_chk.numel(),
+                                    F._capacity(H, thr, None), torch.cuda.current_stream().cuda_stream) == 0
+    assert torch.equal(colmax, F.colmax_region(ws_chk, M, H, N2, thr))
+    y, _ = I.forward(a, CB2, SCB2, H, b2, thr, ws=ws2, colmax_ready=True)
+    assert torch.equal(y.view(torch.uint8), y_ref.view(torch.uint8))
