@@ -321,6 +321,35 @@ def backward_input(G, dtype, CB, SCB, addend=None, rows=None):
     return dict(G16=G16, Wdq=Wdq, grad64=acc, grad_A=round_to(acc, dtype))
 
 
+def quantize_cols(X16: np.ndarray):
+    """Column-wise (vector-wise along the tokens) absmax int8 quantization of
+    a token-major matrix X16 [M, C] (fp16 values): SC[c] = max_m |X16[m, c]|
+    (fp32), Xt[c, m] = round_half_even(fp32(X16[m, c]) * (127 / SC[c])),
+    returned transposed (C x M), the layout whose rows the weight-gradient
+    product contracts.  It is the row-wise quantization of the transpose."""
+    Xt = np.ascontiguousarray(X16.T).astype(np.float32)
+    SC = (np.abs(Xt).max(axis=1) if Xt.shape[1] else np.zeros(Xt.shape[0])).astype(np.float32)
+    return SC, _codes(Xt, SC)
+
+
+def grad_weight(G, A, dtype):
+    """Weight gradient of the trainable-weight mode (has_fp16_weights=True):
+    grad_W[n, k] = sum_m G[m, n] A[m, k] with both operands quantized column
+    by column (scales per output feature n and per input feature k, taken
+    over the tokens), an exact int32 product of the codes, and the dequant
+    SCG[n] * SCA[k] / 127^2 in float64, rounded once to ``dtype``.
+
+    ``G`` [M, N] and ``A`` [M, K] in ``dtype`` storage; both are cast to fp16
+    first, like every quantized operand of the layer."""
+    G16 = cast_f16(G, dtype)
+    A16 = cast_f16(A, dtype)
+    SCG, Gt = quantize_cols(G16)
+    SCA, At = quantize_cols(A16)
+    Cacc = int_gemm(Gt, At)
+    acc = Cacc.astype(np.float64) * (SCG.astype(np.float64)[:, None] * SCA.astype(np.float64)[None, :]) / _Q2
+    return dict(SCG=SCG, Gt=Gt, SCA=SCA, At=At, Cacc=Cacc, grad64=acc, grad_W=round_to(acc, dtype))
+
+
 # ---------------------------------------------------------------------------
 # SiLU between the two layers of the MLP workloads (float64, one rounding)
 # ---------------------------------------------------------------------------

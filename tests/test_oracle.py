@@ -431,3 +431,72 @@ def test_tiny_mlp_deviation_matches_the_printed_example():
         devs.append(float(np.abs(y.astype(np.float64) - y64).mean() / np.abs(y64).mean()))
     dev = float(np.mean(devs))
     assert ref / 4 < dev < ref * 4, (dev, ref)
+
+
+# ---------------------------------------------------------------------------
+# weight gradient of the trainable-weight mode (column-wise quantization)
+# ---------------------------------------------------------------------------
+
+def test_quantize_cols_bruteforce():
+    rng = np.random.default_rng(31)
+    X = (rng.standard_normal((9, 6)) * 3).astype(np.float16)
+    X[:, 4] = 0                   # an all-zero column: scale 0, codes 0
+    SC, Xt = O.quantize_cols(X)
+    assert Xt.shape == (6, 9)
+    for c in range(6):
+        col = [float(X[m, c]) for m in range(9)]
+        am = max(abs(v) for v in col)
+        assert SC[c] == am
+        assert Xt[c].tolist() == py_codes(col, am)
+
+
+def test_grad_weight_bruteforce():
+    rng = np.random.default_rng(32)
+    M, N, K = 7, 5, 6
+    G = (rng.standard_normal((M, N))).astype(np.float16)
+    A = (rng.standard_normal((M, K)) * 2).astype(np.float16)
+    r = O.grad_weight(G, A, O.F16)
+    for n in range(N):
+        gcol = [float(G[m, n]) for m in range(M)]
+        gam = max(abs(v) for v in gcol)
+        gq = py_codes(gcol, gam)
+        for k in range(K):
+            acol = [float(A[m, k]) for m in range(M)]
+            aam = max(abs(v) for v in acol)
+            aq = py_codes(acol, aam)
+            c = sum(x * y for x, y in zip(gq, aq))
+            assert r["Cacc"][n, k] == c
+            assert r["grad64"][n, k] == c * gam * aam / 16129.0
+
+
+def test_grad_weight_lossless_exact():
+    # G = (codes x power-of-two steps per column), A likewise, +-127 in every
+    # column: the column-wise quantization is lossless, so grad_W must be the
+    # exact product G^T A rounded once
+    M, N, K = 40, 12, 20
+    case = W.lossless_case(N, M, K, seed=33)          # rows of A' / W' are the columns of G / A
+    G = case["A"].numpy().T.copy()
+    A = case["W"].numpy().T.copy()
+    r = O.grad_weight(G, A, O.F16)
+    assert np.array_equal(r["Gt"], case["qa"].numpy().astype(np.int8))
+    assert np.array_equal(r["At"], case["qw"].numpy().astype(np.int8))
+    exact = G.astype(np.float64).T @ A.astype(np.float64)
+    assert np.array_equal(r["grad64"], exact)
+    assert np.array_equal(r["grad_W"], O.round_to(exact, O.F16))
+
+
+def test_grad_weight_error_bound():
+    # generic inputs: |grad_W - G^T A| within the column quantization errors
+    spec = W.LayerSpec(64, 48, 24, torch.float16, 0.02, 0.01)
+    A = O.cast_f16(W.activation(spec, 34).numpy(), O.F16)
+    G = O.cast_f16((np.random.default_rng(34).standard_normal((64, 24))).astype(np.float16), O.F16)
+    r = O.grad_weight(G, A, O.F16)
+    exact = G.astype(np.float64).T @ A.astype(np.float64)
+    eg = r["SCG"].astype(np.float64) / 254          # |g - dq(g)| <= SCG / 254 per element
+    ea = r["SCA"].astype(np.float64) / 254
+    M = G.shape[0]
+    bound = (eg[:, None] * np.abs(A.astype(np.float64)).sum(0)[None, :]
+             + ea[None, :] * np.abs(G.astype(np.float64)).sum(0)[:, None]
+             + M * eg[:, None] * ea[None, :]) * (1 + 1e-6)
+    assert np.all(np.abs(r["grad64"] - exact) <= bound)
+    assert np.abs(r["grad64"] - exact).max() > 0      # generic inputs do lose precision
