@@ -163,7 +163,7 @@ class Layer:
         wdt = wl.w_dtype or spec.dtype
         Wf = (torch.randn(spec.N, spec.K, device=gen_dev) * spec.w_std).to(wdt)
         self.CB, self.SCB = I.quantize_weight(Wf)
-        del Wf
+        self.W = Wf                           # the float weight of the trainable-weight mode
         self.bias = (torch.randn(spec.N, device=gen_dev) * (spec.bias_std or 0.0)).to(wdt)
         self.G = torch.randn(spec.M, spec.N, device=gen_dev).to(spec.dtype)
         cap = I.default_max_outliers(spec.K)
@@ -310,6 +310,8 @@ def run_ours(args):
         kernels[k] = e
     # --- end to end through host buffers (pinned), inputs and results copied each step
     e2e = run_e2e(layers, stream, max(2, min(args.steps, 10)), device)
+    # --- the trainable-weight mode on the same layers (context, not the headline)
+    trainable = time_trainable(layers, stream, max(2, min(args.steps, 10)), device)
     # --- the same step with the other backward schedule (context, not the headline)
     alt = time_schedule(layers, stream, max(2, min(args.steps, 10)), device, not mat)
 
@@ -329,6 +331,7 @@ def run_ours(args):
         "bwd_schedule": args.bwd_schedule,
         **({"mlp_chain": time_mlp_chain(wl, layers, stream, max(2, min(args.steps, 10)), device)}
            if wl.kind == "mlp" and len(layers) == 2 else {}),
+        "trainable_mode": trainable,
         ("bwd_fused" if mat else "bwd_materialized"): alt,
         "gpu_launches": n_launches,
         "gemm_launch": {k: dict(zip(("status", "ctas", "threads", "smem"), _lib.i8lt_gemm_launch_info(k)))
@@ -363,6 +366,57 @@ def launches_per_layer(L, materialized=False) -> int:
     import math
     fwd = 6 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 3
     return fwd + (4 if materialized else 3)
+
+
+def time_trainable(layers, stream, steps, device):
+    """The trainable-weight mode (has_fp16_weights=True) on the same layers:
+    per layer and step the weight is quantized afresh, then the forward,
+    grad_A (fused schedule), grad_bias and grad_W (int8 column-wise
+    product).  Ops counted: 6 M N K per layer (three GEMMs)."""
+    from int8_quantized_linear_i8lt_gb300 import _lib
+    from int8_quantized_linear_i8lt_gb300.functional import DTYPE_CODE
+    sp = stream.cuda_stream
+    extra = []
+    for L in layers:
+        s = L.spec
+        gW = torch.empty(s.N, s.K, dtype=L.W.dtype, device=device)
+        wsw = torch.empty(_lib.i8lt_grad_weight_workspace_size(s.M, s.N, s.K), dtype=torch.uint8, device=device)
+        extra.append((gW, wsw))
+
+    def step():
+        for L, (gW, wsw) in zip(layers, extra):
+            s = L.spec
+            st = _lib.i8lt_quantize_weight(L.W.data_ptr(), DTYPE_CODE[L.W.dtype], s.N, s.K, L.CB.data_ptr(),
+                                           L.SCB.data_ptr(), sp)
+            assert st == 0, _lib.i8lt_status_string(st)
+            _launch_layer(L, sp)
+            st = _lib.i8lt_grad_weight(L.G.data_ptr(), DTYPE_CODE[s.dtype], L.A.data_ptr(), DTYPE_CODE[s.dtype], s.M,
+                                       s.N, s.K, gW.data_ptr(), DTYPE_CODE[L.W.dtype], wsw.data_ptr(), wsw.numel(), sp)
+            assert st == 0, _lib.i8lt_status_string(st)
+
+    step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _lib.i8lt_profile_start(1 << 16)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    _, recs, _ = _lib.i8lt_profile_stop(1 << 16)
+    ms = reduce_max(ev0.elapsed_time(ev1), device)
+    ops = reduce_sum(sum(6.0 * L.spec.M * L.spec.N * L.spec.K for L in layers) * steps, device)
+    wg_ms = sum(t for n, t in recs if n == "wgrad_gemm")
+    cq_ms = sum(t for n, t in recs if n == "col_quantize")
+    qw_ms = sum(t for n, t in recs if n == "quantize_weight")
+    flops = sum(2.0 * L.spec.M * L.spec.N * L.spec.K for L in layers) * steps
+    peaks, _ = load_peaks()
+    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    wg_tf = flops / (wg_ms * 1e-3) / 1e12 if wg_ms else None
+    return {"value": round(ops / (ms * 1e-3) / 1e12, 2), "unit": "TOPS", "ms_per_step": round(ms / steps, 3),
+            "steps": steps, "wgrad_gemm_tflops": round(wg_tf, 1) if wg_tf else None,
+            "wgrad_gemm_frac_tensor": round(wg_tf / peak_t, 4) if wg_tf else None,
+            "col_quantize_ms_per_step": round(cq_ms / steps, 4), "quantize_weight_ms_per_step": round(qw_ms / steps, 4)}
 
 
 def time_mlp_chain(wl, layers, stream, steps, device):

@@ -272,6 +272,26 @@ int i8lt_backward_input_noalloc(const void* G, int gt, int64_t M, int64_t N,
                                 const void* addend, void* grad_A,
                                 void* grad_bias, int bt, void* stream);
 
+/*
+ * Weight gradient of the trainable-weight mode (bitsandbytes'
+ * has_fp16_weights=True: the float weight is the parameter and is quantized
+ * afresh on every forward with i8lt_quantize_weight):
+ *   grad_W [N, K] dtype `wt` = sum over the M tokens of G[m, n] A[m, k],
+ * computed in int8: G [M, N] (dtype gt) and A [M, K] (dtype at), both cast to
+ * fp16, are quantized column by column -- one absmax scale per output
+ * feature n and per input feature k, taken over the tokens -- the codes are
+ * multiplied exactly (int32, so M <= I8LT_MAX_K, else I8LT_ERR_K_TOO_LARGE)
+ * and grad_W = Cacc * scale_G[n] * scale_A[k] / 127^2, rounded once.  The
+ * per-column scales keep an outlier feature from spoiling the others, so no
+ * separate outlier product is taken.  Interface addition: the pages' layer
+ * runs in the memory-efficient mode, where the weight is frozen.
+ *   ws  at least i8lt_grad_weight_workspace_size(M, N, K) bytes
+ */
+size_t i8lt_grad_weight_workspace_size(int64_t M, int64_t N, int64_t K);
+int i8lt_grad_weight(const void* G, int gt, const void* A, int at,
+                     int64_t M, int64_t N, int64_t K,
+                     void* grad_W, int wt, void* ws, size_t ws_bytes, void* stream);
+
 /* SiLU between the two layers of an MLP: out = h * sigmoid(h), and its
  * backward out = g * silu'(h).  n elements of dtype dt. */
 int i8lt_silu_forward(const void* h, int dt, int64_t n, void* out, void* stream);
@@ -290,7 +310,7 @@ typedef enum {
   I8LT_K_QUANTIZE_WEIGHT = 0, I8LT_K_COLMAX = 1, I8LT_K_OUTLIER_INDEX = 2, I8LT_K_ROW_QUANTIZE = 3,
   I8LT_K_SUBB = 4, I8LT_K_FWD_GEMM = 5, I8LT_K_GRADOUT_PREPASS = 6, I8LT_K_GRAD_BIAS_FINALIZE = 7,
   I8LT_K_BWD_GEMM = 8, I8LT_K_SILU = 9, I8LT_K_SILU_BACKWARD = 10, I8LT_K_WIDEN_CODES = 11,
-  I8LT_K_DEQUANT_WEIGHT = 12, I8LT_K_COUNT = 13
+  I8LT_K_DEQUANT_WEIGHT = 12, I8LT_K_COL_QUANTIZE = 13, I8LT_K_WGRAD_GEMM = 14, I8LT_K_COUNT = 15
 } i8lt_kernel_id;
 typedef struct {
   int kernel;

@@ -10,11 +10,12 @@
 The arithmetic runs in libi8lt.so (hand-written CUDA for sm_103a, C ABI in
 include/i8lt.h); build it with ``python -m int8_quantized_linear_i8lt_gb300.build``.
 """
-from .functional import (I8LTError, Int8LinearFunction, Int8MLPFunction, SiLUFunction, backward_input,
-                         default_max_outliers, device_status, forward, quantize_weight, silu, silu_backward,
-                         weight_ld)
-from .module import Int8MLP, Linear8bitLt
+from .functional import (I8LTError, Int8LinearFunction, Int8LinearTrainableFunction, Int8MLPFunction, SiLUFunction,
+                         backward_input, default_max_outliers, device_status, forward, grad_weight, quantize_weight,
+                         silu, silu_backward, weight_ld)
+from .module import Int8MLP, Linear8bitLt, Linear8bitLtTrainable
 
-__all__ = ["Linear8bitLt", "Int8MLP", "I8LTError", "Int8LinearFunction", "Int8MLPFunction", "SiLUFunction",
-           "forward", "backward_input", "quantize_weight", "silu", "silu_backward", "device_status",
-           "default_max_outliers", "weight_ld"]
+__all__ = ["Linear8bitLt", "Linear8bitLtTrainable", "Int8MLP", "I8LTError", "Int8LinearFunction",
+           "Int8LinearTrainableFunction", "Int8MLPFunction", "SiLUFunction", "forward", "backward_input",
+           "grad_weight", "quantize_weight", "silu", "silu_backward", "device_status", "default_max_outliers",
+           "weight_ld"]

@@ -49,7 +49,7 @@ class i8lt_kernel_time(Structure):
 
 KERNELS = ("quantize_weight", "colmax", "outlier_index", "row_quantize", "build_subB", "fwd_gemm",
            "gradout_prepass", "grad_bias_finalize", "bwd_gemm", "silu", "silu_backward", "widen_codes",
-           "dequant_weight")
+           "dequant_weight", "col_quantize", "wgrad_gemm")
 
 
 # name -> (restype, argtypes); the same names and order as include/i8lt.h
@@ -72,6 +72,9 @@ SIGNATURES = {
                                          c_void_p, c_int, c_float, c_void_p, c_void_p,
                                          c_void_p, c_size_t, c_int64, POINTER(i8lt_fwd_debug), c_void_p]),
     "i8lt_backward_workspace_size": (c_size_t, [c_int64, c_int64, c_int]),
+    "i8lt_grad_weight_workspace_size": (c_size_t, [c_int64, c_int64, c_int64]),
+    "i8lt_grad_weight": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int64, c_int64, c_int64, c_void_p, c_int,
+                                 c_void_p, c_size_t, c_void_p]),
     "i8lt_backward_workspace_size_dq": (c_size_t, [c_int64, c_int64, c_int64, c_int]),
     "i8lt_backward_input": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
                                     c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
@@ -171,6 +174,14 @@ def i8lt_forward_from_colmax(A, at, M, K, CB, SCB, N, bias, bt, threshold, resid
     dbg = ctypes.byref(i8lt_fwd_debug(_p(acc_i32))) if acc_i32 else None
     return load().i8lt_forward_from_colmax(_p(A), at, M, K, _p(CB), _p(SCB), N, _p(bias), bt, c_float(threshold),
                                            _p(residual), _p(out), _p(ws), ws_bytes, max_outliers, dbg, _p(stream))
+
+
+def i8lt_grad_weight_workspace_size(M, N, K) -> int:
+    return load().i8lt_grad_weight_workspace_size(M, N, K)
+
+
+def i8lt_grad_weight(G, gt, A, at, M, N, K, grad_W, wt, ws, ws_bytes, stream=None) -> int:
+    return load().i8lt_grad_weight(_p(G), gt, _p(A), at, M, N, K, _p(grad_W), wt, _p(ws), ws_bytes, _p(stream))
 
 
 def i8lt_backward_workspace_size(M, N, gt) -> int:

@@ -135,6 +135,42 @@ BwdLayout bwd_layout(int64_t M, int64_t N, int64_t K, int gt) {
   return L;
 }
 
+// Weight-gradient workspace (trainable-weight mode):
+// [status][colmax G, N][colmax A, K][scale G, N][scale A, K][rowsmall G, N]
+// [l1 G, N x chunks][Gt fp16, N x R_pad][At fp16, K x R_pad], R_pad = M
+// rounded up to 16 (the reduction dimension of the GEMM).
+struct WgradLayout {
+  size_t status, colmax_g, colmax_a, scale_g, scale_a, rowsmall_g, l1_g, gt, at, total;
+  int64_t r_pad, chunks;
+};
+
+WgradLayout wgrad_layout(int64_t M, int64_t N, int64_t K) {
+  WgradLayout L;
+  L.r_pad = round_up(M, 16);
+  L.chunks = ceil_div(L.r_pad, 1024);
+  size_t off = 0;
+  L.status = off;
+  off += kAlign;
+  L.colmax_g = off;
+  off += align_up(static_cast<size_t>(N) * 4);
+  L.colmax_a = off;
+  off += align_up(static_cast<size_t>(K) * 4);
+  L.scale_g = off;
+  off += align_up(static_cast<size_t>(N) * 4);
+  L.scale_a = off;
+  off += align_up(static_cast<size_t>(K) * 4);
+  L.rowsmall_g = off;
+  off += align_up(static_cast<size_t>(N));
+  L.l1_g = off;
+  off += align_up(static_cast<size_t>(N) * L.chunks * 4);
+  L.gt = off;
+  off += align_up(static_cast<size_t>(N) * L.r_pad * 2);
+  L.at = off;
+  off += align_up(static_cast<size_t>(K) * L.r_pad * 2);
+  L.total = off;
+  return L;
+}
+
 // ---- kernel timing --------------------------------------------------------
 struct ProfRec {
   int id;
@@ -433,6 +469,74 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_
   return cuda_status(launch_bwd_gemm(g, ea, !materialize, s));
 }
 
+size_t i8lt_grad_weight_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return 0;
+  return wgrad_layout(M, N, K).total;
+}
+
+int i8lt_grad_weight(const void* G, int gt, const void* A, int at, int64_t M, int64_t N, int64_t K, void* grad_W,
+                     int wt, void* ws, size_t ws_bytes, void* stream) {
+  if (!valid_dt(gt) || !valid_dt(at) || !valid_dt(wt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (M < 0 || N <= 0 || K <= 0) return I8LT_ERR_INVALID_ARG;
+  if (round_up(M, 16) > I8LT_MAX_K) return I8LT_ERR_K_TOO_LARGE;   // the tokens are the reduction
+  if (N > INT32_MAX / 2 || K > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
+  if (grad_W == nullptr || ws == nullptr || (M > 0 && (G == nullptr || A == nullptr))) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(G) || !aligned16(A) || !aligned16(grad_W)) return I8LT_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
+  const WgradLayout L = wgrad_layout(M, N, K);
+  if (ws_bytes < L.total) return I8LT_ERR_WORKSPACE;
+  if (int d = check_device()) return d;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  // one memset: status, both column maxima; another: the l1 sums
+  if (cudaMemsetAsync(w, 0, L.scale_g, s) != cudaSuccess) return I8LT_ERR_CUDA;
+  if (M == 0) {
+    const size_t bytes = static_cast<size_t>(N) * K * (wt == DT_F32 ? 4 : 2);
+    return cuda_status(cudaMemsetAsync(grad_W, 0, bytes, s));
+  }
+  if (cudaMemsetAsync(w + L.l1_g, 0, static_cast<size_t>(N) * L.chunks * 4, s) != cudaSuccess) return I8LT_ERR_CUDA;
+  DevStatus* st = reinterpret_cast<DevStatus*>(w + L.status);
+  uint32_t* cm_g = reinterpret_cast<uint32_t*>(w + L.colmax_g);
+  uint32_t* cm_a = reinterpret_cast<uint32_t*>(w + L.colmax_a);
+  float* sc_g = reinterpret_cast<float*>(w + L.scale_g);
+  float* sc_a = reinterpret_cast<float*>(w + L.scale_a);
+  uint8_t* small_g = w + L.rowsmall_g;
+  int* l1_g = reinterpret_cast<int*>(w + L.l1_g);
+  __half* Gt = reinterpret_cast<__half*>(w + L.gt);
+  __half* At = reinterpret_cast<__half*>(w + L.at);
+  if (launch_colmax(G, gt, M, N, (N % 8) == 0, cm_g, s) != cudaSuccess ||
+      launch_colmax(A, at, M, K, (K % 8) == 0, cm_a, s) != cudaSuccess ||
+      launch_col_quantize(G, gt, M, N, (N % 8) == 0, cm_g, L.r_pad, sc_g, Gt, l1_g, small_g, s) != cudaSuccess ||
+      launch_col_quantize(A, at, M, K, (K % 8) == 0, cm_a, L.r_pad, sc_a, At, nullptr, nullptr, s) != cudaSuccess)
+    return I8LT_ERR_CUDA;
+  // grad_W[n, k] = sum_m Gt[n, m] At[k, m] * scale_g[n] * scale_a[k] / 127^2: the
+  // forward GEMM with the tokens as its reduction dimension
+  FwdGemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  if (!make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Gt, L.r_pad, N, L.r_pad * 2, kBK, kBoxRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, At, L.r_pad, K, L.r_pad * 2, kBK, kBoxRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return I8LT_ERR_CUDA;
+  FwdEpiArgs ea;
+  std::memset(&ea, 0, sizeof(ea));
+  ea.M = static_cast<int>(N);
+  ea.N = static_cast<int>(K);
+  ea.K_pad = static_cast<int>(L.r_pad);
+  ea.use_outliers = 0;
+  ea.SCA = sc_g;
+  ea.rowsmall = small_g;
+  ea.SCB = sc_a;
+  ea.bias = nullptr;
+  ea.bias_dt = 0;
+  ea.residual = nullptr;
+  ea.out = grad_W;
+  ea.out_dt = wt;
+  ea.acc_i32 = nullptr;
+  ea.st = st;
+  return cuda_status(launch_fwd_gemm(g, ea, s, K_WGRAD_GEMM));
+}
+
 int i8lt_silu_forward(const void* h, int dt, int64_t n, void* out, void* stream) {
   if (!valid_dt(dt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
   if (n < 0 || (n > 0 && (h == nullptr || out == nullptr))) return I8LT_ERR_INVALID_ARG;
@@ -490,7 +594,7 @@ const char* i8lt_kernel_name(int k) {
   static const char* names[] = {"quantize_weight", "colmax",          "outlier_index",      "row_quantize",
                                 "build_subB",      "fwd_gemm",        "gradout_prepass",    "grad_bias_finalize",
                                 "bwd_gemm",        "silu",            "silu_backward",      "widen_codes",
-                                "dequant_weight"};
+                                "dequant_weight",  "col_quantize",    "wgrad_gemm"};
   return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
 }
 

@@ -1084,7 +1084,7 @@ cudaError_t launch_widen_codes(const int8_t* CB, __half* CBh, int64_t n, cudaStr
 }
 
 template <bool kSilu>
-cudaError_t launch_fwd_variant(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s) {
+cudaError_t launch_fwd_variant(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s, int prof_id) {
   const int num_m = static_cast<int>(ceil_div(e.M, kPairM));
   const int num_n = static_cast<int>(ceil_div(e.N, kPairN));
   if (num_m == 0 || num_n == 0) return cudaSuccess;
@@ -1093,13 +1093,14 @@ cudaError_t launch_fwd_variant(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaSt
   const int tiles = num_m * num_n;
   const int clusters = std::min(tiles, resident_pairs(fn, kThreads, kFwdSmemBytes, kSilu ? g_pairs_fwd_silu : g_pairs_fwd));
   const int group = std::min(num_m, 8);
-  ProfScope ps(K_FWD_GEMM, s);
+  ProfScope ps(prof_id, s);
   fwd_gemm_kernel<kSilu><<<2 * clusters, kThreads, kFwdSmemBytes, s>>>(g, e, num_m, num_n, group);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s) {
-  return e.act != nullptr ? launch_fwd_variant<true>(g, e, s) : launch_fwd_variant<false>(g, e, s);
+cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s, int prof_id) {
+  static_assert(K_FWD_GEMM == 5, "default profile id of launch_fwd_gemm");
+  return e.act != nullptr ? launch_fwd_variant<true>(g, e, s, prof_id) : launch_fwd_variant<false>(g, e, s, prof_id);
 }
 
 template <bool kFused>

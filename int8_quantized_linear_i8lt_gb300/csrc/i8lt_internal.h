@@ -58,6 +58,13 @@ cudaError_t launch_gradout_prepass(const void* G, int gt, int64_t M, int64_t N, 
 int64_t gradout_partial_chunks(int64_t M);
 
 cudaError_t launch_silu(const void* h, int dt, int64_t n, bool vec, void* out, cudaStream_t s);
+
+// Trainable-weight mode: column-wise quantization of X [R, C] (dtype xt) into
+// Xt [C, R_pad] fp16 codes and scale [C], from the column maxima colmax [C]
+// (launch_colmax).  With l1 ([C, ceil(R_pad / 1024)] int32, zeroed) and
+// rowsmall ([C]): the fast-drain flags of the GEMM rows c.
+cudaError_t launch_col_quantize(const void* X, int xt, int64_t R, int64_t C, bool vec, const uint32_t* colmax,
+                                int64_t R_pad, float* scale, __half* Xt, int* l1, uint8_t* rowsmall, cudaStream_t s);
 cudaError_t launch_silu_backward(const void* g, const void* h, int dt, int64_t n, bool vec, void* out,
                                  cudaStream_t s);
 
@@ -87,7 +94,7 @@ struct FwdEpiArgs {
   DevStatus* st;
 };
 
-cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s);
+cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s, int prof_id = 5 /*K_FWD_GEMM*/);
 
 // Forward prepass: CBh[i] = fp16(CB[i]) (exact) for n (multiple of 16) codes.
 cudaError_t launch_widen_codes(const int8_t* CB, __half* CBh, int64_t n, cudaStream_t s);
@@ -123,7 +130,8 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
 // Kernel ids of the timing records (match i8lt_kernel_id in i8lt.h).
 enum KernelId {
   K_QUANTIZE_WEIGHT = 0, K_COLMAX, K_OUTLIER_INDEX, K_ROW_QUANTIZE, K_SUBB, K_FWD_GEMM, K_GRADOUT_PREPASS,
-  K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_WIDEN_CODES, K_DEQUANT_WEIGHT, K_COUNT
+  K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_WIDEN_CODES, K_DEQUANT_WEIGHT, K_COL_QUANTIZE,
+  K_WGRAD_GEMM, K_COUNT
 };
 
 // Box sizes of the tensor maps (each CTA of a pair stages 128 rows of each

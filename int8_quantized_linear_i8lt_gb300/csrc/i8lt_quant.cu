@@ -444,6 +444,97 @@ __global__ void __launch_bounds__(kThreads) silu_backward_kernel(const T* __rest
   }
 }
 
+// ---------------------------------------------------------------------------
+// Trainable-weight mode: column-wise (vector-wise along the tokens) absmax
+// quantization of a token-major X [R, C], written transposed, Xt [C, R_pad]
+// as exact fp16 codes (the K-major operand rows of the weight-gradient GEMM):
+// scale[c] = max_r |fp16(X[r, c])| (the colmax kernel's bits), Xt[c, r] =
+// rint(fp32(fp16(X[r, c])) * (127 / scale[c])), 0 for R <= r < R_pad.  One
+// block per 64 (r) x 64 (c) tile: coalesced 16-byte loads of 8 columns, the
+// codes transposed through shared memory, 16-byte stores of 8 tokens.  With
+// `l1` it also adds the sum of |code| of each column over the tile's rows
+// to l1[c, r / 1024] (the fast-drain test of the GEMM's rows).
+// ---------------------------------------------------------------------------
+constexpr int kCqTile = 64;
+constexpr int kCqPitch = kCqTile + 2;   // halves; a 132-byte row keeps the transposed writes at 2-way
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) col_quantize_kernel(const T* __restrict__ X, int64_t R, int64_t C, int vec,
+                                                                const uint32_t* __restrict__ colmax, int64_t R_pad,
+                                                                float* __restrict__ scale, __half* __restrict__ Xt,
+                                                                int* __restrict__ l1, int64_t nchunks) {
+  __shared__ __align__(16) __half tile[kCqTile * kCqPitch];   // [c][r]
+  __shared__ float s_s[kCqTile];
+  __shared__ int l1_s[kCqTile];
+  const int t = threadIdx.x, lane = t & 31;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kCqTile;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kCqTile;
+  if (t < kCqTile) {
+    const int64_t c = c0 + t;
+    const float am = c < C ? __half2float(__ushort_as_half(static_cast<unsigned short>(colmax[c]))) : 0.f;
+    s_s[t] = am > 0.f ? __fdiv_rn(127.0f, am) : 0.f;
+    l1_s[t] = 0;
+    if (blockIdx.x == 0 && c < C) scale[c] = am;
+  }
+  __syncthreads();
+  const int cg = (t & 7) * 8;              // 8 consecutive columns
+  int l1c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int rl = (t >> 3) + 32 * i;
+    const int64_t r = r0 + rl, c = c0 + cg;
+    __half h[8];
+    if (r < R && c < C) {
+      load8_half(X + r * C + c, C - c, vec != 0 && c + 8 <= C, h);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) h[j] = __float2half_rn(0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float q = fminf(127.f, fmaxf(-127.f, rint_small(__fmul_rn(__half2float(h[j]), s_s[cg + j]))));
+      tile[(cg + j) * kCqPitch + rl] = __float2half_rn(q);   // exact: an integer of magnitude <= 127
+      l1c[j] += static_cast<int>(fabsf(q));
+    }
+  }
+  if (l1 != nullptr) {
+    // lanes l, l ^ 8, l ^ 16, l ^ 24 hold the same 8 columns
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      l1c[j] += __shfl_xor_sync(0xffffffffu, l1c[j], 8);
+      l1c[j] += __shfl_xor_sync(0xffffffffu, l1c[j], 16);
+    }
+    if (lane < 8)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) atomicAdd(&l1_s[cg + j], l1c[j]);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int idx = t + kThreads * i;
+    const int cl = idx >> 3, rc = (idx & 7) * 8;
+    const int64_t c = c0 + cl, r = r0 + rc;
+    if (c < C && r < R_pad) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(tile + cl * kCqPitch + rc);
+      *reinterpret_cast<uint4*>(Xt + c * R_pad + r) = make_uint4(src[0], src[1], src[2], src[3]);
+    }
+  }
+  if (l1 != nullptr && t < kCqTile && c0 + t < C && l1_s[t] != 0)
+    atomicAdd(&l1[(c0 + t) * nchunks + (r0 >> 10)], l1_s[t]);
+}
+
+// rowsmall[c] = 1 when every 1024-token chunk of column c has sum |code| <=
+// kSmallChunkL1 (so the GEMM's chunk sums of that output row stay below 2^22).
+__global__ void __launch_bounds__(kThreads) chunk_small_kernel(const int* __restrict__ l1, int64_t C, int64_t nchunks,
+                                                               uint8_t* __restrict__ rowsmall) {
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; c < C;
+       c += static_cast<int64_t>(gridDim.x) * kThreads) {
+    bool small = true;
+    for (int64_t k = 0; k < nchunks; ++k) small = small && l1[c * nchunks + k] <= kSmallChunkL1;
+    rowsmall[c] = small ? 1 : 0;
+  }
+}
+
 int grid_rows(int64_t rows) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
@@ -570,6 +661,25 @@ cudaError_t launch_gradout_prepass(const void* G, int gt, int64_t M, int64_t N, 
     grad_bias_finalize_kernel<BT><<<blocks, kThreads, 0, s>>>(partial, chunks, N, static_cast<BT*>(grad_bias));
     return cudaGetLastError();
   });
+}
+
+cudaError_t launch_col_quantize(const void* X, int xt, int64_t R, int64_t C, bool vec, const uint32_t* colmax,
+                                int64_t R_pad, float* scale, __half* Xt, int* l1, uint8_t* rowsmall, cudaStream_t s) {
+  if (R_pad == 0 || C == 0) return cudaSuccess;
+  const int64_t nchunks = ceil_div(R_pad, 1024);
+  const dim3 grid(static_cast<unsigned>(ceil_div(R_pad, kCqTile)), static_cast<unsigned>(ceil_div(C, kCqTile)));
+  cudaError_t e = dispatch_dt(xt, [&](auto* tag) {
+    using T = std::remove_pointer_t<decltype(tag)>;
+    ProfScope ps(K_COL_QUANTIZE, s);
+    col_quantize_kernel<T><<<grid, kThreads, 0, s>>>(static_cast<const T*>(X), R, C, vec ? 1 : 0, colmax, R_pad, scale,
+                                                    Xt, l1, nchunks);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess || rowsmall == nullptr) return e;
+  ProfScope ps(K_COL_QUANTIZE, s);
+  chunk_small_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(C, kThreads), 1024)), kThreads, 0, s>>>(
+      l1, C, nchunks, rowsmall);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_silu(const void* h, int dt, int64_t n, bool vec, void* out, cudaStream_t s) {

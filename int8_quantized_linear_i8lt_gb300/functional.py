@@ -281,6 +281,63 @@ class Int8LinearFunction(torch.autograd.Function):
         return gA, None, None, gb, None, None
 
 
+def grad_weight(G: torch.Tensor, A: torch.Tensor, out_dtype: torch.dtype | None = None,
+                ws: torch.Tensor | None = None) -> torch.Tensor:
+    """grad_W [N, K] = G^T A over the tokens, int8 with column-wise scales
+    (i8lt_grad_weight); G [M, N], A [M, K]."""
+    _require_cuda(G, A)
+    G, A = G.contiguous(), A.contiguous()
+    M, N = G.shape
+    K = A.shape[1]
+    if A.shape[0] != M:
+        raise I8LTError(f"G has {M} tokens, A {A.shape[0]}")
+    out_dtype = out_dtype or G.dtype
+    gW = torch.empty(N, K, dtype=out_dtype, device=G.device)
+    if ws is None:
+        ws = torch.empty(max(_lib.i8lt_grad_weight_workspace_size(M, N, K), 256), dtype=torch.uint8,
+                         device=G.device)
+    _check(_lib.i8lt_grad_weight(G.data_ptr(), _code(G.dtype), A.data_ptr(), _code(A.dtype), M, N, K, gW.data_ptr(),
+                                 _code(out_dtype), ws.data_ptr(), ws.numel(), _stream(G)), "i8lt_grad_weight")
+    return gW
+
+
+class Int8LinearTrainableFunction(torch.autograd.Function):
+    """y = int8 linear(x) with a trainable float weight W (bitsandbytes'
+    has_fp16_weights=True): every forward quantizes W row-wise (CB, SCB) and
+    runs the same int8 forward; the backward gives grad_A through the
+    dequantized CB (as the memory-efficient mode does), grad_W through the
+    int8 column-wise product (i8lt_grad_weight) and grad_bias."""
+
+    @staticmethod
+    def forward(ctx, x, W, bias, threshold, max_outliers):
+        _warn_cast(x.dtype)
+        shape = x.shape
+        K = shape[-1]
+        x2 = x.reshape(-1, K)
+        CB, SCB = quantize_weight(W)
+        out, _ = forward(x2, CB, SCB, K, bias, threshold, max_outliers=max_outliers)
+        ctx.save_for_backward(x2, CB, SCB)
+        ctx.K = K
+        ctx.x_shape = shape
+        ctx.w_dtype = W.dtype
+        ctx.bias_dtype = None if bias is None else bias.dtype
+        return out.reshape(*shape[:-1], CB.shape[0])
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        x2, CB, SCB = ctx.saved_tensors
+        need_x = ctx.needs_input_grad[0]
+        need_w = ctx.needs_input_grad[1]
+        need_b = ctx.needs_input_grad[2] and ctx.bias_dtype is not None
+        G = grad_out.reshape(-1, grad_out.shape[-1])
+        gA, gb = backward_input(G, CB, SCB, ctx.K, need_grad_A=need_x,
+                                bias_dtype=ctx.bias_dtype if need_b else None)
+        gW = grad_weight(G, x2, ctx.w_dtype) if need_w else None
+        if gA is not None:
+            gA = gA.reshape(ctx.x_shape)
+        return gA, gW, gb, None, None
+
+
 class SiLUFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, h):

@@ -56,6 +56,34 @@ class Linear8bitLt(torch.nn.Module):
                 f"bias={self.bias is not None}, threshold={self.threshold}")
 
 
+class Linear8bitLtTrainable(torch.nn.Module):
+    """The trainable-weight mode of the same layer (bitsandbytes'
+    has_fp16_weights=True): the float weight is a parameter, quantized afresh
+    on every forward; its gradient comes from the int8 column-wise product
+    G^T A (i8lt_grad_weight)."""
+
+    def __init__(self, in_features: int, out_features: int, bias: bool = True, threshold: float = 6.0,
+                 device=None, dtype: torch.dtype = torch.float16, max_outliers: int | None = None):
+        super().__init__()
+        self.in_features = in_features
+        self.out_features = out_features
+        self.threshold = float(threshold)
+        self.max_outliers = max_outliers
+        self.weight = torch.nn.Parameter(torch.empty(out_features, in_features, dtype=dtype, device=device))
+        torch.nn.init.kaiming_uniform_(self.weight, a=5 ** 0.5)
+        if bias:
+            self.bias = torch.nn.Parameter(torch.zeros(out_features, dtype=dtype, device=device))
+        else:
+            self.register_parameter("bias", None)
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return F.Int8LinearTrainableFunction.apply(x, self.weight, self.bias, self.threshold, self.max_outliers)
+
+    def extra_repr(self) -> str:
+        return (f"in_features={self.in_features}, out_features={self.out_features}, "
+                f"bias={self.bias is not None}, threshold={self.threshold}, trainable weight")
+
+
 class Int8MLP(torch.nn.Module):
     """y = fc2(silu(fc1(x))) (+ x when ``residual``), both layers int8."""
 
