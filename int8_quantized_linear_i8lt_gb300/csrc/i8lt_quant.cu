@@ -141,11 +141,13 @@ __device__ __forceinline__ float rint_small(float y) {
   return __fsub_rn(__fadd_rn(y, 12582912.0f), 12582912.0f);
 }
 
-template <typename T>
+// OutT = __half: activation codes (K3); OutT = int8_t: weight codes (K1, with
+// no outlier mask, no subA and no rowsmall).
+template <typename T, typename OutT>
 __global__ void __launch_bounds__(kThreads) act_quantize_staged_kernel(
     const T* __restrict__ A, int64_t M, int64_t K, int64_t ld, int vec, const uint32_t* __restrict__ mask,
     const int* __restrict__ idx, const DevStatus* __restrict__ st, int64_t cap_pad, float* __restrict__ scale,
-    __half* __restrict__ codes, __half* __restrict__ sub, uint8_t* __restrict__ rowsmall) {
+    OutT* __restrict__ codes, __half* __restrict__ sub, uint8_t* __restrict__ rowsmall) {
   extern __shared__ uint4 srow4[];   // ld fp16 values of the current row
   __shared__ float red[32];
   __shared__ int chunk_l1[kStagedMaxChunks];
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) act_quantize_staged_kernel(
       for (int i = threadIdx.x; i < nchunks; i += kThreads) chunk_l1[i] = 0;
     amax = block_max(amax, red);   // its barriers also publish the staged row and the cleared sums
     const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
-    __half* out = codes + m * ld;
+    OutT* out = codes + m * ld;
     // every thread runs every iteration (the shuffles below need all 32 lanes)
     for (int64_t c0 = 0; c0 < ld; c0 += kThreads * 8) {
       const int64_t c = c0 + static_cast<int64_t>(threadIdx.x) * 8;
@@ -190,11 +192,19 @@ __global__ void __launch_bounds__(kThreads) act_quantize_staged_kernel(
           q[i] = ((bits >> i) & 1u) ? 0.f : fminf(127.f, fmaxf(-127.f, r));
           l1 += fabsf(q[i]);
         }
-        uint4 o;
-        __half2* o2 = reinterpret_cast<__half2*>(&o);
+        if constexpr (sizeof(OutT) == 1) {
+          uint32_t b[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o2[i] = __floats2half2_rn(q[2 * i], q[2 * i + 1]);
-        *reinterpret_cast<uint4*>(out + c) = o;
+          for (int i = 0; i < 8; ++i) b[i] = static_cast<uint32_t>(static_cast<int>(q[i])) & 0xFFu;
+          *reinterpret_cast<uint2*>(out + c) = make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                                                          b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+        } else {
+          uint4 o;
+          __half2* o2 = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o2[i] = __floats2half2_rn(q[2 * i], q[2 * i + 1]);
+          *reinterpret_cast<uint4*>(out + c) = o;
+        }
       }
       if (rowsmall != nullptr) {
         // a warp's 256 columns lie in one 1024-column chunk; a warp past the
@@ -555,11 +565,44 @@ cudaError_t dispatch_dt(int dt, F&& f) {
 
 }  // namespace
 
+// Launch of the staged row quantization (K_pad <= kStagedMaxLd): one row per
+// block at a time, as many blocks as fit with the row in shared memory.
+template <typename T, typename OutT>
+cudaError_t launch_staged(int prof_id, const T* A, int64_t M, int64_t K, int64_t K_pad, bool vec, const uint32_t* mask,
+                          const int* idx, const DevStatus* st, int64_t cap_pad, float* scale, OutT* codes,
+                          __half* sub, uint8_t* rowsmall, cudaStream_t s) {
+  const int smem = static_cast<int>(K_pad * 2);
+  static bool done = false;
+  if (!done) {
+    if (cudaFuncSetAttribute(act_quantize_staged_kernel<T, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kStagedMaxLd * 2) != cudaSuccess)
+      return cudaGetLastError();
+    done = true;
+  }
+  int dev = 0, sms = 152, per_sm = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, act_quantize_staged_kernel<T, OutT>, kThreads, smem) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(sms) * per_sm));
+  ProfScope ps(prof_id, s);
+  act_quantize_staged_kernel<T, OutT><<<grid, kThreads, smem, s>>>(A, M, K, K_pad, vec ? 1 : 0, mask, idx, st, cap_pad,
+                                                                   scale, codes, sub, rowsmall);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_weight(const void* W, int wt, int64_t N, int64_t K, int64_t ld, bool vec, int8_t* CB,
                                    float* SCB, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   return dispatch_dt(wt, [&](auto* tag) {
     using T = std::remove_pointer_t<decltype(tag)>;
+    if (ld <= kStagedMaxLd)
+      return launch_staged<T, int8_t>(K_QUANTIZE_WEIGHT, static_cast<const T*>(W), N, K, ld, vec, nullptr, nullptr,
+                                      nullptr, 0, SCB, CB, nullptr, nullptr, s);
     ProfScope ps(K_QUANTIZE_WEIGHT, s);
     row_quantize_kernel<T, int8_t><<<grid_rows(N), kThreads, 0, s>>>(
         static_cast<const T*>(W), N, K, ld, vec ? 1 : 0, nullptr, nullptr, nullptr, 0, SCB, CB, nullptr, nullptr);
@@ -592,31 +635,9 @@ cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int
   if (M == 0) return cudaSuccess;
   return dispatch_dt(at, [&](auto* tag) {
     using T = std::remove_pointer_t<decltype(tag)>;
-    if (K_pad <= kStagedMaxLd) {
-      const int smem = static_cast<int>(K_pad * 2);
-      static bool attr[3] = {false, false, false};
-      bool& done = attr[std::is_same_v<T, __half> ? 0 : (std::is_same_v<T, __nv_bfloat16> ? 1 : 2)];
-      if (!done) {
-        if (cudaFuncSetAttribute(act_quantize_staged_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kStagedMaxLd * 2) != cudaSuccess)
-          return cudaGetLastError();
-        done = true;
-      }
-      int dev = 0, sms = 152, per_sm = 1;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, act_quantize_staged_kernel<T>, kThreads, smem) !=
-              cudaSuccess ||
-          per_sm < 1) {
-        cudaGetLastError();
-        per_sm = 1;
-      }
-      const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(sms) * per_sm));
-      ProfScope ps(K_ROW_QUANTIZE, s);
-      act_quantize_staged_kernel<T><<<grid, kThreads, smem, s>>>(static_cast<const T*>(A), M, K, K_pad, vec ? 1 : 0,
-                                                                  mask, idx, st, cap_pad, SCA, Aq, subA, rowsmall);
-      return cudaGetLastError();
-    }
+    if (K_pad <= kStagedMaxLd)
+      return launch_staged<T, __half>(K_ROW_QUANTIZE, static_cast<const T*>(A), M, K, K_pad, vec, mask, idx, st,
+                                      cap_pad, SCA, Aq, subA, rowsmall, s);
     ProfScope ps(K_ROW_QUANTIZE, s);
     row_quantize_kernel<T, __half><<<grid_rows(M), kThreads, 0, s>>>(
         static_cast<const T*>(A), M, K, K_pad, vec ? 1 : 0, mask, idx, st, cap_pad, SCA, Aq, subA, rowsmall);
