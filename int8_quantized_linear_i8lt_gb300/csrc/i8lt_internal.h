@@ -43,7 +43,7 @@ cudaError_t launch_outlier_index(const uint32_t* colmax, int64_t K, float thr, i
 // kSmallChunkL1 (its int32 accumulator chunks then stay below 2^22).
 constexpr int kSmallChunkL1 = 33026;   // 33026 * 127 < 2^22
 cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int64_t K_pad, bool vec,
-                                const uint32_t* mask, const int* idx, const DevStatus* st, int64_t cap_pad,
+                                const uint32_t* mask, const int* idx, DevStatus* st, int64_t cap_pad,
                                 float* SCA, __half* Aq, __half* subA, uint8_t* rowsmall, cudaStream_t s);
 
 // K4: subB[n, j] = fp16(fp32(CB[n, idx[j]]) * SCB[n] * fp32(1/127)).

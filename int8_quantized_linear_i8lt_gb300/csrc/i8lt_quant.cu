@@ -565,6 +565,178 @@ cudaError_t dispatch_dt(int dt, F&& f) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Row quantization with the rows streamed by bulk copies (16-bit input, K a
+// multiple of 8): two row buffers in shared memory; while the block
+// quantizes row i from one, a bulk copy brings row i + 1 into the other, so
+// the HBM reads never wait for the arithmetic.  Same arithmetic as
+// act_quantize_staged_kernel.  Waits are bounded: on a timeout the block
+// records ST_TIMEOUT, lets its copy in flight land (bounded) and returns.
+// ---------------------------------------------------------------------------
+constexpr int kBulkMaxRowBytes = 100 * 1024;   // two buffers fit one block per SM
+
+// 8 consecutive elements of a row staged in shared memory (16-byte aligned),
+// cast to fp16 (RNE), with 16-byte loads.
+template <typename T>
+__device__ __forceinline__ void smem_load8_half(const T* p, __half (&h)[8]) {
+  constexpr int kVec = 16 / static_cast<int>(sizeof(T));   // elements per 16-byte load
+#pragma unroll
+  for (int v = 0; v < 8 / kVec; ++v) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p + v * kVec);
+    const T* x = reinterpret_cast<const T*>(&u);
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) h[v * kVec + j] = to_half(x[j]);
+  }
+}
+constexpr int kWhereQuantize = 6;               // status `where` of a timed-out row copy
+
+template <typename T, typename OutT, int kBlock>
+__global__ void __launch_bounds__(kBlock) row_quantize_bulk_kernel(
+    const T* __restrict__ A, int64_t M, int64_t K, int64_t ld, const uint32_t* __restrict__ mask,
+    const int* __restrict__ idx, DevStatus* st, int64_t cap_pad, float* __restrict__ scale,
+    OutT* __restrict__ codes, __half* __restrict__ sub, uint8_t* __restrict__ rowsmall, int row_bytes) {
+  extern __shared__ __align__(16) uint8_t rowbuf[];   // two buffers of row_bytes (a multiple of 16)
+  __shared__ float red[32];
+  __shared__ int chunk_l1[kStagedMaxChunks];
+  __shared__ __align__(8) uint64_t full[2];
+  __shared__ int abort_flag;
+  const int used = (mask != nullptr) ? st->used : 0;
+  const int used_pad = (used + 63) / 64 * 64;
+  const int nchunks = static_cast<int>((ld + 1023) / 1024);
+  const uint32_t bytes = static_cast<uint32_t>(K * static_cast<int64_t>(sizeof(T)));
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t m0 = blockIdx.x;
+  if (threadIdx.x == 0 && m0 < M) {
+    mbar_arrive_expect_tx(&full[0], bytes);
+    bulk_load(rowbuf, A + m0 * K, bytes, &full[0]);
+  }
+  int i = 0;
+  for (int64_t m = m0; m < M; m += gridDim.x, ++i) {
+    const int b = i & 1;
+    const int64_t mn = m + gridDim.x;
+    if (threadIdx.x == 0 && mn < M) {   // the other buffer was released at the end of the previous row
+      mbar_arrive_expect_tx(&full[b ^ 1], bytes);
+      bulk_load(rowbuf + (b ^ 1) * row_bytes, A + mn * K, bytes, &full[b ^ 1]);
+    }
+    volatile int* abort_p = &abort_flag;
+    if (!__syncthreads_and(mbar_wait(&full[b], (i >> 1) & 1, abort_p, st, kWhereQuantize))) {
+      // let the copy in flight into the other buffer land before the block exits
+      if (threadIdx.x == 0 && mn < M) {
+        *abort_p = 0;
+        mbar_wait(&full[b ^ 1], ((i + 1) >> 1) & 1, abort_p, nullptr, 0);
+      }
+      return;
+    }
+    const T* row = reinterpret_cast<const T*>(rowbuf + b * row_bytes);
+    float amax = 0.f;
+    for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < K; c += kBlock * 8) {
+      __half h[8];
+      smem_load8_half(row + c, h);
+      const uint32_t bits = (mask != nullptr) ? ((mask[c >> 5] >> (c & 31)) & 0xFFu) : 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (!((bits >> j) & 1u)) amax = fmaxf(amax, fabsf(__half2float(h[j])));
+    }
+    if (rowsmall != nullptr)
+      for (int k = threadIdx.x; k < nchunks; k += kBlock) chunk_l1[k] = 0;
+    amax = block_max(amax, red);
+    const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
+    OutT* out = codes + m * ld;
+    for (int64_t c0 = 0; c0 < ld; c0 += kBlock * 8) {   // every thread runs every iteration
+      const int64_t c = c0 + static_cast<int64_t>(threadIdx.x) * 8;
+      float l1 = 0.f;
+      if (c < ld) {
+        __half h[8];
+        if (c < K) {
+          smem_load8_half(row + c, h);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) h[j] = __float2half_rn(0.f);
+        }
+        const uint32_t bits = (mask != nullptr && c < K) ? ((mask[c >> 5] >> (c & 31)) & 0xFFu) : 0u;
+        float q[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float r = rint_small(__fmul_rn(__half2float(h[j]), s));
+          q[j] = ((bits >> j) & 1u) ? 0.f : fminf(127.f, fmaxf(-127.f, r));
+          l1 += fabsf(q[j]);
+        }
+        if constexpr (sizeof(OutT) == 1) {
+          uint32_t w[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) w[j] = static_cast<uint32_t>(static_cast<int>(q[j])) & 0xFFu;
+          *reinterpret_cast<uint2*>(out + c) = make_uint2(w[0] | (w[1] << 8) | (w[2] << 16) | (w[3] << 24),
+                                                          w[4] | (w[5] << 8) | (w[6] << 16) | (w[7] << 24));
+        } else {
+          uint4 o;
+          __half2* o2 = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o2[j] = __floats2half2_rn(q[2 * j], q[2 * j + 1]);
+          *reinterpret_cast<uint4*>(out + c) = o;
+        }
+      }
+      if (rowsmall != nullptr) {
+        int v = static_cast<int>(l1);
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1) v += __shfl_xor_sync(0xffffffffu, v, k);
+        const int64_t cw = c0 + static_cast<int64_t>(threadIdx.x & ~31) * 8;
+        if ((threadIdx.x & 31) == 0 && v != 0) atomicAdd(&chunk_l1[cw >> 10], v);
+      }
+    }
+    if (sub != nullptr) {
+      for (int j = threadIdx.x; j < used_pad; j += kBlock)
+        sub[m * cap_pad + j] = (j < used) ? to_half(row[idx[j]]) : __float2half_rn(0.f);
+    }
+    bool small = true;
+    if (rowsmall != nullptr) {
+      __syncthreads();
+      for (int k = threadIdx.x; k < nchunks; k += kBlock) small = small && chunk_l1[k] <= kSmallChunkL1;
+    }
+    small = __syncthreads_and(small) != 0;   // also: this row buffer is no longer read
+    if (threadIdx.x == 0) {
+      if (rowsmall != nullptr) rowsmall[m] = small ? 1 : 0;
+      scale[m] = amax;
+    }
+  }
+}
+
+template <typename T, typename OutT>
+cudaError_t launch_bulk(int prof_id, const T* A, int64_t M, int64_t K, int64_t K_pad, const uint32_t* mask,
+                        const int* idx, DevStatus* st, int64_t cap_pad, float* scale, OutT* codes, __half* sub,
+                        uint8_t* rowsmall, cudaStream_t s) {
+  const int row_bytes = static_cast<int>(round_up(K * static_cast<int64_t>(sizeof(T)), 16));
+  const int smem = 2 * row_bytes;
+  // long rows: one block per SM holds both buffers, so it gets 1024 threads
+  constexpr int kBlock = 1024;
+  static bool done = false;
+  if (!done) {
+    if (cudaFuncSetAttribute(row_quantize_bulk_kernel<T, OutT, kBlock>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             2 * kBulkMaxRowBytes) != cudaSuccess)
+      return cudaGetLastError();
+    done = true;
+  }
+  int dev = 0, sms = 152, per_sm = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_quantize_bulk_kernel<T, OutT, kBlock>, kBlock, smem) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(sms) * per_sm));
+  ProfScope ps(prof_id, s);
+  row_quantize_bulk_kernel<T, OutT, kBlock><<<grid, kBlock, smem, s>>>(A, M, K, K_pad, mask, idx, st, cap_pad, scale, codes,
+                                                                 sub, rowsmall, row_bytes);
+  return cudaGetLastError();
+}
+
 // Launch of the staged row quantization (K_pad <= kStagedMaxLd): one row per
 // block at a time, as many blocks as fit with the row in shared memory.
 template <typename T, typename OutT>
@@ -600,6 +772,9 @@ cudaError_t launch_quantize_weight(const void* W, int wt, int64_t N, int64_t K, 
   if (N == 0) return cudaSuccess;
   return dispatch_dt(wt, [&](auto* tag) {
     using T = std::remove_pointer_t<decltype(tag)>;
+    if (vec && K * static_cast<int64_t>(sizeof(T)) <= kBulkMaxRowBytes)
+      return launch_bulk<T, int8_t>(K_QUANTIZE_WEIGHT, static_cast<const T*>(W), N, K, ld, nullptr, nullptr, nullptr, 0,
+                                    SCB, CB, nullptr, nullptr, s);
     if (ld <= kStagedMaxLd)
       return launch_staged<T, int8_t>(K_QUANTIZE_WEIGHT, static_cast<const T*>(W), N, K, ld, vec, nullptr, nullptr,
                                       nullptr, 0, SCB, CB, nullptr, nullptr, s);
@@ -630,11 +805,14 @@ cudaError_t launch_outlier_index(const uint32_t* colmax, int64_t K, float thr, i
 }
 
 cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int64_t K_pad, bool vec,
-                                const uint32_t* mask, const int* idx, const DevStatus* st, int64_t cap_pad,
+                                const uint32_t* mask, const int* idx, DevStatus* st, int64_t cap_pad,
                                 float* SCA, __half* Aq, __half* subA, uint8_t* rowsmall, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
   return dispatch_dt(at, [&](auto* tag) {
     using T = std::remove_pointer_t<decltype(tag)>;
+    if (vec && K * static_cast<int64_t>(sizeof(T)) <= kBulkMaxRowBytes)
+      return launch_bulk<T, __half>(K_ROW_QUANTIZE, static_cast<const T*>(A), M, K, K_pad, mask, idx, st, cap_pad,
+                                    SCA, Aq, subA, rowsmall, s);
     if (K_pad <= kStagedMaxLd)
       return launch_staged<T, __half>(K_ROW_QUANTIZE, static_cast<const T*>(A), M, K, K_pad, vec, mask, idx, st,
                                       cap_pad, SCA, Aq, subA, rowsmall, s);
