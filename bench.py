@@ -652,12 +652,14 @@ def oracle_sample_step(wl, rows_per_layer, seed=0):
 
 
 def cpu_baseline(wl, budget_s=20.0):
+    """The oracle on a bounded row sample: the sample doubles until one
+    measurement takes at least half of ``budget_s`` seconds (or holds every
+    row, or 4096 rows)."""
     rows = 16
     secs, ops = oracle_sample_step(wl, rows)
-    # grow the sample towards the budget (rows scale the GEMM work linearly)
-    if secs < budget_s / 4:
-        rows = int(min(max(wl.layers[0].M, 16), rows * max(1.0, (budget_s / 2) / max(secs, 1e-3))))
-        rows = max(16, min(rows, 512))
+    cap = min(4096, max(16, max(s.M for s in wl.layers)))
+    while secs < budget_s / 2 and rows < cap:
+        rows = min(cap, rows * 2 if secs > budget_s / 8 else rows * 4)
         secs, ops = oracle_sample_step(wl, rows)
     return {"value": round(ops / secs / 1e12, 6), "unit": "TOPS", "cores": _blas_threads(), "kind": "oracle",
             "sample": f"{rows} rows of every layer of {wl.name}: forward + backward to the input + grad_bias, "
