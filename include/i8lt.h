@@ -317,6 +317,16 @@ typedef struct {
   float ms;
 } i8lt_kernel_time;
 int i8lt_profile_start(int max_launches);
+/* Diagnostic of the failure path.  Every pipeline wait of the library is
+ * bounded: a wait that has not completed after its limit (4 s in the
+ * kernels) records I8LT_ERR_TIMEOUT in the workspace status word, the kernel
+ * winds down and the CUDA context stays usable.  This entry point runs that
+ * same wait, limit_ns long (0 < limit_ns <= 2e9), on a barrier that nothing
+ * completes, so that a caller or a test can see the error come back through
+ * i8lt_read_device_status.  ws: at least 256 bytes, 256-byte aligned (its
+ * status word is cleared first).  No counterpart on the pages. */
+int i8lt_debug_wait_timeout(int64_t limit_ns, void* ws, size_t ws_bytes, void* stream);
+
 /* Launch shape the library uses for the persistent GEMM kernels
  * (kernel = I8LT_K_FWD_GEMM or I8LT_K_BWD_GEMM): CTAs (pairs x 2), threads
  * per CTA and dynamic shared memory per CTA on the current device.  Any

@@ -598,6 +598,16 @@ const char* i8lt_kernel_name(int k) {
   return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
 }
 
+int i8lt_debug_wait_timeout(int64_t limit_ns, void* ws, size_t ws_bytes, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 2000000000LL) return I8LT_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < kAlign) return I8LT_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
+  if (int d = check_device()) return d;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return I8LT_ERR_CUDA;
+  return cuda_status(launch_wait_limit(static_cast<DevStatus*>(ws), static_cast<unsigned long long>(limit_ns), s));
+}
+
 int i8lt_read_device_status(void* ws, int32_t* status, int32_t* outliers, void* stream) {
   if (ws == nullptr) return I8LT_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

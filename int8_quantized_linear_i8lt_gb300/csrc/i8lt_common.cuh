@@ -211,8 +211,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // the latter case it raises the CTA's abort flag and records ST_TIMEOUT.
 // `sleep_ns` > 0 backs off between polls (for waiters that are not on the
 // critical path, so that they leave issue slots to the warps that are).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          DevStatus* st, int where, unsigned sleep_ns = 0) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                DevStatus* st, int where, unsigned sleep_ns,
+                                                unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
@@ -220,13 +221,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 0) {
       if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitTimeoutNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         set_status(st, ST_TIMEOUT, where);
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          DevStatus* st, int where, unsigned sleep_ns = 0) {
+  return mbar_wait_limit(bar, parity, abort_flag, st, where, sleep_ns, kWaitTimeoutNs);
 }
 
 // ---------------------------------------------------------------------------

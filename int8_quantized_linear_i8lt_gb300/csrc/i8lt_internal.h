@@ -59,6 +59,9 @@ int64_t gradout_partial_chunks(int64_t M);
 
 cudaError_t launch_silu(const void* h, int dt, int64_t n, bool vec, void* out, cudaStream_t s);
 
+// Diagnostic of the bounded waits: a wait that nothing completes, limit_ns long.
+cudaError_t launch_wait_limit(DevStatus* st, unsigned long long limit_ns, cudaStream_t s);
+
 // Trainable-weight mode: column-wise quantization of X [R, C] (dtype xt) into
 // Xt [C, R_pad] fp16 codes and scale [C], from the column maxima colmax [C]
 // (launch_colmax).  With l1 ([C, ceil(R_pad / 1024)] int32, zeroed) and

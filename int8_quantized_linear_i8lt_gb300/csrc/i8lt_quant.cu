@@ -545,6 +545,22 @@ __global__ void __launch_bounds__(kThreads) chunk_small_kernel(const int* __rest
   }
 }
 
+// Diagnostic: one block waits, through the same bounded wait as every
+// pipeline of the library, on an mbarrier that nothing arrives on; after
+// limit_ns it records ST_TIMEOUT (where = kWhereDiagnostic) and returns.
+constexpr int kWhereDiagnostic = 9;
+__global__ void __launch_bounds__(32) wait_limit_kernel(DevStatus* st, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  mbar_wait_limit(&bar, 0, &abort_flag, st, kWhereDiagnostic, 0, limit_ns);
+}
+
 int grid_rows(int64_t rows) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
@@ -878,6 +894,11 @@ cudaError_t launch_col_quantize(const void* X, int xt, int64_t R, int64_t C, boo
   ProfScope ps(K_COL_QUANTIZE, s);
   chunk_small_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(C, kThreads), 1024)), kThreads, 0, s>>>(
       l1, C, nchunks, rowsmall);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_limit(DevStatus* st, unsigned long long limit_ns, cudaStream_t s) {
+  wait_limit_kernel<<<1, 32, 0, s>>>(st, limit_ns);
   return cudaGetLastError();
 }
 

@@ -149,6 +149,14 @@ def test_other_entry_points_argument_errors(L):
     assert r == _lib.I8LT_ERR_INVALID_ARG
 
 
+def test_debug_wait_timeout_argument_errors(L):
+    assert _lib.i8lt_debug_wait_timeout(0, FAKE, 256) == _lib.I8LT_ERR_INVALID_ARG
+    assert _lib.i8lt_debug_wait_timeout(3_000_000_000, FAKE, 256) == _lib.I8LT_ERR_INVALID_ARG
+    assert _lib.i8lt_debug_wait_timeout(1000, FAKE, 255) == _lib.I8LT_ERR_WORKSPACE
+    assert _lib.i8lt_debug_wait_timeout(1000, None, 256) == _lib.I8LT_ERR_WORKSPACE
+    assert _lib.i8lt_debug_wait_timeout(1000, FAKE + 16, 256) == _lib.I8LT_ERR_MISALIGNED
+
+
 def test_valid_call_without_gpu_reports_error_not_crash(L):
     import torch
     if torch.cuda.is_available():
