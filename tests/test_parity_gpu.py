@@ -240,19 +240,25 @@ def _rows(M, n=40, seed=0):
     return np.array(sorted(r))
 
 
-@pytest.mark.parametrize("name", ["linear_4096", "linear_bf16_4096x11008", "proj_8192x28672"])
-def test_workload_layers(name):
+# every config over 10 seeds (the pages run their tests 10 times for
+# stability), the 16384-token projection over 2 (its oracle rows are sampled)
+WORKLOAD_SEEDS = ([("linear_4096", s) for s in range(10)] + [("linear_bf16_4096x11008", s) for s in range(10)]
+                  + [("proj_8192x28672", s) for s in range(2)])
+
+
+@pytest.mark.parametrize("name,base", WORKLOAD_SEEDS, ids=lambda v: str(v))
+def test_workload_layers(name, base):
     wl = W.WORKLOADS[name]
     for li, spec in enumerate(wl.layers):
-        seed = li * W.OFF_LAYER2
+        seed = base + li * W.OFF_LAYER2
         A = W.activation(spec, seed)
-        Wf, b, G = W.layer_tensors(wl, li, 0)
+        Wf, b, G = W.layer_tensors(wl, li, base)
         K = spec.K
         CB, SCB = I.quantize_weight(Wf.to(DEV))
         CB_ref, SCB_ref = check_weight(CB, SCB, Wf, K)
         del Wf
         g = gpu_forward(A.to(DEV), CB, SCB, K, b.to(DEV), spec.threshold)
-        rows = _rows(spec.M, seed=li)
+        rows = _rows(spec.M, seed=li + 7 * base)
         ref = O.forward_rows(to_np(A), ODT[A.dtype], CB_ref, SCB_ref, rows, to_np(b), ODT[b.dtype],
                              spec.threshold)
         heavy = W.heavy_columns(K, spec.heavy_frac, seed + W.OFF_HEAVY).numpy()
@@ -271,16 +277,17 @@ def test_workload_layers(name):
         torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("name", ["tiny_mlp", "mlp_7b"])
-def test_workload_mlp(name):
+@pytest.mark.parametrize("name,base", [("tiny_mlp", s) for s in range(10)] + [("mlp_7b", s) for s in range(2)],
+                         ids=lambda v: str(v))
+def test_workload_mlp(name, base):
     """The chained MLPs: every layer checked against the oracle fed with the
     same input the GPU layer saw (so integer stages stay bit-exact); the
     whole chain against the oracle chain within the tolerance."""
     wl = W.WORKLOADS[name]
     s1, s2 = wl.layers
-    x = W.layer_input(wl, 0, 0)
-    W1, b1, _ = W.layer_tensors(wl, 0, 0)
-    W2, b2, G = W.layer_tensors(wl, 1, 0)
+    x = W.layer_input(wl, 0, base)
+    W1, b1, _ = W.layer_tensors(wl, 0, base)
+    W2, b2, G = W.layer_tensors(wl, 1, base)
     dt = ODT[x.dtype]
     thr = s1.threshold
     CB1, SCB1 = I.quantize_weight(W1.to(DEV))
@@ -288,7 +295,7 @@ def test_workload_mlp(name):
     CB1r, SCB1r = check_weight(CB1, SCB1, W1, s1.K)
     CB2r, SCB2r = check_weight(CB2, SCB2, W2, s2.K)
     full = s1.M <= 4096
-    rows = None if full else _rows(s1.M, seed=3)
+    rows = None if full else _rows(s1.M, seed=3 + base)
     rsel = (lambda t: t) if full else (lambda t: t[torch.as_tensor(rows, device=DEV)])
     fwd = O.forward if full else (lambda *a, **k: O.forward_rows(a[0], a[1], a[2], a[3], rows, *a[4:], **k))
     xd = x.to(DEV)
