@@ -96,9 +96,16 @@ size_t i8lt_forward_workspace_size(int64_t M, int64_t K, int64_t N,
  *   mask    uint32[ceil(K/32)]: bit k set when column k is an outlier
  *   idx     int32[cap_pad]: ascending outlier column indices
  *   SCA     fp32[M]: row absmax of A16 outside the outlier columns
- *   rowsmall uint8[M]: 1 when every 1024-column chunk of the row's int8 codes
- *                      has sum |code| <= 33026, i.e. every chunk of the
- *                      row's int32 accumulator is below 2^22 in magnitude
+ *   asq     uint32[ceil(M/256), nch]: per 256-row tile and 1024-column chunk
+ *                      (nch = ceil(K_pad/1024)), the largest sum of squared
+ *                      codes of a row of the tile in that chunk
+ *   bsq     uint32[ceil(N/256), nch]: the same for the weight's code rows
+ *   plan    uint32[ceil(M/256) * ceil(N/256)]: per tile pair, the chunks per
+ *                      exact fp32 accumulation unit (bits 0-15; a group of
+ *                      chunks G qualifies when sum_G asq * sum_G bsq < 2^48,
+ *                      which bounds every partial sum below 2^24 by
+ *                      Cauchy-Schwarz) and bit 16 set when every unit stays
+ *                      below 2^22
  *   Aq      fp16[M, K_pad]: the int8 codes of A, stored as exact fp16 integers
  *                           (the form the fp16 tensor cores read)
  *   subA    fp16[M, cap_pad]: A16[:, idx], zero past the count
@@ -108,7 +115,7 @@ size_t i8lt_forward_workspace_size(int64_t M, int64_t K, int64_t N,
  *                           tensor-core pipeline loads)
  * cap = min(max_outliers, K); cap_pad = cap rounded up to a multiple of 64. */
 typedef struct {
-  size_t status, colmax, mask, idx, sca, rowsmall, aq, suba, subb, cbh, total;
+  size_t status, asq, bsq, colmax, mask, idx, sca, plan, aq, suba, subb, cbh, total;
   int64_t k_pad, cap_pad;
 } i8lt_fwd_layout;
 int i8lt_forward_workspace_layout(int64_t M, int64_t K, int64_t N,
@@ -310,7 +317,8 @@ typedef enum {
   I8LT_K_QUANTIZE_WEIGHT = 0, I8LT_K_COLMAX = 1, I8LT_K_OUTLIER_INDEX = 2, I8LT_K_ROW_QUANTIZE = 3,
   I8LT_K_SUBB = 4, I8LT_K_FWD_GEMM = 5, I8LT_K_GRADOUT_PREPASS = 6, I8LT_K_GRAD_BIAS_FINALIZE = 7,
   I8LT_K_BWD_GEMM = 8, I8LT_K_SILU = 9, I8LT_K_SILU_BACKWARD = 10, I8LT_K_WIDEN_CODES = 11,
-  I8LT_K_DEQUANT_WEIGHT = 12, I8LT_K_COL_QUANTIZE = 13, I8LT_K_WGRAD_GEMM = 14, I8LT_K_COUNT = 15
+  I8LT_K_DEQUANT_WEIGHT = 12, I8LT_K_COL_QUANTIZE = 13, I8LT_K_WGRAD_GEMM = 14, I8LT_K_UNIT_PLAN = 15,
+  I8LT_K_COUNT = 16
 } i8lt_kernel_id;
 typedef struct {
   int kernel;

@@ -34,9 +34,10 @@ I8LT_MAX_K = 133144
 
 
 class i8lt_fwd_layout(Structure):
-    _fields_ = [("status", c_size_t), ("colmax", c_size_t), ("mask", c_size_t), ("idx", c_size_t),
-                ("sca", c_size_t), ("rowsmall", c_size_t), ("aq", c_size_t), ("suba", c_size_t), ("subb", c_size_t),
-                ("cbh", c_size_t), ("total", c_size_t), ("k_pad", c_int64), ("cap_pad", c_int64)]
+    _fields_ = [("status", c_size_t), ("asq", c_size_t), ("bsq", c_size_t), ("colmax", c_size_t),
+                ("mask", c_size_t), ("idx", c_size_t), ("sca", c_size_t), ("plan", c_size_t), ("aq", c_size_t),
+                ("suba", c_size_t), ("subb", c_size_t), ("cbh", c_size_t), ("total", c_size_t),
+                ("k_pad", c_int64), ("cap_pad", c_int64)]
 
 
 class i8lt_fwd_debug(Structure):
@@ -49,7 +50,7 @@ class i8lt_kernel_time(Structure):
 
 KERNELS = ("quantize_weight", "colmax", "outlier_index", "row_quantize", "build_subB", "fwd_gemm",
            "gradout_prepass", "grad_bias_finalize", "bwd_gemm", "silu", "silu_backward", "widen_codes",
-           "dequant_weight", "col_quantize", "wgrad_gemm")
+           "dequant_weight", "col_quantize", "wgrad_gemm", "unit_plan")
 
 
 # name -> (restype, argtypes); the same names and order as include/i8lt.h

@@ -16,7 +16,7 @@ using namespace i8lt;
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -82,9 +82,14 @@ i8lt_fwd_layout fwd_layout(int64_t M, int64_t K, int64_t N, int64_t cap) {
   std::memset(&L, 0, sizeof(L));
   L.k_pad = round_up(K, 16);
   L.cap_pad = cap_pad_of(cap < K ? cap : K);
+  const int64_t nch = ceil_div(L.k_pad, 1024);
   size_t off = 0;
   L.status = off;
   off += kAlign;
+  L.asq = off;
+  off += align_up(static_cast<size_t>(ceil_div(M, 256)) * nch * 4);
+  L.bsq = off;
+  off += align_up(static_cast<size_t>(ceil_div(N, 256)) * nch * 4);
   L.colmax = off;
   off += align_up(static_cast<size_t>(K) * 4);
   L.mask = off;
@@ -93,8 +98,8 @@ i8lt_fwd_layout fwd_layout(int64_t M, int64_t K, int64_t N, int64_t cap) {
   off += align_up(static_cast<size_t>(L.cap_pad) * 4);
   L.sca = off;
   off += align_up(static_cast<size_t>(M) * 4);
-  L.rowsmall = off;
-  off += align_up(static_cast<size_t>(M));
+  L.plan = off;
+  off += align_up(static_cast<size_t>(ceil_div(M, 256)) * ceil_div(N, 256) * 4);
   L.aq = off;
   off += align_up(static_cast<size_t>(M) * L.k_pad * 2);
   L.suba = off;
@@ -136,11 +141,12 @@ BwdLayout bwd_layout(int64_t M, int64_t N, int64_t K, int gt) {
 }
 
 // Weight-gradient workspace (trainable-weight mode):
-// [status][colmax G, N][colmax A, K][scale G, N][scale A, K][rowsmall G, N]
-// [l1 G, N x chunks][Gt fp16, N x R_pad][At fp16, K x R_pad], R_pad = M
-// rounded up to 16 (the reduction dimension of the GEMM).
+// [status][colmax G, N][colmax A, K][scale G, N][scale A, K]
+// [tile chunk maxima G, A][chunk sums G, N x chunks][chunk sums A, K x chunks]
+// [plan][Gt fp16, N x R_pad][At fp16, K x R_pad], R_pad = M rounded up to 16
+// (the reduction dimension of the GEMM).
 struct WgradLayout {
-  size_t status, colmax_g, colmax_a, scale_g, scale_a, rowsmall_g, l1_g, gt, at, total;
+  size_t status, colmax_g, colmax_a, scale_g, scale_a, tsq_g, tsq_a, sq_g, sq_a, plan, gt, at, total;
   int64_t r_pad, chunks;
 };
 
@@ -159,10 +165,16 @@ WgradLayout wgrad_layout(int64_t M, int64_t N, int64_t K) {
   off += align_up(static_cast<size_t>(N) * 4);
   L.scale_a = off;
   off += align_up(static_cast<size_t>(K) * 4);
-  L.rowsmall_g = off;
-  off += align_up(static_cast<size_t>(N));
-  L.l1_g = off;
+  L.tsq_g = off;
+  off += align_up(static_cast<size_t>(ceil_div(N, 256)) * L.chunks * 4);
+  L.tsq_a = off;
+  off += align_up(static_cast<size_t>(ceil_div(K, 256)) * L.chunks * 4);
+  L.sq_g = off;
   off += align_up(static_cast<size_t>(N) * L.chunks * 4);
+  L.sq_a = off;
+  off += align_up(static_cast<size_t>(K) * L.chunks * 4);
+  L.plan = off;
+  off += align_up(static_cast<size_t>(ceil_div(N, 256)) * ceil_div(K, 256) * 4);
   L.gt = off;
   off += align_up(static_cast<size_t>(N) * L.r_pad * 2);
   L.at = off;
@@ -251,38 +263,42 @@ int forward_impl(FwdMode mode, const void* A, int at, int64_t M, int64_t K, cons
   uint32_t* mask = reinterpret_cast<uint32_t*>(w + L.mask);
   int* idx = reinterpret_cast<int*>(w + L.idx);
   float* SCA = reinterpret_cast<float*>(w + L.sca);
-  uint8_t* rowsmall = w + L.rowsmall;
+  uint32_t* asq = reinterpret_cast<uint32_t*>(w + L.asq);
+  uint32_t* bsq = reinterpret_cast<uint32_t*>(w + L.bsq);
+  uint32_t* plan = reinterpret_cast<uint32_t*>(w + L.plan);
   __half* Aq = reinterpret_cast<__half*>(w + L.aq);
   __half* subA = reinterpret_cast<__half*>(w + L.suba);
   __half* subB = reinterpret_cast<__half*>(w + L.subb);
   __half* CBh = reinterpret_cast<__half*>(w + L.cbh);
   const bool enabled = threshold_enabled(threshold);
   const bool vec = (K % 8) == 0;
-  cudaError_t e = cudaSuccess;
 
-  // one memset clears the status word of this call and (unless they are
-  // given) the column maxima
+  // one memset clears the status word of this call, the chunk maxima of the
+  // accumulation plan and (unless they are given) the column maxima
   const bool own_colmax = enabled && mode != kFwdFromColmax;
-  const size_t clear = own_colmax ? L.colmax + static_cast<size_t>(K) * 4 : sizeof(DevStatus);
-  if ((e = cudaMemsetAsync(w, 0, clear, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+  const size_t clear = own_colmax ? L.colmax + static_cast<size_t>(K) * 4 : L.colmax;
+  if ((cudaMemsetAsync(w, 0, clear, s)) != cudaSuccess) return I8LT_ERR_CUDA;
   if (own_colmax && M > 0) {
-    if ((e = launch_colmax(A, at, M, K, vec, colmax, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+    if ((launch_colmax(A, at, M, K, vec, colmax, s)) != cudaSuccess) return I8LT_ERR_CUDA;
   }
   if (colmax_only) return I8LT_OK;
   if (enabled) {
-    if ((e = launch_outlier_index(colmax, K, threshold, max_outliers, idx, mask, st, s)) != cudaSuccess)
+    if ((launch_outlier_index(colmax, K, threshold, max_outliers, idx, mask, st, s)) != cudaSuccess)
       return I8LT_ERR_CUDA;
   }
-  if ((e = launch_row_quantize(A, at, M, K, L.k_pad, vec, enabled ? mask : nullptr, idx, st, L.cap_pad, SCA, Aq,
-                               enabled ? subA : nullptr, rowsmall, s)) != cudaSuccess)
+  if ((launch_row_quantize(A, at, M, K, L.k_pad, vec, enabled ? mask : nullptr, idx, st, L.cap_pad, SCA, Aq,
+                               enabled ? subA : nullptr, asq, s)) != cudaSuccess)
     return I8LT_ERR_CUDA;
   const bool with_outliers = enabled && L.cap_pad > 0;
   if (with_outliers) {
-    if ((e = launch_build_subB(CB, L.k_pad, SCB, N, idx, st, L.cap_pad, subB, s)) != cudaSuccess)
+    if ((launch_build_subB(CB, L.k_pad, SCB, N, idx, st, L.cap_pad, subB, s)) != cudaSuccess)
       return I8LT_ERR_CUDA;
   }
 
-  if ((e = launch_widen_codes(CB, CBh, N * L.k_pad, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+  if ((launch_widen_codes(CB, CBh, N, L.k_pad, bsq, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+  if ((launch_unit_plan(asq, bsq, static_cast<int>(ceil_div(M, 256)), static_cast<int>(ceil_div(N, 256)),
+                            static_cast<int>(ceil_div(L.k_pad, 1024)), plan, s)) != cudaSuccess)
+    return I8LT_ERR_CUDA;
 
   FwdGemmArgs g;
   std::memset(&g, 0, sizeof(g));
@@ -304,7 +320,7 @@ int forward_impl(FwdMode mode, const void* A, int at, int64_t M, int64_t K, cons
   ea.K_pad = static_cast<int>(L.k_pad);
   ea.use_outliers = with_outliers ? 1 : 0;
   ea.SCA = SCA;
-  ea.rowsmall = rowsmall;
+  ea.plan = plan;
   ea.SCB = SCB;
   ea.bias = bias;
   ea.bias_dt = bt;
@@ -488,26 +504,31 @@ int i8lt_grad_weight(const void* G, int gt, const void* A, int at, int64_t M, in
   if (int d = check_device()) return d;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  // one memset: status, both column maxima; another: the l1 sums
+  // one memset: status, both column maxima; another: the chunk sums and maxima
   if (cudaMemsetAsync(w, 0, L.scale_g, s) != cudaSuccess) return I8LT_ERR_CUDA;
   if (M == 0) {
     const size_t bytes = static_cast<size_t>(N) * K * (wt == DT_F32 ? 4 : 2);
     return cuda_status(cudaMemsetAsync(grad_W, 0, bytes, s));
   }
-  if (cudaMemsetAsync(w + L.l1_g, 0, static_cast<size_t>(N) * L.chunks * 4, s) != cudaSuccess) return I8LT_ERR_CUDA;
+  if (cudaMemsetAsync(w + L.tsq_g, 0, L.plan - L.tsq_g, s) != cudaSuccess) return I8LT_ERR_CUDA;
   DevStatus* st = reinterpret_cast<DevStatus*>(w + L.status);
   uint32_t* cm_g = reinterpret_cast<uint32_t*>(w + L.colmax_g);
   uint32_t* cm_a = reinterpret_cast<uint32_t*>(w + L.colmax_a);
   float* sc_g = reinterpret_cast<float*>(w + L.scale_g);
   float* sc_a = reinterpret_cast<float*>(w + L.scale_a);
-  uint8_t* small_g = w + L.rowsmall_g;
-  int* l1_g = reinterpret_cast<int*>(w + L.l1_g);
+  uint32_t* tsq_g = reinterpret_cast<uint32_t*>(w + L.tsq_g);
+  uint32_t* tsq_a = reinterpret_cast<uint32_t*>(w + L.tsq_a);
+  int* sq_g = reinterpret_cast<int*>(w + L.sq_g);
+  int* sq_a = reinterpret_cast<int*>(w + L.sq_a);
+  uint32_t* plan = reinterpret_cast<uint32_t*>(w + L.plan);
   __half* Gt = reinterpret_cast<__half*>(w + L.gt);
   __half* At = reinterpret_cast<__half*>(w + L.at);
   if (launch_colmax(G, gt, M, N, (N % 8) == 0, cm_g, s) != cudaSuccess ||
       launch_colmax(A, at, M, K, (K % 8) == 0, cm_a, s) != cudaSuccess ||
-      launch_col_quantize(G, gt, M, N, (N % 8) == 0, cm_g, L.r_pad, sc_g, Gt, l1_g, small_g, s) != cudaSuccess ||
-      launch_col_quantize(A, at, M, K, (K % 8) == 0, cm_a, L.r_pad, sc_a, At, nullptr, nullptr, s) != cudaSuccess)
+      launch_col_quantize(G, gt, M, N, (N % 8) == 0, cm_g, L.r_pad, sc_g, Gt, sq_g, tsq_g, s) != cudaSuccess ||
+      launch_col_quantize(A, at, M, K, (K % 8) == 0, cm_a, L.r_pad, sc_a, At, sq_a, tsq_a, s) != cudaSuccess ||
+      launch_unit_plan(tsq_g, tsq_a, static_cast<int>(ceil_div(N, 256)), static_cast<int>(ceil_div(K, 256)),
+                       static_cast<int>(L.chunks), plan, s) != cudaSuccess)
     return I8LT_ERR_CUDA;
   // grad_W[n, k] = sum_m Gt[n, m] At[k, m] * scale_g[n] * scale_a[k] / 127^2: the
   // forward GEMM with the tokens as its reduction dimension
@@ -525,7 +546,7 @@ int i8lt_grad_weight(const void* G, int gt, const void* A, int at, int64_t M, in
   ea.K_pad = static_cast<int>(L.r_pad);
   ea.use_outliers = 0;
   ea.SCA = sc_g;
-  ea.rowsmall = small_g;
+  ea.plan = plan;
   ea.SCB = sc_a;
   ea.bias = nullptr;
   ea.bias_dt = 0;
@@ -594,7 +615,7 @@ const char* i8lt_kernel_name(int k) {
   static const char* names[] = {"quantize_weight", "colmax",          "outlier_index",      "row_quantize",
                                 "build_subB",      "fwd_gemm",        "gradout_prepass",    "grad_bias_finalize",
                                 "bwd_gemm",        "silu",            "silu_backward",      "widen_codes",
-                                "dequant_weight",  "col_quantize",    "wgrad_gemm"};
+                                "dequant_weight",  "col_quantize",    "wgrad_gemm",         "unit_plan"};
   return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
 }
 

@@ -374,7 +374,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int used = e.use_outliers ? e.st->used : 0;
   const int OB = (used + kBK - 1) / kBK;
   const int blocks = KB + OB;                      // pipeline stages per tile
-  const int units = nchunks + (OB > 0 ? 1 : 0);    // accumulation units per tile
+  // accumulation units of a tile: groups of `per` 1024-product chunks (the
+  // tile's plan word), then the outlier unit
+  auto tile_units = [&](uint32_t plan, int& per, int& n_int, bool& fast) {
+    per = max(1, min(nchunks, static_cast<int>(plan & 0xFFFFu)));
+    fast = ((plan >> 16) & 1u) != 0;
+    n_int = (nchunks + per - 1) / per;
+    return n_int + (OB > 0 ? 1 : 0);
+  };
 
   if (threadIdx.x == 0) init_barriers(bars, kEpiWarps);
   if (warp == kWarpMMA) {
@@ -436,6 +443,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int it = 0, u = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl) {
+        int tm, tn;
+        tile_coords(t, num_m, num_n, group, tm, tn);
+        int per, n_int;
+        bool fast;
+        const int units = tile_units(e.plan[tm * num_n + tn], per, n_int, fast);
         for (int uu = 0; uu < units && ok; ++uu, ++u) {
           // the epilogues of both CTAs released the accumulator of unit u-1
           if (u > 0 && !mbar_wait_cluster(&bars->acc_empty[0], (u - 1) & 1, abort_flag, e.st, kWhereMMA)) {
@@ -443,9 +455,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const bool is_int = uu < nchunks;
-          const int b0 = is_int ? uu * kChunkKB : KB;
-          const int b1 = is_int ? min(KB, b0 + kChunkKB) : blocks;
+          const bool is_int = uu < n_int;
+          const int b0 = is_int ? uu * per * kChunkKB : KB;
+          const int b1 = is_int ? min(KB, b0 + per * kChunkKB) : blocks;
           for (int b = b0; b < b1; ++b, ++it) {
             const int s = it % kFwdStages;
             const uint32_t ph = (it / kFwdStages) & 1;
@@ -505,7 +517,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       named_bar_sync(kBarEpi, kEpiThreads);
       const int64_t m = static_cast<int64_t>(tm) * kPairM + static_cast<int64_t>(rank) * kCtaRows + quad * 32 + lane;
       const bool row_ok = m < e.M;
-      const bool small = !row_ok || e.rowsmall[m] != 0;
+      int per, n_int;
+      bool small;   // every partial sum of the tile's units below 2^22: the fast exact conversion
+      const int units = tile_units(e.plan[tm * num_n + tn], per, n_int, small);
       for (int uu = 0; uu < units; ++uu, ++u) {
         // all 256 epilogue threads agree, so none is left at a named barrier
         if (!named_bar_and(kBarEpi, kEpiThreads,
@@ -531,7 +545,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // residual, written over the running sum in R, so that X can be
           // handed back to the MMA before the slower stores of phase 2
           const bool has_o = OB > 0;
-          const bool r_live = has_o ? (nchunks > 0) : (nchunks > 1);
+          const bool r_live = has_o ? (n_int > 0) : (n_int > 1);
           const float rs = row_ok ? __fmul_rn(e.SCA[m], 1.0f / 16129.0f) : 0.f;
 #pragma unroll 1
           for (int gc = 0; gc < 128; gc += 16) {
@@ -938,21 +952,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// Forward prepass: CB int8 codes -> the same values as fp16 (exact), 16
-// codes per thread and iteration, 16-byte loads and stores.
+// Forward prepass: CB int8 codes -> the same values as fp16 (exact).  One
+// warp per (row, 1024-column chunk): 32 bytes per lane, 16-byte loads and
+// stores; the chunk's sum of squares of the codes (dp4a) raises the row tile's
+// entry of bsq, the weight side of the accumulation plan.
 __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restrict__ CB, __half* __restrict__ CBh,
-                                                          int64_t n16) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n16;
-       i += static_cast<int64_t>(gridDim.x) * 256) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(CB) + i);
-    uint4 o0, o1;
-    i8x4_to_h4(v.x, o0.x, o0.y);
-    i8x4_to_h4(v.y, o0.z, o0.w);
-    i8x4_to_h4(v.z, o1.x, o1.y);
-    i8x4_to_h4(v.w, o1.z, o1.w);
-    uint4* dst = reinterpret_cast<uint4*>(CBh) + 2 * i;
-    dst[0] = o0;
-    dst[1] = o1;
+                                                          int64_t N, int64_t k_pad, int nchunks,
+                                                          uint32_t* __restrict__ bsq) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * 8;
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); w < N * nchunks; w += nwarps) {
+    const int64_t n = w / nchunks;
+    const int c = static_cast<int>(w - n * nchunks);
+    const int64_t k0 = static_cast<int64_t>(c) * 1024;
+    int sq = 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int64_t k = k0 + lane * 32 + j * 16;
+      if (k < k_pad) {   // k_pad is a multiple of 16
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(CB + n * k_pad + k));
+        sq = __dp4a(static_cast<int>(v.x), static_cast<int>(v.x), sq);
+        sq = __dp4a(static_cast<int>(v.y), static_cast<int>(v.y), sq);
+        sq = __dp4a(static_cast<int>(v.z), static_cast<int>(v.z), sq);
+        sq = __dp4a(static_cast<int>(v.w), static_cast<int>(v.w), sq);
+        uint4 o0, o1;
+        i8x4_to_h4(v.x, o0.x, o0.y);
+        i8x4_to_h4(v.y, o0.z, o0.w);
+        i8x4_to_h4(v.z, o1.x, o1.y);
+        i8x4_to_h4(v.w, o1.z, o1.w);
+        uint4* dst = reinterpret_cast<uint4*>(CBh + n * k_pad + k);
+        dst[0] = o0;
+        dst[1] = o1;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if (lane == 0 && sq != 0) atomicMax(bsq + (n >> 8) * nchunks + c, static_cast<uint32_t>(sq));
+  }
+}
+
+// The accumulation plan (see launch_unit_plan): one block per row tile tm of
+// the first operand, its chunk sums staged in shared memory, one thread per
+// column tile tn.  L is searched downwards from all chunks; uniform data stop
+// at the first candidate.
+constexpr int kPlanMaxChunks = 160;   // K <= 163840
+__global__ void __launch_bounds__(256) unit_plan_kernel(const uint32_t* __restrict__ asq,
+                                                        const uint32_t* __restrict__ bsq, int num_n, int nchunks,
+                                                        uint32_t* __restrict__ plan) {
+  __shared__ uint32_t a_s[kPlanMaxChunks];
+  const int tm = blockIdx.x;
+  for (int c = threadIdx.x; c < nchunks; c += blockDim.x) a_s[c] = asq[static_cast<int64_t>(tm) * nchunks + c];
+  __syncthreads();
+  constexpr unsigned long long kExact = 1ull << 48, kFast = 1ull << 44;
+  for (int tn = threadIdx.x; tn < num_n; tn += blockDim.x) {
+    const uint32_t* b = bsq + static_cast<int64_t>(tn) * nchunks;
+    int best = 1;
+    bool fast = true;
+    for (int L = nchunks; L >= 1; --L) {
+      bool ok = true, f = true;
+      for (int c0 = 0; c0 < nchunks && ok; c0 += L) {
+        unsigned long long sa = 0, sb = 0;
+        for (int c = c0; c < min(nchunks, c0 + L); ++c) {
+          sa += a_s[c];
+          sb += b[c];
+        }
+        const unsigned long long p = sa * sb;   // < 160^2 * 2^48: no overflow
+        ok = p < kExact;
+        f = f && p < kFast;
+      }
+      if (ok) {
+        best = L;
+        fast = f;
+        break;
+      }
+    }
+    plan[static_cast<int64_t>(tm) * num_n + tn] = static_cast<uint32_t>(best) | (fast ? 1u << 16 : 0u);
   }
 }
 
@@ -1071,15 +1145,25 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
   return cudaSuccess;
 }
 
-cudaError_t launch_widen_codes(const int8_t* CB, __half* CBh, int64_t n, cudaStream_t s) {
-  if (n == 0) return cudaSuccess;
+cudaError_t launch_widen_codes(const int8_t* CB, __half* CBh, int64_t N, int64_t k_pad, uint32_t* bsq,
+                               cudaStream_t s) {
+  if (N == 0 || k_pad == 0) return cudaSuccess;
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t n16 = n / 16;   // n is a multiple of 16 (rows padded to 16)
-  const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(n16, 256), static_cast<int64_t>(sms) * 8));
+  const int nchunks = static_cast<int>(ceil_div(k_pad, 1024));
+  const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(N * nchunks, 8), static_cast<int64_t>(sms) * 8));
   ProfScope ps(K_WIDEN_CODES, s);
-  widen_codes_kernel<<<blocks, 256, 0, s>>>(CB, CBh, n16);
+  widen_codes_kernel<<<blocks, 256, 0, s>>>(CB, CBh, N, k_pad, nchunks, bsq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unit_plan(const uint32_t* asq, const uint32_t* bsq, int num_m, int num_n, int nchunks,
+                             uint32_t* plan, cudaStream_t s) {
+  if (num_m == 0 || num_n == 0) return cudaSuccess;
+  if (nchunks > kPlanMaxChunks) return cudaErrorInvalidValue;
+  ProfScope ps(K_UNIT_PLAN, s);
+  unit_plan_kernel<<<num_m, 256, 0, s>>>(asq, bsq, num_n, nchunks, plan);
   return cudaGetLastError();
 }
 

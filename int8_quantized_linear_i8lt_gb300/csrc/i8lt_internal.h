@@ -39,12 +39,12 @@ cudaError_t launch_outlier_index(const uint32_t* colmax, int64_t K, float thr, i
                                  uint32_t* mask, DevStatus* st, cudaStream_t s);
 
 // K3: SCA[m], Aq [M, K_pad] (codes as exact fp16), subA [M, cap_pad], and
-// rowsmall[m] = 1 when every 1024-column chunk of row m has sum |code| <=
-// kSmallChunkL1 (its int32 accumulator chunks then stay below 2^22).
-constexpr int kSmallChunkL1 = 33026;   // 33026 * 127 < 2^22
+// the activation side of the accumulation plan: asq[(m / 256) * nchunks + c]
+// raised to the sum of squared codes of row m in the 1024-column chunk c
+// (asq zeroed, [ceil(M / 256), ceil(K_pad / 1024)]).
 cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int64_t K_pad, bool vec,
                                 const uint32_t* mask, const int* idx, DevStatus* st, int64_t cap_pad,
-                                float* SCA, __half* Aq, __half* subA, uint8_t* rowsmall, cudaStream_t s);
+                                float* SCA, __half* Aq, __half* subA, uint32_t* asq, cudaStream_t s);
 
 // K4: subB[n, j] = fp16(fp32(CB[n, idx[j]]) * SCB[n] * fp32(1/127)).
 cudaError_t launch_build_subB(const int8_t* CB, int64_t ld, const float* SCB, int64_t N, const int* idx,
@@ -64,10 +64,11 @@ cudaError_t launch_wait_limit(DevStatus* st, unsigned long long limit_ns, cudaSt
 
 // Trainable-weight mode: column-wise quantization of X [R, C] (dtype xt) into
 // Xt [C, R_pad] fp16 codes and scale [C], from the column maxima colmax [C]
-// (launch_colmax).  With l1 ([C, ceil(R_pad / 1024)] int32, zeroed) and
-// rowsmall ([C]): the fast-drain flags of the GEMM rows c.
+// (launch_colmax).  With sq ([C, ceil(R_pad / 1024)] int32, zeroed) and tsq
+// ([ceil(C / 256), ceil(R_pad / 1024)] uint32, zeroed): the per-tile chunk
+// maxima of the squared codes, for the GEMM's accumulation plan.
 cudaError_t launch_col_quantize(const void* X, int xt, int64_t R, int64_t C, bool vec, const uint32_t* colmax,
-                                int64_t R_pad, float* scale, __half* Xt, int* l1, uint8_t* rowsmall, cudaStream_t s);
+                                int64_t R_pad, float* scale, __half* Xt, int* sq, uint32_t* tsq, cudaStream_t s);
 cudaError_t launch_silu_backward(const void* g, const void* h, int dt, int64_t n, bool vec, void* out,
                                  cudaStream_t s);
 
@@ -84,7 +85,8 @@ struct FwdEpiArgs {
   int M, N, K_pad;
   int use_outliers;       // 0: decomposition disabled
   const float* SCA;
-  const uint8_t* rowsmall;  // per row: chunk sums below 2^22 (fast exact conversion)
+  const uint32_t* plan;   // per pair tile [num_m x num_n] (launch_unit_plan): bits 0-15 chunks of
+                          // 1024 products per accumulation unit, bit 16 fast exact conversion
   const float* SCB;
   const void* bias;
   int bias_dt;
@@ -99,8 +101,27 @@ struct FwdEpiArgs {
 
 cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStream_t s, int prof_id = 5 /*K_FWD_GEMM*/);
 
-// Forward prepass: CBh[i] = fp16(CB[i]) (exact) for n (multiple of 16) codes.
-cudaError_t launch_widen_codes(const int8_t* CB, __half* CBh, int64_t n, cudaStream_t s);
+// Forward prepass: CBh = fp16(CB) (exact), CB [N, k_pad]; and, for the
+// accumulation plan, bsq[n / 256, c] raised to the sum of squares of the codes
+// of row n in the 1024-column chunk c (bsq zeroed, [ceil(N / 256), nchunks]).
+cudaError_t launch_widen_codes(const int8_t* CB, __half* CBh, int64_t N, int64_t k_pad, uint32_t* bsq,
+                               cudaStream_t s);
+
+// Exact-accumulation plan of the int8 GEMM.  asq [num_m, nchunks] and bsq
+// [num_n, nchunks] hold, per 256-row tile of each operand and per 1024-deep
+// chunk of the reduction, the largest sum of squares of a row's codes in that
+// chunk.  By Cauchy-Schwarz every partial sum of a group of chunks G is at
+// most sqrt(sum_G asq * sum_G bsq), so a group with sum_G asq * sum_G bsq <
+// 2^48 accumulates exactly in fp32 (|partial| < 2^24), and one below 2^44
+// (|partial| < 2^22) drains with the fast conversion.  plan[tm * num_n + tn] =
+// L | fast << 16 with L the largest number of chunks per group such that every
+// aligned group of L chunks of that tile pair is below 2^48 (a single chunk
+// always is: (1024 * 127^2)^2 < 2^48).
+cudaError_t launch_unit_plan(const uint32_t* asq, const uint32_t* bsq, int num_m, int num_n, int nchunks,
+                             uint32_t* plan, cudaStream_t s);
+
+// The largest sum of squares of the codes of one 1024-column chunk.
+constexpr uint32_t kChunkSqMax = 1024u * 127u * 127u;
 
 struct BwdGemmArgs {
   CUtensorMap tmW;    // fused schedule: CB int8 [N, K_pad] (inner K_pad, outer N), box 128 x 64, 128B swizzle
@@ -134,7 +155,7 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
 enum KernelId {
   K_QUANTIZE_WEIGHT = 0, K_COLMAX, K_OUTLIER_INDEX, K_ROW_QUANTIZE, K_SUBB, K_FWD_GEMM, K_GRADOUT_PREPASS,
   K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_WIDEN_CODES, K_DEQUANT_WEIGHT, K_COL_QUANTIZE,
-  K_WGRAD_GEMM, K_COUNT
+  K_WGRAD_GEMM, K_UNIT_PLAN, K_COUNT
 };
 
 // Box sizes of the tensor maps (each CTA of a pair stages 128 rows of each

@@ -52,9 +52,10 @@ template <typename T, typename OutT>
 __global__ void __launch_bounds__(kThreads) row_quantize_kernel(
     const T* __restrict__ A, int64_t M, int64_t K, int64_t ld, int vec, const uint32_t* __restrict__ mask,
     const int* __restrict__ idx, const DevStatus* __restrict__ st, int64_t cap_pad, float* __restrict__ scale,
-    OutT* __restrict__ codes, __half* __restrict__ sub, uint8_t* __restrict__ rowsmall) {
+    OutT* __restrict__ codes, __half* __restrict__ sub, uint32_t* __restrict__ asq) {
   __shared__ float red[32];
-  __shared__ int chunk_l1[2];   // sum |code| of the two 1024-column chunks of one pass-2 step
+  __shared__ int chunk_sq[2];   // sum of code^2 of the two 1024-column chunks of one pass-2 step
+  const int nchunks = static_cast<int>((ld + 1023) / 1024);
   const int used = (mask != nullptr) ? st->used : 0;
   const int used_pad = (used + 63) / 64 * 64;
   for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
@@ -71,12 +72,11 @@ __global__ void __launch_bounds__(kThreads) row_quantize_kernel(
     amax = block_max(amax, red);
     const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
     OutT* out = codes + m * ld;
-    bool small = true;   // block-uniform
     for (int64_t c0 = 0; c0 < ld; c0 += kThreads * 8) {
       const int64_t c = c0 + static_cast<int64_t>(threadIdx.x) * 8;
-      if (rowsmall != nullptr && threadIdx.x < 2) chunk_l1[threadIdx.x] = 0;
-      if (rowsmall != nullptr) __syncthreads();
-      int l1 = 0;
+      if (asq != nullptr && threadIdx.x < 2) chunk_sq[threadIdx.x] = 0;
+      if (asq != nullptr) __syncthreads();
+      int sq = 0;
       if (c < ld) {
       __half h[8];
       if (c < K) {
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kThreads) row_quantize_kernel(
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         q[i] = (amax > 0.f && !((bits >> i) & 1u)) ? quant_code(__half2float(h[i]), s) : 0;
-        l1 += abs(q[i]);
+        sq += q[i] * q[i];
       }
       if constexpr (sizeof(OutT) == 1) {
         uint2 u;
@@ -105,17 +105,18 @@ __global__ void __launch_bounds__(kThreads) row_quantize_kernel(
         *reinterpret_cast<uint4*>(out + c) = u;
       }
       }
-      if (rowsmall != nullptr) {
+      if (asq != nullptr) {
         // threads 0-127 cover columns c0 .. c0+1023, threads 128-255 the next 1024
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-        if ((threadIdx.x & 31) == 0 && l1 != 0) atomicAdd(&chunk_l1[threadIdx.x >> 7], l1);
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if ((threadIdx.x & 31) == 0 && sq != 0) atomicAdd(&chunk_sq[threadIdx.x >> 7], sq);
         __syncthreads();
-        small = small && chunk_l1[0] <= kSmallChunkL1 && chunk_l1[1] <= kSmallChunkL1;
+        const int64_t ck = (c0 >> 10) + threadIdx.x;
+        if (threadIdx.x < 2 && ck < nchunks && chunk_sq[threadIdx.x] != 0)
+          atomicMax(asq + (m >> 8) * nchunks + ck, static_cast<uint32_t>(chunk_sq[threadIdx.x]));
         __syncthreads();
       }
     }
-    if (rowsmall != nullptr && threadIdx.x == 0) rowsmall[m] = small ? 1 : 0;
     if (sub != nullptr) {
       for (int j = threadIdx.x; j < used_pad; j += kThreads)
         sub[m * cap_pad + j] = (j < used) ? to_half(row[idx[j]]) : __float2half_rn(0.f);
@@ -131,8 +132,10 @@ __global__ void __launch_bounds__(kThreads) row_quantize_kernel(
 // rounded with an IEEE fp32 add of 1.5 * 2^23 (round to nearest even, exact
 // for |x * s| < 2^22; here |x * s| <= 127 + 2^-16), the same rounding as
 // __float2int_rn, and stored two at a time with one fp32x2 -> fp16x2
-// conversion (exact: integers of magnitude <= 127).  The per-1024-column
-// absolute code sums that decide rowsmall are reduced once per row.
+// conversion (exact: integers of magnitude <= 127).  With `asq`, each row's
+// sums of squared codes per 1024-column chunk raise its 256-row tile's entries
+// (asq[(m / 256) * nchunks + chunk], the activation side of the GEMM's exact
+// accumulation plan).
 // ---------------------------------------------------------------------------
 constexpr int kStagedMaxLd = 49152;   // 96 KB of fp16 per row
 constexpr int kStagedMaxChunks = kStagedMaxLd / 1024;
@@ -142,15 +145,15 @@ __device__ __forceinline__ float rint_small(float y) {
 }
 
 // OutT = __half: activation codes (K3); OutT = int8_t: weight codes (K1, with
-// no outlier mask, no subA and no rowsmall).
+// no outlier mask, no subA and no asq).
 template <typename T, typename OutT>
 __global__ void __launch_bounds__(kThreads) act_quantize_staged_kernel(
     const T* __restrict__ A, int64_t M, int64_t K, int64_t ld, int vec, const uint32_t* __restrict__ mask,
     const int* __restrict__ idx, const DevStatus* __restrict__ st, int64_t cap_pad, float* __restrict__ scale,
-    OutT* __restrict__ codes, __half* __restrict__ sub, uint8_t* __restrict__ rowsmall) {
+    OutT* __restrict__ codes, __half* __restrict__ sub, uint32_t* __restrict__ asq) {
   extern __shared__ uint4 srow4[];   // ld fp16 values of the current row
   __shared__ float red[32];
-  __shared__ int chunk_l1[kStagedMaxChunks];
+  __shared__ int chunk_sq[kStagedMaxChunks];
   const __half* srow = reinterpret_cast<const __half*>(srow4);
   const int used = (mask != nullptr) ? st->used : 0;
   const int used_pad = (used + 63) / 64 * 64;
@@ -172,15 +175,15 @@ __global__ void __launch_bounds__(kThreads) act_quantize_staged_kernel(
       for (int i = 0; i < 8; ++i)
         if (!((bits >> i) & 1u)) amax = fmaxf(amax, fabsf(__half2float(h[i])));
     }
-    if (rowsmall != nullptr)
-      for (int i = threadIdx.x; i < nchunks; i += kThreads) chunk_l1[i] = 0;
+    if (asq != nullptr)
+      for (int i = threadIdx.x; i < nchunks; i += kThreads) chunk_sq[i] = 0;
     amax = block_max(amax, red);   // its barriers also publish the staged row and the cleared sums
     const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
     OutT* out = codes + m * ld;
     // every thread runs every iteration (the shuffles below need all 32 lanes)
     for (int64_t c0 = 0; c0 < ld; c0 += kThreads * 8) {
       const int64_t c = c0 + static_cast<int64_t>(threadIdx.x) * 8;
-      float l1 = 0.f;
+      float sq = 0.f;
       if (c < ld) {
         const uint4 u = srow4[c >> 3];
         const __half* h = reinterpret_cast<const __half*>(&u);
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(kThreads) act_quantize_staged_kernel(
         for (int i = 0; i < 8; ++i) {
           const float r = rint_small(__fmul_rn(__half2float(h[i]), s));
           q[i] = ((bits >> i) & 1u) ? 0.f : fminf(127.f, fmaxf(-127.f, r));
-          l1 += fabsf(q[i]);
+          sq += q[i] * q[i];
         }
         if constexpr (sizeof(OutT) == 1) {
           uint32_t b[8];
@@ -206,30 +209,27 @@ __global__ void __launch_bounds__(kThreads) act_quantize_staged_kernel(
           *reinterpret_cast<uint4*>(out + c) = o;
         }
       }
-      if (rowsmall != nullptr) {
+      if (asq != nullptr) {
         // a warp's 256 columns lie in one 1024-column chunk; a warp past the
         // end of the row sums to 0 and adds nothing
-        int v = static_cast<int>(l1);
+        int v = static_cast<int>(sq);
 #pragma unroll
         for (int k = 16; k > 0; k >>= 1) v += __shfl_xor_sync(0xffffffffu, v, k);
         const int64_t cw = c0 + static_cast<int64_t>(threadIdx.x & ~31) * 8;
-        if ((threadIdx.x & 31) == 0 && v != 0) atomicAdd(&chunk_l1[cw >> 10], v);
+        if ((threadIdx.x & 31) == 0 && v != 0) atomicAdd(&chunk_sq[cw >> 10], v);
       }
     }
     if (sub != nullptr) {
       for (int j = threadIdx.x; j < used_pad; j += kThreads)
         sub[m * cap_pad + j] = (j < used) ? srow[idx[j]] : __float2half_rn(0.f);
     }
-    bool small = true;
-    if (rowsmall != nullptr) {
+    if (asq != nullptr) {
       __syncthreads();
-      for (int i = threadIdx.x; i < nchunks; i += kThreads) small = small && chunk_l1[i] <= kSmallChunkL1;
+      for (int i = threadIdx.x; i < nchunks; i += kThreads)
+        if (chunk_sq[i] != 0) atomicMax(asq + (m >> 8) * nchunks + i, static_cast<uint32_t>(chunk_sq[i]));
     }
-    small = __syncthreads_and(small) != 0;   // also: the staged row is no longer read
-    if (threadIdx.x == 0) {
-      if (rowsmall != nullptr) rowsmall[m] = small ? 1 : 0;
-      scale[m] = amax;
-    }
+    __syncthreads();   // also: the staged row is no longer read
+    if (threadIdx.x == 0) scale[m] = amax;
   }
 }
 
@@ -462,8 +462,8 @@ __global__ void __launch_bounds__(kThreads) silu_backward_kernel(const T* __rest
 // rint(fp32(fp16(X[r, c])) * (127 / scale[c])), 0 for R <= r < R_pad.  One
 // block per 64 (r) x 64 (c) tile: coalesced 16-byte loads of 8 columns, the
 // codes transposed through shared memory, 16-byte stores of 8 tokens.  With
-// `l1` it also adds the sum of |code| of each column over the tile's rows
-// to l1[c, r / 1024] (the fast-drain test of the GEMM's rows).
+// `sq` it also adds the sum of squared codes of each column over the tile's
+// rows to sq[c, r / 1024] (the GEMM's accumulation plan).
 // ---------------------------------------------------------------------------
 constexpr int kCqTile = 64;
 constexpr int kCqPitch = kCqTile + 2;   // halves; a 132-byte row keeps the transposed writes at 2-way
@@ -472,10 +472,10 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) col_quantize_kernel(const T* __restrict__ X, int64_t R, int64_t C, int vec,
                                                                 const uint32_t* __restrict__ colmax, int64_t R_pad,
                                                                 float* __restrict__ scale, __half* __restrict__ Xt,
-                                                                int* __restrict__ l1, int64_t nchunks) {
+                                                                int* __restrict__ sq, int64_t nchunks) {
   __shared__ __align__(16) __half tile[kCqTile * kCqPitch];   // [c][r]
   __shared__ float s_s[kCqTile];
-  __shared__ int l1_s[kCqTile];
+  __shared__ int sq_s[kCqTile];
   const int t = threadIdx.x, lane = t & 31;
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kCqTile;
   const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kCqTile;
@@ -483,12 +483,12 @@ __global__ void __launch_bounds__(kThreads) col_quantize_kernel(const T* __restr
     const int64_t c = c0 + t;
     const float am = c < C ? __half2float(__ushort_as_half(static_cast<unsigned short>(colmax[c]))) : 0.f;
     s_s[t] = am > 0.f ? __fdiv_rn(127.0f, am) : 0.f;
-    l1_s[t] = 0;
+    sq_s[t] = 0;
     if (blockIdx.x == 0 && c < C) scale[c] = am;
   }
   __syncthreads();
   const int cg = (t & 7) * 8;              // 8 consecutive columns
-  int l1c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  int sqc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int rl = (t >> 3) + 32 * i;
@@ -504,19 +504,19 @@ __global__ void __launch_bounds__(kThreads) col_quantize_kernel(const T* __restr
     for (int j = 0; j < 8; ++j) {
       const float q = fminf(127.f, fmaxf(-127.f, rint_small(__fmul_rn(__half2float(h[j]), s_s[cg + j]))));
       tile[(cg + j) * kCqPitch + rl] = __float2half_rn(q);   // exact: an integer of magnitude <= 127
-      l1c[j] += static_cast<int>(fabsf(q));
+      sqc[j] += static_cast<int>(q * q);
     }
   }
-  if (l1 != nullptr) {
+  if (sq != nullptr) {
     // lanes l, l ^ 8, l ^ 16, l ^ 24 hold the same 8 columns
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      l1c[j] += __shfl_xor_sync(0xffffffffu, l1c[j], 8);
-      l1c[j] += __shfl_xor_sync(0xffffffffu, l1c[j], 16);
+      sqc[j] += __shfl_xor_sync(0xffffffffu, sqc[j], 8);
+      sqc[j] += __shfl_xor_sync(0xffffffffu, sqc[j], 16);
     }
     if (lane < 8)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) atomicAdd(&l1_s[cg + j], l1c[j]);
+      for (int j = 0; j < 8; ++j) atomicAdd(&sq_s[cg + j], sqc[j]);
   }
   __syncthreads();
 #pragma unroll
@@ -529,19 +529,18 @@ __global__ void __launch_bounds__(kThreads) col_quantize_kernel(const T* __restr
       *reinterpret_cast<uint4*>(Xt + c * R_pad + r) = make_uint4(src[0], src[1], src[2], src[3]);
     }
   }
-  if (l1 != nullptr && t < kCqTile && c0 + t < C && l1_s[t] != 0)
-    atomicAdd(&l1[(c0 + t) * nchunks + (r0 >> 10)], l1_s[t]);
+  if (sq != nullptr && t < kCqTile && c0 + t < C && sq_s[t] != 0)
+    atomicAdd(&sq[(c0 + t) * nchunks + (r0 >> 10)], sq_s[t]);
 }
 
-// rowsmall[c] = 1 when every 1024-token chunk of column c has sum |code| <=
-// kSmallChunkL1 (so the GEMM's chunk sums of that output row stay below 2^22).
-__global__ void __launch_bounds__(kThreads) chunk_small_kernel(const int* __restrict__ l1, int64_t C, int64_t nchunks,
-                                                               uint8_t* __restrict__ rowsmall) {
-  for (int64_t c = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; c < C;
-       c += static_cast<int64_t>(gridDim.x) * kThreads) {
-    bool small = true;
-    for (int64_t k = 0; k < nchunks; ++k) small = small && l1[c * nchunks + k] <= kSmallChunkL1;
-    rowsmall[c] = small ? 1 : 0;
+// tsq[(c / 256) * nchunks + k] = max over the 256 columns c of a tile of
+// sq[c, k] (the per-tile chunk maxima of the accumulation plan).
+__global__ void __launch_bounds__(kThreads) tile_sq_kernel(const int* __restrict__ sq, int64_t C, int64_t nchunks,
+                                                           uint32_t* __restrict__ tsq) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < C * nchunks;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t c = i / nchunks, k = i - c * nchunks;
+    if (sq[i] != 0) atomicMax(tsq + (c >> 8) * nchunks + k, static_cast<uint32_t>(sq[i]));
   }
 }
 
@@ -610,10 +609,10 @@ template <typename T, typename OutT, int kBlock>
 __global__ void __launch_bounds__(kBlock) row_quantize_bulk_kernel(
     const T* __restrict__ A, int64_t M, int64_t K, int64_t ld, const uint32_t* __restrict__ mask,
     const int* __restrict__ idx, DevStatus* st, int64_t cap_pad, float* __restrict__ scale,
-    OutT* __restrict__ codes, __half* __restrict__ sub, uint8_t* __restrict__ rowsmall, int row_bytes) {
+    OutT* __restrict__ codes, __half* __restrict__ sub, uint32_t* __restrict__ asq, int row_bytes) {
   extern __shared__ __align__(16) uint8_t rowbuf[];   // two buffers of row_bytes (a multiple of 16)
   __shared__ float red[32];
-  __shared__ int chunk_l1[kStagedMaxChunks];
+  __shared__ int chunk_sq[kStagedMaxChunks];
   __shared__ __align__(8) uint64_t full[2];
   __shared__ int abort_flag;
   const int used = (mask != nullptr) ? st->used : 0;
@@ -659,14 +658,14 @@ __global__ void __launch_bounds__(kBlock) row_quantize_bulk_kernel(
       for (int j = 0; j < 8; ++j)
         if (!((bits >> j) & 1u)) amax = fmaxf(amax, fabsf(__half2float(h[j])));
     }
-    if (rowsmall != nullptr)
-      for (int k = threadIdx.x; k < nchunks; k += kBlock) chunk_l1[k] = 0;
+    if (asq != nullptr)
+      for (int k = threadIdx.x; k < nchunks; k += kBlock) chunk_sq[k] = 0;
     amax = block_max(amax, red);
     const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
     OutT* out = codes + m * ld;
     for (int64_t c0 = 0; c0 < ld; c0 += kBlock * 8) {   // every thread runs every iteration
       const int64_t c = c0 + static_cast<int64_t>(threadIdx.x) * 8;
-      float l1 = 0.f;
+      float sq = 0.f;
       if (c < ld) {
         __half h[8];
         if (c < K) {
@@ -681,7 +680,7 @@ __global__ void __launch_bounds__(kBlock) row_quantize_bulk_kernel(
         for (int j = 0; j < 8; ++j) {
           const float r = rint_small(__fmul_rn(__half2float(h[j]), s));
           q[j] = ((bits >> j) & 1u) ? 0.f : fminf(127.f, fmaxf(-127.f, r));
-          l1 += fabsf(q[j]);
+          sq += q[j] * q[j];
         }
         if constexpr (sizeof(OutT) == 1) {
           uint32_t w[8];
@@ -697,35 +696,32 @@ __global__ void __launch_bounds__(kBlock) row_quantize_bulk_kernel(
           *reinterpret_cast<uint4*>(out + c) = o;
         }
       }
-      if (rowsmall != nullptr) {
-        int v = static_cast<int>(l1);
+      if (asq != nullptr) {
+        int v = static_cast<int>(sq);
 #pragma unroll
         for (int k = 16; k > 0; k >>= 1) v += __shfl_xor_sync(0xffffffffu, v, k);
         const int64_t cw = c0 + static_cast<int64_t>(threadIdx.x & ~31) * 8;
-        if ((threadIdx.x & 31) == 0 && v != 0) atomicAdd(&chunk_l1[cw >> 10], v);
+        if ((threadIdx.x & 31) == 0 && v != 0) atomicAdd(&chunk_sq[cw >> 10], v);
       }
     }
     if (sub != nullptr) {
       for (int j = threadIdx.x; j < used_pad; j += kBlock)
         sub[m * cap_pad + j] = (j < used) ? to_half(row[idx[j]]) : __float2half_rn(0.f);
     }
-    bool small = true;
-    if (rowsmall != nullptr) {
+    if (asq != nullptr) {
       __syncthreads();
-      for (int k = threadIdx.x; k < nchunks; k += kBlock) small = small && chunk_l1[k] <= kSmallChunkL1;
+      for (int k = threadIdx.x; k < nchunks; k += kBlock)
+        if (chunk_sq[k] != 0) atomicMax(asq + (m >> 8) * nchunks + k, static_cast<uint32_t>(chunk_sq[k]));
     }
-    small = __syncthreads_and(small) != 0;   // also: this row buffer is no longer read
-    if (threadIdx.x == 0) {
-      if (rowsmall != nullptr) rowsmall[m] = small ? 1 : 0;
-      scale[m] = amax;
-    }
+    __syncthreads();   // also: this row buffer is no longer read
+    if (threadIdx.x == 0) scale[m] = amax;
   }
 }
 
 template <typename T, typename OutT>
 cudaError_t launch_bulk(int prof_id, const T* A, int64_t M, int64_t K, int64_t K_pad, const uint32_t* mask,
                         const int* idx, DevStatus* st, int64_t cap_pad, float* scale, OutT* codes, __half* sub,
-                        uint8_t* rowsmall, cudaStream_t s) {
+                        uint32_t* asq, cudaStream_t s) {
   const int row_bytes = static_cast<int>(round_up(K * static_cast<int64_t>(sizeof(T)), 16));
   const int smem = 2 * row_bytes;
   // long rows: one block per SM holds both buffers, so it gets 1024 threads
@@ -749,7 +745,7 @@ cudaError_t launch_bulk(int prof_id, const T* A, int64_t M, int64_t K, int64_t K
   const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(sms) * per_sm));
   ProfScope ps(prof_id, s);
   row_quantize_bulk_kernel<T, OutT, kBlock><<<grid, kBlock, smem, s>>>(A, M, K, K_pad, mask, idx, st, cap_pad, scale, codes,
-                                                                 sub, rowsmall, row_bytes);
+                                                                 sub, asq, row_bytes);
   return cudaGetLastError();
 }
 
@@ -758,7 +754,7 @@ cudaError_t launch_bulk(int prof_id, const T* A, int64_t M, int64_t K, int64_t K
 template <typename T, typename OutT>
 cudaError_t launch_staged(int prof_id, const T* A, int64_t M, int64_t K, int64_t K_pad, bool vec, const uint32_t* mask,
                           const int* idx, const DevStatus* st, int64_t cap_pad, float* scale, OutT* codes,
-                          __half* sub, uint8_t* rowsmall, cudaStream_t s) {
+                          __half* sub, uint32_t* asq, cudaStream_t s) {
   const int smem = static_cast<int>(K_pad * 2);
   static bool done = false;
   if (!done) {
@@ -779,7 +775,7 @@ cudaError_t launch_staged(int prof_id, const T* A, int64_t M, int64_t K, int64_t
   const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(sms) * per_sm));
   ProfScope ps(prof_id, s);
   act_quantize_staged_kernel<T, OutT><<<grid, kThreads, smem, s>>>(A, M, K, K_pad, vec ? 1 : 0, mask, idx, st, cap_pad,
-                                                                   scale, codes, sub, rowsmall);
+                                                                   scale, codes, sub, asq);
   return cudaGetLastError();
 }
 
@@ -822,19 +818,19 @@ cudaError_t launch_outlier_index(const uint32_t* colmax, int64_t K, float thr, i
 
 cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int64_t K_pad, bool vec,
                                 const uint32_t* mask, const int* idx, DevStatus* st, int64_t cap_pad,
-                                float* SCA, __half* Aq, __half* subA, uint8_t* rowsmall, cudaStream_t s) {
+                                float* SCA, __half* Aq, __half* subA, uint32_t* asq, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
   return dispatch_dt(at, [&](auto* tag) {
     using T = std::remove_pointer_t<decltype(tag)>;
     if (vec && K * static_cast<int64_t>(sizeof(T)) <= kBulkMaxRowBytes)
       return launch_bulk<T, __half>(K_ROW_QUANTIZE, static_cast<const T*>(A), M, K, K_pad, mask, idx, st, cap_pad,
-                                    SCA, Aq, subA, rowsmall, s);
+                                    SCA, Aq, subA, asq, s);
     if (K_pad <= kStagedMaxLd)
       return launch_staged<T, __half>(K_ROW_QUANTIZE, static_cast<const T*>(A), M, K, K_pad, vec, mask, idx, st,
-                                      cap_pad, SCA, Aq, subA, rowsmall, s);
+                                      cap_pad, SCA, Aq, subA, asq, s);
     ProfScope ps(K_ROW_QUANTIZE, s);
     row_quantize_kernel<T, __half><<<grid_rows(M), kThreads, 0, s>>>(
-        static_cast<const T*>(A), M, K, K_pad, vec ? 1 : 0, mask, idx, st, cap_pad, SCA, Aq, subA, rowsmall);
+        static_cast<const T*>(A), M, K, K_pad, vec ? 1 : 0, mask, idx, st, cap_pad, SCA, Aq, subA, asq);
     return cudaGetLastError();
   });
 }
@@ -879,7 +875,7 @@ cudaError_t launch_gradout_prepass(const void* G, int gt, int64_t M, int64_t N, 
 }
 
 cudaError_t launch_col_quantize(const void* X, int xt, int64_t R, int64_t C, bool vec, const uint32_t* colmax,
-                                int64_t R_pad, float* scale, __half* Xt, int* l1, uint8_t* rowsmall, cudaStream_t s) {
+                                int64_t R_pad, float* scale, __half* Xt, int* sq, uint32_t* tsq, cudaStream_t s) {
   if (R_pad == 0 || C == 0) return cudaSuccess;
   const int64_t nchunks = ceil_div(R_pad, 1024);
   const dim3 grid(static_cast<unsigned>(ceil_div(R_pad, kCqTile)), static_cast<unsigned>(ceil_div(C, kCqTile)));
@@ -887,13 +883,13 @@ cudaError_t launch_col_quantize(const void* X, int xt, int64_t R, int64_t C, boo
     using T = std::remove_pointer_t<decltype(tag)>;
     ProfScope ps(K_COL_QUANTIZE, s);
     col_quantize_kernel<T><<<grid, kThreads, 0, s>>>(static_cast<const T*>(X), R, C, vec ? 1 : 0, colmax, R_pad, scale,
-                                                    Xt, l1, nchunks);
+                                                    Xt, sq, nchunks);
     return cudaGetLastError();
   });
-  if (e != cudaSuccess || rowsmall == nullptr) return e;
+  if (e != cudaSuccess || sq == nullptr) return e;
   ProfScope ps(K_COL_QUANTIZE, s);
-  chunk_small_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(C, kThreads), 1024)), kThreads, 0, s>>>(
-      l1, C, nchunks, rowsmall);
+  tile_sq_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(C * nchunks, kThreads), 4096)), kThreads, 0, s>>>(
+      sq, C, nchunks, tsq);
   return cudaGetLastError();
 }
 

@@ -61,6 +61,7 @@ def gpu_forward(A, CB, SCB, K, bias=None, threshold=6.0, residual=None, max_outl
     out, ws = I.forward(A, CB, SCB, K, bias, threshold, residual=residual, max_outliers=cap, acc_i32=acc)
     st, found = I.device_status(ws)
     lay = _lib.i8lt_forward_workspace_layout(M, K, N, cap)
+    nch = (lay.k_pad + 1023) // 1024
     w = ws
 
     def region(off, nbytes, dtype, shape):
@@ -70,7 +71,10 @@ def gpu_forward(A, CB, SCB, K, bias=None, threshold=6.0, residual=None, max_outl
     used = int(status[2]) if cap > 0 else 0
     res = dict(out=out, acc=acc, status=st, found=found, used=used, ws=ws,
                SCA=region(lay.sca, M * 4, torch.float32, (M,)),
-               rowsmall=region(lay.rowsmall, M, torch.uint8, (M,)),
+               asq=region(lay.asq, (M + 255) // 256 * nch * 4, torch.int32, ((M + 255) // 256, nch)),
+               bsq=region(lay.bsq, (N + 255) // 256 * nch * 4, torch.int32, ((N + 255) // 256, nch)),
+               plan=region(lay.plan, (M + 255) // 256 * ((N + 255) // 256) * 4, torch.int32,
+                           ((M + 255) // 256, (N + 255) // 256)),
                Aq=region(lay.aq, M * lay.k_pad * 2, torch.float16, (M, lay.k_pad)),
                k_pad=lay.k_pad, cap_pad=lay.cap_pad)
     if cap > 0:

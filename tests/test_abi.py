@@ -29,7 +29,7 @@ def test_exports_every_declared_function(L):
 
 
 def test_version_and_strings(L):
-    assert _lib.i8lt_abi_version() == 1
+    assert _lib.i8lt_abi_version() == 2
     for code in range(10):
         assert _lib.i8lt_status_string(code) != "unknown status"
     assert _lib.i8lt_status_string(42) == "unknown status"
@@ -46,12 +46,15 @@ def test_forward_layout(L):
     assert lay.k_pad == 16 and lay.cap_pad == 0
     M, K, N, cap = 2048, 4096, 4096, 256
     lay = _lib.i8lt_forward_workspace_layout(M, K, N, cap)
-    offs = [lay.status, lay.colmax, lay.mask, lay.idx, lay.sca, lay.rowsmall, lay.aq, lay.suba, lay.subb, lay.cbh,
-            lay.total]
+    offs = [lay.status, lay.asq, lay.bsq, lay.colmax, lay.mask, lay.idx, lay.sca, lay.plan, lay.aq, lay.suba,
+            lay.subb, lay.cbh, lay.total]
     assert offs == sorted(offs)
     assert all(o % 256 == 0 for o in offs)
-    assert lay.rowsmall - lay.sca >= M * 4
-    assert lay.aq - lay.rowsmall >= M
+    nch = (lay.k_pad + 1023) // 1024
+    assert lay.bsq - lay.asq >= (M + 255) // 256 * nch * 4
+    assert lay.colmax - lay.bsq >= (N + 255) // 256 * nch * 4
+    assert lay.plan - lay.sca >= M * 4
+    assert lay.aq - lay.plan >= (M + 255) // 256 * ((N + 255) // 256) * 4
     assert lay.suba - lay.aq >= M * lay.k_pad * 2
     assert lay.subb - lay.suba >= M * lay.cap_pad * 2
     assert lay.cbh - lay.subb >= N * lay.cap_pad * 2

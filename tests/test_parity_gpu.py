@@ -125,29 +125,66 @@ def test_exact_int32_beyond_fp32_range():
     check_forward_stages(res, ref)
 
 
-def test_mixed_row_magnitudes_in_one_tile():
-    """Rows whose 1024-deep chunk sums stay below 2^22 use the fast exact
-    conversion, the others the conversion instruction; both kinds share
-    tiles here.  The per-row flag equals its definition on the oracle's
-    codes and the int32 accumulator is exact for every row."""
-    M, K, N = 200, 2100, 300
-    g = torch.Generator().manual_seed(17)
+def _chunk_tile_max(codes, k_pad):
+    """Per 256-row tile and 1024-column chunk, the largest sum of squared
+    codes of one row of the tile in that chunk (zero padding past K)."""
+    R, Kc = codes.shape
+    q = np.zeros((R, k_pad), np.int64)
+    q[:, :Kc] = codes
+    nch = (k_pad + 1023) // 1024
+    sq = np.stack([(q[:, c * 1024:(c + 1) * 1024] ** 2).sum(1) for c in range(nch)], 1)
+    return np.stack([sq[t:t + 256].max(0) for t in range(0, R, 256)])
+
+
+def _plan(asq, bsq):
+    """The accumulation plan by its definition: per tile pair, the largest
+    L such that every group of L consecutive chunks (the last one ragged)
+    has sum(asq) * sum(bsq) < 2^48, and the fast-conversion bit when every
+    such group stays below 2^44."""
+    nch = asq.shape[1]
+    plan = np.zeros((asq.shape[0], bsq.shape[0]), np.int64)
+    for i in range(asq.shape[0]):
+        for j in range(bsq.shape[0]):
+            for L in range(nch, 0, -1):
+                p = [int(asq[i, c:c + L].sum()) * int(bsq[j, c:c + L].sum()) for c in range(0, nch, L)]
+                if all(x < 2 ** 48 for x in p) or L == 1:
+                    plan[i, j] = L | ((1 << 16) if all(x < 2 ** 44 for x in p) else 0)
+                    break
+    return plan
+
+
+def test_accumulation_plan():
+    """The GEMM accumulates exactly in fp32 over groups of 1024-deep chunks
+    chosen per tile pair from the chunk sums of squared codes (Cauchy-Schwarz
+    bounds every partial sum below 2^24).  Row tiles of saturated, ordinary
+    and small codes against weight tiles of the same kinds give groups of one
+    chunk, of all chunks and in between, fast and slow conversions; the chunk
+    maxima and the plan equal their definitions on the oracle's codes and the
+    int32 accumulator is exact for every tile pair."""
+    M, K, N = 700, 5000, 600
+    g = torch.Generator().manual_seed(29)
     A = torch.randn(M, K, generator=g).half()
-    A[::3] = 1.0                      # constant rows: every code 127, chunk sums ~ 1024 * 127^2
-    A[1::7] = -0.5
+    A[:256] = 1.0                                   # tile 0: every code 127
+    A[512:] = (torch.rand(M - 512, K, generator=g) < 0.01).half() * torch.randn(M - 512, K, generator=g).half()
     Wf = (torch.randn(N, K, generator=g) * 0.02).half()
-    Wf[:40] = 0.25                    # constant weight rows: sums of the constant A rows hit K * 127^2
+    Wf[:256] = 0.25                                 # weight tile 0: every code 127
+    Wf[512:] = Wf[512:] * (torch.rand(N - 512, K, generator=g) < 0.02).half()
     CB, SCB = I.quantize_weight(Wf.to(DEV))
     CB_ref, SCB_ref = check_weight(CB, SCB, Wf, K)
     res = gpu_forward(A.to(DEV), CB, SCB, K, None, math.inf)
     ref = O.forward(to_np(A), O.F16, CB_ref, SCB_ref, threshold=math.inf)
     check_forward_stages(res, ref)
-    aq = np.abs(ref["Aq"].astype(np.int64))
-    chunks = [aq[:, c:c + 1024].sum(1) for c in range(0, K, 1024)]
-    want = np.all(np.stack(chunks, 1) <= 33026, axis=1)
-    got = to_np(res["rowsmall"]).astype(bool)
-    assert np.array_equal(got, want)
-    assert want.any() and (~want).any()
+    k_pad = res["k_pad"]
+    asq = _chunk_tile_max(ref["Aq"].astype(np.int64), k_pad)
+    bsq = _chunk_tile_max(CB_ref.astype(np.int64), k_pad)
+    assert np.array_equal(to_np(res["asq"]).astype(np.int64), asq)
+    assert np.array_equal(to_np(res["bsq"]).astype(np.int64), bsq)
+    plan = _plan(asq, bsq)
+    assert np.array_equal(to_np(res["plan"]).astype(np.int64), plan)
+    L, fast = plan & 0xFFFF, plan >> 16
+    nch = asq.shape[1]
+    assert L.min() == 1 and L.max() == nch and ((L > 1) & (L < nch)).any()
+    assert fast.any() and (fast == 0).any()
 
 
 def test_max_k_accumulator():

@@ -29,19 +29,23 @@ def _built():
 
 def _ws_regions(ws, M, N, K):
     """Workspace regions in the order i8lt_grad_weight lays them out (each
-    256-byte aligned): status, colmax G, colmax A, scale G, scale A,
-    rowsmall G, l1 G, Gt, At."""
+    256-byte aligned): status, colmax G, colmax A, scale G, scale A, tile
+    chunk maxima G and A, chunk sums G and A, plan, Gt, At."""
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
     r_pad = (M + 15) // 16 * 16
     chunks = (r_pad + 1023) // 1024
-    sizes = [256, up(N * 4), up(K * 4), up(N * 4), up(K * 4), up(N), up(N * chunks * 4), up(N * r_pad * 2),
-             up(K * r_pad * 2)]
+    tn, tk = (N + 255) // 256, (K + 255) // 256
+    sizes = [256, up(N * 4), up(K * 4), up(N * 4), up(K * 4), up(tn * chunks * 4), up(tk * chunks * 4),
+             up(N * chunks * 4), up(K * chunks * 4), up(tn * tk * 4), up(N * r_pad * 2), up(K * r_pad * 2)]
     off = np.cumsum([0] + sizes)
     assert off[-1] == _lib.i8lt_grad_weight_workspace_size(M, N, K)
     return dict(scale_g=ws[off[3]:off[3] + 4 * N].view(torch.float32),
                 scale_a=ws[off[4]:off[4] + 4 * K].view(torch.float32),
-                gt=ws[off[7]:off[7] + N * r_pad * 2].view(torch.float16).reshape(N, r_pad),
-                at=ws[off[8]:off[8] + K * r_pad * 2].view(torch.float16).reshape(K, r_pad))
+                tsq_g=ws[off[5]:off[5] + 4 * tn * chunks].view(torch.int32).reshape(tn, chunks),
+                tsq_a=ws[off[6]:off[6] + 4 * tk * chunks].view(torch.int32).reshape(tk, chunks),
+                plan=ws[off[9]:off[9] + 4 * tn * tk].view(torch.int32).reshape(tn, tk),
+                gt=ws[off[10]:off[10] + N * r_pad * 2].view(torch.float16).reshape(N, r_pad),
+                at=ws[off[11]:off[11] + K * r_pad * 2].view(torch.float16).reshape(K, r_pad))
 
 
 @pytest.mark.parametrize("M,N,K,dtype", [(300, 520, 1100, torch.float16),    # 2 exact chunks of tokens, ragged
