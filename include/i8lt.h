@@ -299,6 +299,68 @@ int i8lt_grad_weight(const void* G, int gt, const void* A, int at,
                      int64_t M, int64_t N, int64_t K,
                      void* grad_W, int wt, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * 4-bit NormalFloat (NF4) weight-only layer: QLoRA fine-tuning keeps the
+ * frozen base weights in 4 bits and runs every matmul in the 16-bit compute
+ * dtype ("Support QLoRA 4-bit finetuning with bitsandbytes", lit-gpt PR #275:
+ * the bnb.nf4 quantize option, Llama-2-7B runs with --precision bf16-true).
+ * The page does not define the format; the library follows QLoRA's published
+ * 4-bit NormalFloat construction:
+ *   levels   16 fp32 values from -1 to 1 with an exact 0 (index 7): 7 negated
+ *            and 8 positive standard-normal quantiles of evenly spaced
+ *            probabilities between 1/2 and ((1 - 1/30) + (1 - 1/32)) / 2,
+ *            divided by the largest (i8lt_nf4_levels returns them);
+ *   blocks   64 consecutive elements of a weight row share one fp32 absmax;
+ *   codes    the nearest level to x / absmax (one fp32 division), decided
+ *            against the fp32 midpoints of adjacent levels (a value equal to
+ *            a midpoint takes the lower level); all-zero blocks and the
+ *            padding take the zero level;
+ *   packing  row n of `packed` holds i8lt_nf4_row_bytes(K) bytes, two codes
+ *            per byte, element 2j in the high nibble of byte j;
+ *   dequantization  Wdq[n, k] = rn(levels[code] * absmax[n, k / 64]), one
+ *            fp32 multiply rounded once to the compute dtype.
+ * The nf4-dq variant (absmax stored in 8 bits) is not provided.
+ */
+#define I8LT_NF4_BLOCK 64
+/* out[16]: the levels, ascending. */
+int i8lt_nf4_levels(float* out);
+/* Bytes per packed row: round_up(K, 64) / 2 (a multiple of 32); -1 for K < 0. */
+int64_t i8lt_nf4_row_bytes(int64_t K);
+/* absmax values per row: ceil(K / 64); -1 for K < 0. */
+int64_t i8lt_nf4_blocks(int64_t K);
+/* W [N, K] row-major (dtype wt, device) -> packed [N, row_bytes] uint8 and
+ * absmax [N, blocks] fp32, both device, caller-owned.  packed 16-byte
+ * aligned. */
+int i8lt_nf4_quantize(const void* W, int wt, int64_t N, int64_t K,
+                      uint8_t* packed, float* absmax, void* stream);
+/* The dequantized weight Wdq [N, K] row-major in dtype dt (device). */
+int i8lt_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N,
+                        int64_t K, void* out, int dt, void* stream);
+/* Workspace of the two matmuls: the device status word (256 bytes). */
+size_t i8lt_nf4_workspace_size(void);
+/*
+ * out [M, N] = rn(A [M, K] @ Wdq^T + bias), A and out in the compute dtype
+ * at (I8LT_F16 or I8LT_BF16), fp32 accumulation on the tensor
+ * cores; the weight is decoded stage by stage in shared memory and never
+ * stored.  bias [N] of dtype bt or NULL.  K a multiple of 8 (16-byte rows
+ * for the tensor-memory copies), else I8LT_ERR_INVALID_ARG; A, packed, out
+ * 16-byte aligned; ws of i8lt_nf4_workspace_size bytes, 256-byte aligned.
+ */
+int i8lt_nf4_forward(const void* A, int at, int64_t M, int64_t K,
+                     const uint8_t* packed, const float* absmax, int64_t N,
+                     const void* bias, int bt, void* out,
+                     void* ws, size_t ws_bytes, void* stream);
+/*
+ * grad_A [M, K] = rn(G [M, N] @ Wdq) in the compute dtype gt, the gradient
+ * to the input of the frozen 4-bit layer (the weight has none), with the
+ * weight decoded the same way.  N a multiple of 8; other rules as
+ * i8lt_nf4_forward.
+ */
+int i8lt_nf4_backward_input(const void* G, int gt, int64_t M, int64_t N,
+                            const uint8_t* packed, const float* absmax,
+                            int64_t K, void* grad_A, void* ws, size_t ws_bytes,
+                            void* stream);
+
 /* SiLU between the two layers of an MLP: out = h * sigmoid(h), and its
  * backward out = g * silu'(h).  n elements of dtype dt. */
 int i8lt_silu_forward(const void* h, int dt, int64_t n, void* out, void* stream);
@@ -318,7 +380,8 @@ typedef enum {
   I8LT_K_SUBB = 4, I8LT_K_FWD_GEMM = 5, I8LT_K_GRADOUT_PREPASS = 6, I8LT_K_GRAD_BIAS_FINALIZE = 7,
   I8LT_K_BWD_GEMM = 8, I8LT_K_SILU = 9, I8LT_K_SILU_BACKWARD = 10, I8LT_K_WIDEN_CODES = 11,
   I8LT_K_DEQUANT_WEIGHT = 12, I8LT_K_COL_QUANTIZE = 13, I8LT_K_WGRAD_GEMM = 14, I8LT_K_UNIT_PLAN = 15,
-  I8LT_K_COUNT = 16
+  I8LT_K_NF4_QUANTIZE = 16, I8LT_K_NF4_DEQUANTIZE = 17, I8LT_K_NF4_GEMM_FWD = 18, I8LT_K_NF4_GEMM_BWD = 19,
+  I8LT_K_COUNT = 20
 } i8lt_kernel_id;
 typedef struct {
   int kernel;

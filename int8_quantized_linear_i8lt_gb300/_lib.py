@@ -50,7 +50,8 @@ class i8lt_kernel_time(Structure):
 
 KERNELS = ("quantize_weight", "colmax", "outlier_index", "row_quantize", "build_subB", "fwd_gemm",
            "gradout_prepass", "grad_bias_finalize", "bwd_gemm", "silu", "silu_backward", "widen_codes",
-           "dequant_weight", "col_quantize", "wgrad_gemm", "unit_plan")
+           "dequant_weight", "col_quantize", "wgrad_gemm", "unit_plan", "nf4_quantize", "nf4_dequantize",
+           "nf4_gemm_fwd", "nf4_gemm_bwd")
 
 
 # name -> (restype, argtypes); the same names and order as include/i8lt.h
@@ -82,6 +83,16 @@ SIGNATURES = {
                                     c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
     "i8lt_backward_input_noalloc": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
                                             c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
+    "i8lt_nf4_levels": (c_int, [POINTER(c_float)]),
+    "i8lt_nf4_row_bytes": (c_int64, [c_int64]),
+    "i8lt_nf4_blocks": (c_int64, [c_int64]),
+    "i8lt_nf4_quantize": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_void_p]),
+    "i8lt_nf4_dequantize": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_int, c_void_p]),
+    "i8lt_nf4_workspace_size": (c_size_t, []),
+    "i8lt_nf4_forward": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64, c_void_p, c_int,
+                                 c_void_p, c_void_p, c_size_t, c_void_p]),
+    "i8lt_nf4_backward_input": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64, c_void_p,
+                                        c_void_p, c_size_t, c_void_p]),
     "i8lt_silu_forward": (c_int, [c_void_p, c_int, c_int64, c_void_p, c_void_p]),
     "i8lt_silu_backward": (c_int, [c_void_p, c_void_p, c_int, c_int64, c_void_p, c_void_p]),
     "i8lt_profile_start": (c_int, [c_int]),
@@ -207,6 +218,42 @@ def i8lt_backward_input(G, gt, M, N, CB, SCB, K, addend, grad_A, grad_bias, bt, 
 def i8lt_backward_input_noalloc(G, gt, M, N, CB, SCB, K, addend, grad_A, grad_bias, bt, stream=None) -> int:
     return load().i8lt_backward_input_noalloc(_p(G), gt, M, N, _p(CB), _p(SCB), K, _p(addend), _p(grad_A),
                                               _p(grad_bias), bt, _p(stream))
+
+
+def i8lt_nf4_levels():
+    out = (c_float * 16)()
+    st = load().i8lt_nf4_levels(out)
+    return st, list(out)
+
+
+def i8lt_nf4_row_bytes(K) -> int:
+    return load().i8lt_nf4_row_bytes(int(K))
+
+
+def i8lt_nf4_blocks(K) -> int:
+    return load().i8lt_nf4_blocks(int(K))
+
+
+def i8lt_nf4_quantize(W, wt, N, K, packed, absmax, stream=None) -> int:
+    return load().i8lt_nf4_quantize(_p(W), wt, N, K, _p(packed), _p(absmax), _p(stream))
+
+
+def i8lt_nf4_dequantize(packed, absmax, N, K, out, dt, stream=None) -> int:
+    return load().i8lt_nf4_dequantize(_p(packed), _p(absmax), N, K, _p(out), dt, _p(stream))
+
+
+def i8lt_nf4_workspace_size() -> int:
+    return load().i8lt_nf4_workspace_size()
+
+
+def i8lt_nf4_forward(A, at, M, K, packed, absmax, N, bias, bt, out, ws, ws_bytes, stream=None) -> int:
+    return load().i8lt_nf4_forward(_p(A), at, M, K, _p(packed), _p(absmax), N, _p(bias), bt, _p(out), _p(ws),
+                                   ws_bytes, _p(stream))
+
+
+def i8lt_nf4_backward_input(G, gt, M, N, packed, absmax, K, grad_A, ws, ws_bytes, stream=None) -> int:
+    return load().i8lt_nf4_backward_input(_p(G), gt, M, N, _p(packed), _p(absmax), K, _p(grad_A), _p(ws), ws_bytes,
+                                          _p(stream))
 
 
 def i8lt_silu_forward(h, dt, n, out, stream=None) -> int:

@@ -474,6 +474,7 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_
     return I8LT_ERR_CUDA;
   }
   BwdEpiArgs ea;
+  std::memset(&ea, 0, sizeof(ea));
   ea.M = static_cast<int>(M);
   ea.N = static_cast<int>(N);
   ea.K = static_cast<int>(K);
@@ -558,6 +559,106 @@ int i8lt_grad_weight(const void* G, int gt, const void* A, int at, int64_t M, in
   return cuda_status(launch_fwd_gemm(g, ea, s, K_WGRAD_GEMM));
 }
 
+int i8lt_nf4_levels(float* out) {
+  if (out == nullptr) return I8LT_ERR_INVALID_ARG;
+  nf4_levels(out);
+  return I8LT_OK;
+}
+
+int64_t i8lt_nf4_row_bytes(int64_t K) { return K < 0 ? -1 : round_up(K, 64) / 2; }
+
+int64_t i8lt_nf4_blocks(int64_t K) { return K < 0 ? -1 : ceil_div(K, 64); }
+
+int i8lt_nf4_quantize(const void* W, int wt, int64_t N, int64_t K, uint8_t* packed, float* absmax, void* stream) {
+  if (!valid_dt(wt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (N < 0 || K < 0 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return I8LT_OK;
+  if (W == nullptr || packed == nullptr || absmax == nullptr) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(packed)) return I8LT_ERR_MISALIGNED;
+  if (int d = check_device()) return d;
+  return cuda_status(launch_nf4_quantize(W, wt, N, K, i8lt_nf4_row_bytes(K), packed, absmax,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int i8lt_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, int64_t K, void* out, int dt,
+                        void* stream) {
+  if (!valid_dt(dt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (N < 0 || K < 0 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return I8LT_OK;
+  if (packed == nullptr || absmax == nullptr || out == nullptr) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(packed)) return I8LT_ERR_MISALIGNED;
+  if (int d = check_device()) return d;
+  return cuda_status(launch_nf4_dequantize(packed, absmax, N, K, i8lt_nf4_row_bytes(K), out, dt,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+size_t i8lt_nf4_workspace_size(void) { return kAlign; }
+
+}  // extern "C"
+
+namespace {
+
+// The two 4-bit matmuls: D[r, m] = sum_c Wdq(r, c) X[m, c] with the packed
+// weight decoded per stage (input_grad: r = k, c = n; forward: r = n, c = k).
+int nf4_gemm(bool input_grad, const void* X, int xt, int64_t M, int64_t C, int64_t R, const uint8_t* packed,
+             const float* absmax, int64_t K, int64_t N, const void* bias, int bt, void* out, void* ws,
+             size_t ws_bytes, void* stream) {
+  if (xt != DT_F16 && xt != DT_BF16) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (bias != nullptr && !valid_dt(bt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if (M < 0 || K <= 0 || N <= 0) return I8LT_ERR_INVALID_ARG;
+  if (M > INT32_MAX / 2 || K > INT32_MAX / 2 || N > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
+  if (C % 8 != 0) return I8LT_ERR_INVALID_ARG;   // 16-byte rows of X for the tensor copies
+  if (ws == nullptr || packed == nullptr || absmax == nullptr) return I8LT_ERR_INVALID_ARG;
+  if (M > 0 && (X == nullptr || out == nullptr)) return I8LT_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(packed) || !aligned16(out)) return I8LT_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
+  if (ws_bytes < kAlign) return I8LT_ERR_WORKSPACE;
+  if (int d = check_device()) return d;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus* st = static_cast<DevStatus*>(ws);
+  if (cudaMemsetAsync(st, 0, sizeof(DevStatus), s) != cudaSuccess) return I8LT_ERR_CUDA;
+  if (M == 0) return I8LT_OK;
+  const int64_t row_bytes = i8lt_nf4_row_bytes(K);
+  const CUtensorMapDataType xdt = xt == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  BwdGemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  if (!make_tmap(&g.tmG, xdt, X, C, M, C * 2, kBK, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B)) return I8LT_ERR_CUDA;
+  // weight tiles: [64 n][128 k] (64 bytes a row) for the input gradient,
+  // [128 n][64 k] (32 bytes a row) for the forward
+  if (!make_tmap(&g.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, row_bytes, N, row_bytes, input_grad ? 64 : 32,
+                 input_grad ? kBK : kBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return I8LT_ERR_CUDA;
+  BwdEpiArgs ea;
+  std::memset(&ea, 0, sizeof(ea));
+  ea.M = static_cast<int>(M);
+  ea.N = static_cast<int>(C);
+  ea.K = static_cast<int>(R);
+  ea.grad_A = out;
+  ea.dt = xt;
+  ea.st = st;
+  ea.bias = bias;
+  ea.bias_dt = bt;
+  ea.ab_fmt = xt == DT_BF16 ? ((1u << 7) | (1u << 10)) : 0u;   // A and B format: bf16
+  ea.absmax = absmax;
+  ea.nblk = static_cast<int>(ceil_div(K, 64));
+  nf4_levels(ea.lv);
+  return cuda_status(launch_nf4_gemm(g, ea, input_grad, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int i8lt_nf4_forward(const void* A, int at, int64_t M, int64_t K, const uint8_t* packed, const float* absmax,
+                     int64_t N, const void* bias, int bt, void* out, void* ws, size_t ws_bytes, void* stream) {
+  return nf4_gemm(false, A, at, M, K, N, packed, absmax, K, N, bias, bt, out, ws, ws_bytes, stream);
+}
+
+int i8lt_nf4_backward_input(const void* G, int gt, int64_t M, int64_t N, const uint8_t* packed, const float* absmax,
+                            int64_t K, void* grad_A, void* ws, size_t ws_bytes, void* stream) {
+  return nf4_gemm(true, G, gt, M, N, K, packed, absmax, K, N, nullptr, 0, grad_A, ws, ws_bytes, stream);
+}
+
 int i8lt_silu_forward(const void* h, int dt, int64_t n, void* out, void* stream) {
   if (!valid_dt(dt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
   if (n < 0 || (n > 0 && (h == nullptr || out == nullptr))) return I8LT_ERR_INVALID_ARG;
@@ -615,7 +716,8 @@ const char* i8lt_kernel_name(int k) {
   static const char* names[] = {"quantize_weight", "colmax",          "outlier_index",      "row_quantize",
                                 "build_subB",      "fwd_gemm",        "gradout_prepass",    "grad_bias_finalize",
                                 "bwd_gemm",        "silu",            "silu_backward",      "widen_codes",
-                                "dequant_weight",  "col_quantize",    "wgrad_gemm",         "unit_plan"};
+                                "dequant_weight",  "col_quantize",    "wgrad_gemm",         "unit_plan",
+                                "nf4_quantize",    "nf4_dequantize",  "nf4_gemm_fwd",       "nf4_gemm_bwd"};
   return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
 }
 

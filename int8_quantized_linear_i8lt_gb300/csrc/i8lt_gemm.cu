@@ -105,12 +105,14 @@ struct __align__(8) Barriers {
   uint64_t teardown;            // even CTA: every MMA finished
   uint32_t tmem_base;
   int abort_flag;
+  float lv[16];                 // 4-bit schedules: the code levels, for the converters
 };
 
 // stage s of each CTA: [A operand 16 KB][B operand(s) 16 KB each] fp16,
 // 128B-swizzled.
 constexpr int kOpBytes = kCtaRows * kBK * 2;   // 16 KB
 constexpr int kI8Bytes = kCtaRows * kBK;       // 8 KB
+constexpr int kNf4Bytes = kCtaRows * kBK / 2;  // 4 KB: 4-bit weight tiles
 constexpr int kFwdStageBytes = 2 * kOpBytes;
 constexpr int kFwdSmemBytes = 1024 /*align slack*/ + kFwdStages * kFwdStageBytes + 3 * kPairN * 4 /*epilogue vectors*/ +
                               static_cast<int>(sizeof(Barriers));
@@ -126,21 +128,34 @@ constexpr int kFwdSmemBytes = 1024 /*align slack*/ + kFwdStages * kFwdStageBytes
 // it will be converted into is still being read by the tensor cores, so the
 // copy latency and the conversion and hand-over latency overlap instead of
 // adding up.
-template <bool kFused>
+//
+// The same kernel runs the 4-bit NormalFloat weight-only matmuls (QLoRA
+// fine-tuning with frozen 4-bit weights): the converters decode 4-bit codes
+// with per-64-element absmax scales instead of int8 rows with a row scale.
+// kModeNf4T is the input gradient (D[k, m] = sum_n Wdq[n, k] G[m, n], the
+// converted tile MN-major like the int8 one); kModeNf4 the forward
+// (D[n, m] = sum_k Wdq[n, k] A[m, k], the converted tile K-major).
+enum BwdMode { kModeMat = 0, kModeI8 = 1, kModeNf4T = 2, kModeNf4 = 3 };
+
+template <int kMode>
 struct BwdGeom {
+  static constexpr bool kFused = kMode != kModeMat;
+  static constexpr bool kNf4 = kMode == kModeNf4T || kMode == kModeNf4;
+  static constexpr bool kAmn = kMode == kModeI8 || kMode == kModeNf4T;   // converted tile MN-major
+  static constexpr int kRingBytes = kNf4 ? kNf4Bytes : kI8Bytes;
   static constexpr int kSub = kFused ? 2 : 1;                  // N = 256 MMAs per k step
   static constexpr int kTileTokens = kSub * kPairN;            // tokens per pair tile
   static constexpr int kStages = kFused ? 4 : 6;
   static constexpr int kStageBytes = (1 + kSub) * kOpBytes;
   static constexpr int kI8Offset = kStages * kStageBytes;
-  static constexpr int kTiles = kI8Offset + (kFused ? kI8Stages * kI8Bytes : 0);
+  static constexpr int kTiles = kI8Offset + (kFused ? kI8Stages * kRingBytes : 0);
   static constexpr int kAccBufs = kFused ? 1 : 2;
   static constexpr int kSmemBytes = 1024 /*align slack*/ + kTiles + static_cast<int>(sizeof(Barriers));
 };
-static_assert(BwdGeom<true>::kSmemBytes <= 232448 && BwdGeom<false>::kSmemBytes <= 232448 &&
-                  kFwdSmemBytes <= 232448,
+static_assert(BwdGeom<kModeI8>::kSmemBytes <= 232448 && BwdGeom<kModeMat>::kSmemBytes <= 232448 &&
+                  BwdGeom<kModeNf4>::kSmemBytes <= 232448 && kFwdSmemBytes <= 232448,
               "shared memory per CTA");
-static_assert(BwdGeom<true>::kStages <= kMaxStages && BwdGeom<false>::kStages <= kMaxStages, "barrier arrays");
+static_assert(BwdGeom<kModeI8>::kStages <= kMaxStages && BwdGeom<kModeMat>::kStages <= kMaxStages, "barrier arrays");
 
 __device__ __forceinline__ uint32_t f2i_rn(uint32_t fbits) {
   return static_cast<uint32_t>(__float2int_rn(__uint_as_float(fbits)));
@@ -663,25 +678,50 @@ template <typename OutT>
 __device__ __forceinline__ void bwd_store16(const BwdEpiArgs& e, int64_t kk, int m_base, const uint32_t (&x)[16]) {
   OutT* out = static_cast<OutT*>(e.grad_A);
   const OutT* add = static_cast<const OutT*>(e.addend);
+  const float bv = e.bias != nullptr ? load_any(e.bias, e.bias_dt, kk) : 0.f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int64_t mm = m_base + j;
     if (mm < e.M) {
       float v = __uint_as_float(x[j]);
       if (add != nullptr) v = __fadd_rn(v, to_float(add[mm * e.K + kk]));
+      if (e.bias != nullptr) v = __fadd_rn(v, bv);
       out[mm * e.K + kk] = from_float<OutT>(v);
     }
   }
 }
 
-// kFused: the A operand (Wdq^T) is rebuilt per stage from the int8 weight
-// tiles by the converter warps; otherwise it is loaded by TMA from the
-// materialized WdqT (K-major, like G16) and the converter, int8-producer and
-// relay warps stay idle.
-template <bool kFused>
+// 16 packed 4-bit codes (8 bytes, the even element of each pair in the high
+// nibble) -> lv[code] * am as one IEEE fp32 multiply each, rounded to the
+// 16-bit operand type; element 2i in the low half of word i.
+__device__ __forceinline__ void nf4x16_decode(uint2 v, float am, const float* lv, bool bf16, uint4& o0, uint4& o1) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = ((i < 4 ? v.x : v.y) >> (8 * (i & 3))) & 0xFFu;
+    const float e0 = __fmul_rn(lv[byte >> 4], am);
+    const float e1 = __fmul_rn(lv[byte & 15u], am);
+    if (bf16) {
+      const __nv_bfloat162 p = __floats2bfloat162_rn(e0, e1);
+      w[i] = *reinterpret_cast<const uint32_t*>(&p);
+    } else {
+      const __half2 p = __floats2half2_rn(e0, e1);
+      w[i] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+  }
+  o0 = make_uint4(w[0], w[1], w[2], w[3]);
+  o1 = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Fused modes: the A operand (the dequantized weight tile) is rebuilt per
+// stage from the int8 or 4-bit weight tiles by the converter warps;
+// kModeMat: it is loaded by TMA from the materialized WdqT (K-major, like
+// G16) and the converter, weight-producer and relay warps stay idle.
+template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     bwd_gemm_kernel(const __grid_constant__ BwdGemmArgs g, const BwdEpiArgs e, int num_k, int num_m, int group) {
-  using Geo = BwdGeom<kFused>;
+  using Geo = BwdGeom<kMode>;
+  constexpr bool kFused = Geo::kFused;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Barriers* bars = reinterpret_cast<Barriers*>(smem + Geo::kTiles);
@@ -695,6 +735,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
   const int NB = (e.N + kBK - 1) / kBK;   // reduction blocks over n
 
   if (threadIdx.x == 0) init_barriers(bars, kBwdEpiWarps);
+  if (Geo::kNf4 && threadIdx.x < 16) bars->lv[threadIdx.x] = e.lv[threadIdx.x];
   if (warp == kWarpMMA) {
     tmem_alloc_pair(&bars->tmem_base, 512);
     tmem_relinquish_pair();
@@ -740,20 +781,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
           mbar_wait_teardown(&bars->full[j % Geo::kStages], (j / Geo::kStages) & 1, e.st);
     }
   } else if (warp == kWarpI8Producer) {
-    // ---- int8 weight tiles CB[n:+64][k:+128], this CTA's own ring
+    // ---- weight tiles, this CTA's own ring: int8 CB[n:+64][k:+128]; 4-bit,
+    // input gradient: packed[n:+64][k:+128] (64 bytes a row); 4-bit, forward:
+    // packed[n:+128][k:+64] (32 bytes a row)
+    // (x = the byte column, y = the row of the weight)
+    auto ring_xy = [&](int tk, int b, int& x, int& y) {
+      const int r_cta = tk * kPairM + static_cast<int>(rank) * kCtaRows;
+      if (kMode == kModeNf4) {
+        x = b * (kBK / 2);
+        y = r_cta;
+      } else {
+        x = Geo::kNf4 ? r_cta / 2 : r_cta;
+        y = b * kBK;
+      }
+    };
     if (kFused && lane == 0) {
       int it = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl) {
         int tm, tk;
         tile_coords(t, num_m, num_k, group, tm, tk);
-        const int k_cta = tk * kPairM + static_cast<int>(rank) * kCtaRows;
         for (int b = 0; b < NB; ++b, ++it) {
           const int j = it % kI8Stages;
           const uint32_t ph = (it / kI8Stages) & 1;
           if (!mbar_wait(&bars->i8_empty[j], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->i8_full[j], kI8Bytes);
-          tma_load_2d(i8_ring + j * kI8Bytes, &g.tmW, k_cta, b * kBK, &bars->i8_full[j]);
+          mbar_arrive_expect_tx(&bars->i8_full[j], Geo::kRingBytes);
+          int x, y;
+          ring_xy(tk, b, x, y);
+          tma_load_2d(i8_ring + j * Geo::kRingBytes, &g.tmW, x, y, &bars->i8_full[j]);
           // the copy above waits on DRAM for about a microsecond; a tile a few
           // stages ahead is pulled into L2 now, so its own copy finds it there
           int bp = b + kI8PrefetchAhead, tp = t;
@@ -764,7 +819,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
           if (tp < num_tiles) {
             int tmp, tkp;
             tile_coords(tp, num_m, num_k, group, tmp, tkp);
-            tma_prefetch_l2_2d(&g.tmW, tkp * kPairM + static_cast<int>(rank) * kCtaRows, bp * kBK);
+            ring_xy(tkp, bp, x, y);
+            tma_prefetch_l2_2d(&g.tmW, x, y);
           }
         }
       }
@@ -773,9 +829,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpMMA) {
     if (rank == 0 && lane == 0) {
-      // A, fused: MN-major, 128B swizzle; MN atoms (64 k) 1024 B apart, K atoms
-      // (8 n) 2048 B apart.  Materialized: K-major like B.
-      const uint32_t idesc = make_idesc_f16(kPairM, kPairN, kFused, false);
+      // A, int8 and 4-bit input gradient: MN-major, 128B swizzle; MN atoms
+      // (64 k) 1024 B apart, K atoms (8 n) 2048 B apart.  Materialized and
+      // 4-bit forward: K-major like B.  ab_fmt: bf16 operands.
+      const uint32_t idesc = make_idesc_f16(kPairM, kPairN, Geo::kAmn, false) | e.ab_fmt;
       int it = 0, tl = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl, ++tl) {
@@ -799,8 +856,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
           const uint32_t a_base = smem_u32(smem + s * Geo::kStageBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = kFused ? make_sdesc(a_base + k * 4096, 1024, 2048, kSwizzle128B)
-                                       : make_sdesc(a_base + k * 32, 16, 1024, kSwizzle128B);
+            const uint64_t ad = Geo::kAmn ? make_sdesc(a_base + k * 4096, 1024, 2048, kSwizzle128B)
+                                          : make_sdesc(a_base + k * 32, 16, 1024, kSwizzle128B);
 #pragma unroll
             for (int u = 0; u < Geo::kSub; ++u) {   // token sub-tile u -> accumulator columns [256 u, 256 u + 256)
               const uint64_t bd = make_sdesc(a_base + (1 + u) * kOpBytes + k * 32, 16, 1024, kSwizzle128B);
@@ -821,7 +878,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       relay_loop(bars, cid, ncl, num_tiles, NB, warp == kWarpRelayLast ? 3 : 1 + (warp - kWarpRelay0), Geo::kStages,
                  abort_flag, e.st);
   } else if (warp < kBwdWarpEpi0) {
-    if constexpr (kFused) {
+    if constexpr (kMode == kModeI8) {
       // ---- converters: CB int8 [64 n][128 k] (128B-swizzled rows) -> Wdq^T
       // fp16, MN-major 128B-swizzled.  All eight warps work on every stage: a
       // thread takes the 16-byte chunk q of rows nl0 and nl0 + 32 (16 k x 1 n
@@ -889,6 +946,104 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
             mbar_arrive(&bars->i8_empty[j8]);
             // the even CTA's MMA thread reads this CTA's tiles: local arrive there,
             // a relay (cluster-scope release) from the odd CTA
+            mbar_arrive(rank == 0 ? &bars->ready[s] : &bars->cvt_done[s]);
+          }
+        }
+      }
+    } else if constexpr (Geo::kNf4) {
+      // ---- converters, 4-bit codes -> Wdq = lv[code] * absmax in the operand
+      // type.  Every thread takes two (row, 16-code segment) items of each
+      // weight tile.  Input gradient: tile [64 n][128 k] -> Wdq^T MN-major,
+      // rows nl0 and nl0 + 32, segment q, the thread layout of the int8
+      // converters (same output positions).  Forward: tile [128 n][64 k] ->
+      // Wdq K-major (8-row atoms of 128-byte rows, 16-byte chunks swizzled by
+      // the row), rows rr0 and rr0 + 64, segment sg; a quarter warp reads 64
+      // consecutive bytes and writes 8 distinct bank groups.  The absmax
+      // values of a stage are loaded one stage ahead.
+      const int gt = threadIdx.x - kWarpCvt0 * 32;   // 0..255
+      const bool bf16 = e.ab_fmt != 0u;
+      const float* lv = bars->lv;
+      int row[2], seg;
+      if (kMode == kModeNf4T) {
+        seg = (gt >> 3) & 7;
+        row[0] = (gt & 7) + 8 * (gt >> 6);
+        row[1] = row[0] + 32;
+      } else {
+        seg = gt & 3;
+        row[0] = gt >> 2;
+        row[1] = row[0] + 64;
+      }
+      constexpr int kRowBytes = kMode == kModeNf4T ? 64 : 32;
+      auto load_am = [&](int t, int b, float (&f)[2]) {
+        int tm, tk;
+        tile_coords(t, num_m, num_k, group, tm, tk);
+        const int r_cta = tk * kPairM + static_cast<int>(rank) * kCtaRows;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          int n, kb;
+          bool ok;
+          if (kMode == kModeNf4T) {   // weight row n = reduction index, block of this CTA's k
+            n = b * kBK + row[j];
+            kb = (r_cta >> 6) + (seg >> 2);
+            ok = n < e.N;
+          } else {                    // weight row n = output row, block b of the reduction
+            n = r_cta + row[j];
+            kb = b;
+            ok = n < e.K;
+          }
+          f[j] = ok && kb < e.nblk ? __ldg(e.absmax + static_cast<int64_t>(n) * e.nblk + kb) : 0.f;
+        }
+      };
+      float am_next[2] = {0.f, 0.f};
+      if (cid < num_tiles) load_am(cid, 0, am_next);
+      int it = 0;
+      bool go = true;
+      for (int t = cid; t < num_tiles && go; t += ncl) {
+        for (int b = 0; b < NB; ++b, ++it) {
+          const float am[2] = {am_next[0], am_next[1]};
+          if (b + 1 < NB) {
+            load_am(t, b + 1, am_next);
+          } else if (t + ncl < num_tiles) {
+            load_am(t + ncl, 0, am_next);
+          }
+          const int s = it % Geo::kStages;
+          const uint32_t ph = (it / Geo::kStages) & 1;
+          const int j8 = it % kI8Stages;
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(&bars->i8_full[j8], (it / kI8Stages) & 1, abort_flag, e.st, kWhereCvt))) {
+            go = false;
+            break;
+          }
+          const uint8_t* src = i8_ring + j8 * Geo::kRingBytes;
+          uint2 v[2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) v[j] = *reinterpret_cast<const uint2*>(src + row[j] * kRowBytes + seg * 8);
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereCvt))) {
+            go = false;
+            break;
+          }
+          uint8_t* sa = smem + s * Geo::kStageBytes;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            uint4 o0, o1;
+            nf4x16_decode(v[j], am[j], lv, bf16, o0, o1);
+            const int r = row[j] & 7;
+            int c0;
+            uint8_t* rowp;
+            if (kMode == kModeNf4T) {
+              rowp = sa + (row[j] >> 3) * 2048 + (seg >> 2) * 1024 + r * 128;
+              c0 = (seg & 3) * 2;
+            } else {
+              rowp = sa + (row[j] >> 3) * 1024 + r * 128;
+              c0 = seg * 2;
+            }
+            *reinterpret_cast<uint4*>(rowp + ((c0 ^ r) << 4)) = o0;
+            *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ r) << 4)) = o1;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars->i8_empty[j8]);
             mbar_arrive(rank == 0 ? &bars->ready[s] : &bars->cvt_done[s]);
           }
         }
@@ -1032,8 +1187,7 @@ __global__ void __launch_bounds__(256) unit_plan_kernel(const uint32_t* __restri
 
 int g_pairs_fwd[64] = {};   // resident pairs per device, per kernel
 int g_pairs_fwd_silu[64] = {};
-int g_pairs_bwd_fused[64] = {};
-int g_pairs_bwd_dq[64] = {};
+int g_pairs_bwd[4][64] = {};   // per BwdMode
 
 // Backward prepass of the materialized schedule: WdqT[k][n] =
 // fp16_rn(fp32(CB[n][k]) * (SCB[n] * fp32(1/127))) -- the page's per-call
@@ -1115,7 +1269,7 @@ bool set_smem_attr(const void* fn, int smem_bytes, bool& done) {
 
 }  // namespace
 
-bool g_attr_fwd = false, g_attr_fwd_silu = false, g_attr_bwd_fused = false, g_attr_bwd_dq = false;
+bool g_attr_fwd = false, g_attr_fwd_silu = false, g_attr_bwd[4] = {false, false, false, false};
 
 cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_bytes) {
   // the backward reports the schedule the workspace-sized default picks: fused
@@ -1130,11 +1284,11 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
     done = &g_attr_fwd;
     cache = g_pairs_fwd;
   } else if (kernel_id == K_BWD_GEMM) {
-    fn = reinterpret_cast<const void*>(bwd_gemm_kernel<true>);
+    fn = reinterpret_cast<const void*>(bwd_gemm_kernel<kModeI8>);
     nthreads = kBwdThreads;
-    smem = BwdGeom<true>::kSmemBytes;
-    done = &g_attr_bwd_fused;
-    cache = g_pairs_bwd_fused;
+    smem = BwdGeom<kModeI8>::kSmemBytes;
+    done = &g_attr_bwd[kModeI8];
+    cache = g_pairs_bwd[kModeI8];
   } else {
     return cudaErrorInvalidValue;
   }
@@ -1187,25 +1341,29 @@ cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStrea
   return e.act != nullptr ? launch_fwd_variant<true>(g, e, s, prof_id) : launch_fwd_variant<false>(g, e, s, prof_id);
 }
 
-template <bool kFused>
-cudaError_t launch_bwd_schedule(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaStream_t s) {
-  using Geo = BwdGeom<kFused>;
+template <int kMode>
+cudaError_t launch_bwd_schedule(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaStream_t s, int prof_id) {
+  using Geo = BwdGeom<kMode>;
   const int num_k = static_cast<int>(ceil_div(e.K, kPairM));
   const int num_m = static_cast<int>(ceil_div(e.M, Geo::kTileTokens));
   if (num_k == 0 || num_m == 0) return cudaSuccess;
-  const void* fn = reinterpret_cast<const void*>(bwd_gemm_kernel<kFused>);
-  if (!set_smem_attr(fn, Geo::kSmemBytes, kFused ? g_attr_bwd_fused : g_attr_bwd_dq)) return cudaGetLastError();
+  const void* fn = reinterpret_cast<const void*>(bwd_gemm_kernel<kMode>);
+  if (!set_smem_attr(fn, Geo::kSmemBytes, g_attr_bwd[kMode])) return cudaGetLastError();
   const int tiles = num_k * num_m;
-  const int clusters =
-      std::min(tiles, resident_pairs(fn, kBwdThreads, Geo::kSmemBytes, kFused ? g_pairs_bwd_fused : g_pairs_bwd_dq));
+  const int clusters = std::min(tiles, resident_pairs(fn, kBwdThreads, Geo::kSmemBytes, g_pairs_bwd[kMode]));
   const int group = std::min(num_m, 8);
-  ProfScope ps(K_BWD_GEMM, s);
-  bwd_gemm_kernel<kFused><<<2 * clusters, kBwdThreads, Geo::kSmemBytes, s>>>(g, e, num_k, num_m, group);
+  ProfScope ps(prof_id, s);
+  bwd_gemm_kernel<kMode><<<2 * clusters, kBwdThreads, Geo::kSmemBytes, s>>>(g, e, num_k, num_m, group);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool fused, cudaStream_t s) {
-  return fused ? launch_bwd_schedule<true>(g, e, s) : launch_bwd_schedule<false>(g, e, s);
+  return fused ? launch_bwd_schedule<kModeI8>(g, e, s, K_BWD_GEMM) : launch_bwd_schedule<kModeMat>(g, e, s, K_BWD_GEMM);
+}
+
+cudaError_t launch_nf4_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool input_grad, cudaStream_t s) {
+  return input_grad ? launch_bwd_schedule<kModeNf4T>(g, e, s, K_NF4_GEMM_BWD)
+                    : launch_bwd_schedule<kModeNf4>(g, e, s, K_NF4_GEMM_FWD);
 }
 
 cudaError_t launch_dequant_weight(const int8_t* CB, const float* SCB, int64_t N, int64_t k_pad, __half* WdqT,

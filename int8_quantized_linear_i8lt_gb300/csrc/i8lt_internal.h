@@ -129,18 +129,42 @@ struct BwdGemmArgs {
   CUtensorMap tmG;    // G16 fp16 [M, N_pad], box 64 x 128, 128B swizzle
 };
 
+// D[r, m] = sum_c W(r, c) X[m, c], stored at out[m * K + r]: r < K output
+// rows (the input features k of the int8 and 4-bit input gradients, the
+// output features n of the 4-bit forward), c < N the reduction, m < M tokens.
 struct BwdEpiArgs {
   int M, N, K;
-  const float* SCB;
-  const void* addend;
-  void* grad_A;
+  const float* SCB;      // int8: per weight row n, the absmax scale
+  const void* addend;    // [M, K] in dt, or NULL
+  void* grad_A;          // [M, K] in dt
   int dt;
   DevStatus* st;
+  const void* bias;      // [K] in bias_dt, or NULL
+  int bias_dt;
+  uint32_t ab_fmt;       // instruction-descriptor bits of the operand type (0: fp16)
+  const float* absmax;   // 4-bit: [weight rows, nblk] per-64-element scales
+  int nblk;
+  float lv[16];          // 4-bit: the code levels
 };
 
 // fused: the dequantized weight is rebuilt in shared memory from CB (tmW);
 // otherwise it is read from WdqT (tmWT), written by launch_dequant_weight.
 cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool fused, cudaStream_t s);
+
+// 4-bit NormalFloat matmuls with the weight decoded per stage in shared memory
+// (tmW: the packed codes [rows, row_bytes] uint8, no swizzle; box 64 x 64 for
+// the input gradient, 32 x 128 for the forward; tmG: the 16-bit activations
+// or output gradient, box 64 x 128, 128B swizzle).
+cudaError_t launch_nf4_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool input_grad, cudaStream_t s);
+
+// The 16 NF4 levels (ascending fp32), computed once on the host.
+void nf4_levels(float out[16]);
+// W [N, K] (dtype wt) -> packed [N, row_bytes] codes and absmax [N, ceil(K / 64)].
+cudaError_t launch_nf4_quantize(const void* W, int wt, int64_t N, int64_t K, int64_t row_bytes, uint8_t* packed,
+                                float* absmax, cudaStream_t s);
+// packed + absmax -> out [N, K] (dtype dt): lv[code] * absmax, rounded once.
+cudaError_t launch_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, int64_t K,
+                                  int64_t row_bytes, void* out, int dt, cudaStream_t s);
 
 // Backward prepass of the materialized schedule: WdqT[k, n] =
 // fp16_rn(fp32(CB[n, k]) * (SCB[n] * fp32(1/127))) for k < k_pad, n < N, and
@@ -155,7 +179,7 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
 enum KernelId {
   K_QUANTIZE_WEIGHT = 0, K_COLMAX, K_OUTLIER_INDEX, K_ROW_QUANTIZE, K_SUBB, K_FWD_GEMM, K_GRADOUT_PREPASS,
   K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_WIDEN_CODES, K_DEQUANT_WEIGHT, K_COL_QUANTIZE,
-  K_WGRAD_GEMM, K_UNIT_PLAN, K_COUNT
+  K_WGRAD_GEMM, K_UNIT_PLAN, K_NF4_QUANTIZE, K_NF4_DEQUANTIZE, K_NF4_GEMM_FWD, K_NF4_GEMM_BWD, K_COUNT
 };
 
 // Box sizes of the tensor maps (each CTA of a pair stages 128 rows of each

@@ -1,0 +1,206 @@
+// 4-bit NormalFloat (NF4) weight storage for the weight-only matmuls of
+// QLoRA fine-tuning ("Support QLoRA 4-bit finetuning with bitsandbytes",
+// lit-gpt PR #275: the bnb.nf4 quantize option; frozen 4-bit base weights,
+// bf16 compute).  The page names the format without defining it; this file
+// follows the published construction of QLoRA's 4-bit NormalFloat:
+//   levels: 7 negated and 8 positive standard-normal quantiles of evenly
+//           spaced probabilities between 1/2 and delta = ((1 - 1/30) +
+//           (1 - 1/32)) / 2, plus 0, divided by the largest (so -1 .. 1);
+//   blocks: 64 consecutive elements of a weight row share one fp32 absmax;
+//   code:   the nearest level to x / absmax, decided in fp32 against the
+//           midpoints of adjacent levels (strictly greater: the upper level);
+//   packing: two codes per byte, the even element in the high nibble, rows
+//           padded to a multiple of 64 elements with the zero level.
+// The matmuls that decode these codes inside the tensor-core pipeline are in
+// i8lt_gemm.cu (kModeNf4, kModeNf4T).
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "i8lt_internal.h"
+
+namespace i8lt {
+
+namespace {
+
+double normal_cdf(double x) { return 0.5 * std::erfc(-x / std::sqrt(2.0)); }
+
+// Standard-normal quantile: bisection on the CDF down to adjacent doubles.
+double normal_quantile(double p) {
+  double lo = -10.0, hi = 10.0;
+  for (int i = 0; i < 200; ++i) {
+    const double mid = 0.5 * (lo + hi);
+    if (mid == lo || mid == hi) break;
+    if (normal_cdf(mid) < p) {
+      lo = mid;
+    } else {
+      hi = mid;
+    }
+  }
+  return 0.5 * (lo + hi);
+}
+
+struct Nf4Tables {
+  float lv[16];
+  float mid[15];
+};
+
+const Nf4Tables& tables() {
+  static Nf4Tables t;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const double delta = ((1.0 - 1.0 / 30.0) + (1.0 - 1.0 / 32.0)) / 2.0;
+    const double step_neg = (0.5 - delta) / 7.0, step_pos = (0.5 - delta) / 8.0;
+    double v[16];
+    int n = 0;
+    for (int i = 0; i < 7; ++i) v[n++] = -normal_quantile(static_cast<double>(i) * step_neg + delta);
+    v[n++] = 0.0;
+    for (int i = 0; i < 8; ++i) v[n++] = normal_quantile(static_cast<double>(i) * step_pos + delta);
+    std::sort(v, v + 16);
+    for (int i = 0; i < 16; ++i) t.lv[i] = static_cast<float>(v[i] / v[15]);
+    for (int i = 0; i < 15; ++i)
+      t.mid[i] = static_cast<float>((static_cast<double>(t.lv[i]) + static_cast<double>(t.lv[i + 1])) / 2.0);
+  });
+  return t;
+}
+
+template <typename T>
+__device__ __forceinline__ float load_w(const T* p, int64_t i) {
+  return to_float(p[i]);
+}
+
+// One thread per 8 consecutive elements of a row (one 32-bit word of packed
+// codes); the 8 threads of a 64-element block reduce its absmax with three
+// shuffles.  Every thread of a block runs every iteration (the shuffles take
+// the whole warp).
+template <typename T>
+__global__ void __launch_bounds__(256) nf4_quantize_kernel(const T* __restrict__ W, int64_t N, int64_t K,
+                                                           int64_t row_bytes, int nblk, Nf4Tables c,
+                                                           uint8_t* __restrict__ packed,
+                                                           float* __restrict__ absmax) {
+  const int64_t gpr = row_bytes / 4;   // groups of 8 per row (a multiple of 8)
+  const int64_t total = N * gpr;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x; base < total; base += stride) {
+    const int64_t g = base + threadIdx.x;
+    const bool act = g < total;
+    const int64_t n = act ? g / gpr : 0;
+    const int64_t kg = act ? g - n * gpr : 0;
+    const int64_t k0 = kg * 8;
+    float x[8];
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[i] = (act && k0 + i < K) ? load_w(W, n * K + k0 + i) : 0.f;
+      am = fmaxf(am, fabsf(x[i]));
+    }
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+    if (!act) continue;
+    if ((kg & 7) == 0) absmax[n * nblk + (kg >> 3)] = am;
+    uint32_t word = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t code = 7u;   // the zero level: padding and all-zero blocks
+      if (k0 + i < K && am > 0.f) {
+        const float xn = __fdiv_rn(x[i], am);
+        code = 0u;
+#pragma unroll
+        for (int j = 0; j < 15; ++j) code += xn > c.mid[j] ? 1u : 0u;
+      }
+      // byte i / 2 holds elements (2j, 2j + 1) as (high, low) nibbles
+      word |= code << (8 * (i >> 1) + ((i & 1) ? 0 : 4));
+    }
+    *reinterpret_cast<uint32_t*>(packed + n * row_bytes + kg * 4) = word;
+  }
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(256) nf4_dequantize_kernel(const uint8_t* __restrict__ packed,
+                                                             const float* __restrict__ absmax, int64_t N, int64_t K,
+                                                             int64_t row_bytes, int nblk, Nf4Tables c,
+                                                             OutT* __restrict__ out) {
+  const int64_t gpr = row_bytes / 4;
+  const int64_t total = N * gpr;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total; g += stride) {
+    const int64_t n = g / gpr;
+    const int64_t kg = g - n * gpr;
+    const int64_t k0 = kg * 8;
+    if (k0 >= K) continue;
+    const uint32_t word = *reinterpret_cast<const uint32_t*>(packed + n * row_bytes + kg * 4);
+    const float am = absmax[n * nblk + (kg >> 3)];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (k0 + i < K) {
+        const uint32_t code = (word >> (8 * (i >> 1) + ((i & 1) ? 0 : 4))) & 15u;
+        out[n * K + k0 + i] = from_float<OutT>(__fmul_rn(c.lv[code], am));
+      }
+    }
+  }
+}
+
+int grid_for(int64_t threads) {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(threads, 256), static_cast<int64_t>(sms) * 8)));
+}
+
+}  // namespace
+
+void nf4_levels(float out[16]) {
+  const Nf4Tables& t = tables();
+  for (int i = 0; i < 16; ++i) out[i] = t.lv[i];
+}
+
+cudaError_t launch_nf4_quantize(const void* W, int wt, int64_t N, int64_t K, int64_t row_bytes, uint8_t* packed,
+                                float* absmax, cudaStream_t s) {
+  if (N == 0 || K == 0) return cudaSuccess;
+  const int nblk = static_cast<int>(ceil_div(K, 64));
+  const int blocks = grid_for(N * (row_bytes / 4));
+  const Nf4Tables& c = tables();
+  ProfScope ps(K_NF4_QUANTIZE, s);
+  switch (wt) {
+    case DT_F16:
+      nf4_quantize_kernel<__half><<<blocks, 256, 0, s>>>(static_cast<const __half*>(W), N, K, row_bytes, nblk, c,
+                                                         packed, absmax);
+      break;
+    case DT_BF16:
+      nf4_quantize_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), N, K,
+                                                                row_bytes, nblk, c, packed, absmax);
+      break;
+    default:
+      nf4_quantize_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(W), N, K, row_bytes, nblk, c,
+                                                        packed, absmax);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, int64_t K,
+                                  int64_t row_bytes, void* out, int dt, cudaStream_t s) {
+  if (N == 0 || K == 0) return cudaSuccess;
+  const int nblk = static_cast<int>(ceil_div(K, 64));
+  const int blocks = grid_for(N * (row_bytes / 4));
+  const Nf4Tables& c = tables();
+  ProfScope ps(K_NF4_DEQUANTIZE, s);
+  switch (dt) {
+    case DT_F16:
+      nf4_dequantize_kernel<__half><<<blocks, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c,
+                                                           static_cast<__half*>(out));
+      break;
+    case DT_BF16:
+      nf4_dequantize_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c,
+                                                                  static_cast<__nv_bfloat16*>(out));
+      break;
+    default:
+      nf4_dequantize_kernel<float><<<blocks, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c,
+                                                          static_cast<float*>(out));
+      break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace i8lt

@@ -403,3 +403,98 @@ class Int8MLPFunction(torch.autograd.Function):
         gx, gb1 = backward_input(gh, CB1, SCB1, ctx.K, addend=G if ctx.residual else None,
                                  bias_dtype=ctx.b1_dtype if ctx.needs_input_grad[3] else None)
         return gx.reshape(ctx.shape), None, None, gb1, None, None, gb2, None, None, None
+
+
+# ---------------------------------------------------------------------------
+# 4-bit NormalFloat weight-only layer (QLoRA fine-tuning: frozen 4-bit base
+# weights, 16-bit compute; see i8lt_nf4_forward in include/i8lt.h)
+# ---------------------------------------------------------------------------
+
+def nf4_levels() -> list[float]:
+    st, lv = _lib.i8lt_nf4_levels()
+    _check(st, "i8lt_nf4_levels")
+    return lv
+
+
+def nf4_quantize(W: torch.Tensor):
+    """W [N, K] (f16 / bf16 / f32, CUDA) -> (packed uint8 [N, row_bytes],
+    absmax fp32 [N, ceil(K / 64)])."""
+    _require_cuda(W)
+    W = W.contiguous()
+    N, K = W.shape
+    packed = torch.empty(N, _lib.i8lt_nf4_row_bytes(K), dtype=torch.uint8, device=W.device)
+    absmax = torch.empty(N, _lib.i8lt_nf4_blocks(K), dtype=torch.float32, device=W.device)
+    _check(_lib.i8lt_nf4_quantize(W.data_ptr(), _code(W.dtype), N, K, packed.data_ptr(), absmax.data_ptr(),
+                                  _stream(W)), "i8lt_nf4_quantize")
+    return packed, absmax
+
+
+def nf4_dequantize(packed: torch.Tensor, absmax: torch.Tensor, K: int, dtype: torch.dtype) -> torch.Tensor:
+    """The dequantized weight [N, K] in ``dtype``."""
+    _require_cuda(packed, absmax)
+    N = packed.shape[0]
+    out = torch.empty(N, K, dtype=dtype, device=packed.device)
+    _check(_lib.i8lt_nf4_dequantize(packed.data_ptr(), absmax.data_ptr(), N, K, out.data_ptr(), _code(dtype),
+                                    _stream(packed)), "i8lt_nf4_dequantize")
+    return out
+
+
+def _nf4_ws(device, ws):
+    if ws is None:
+        ws = torch.empty(_lib.i8lt_nf4_workspace_size(), dtype=torch.uint8, device=device)
+    return ws
+
+
+def nf4_forward(A: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: int,
+                bias: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                ws: torch.Tensor | None = None) -> torch.Tensor:
+    """out [M, N] = A [M, K] @ Wdq^T (+ bias) in A's dtype (f16 or bf16)."""
+    _require_cuda(A, packed, absmax, bias)
+    A = A.contiguous()
+    M = A.shape[0]
+    N = packed.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=A.dtype, device=A.device)
+    ws = _nf4_ws(A.device, ws)
+    _check(_lib.i8lt_nf4_forward(A.data_ptr(), _code(A.dtype), M, K, packed.data_ptr(), absmax.data_ptr(), N,
+                                 _ptr(bias), _code(bias.dtype) if bias is not None else 0, out.data_ptr(),
+                                 ws.data_ptr(), ws.numel(), _stream(A)), "i8lt_nf4_forward")
+    return out
+
+
+def nf4_backward_input(G: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: int,
+                       out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """grad_A [M, K] = G [M, N] @ Wdq in G's dtype (f16 or bf16)."""
+    _require_cuda(G, packed, absmax)
+    G = G.contiguous()
+    M, N = G.shape
+    if out is None:
+        out = torch.empty(M, K, dtype=G.dtype, device=G.device)
+    ws = _nf4_ws(G.device, ws)
+    _check(_lib.i8lt_nf4_backward_input(G.data_ptr(), _code(G.dtype), M, N, packed.data_ptr(), absmax.data_ptr(),
+                                        K, out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(G)),
+           "i8lt_nf4_backward_input")
+    return out
+
+
+class NF4LinearFunction(torch.autograd.Function):
+    """y = x @ Wdq^T + bias with the frozen 4-bit weight decoded inside the
+    matmuls; gradients to x and to the bias (summed over the tokens)."""
+
+    @staticmethod
+    def forward(ctx, x, packed, absmax, K, bias):
+        shape = x.shape
+        x2 = x.reshape(-1, K)
+        y = nf4_forward(x2, packed, absmax, K, bias)
+        ctx.save_for_backward(packed, absmax)
+        ctx.K, ctx.shape, ctx.has_bias = K, shape, bias is not None
+        ctx.bias_dtype = bias.dtype if bias is not None else None
+        return y.reshape(*shape[:-1], packed.shape[0])
+
+    @staticmethod
+    def backward(ctx, gy):
+        packed, absmax = ctx.saved_tensors
+        g2 = gy.reshape(-1, packed.shape[0])
+        gx = nf4_backward_input(g2, packed, absmax, ctx.K).reshape(ctx.shape) if ctx.needs_input_grad[0] else None
+        gb = g2.float().sum(0).to(ctx.bias_dtype) if ctx.has_bias and ctx.needs_input_grad[4] else None
+        return gx, None, None, None, gb

@@ -94,3 +94,45 @@ class Int8MLP(torch.nn.Module):
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         return F.Int8MLPFunction.apply(x, self.fc1.CB, self.fc1.SCB, self.fc1.bias, self.fc2.CB, self.fc2.SCB,
                                        self.fc2.bias, self.fc1.threshold, self.residual, self.fc1.max_outliers)
+
+
+class LinearNF4(torch.nn.Module):
+    """Frozen 4-bit NormalFloat linear layer of QLoRA fine-tuning: the weight
+    is stored as packed 4-bit codes with one fp32 absmax per 64 elements of a
+    row and decoded to the 16-bit compute dtype (the input's: f16 or bf16)
+    inside the tensor-core matmuls of the forward and of the input gradient.
+    The weight takes no gradient; the bias does."""
+
+    def __init__(self, in_features: int, out_features: int, bias: bool = True, device=None,
+                 bias_dtype: torch.dtype = torch.bfloat16):
+        super().__init__()
+        from . import _lib
+        self.in_features = in_features
+        self.out_features = out_features
+        self.register_buffer("packed", torch.zeros(out_features, _lib.i8lt_nf4_row_bytes(in_features),
+                                                   dtype=torch.uint8, device=device))
+        self.register_buffer("absmax", torch.zeros(out_features, _lib.i8lt_nf4_blocks(in_features),
+                                                   dtype=torch.float32, device=device))
+        if bias:
+            self.bias = torch.nn.Parameter(torch.zeros(out_features, dtype=bias_dtype, device=device))
+        else:
+            self.register_parameter("bias", None)
+
+    @classmethod
+    def from_float(cls, weight: torch.Tensor, bias: torch.Tensor | None = None) -> "LinearNF4":
+        N, K = weight.shape
+        layer = cls(K, N, bias=bias is not None, device=weight.device,
+                    bias_dtype=bias.dtype if bias is not None else torch.bfloat16)
+        packed, absmax = F.nf4_quantize(weight)
+        layer.packed.copy_(packed)
+        layer.absmax.copy_(absmax)
+        if bias is not None:
+            with torch.no_grad():
+                layer.bias.copy_(bias)
+        return layer
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return F.NF4LinearFunction.apply(x, self.packed, self.absmax, self.in_features, self.bias)
+
+    def extra_repr(self) -> str:
+        return f"in_features={self.in_features}, out_features={self.out_features}, bias={self.bias is not None}"

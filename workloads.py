@@ -90,6 +90,21 @@ WORKLOADS = {
 ORDER = ("tiny_mlp", "linear_4096", "linear_bf16_4096x11008", "mlp_7b",
          "proj_8192x28672")
 
+# The 4-bit NormalFloat weight-only layer of QLoRA fine-tuning (frozen base
+# weights, bf16 compute): the Llama-2-7B MLP shapes the QLoRA runs use, with
+# the token count of the int8 7B MLP workload.
+NF4_WORKLOADS = {
+    "qlora_mlp_7b_nf4": Workload(
+        "qlora_mlp_7b_nf4",
+        "Llama-2-7B-style MLP layers with frozen NF4 weights: 4096->11008 and "
+        "11008->4096, bf16 activations of 8192 tokens N(0,1), weights "
+        "N(0,0.02) drawn in bf16, no bias; forward and input gradient of each "
+        "layer, each fed its own synthetic input",
+        (LayerSpec(8192, 4096, 11008, torch.bfloat16, 0.02, None),
+         LayerSpec(8192, 11008, 4096, torch.bfloat16, 0.02, None)),
+        w_dtype=torch.bfloat16),
+}
+
 
 def _gen(seed: int) -> torch.Generator:
     g = torch.Generator(device="cpu")
