@@ -105,7 +105,6 @@ struct __align__(8) Barriers {
   uint64_t teardown;            // even CTA: every MMA finished
   uint32_t tmem_base;
   int abort_flag;
-  float lv[16];                 // 4-bit schedules: the code levels, for the converters
 };
 
 // stage s of each CTA: [A operand 16 KB][B operand(s) 16 KB each] fp16,
@@ -691,22 +690,45 @@ __device__ __forceinline__ void bwd_store16(const BwdEpiArgs& e, int64_t kk, int
   }
 }
 
+// Two fp32 values times the splatted scale (one packed IEEE multiply, the
+// same rounding as two scalar ones), rounded to a 16-bit pair; e0 in the low
+// half.
+template <bool kBf16>
+__device__ __forceinline__ uint32_t mul2_to_16(float e0, float e1, uint64_t am2) {
+  uint32_t out;
+  if (kBf16) {
+    asm("{\n .reg .b64 x, p;\n .reg .b32 lo, hi;\n mov.b64 x, {%1, %2};\n mul.rn.f32x2 p, x, %3;\n"
+        " mov.b64 {lo, hi}, p;\n cvt.rn.bf16x2.f32 %0, hi, lo;\n}"
+        : "=r"(out)
+        : "f"(e0), "f"(e1), "l"(am2));
+  } else {
+    asm("{\n .reg .b64 x, p;\n .reg .b32 lo, hi;\n mov.b64 x, {%1, %2};\n mul.rn.f32x2 p, x, %3;\n"
+        " mov.b64 {lo, hi}, p;\n cvt.rn.f16x2.f32 %0, hi, lo;\n}"
+        : "=r"(out)
+        : "f"(e0), "f"(e1), "l"(am2));
+  }
+  return out;
+}
+
 // 16 packed 4-bit codes (8 bytes, the even element of each pair in the high
-// nibble) -> lv[code] * am as one IEEE fp32 multiply each, rounded to the
-// 16-bit operand type; element 2i in the low half of word i.
-__device__ __forceinline__ void nf4x16_decode(uint2 v, float am, const float* lv, bool bf16, uint4& o0, uint4& o1) {
+// nibble) -> lv[code] * am rounded to the operand type; element 2i in the low
+// half of word i.  The level table sits in shared memory at a fixed address:
+// the byte offsets 4 * code are cut out of the packed bytes with two masks,
+// and each lookup is one byte extract and one shared load.
+template <bool kBf16>
+__device__ __forceinline__ void nf4x16_decode(uint2 v, uint64_t am2, const float* lv_s, uint4& o0, uint4& o1) {
   uint32_t w[8];
+  const char* base = reinterpret_cast<const char*>(lv_s);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t byte = ((i < 4 ? v.x : v.y) >> (8 * (i & 3))) & 0xFFu;
-    const float e0 = __fmul_rn(lv[byte >> 4], am);
-    const float e1 = __fmul_rn(lv[byte & 15u], am);
-    if (bf16) {
-      const __nv_bfloat162 p = __floats2bfloat162_rn(e0, e1);
-      w[i] = *reinterpret_cast<const uint32_t*>(&p);
-    } else {
-      const __half2 p = __floats2half2_rn(e0, e1);
-      w[i] = *reinterpret_cast<const uint32_t*>(&p);
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t x = h ? v.y : v.x;
+    const uint32_t hi4 = (x >> 2) & 0x3C3C3C3Cu;   // 4 * high nibble of each byte
+    const uint32_t lo4 = (x << 2) & 0x3C3C3C3Cu;   // 4 * low nibble of each byte
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float e0 = *reinterpret_cast<const float*>(base + __byte_perm(hi4, 0u, 0x4440u + i));
+      const float e1 = *reinterpret_cast<const float*>(base + __byte_perm(lo4, 0u, 0x4440u + i));
+      w[4 * h + i] = mul2_to_16<kBf16>(e0, e1, am2);
     }
   }
   o0 = make_uint4(w[0], w[1], w[2], w[3]);
@@ -735,7 +757,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
   const int NB = (e.N + kBK - 1) / kBK;   // reduction blocks over n
 
   if (threadIdx.x == 0) init_barriers(bars, kBwdEpiWarps);
-  if (Geo::kNf4 && threadIdx.x < 16) bars->lv[threadIdx.x] = e.lv[threadIdx.x];
+  __shared__ float lv_s[16];   // 4-bit modes: the code levels
+  if (Geo::kNf4 && threadIdx.x < 16) lv_s[threadIdx.x] = e.lv[threadIdx.x];
   if (warp == kWarpMMA) {
     tmem_alloc_pair(&bars->tmem_base, 512);
     tmem_relinquish_pair();
@@ -962,7 +985,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       // values of a stage are loaded one stage ahead.
       const int gt = threadIdx.x - kWarpCvt0 * 32;   // 0..255
       const bool bf16 = e.ab_fmt != 0u;
-      const float* lv = bars->lv;
       int row[2], seg;
       if (kMode == kModeNf4T) {
         seg = (gt >> 3) & 7;
@@ -974,10 +996,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
         row[1] = row[0] + 64;
       }
       constexpr int kRowBytes = kMode == kModeNf4T ? 64 : 32;
-      auto load_am = [&](int t, int b, float (&f)[2]) {
+      // first output row of this CTA in tile t
+      auto cta_row0 = [&](int t) {
         int tm, tk;
         tile_coords(t, num_m, num_k, group, tm, tk);
-        const int r_cta = tk * kPairM + static_cast<int>(rank) * kCtaRows;
+        return tk * kPairM + static_cast<int>(rank) * kCtaRows;
+      };
+      // the absmax values of stage b of a tile whose CTA rows start at r_cta
+      auto load_am = [&](int r_cta, int b, float (&f)[2]) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           int n, kb;
@@ -995,16 +1021,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
         }
       };
       float am_next[2] = {0.f, 0.f};
-      if (cid < num_tiles) load_am(cid, 0, am_next);
+      int r_next = cid < num_tiles ? cta_row0(cid) : 0;
+      if (cid < num_tiles) load_am(r_next, 0, am_next);
       int it = 0;
       bool go = true;
       for (int t = cid; t < num_tiles && go; t += ncl) {
+        const int r_cur = r_next;
+        if (t + ncl < num_tiles) r_next = cta_row0(t + ncl);
         for (int b = 0; b < NB; ++b, ++it) {
           const float am[2] = {am_next[0], am_next[1]};
           if (b + 1 < NB) {
-            load_am(t, b + 1, am_next);
+            load_am(r_cur, b + 1, am_next);
           } else if (t + ncl < num_tiles) {
-            load_am(t + ncl, 0, am_next);
+            load_am(r_next, 0, am_next);
           }
           const int s = it % Geo::kStages;
           const uint32_t ph = (it / Geo::kStages) & 1;
@@ -1026,7 +1055,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             uint4 o0, o1;
-            nf4x16_decode(v[j], am[j], lv, bf16, o0, o1);
+            const uint64_t am2 = f32x2_splat(am[j]);
+            if (bf16) {
+              nf4x16_decode<true>(v[j], am2, lv_s, o0, o1);
+            } else {
+              nf4x16_decode<false>(v[j], am2, lv_s, o0, o1);
+            }
             const int r = row[j] & 7;
             int c0;
             uint8_t* rowp;
