@@ -44,10 +44,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 MEASURED_TRAFFIC = {
     "workload": "proj_8192x28672",
     "sources": {"int8_quantized_linear_i8lt_gb300/csrc/i8lt_gemm.cu":
-                "20aed36b7d7ab7c333abb27369e33d866aa3a5c99af707860898743da3a4971e",
+                "cb7798b87d52dc8feaf480d004e18b4e2fc77b45edc20b8d72f05ea8d86e45e1",
                 "int8_quantized_linear_i8lt_gb300/csrc/i8lt_common.cuh":
-                "b70f7b0f5041f01a17044277ef37d0a6e9832bc3625911eb0ec366ce66074e04"},
-    "bytes_per_launch": {"fwd_gemm": 8.05e9, "bwd_gemm": 5.47e9},
+                "ea330a3319c81e6e3ec691a3ae0f938a9410fc9d74d3a5f1ec638eb4245a4274"},
+    "bytes_per_launch": {"fwd_gemm": 8.20e9, "bwd_gemm": 5.61e9},
 }
 
 
@@ -344,6 +344,8 @@ def run_ours(args):
     trainable = time_trainable(layers, stream, max(2, min(args.steps, 10)), device)
     # --- the same step with the other backward schedule (context, not the headline)
     alt = time_schedule(layers, stream, max(2, min(args.steps, 10)), device, not mat)
+    # --- the 4-bit NormalFloat weight-only layers (another workload: context, not the headline)
+    nf4 = time_nf4(stream, max(2, min(args.steps, 10)), device)
 
     clocks = clk.summary()
     line = {
@@ -363,6 +365,7 @@ def run_ours(args):
            if wl.kind == "mlp" and len(layers) == 2 else {}),
         "trainable_mode": trainable,
         ("bwd_fused" if mat else "bwd_materialized"): alt,
+        "nf4_weight_only": nf4,
         "gpu_launches": n_launches,
         "gemm_launch": {k: dict(zip(("status", "ctas", "threads", "smem"), _lib.i8lt_gemm_launch_info(k)))
                         for k in ("fwd_gemm", "bwd_gemm")},
@@ -389,12 +392,12 @@ def _layer_of(i, layers, materialized=False):
 
 
 def launches_per_layer(L, materialized=False) -> int:
-    """Our kernels per layer and step: colmax, outlier index, row quantize,
-    subB (outliers on), weight-code widening, forward GEMM; grad_output
-    prepass, grad_bias finalize, (weight dequantization when materialized,)
-    backward GEMM."""
+    """Our kernels per layer and step: colmax, outlier index (outliers on),
+    row quantize, subB (outliers on), weight-code widening, accumulation
+    plan, forward GEMM; grad_output prepass, grad_bias finalize, (weight
+    dequantization when materialized,) backward GEMM."""
     import math
-    fwd = 6 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 3
+    fwd = 7 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 4
     return fwd + (4 if materialized else 3)
 
 
@@ -447,6 +450,69 @@ def time_trainable(layers, stream, steps, device):
             "steps": steps, "wgrad_gemm_tflops": round(wg_tf, 1) if wg_tf else None,
             "wgrad_gemm_frac_tensor": round(wg_tf / peak_t, 4) if wg_tf else None,
             "col_quantize_ms_per_step": round(cq_ms / steps, 4), "quantize_weight_ms_per_step": round(qw_ms / steps, 4)}
+
+
+def time_nf4(stream, steps, device, warmup=3):
+    """The 4-bit NormalFloat weight-only layers (QLoRA fine-tuning: frozen
+    NF4 weights, bf16 compute) of the qlora_mlp_7b_nf4 workload: per layer
+    and step the forward and the input gradient, each a tensor-core matmul
+    that decodes the 4-bit weight tile by tile.  FLOPs counted: 4 M N K per
+    layer.  The weights are quantized once, outside the timed region (they
+    are frozen)."""
+    import int8_quantized_linear_i8lt_gb300 as I
+    from int8_quantized_linear_i8lt_gb300 import _lib
+    from int8_quantized_linear_i8lt_gb300.functional import DTYPE_CODE
+    wl = W.NF4_WORKLOADS["qlora_mlp_7b_nf4"]
+    sp = stream.cuda_stream
+    ws = torch.empty(_lib.i8lt_nf4_workspace_size(), dtype=torch.uint8, device=device)
+    lay = []
+    for li, spec in enumerate(wl.layers):
+        Wf, _, G = W.layer_tensors(wl, li, 4321, device)
+        A = W.layer_input(wl, li, 4321, device)
+        packed, absmax = I.nf4_quantize(Wf)
+        out = torch.empty(spec.M, spec.N, dtype=spec.dtype, device=device)
+        gA = torch.empty(spec.M, spec.K, dtype=spec.dtype, device=device)
+        lay.append((spec, A, G, packed, absmax, out, gA))
+        del Wf
+
+    def step():
+        for spec, A, G, packed, absmax, out, gA in lay:
+            dt = DTYPE_CODE[spec.dtype]
+            st = _lib.i8lt_nf4_forward(A.data_ptr(), dt, spec.M, spec.K, packed.data_ptr(), absmax.data_ptr(), spec.N,
+                                       None, 0, out.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+            assert st == 0, _lib.i8lt_status_string(st)
+            st = _lib.i8lt_nf4_backward_input(G.data_ptr(), dt, spec.M, spec.N, packed.data_ptr(), absmax.data_ptr(),
+                                              spec.K, gA.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+            assert st == 0, _lib.i8lt_status_string(st)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _lib.i8lt_profile_start(1 << 16)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    _, recs, n_launches = _lib.i8lt_profile_stop(1 << 16)
+    ms = reduce_max(ev0.elapsed_time(ev1), device)
+    flops = sum(4.0 * spec.M * spec.N * spec.K for spec, *_ in lay) * steps
+    half = flops / 2
+    peaks, src = load_peaks()
+    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    res = {"workload": wl.name, "layers": [[s.M, s.K, s.N, str(s.dtype).replace("torch.", "")] for s in wl.layers],
+           "value": round(reduce_sum(flops, device) / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+           "ms_per_step": round(ms / steps, 4), "steps": steps, "gpu_launches": n_launches}
+    for name in ("nf4_gemm_fwd", "nf4_gemm_bwd"):
+        k_ms = sum(t for n, t in recs if n == name)
+        if k_ms:
+            tf = half / (k_ms * 1e-3) / 1e12
+            res[name] = {"tflops": round(tf, 1), "frac_tensor": round(tf / peak_t, 4),
+                         "ms_per_launch": round(k_ms / (steps * len(lay)), 4)}
+    res["peak"] = peak_t
+    res["peak_source"] = f"{src} bf16 sustained"
+    return res
 
 
 def time_mlp_chain(wl, layers, stream, steps, device):
@@ -692,6 +758,18 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_nf4_only(args):
+    """The NF4 section of the bench line on its own (profiling runs of the
+    4-bit matmuls): W warm-up steps, then K timed steps."""
+    import int8_quantized_linear_i8lt_gb300 as I  # noqa: F401  (fails loudly without the library)
+    from int8_quantized_linear_i8lt_gb300 import _lib
+    _lib.load()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    res = time_nf4(torch.cuda.current_stream(device), args.steps, device, warmup=args.warmup)
+    print(json.dumps({"nf4_weight_only": res}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -704,10 +782,14 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--bwd-schedule", default="fused", choices=["fused", "materialized"],
                     help="backward schedule of the timed steps (the other one is timed beside it)")
+    ap.add_argument("--nf4-only", action="store_true",
+                    help="time only the NF4 weight-only layers (qlora_mlp_7b_nf4) and print their line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.nf4_only:
+        run_nf4_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
