@@ -8,12 +8,14 @@
 //   of the forward, and the "Mixed-precision decomposition matmul" review
 //   thread for the outlier part).  sm_103a has no int8 MMA (ptxas rejects
 //   tcgen05.mma .kind::i8 for this target), so the codes enter the fp16
-//   tensor cores as exact fp16 integers and accumulate in fp32 TMEM.  Every
-//   partial sum of at most 1024 products is an integer of magnitude
-//   <= 1024 * 127^2 < 2^24, hence exact in fp32; every 1024-deep chunk is
-//   drained from TMEM into an int32 running sum held in TMEM, so Cacc is exact
-//   for any K <= 133144.  The outlier sub-GEMM subA x subB^T runs as one more
-//   fp32 accumulation unit after the int8 chunks.
+//   tensor cores as exact fp16 integers and accumulate in fp32 TMEM, exact
+//   while every partial sum stays an integer below 2^24.  The reduction is cut
+//   into groups of 1024-deep chunks chosen per tile pair by the accumulation
+//   plan (launch_unit_plan: a Cauchy-Schwarz bound from the chunk sums of
+//   squared codes; one chunk, <= 1024 * 127^2 < 2^24, always qualifies); each
+//   group is drained from TMEM into an int32 running sum held in TMEM, so Cacc
+//   is exact for any K <= 133144.  The outlier sub-GEMM subA x subB^T runs as
+//   one more fp32 accumulation unit after the int8 groups.
 //
 // Backward (K6): grad_A[m,k] = sum_n fp16(G)[m,n] * Wdq[n,k],
 //   Wdq[n,k] = fp16_rn(fp32(CB[n,k]) * (SCB[n] * fp32(1/127))), rebuilt per
@@ -21,6 +23,8 @@
 //   review thread on ".mul(1/127.0)").  Computed transposed,
 //   D[k, m] = Wdq^T G16^T, so the converted operand is the A side, stored
 //   MN-major (k contiguous, as CB's rows are); B = G16 via TMA, K-major.
+//   The backward kernel also runs the 4-bit NormalFloat weight-only matmuls
+//   (forward and input gradient of a frozen NF4 layer, see BwdMode).
 //
 // Both kernels run on CTA pairs (a cluster of 2, tcgen05 cta_group::2): the
 // pair computes a 256 x 256 tile with M = 256 MMAs issued by the even CTA;
