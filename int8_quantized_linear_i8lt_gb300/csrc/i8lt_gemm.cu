@@ -1154,33 +1154,52 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
                                                           uint32_t* __restrict__ bsq) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * 8;
-  for (int64_t w = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); w < N * nchunks; w += nwarps) {
-    const int64_t n = w / nchunks;
-    const int c = static_cast<int>(w - n * nchunks);
-    const int64_t k0 = static_cast<int64_t>(c) * 1024;
-    int sq = 0;
+  const int64_t total = N * nchunks;
+  // two work items per iteration, all four 16-byte loads issued first (the
+  // bounds are uniform over the warp, so the shuffles below are safe)
+  for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); w0 < total; w0 += 2 * nwarps) {
+    uint4 v[2][2];
+    int64_t n[2], k[2][2];
+    int c[2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int64_t k = k0 + lane * 32 + j * 16;
-      if (k < k_pad) {   // k_pad is a multiple of 16
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(CB + n * k_pad + k));
-        sq = __dp4a(static_cast<int>(v.x), static_cast<int>(v.x), sq);
-        sq = __dp4a(static_cast<int>(v.y), static_cast<int>(v.y), sq);
-        sq = __dp4a(static_cast<int>(v.z), static_cast<int>(v.z), sq);
-        sq = __dp4a(static_cast<int>(v.w), static_cast<int>(v.w), sq);
-        uint4 o0, o1;
-        i8x4_to_h4(v.x, o0.x, o0.y);
-        i8x4_to_h4(v.y, o0.z, o0.w);
-        i8x4_to_h4(v.z, o1.x, o1.y);
-        i8x4_to_h4(v.w, o1.z, o1.w);
-        uint4* dst = reinterpret_cast<uint4*>(CBh + n * k_pad + k);
-        dst[0] = o0;
-        dst[1] = o1;
+    for (int i = 0; i < 2; ++i) {
+      const int64_t w = w0 + i * nwarps;
+      n[i] = w < total ? w / nchunks : 0;
+      c[i] = static_cast<int>(w - n[i] * nchunks);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        k[i][j] = static_cast<int64_t>(c[i]) * 1024 + lane * 32 + j * 16;
+        v[i][j] = (w < total && k[i][j] < k_pad)   // k_pad is a multiple of 16
+                      ? __ldg(reinterpret_cast<const uint4*>(CB + n[i] * k_pad + k[i][j]))
+                      : make_uint4(0u, 0u, 0u, 0u);
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if (lane == 0 && sq != 0) atomicMax(bsq + (n >> 8) * nchunks + c, static_cast<uint32_t>(sq));
+    for (int i = 0; i < 2; ++i) {
+      if (w0 + i * nwarps >= total) break;
+      int sq = 0;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (k[i][j] < k_pad) {
+          const uint4 x = v[i][j];
+          sq = __dp4a(static_cast<int>(x.x), static_cast<int>(x.x), sq);
+          sq = __dp4a(static_cast<int>(x.y), static_cast<int>(x.y), sq);
+          sq = __dp4a(static_cast<int>(x.z), static_cast<int>(x.z), sq);
+          sq = __dp4a(static_cast<int>(x.w), static_cast<int>(x.w), sq);
+          uint4 o0, o1;
+          i8x4_to_h4(x.x, o0.x, o0.y);
+          i8x4_to_h4(x.y, o0.z, o0.w);
+          i8x4_to_h4(x.z, o1.x, o1.y);
+          i8x4_to_h4(x.w, o1.z, o1.w);
+          uint4* dst = reinterpret_cast<uint4*>(CBh + n[i] * k_pad + k[i][j]);
+          dst[0] = o0;
+          dst[1] = o1;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      if (lane == 0 && sq != 0) atomicMax(bsq + (n[i] >> 8) * nchunks + c[i], static_cast<uint32_t>(sq));
+    }
   }
 }
 

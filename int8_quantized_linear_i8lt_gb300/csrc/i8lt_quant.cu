@@ -718,14 +718,11 @@ __global__ void __launch_bounds__(kBlock) row_quantize_bulk_kernel(
   }
 }
 
-template <typename T, typename OutT>
-cudaError_t launch_bulk(int prof_id, const T* A, int64_t M, int64_t K, int64_t K_pad, const uint32_t* mask,
-                        const int* idx, DevStatus* st, int64_t cap_pad, float* scale, OutT* codes, __half* sub,
-                        uint32_t* asq, cudaStream_t s) {
-  const int row_bytes = static_cast<int>(round_up(K * static_cast<int64_t>(sizeof(T)), 16));
+template <typename T, typename OutT, int kBlock>
+cudaError_t launch_bulk_block(int prof_id, const T* A, int64_t M, int64_t K, int64_t K_pad, const uint32_t* mask,
+                              const int* idx, DevStatus* st, int64_t cap_pad, float* scale, OutT* codes, __half* sub,
+                              uint32_t* asq, int row_bytes, int sms, cudaStream_t s) {
   const int smem = 2 * row_bytes;
-  // long rows: one block per SM holds both buffers, so it gets 1024 threads
-  constexpr int kBlock = 1024;
   static bool done = false;
   if (!done) {
     if (cudaFuncSetAttribute(row_quantize_bulk_kernel<T, OutT, kBlock>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -733,9 +730,7 @@ cudaError_t launch_bulk(int prof_id, const T* A, int64_t M, int64_t K, int64_t K
       return cudaGetLastError();
     done = true;
   }
-  int dev = 0, sms = 152, per_sm = 1;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int per_sm = 1;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_quantize_bulk_kernel<T, OutT, kBlock>, kBlock, smem) !=
           cudaSuccess ||
       per_sm < 1) {
@@ -744,9 +739,32 @@ cudaError_t launch_bulk(int prof_id, const T* A, int64_t M, int64_t K, int64_t K
   }
   const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(sms) * per_sm));
   ProfScope ps(prof_id, s);
-  row_quantize_bulk_kernel<T, OutT, kBlock><<<grid, kBlock, smem, s>>>(A, M, K, K_pad, mask, idx, st, cap_pad, scale, codes,
-                                                                 sub, asq, row_bytes);
+  row_quantize_bulk_kernel<T, OutT, kBlock><<<grid, kBlock, smem, s>>>(A, M, K, K_pad, mask, idx, st, cap_pad, scale,
+                                                                       codes, sub, asq, row_bytes);
   return cudaGetLastError();
+}
+
+// Rows are streamed through two shared-memory buffers per block; the rows in
+// flight per SM are the blocks that fit.  Short rows get small blocks (up to
+// 7 of 256 threads per SM for 16 KB rows), long rows one or two blocks of
+// 1024 threads.
+template <typename T, typename OutT>
+cudaError_t launch_bulk(int prof_id, const T* A, int64_t M, int64_t K, int64_t K_pad, const uint32_t* mask,
+                        const int* idx, DevStatus* st, int64_t cap_pad, float* scale, OutT* codes, __half* sub,
+                        uint32_t* asq, cudaStream_t s) {
+  const int row_bytes = static_cast<int>(round_up(K * static_cast<int64_t>(sizeof(T)), 16));
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int fit = std::max(1, (220 * 1024) / (2 * row_bytes));   // blocks per SM that shared memory allows
+  if (fit >= 6)
+    return launch_bulk_block<T, OutT, 256>(prof_id, A, M, K, K_pad, mask, idx, st, cap_pad, scale, codes, sub, asq,
+                                           row_bytes, sms, s);
+  if (fit >= 3)
+    return launch_bulk_block<T, OutT, 512>(prof_id, A, M, K, K_pad, mask, idx, st, cap_pad, scale, codes, sub, asq,
+                                           row_bytes, sms, s);
+  return launch_bulk_block<T, OutT, 1024>(prof_id, A, M, K, K_pad, mask, idx, st, cap_pad, scale, codes, sub, asq,
+                                          row_bytes, sms, s);
 }
 
 // Launch of the staged row quantization (K_pad <= kStagedMaxLd): one row per
