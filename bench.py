@@ -299,13 +299,19 @@ def run_ours(args):
     # --- per-kernel totals from the records (launch order repeats per step)
     per_step = len(recs) // args.steps
     kern = {}
+    per_layer = [{"fwd_ms": 0.0, "bwd_ms": 0.0, "fwd_gemm_ms": 0.0, "bwd_gemm_ms": 0.0} for _ in layers]
     for i, (name, ms) in enumerate(recs):
-        L = layers[_layer_of(i % per_step, layers, mat)]
+        li = _layer_of(i % per_step, layers, mat)
+        L = layers[li]
         d = kern.setdefault(name, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
         d["launches"] += 1
         d["ms"] += ms
         d["flops"] += kernel_flops(L, name)
         d["bytes"] += kernel_bytes(L, name)
+        side = "bwd" if name in ("gradout_prepass", "grad_bias_finalize", "dequant_weight", "bwd_gemm") else "fwd"
+        per_layer[li][side + "_ms"] += ms
+        if name in ("fwd_gemm", "bwd_gemm"):
+            per_layer[li][name + "_ms"] += ms
     total_k_ms = sum(d["ms"] for d in kern.values())
     dom = max(kern, key=lambda k: kern[k]["ms"])
     peaks, peak_src = load_peaks()
@@ -338,6 +344,21 @@ def run_ours(args):
             g = v["bytes"] / (v["ms"] * 1e-3) / 1e9
             e.update(gbs=round(g, 1), frac_hbm=round(g / peak_b, 4))
         kernels[k] = e
+    # --- per layer: forward (all its kernels) against the int8 peak, backward against the fp16 peak
+    int8_peak = measure_int8_peak(device)
+    layers_out = []
+    for L, pl in zip(layers, per_layer):
+        s_ = L.spec
+        w = 2.0 * s_.M * s_.N * s_.K * args.steps
+        f_t = w / (pl["fwd_ms"] * 1e-3) / 1e12
+        b_t = w / (pl["bwd_ms"] * 1e-3) / 1e12
+        entry = {"shape": [s_.M, s_.K, s_.N], "fwd_ms": round(pl["fwd_ms"] / args.steps, 4),
+                 "bwd_ms": round(pl["bwd_ms"] / args.steps, 4), "fwd_tops": round(f_t, 1),
+                 "bwd_tflops": round(b_t, 1), "fwd_bwd_tops": round(2 * w / ((pl["fwd_ms"] + pl["bwd_ms"]) * 1e-3) / 1e12, 1),
+                 "bwd_frac_fp16_peak": round(b_t / peak_t, 4)}
+        if int8_peak.get("tops"):
+            entry["fwd_frac_int8_peak"] = round(f_t / int8_peak["tops"], 4)
+        layers_out.append(entry)
     # --- end to end through host buffers (pinned), inputs and results copied each step
     e2e = run_e2e(layers, stream, max(2, min(args.steps, 10)), device)
     # --- the trainable-weight mode on the same layers (context, not the headline)
@@ -359,6 +380,8 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (126 MB); no flush", "parallelism": f"replicas x{ws}"},
         "roofline": roof,
         "kernels": kernels,
+        "per_layer": layers_out,
+        "int8_tensor_peak": int8_peak,
         "e2e": e2e,
         "bwd_schedule": args.bwd_schedule,
         **({"mlp_chain": time_mlp_chain(wl, layers, stream, max(2, min(args.steps, 10)), device)}
@@ -379,6 +402,32 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def measure_int8_peak(device, n=8192, iters=10):
+    """The int8 tensor-core rate of this GPU as the CUDA libraries reach it
+    (torch._int_mm, cuBLASLt int8 x int8 -> int32, n^3), for the forward's
+    fraction of the int8 peak.  sm_103a offers no int8 tcgen05 MMA, so this
+    is the legacy int8 tensor path; the library's forward runs the int8
+    codes on the fp16 tensor cores instead.  Context only, off the timed
+    region."""
+    try:
+        a = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=device)
+        b = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=device)
+        for _ in range(3):
+            torch._int_mm(a, b.t())
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            torch._int_mm(a, b.t())
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        return {"tops": round(2.0 * n ** 3 / (ms * 1e-3) / 1e12, 1), "how": f"torch._int_mm {n}^3, best path of "
+                "the installed cuBLASLt, mean of 10 after 3 warm-up"}
+    except Exception as exc:   # no int8 GEMM in this build of the libraries
+        return {"tops": None, "how": f"torch._int_mm unavailable: {type(exc).__name__}: {exc}"[:200]}
 
 
 def _layer_of(i, layers, materialized=False):
