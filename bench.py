@@ -365,6 +365,8 @@ def run_ours(args):
     trainable = time_trainable(layers, stream, max(2, min(args.steps, 10)), device)
     # --- the same step with the other backward schedule (context, not the headline)
     alt = time_schedule(layers, stream, max(2, min(args.steps, 10)), device, not mat)
+    # --- the step replayed from a CUDA graph (context, not the headline)
+    graph = time_graph(layers, max(3, min(args.steps, 20)), device)
     # --- the 4-bit NormalFloat weight-only layers (another workload: context, not the headline)
     nf4 = time_nf4(stream, max(2, min(args.steps, 10)), device)
 
@@ -388,6 +390,7 @@ def run_ours(args):
            if wl.kind == "mlp" and len(layers) == 2 else {}),
         "trainable_mode": trainable,
         ("bwd_fused" if mat else "bwd_materialized"): alt,
+        "cuda_graph": graph,
         "nf4_weight_only": nf4,
         "gpu_launches": n_launches,
         "gemm_launch": {k: dict(zip(("status", "ctas", "threads", "smem"), _lib.i8lt_gemm_launch_info(k)))
@@ -643,6 +646,39 @@ def time_schedule(layers, stream, steps, device, materialized):
     return {"value": round(ops / (ms * 1e-3) / 1e12, 2), "unit": "TOPS", "ms_per_step": round(ms / steps, 3),
             "steps": steps, "bwd_gemm_tflops": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 1) if bwd_ms else None,
             "dequant_weight_ms_per_step": round(dq_ms / steps, 4)}
+
+
+def time_graph(layers, steps, device):
+    """The same step captured once in a CUDA graph and replayed: every launch
+    of the library goes through the caller's stream, so a captured step
+    replays with no host work per kernel.  For the large workloads this
+    matches the eager step; for the tiny MLP it removes the launch latency."""
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        for L in layers:                      # warm-up outside the capture (attributes, caches)
+            _launch_layer(L, side.cuda_stream)
+    torch.cuda.current_stream(device).wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sp = torch.cuda.current_stream(device).cuda_stream
+        for L in layers:
+            _launch_layer(L, sp)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(ev0.elapsed_time(ev1), device)
+    ops = reduce_sum(sum(L.ops() for L in layers) * steps, device)
+    return {"value": round(ops / (ms * 1e-3) / 1e12, 4), "unit": "TOPS", "ms_per_step": round(ms / steps, 4),
+            "us_per_step": round(1e3 * ms / steps, 2), "steps": steps}
 
 
 def run_e2e(layers, stream, steps, device):

@@ -10,6 +10,8 @@
 #include <algorithm>
 #include <type_traits>
 
+#include <mutex>
+
 #include "i8lt_internal.h"
 
 namespace i8lt {
@@ -603,6 +605,32 @@ __device__ __forceinline__ void smem_load8_half(const T* p, __half (&h)[8]) {
     for (int j = 0; j < kVec; ++j) h[v * kVec + j] = to_half(x[j]);
   }
 }
+// Blocks per SM of a kernel at a given dynamic shared-memory size, cached
+// per (kernel, device, size) so that launches made while a stream is being
+// captured into a CUDA graph query nothing.
+int cached_blocks_per_sm(const void* fn, int threads, int smem) {
+  struct Entry {
+    const void* fn;
+    int dev, threads, smem, per_sm;
+  };
+  static Entry cache[64];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].fn == fn && cache[i].dev == dev && cache[i].threads == threads && cache[i].smem == smem)
+      return cache[i].per_sm;
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  if (used < 64) cache[used++] = Entry{fn, dev, threads, smem, per_sm};
+  return per_sm;
+}
+
 constexpr int kWhereQuantize = 6;               // status `where` of a timed-out row copy
 
 template <typename T, typename OutT, int kBlock>
@@ -730,13 +758,8 @@ cudaError_t launch_bulk_block(int prof_id, const T* A, int64_t M, int64_t K, int
       return cudaGetLastError();
     done = true;
   }
-  int per_sm = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_quantize_bulk_kernel<T, OutT, kBlock>, kBlock, smem) !=
-          cudaSuccess ||
-      per_sm < 1) {
-    cudaGetLastError();
-    per_sm = 1;
-  }
+  const int per_sm =
+      cached_blocks_per_sm(reinterpret_cast<const void*>(row_quantize_bulk_kernel<T, OutT, kBlock>), kBlock, smem);
   const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(sms) * per_sm));
   ProfScope ps(prof_id, s);
   row_quantize_bulk_kernel<T, OutT, kBlock><<<grid, kBlock, smem, s>>>(A, M, K, K_pad, mask, idx, st, cap_pad, scale,
@@ -781,15 +804,11 @@ cudaError_t launch_staged(int prof_id, const T* A, int64_t M, int64_t K, int64_t
       return cudaGetLastError();
     done = true;
   }
-  int dev = 0, sms = 152, per_sm = 1;
+  int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, act_quantize_staged_kernel<T, OutT>, kThreads, smem) !=
-          cudaSuccess ||
-      per_sm < 1) {
-    cudaGetLastError();
-    per_sm = 1;
-  }
+  const int per_sm = cached_blocks_per_sm(reinterpret_cast<const void*>(act_quantize_staged_kernel<T, OutT>), kThreads,
+                                          smem);
   const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(sms) * per_sm));
   ProfScope ps(prof_id, s);
   act_quantize_staged_kernel<T, OutT><<<grid, kThreads, smem, s>>>(A, M, K, K_pad, vec ? 1 : 0, mask, idx, st, cap_pad,
