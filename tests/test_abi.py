@@ -171,3 +171,47 @@ def test_valid_call_without_gpu_reports_error_not_crash(L):
 def test_max_k_is_the_int32_bound():
     assert _lib.I8LT_MAX_K * 127 * 127 < 2 ** 31 <= (_lib.I8LT_MAX_K + 1) * 127 * 127
     assert math.floor((2 ** 31 - 1) / 16129) == _lib.I8LT_MAX_K
+
+
+def test_nf4_sizes_and_levels(L):
+    assert _lib.i8lt_nf4_row_bytes(0) == 0 and _lib.i8lt_nf4_row_bytes(1) == 32 and _lib.i8lt_nf4_row_bytes(64) == 32
+    assert _lib.i8lt_nf4_row_bytes(65) == 64 and _lib.i8lt_nf4_row_bytes(-1) == -1
+    assert _lib.i8lt_nf4_blocks(0) == 0 and _lib.i8lt_nf4_blocks(1) == 1 and _lib.i8lt_nf4_blocks(129) == 3
+    assert _lib.i8lt_nf4_workspace_size() == 256
+    # the levels are computed on the host: no GPU needed
+    st, lv = _lib.i8lt_nf4_levels()
+    assert st == _lib.I8LT_OK and len(lv) == 16 and lv[0] == -1.0 and lv[7] == 0.0 and lv[15] == 1.0
+    assert all(a < b for a, b in zip(lv, lv[1:]))
+
+
+def nf4(which, **kw):
+    a = dict(X=FAKE, xt=1, M=64, K=64, packed=FAKE, absmax=FAKE, N=64, bias=None, bt=0, out=FAKE, ws=FAKE,
+             ws_bytes=256)
+    a.update(kw)
+    if which == "fwd":
+        return _lib.i8lt_nf4_forward(a["X"], a["xt"], a["M"], a["K"], a["packed"], a["absmax"], a["N"], a["bias"],
+                                     a["bt"], a["out"], a["ws"], a["ws_bytes"])
+    return _lib.i8lt_nf4_backward_input(a["X"], a["xt"], a["M"], a["N"], a["packed"], a["absmax"], a["K"], a["out"],
+                                        a["ws"], a["ws_bytes"])
+
+
+@pytest.mark.parametrize("which", ["fwd", "bwd"])
+def test_nf4_argument_errors(L, which):
+    assert nf4(which, xt=2) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE      # compute dtype f16 or bf16 only
+    assert nf4(which, xt=7) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert nf4(which, K=0) == _lib.I8LT_ERR_INVALID_ARG
+    assert nf4(which, N=0) == _lib.I8LT_ERR_INVALID_ARG
+    assert nf4(which, M=-1) == _lib.I8LT_ERR_INVALID_ARG
+    # the reduction dimension of X must give 16-byte rows
+    assert nf4(which, **({"K": 100} if which == "fwd" else {"N": 100})) == _lib.I8LT_ERR_INVALID_ARG
+    assert nf4(which, packed=None) == _lib.I8LT_ERR_INVALID_ARG
+    assert nf4(which, X=None) == _lib.I8LT_ERR_INVALID_ARG
+    assert nf4(which, X=FAKE + 8) == _lib.I8LT_ERR_MISALIGNED
+    assert nf4(which, ws=FAKE + 16) == _lib.I8LT_ERR_MISALIGNED
+    assert nf4(which, ws_bytes=255) == _lib.I8LT_ERR_WORKSPACE
+    if which == "fwd":
+        assert nf4(which, bias=FAKE, bt=9) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert _lib.i8lt_nf4_quantize(FAKE, 5, 4, 4, FAKE, FAKE) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert _lib.i8lt_nf4_quantize(FAKE, 0, 4, 4, FAKE + 4, FAKE) == _lib.I8LT_ERR_MISALIGNED
+    assert _lib.i8lt_nf4_quantize(FAKE, 0, 4, 0, FAKE, FAKE) == _lib.I8LT_OK    # nothing to do
+    assert _lib.i8lt_nf4_dequantize(FAKE, FAKE, 4, 4, FAKE, 3) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
