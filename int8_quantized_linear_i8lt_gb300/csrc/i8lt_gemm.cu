@@ -1317,39 +1317,29 @@ int resident_pairs(const void* fn, int threads, int smem_bytes, int* cached /* [
   return n;
 }
 
-bool set_smem_attr(const void* fn, int smem_bytes, bool& done) {
-  if (done) return true;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess) return false;
-  done = true;
-  return true;
-}
 
 }  // namespace
 
-bool g_attr_fwd = false, g_attr_fwd_silu = false, g_attr_bwd[4] = {false, false, false, false};
 
 cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_bytes) {
   // the backward reports the schedule the workspace-sized default picks: fused
   const void* fn = nullptr;
   int nthreads = 0, smem = 0;
-  bool* done = nullptr;
   int* cache = nullptr;
   if (kernel_id == K_FWD_GEMM) {
     fn = reinterpret_cast<const void*>(fwd_gemm_kernel<false>);
     nthreads = kThreads;
     smem = kFwdSmemBytes;
-    done = &g_attr_fwd;
     cache = g_pairs_fwd;
   } else if (kernel_id == K_BWD_GEMM) {
     fn = reinterpret_cast<const void*>(bwd_gemm_kernel<kModeI8>);
     nthreads = kBwdThreads;
     smem = BwdGeom<kModeI8>::kSmemBytes;
-    done = &g_attr_bwd[kModeI8];
     cache = g_pairs_bwd[kModeI8];
   } else {
     return cudaErrorInvalidValue;
   }
-  if (!set_smem_attr(fn, smem, *done)) return cudaGetLastError();
+  if (!ensure_smem_attr(fn, smem)) return cudaGetLastError();
   if (ctas != nullptr) *ctas = 2 * resident_pairs(fn, nthreads, smem, cache);
   if (threads != nullptr) *threads = nthreads;
   if (smem_bytes != nullptr) *smem_bytes = smem;
@@ -1384,7 +1374,7 @@ cudaError_t launch_fwd_variant(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaSt
   const int num_n = static_cast<int>(ceil_div(e.N, kPairN));
   if (num_m == 0 || num_n == 0) return cudaSuccess;
   const void* fn = reinterpret_cast<const void*>(fwd_gemm_kernel<kSilu>);
-  if (!set_smem_attr(fn, kFwdSmemBytes, kSilu ? g_attr_fwd_silu : g_attr_fwd)) return cudaGetLastError();
+  if (!ensure_smem_attr(fn, kFwdSmemBytes)) return cudaGetLastError();
   const int tiles = num_m * num_n;
   const int clusters = std::min(tiles, resident_pairs(fn, kThreads, kFwdSmemBytes, kSilu ? g_pairs_fwd_silu : g_pairs_fwd));
   const int group = std::min(num_m, 8);
@@ -1405,7 +1395,7 @@ cudaError_t launch_bwd_schedule(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaS
   const int num_m = static_cast<int>(ceil_div(e.M, Geo::kTileTokens));
   if (num_k == 0 || num_m == 0) return cudaSuccess;
   const void* fn = reinterpret_cast<const void*>(bwd_gemm_kernel<kMode>);
-  if (!set_smem_attr(fn, Geo::kSmemBytes, g_attr_bwd[kMode])) return cudaGetLastError();
+  if (!ensure_smem_attr(fn, Geo::kSmemBytes)) return cudaGetLastError();
   const int tiles = num_k * num_m;
   const int clusters = std::min(tiles, resident_pairs(fn, kBwdThreads, Geo::kSmemBytes, g_pairs_bwd[kMode]));
   const int group = std::min(num_m, 8);

@@ -172,6 +172,11 @@ cudaError_t launch_nf4_dequantize(const uint8_t* packed, const float* absmax, in
 cudaError_t launch_dequant_weight(const int8_t* CB, const float* SCB, int64_t N, int64_t k_pad, __half* WdqT,
                                   int64_t n_pad, cudaStream_t s);
 
+// Raise a kernel's dynamic shared-memory limit to smem_bytes on the current
+// device, once per (kernel, device): later calls, also those made while a
+// stream is being captured, issue no CUDA call.
+bool ensure_smem_attr(const void* fn, int smem_bytes);
+
 // Persistent launch shape of a GEMM kernel (K_FWD_GEMM / K_BWD_GEMM).
 cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_bytes);
 

@@ -605,6 +605,24 @@ __device__ __forceinline__ void smem_load8_half(const T* p, __half (&h)[8]) {
     for (int j = 0; j < kVec; ++j) h[v * kVec + j] = to_half(x[j]);
   }
 }
+bool ensure_smem_attr(const void* fn, int smem_bytes) {
+  struct Entry {
+    const void* fn;
+    int dev, smem;
+  };
+  static Entry done[128];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (done[i].fn == fn && done[i].dev == dev && done[i].smem >= smem_bytes) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess) return false;
+  if (used < 128) done[used++] = Entry{fn, dev, smem_bytes};
+  return true;
+}
+
 // Blocks per SM of a kernel at a given dynamic shared-memory size, cached
 // per (kernel, device, size) so that launches made while a stream is being
 // captured into a CUDA graph query nothing.
@@ -751,13 +769,9 @@ cudaError_t launch_bulk_block(int prof_id, const T* A, int64_t M, int64_t K, int
                               const int* idx, DevStatus* st, int64_t cap_pad, float* scale, OutT* codes, __half* sub,
                               uint32_t* asq, int row_bytes, int sms, cudaStream_t s) {
   const int smem = 2 * row_bytes;
-  static bool done = false;
-  if (!done) {
-    if (cudaFuncSetAttribute(row_quantize_bulk_kernel<T, OutT, kBlock>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             2 * kBulkMaxRowBytes) != cudaSuccess)
-      return cudaGetLastError();
-    done = true;
-  }
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(row_quantize_bulk_kernel<T, OutT, kBlock>),
+                        2 * kBulkMaxRowBytes))
+    return cudaGetLastError();
   const int per_sm =
       cached_blocks_per_sm(reinterpret_cast<const void*>(row_quantize_bulk_kernel<T, OutT, kBlock>), kBlock, smem);
   const int grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(sms) * per_sm));
@@ -797,13 +811,8 @@ cudaError_t launch_staged(int prof_id, const T* A, int64_t M, int64_t K, int64_t
                           const int* idx, const DevStatus* st, int64_t cap_pad, float* scale, OutT* codes,
                           __half* sub, uint32_t* asq, cudaStream_t s) {
   const int smem = static_cast<int>(K_pad * 2);
-  static bool done = false;
-  if (!done) {
-    if (cudaFuncSetAttribute(act_quantize_staged_kernel<T, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStagedMaxLd * 2) != cudaSuccess)
-      return cudaGetLastError();
-    done = true;
-  }
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(act_quantize_staged_kernel<T, OutT>), kStagedMaxLd * 2))
+    return cudaGetLastError();
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
