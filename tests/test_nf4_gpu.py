@@ -143,3 +143,23 @@ def test_module_autograd():
     assert torch.equal(x.grad.reshape(M, K), I.nf4_backward_input(G.reshape(M, N), layer.packed, layer.absmax, K))
     ref_gb = G.reshape(M, N).double().sum(0)
     assert torch.allclose(layer.bias.grad.double(), ref_gb, rtol=1e-2, atol=1e-1)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_decoded_weight_inside_the_matmuls_is_bit_exact(dtype):
+    """With one-hot inputs every output is a single product 1 * Wdq, exact
+    in the fp32 accumulator and in the 16-bit output, so the forward returns
+    rows of Wdq^T and the input gradient rows of Wdq: the weight decoded
+    inside the tensor-core pipeline equals the oracle's dequantized weight
+    bit for bit, in both orientations."""
+    N, K = 712, 1000                                   # ragged: 256-row tiles and 64-element blocks
+    Wf = _weight(N, K, dtype, 21, std=0.05)
+    packed, absmax, p_ref, a_ref = _check_quant(Wf, K)
+    wdq = ON.dequantize(p_ref, a_ref, K, ODT[dtype])   # [N, K] storage of the oracle
+    eye_k = torch.eye(K, dtype=dtype, device=DEV)
+    ref = O.widen(wdq, ODT[dtype])                     # values: a zero level may come back as -0
+    out = I.nf4_forward(eye_k, packed, absmax, K)      # [K, N] = Wdq^T
+    assert np.array_equal(O.widen(to_np(out), ODT[dtype]), ref.T)
+    eye_n = torch.eye(N, dtype=dtype, device=DEV)
+    gA = I.nf4_backward_input(eye_n, packed, absmax, K)  # [N, K] = Wdq
+    assert np.array_equal(O.widen(to_np(gA), ODT[dtype]), ref)
