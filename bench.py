@@ -535,28 +535,35 @@ def time_nf4(stream, steps, device, warmup=3):
         lay.append((spec, A, G, packed, absmax, out, gA))
         del Wf
 
-    def step():
+    ws_dq = torch.empty(max(_lib.i8lt_nf4_workspace_size_dq(s_.K, s_.N) for s_ in wl.layers), dtype=torch.uint8,
+                        device=device)
+
+    def step(w):
         for spec, A, G, packed, absmax, out, gA in lay:
             dt = DTYPE_CODE[spec.dtype]
             st = _lib.i8lt_nf4_forward(A.data_ptr(), dt, spec.M, spec.K, packed.data_ptr(), absmax.data_ptr(), spec.N,
-                                       None, 0, out.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+                                       None, 0, out.data_ptr(), w.data_ptr(), w.numel(), sp)
             assert st == 0, _lib.i8lt_status_string(st)
             st = _lib.i8lt_nf4_backward_input(G.data_ptr(), dt, spec.M, spec.N, packed.data_ptr(), absmax.data_ptr(),
-                                              spec.K, gA.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+                                              spec.K, gA.data_ptr(), w.data_ptr(), w.numel(), sp)
             assert st == 0, _lib.i8lt_status_string(st)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    _lib.i8lt_profile_start(1 << 16)
-    ev0.record(stream)
-    for _ in range(steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    _, recs, n_launches = _lib.i8lt_profile_stop(1 << 16)
-    ms = reduce_max(ev0.elapsed_time(ev1), device)
+    def timed(w):
+        for _ in range(warmup):
+            step(w)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _lib.i8lt_profile_start(1 << 16)
+        e0.record(stream)
+        for _ in range(steps):
+            step(w)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        _, r, n = _lib.i8lt_profile_stop(1 << 16)
+        return reduce_max(e0.elapsed_time(e1), device), r, n
+
+    ms, recs, n_launches = timed(ws)          # fused: the weight decoded inside the GEMM
+    ms_dq, recs_dq, _ = timed(ws_dq)          # materialized: dequantized weight in the workspace
     flops = sum(4.0 * spec.M * spec.N * spec.K for spec, *_ in lay) * steps
     half = flops / 2
     peaks, src = load_peaks()
@@ -570,6 +577,15 @@ def time_nf4(stream, steps, device, warmup=3):
             tf = half / (k_ms * 1e-3) / 1e12
             res[name] = {"tflops": round(tf, 1), "frac_tensor": round(tf / peak_t, 4),
                          "ms_per_launch": round(k_ms / (steps * len(lay)), 4)}
+    res["materialized"] = {"value": round(reduce_sum(flops, device) / (ms_dq * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                           "ms_per_step": round(ms_dq / steps, 4),
+                           "dequantize_ms_per_step": round(sum(t for n, t in recs_dq if n == "nf4_dequantize") / steps,
+                                                           4)}
+    for name in ("nf4_gemm_fwd", "nf4_gemm_bwd"):
+        k_ms = sum(t for n, t in recs_dq if n == name)
+        if k_ms:
+            tf = half / (k_ms * 1e-3) / 1e12
+            res["materialized"][name] = {"tflops": round(tf, 1), "frac_tensor": round(tf / peak_t, 4)}
     res["peak"] = peak_t
     res["peak_source"] = f"{src} bf16 sustained"
     return res

@@ -336,15 +336,23 @@ int i8lt_nf4_quantize(const void* W, int wt, int64_t N, int64_t K,
 /* The dequantized weight Wdq [N, K] row-major in dtype dt (device). */
 int i8lt_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N,
                         int64_t K, void* out, int dt, void* stream);
-/* Workspace of the two matmuls: the device status word (256 bytes). */
+/* Workspace of the two matmuls: the device status word (256 bytes).  The
+ * weight is then decoded stage by stage inside the GEMM and never stored. */
 size_t i8lt_nf4_workspace_size(void);
+/* A workspace of at least this many bytes (256 + N * K * 2; 0 for invalid
+ * sizes) selects the materialized schedule instead: a prepass writes the
+ * dequantized weight into the workspace (Wdq [N, K] for the forward, Wdq^T
+ * [K, N] for the input gradient) and a TMA-fed GEMM reads it.  Same results
+ * bit for bit, more memory, faster. */
+size_t i8lt_nf4_workspace_size_dq(int64_t K, int64_t N);
 /*
  * out [M, N] = rn(A [M, K] @ Wdq^T + bias), A and out in the compute dtype
  * at (I8LT_F16 or I8LT_BF16), fp32 accumulation on the tensor
  * cores; the weight is decoded stage by stage in shared memory and never
  * stored.  bias [N] of dtype bt or NULL.  K a multiple of 8 (16-byte rows
  * for the tensor-memory copies), else I8LT_ERR_INVALID_ARG; A, packed, out
- * 16-byte aligned; ws of i8lt_nf4_workspace_size bytes, 256-byte aligned.
+ * 16-byte aligned; ws of i8lt_nf4_workspace_size bytes (or
+ * i8lt_nf4_workspace_size_dq, see there), 256-byte aligned.
  */
 int i8lt_nf4_forward(const void* A, int at, int64_t M, int64_t K,
                      const uint8_t* packed, const float* absmax, int64_t N,

@@ -89,6 +89,7 @@ SIGNATURES = {
     "i8lt_nf4_quantize": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_void_p]),
     "i8lt_nf4_dequantize": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_int, c_void_p]),
     "i8lt_nf4_workspace_size": (c_size_t, []),
+    "i8lt_nf4_workspace_size_dq": (c_size_t, [c_int64, c_int64]),
     "i8lt_nf4_forward": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64, c_void_p, c_int,
                                  c_void_p, c_void_p, c_size_t, c_void_p]),
     "i8lt_nf4_backward_input": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64, c_void_p,
@@ -244,6 +245,10 @@ def i8lt_nf4_dequantize(packed, absmax, N, K, out, dt, stream=None) -> int:
 
 def i8lt_nf4_workspace_size() -> int:
     return load().i8lt_nf4_workspace_size()
+
+
+def i8lt_nf4_workspace_size_dq(K, N) -> int:
+    return load().i8lt_nf4_workspace_size_dq(int(K), int(N))
 
 
 def i8lt_nf4_forward(A, at, M, K, packed, absmax, N, bias, bt, out, ws, ws_bytes, stream=None) -> int:

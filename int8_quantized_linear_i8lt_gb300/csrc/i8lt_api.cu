@@ -594,6 +594,11 @@ int i8lt_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, i
 
 size_t i8lt_nf4_workspace_size(void) { return kAlign; }
 
+size_t i8lt_nf4_workspace_size_dq(int64_t K, int64_t N) {
+  if (K < 0 || N < 0 || K > INT32_MAX / 2 || N > INT32_MAX / 2) return 0;
+  return kAlign + align_up(static_cast<size_t>(N) * static_cast<size_t>(K) * 2);
+}
+
 }  // extern "C"
 
 namespace {
@@ -623,11 +628,23 @@ int nf4_gemm(bool input_grad, const void* X, int xt, int64_t M, int64_t C, int64
   BwdGemmArgs g;
   std::memset(&g, 0, sizeof(g));
   if (!make_tmap(&g.tmG, xdt, X, C, M, C * 2, kBK, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B)) return I8LT_ERR_CUDA;
-  // weight tiles: [64 n][128 k] (64 bytes a row) for the input gradient,
-  // [128 n][64 k] (32 bytes a row) for the forward
-  if (!make_tmap(&g.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, row_bytes, N, row_bytes, input_grad ? 64 : 32,
-                 input_grad ? kBK : kBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+  // a workspace with room for the dequantized weight selects the materialized
+  // schedule: a prepass writes Wdq [N, K] (forward) or Wdq^T [K, N] (input
+  // gradient) and the GEMM reads it by TMA; otherwise the weight is decoded
+  // per stage inside the GEMM
+  const bool materialize = ws_bytes >= i8lt_nf4_workspace_size_dq(K, N);
+  if (materialize) {
+    void* wdq = static_cast<uint8_t*>(ws) + kAlign;
+    cudaError_t e = input_grad ? launch_nf4_dequantize_t(packed, absmax, N, K, row_bytes, wdq, xt, s)
+                               : launch_nf4_dequantize(packed, absmax, N, K, row_bytes, wdq, xt, s);
+    if (e != cudaSuccess) return I8LT_ERR_CUDA;
+    if (!make_tmap(&g.tmWT, xdt, wdq, C, R, C * 2, kBK, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B)) return I8LT_ERR_CUDA;
+  } else if (!make_tmap(&g.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, row_bytes, N, row_bytes,
+                        input_grad ? 64 : 32, input_grad ? kBK : kBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+    // weight tiles: [64 n][128 k] (64 bytes a row) for the input gradient,
+    // [128 n][64 k] (32 bytes a row) for the forward
     return I8LT_ERR_CUDA;
+  }
   BwdEpiArgs ea;
   std::memset(&ea, 0, sizeof(ea));
   ea.M = static_cast<int>(M);
@@ -642,7 +659,7 @@ int nf4_gemm(bool input_grad, const void* X, int xt, int64_t M, int64_t C, int64
   ea.absmax = absmax;
   ea.nblk = static_cast<int>(ceil_div(K, 64));
   nf4_levels(ea.lv);
-  return cuda_status(launch_nf4_gemm(g, ea, input_grad, s));
+  return cuda_status(launch_nf4_gemm(g, ea, input_grad, materialize, s));
 }
 
 }  // namespace

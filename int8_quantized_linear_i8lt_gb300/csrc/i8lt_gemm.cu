@@ -1408,9 +1408,11 @@ cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool fuse
   return fused ? launch_bwd_schedule<kModeI8>(g, e, s, K_BWD_GEMM) : launch_bwd_schedule<kModeMat>(g, e, s, K_BWD_GEMM);
 }
 
-cudaError_t launch_nf4_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool input_grad, cudaStream_t s) {
-  return input_grad ? launch_bwd_schedule<kModeNf4T>(g, e, s, K_NF4_GEMM_BWD)
-                    : launch_bwd_schedule<kModeNf4>(g, e, s, K_NF4_GEMM_FWD);
+cudaError_t launch_nf4_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool input_grad, bool materialized,
+                            cudaStream_t s) {
+  const int prof = input_grad ? K_NF4_GEMM_BWD : K_NF4_GEMM_FWD;
+  if (materialized) return launch_bwd_schedule<kModeMat>(g, e, s, prof);
+  return input_grad ? launch_bwd_schedule<kModeNf4T>(g, e, s, prof) : launch_bwd_schedule<kModeNf4>(g, e, s, prof);
 }
 
 cudaError_t launch_dequant_weight(const int8_t* CB, const float* SCB, int64_t N, int64_t k_pad, __half* WdqT,

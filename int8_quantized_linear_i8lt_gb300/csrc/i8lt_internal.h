@@ -155,13 +155,19 @@ cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool fuse
 // (tmW: the packed codes [rows, row_bytes] uint8, no swizzle; box 64 x 64 for
 // the input gradient, 32 x 128 for the forward; tmG: the 16-bit activations
 // or output gradient, box 64 x 128, 128B swizzle).
-cudaError_t launch_nf4_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool input_grad, cudaStream_t s);
+// materialized: A operand read by TMA from a dequantized copy (tmWT: [R, C]
+// 16-bit, box 64 x 128, 128B swizzle) instead of decoded per stage.
+cudaError_t launch_nf4_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool input_grad, bool materialized,
+                            cudaStream_t s);
 
 // The 16 NF4 levels (ascending fp32), computed once on the host.
 void nf4_levels(float out[16]);
 // W [N, K] (dtype wt) -> packed [N, row_bytes] codes and absmax [N, ceil(K / 64)].
 cudaError_t launch_nf4_quantize(const void* W, int wt, int64_t N, int64_t K, int64_t row_bytes, uint8_t* packed,
                                 float* absmax, cudaStream_t s);
+// packed + absmax -> WdqT [K, N] (dtype dt, f16 or bf16; N a multiple of 8).
+cudaError_t launch_nf4_dequantize_t(const uint8_t* packed, const float* absmax, int64_t N, int64_t K,
+                                    int64_t row_bytes, void* WdqT, int dt, cudaStream_t s);
 // packed + absmax -> out [N, K] (dtype dt): lv[code] * absmax, rounded once.
 cudaError_t launch_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, int64_t K,
                                   int64_t row_bytes, void* out, int dt, cudaStream_t s);

@@ -120,7 +120,7 @@ template <typename OutT>
 __global__ void __launch_bounds__(256) nf4_dequantize_kernel(const uint8_t* __restrict__ packed,
                                                              const float* __restrict__ absmax, int64_t N, int64_t K,
                                                              int64_t row_bytes, int nblk, Nf4Tables c,
-                                                             OutT* __restrict__ out) {
+                                                             bool vec, OutT* __restrict__ out) {
   const int64_t gpr = row_bytes / 4;
   const int64_t total = N * gpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -131,13 +131,75 @@ __global__ void __launch_bounds__(256) nf4_dequantize_kernel(const uint8_t* __re
     if (k0 >= K) continue;
     const uint32_t word = *reinterpret_cast<const uint32_t*>(packed + n * row_bytes + kg * 4);
     const float am = absmax[n * nblk + (kg >> 3)];
+    OutT o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      if (k0 + i < K) {
-        const uint32_t code = (word >> (8 * (i >> 1) + ((i & 1) ? 0 : 4))) & 15u;
-        out[n * K + k0 + i] = from_float<OutT>(__fmul_rn(c.lv[code], am));
-      }
+      const uint32_t code = (word >> (8 * (i >> 1) + ((i & 1) ? 0 : 4))) & 15u;
+      o[i] = from_float<OutT>(__fmul_rn(c.lv[code], am));
     }
+    OutT* dst = out + n * K + k0;
+    if (vec && k0 + 8 <= K) {   // 16 or 32 bytes at an aligned address
+      if constexpr (sizeof(OutT) == 2) {
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
+      } else {
+        reinterpret_cast<uint4*>(dst)[0] = reinterpret_cast<const uint4*>(o)[0];
+        reinterpret_cast<uint4*>(dst)[1] = reinterpret_cast<const uint4*>(o)[1];
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (k0 + i < K) dst[i] = o[i];
+    }
+  }
+}
+
+// Transposed dequantization for the materialized input gradient: WdqT[k, n]
+// = Wdq[n, k], [K, N] with N a multiple of 8.  One block per 64 (n) x 128 (k)
+// tile: the packed bytes (64 a row) and the two absmax values of each row
+// are staged in shared memory, then each thread writes 8 consecutive n of one
+// k with one 16-byte store.
+constexpr int kTn = 64, kTk = 128, kTPitch = kTk / 2 + 4;
+template <typename OutT>
+__global__ void __launch_bounds__(256) nf4_dequantize_t_kernel(const uint8_t* __restrict__ packed,
+                                                               const float* __restrict__ absmax, int64_t N, int64_t K,
+                                                               int64_t row_bytes, int nblk, Nf4Tables c,
+                                                               OutT* __restrict__ WdqT) {
+  __shared__ __align__(16) uint8_t tile[kTn * kTPitch];
+  __shared__ float am_s[kTn][2];
+  __shared__ float lv_s[16];
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTn;
+  const int64_t k0 = static_cast<int64_t>(blockIdx.y) * kTk;
+  {
+    const int nl = threadIdx.x >> 2, q = threadIdx.x & 3;   // 64 rows x 4 chunks of 16 bytes
+    const int64_t n = n0 + nl, byte = k0 / 2 + q * 16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < N && byte < row_bytes) v = *reinterpret_cast<const uint4*>(packed + n * row_bytes + byte);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(tile + nl * kTPitch + q * 16);
+    dst[0] = v.x;
+    dst[1] = v.y;
+    dst[2] = v.z;
+    dst[3] = v.w;
+  }
+  if (threadIdx.x < 2 * kTn) {
+    const int nl = threadIdx.x >> 1, b = threadIdx.x & 1;
+    const int64_t n = n0 + nl, kb = k0 / 64 + b;
+    am_s[nl][b] = (n < N && kb < nblk) ? absmax[n * nblk + kb] : 0.f;
+  }
+  if (threadIdx.x < 16) lv_s[threadIdx.x] = c.lv[threadIdx.x];
+  __syncthreads();
+  for (int it = threadIdx.x; it < kTk * (kTn / 8); it += 256) {
+    const int g8 = it & 7, kl = it >> 3;
+    const int64_t k = k0 + kl, n = n0 + g8 * 8;
+    if (k >= K || n >= N) continue;
+    OutT o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int nl = g8 * 8 + i;
+      const uint32_t byte = tile[nl * kTPitch + (kl >> 1)];
+      const uint32_t code = (kl & 1) ? (byte & 15u) : (byte >> 4);
+      o[i] = from_float<OutT>(__fmul_rn(lv_s[code], am_s[nl][kl >> 6]));
+    }
+    *reinterpret_cast<uint4*>(WdqT + k * N + n) = *reinterpret_cast<const uint4*>(o);
   }
 }
 
@@ -185,20 +247,40 @@ cudaError_t launch_nf4_dequantize(const uint8_t* packed, const float* absmax, in
   const int nblk = static_cast<int>(ceil_div(K, 64));
   const int blocks = grid_for(N * (row_bytes / 4));
   const Nf4Tables& c = tables();
+  // rows of K elements start 16-byte aligned when K is a multiple of 8 and
+  // the output is 16-byte aligned
+  const bool vec = (K % 8) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
   ProfScope ps(K_NF4_DEQUANTIZE, s);
   switch (dt) {
     case DT_F16:
-      nf4_dequantize_kernel<__half><<<blocks, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c,
+      nf4_dequantize_kernel<__half><<<blocks, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c, vec,
                                                            static_cast<__half*>(out));
       break;
     case DT_BF16:
-      nf4_dequantize_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c,
+      nf4_dequantize_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c, vec,
                                                                   static_cast<__nv_bfloat16*>(out));
       break;
     default:
-      nf4_dequantize_kernel<float><<<blocks, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c,
+      nf4_dequantize_kernel<float><<<blocks, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c, vec,
                                                           static_cast<float*>(out));
       break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nf4_dequantize_t(const uint8_t* packed, const float* absmax, int64_t N, int64_t K,
+                                    int64_t row_bytes, void* WdqT, int dt, cudaStream_t s) {
+  if (N == 0 || K == 0) return cudaSuccess;
+  const int nblk = static_cast<int>(ceil_div(K, 64));
+  const dim3 grid(static_cast<unsigned>(ceil_div(N, kTn)), static_cast<unsigned>(ceil_div(K, kTk)));
+  const Nf4Tables& c = tables();
+  ProfScope ps(K_NF4_DEQUANTIZE, s);
+  if (dt == DT_BF16) {
+    nf4_dequantize_t_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c,
+                                                                 static_cast<__nv_bfloat16*>(WdqT));
+  } else {
+    nf4_dequantize_t_kernel<__half><<<grid, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c,
+                                                          static_cast<__half*>(WdqT));
   }
   return cudaGetLastError();
 }

@@ -439,15 +439,20 @@ def nf4_dequantize(packed: torch.Tensor, absmax: torch.Tensor, K: int, dtype: to
     return out
 
 
-def _nf4_ws(device, ws):
+def _nf4_ws(device, ws, K, N, materialized):
+    """Workspace of the 4-bit matmuls: the status word only (the weight is
+    decoded inside the GEMM), or room for the dequantized weight
+    (``materialized``: a prepass writes it, a plain 16-bit GEMM reads it;
+    same bits, faster, N * K * 2 bytes more)."""
     if ws is None:
-        ws = torch.empty(_lib.i8lt_nf4_workspace_size(), dtype=torch.uint8, device=device)
+        n = _lib.i8lt_nf4_workspace_size_dq(K, N) if materialized else _lib.i8lt_nf4_workspace_size()
+        ws = torch.empty(n, dtype=torch.uint8, device=device)
     return ws
 
 
 def nf4_forward(A: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: int,
                 bias: torch.Tensor | None = None, out: torch.Tensor | None = None,
-                ws: torch.Tensor | None = None) -> torch.Tensor:
+                ws: torch.Tensor | None = None, materialized: bool = False) -> torch.Tensor:
     """out [M, N] = A [M, K] @ Wdq^T (+ bias) in A's dtype (f16 or bf16)."""
     _require_cuda(A, packed, absmax, bias)
     A = A.contiguous()
@@ -455,7 +460,7 @@ def nf4_forward(A: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: 
     N = packed.shape[0]
     if out is None:
         out = torch.empty(M, N, dtype=A.dtype, device=A.device)
-    ws = _nf4_ws(A.device, ws)
+    ws = _nf4_ws(A.device, ws, K, N, materialized)
     _check(_lib.i8lt_nf4_forward(A.data_ptr(), _code(A.dtype), M, K, packed.data_ptr(), absmax.data_ptr(), N,
                                  _ptr(bias), _code(bias.dtype) if bias is not None else 0, out.data_ptr(),
                                  ws.data_ptr(), ws.numel(), _stream(A)), "i8lt_nf4_forward")
@@ -463,14 +468,15 @@ def nf4_forward(A: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: 
 
 
 def nf4_backward_input(G: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: int,
-                       out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+                       out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                       materialized: bool = False) -> torch.Tensor:
     """grad_A [M, K] = G [M, N] @ Wdq in G's dtype (f16 or bf16)."""
     _require_cuda(G, packed, absmax)
     G = G.contiguous()
     M, N = G.shape
     if out is None:
         out = torch.empty(M, K, dtype=G.dtype, device=G.device)
-    ws = _nf4_ws(G.device, ws)
+    ws = _nf4_ws(G.device, ws, K, N, materialized)
     _check(_lib.i8lt_nf4_backward_input(G.data_ptr(), _code(G.dtype), M, N, packed.data_ptr(), absmax.data_ptr(),
                                         K, out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(G)),
            "i8lt_nf4_backward_input")

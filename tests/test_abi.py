@@ -178,6 +178,9 @@ def test_nf4_sizes_and_levels(L):
     assert _lib.i8lt_nf4_row_bytes(65) == 64 and _lib.i8lt_nf4_row_bytes(-1) == -1
     assert _lib.i8lt_nf4_blocks(0) == 0 and _lib.i8lt_nf4_blocks(1) == 1 and _lib.i8lt_nf4_blocks(129) == 3
     assert _lib.i8lt_nf4_workspace_size() == 256
+    assert _lib.i8lt_nf4_workspace_size_dq(64, 64) == 256 + 64 * 64 * 2
+    assert _lib.i8lt_nf4_workspace_size_dq(100, 3) == 256 + 768       # rounded up to 256 bytes
+    assert _lib.i8lt_nf4_workspace_size_dq(-1, 8) == 0
     # the levels are computed on the host: no GPU needed
     st, lv = _lib.i8lt_nf4_levels()
     assert st == _lib.I8LT_OK and len(lv) == 16 and lv[0] == -1.0 and lv[7] == 0.0 and lv[15] == 1.0

@@ -76,6 +76,9 @@ def test_forward_and_input_gradient(M, K, N, dtype, bias):
     gA = I.nf4_backward_input(G.to(DEV), packed, absmax, K)
     rb = ON.backward_input(to_np(G), ODT[dtype], p_ref, a_ref, K)
     assert_tol(O.widen(to_np(gA), ODT[dtype]), rb["grad64"], "nf4 grad_A")
+    # the materialized schedule (dequantized weight in the workspace) gives the same bits
+    assert torch.equal(I.nf4_forward(A.to(DEV), packed, absmax, K, b.to(DEV) if bias else None, materialized=True), out)
+    assert torch.equal(I.nf4_backward_input(G.to(DEV), packed, absmax, K, materialized=True), gA)
 
 
 @pytest.mark.parametrize("li", [0, 1])
@@ -89,6 +92,8 @@ def test_qlora_7b_layers_sampled_rows(li):
     packed, absmax, p_ref, a_ref = _check_quant(Wf, spec.K)
     out = I.nf4_forward(A.to(DEV), packed, absmax, spec.K)
     gA = I.nf4_backward_input(G.to(DEV), packed, absmax, spec.K)
+    assert torch.equal(I.nf4_forward(A.to(DEV), packed, absmax, spec.K, materialized=True), out)
+    assert torch.equal(I.nf4_backward_input(G.to(DEV), packed, absmax, spec.K, materialized=True), gA)
     rows = np.unique(np.concatenate([[0, spec.M - 1], np.random.default_rng(li).integers(0, spec.M, 62)]))
     dt = ODT[spec.dtype]
     ref = ON.forward(to_np(A), dt, p_ref, a_ref, spec.K, rows=rows)
