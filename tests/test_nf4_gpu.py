@@ -168,3 +168,24 @@ def test_decoded_weight_inside_the_matmuls_is_bit_exact(dtype):
     eye_n = torch.eye(N, dtype=dtype, device=DEV)
     gA = I.nf4_backward_input(eye_n, packed, absmax, K)  # [N, K] = Wdq
     assert np.array_equal(O.widen(to_np(gA), ODT[dtype]), ref)
+
+
+@pytest.mark.parametrize("M,K,N,dtype,bias_dtype", [(1, 8, 8, torch.bfloat16, None),          # smallest legal shape
+                                                    (3, 8, 264, torch.float16, torch.float32),  # fp32 bias
+                                                    (513, 72, 8, torch.bfloat16, torch.bfloat16)])
+def test_small_and_edge_shapes(M, K, N, dtype, bias_dtype):
+    Wf = _weight(N, K, dtype, 31)
+    A = W.normal((M, K), 1.0, 32, dtype)
+    G = W.normal((M, N), 1.0, 33, dtype)
+    b = W.normal((N,), 0.1, 34, bias_dtype) if bias_dtype is not None else None
+    packed, absmax, p_ref, a_ref = _check_quant(Wf, K)
+    out = I.nf4_forward(A.to(DEV), packed, absmax, K, b.to(DEV) if b is not None else None)
+    ref = ON.forward(to_np(A), ODT[dtype], p_ref, a_ref, K, to_np(b) if b is not None else None,
+                     ODT[bias_dtype] if b is not None else None)
+    assert_tol(O.widen(to_np(out), ODT[dtype]), ref["out64"], "nf4 forward")
+    gA = I.nf4_backward_input(G.to(DEV), packed, absmax, K)
+    rb = ON.backward_input(to_np(G), ODT[dtype], p_ref, a_ref, K)
+    assert_tol(O.widen(to_np(gA), ODT[dtype]), rb["grad64"], "nf4 grad_A")
+    assert torch.equal(I.nf4_forward(A.to(DEV), packed, absmax, K, b.to(DEV) if b is not None else None,
+                                     materialized=True), out)
+    assert torch.equal(I.nf4_backward_input(G.to(DEV), packed, absmax, K, materialized=True), gA)
