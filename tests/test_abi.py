@@ -7,6 +7,7 @@ every call returns at its argument checks.
 """
 import ctypes
 import math
+import os
 
 import pytest
 
@@ -218,3 +219,22 @@ def test_nf4_argument_errors(L, which):
     assert _lib.i8lt_nf4_quantize(FAKE, 0, 4, 4, FAKE + 4, FAKE) == _lib.I8LT_ERR_MISALIGNED
     assert _lib.i8lt_nf4_quantize(FAKE, 0, 4, 0, FAKE, FAKE) == _lib.I8LT_OK    # nothing to do
     assert _lib.i8lt_nf4_dequantize(FAKE, FAKE, 4, 4, FAKE, 3) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+
+
+def test_header_compiles_as_c_and_links(L, tmp_path):
+    """A C99 program includes include/i8lt.h, links libi8lt.so and runs the
+    host-side entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    exe = str(tmp_path / "abi_smoke")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                        os.path.join(root, "tests", "c", "abi_smoke.c"), "-L", libdir, "-li8lt",
+                        "-Wl,-rpath," + libdir, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
