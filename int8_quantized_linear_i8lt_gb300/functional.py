@@ -488,12 +488,12 @@ class NF4LinearFunction(torch.autograd.Function):
     matmuls; gradients to x and to the bias (summed over the tokens)."""
 
     @staticmethod
-    def forward(ctx, x, packed, absmax, K, bias):
+    def forward(ctx, x, packed, absmax, K, bias, materialized=False):
         shape = x.shape
         x2 = x.reshape(-1, K)
-        y = nf4_forward(x2, packed, absmax, K, bias)
+        y = nf4_forward(x2, packed, absmax, K, bias, materialized=materialized)
         ctx.save_for_backward(packed, absmax)
-        ctx.K, ctx.shape, ctx.has_bias = K, shape, bias is not None
+        ctx.K, ctx.shape, ctx.has_bias, ctx.materialized = K, shape, bias is not None, materialized
         ctx.bias_dtype = bias.dtype if bias is not None else None
         return y.reshape(*shape[:-1], packed.shape[0])
 
@@ -501,6 +501,8 @@ class NF4LinearFunction(torch.autograd.Function):
     def backward(ctx, gy):
         packed, absmax = ctx.saved_tensors
         g2 = gy.reshape(-1, packed.shape[0])
-        gx = nf4_backward_input(g2, packed, absmax, ctx.K).reshape(ctx.shape) if ctx.needs_input_grad[0] else None
+        gx = None
+        if ctx.needs_input_grad[0]:
+            gx = nf4_backward_input(g2, packed, absmax, ctx.K, materialized=ctx.materialized).reshape(ctx.shape)
         gb = g2.float().sum(0).to(ctx.bias_dtype) if ctx.has_bias and ctx.needs_input_grad[4] else None
-        return gx, None, None, None, gb
+        return gx, None, None, None, gb, None

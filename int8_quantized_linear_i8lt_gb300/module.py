@@ -101,14 +101,18 @@ class LinearNF4(torch.nn.Module):
     is stored as packed 4-bit codes with one fp32 absmax per 64 elements of a
     row and decoded to the 16-bit compute dtype (the input's: f16 or bf16)
     inside the tensor-core matmuls of the forward and of the input gradient.
-    The weight takes no gradient; the bias does."""
+    The weight takes no gradient; the bias does.  ``materialized``: each
+    matmul first writes the 16-bit weight to a temporary workspace and reads
+    it with a plain GEMM (faster, N * K * 2 bytes of transient memory);
+    the results are the same bits."""
 
     def __init__(self, in_features: int, out_features: int, bias: bool = True, device=None,
-                 bias_dtype: torch.dtype = torch.bfloat16):
+                 bias_dtype: torch.dtype = torch.bfloat16, materialized: bool = False):
         super().__init__()
         from . import _lib
         self.in_features = in_features
         self.out_features = out_features
+        self.materialized = bool(materialized)
         self.register_buffer("packed", torch.zeros(out_features, _lib.i8lt_nf4_row_bytes(in_features),
                                                    dtype=torch.uint8, device=device))
         self.register_buffer("absmax", torch.zeros(out_features, _lib.i8lt_nf4_blocks(in_features),
@@ -119,10 +123,11 @@ class LinearNF4(torch.nn.Module):
             self.register_parameter("bias", None)
 
     @classmethod
-    def from_float(cls, weight: torch.Tensor, bias: torch.Tensor | None = None) -> "LinearNF4":
+    def from_float(cls, weight: torch.Tensor, bias: torch.Tensor | None = None,
+                   materialized: bool = False) -> "LinearNF4":
         N, K = weight.shape
         layer = cls(K, N, bias=bias is not None, device=weight.device,
-                    bias_dtype=bias.dtype if bias is not None else torch.bfloat16)
+                    bias_dtype=bias.dtype if bias is not None else torch.bfloat16, materialized=materialized)
         packed, absmax = F.nf4_quantize(weight)
         layer.packed.copy_(packed)
         layer.absmax.copy_(absmax)
@@ -132,7 +137,7 @@ class LinearNF4(torch.nn.Module):
         return layer
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
-        return F.NF4LinearFunction.apply(x, self.packed, self.absmax, self.in_features, self.bias)
+        return F.NF4LinearFunction.apply(x, self.packed, self.absmax, self.in_features, self.bias, self.materialized)
 
     def extra_repr(self) -> str:
         return f"in_features={self.in_features}, out_features={self.out_features}, bias={self.bias is not None}"

@@ -148,6 +148,12 @@ def test_module_autograd():
     assert torch.equal(x.grad.reshape(M, K), I.nf4_backward_input(G.reshape(M, N), layer.packed, layer.absmax, K))
     ref_gb = G.reshape(M, N).double().sum(0)
     assert torch.allclose(layer.bias.grad.double(), ref_gb, rtol=1e-2, atol=1e-1)
+    # the materialized schedule through the module: the same bits
+    mat = I.LinearNF4.from_float(Wf.to(DEV), b.to(DEV), materialized=True)
+    x2 = x.detach().clone().requires_grad_(True)
+    y2 = mat(x2)
+    y2.backward(G)
+    assert torch.equal(y2, y) and torch.equal(x2.grad, x.grad)
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
