@@ -16,6 +16,11 @@
  *     and never stores them (PR description, backward bullet; review thread on
  *     ".mul(1/127.0)"), and sums grad_bias from the uncast grad_output (PR
  *     conversation, "grad_bias is now computed on natural grad_output").
+ * Beside it: the MLP's SiLU (with an optional fusion into the forward
+ * epilogue), a token-sharded forward, the weight gradient of the
+ * trainable-weight mode, the 4-bit NormalFloat weight-only layer of QLoRA
+ * fine-tuning, an entry point that allocates nothing, per-launch timing and
+ * a diagnostic of the bounded waits (each documented below).
  *
  * Conventions for every entry point:
  *   - Matrices are row-major and contiguous.  Device pointers unless stated.
