@@ -242,7 +242,8 @@ def kernel_bytes(L, name):
     kp = (s.K + 15) // 16 * 16
     return {
         "colmax": s.M * s.K * a + s.K * 4,
-        "row_quantize": s.M * s.K * a + s.M * kp * 2 + s.M * 4 + s.M * cap_pad * 2,
+        # the codes count as int8, one byte each, whatever form the kernel stores
+        "row_quantize": s.M * s.K * a + s.M * kp + s.M * 4 + s.M * cap_pad * 2,
         "gradout_prepass": s.M * s.N * a,
         "build_subB": s.N * cap_pad * 3,
         "widen_codes": s.N * kp * 3,
@@ -321,13 +322,20 @@ def run_ours(args):
     dom = max(kern, key=lambda k: kern[k]["ms"])
     peaks, peak_src = load_peaks()
     peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak_t_burst = float(peaks.get("bf16_tflops", peak_t))
     peak_b = float(peaks.get("hbm_gbs"))
     d = kern[dom]
     if d["flops"] > 0:
         achieved = d["flops"] / (d["ms"] * 1e-3) / 1e12
+        # the GEMMs run inside a seconds-long loop of steps under the power
+        # cap, so the headline fraction is against the sustained peak; the
+        # burst fraction is given beside it
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak_t,
                 "unit": "TFLOP/s", "frac": round(achieved / peak_t, 4),
-                "peak_source": f"{peak_src} bf16 sustained (fp16 runs at the bf16 rate)"}
+                "peak_source": f"{peak_src} bf16 sustained (fp16 runs at the bf16 rate; kind::f16 is the "
+                               "only tensor path of these GEMMs, sm_103a has no int8 tcgen05 MMA)",
+                "peak_burst": peak_t_burst, "frac_burst": round(achieved / peak_t_burst, 4),
+                "headline_peak": "sustained"}
     else:
         achieved = d["bytes"] / (d["ms"] * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak_b, "unit": "GB/s",
@@ -344,12 +352,15 @@ def run_ours(args):
              "share": round(v["ms"] / total_k_ms, 4)}
         if v["flops"]:
             t = v["flops"] / (v["ms"] * 1e-3) / 1e12
-            e.update(tflops=round(t, 1), frac_tensor=round(t / peak_t, 4))
+            e.update(tflops=round(t, 1), frac_tensor=round(t / peak_t, 4), frac_tensor_burst=round(t / peak_t_burst, 4))
         elif v["bytes"]:
             g = v["bytes"] / (v["ms"] * 1e-3) / 1e9
             e.update(gbs=round(g, 1), frac_hbm=round(g / peak_b, 4))
         kernels[k] = e
-    # --- per layer: forward (all its kernels) against the int8 peak, backward against the fp16 peak
+    # --- per layer: forward and backward (all their kernels) against the fp16 tensor peak.  The
+    # forward's int8 products run on the fp16 tensor cores (kind::f16, exact integer operands):
+    # sm_103a has no int8 tcgen05 MMA, so the kind::f16 rate is the forward's ceiling.  The int8
+    # rate the installed libraries reach through the legacy path is measured beside it as context.
     int8_peak = measure_int8_peak(device)
     layers_out = []
     for L, pl in zip(layers, per_layer):
@@ -360,9 +371,9 @@ def run_ours(args):
         entry = {"shape": [s_.M, s_.K, s_.N], "fwd_ms": round(pl["fwd_ms"] / args.steps, 4),
                  "bwd_ms": round(pl["bwd_ms"] / args.steps, 4), "fwd_tops": round(f_t, 1),
                  "bwd_tflops": round(b_t, 1), "fwd_bwd_tops": round(2 * w / ((pl["fwd_ms"] + pl["bwd_ms"]) * 1e-3) / 1e12, 1),
-                 "bwd_frac_fp16_peak": round(b_t / peak_t, 4)}
+                 "fwd_frac_fp16_peak": round(f_t / peak_t, 4), "bwd_frac_fp16_peak": round(b_t / peak_t, 4)}
         if int8_peak.get("tops"):
-            entry["fwd_frac_int8_peak"] = round(f_t / int8_peak["tops"], 4)
+            entry["fwd_vs_library_int8_rate"] = round(f_t / int8_peak["tops"], 2)
         layers_out.append(entry)
     # --- end to end through host buffers (pinned), inputs and results copied each step
     e2e = run_e2e(layers, stream, max(2, min(args.steps, 10)), device)
@@ -416,12 +427,11 @@ def run_ours(args):
 
 
 def measure_int8_peak(device, n=8192, iters=10):
-    """The int8 tensor-core rate of this GPU as the CUDA libraries reach it
-    (torch._int_mm, cuBLASLt int8 x int8 -> int32, n^3), for the forward's
-    fraction of the int8 peak.  sm_103a offers no int8 tcgen05 MMA, so this
-    is the legacy int8 tensor path; the library's forward runs the int8
-    codes on the fp16 tensor cores instead.  Context only, off the timed
-    region."""
+    """The int8 tensor rate of this GPU as the CUDA libraries reach it
+    (torch._int_mm, cuBLASLt int8 x int8 -> int32, n^3).  sm_103a offers no
+    int8 tcgen05 MMA, so this is the legacy int8 tensor path and not a
+    ceiling of the forward, which runs the int8 codes on the fp16 tensor
+    cores.  Context only, off the timed region."""
     try:
         a = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=device)
         b = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=device)
@@ -436,7 +446,10 @@ def measure_int8_peak(device, n=8192, iters=10):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / iters
         return {"tops": round(2.0 * n ** 3 / (ms * 1e-3) / 1e12, 1), "how": f"torch._int_mm {n}^3, best path of "
-                "the installed cuBLASLt, mean of 10 after 3 warm-up"}
+                "the installed cuBLASLt, mean of 10 after 3 warm-up",
+                "note": "context only, not a roofline: the legacy int8 tensor path of the libraries; sm_103a has no "
+                        "int8 tcgen05 MMA, so the forward runs its exact int8 products on the fp16 tensor cores "
+                        "and is judged against the fp16 peak (per_layer[*].fwd_frac_fp16_peak)"}
     except Exception as exc:   # no int8 GEMM in this build of the libraries
         return {"tops": None, "how": f"torch._int_mm unavailable: {type(exc).__name__}: {exc}"[:200]}
 

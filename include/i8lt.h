@@ -28,7 +28,8 @@
  *   - The caller owns every buffer, including the workspace.  The library
  *     allocates no device memory.
  *   - `stream` is a cudaStream_t passed as void*.  Work is asynchronous on it;
- *     nothing synchronizes except i8lt_read_device_status.
+ *     nothing synchronizes except i8lt_read_device_status and
+ *     i8lt_noalloc_read_device_status.
  *   - Errors found on the host are returned before anything is launched.
  *     Errors found on the device (outlier capacity exceeded, a pipeline wait
  *     that timed out) are written to the status word at the start of the
@@ -270,19 +271,29 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N,
  * CUDA events, so such callers should leave timing off.
  *
  * The first call on each device looks up the device address of the array
- * (once per device, with that device current); make that first call before
- * any stream capture.  Every call shares the one array, which keeps the last
- * call's contents (each call clears the status word it needs): calls whose
- * work overlaps on the GPU (other streams, other threads) race on it and
- * must be serialised by the caller.  The status word of this scratch is not
- * visible to the caller: device-side errors of this entry point go
- * unreported (host-side errors are returned as usual).
+ * (once per device, with that device current) and keeps it for the life of
+ * the process; make that first call before any stream capture.  A
+ * cudaDeviceReset of a device that has used this entry point leaves that
+ * address stale: do not reset such a device while the library is loaded.
+ * Every call shares the one array, which keeps the last call's contents
+ * (each call clears the status word it needs): calls whose work overlaps on
+ * the GPU (other streams, other threads) race on it and must be serialised
+ * by the caller.  Device-side errors (a pipeline wait that timed out) are
+ * recorded in the array's status word; read them with
+ * i8lt_noalloc_read_device_status.
  */
 #define I8LT_NOALLOC_SCRATCH_BYTES (32u << 20)
 int i8lt_backward_input_noalloc(const void* G, int gt, int64_t M, int64_t N,
                                 const int8_t* CB, const float* SCB, int64_t K,
                                 const void* addend, void* grad_A,
                                 void* grad_bias, int bt, void* stream);
+/* Synchronizes `stream`, then reads the status word of the no-alloc scratch
+ * on the current device (the result of the last i8lt_backward_input_noalloc
+ * call there) into *status (may be NULL) and clears a recorded error, like
+ * i8lt_read_device_status does for a workspace.  Allocates nothing (one
+ * small device-to-host copy into this function's own stack).  Returns
+ * I8LT_OK or the status the device recorded. */
+int i8lt_noalloc_read_device_status(int32_t* status, void* stream);
 
 /*
  * Weight gradient of the trainable-weight mode (bitsandbytes'

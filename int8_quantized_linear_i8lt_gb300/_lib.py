@@ -83,6 +83,7 @@ SIGNATURES = {
                                     c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
     "i8lt_backward_input_noalloc": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64,
                                             c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
+    "i8lt_noalloc_read_device_status": (c_int, [POINTER(c_int32), c_void_p]),
     "i8lt_nf4_levels": (c_int, [POINTER(c_float)]),
     "i8lt_nf4_row_bytes": (c_int64, [c_int64]),
     "i8lt_nf4_blocks": (c_int64, [c_int64]),
@@ -219,6 +220,13 @@ def i8lt_backward_input(G, gt, M, N, CB, SCB, K, addend, grad_A, grad_bias, bt, 
 def i8lt_backward_input_noalloc(G, gt, M, N, CB, SCB, K, addend, grad_A, grad_bias, bt, stream=None) -> int:
     return load().i8lt_backward_input_noalloc(_p(G), gt, M, N, _p(CB), _p(SCB), K, _p(addend), _p(grad_A),
                                               _p(grad_bias), bt, _p(stream))
+
+
+def i8lt_noalloc_read_device_status(stream=None):
+    """-> (return code, status word) of the no-alloc scratch on the current device."""
+    st = c_int32(0)
+    r = load().i8lt_noalloc_read_device_status(ctypes.byref(st), _p(stream))
+    return r, int(st.value)
 
 
 def i8lt_nf4_levels():

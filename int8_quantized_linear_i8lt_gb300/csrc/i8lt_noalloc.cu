@@ -21,7 +21,8 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  The host-side
 // symbol is only a stand-in: the address comes from the runtime, once per
-// device, with that device current.
+// device, with that device current, and is kept for the life of the process
+// (a cudaDeviceReset would invalidate it; the header says so).
 int scratch_on_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return I8LT_ERR_CUDA;
@@ -50,4 +51,11 @@ extern "C" int i8lt_backward_input_noalloc(const void* G, int gt, int64_t M, int
   if (int st = scratch_on_current_device(&scratch)) return st;
   return i8lt_backward_input(G, gt, M, N, CB, SCB, K, addend, grad_A, grad_bias, bt, scratch,
                              kNoAllocScratchBytes, stream);
+}
+
+extern "C" int i8lt_noalloc_read_device_status(int32_t* status, void* stream) {
+  void* scratch = nullptr;
+  if (int st = scratch_on_current_device(&scratch)) return st;
+  // the status word sits at the start of the scratch, as in every workspace
+  return i8lt_read_device_status(scratch, status, nullptr, stream);
 }

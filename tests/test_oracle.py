@@ -294,14 +294,27 @@ def test_forward_lossless_exact(outliers, dtype):
         assert np.array_equal(r["Aq"], case["qa"].numpy().astype(np.int8))
 
 
-def test_forward_residual_is_added_once():
-    M, K, N = 8, 32, 8
-    case = W.lossless_case(M, K, N, seed=12)
+@pytest.mark.parametrize("dtype", [O.F16, O.BF16, O.F32])
+def test_forward_lossless_with_residual_exact(dtype):
+    """Lossless case plus a residual and a bias on the grid (the tiny MLP's
+    "+ x" goes through the residual): the output must be the fp64 product of
+    the grid values plus both, rounded once.  The expected value comes from a
+    float64 matmul of the grid values, not from the oracle's formula."""
+    M, K, N = 12, 40, 10
+    case = W.lossless_case(M, K, N, seed=12, outlier_cols=(5,), threshold=6.0)
+    A64 = case["A"].double().numpy()
+    W64 = case["W"].double().numpy()
+    res64 = W.grid_values((M, N), 255, -6, 99).numpy()
+    bias64 = W.grid_values((N,), 127, -7, 98).numpy()
     CB, SCB = O.quantize_weight(case["W"].numpy(), O.F16)
-    res = (np.arange(M * N).reshape(M, N) / 32.0).astype(np.float16)
-    r0 = O.forward(case["A"].numpy(), O.F16, CB, SCB, threshold=math.inf)
-    r1 = O.forward(case["A"].numpy(), O.F16, CB, SCB, threshold=math.inf, residual=res)
-    assert np.array_equal(r1["out64"], r0["out64"] + res.astype(np.float64))
+    A_in, res_in, b_in = O.round_to(A64, dtype), O.round_to(res64, dtype), O.round_to(bias64, dtype)
+    assert np.array_equal(O.widen(res_in, dtype), res64) and np.array_equal(O.widen(b_in, dtype), bias64)
+    r = O.forward(A_in, dtype, CB, SCB, b_in, dtype, threshold=6.0, residual=res_in)
+    exact = A64 @ W64.T + bias64[None, :] + res64
+    assert np.array_equal(r["out64"], exact)
+    assert np.array_equal(r["out"], O.round_to(exact, dtype))
+    # a residual added twice, or dropped, is caught
+    assert not np.array_equal(r["out64"], exact + res64) and not np.array_equal(r["out64"], exact - res64)
 
 
 def test_forward_reconstruction_bound():
@@ -392,6 +405,26 @@ def test_silu_closed_forms():
     assert g[0] == 0.5                                  # silu'(0) = 1/2
     sg = 1 / (1 + math.exp(-1))
     assert g[1] == f32(sg * (1 + 1 * (1 - sg)))
+
+
+def test_silu_backward_matches_a_numerical_derivative():
+    """silu_backward(g, h) = g * d/dh silu(h), checked against a central
+    difference of x / (1 + e^-x) in float64 (step 1e-5: truncation and
+    rounding errors near 1e-10) at 400 points in [-30, 30] and random g; the
+    oracle's result is rounded once to fp32."""
+    rng = np.random.default_rng(5)
+    h = np.concatenate([np.linspace(-30, 30, 397), [0.0, 1e-3, -1e-3]]).astype(np.float32)
+    g = rng.uniform(-4, 4, h.shape).astype(np.float32)
+    got = O.silu_backward(g, h, O.F32).astype(np.float64)
+    x = h.astype(np.float64)
+    sl = lambda t: t / (1.0 + np.exp(-t))  # noqa: E731
+    d = (sl(x + 1e-5) - sl(x - 1e-5)) / 2e-5
+    want = g.astype(np.float64) * d
+    assert np.all(np.abs(got - want) <= 2e-7 * np.abs(want) + 1e-9)
+    # the derivative runs from 0 (far left) through 1/2 (at 0) to 1 (far right)
+    # and overshoots 1 near x = 2.4; a sign or term slip moves these values
+    one = O.silu_backward(np.ones_like(h), h, O.F32).astype(np.float64)
+    assert abs(one[0]) < 1e-10 and abs(one[-4] - 1.0) < 1e-6 and one.max() > 1.09
 
 
 def _page_tiny_mlp_deviation():

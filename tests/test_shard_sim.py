@@ -96,3 +96,52 @@ def test_column_absmax_merge_is_the_whole_batch_reduction():
     assert np.array_equal(O.outlier_columns_from_absmax(merged, 6.0), O.outlier_columns(A16, 6.0))
     assert len(O.outlier_columns_from_absmax(merged, float("inf"))) == 0
     assert np.array_equal(O.column_absmax(A16[:0]), np.zeros(K))
+
+
+def _fp16_magnitude_bits(colmax64):
+    """The library's colmax format: per column the fp16 bit pattern of the
+    magnitude (sign cleared), held as int32; integer order = magnitude order."""
+    return torch.from_numpy(colmax64.astype(np.float16).view(np.uint16).astype(np.int32))
+
+
+def _hook_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    import oracle as O
+    from int8_quantized_linear_i8lt_gb300 import functional as F
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        A, _, _, _ = _inputs()
+        rows = slice(rank * M // world, (rank + 1) * M // world)
+        local = _fp16_magnitude_bits(O.column_absmax(O.cast_f16(A[rows], O.F16)))
+        t = local.clone()
+        F.allreduce_colmax()(t)            # the product's merge hook, in place
+        q.put((rank, local.numpy(), t.numpy()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_allreduce_colmax_hook_on_two_gloo_ranks():
+    """functional.allreduce_colmax, the exchange step of the token-sharded
+    forward, run by two gloo ranks on the column maxima of their rows in the
+    library's format: every rank ends with the element-wise maximum, which
+    is the whole batch's column maxima, and the outlier set read from it is
+    the whole batch's."""
+    import oracle as O
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_hook_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted((q.get(timeout=120) for _ in range(2)), key=lambda t: t[0])
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    A, _, _, _ = _inputs()
+    whole = _fp16_magnitude_bits(O.column_absmax(O.cast_f16(A, O.F16))).numpy()
+    (_, l0, m0), (_, l1, m1) = res
+    assert np.array_equal(m0, np.maximum(l0, l1)) and np.array_equal(m1, m0)
+    assert np.array_equal(m0, whole)
+    assert not np.array_equal(l0, whole)          # rank 0's rows alone miss the planted outlier
+    mags = m0.astype(np.uint16).view(np.float16).astype(np.float64)
+    assert np.array_equal(O.outlier_columns_from_absmax(mags, 6.0), O.outlier_columns(O.cast_f16(A, O.F16), 6.0))

@@ -161,7 +161,7 @@ def layer_input(wl: Workload, li: int, seed: int, device="cpu"):
     return activation(spec, seed + li * OFF_LAYER2, device)
 
 
-def lossless_case(M, K, N, seed, outlier_cols=(), threshold=6.0):
+def lossless_case(M, K, N, seed, outlier_cols=(), threshold=6.0, ea_range=(-9, -4), ew_range=(-12, -7)):
     """Inputs on the quantization grid, for an exact check of the method.
 
     A[m, k] = qa[m, k] * ua[m], W[n, k] = qw[n, k] * uw[n] with integer codes
@@ -170,6 +170,7 @@ def lossless_case(M, K, N, seed, outlier_cols=(), threshold=6.0):
     dequantization is exact, so the layer must reproduce the fp64 product.
     ``outlier_cols`` get values of magnitude above ``threshold`` (these leave
     the int8 part and go through the fp16 outlier product).
+    ``ea_range`` / ``ew_range``: half-open ranges of the exponents of ua / uw.
 
     Returned as fp16 tensors: (A, W) plus the codes and steps.
     """
@@ -182,8 +183,8 @@ def lossless_case(M, K, N, seed, outlier_cols=(), threshold=6.0):
         qa[r, keep[int(torch.randint(len(keep), (1,), generator=g))]] = 127 * (1 if r % 2 else -1)
     for r in range(N):
         qw[r, int(torch.randint(K, (1,), generator=g))] = -127 if r % 3 else 127
-    ea = torch.randint(-9, -4, (M,), generator=g)       # steps 2^-9 .. 2^-5
-    ew = torch.randint(-12, -7, (N,), generator=g)
+    ea = torch.randint(ea_range[0], ea_range[1], (M,), generator=g)    # default steps 2^-9 .. 2^-5
+    ew = torch.randint(ew_range[0], ew_range[1], (N,), generator=g)    # default 2^-12 .. 2^-8
     ua = torch.pow(2.0, ea.double())
     uw = torch.pow(2.0, ew.double())
     A = qa.double() * ua[:, None]
@@ -196,3 +197,11 @@ def lossless_case(M, K, N, seed, outlier_cols=(), threshold=6.0):
         # most rows must keep their absmax (127*ua) outside column k: it is
         # already planted in ``keep``
     return dict(A=A.half(), W=W.half(), qa=qa, qw=qw, ua=ua, uw=uw)
+
+
+def grid_values(shape, qmax, step_exp, seed) -> torch.Tensor:
+    """Integers uniform in [-qmax, qmax] times 2**step_exp (float64): values
+    that fp16 and bf16 hold exactly while qmax < 256, for inputs whose every
+    sum the exact checks can predict."""
+    q = torch.randint(-qmax, qmax + 1, tuple(shape), generator=_gen(seed))
+    return q.double() * (2.0 ** step_exp)
