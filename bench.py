@@ -467,11 +467,14 @@ def _layer_of(i, layers, materialized=False):
 def launches_per_layer(L, materialized=False) -> int:
     """Our kernels per layer and step: colmax, outlier index (outliers on),
     row quantize, subB (outliers on), weight-code widening, accumulation
-    plan, forward GEMM; grad_output prepass, grad_bias finalize, (weight
-    dequantization when materialized,) backward GEMM."""
+    plan, forward GEMM; then (weight dequantization when materialized,) the
+    backward GEMM and the grad_bias finalize -- with a grad_output prepass
+    first when G is not fp16 with N a multiple of 8 (the GEMM reads fp16 G
+    as it is and reduces grad_bias from it itself)."""
     import math
     fwd = 7 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 4
-    return fwd + (4 if materialized else 3)
+    prepass = 0 if (L.spec.dtype == torch.float16 and L.spec.N % 8 == 0) else 1
+    return fwd + 2 + prepass + (1 if materialized else 0)
 
 
 def time_trainable(layers, stream, steps, device):

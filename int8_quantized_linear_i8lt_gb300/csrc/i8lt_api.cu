@@ -447,10 +447,15 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_
   const bool g16_needed = grad_A != nullptr && M > 0 && needs_g16(N, gt);
   __half* G16 = g16_needed ? reinterpret_cast<__half*>(w + L.g16) : nullptr;
   const bool vec = (N % 8) == 0;
+  // fp16 G that the GEMM reads as it is: grad_bias is reduced inside the
+  // GEMM (its epilogue warps, from the uncast G) and no pass of its own
+  // reads G; otherwise the prepass casts G and sums it in the same order
+  const bool bias_in_gemm = grad_bias != nullptr && grad_A != nullptr && M > 0 && !g16_needed;
   if (cudaMemsetAsync(st, 0, sizeof(DevStatus), s) != cudaSuccess) return I8LT_ERR_CUDA;
 
-  if (grad_bias != nullptr || G16 != nullptr) {
-    if (launch_gradout_prepass(G, gt, M, N, vec, G16, L.n_pad, grad_bias, bt, partial, L.chunks, s) != cudaSuccess)
+  if ((grad_bias != nullptr && !bias_in_gemm) || G16 != nullptr) {
+    if (launch_gradout_prepass(G, gt, M, N, vec, G16, L.n_pad, bias_in_gemm ? nullptr : grad_bias, bt, partial,
+                               L.chunks, s) != cudaSuccess)
       return I8LT_ERR_CUDA;
   }
   if (grad_A == nullptr || M == 0) return I8LT_OK;
@@ -483,7 +488,14 @@ int i8lt_backward_input(const void* G, int gt, int64_t M, int64_t N, const int8_
   ea.grad_A = grad_A;
   ea.dt = gt;
   ea.st = st;
-  return cuda_status(launch_bwd_gemm(g, ea, !materialize, s));
+  if (bias_in_gemm) {
+    ea.gsum = G;
+    ea.gsum_dt = gt;
+    ea.partial = partial;
+  }
+  if (launch_bwd_gemm(g, ea, !materialize, s) != cudaSuccess) return I8LT_ERR_CUDA;
+  if (bias_in_gemm) return cuda_status(launch_grad_bias_finalize(partial, M, N, grad_bias, bt, s));
+  return I8LT_OK;
 }
 
 size_t i8lt_grad_weight_workspace_size(int64_t M, int64_t N, int64_t K) {

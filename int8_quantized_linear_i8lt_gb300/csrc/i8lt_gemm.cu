@@ -739,6 +739,56 @@ __device__ __forceinline__ void nf4x16_decode(uint2 v, uint64_t am2, const float
   o1 = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// grad_bias partial sums of one kBiasChunkRows-row chunk c of G over the 64
+// columns [n0, n0 + 64), by one warp, read from global memory (G is constant
+// during the GEMM, so no stage of the pipeline is involved):
+//   partial[c, n] = sum_{y=0..7} ( sum_{j=0..15} G[128 c + y + 8 j, n] ),
+// each inner sum in increasing j from 0.f, the outer one in increasing y
+// from 0.f -- the order of the grad_output prepass, so both give the same
+// bits.  Lane (cg, yy) = (lane & 7, lane >> 3) loads 8 columns (16 bytes) of
+// the rows of the two lanes y = yy and yy + 4; lanes cg then gather the
+// eight sums in order with shuffles.  Rows past M add nothing; N is a
+// multiple of 8, so a 16-byte group is all inside or all past N.
+template <typename T>
+__device__ __forceinline__ void bias_chunk_sums(const T* __restrict__ G, int M, int N, int c, int n0,
+                                                float* __restrict__ partial, int lane) {
+  const int cg = lane & 7, yy = lane >> 3;
+  const int n = n0 + cg * 8;
+  const bool col_ok = n < N;
+  float p[2][8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p[h][i] = 0.f;
+  const int64_t r0 = static_cast<int64_t>(c) * kBiasChunkRows;
+#pragma unroll 4
+  for (int j = 0; j < kBiasChunkRows / 8; ++j) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t r = r0 + yy + 4 * h + 8 * j;
+      if (col_ok && r < M) {
+        float f[8];
+        load8_float(G + r * N + n, 8, true, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[h][i] += f[i];
+      }
+    }
+  }
+  float out[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float acc = 0.f;
+#pragma unroll
+    for (int y = 0; y < 8; ++y) acc += __shfl_sync(0xffffffffu, p[y >> 2][i], cg + 8 * (y & 3));
+    out[i] = acc;
+  }
+  if (yy == 0 && col_ok) {
+    float* dst = partial + static_cast<int64_t>(c) * N + n;
+    reinterpret_cast<float4*>(dst)[0] = make_float4(out[0], out[1], out[2], out[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(out[4], out[5], out[6], out[7]);
+  }
+}
+
 // Fused modes: the A operand (the dequantized weight tile) is rebuilt per
 // stage from the int8 or 4-bit weight tiles by the converter warps;
 // kModeMat: it is loaded by TMA from the materialized WdqT (K-major, like
@@ -1096,11 +1146,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     const int col0 = warp >= kBwdWarpEpi1 ? kHalf : 0;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t acc_empty_pair[2] = {mapa_shared(&bars->acc_empty[0], 0), mapa_shared(&bars->acc_empty[1], 0)};
+    const int ew = (warp >= kBwdWarpEpi1 ? 4 : 0) + quad;   // epilogue warp 0..7
     int tl = 0;
     for (int t = cid; t < num_tiles; t += ncl, ++tl) {
       int tm, tk;
       tile_coords(t, num_m, num_k, group, tm, tk);
       const int buf = tl % Geo::kAccBufs;
+      if (e.partial != nullptr) {
+        // while the tensor cores run this tile: the grad_bias partial sums of
+        // the reduction blocks b = tk, tk + num_k, ... over this CTA's token
+        // chunks of the tile (every (chunk, block) is owned by exactly one
+        // tile), one (chunk, block) item per warp in turn
+        int item = 0;
+        for (int b = tk; b < NB; b += num_k) {
+#pragma unroll
+          for (int u = 0; u < Geo::kSub; ++u, ++item) {
+            const int c = (tm * Geo::kTileTokens + u * kPairN) / kBiasChunkRows + static_cast<int>(rank);
+            if (item % kBwdEpiWarps != ew || c * kBiasChunkRows >= e.M) continue;
+            if (e.gsum_dt == DT_BF16)
+              bias_chunk_sums(static_cast<const __nv_bfloat16*>(e.gsum), e.M, e.N, c, b * kBK, e.partial, lane);
+            else
+              bias_chunk_sums(static_cast<const __half*>(e.gsum), e.M, e.N, c, b * kBK, e.partial, lane);
+          }
+        }
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->acc_full[buf], (tl / Geo::kAccBufs) & 1, abort_flag, e.st,
                                              kWhereEpi, kEpiSleepNs)))
         break;

@@ -50,11 +50,20 @@ cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int
 cudaError_t launch_build_subB(const int8_t* CB, int64_t ld, const float* SCB, int64_t N, const int* idx,
                               const DevStatus* st, int64_t cap_pad, __half* subB, cudaStream_t s);
 
+// grad_bias is reduced in chunks of this many rows of G: partial[c, n] = the
+// sum of G[m, n] over the rows m of chunk c (128 c <= m < 128 c + 128), in a
+// fixed order that every kernel producing partial sums follows; then
+// grad_bias[n] = sum over c, in order.
+constexpr int kBiasChunkRows = 128;
+
 // K7: grad_bias partial sums of the uncast G and (optionally) G16 = fp16(G)
-// with N padded to N_pad.
+// with N padded to N_pad; then the finalize (when grad_bias is given).
 cudaError_t launch_gradout_prepass(const void* G, int gt, int64_t M, int64_t N, bool vec, __half* G16,
                                    int64_t N_pad, void* grad_bias, int bt, float* partial,
                                    int64_t max_chunks, cudaStream_t s);
+// grad_bias[n] = sum over the chunks c (in order) of partial[c, n].
+cudaError_t launch_grad_bias_finalize(const float* partial, int64_t M, int64_t N, void* grad_bias, int bt,
+                                      cudaStream_t s);
 int64_t gradout_partial_chunks(int64_t M);
 
 cudaError_t launch_silu(const void* h, int dt, int64_t n, bool vec, void* out, cudaStream_t s);
@@ -145,6 +154,14 @@ struct BwdEpiArgs {
   const float* absmax;   // 4-bit: [weight rows, nblk] per-64-element scales
   int nblk;
   float lv[16];          // 4-bit: the code levels
+  // grad_bias reduced inside the GEMM (the uncast X = G of the input-gradient
+  // modes, row-major [M, N], N a multiple of 8, 16-byte aligned), or NULL:
+  // the epilogue warps write partial[c, n] (kBiasChunkRows-row chunks c of
+  // the tokens) for the 64-wide blocks n of the reduction that their tile
+  // owns (block b belongs to the output tile row b % num_k)
+  const void* gsum;
+  int gsum_dt;           // DT_F16 or DT_BF16
+  float* partial;        // [ceil(M / kBiasChunkRows), N]
 };
 
 // fused: the dequantized weight is rebuilt in shared memory from CB (tmW);

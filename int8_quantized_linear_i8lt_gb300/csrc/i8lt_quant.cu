@@ -358,10 +358,15 @@ __global__ void __launch_bounds__(kThreads) build_subB_kernel(const int8_t* __re
 
 // ---------------------------------------------------------------------------
 // K7: grad_output prepass.  Column sums of the uncast G in fp32 per chunk of
-// kSumRows rows (deterministic order), optional G16 = fp16_rn(G) padded to
-// N_pad columns.  Then a finalize kernel sums the chunks in order.
+// kBiasChunkRows = 128 rows, optional G16 = fp16_rn(G) padded to N_pad
+// columns.  Within a chunk the order is fixed: eight row lanes y = 0..7 each
+// sum the rows y, y + 8, ..., y + 120 in increasing order, then the eight
+// lane sums are added in the order y = 0..7 -- the same order as the
+// backward GEMM's own grad_bias reduction (bias_chunk_sums in
+// i8lt_gemm.cu), so that every path gives the same bits.  A finalize
+// kernel then sums the chunks in order.
 // ---------------------------------------------------------------------------
-constexpr int kSumRows = 512;
+constexpr int kSumRows = kBiasChunkRows;
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) gradout_prepass_kernel(const T* __restrict__ G, int64_t M, int64_t N,
@@ -910,7 +915,14 @@ cudaError_t launch_gradout_prepass(const void* G, int gt, int64_t M, int64_t N, 
     if (e != cudaSuccess) return e;
   }
   if (grad_bias == nullptr || N == 0) return cudaSuccess;
+  return launch_grad_bias_finalize(partial, M, N, grad_bias, bt, s);
+}
+
+cudaError_t launch_grad_bias_finalize(const float* partial, int64_t M, int64_t N, void* grad_bias, int bt,
+                                      cudaStream_t s) {
+  if (grad_bias == nullptr || N == 0) return cudaSuccess;
   if (M == 0) return cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(N) * (bt == DT_F32 ? 4 : 2), s);
+  const int64_t chunks = gradout_partial_chunks(M);
   const int blocks = static_cast<int>(std::min<int64_t>(ceil_div(N, kThreads), 152 * 4));
   return dispatch_dt(bt, [&](auto* tag) {
     using BT = std::remove_pointer_t<decltype(tag)>;

@@ -84,9 +84,10 @@ def gpu_forward(A, CB, SCB, K, bias=None, threshold=6.0, residual=None, max_outl
     return res
 
 
-def check_forward_stages(g, ref, rows=None, K=None):
+def check_forward_stages(g, ref, rows=None, K=None, out_tol=True):
     """Bit-exact integer stages + tolerance on the output.  ``rows``: the
-    GPU rows the oracle result ``ref`` covers (None: all)."""
+    GPU rows the oracle result ``ref`` covers (None: all).  ``out_tol``
+    False: the caller checks the output itself (bit for bit)."""
     sel = (lambda t: t) if rows is None else (lambda t: t[rows])
     idx = ref["idx"]
     assert g["status"] == 0, _lib.i8lt_status_string(g["status"])
@@ -102,6 +103,8 @@ def check_forward_stages(g, ref, rows=None, K=None):
     assert np.array_equal(aq[:, :Kq], ref["Aq"].astype(np.float32)), "int8 codes differ"
     assert not np.any(aq[:, Kq:]), "padding codes not zero"
     assert np.array_equal(to_np(sel(g["acc"])), ref["Cacc"]), "int32 accumulator differs"
+    if not out_tol:
+        return None
     out = widen(sel(g["out"]))
     return assert_tol(out, ref["out64"], "out")
 

@@ -423,3 +423,37 @@ def test_fused_silu_epilogue_matches_the_unfused_chain(M, K, H, N2, dtype, thr):
     assert torch.equal(colmax, F.colmax_region(ws_chk, M, H, N2, thr))
     y, _ = I.forward(a, CB2, SCB2, H, b2, thr, ws=ws2, colmax_ready=True)
     assert torch.equal(y.view(torch.uint8), y_ref.view(torch.uint8))
+
+
+@pytest.mark.parametrize("M,K,N", [(300, 1100, 520),      # ragged chunks of 128 tokens, ragged 64-wide blocks
+                                   (1000, 256, 4104),     # one output row tile: every block owned by it
+                                   (129, 9000, 200),      # more row tiles than reduction blocks
+                                   (2048, 4096, 4096)])   # the fp16 single-layer workload's shape
+def test_grad_bias_in_gemm_equals_the_prepass(M, K, N):
+    """fp16 grad_output: the backward GEMM reduces grad_bias itself (its
+    epilogue warps sum the uncast G in 128-token chunks while the tensor
+    cores run) and no prepass reads G.  Both schedules must give the bits
+    of the prepass path (taken when grad_A is not requested), which sums in
+    the same order, and the result must match the oracle."""
+    spec = W.LayerSpec(M, K, N, torch.float16, 0.02, 0.01)
+    A, Wf, b, G = _layer(spec, 61)
+    Gd = G.to(DEV)
+    CB, SCB = I.quantize_weight(Wf.to(DEV))
+    _lib.i8lt_profile_start(64)
+    gA_f, gb_f = I.backward_input(Gd, CB, SCB, K, bias_dtype=torch.float32, fused=True)
+    torch.cuda.synchronize()
+    _, recs, _ = _lib.i8lt_profile_stop(64)
+    names = [n for n, _ in recs]
+    assert "gradout_prepass" not in names and names == ["bwd_gemm", "grad_bias_finalize"], names
+    _, gb_m = I.backward_input(Gd, CB, SCB, K, bias_dtype=torch.float32, fused=False)
+    _lib.i8lt_profile_start(64)
+    _, gb_p = I.backward_input(Gd, CB, SCB, K, need_grad_A=False, bias_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _, recs, _ = _lib.i8lt_profile_stop(64)
+    assert [n for n, _ in recs] == ["gradout_prepass", "grad_bias_finalize"]
+    assert torch.equal(gb_f.view(torch.int32), gb_p.view(torch.int32)), "in-GEMM grad_bias differs from the prepass"
+    assert torch.equal(gb_m.view(torch.int32), gb_p.view(torch.int32))
+    Gn = to_np(G)
+    assert_tol(widen(gb_f), O.widen(Gn, O.F16).sum(0), "grad_bias")
+    # fp32 sums of fp16 values in 128-row chunks: far inside the tolerance
+    assert np.abs(widen(gb_f) - O.widen(Gn, O.F16).sum(0)).max() < 1e-3
