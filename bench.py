@@ -383,8 +383,10 @@ def run_ours(args):
     alt = time_schedule(layers, stream, max(2, min(args.steps, 10)), device, not mat)
     # --- the step replayed from a CUDA graph (context, not the headline)
     graph = time_graph(layers, max(3, min(args.steps, 20)), device)
-    # --- the 4-bit NormalFloat weight-only layers (another workload: context, not the headline)
+    # --- the 4-bit weight-only layers (another workload: context, not the headline); FP4 runs the
+    # same matmul kernels with another level table
     nf4 = time_nf4(stream, max(2, min(args.steps, 10)), device)
+    fp4 = time_nf4(stream, max(2, min(args.steps, 10)), device, fmt="fp4", materialized_too=False)
 
     clocks = clk.summary()
     line = {
@@ -411,6 +413,7 @@ def run_ours(args):
         ("bwd_fused" if mat else "bwd_materialized"): alt,
         "cuda_graph": graph,
         "nf4_weight_only": nf4,
+        "fp4_weight_only": fp4,
         "gpu_launches": n_launches,
         "gemm_launch": {k: dict(zip(("status", "ctas", "threads", "smem"), _lib.i8lt_gemm_launch_info(k)))
                         for k in ("fwd_gemm", "bwd_gemm")},
@@ -528,7 +531,7 @@ def time_trainable(layers, stream, steps, device):
             "col_quantize_ms_per_step": round(cq_ms / steps, 4), "quantize_weight_ms_per_step": round(qw_ms / steps, 4)}
 
 
-def time_nf4(stream, steps, device, warmup=3):
+def time_nf4(stream, steps, device, warmup=3, fmt="nf4", materialized_too=True):
     """The 4-bit NormalFloat weight-only layers (QLoRA fine-tuning: frozen
     NF4 weights, bf16 compute) of the qlora_mlp_7b_nf4 workload: per layer
     and step the forward and the input gradient, each a tensor-core matmul
@@ -540,28 +543,30 @@ def time_nf4(stream, steps, device, warmup=3):
     from int8_quantized_linear_i8lt_gb300.functional import DTYPE_CODE
     wl = W.NF4_WORKLOADS["qlora_mlp_7b_nf4"]
     sp = stream.cuda_stream
+    fwd_fn = getattr(_lib, f"i8lt_{fmt}_forward")
+    bwd_fn = getattr(_lib, f"i8lt_{fmt}_backward_input")
     ws = torch.empty(_lib.i8lt_nf4_workspace_size(), dtype=torch.uint8, device=device)
     lay = []
     for li, spec in enumerate(wl.layers):
         Wf, _, G = W.layer_tensors(wl, li, 4321, device)
         A = W.layer_input(wl, li, 4321, device)
-        packed, absmax = I.nf4_quantize(Wf)
+        packed, absmax = I.quantize_4bit(Wf, fmt)
         out = torch.empty(spec.M, spec.N, dtype=spec.dtype, device=device)
         gA = torch.empty(spec.M, spec.K, dtype=spec.dtype, device=device)
         lay.append((spec, A, G, packed, absmax, out, gA))
         del Wf
 
     ws_dq = torch.empty(max(_lib.i8lt_nf4_workspace_size_dq(s_.K, s_.N) for s_ in wl.layers), dtype=torch.uint8,
-                        device=device)
+                        device=device) if materialized_too else None
 
     def step(w):
         for spec, A, G, packed, absmax, out, gA in lay:
             dt = DTYPE_CODE[spec.dtype]
-            st = _lib.i8lt_nf4_forward(A.data_ptr(), dt, spec.M, spec.K, packed.data_ptr(), absmax.data_ptr(), spec.N,
-                                       None, 0, out.data_ptr(), w.data_ptr(), w.numel(), sp)
+            st = fwd_fn(A.data_ptr(), dt, spec.M, spec.K, packed.data_ptr(), absmax.data_ptr(), spec.N,
+                        None, 0, out.data_ptr(), w.data_ptr(), w.numel(), sp)
             assert st == 0, _lib.i8lt_status_string(st)
-            st = _lib.i8lt_nf4_backward_input(G.data_ptr(), dt, spec.M, spec.N, packed.data_ptr(), absmax.data_ptr(),
-                                              spec.K, gA.data_ptr(), w.data_ptr(), w.numel(), sp)
+            st = bwd_fn(G.data_ptr(), dt, spec.M, spec.N, packed.data_ptr(), absmax.data_ptr(),
+                        spec.K, gA.data_ptr(), None, 0, w.data_ptr(), w.numel(), sp)
             assert st == 0, _lib.i8lt_status_string(st)
 
     def timed(w):
@@ -579,12 +584,12 @@ def time_nf4(stream, steps, device, warmup=3):
         return reduce_max(e0.elapsed_time(e1), device), r, n
 
     ms, recs, n_launches = timed(ws)          # fused: the weight decoded inside the GEMM
-    ms_dq, recs_dq, _ = timed(ws_dq)          # materialized: dequantized weight in the workspace
     flops = sum(4.0 * spec.M * spec.N * spec.K for spec, *_ in lay) * steps
     half = flops / 2
     peaks, src = load_peaks()
     peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    res = {"workload": wl.name, "layers": [[s.M, s.K, s.N, str(s.dtype).replace("torch.", "")] for s in wl.layers],
+    res = {"workload": wl.name, "format": fmt,
+           "layers": [[s.M, s.K, s.N, str(s.dtype).replace("torch.", "")] for s in wl.layers],
            "value": round(reduce_sum(flops, device) / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
            "ms_per_step": round(ms / steps, 4), "steps": steps, "gpu_launches": n_launches}
     for name in ("nf4_gemm_fwd", "nf4_gemm_bwd"):
@@ -593,15 +598,17 @@ def time_nf4(stream, steps, device, warmup=3):
             tf = half / (k_ms * 1e-3) / 1e12
             res[name] = {"tflops": round(tf, 1), "frac_tensor": round(tf / peak_t, 4),
                          "ms_per_launch": round(k_ms / (steps * len(lay)), 4)}
-    res["materialized"] = {"value": round(reduce_sum(flops, device) / (ms_dq * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
-                           "ms_per_step": round(ms_dq / steps, 4),
-                           "dequantize_ms_per_step": round(sum(t for n, t in recs_dq if n == "nf4_dequantize") / steps,
-                                                           4)}
-    for name in ("nf4_gemm_fwd", "nf4_gemm_bwd"):
-        k_ms = sum(t for n, t in recs_dq if n == name)
-        if k_ms:
-            tf = half / (k_ms * 1e-3) / 1e12
-            res["materialized"][name] = {"tflops": round(tf, 1), "frac_tensor": round(tf / peak_t, 4)}
+    if materialized_too:
+        ms_dq, recs_dq, _ = timed(ws_dq)      # materialized: dequantized weight in the workspace
+        res["materialized"] = {"value": round(reduce_sum(flops, device) / (ms_dq * 1e-3) / 1e12, 1),
+                               "unit": "TFLOP/s", "ms_per_step": round(ms_dq / steps, 4),
+                               "dequantize_ms_per_step": round(sum(t for n, t in recs_dq if n == "nf4_dequantize")
+                                                               / steps, 4)}
+        for name in ("nf4_gemm_fwd", "nf4_gemm_bwd"):
+            k_ms = sum(t for n, t in recs_dq if n == name)
+            if k_ms:
+                tf = half / (k_ms * 1e-3) / 1e12
+                res["materialized"][name] = {"tflops": round(tf, 1), "frac_tensor": round(tf / peak_t, 4)}
     res["peak"] = peak_t
     res["peak_source"] = f"{src} bf16 sustained"
     return res

@@ -18,7 +18,7 @@
  *     conversation, "grad_bias is now computed on natural grad_output").
  * Beside it: the MLP's SiLU (with an optional fusion into the forward
  * epilogue), a token-sharded forward, the weight gradient of the
- * trainable-weight mode, the 4-bit NormalFloat weight-only layer of QLoRA
+ * trainable-weight mode, the 4-bit (NF4 and FP4) weight-only layers of QLoRA
  * fine-tuning, an entry point that allocates nothing, per-launch timing and
  * a diagnostic of the bounded waits (each documented below).
  *
@@ -67,7 +67,8 @@ typedef enum { I8LT_F16 = 0, I8LT_BF16 = 1, I8LT_F32 = 2 } i8lt_dtype;
 /* Largest in_features for which K * 127 * 127 < 2^31 (exact int32 sums). */
 #define I8LT_MAX_K 133144
 
-/* Version of this ABI; bumped on any incompatible change. */
+/* Version of this ABI; bumped on any incompatible change (3: the 4-bit
+ * input gradients take grad_bias). */
 int i8lt_abi_version(void);
 
 /* Human-readable name of a status code (static storage). */
@@ -316,30 +317,44 @@ int i8lt_grad_weight(const void* G, int gt, const void* A, int at,
                      void* grad_W, int wt, void* ws, size_t ws_bytes, void* stream);
 
 /*
- * 4-bit NormalFloat (NF4) weight-only layer: QLoRA fine-tuning keeps the
- * frozen base weights in 4 bits and runs every matmul in the 16-bit compute
- * dtype ("Support QLoRA 4-bit finetuning with bitsandbytes", lit-gpt PR #275:
- * the bnb.nf4 quantize option, Llama-2-7B runs with --precision bf16-true).
- * The page does not define the format; the library follows QLoRA's published
- * 4-bit NormalFloat construction:
- *   levels   16 fp32 values from -1 to 1 with an exact 0 (index 7): 7 negated
+ * 4-bit weight-only layers: QLoRA fine-tuning keeps the frozen base weights
+ * in 4 bits and runs every matmul in the 16-bit compute dtype ("Support
+ * QLoRA 4-bit finetuning with bitsandbytes", lit-gpt PR #275: the bnb.nf4
+ * and bnb.fp4 quantize options, Llama-2-7B runs with --precision
+ * bf16-true).  The page names both formats without defining them.  Both
+ * share one storage:
+ *   blocks   64 consecutive elements of a weight row share one fp32 absmax;
+ *   packing  row n of `packed` holds i8lt_nf4_row_bytes(K) bytes, two codes
+ *            per byte, element 2j in the high nibble of byte j; padding and
+ *            all-zero blocks hold the zero code;
+ *   dequantization  Wdq[n, k] = rn(levels[code] * absmax[n, k / 64]), one
+ *            fp32 multiply rounded once to the compute dtype.
+ * NF4 follows QLoRA's published 4-bit NormalFloat construction:
+ *   levels   16 fp32 values from -1 to 1 with an exact 0 (code 7): 7 negated
  *            and 8 positive standard-normal quantiles of evenly spaced
  *            probabilities between 1/2 and ((1 - 1/30) + (1 - 1/32)) / 2,
  *            divided by the largest (i8lt_nf4_levels returns them);
- *   blocks   64 consecutive elements of a weight row share one fp32 absmax;
  *   codes    the nearest level to x / absmax (one fp32 division), decided
  *            against the fp32 midpoints of adjacent levels (a value equal to
- *            a midpoint takes the lower level); all-zero blocks and the
- *            padding take the zero level;
- *   packing  row n of `packed` holds i8lt_nf4_row_bytes(K) bytes, two codes
- *            per byte, element 2j in the high nibble of byte j;
- *   dequantization  Wdq[n, k] = rn(levels[code] * absmax[n, k / 64]), one
- *            fp32 multiply rounded once to the compute dtype.
- * The nf4-dq variant (absmax stored in 8 bits) is not provided.
+ *            a midpoint takes the lower level).
+ * FP4 is the 4-bit floating-point format E2M1 (1 sign, 2 exponent, 1
+ * mantissa bits; exponent 0 subnormal), scaled so that the block's absmax
+ * is its largest magnitude 6:
+ *   levels   code = 8 s + c, c = the 3 exponent-mantissa bits with the
+ *            magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; levels[code] =
+ *            (-1)^s * E2M1(c) / 6 in fp32 (i8lt_fp4_levels; code 8 is -0);
+ *   codes    c is the magnitude nearest to |x / absmax| (one fp32
+ *            division), decided against the fp32 midpoints of adjacent
+ *            magnitude levels, a tie taking the c whose mantissa bit is 0
+ *            (round half to even); s = 1 for x < 0 unless c = 0 (zero is
+ *            always code 0).
+ * The nf4-dq / fp4-dq variants (absmax stored in 8 bits) are not provided.
+ * The entry points of the two formats take the same arguments.
  */
 #define I8LT_NF4_BLOCK 64
-/* out[16]: the levels, ascending. */
+/* out[16]: the levels, by code (ascending for NF4). */
 int i8lt_nf4_levels(float* out);
+int i8lt_fp4_levels(float* out);
 /* Bytes per packed row: round_up(K, 64) / 2 (a multiple of 32); -1 for K < 0. */
 int64_t i8lt_nf4_row_bytes(int64_t K);
 /* absmax values per row: ceil(K / 64); -1 for K < 0. */
@@ -349,8 +364,12 @@ int64_t i8lt_nf4_blocks(int64_t K);
  * aligned. */
 int i8lt_nf4_quantize(const void* W, int wt, int64_t N, int64_t K,
                       uint8_t* packed, float* absmax, void* stream);
+int i8lt_fp4_quantize(const void* W, int wt, int64_t N, int64_t K,
+                      uint8_t* packed, float* absmax, void* stream);
 /* The dequantized weight Wdq [N, K] row-major in dtype dt (device). */
 int i8lt_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N,
+                        int64_t K, void* out, int dt, void* stream);
+int i8lt_fp4_dequantize(const uint8_t* packed, const float* absmax, int64_t N,
                         int64_t K, void* out, int dt, void* stream);
 /* Workspace of the two matmuls: the device status word (256 bytes).  The
  * weight is then decoded stage by stage inside the GEMM and never stored. */
@@ -361,6 +380,11 @@ size_t i8lt_nf4_workspace_size(void);
  * [K, N] for the input gradient) and a TMA-fed GEMM reads it.  Same results
  * bit for bit, more memory, faster. */
 size_t i8lt_nf4_workspace_size_dq(int64_t K, int64_t N);
+/* Extra workspace bytes of an input gradient that also returns grad_bias
+ * (the fp32 partial sums of 128-token chunks, ceil(M / 128) x N): they
+ * follow the status word, and the dequantized weight of the materialized
+ * schedule, if it fits, follows them. */
+size_t i8lt_nf4_grad_bias_bytes(int64_t M, int64_t N);
 /*
  * out [M, N] = rn(A [M, K] @ Wdq^T + bias), A and out in the compute dtype
  * at (I8LT_F16 or I8LT_BF16), fp32 accumulation on the tensor
@@ -374,16 +398,32 @@ int i8lt_nf4_forward(const void* A, int at, int64_t M, int64_t K,
                      const uint8_t* packed, const float* absmax, int64_t N,
                      const void* bias, int bt, void* out,
                      void* ws, size_t ws_bytes, void* stream);
+int i8lt_fp4_forward(const void* A, int at, int64_t M, int64_t K,
+                     const uint8_t* packed, const float* absmax, int64_t N,
+                     const void* bias, int bt, void* out,
+                     void* ws, size_t ws_bytes, void* stream);
 /*
- * grad_A [M, K] = rn(G [M, N] @ Wdq) in the compute dtype gt, the gradient
- * to the input of the frozen 4-bit layer (the weight has none), with the
- * weight decoded the same way.  N a multiple of 8; other rules as
- * i8lt_nf4_forward.
+ * The gradients of the frozen 4-bit layer (the weight has none):
+ *   grad_A [M, K] = rn(G [M, N] @ Wdq) in the compute dtype gt, or NULL to
+ *            skip, with the weight decoded the same way;
+ *   grad_bias [N] = the sum over the tokens of G, dtype bt, or NULL: fp32
+ *            partial sums of 128-token chunks (each in a fixed order), then
+ *            summed over the chunks in order; reduced inside the GEMM by its
+ *            epilogue warps while the tensor cores run, or by a pass of its
+ *            own when grad_A is NULL -- the same bits either way.
+ * N a multiple of 8; ws at least i8lt_nf4_workspace_size() +
+ * (grad_bias ? i8lt_nf4_grad_bias_bytes(M, N) : 0) bytes, and that plus
+ * N * K * 2 (rounded up to 256) selects the materialized schedule; other
+ * rules as i8lt_nf4_forward.
  */
 int i8lt_nf4_backward_input(const void* G, int gt, int64_t M, int64_t N,
                             const uint8_t* packed, const float* absmax,
-                            int64_t K, void* grad_A, void* ws, size_t ws_bytes,
-                            void* stream);
+                            int64_t K, void* grad_A, void* grad_bias, int bt,
+                            void* ws, size_t ws_bytes, void* stream);
+int i8lt_fp4_backward_input(const void* G, int gt, int64_t M, int64_t N,
+                            const uint8_t* packed, const float* absmax,
+                            int64_t K, void* grad_A, void* grad_bias, int bt,
+                            void* ws, size_t ws_bytes, void* stream);
 
 /* SiLU between the two layers of an MLP: out = h * sigmoid(h), and its
  * backward out = g * silu'(h).  n elements of dtype dt. */

@@ -85,16 +85,24 @@ SIGNATURES = {
                                             c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
     "i8lt_noalloc_read_device_status": (c_int, [POINTER(c_int32), c_void_p]),
     "i8lt_nf4_levels": (c_int, [POINTER(c_float)]),
+    "i8lt_fp4_levels": (c_int, [POINTER(c_float)]),
     "i8lt_nf4_row_bytes": (c_int64, [c_int64]),
     "i8lt_nf4_blocks": (c_int64, [c_int64]),
     "i8lt_nf4_quantize": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_void_p]),
+    "i8lt_fp4_quantize": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_void_p]),
     "i8lt_nf4_dequantize": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_int, c_void_p]),
+    "i8lt_fp4_dequantize": (c_int, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_int, c_void_p]),
     "i8lt_nf4_workspace_size": (c_size_t, []),
     "i8lt_nf4_workspace_size_dq": (c_size_t, [c_int64, c_int64]),
+    "i8lt_nf4_grad_bias_bytes": (c_size_t, [c_int64, c_int64]),
     "i8lt_nf4_forward": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64, c_void_p, c_int,
                                  c_void_p, c_void_p, c_size_t, c_void_p]),
+    "i8lt_fp4_forward": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64, c_void_p, c_int,
+                                 c_void_p, c_void_p, c_size_t, c_void_p]),
     "i8lt_nf4_backward_input": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64, c_void_p,
-                                        c_void_p, c_size_t, c_void_p]),
+                                        c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
+    "i8lt_fp4_backward_input": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64, c_void_p,
+                                        c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
     "i8lt_silu_forward": (c_int, [c_void_p, c_int, c_int64, c_void_p, c_void_p]),
     "i8lt_silu_backward": (c_int, [c_void_p, c_void_p, c_int, c_int64, c_void_p, c_void_p]),
     "i8lt_profile_start": (c_int, [c_int]),
@@ -235,6 +243,12 @@ def i8lt_nf4_levels():
     return st, list(out)
 
 
+def i8lt_fp4_levels():
+    out = (c_float * 16)()
+    st = load().i8lt_fp4_levels(out)
+    return st, list(out)
+
+
 def i8lt_nf4_row_bytes(K) -> int:
     return load().i8lt_nf4_row_bytes(int(K))
 
@@ -247,8 +261,16 @@ def i8lt_nf4_quantize(W, wt, N, K, packed, absmax, stream=None) -> int:
     return load().i8lt_nf4_quantize(_p(W), wt, N, K, _p(packed), _p(absmax), _p(stream))
 
 
+def i8lt_fp4_quantize(W, wt, N, K, packed, absmax, stream=None) -> int:
+    return load().i8lt_fp4_quantize(_p(W), wt, N, K, _p(packed), _p(absmax), _p(stream))
+
+
 def i8lt_nf4_dequantize(packed, absmax, N, K, out, dt, stream=None) -> int:
     return load().i8lt_nf4_dequantize(_p(packed), _p(absmax), N, K, _p(out), dt, _p(stream))
+
+
+def i8lt_fp4_dequantize(packed, absmax, N, K, out, dt, stream=None) -> int:
+    return load().i8lt_fp4_dequantize(_p(packed), _p(absmax), N, K, _p(out), dt, _p(stream))
 
 
 def i8lt_nf4_workspace_size() -> int:
@@ -259,14 +281,28 @@ def i8lt_nf4_workspace_size_dq(K, N) -> int:
     return load().i8lt_nf4_workspace_size_dq(int(K), int(N))
 
 
+def i8lt_nf4_grad_bias_bytes(M, N) -> int:
+    return load().i8lt_nf4_grad_bias_bytes(int(M), int(N))
+
+
 def i8lt_nf4_forward(A, at, M, K, packed, absmax, N, bias, bt, out, ws, ws_bytes, stream=None) -> int:
     return load().i8lt_nf4_forward(_p(A), at, M, K, _p(packed), _p(absmax), N, _p(bias), bt, _p(out), _p(ws),
                                    ws_bytes, _p(stream))
 
 
-def i8lt_nf4_backward_input(G, gt, M, N, packed, absmax, K, grad_A, ws, ws_bytes, stream=None) -> int:
-    return load().i8lt_nf4_backward_input(_p(G), gt, M, N, _p(packed), _p(absmax), K, _p(grad_A), _p(ws), ws_bytes,
-                                          _p(stream))
+def i8lt_fp4_forward(A, at, M, K, packed, absmax, N, bias, bt, out, ws, ws_bytes, stream=None) -> int:
+    return load().i8lt_fp4_forward(_p(A), at, M, K, _p(packed), _p(absmax), N, _p(bias), bt, _p(out), _p(ws),
+                                   ws_bytes, _p(stream))
+
+
+def i8lt_nf4_backward_input(G, gt, M, N, packed, absmax, K, grad_A, grad_bias, bt, ws, ws_bytes, stream=None) -> int:
+    return load().i8lt_nf4_backward_input(_p(G), gt, M, N, _p(packed), _p(absmax), K, _p(grad_A), _p(grad_bias), bt,
+                                          _p(ws), ws_bytes, _p(stream))
+
+
+def i8lt_fp4_backward_input(G, gt, M, N, packed, absmax, K, grad_A, grad_bias, bt, ws, ws_bytes, stream=None) -> int:
+    return load().i8lt_fp4_backward_input(_p(G), gt, M, N, _p(packed), _p(absmax), K, _p(grad_A), _p(grad_bias), bt,
+                                          _p(ws), ws_bytes, _p(stream))
 
 
 def i8lt_silu_forward(h, dt, n, out, stream=None) -> int:

@@ -16,7 +16,7 @@ using namespace i8lt;
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -577,11 +577,18 @@ int i8lt_nf4_levels(float* out) {
   return I8LT_OK;
 }
 
+int i8lt_fp4_levels(float* out) {
+  if (out == nullptr) return I8LT_ERR_INVALID_ARG;
+  fmt4_levels(kFmtFp4, out);
+  return I8LT_OK;
+}
+
 int64_t i8lt_nf4_row_bytes(int64_t K) { return K < 0 ? -1 : round_up(K, 64) / 2; }
 
 int64_t i8lt_nf4_blocks(int64_t K) { return K < 0 ? -1 : ceil_div(K, 64); }
 
-int i8lt_nf4_quantize(const void* W, int wt, int64_t N, int64_t K, uint8_t* packed, float* absmax, void* stream) {
+static int quantize_4bit(int fmt, const void* W, int wt, int64_t N, int64_t K, uint8_t* packed, float* absmax,
+                  void* stream) {
   if (!valid_dt(wt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
   if (N < 0 || K < 0 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
   if (N == 0 || K == 0) return I8LT_OK;
@@ -589,11 +596,11 @@ int i8lt_nf4_quantize(const void* W, int wt, int64_t N, int64_t K, uint8_t* pack
   if (!aligned16(packed)) return I8LT_ERR_MISALIGNED;
   if (int d = check_device()) return d;
   return cuda_status(launch_nf4_quantize(W, wt, N, K, i8lt_nf4_row_bytes(K), packed, absmax,
-                                         static_cast<cudaStream_t>(stream)));
+                                         static_cast<cudaStream_t>(stream), fmt));
 }
 
-int i8lt_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, int64_t K, void* out, int dt,
-                        void* stream) {
+static int dequantize_4bit(int fmt, const uint8_t* packed, const float* absmax, int64_t N, int64_t K, void* out, int dt,
+                    void* stream) {
   if (!valid_dt(dt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
   if (N < 0 || K < 0 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
   if (N == 0 || K == 0) return I8LT_OK;
@@ -601,7 +608,25 @@ int i8lt_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, i
   if (!aligned16(packed)) return I8LT_ERR_MISALIGNED;
   if (int d = check_device()) return d;
   return cuda_status(launch_nf4_dequantize(packed, absmax, N, K, i8lt_nf4_row_bytes(K), out, dt,
-                                           static_cast<cudaStream_t>(stream)));
+                                           static_cast<cudaStream_t>(stream), fmt));
+}
+
+int i8lt_nf4_quantize(const void* W, int wt, int64_t N, int64_t K, uint8_t* packed, float* absmax, void* stream) {
+  return quantize_4bit(kFmtNf4, W, wt, N, K, packed, absmax, stream);
+}
+
+int i8lt_fp4_quantize(const void* W, int wt, int64_t N, int64_t K, uint8_t* packed, float* absmax, void* stream) {
+  return quantize_4bit(kFmtFp4, W, wt, N, K, packed, absmax, stream);
+}
+
+int i8lt_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, int64_t K, void* out, int dt,
+                        void* stream) {
+  return dequantize_4bit(kFmtNf4, packed, absmax, N, K, out, dt, stream);
+}
+
+int i8lt_fp4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, int64_t K, void* out, int dt,
+                        void* stream) {
+  return dequantize_4bit(kFmtFp4, packed, absmax, N, K, out, dt, stream);
 }
 
 size_t i8lt_nf4_workspace_size(void) { return kAlign; }
@@ -611,30 +636,44 @@ size_t i8lt_nf4_workspace_size_dq(int64_t K, int64_t N) {
   return kAlign + align_up(static_cast<size_t>(N) * static_cast<size_t>(K) * 2);
 }
 
+size_t i8lt_nf4_grad_bias_bytes(int64_t M, int64_t N) {
+  if (M < 0 || N < 0 || M > INT32_MAX / 2 || N > INT32_MAX / 2) return 0;
+  return align_up(static_cast<size_t>(gradout_partial_chunks(M)) * static_cast<size_t>(N) * 4);
+}
+
 }  // extern "C"
 
 namespace {
 
 // The two 4-bit matmuls: D[r, m] = sum_c Wdq(r, c) X[m, c] with the packed
 // weight decoded per stage (input_grad: r = k, c = n; forward: r = n, c = k).
-int nf4_gemm(bool input_grad, const void* X, int xt, int64_t M, int64_t C, int64_t R, const uint8_t* packed,
-             const float* absmax, int64_t K, int64_t N, const void* bias, int bt, void* out, void* ws,
-             size_t ws_bytes, void* stream) {
+// Workspace: [status][grad_bias partial sums, input gradient with grad_bias]
+// [the dequantized weight, materialized schedule].
+int nf4_gemm(int fmt, bool input_grad, const void* X, int xt, int64_t M, int64_t C, int64_t R, const uint8_t* packed,
+             const float* absmax, int64_t K, int64_t N, const void* bias, int bt, void* out, void* grad_bias,
+             void* ws, size_t ws_bytes, void* stream) {
   if (xt != DT_F16 && xt != DT_BF16) return I8LT_ERR_UNSUPPORTED_DTYPE;
-  if (bias != nullptr && !valid_dt(bt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
+  if ((bias != nullptr || grad_bias != nullptr) && !valid_dt(bt)) return I8LT_ERR_UNSUPPORTED_DTYPE;
   if (M < 0 || K <= 0 || N <= 0) return I8LT_ERR_INVALID_ARG;
   if (M > INT32_MAX / 2 || K > INT32_MAX / 2 || N > INT32_MAX / 2) return I8LT_ERR_INVALID_ARG;
   if (C % 8 != 0) return I8LT_ERR_INVALID_ARG;   // 16-byte rows of X for the tensor copies
   if (ws == nullptr || packed == nullptr || absmax == nullptr) return I8LT_ERR_INVALID_ARG;
-  if (M > 0 && (X == nullptr || out == nullptr)) return I8LT_ERR_INVALID_ARG;
+  if (M > 0 && (X == nullptr || (out == nullptr && (grad_bias == nullptr || !input_grad)))) return I8LT_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(packed) || !aligned16(out)) return I8LT_ERR_MISALIGNED;
   if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
-  if (ws_bytes < kAlign) return I8LT_ERR_WORKSPACE;
+  const size_t base = kAlign + (grad_bias != nullptr ? i8lt_nf4_grad_bias_bytes(M, N) : 0);
+  if (ws_bytes < base) return I8LT_ERR_WORKSPACE;
   if (int d = check_device()) return d;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   DevStatus* st = static_cast<DevStatus*>(ws);
+  float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kAlign);
   if (cudaMemsetAsync(st, 0, sizeof(DevStatus), s) != cudaSuccess) return I8LT_ERR_CUDA;
-  if (M == 0) return I8LT_OK;
+  if (M == 0 || out == nullptr) {
+    // the bias gradient alone (or of an empty batch): the prepass reduction
+    if (grad_bias == nullptr) return I8LT_OK;
+    return cuda_status(launch_gradout_prepass(X, xt, M, N, true, nullptr, 0, grad_bias, bt, partial,
+                                              gradout_partial_chunks(M), s));
+  }
   const int64_t row_bytes = i8lt_nf4_row_bytes(K);
   const CUtensorMapDataType xdt = xt == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   BwdGemmArgs g;
@@ -644,11 +683,12 @@ int nf4_gemm(bool input_grad, const void* X, int xt, int64_t M, int64_t C, int64
   // schedule: a prepass writes Wdq [N, K] (forward) or Wdq^T [K, N] (input
   // gradient) and the GEMM reads it by TMA; otherwise the weight is decoded
   // per stage inside the GEMM
-  const bool materialize = ws_bytes >= i8lt_nf4_workspace_size_dq(K, N);
+  const size_t wdq_bytes = i8lt_nf4_workspace_size_dq(K, N) - kAlign;
+  const bool materialize = ws_bytes >= base + wdq_bytes;
   if (materialize) {
-    void* wdq = static_cast<uint8_t*>(ws) + kAlign;
-    cudaError_t e = input_grad ? launch_nf4_dequantize_t(packed, absmax, N, K, row_bytes, wdq, xt, s)
-                               : launch_nf4_dequantize(packed, absmax, N, K, row_bytes, wdq, xt, s);
+    void* wdq = static_cast<uint8_t*>(ws) + base;
+    cudaError_t e = input_grad ? launch_nf4_dequantize_t(packed, absmax, N, K, row_bytes, wdq, xt, s, fmt)
+                               : launch_nf4_dequantize(packed, absmax, N, K, row_bytes, wdq, xt, s, fmt);
     if (e != cudaSuccess) return I8LT_ERR_CUDA;
     if (!make_tmap(&g.tmWT, xdt, wdq, C, R, C * 2, kBK, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B)) return I8LT_ERR_CUDA;
   } else if (!make_tmap(&g.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, row_bytes, N, row_bytes,
@@ -670,8 +710,15 @@ int nf4_gemm(bool input_grad, const void* X, int xt, int64_t M, int64_t C, int64
   ea.ab_fmt = xt == DT_BF16 ? ((1u << 7) | (1u << 10)) : 0u;   // A and B format: bf16
   ea.absmax = absmax;
   ea.nblk = static_cast<int>(ceil_div(K, 64));
-  nf4_levels(ea.lv);
-  return cuda_status(launch_nf4_gemm(g, ea, input_grad, materialize, s));
+  fmt4_levels(fmt, ea.lv);
+  if (grad_bias != nullptr) {   // input gradient: the GEMM reduces grad_bias from G (16-bit, N % 8 == 0)
+    ea.gsum = X;
+    ea.gsum_dt = xt;
+    ea.partial = partial;
+  }
+  if (launch_nf4_gemm(g, ea, input_grad, materialize, s) != cudaSuccess) return I8LT_ERR_CUDA;
+  if (grad_bias != nullptr) return cuda_status(launch_grad_bias_finalize(partial, M, N, grad_bias, bt, s));
+  return I8LT_OK;
 }
 
 }  // namespace
@@ -680,12 +727,26 @@ extern "C" {
 
 int i8lt_nf4_forward(const void* A, int at, int64_t M, int64_t K, const uint8_t* packed, const float* absmax,
                      int64_t N, const void* bias, int bt, void* out, void* ws, size_t ws_bytes, void* stream) {
-  return nf4_gemm(false, A, at, M, K, N, packed, absmax, K, N, bias, bt, out, ws, ws_bytes, stream);
+  return nf4_gemm(kFmtNf4, false, A, at, M, K, N, packed, absmax, K, N, bias, bt, out, nullptr, ws, ws_bytes, stream);
+}
+
+int i8lt_fp4_forward(const void* A, int at, int64_t M, int64_t K, const uint8_t* packed, const float* absmax,
+                     int64_t N, const void* bias, int bt, void* out, void* ws, size_t ws_bytes, void* stream) {
+  return nf4_gemm(kFmtFp4, false, A, at, M, K, N, packed, absmax, K, N, bias, bt, out, nullptr, ws, ws_bytes, stream);
 }
 
 int i8lt_nf4_backward_input(const void* G, int gt, int64_t M, int64_t N, const uint8_t* packed, const float* absmax,
-                            int64_t K, void* grad_A, void* ws, size_t ws_bytes, void* stream) {
-  return nf4_gemm(true, G, gt, M, N, K, packed, absmax, K, N, nullptr, 0, grad_A, ws, ws_bytes, stream);
+                            int64_t K, void* grad_A, void* grad_bias, int bt, void* ws, size_t ws_bytes,
+                            void* stream) {
+  return nf4_gemm(kFmtNf4, true, G, gt, M, N, K, packed, absmax, K, N, nullptr, bt, grad_A, grad_bias, ws, ws_bytes,
+                  stream);
+}
+
+int i8lt_fp4_backward_input(const void* G, int gt, int64_t M, int64_t N, const uint8_t* packed, const float* absmax,
+                            int64_t K, void* grad_A, void* grad_bias, int bt, void* ws, size_t ws_bytes,
+                            void* stream) {
+  return nf4_gemm(kFmtFp4, true, G, gt, M, N, K, packed, absmax, K, N, nullptr, bt, grad_A, grad_bias, ws, ws_bytes,
+                  stream);
 }
 
 int i8lt_silu_forward(const void* h, int dt, int64_t n, void* out, void* stream) {

@@ -177,17 +177,24 @@ cudaError_t launch_bwd_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool fuse
 cudaError_t launch_nf4_gemm(const BwdGemmArgs& g, const BwdEpiArgs& e, bool input_grad, bool materialized,
                             cudaStream_t s);
 
+// The 4-bit formats sharing the packed storage (two codes per byte, one fp32
+// absmax per 64 elements of a row) and the table-driven decode of the
+// matmuls: 4-bit NormalFloat and E2M1 floating point (i8lt_nf4.cu).
+enum Fmt4 { kFmtNf4 = 0, kFmtFp4 = 1 };
+
 // The 16 NF4 levels (ascending fp32), computed once on the host.
 void nf4_levels(float out[16]);
+// The 16 levels of a format, indexed by code, computed once on the host.
+void fmt4_levels(int fmt, float out[16]);
 // W [N, K] (dtype wt) -> packed [N, row_bytes] codes and absmax [N, ceil(K / 64)].
 cudaError_t launch_nf4_quantize(const void* W, int wt, int64_t N, int64_t K, int64_t row_bytes, uint8_t* packed,
-                                float* absmax, cudaStream_t s);
+                                float* absmax, cudaStream_t s, int fmt = kFmtNf4);
 // packed + absmax -> WdqT [K, N] (dtype dt, f16 or bf16; N a multiple of 8).
 cudaError_t launch_nf4_dequantize_t(const uint8_t* packed, const float* absmax, int64_t N, int64_t K,
-                                    int64_t row_bytes, void* WdqT, int dt, cudaStream_t s);
+                                    int64_t row_bytes, void* WdqT, int dt, cudaStream_t s, int fmt = kFmtNf4);
 // packed + absmax -> out [N, K] (dtype dt): lv[code] * absmax, rounded once.
 cudaError_t launch_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, int64_t K,
-                                  int64_t row_bytes, void* out, int dt, cudaStream_t s);
+                                  int64_t row_bytes, void* out, int dt, cudaStream_t s, int fmt = kFmtNf4);
 
 // Backward prepass of the materialized schedule: WdqT[k, n] =
 // fp16_rn(fp32(CB[n, k]) * (SCB[n] * fp32(1/127))) for k < k_pad, n < N, and

@@ -11,8 +11,20 @@
 //           midpoints of adjacent levels (strictly greater: the upper level);
 //   packing: two codes per byte, the even element in the high nibble, rows
 //           padded to a multiple of 64 elements with the zero level.
+// Beside NF4, the same storage holds FP4 (the bnb.fp4 quantize option of the
+// same page, also named there without a definition): the 4-bit floating-point
+// format with 1 sign, 2 exponent and 1 mantissa bits (E2M1: magnitudes 0,
+// 0.5, 1, 1.5, 2, 3, 4, 6 for the codes 0..7 of the exponent-mantissa bits,
+// the sign in bit 3), the block's absmax mapped to 6:
+//   levels: lv[code] = +-E2M1(code) / 6 in fp32 (code 8 is -0);
+//   code:   the magnitude code of the level nearest to |x / absmax|, decided
+//           in fp32 against the midpoints of adjacent magnitude levels, a tie
+//           going to the code whose mantissa bit is 0 (round half to even);
+//           the sign bit set for x < 0 unless the magnitude code is 0 (one
+//           zero code, 0, also for padding and all-zero blocks).
 // The matmuls that decode these codes inside the tensor-core pipeline are in
-// i8lt_gemm.cu (kModeNf4, kModeNf4T).
+// i8lt_gemm.cu (kModeNf4, kModeNf4T): they look every code up in the
+// 16-entry level table, so both formats run through them unchanged.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -40,15 +52,45 @@ double normal_quantile(double p) {
   return 0.5 * (lo + hi);
 }
 
+// Level table and decision thresholds of a 4-bit format.  NF4: lv ascending
+// with the code, mid[0..14] between adjacent levels.  FP4: lv by code
+// (sign-magnitude), mid[0..6] between adjacent magnitude levels lv[0..7],
+// bit j of tie_up set when a value equal to mid[j] takes the upper level.
 struct Nf4Tables {
   float lv[16];
   float mid[15];
+  uint32_t tie_up;
 };
+
+const Nf4Tables& fp4_tables() {
+  static Nf4Tables t;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    t = Nf4Tables{};
+    // E2M1 magnitude of the exponent-mantissa bits c = (e1 e0 m): e = 0 is
+    // subnormal (m / 2), otherwise 2^(e - 1) (1 + m / 2)
+    double mag[8];
+    for (int c = 0; c < 8; ++c) {
+      const int e = c >> 1, m = c & 1;
+      mag[c] = e == 0 ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+    }
+    for (int c = 0; c < 8; ++c) {
+      t.lv[c] = static_cast<float>(mag[c] / mag[7]);
+      t.lv[8 + c] = -t.lv[c];
+    }
+    for (int j = 0; j < 7; ++j) {
+      t.mid[j] = static_cast<float>((static_cast<double>(t.lv[j]) + static_cast<double>(t.lv[j + 1])) / 2.0);
+      if (((j + 1) & 1) == 0) t.tie_up |= 1u << j;   // the upper code's mantissa bit is 0
+    }
+  });
+  return t;
+}
 
 const Nf4Tables& tables() {
   static Nf4Tables t;
   static std::once_flag once;
   std::call_once(once, [] {
+    t.tie_up = 0;
     const double delta = ((1.0 - 1.0 / 30.0) + (1.0 - 1.0 / 32.0)) / 2.0;
     const double step_neg = (0.5 - delta) / 7.0, step_pos = (0.5 - delta) / 8.0;
     double v[16];
@@ -73,11 +115,12 @@ __device__ __forceinline__ float load_w(const T* p, int64_t i) {
 // codes); the 8 threads of a 64-element block reduce its absmax with three
 // shuffles.  Every thread of a block runs every iteration (the shuffles take
 // the whole warp).
-template <typename T>
+template <typename T, bool kFp4>
 __global__ void __launch_bounds__(256) nf4_quantize_kernel(const T* __restrict__ W, int64_t N, int64_t K,
                                                            int64_t row_bytes, int nblk, Nf4Tables c,
                                                            uint8_t* __restrict__ packed,
                                                            float* __restrict__ absmax) {
+  constexpr uint32_t kZero = kFp4 ? 0u : 7u;   // the code of the zero level
   const int64_t gpr = row_bytes / 4;   // groups of 8 per row (a multiple of 8)
   const int64_t total = N * gpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -102,12 +145,19 @@ __global__ void __launch_bounds__(256) nf4_quantize_kernel(const T* __restrict__
     uint32_t word = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      uint32_t code = 7u;   // the zero level: padding and all-zero blocks
+      uint32_t code = kZero;   // padding and all-zero blocks
       if (k0 + i < K && am > 0.f) {
         const float xn = __fdiv_rn(x[i], am);
         code = 0u;
+        if constexpr (kFp4) {
+          const float a = fabsf(xn);
 #pragma unroll
-        for (int j = 0; j < 15; ++j) code += xn > c.mid[j] ? 1u : 0u;
+          for (int j = 0; j < 7; ++j) code += (a > c.mid[j] || (a == c.mid[j] && ((c.tie_up >> j) & 1u))) ? 1u : 0u;
+          if (xn < 0.f && code != 0u) code |= 8u;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 15; ++j) code += xn > c.mid[j] ? 1u : 0u;
+        }
       }
       // byte i / 2 holds elements (2j, 2j + 1) as (high, low) nibbles
       word |= code << (8 * (i >> 1) + ((i & 1) ? 0 : 4));
@@ -212,41 +262,54 @@ int grid_for(int64_t threads) {
 
 }  // namespace
 
-void nf4_levels(float out[16]) {
-  const Nf4Tables& t = tables();
+void nf4_levels(float out[16]) { fmt4_levels(kFmtNf4, out); }
+
+void fmt4_levels(int fmt, float out[16]) {
+  const Nf4Tables& t = fmt == kFmtFp4 ? fp4_tables() : tables();
   for (int i = 0; i < 16; ++i) out[i] = t.lv[i];
 }
 
+namespace {
+template <bool kFp4>
+void quantize_launch(const void* W, int wt, int64_t N, int64_t K, int64_t row_bytes, int nblk, int blocks,
+                     const Nf4Tables& c, uint8_t* packed, float* absmax, cudaStream_t s) {
+  switch (wt) {
+    case DT_F16:
+      nf4_quantize_kernel<__half, kFp4><<<blocks, 256, 0, s>>>(static_cast<const __half*>(W), N, K, row_bytes, nblk,
+                                                               c, packed, absmax);
+      break;
+    case DT_BF16:
+      nf4_quantize_kernel<__nv_bfloat16, kFp4><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), N, K,
+                                                                      row_bytes, nblk, c, packed, absmax);
+      break;
+    default:
+      nf4_quantize_kernel<float, kFp4><<<blocks, 256, 0, s>>>(static_cast<const float*>(W), N, K, row_bytes, nblk,
+                                                              c, packed, absmax);
+      break;
+  }
+}
+}  // namespace
+
 cudaError_t launch_nf4_quantize(const void* W, int wt, int64_t N, int64_t K, int64_t row_bytes, uint8_t* packed,
-                                float* absmax, cudaStream_t s) {
+                                float* absmax, cudaStream_t s, int fmt) {
   if (N == 0 || K == 0) return cudaSuccess;
   const int nblk = static_cast<int>(ceil_div(K, 64));
   const int blocks = grid_for(N * (row_bytes / 4));
-  const Nf4Tables& c = tables();
   ProfScope ps(K_NF4_QUANTIZE, s);
-  switch (wt) {
-    case DT_F16:
-      nf4_quantize_kernel<__half><<<blocks, 256, 0, s>>>(static_cast<const __half*>(W), N, K, row_bytes, nblk, c,
-                                                         packed, absmax);
-      break;
-    case DT_BF16:
-      nf4_quantize_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), N, K,
-                                                                row_bytes, nblk, c, packed, absmax);
-      break;
-    default:
-      nf4_quantize_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(W), N, K, row_bytes, nblk, c,
-                                                        packed, absmax);
-      break;
+  if (fmt == kFmtFp4) {
+    quantize_launch<true>(W, wt, N, K, row_bytes, nblk, blocks, fp4_tables(), packed, absmax, s);
+  } else {
+    quantize_launch<false>(W, wt, N, K, row_bytes, nblk, blocks, tables(), packed, absmax, s);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, int64_t K,
-                                  int64_t row_bytes, void* out, int dt, cudaStream_t s) {
+                                  int64_t row_bytes, void* out, int dt, cudaStream_t s, int fmt) {
   if (N == 0 || K == 0) return cudaSuccess;
   const int nblk = static_cast<int>(ceil_div(K, 64));
   const int blocks = grid_for(N * (row_bytes / 4));
-  const Nf4Tables& c = tables();
+  const Nf4Tables& c = fmt == kFmtFp4 ? fp4_tables() : tables();
   // rows of K elements start 16-byte aligned when K is a multiple of 8 and
   // the output is 16-byte aligned
   const bool vec = (K % 8) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
@@ -269,11 +332,11 @@ cudaError_t launch_nf4_dequantize(const uint8_t* packed, const float* absmax, in
 }
 
 cudaError_t launch_nf4_dequantize_t(const uint8_t* packed, const float* absmax, int64_t N, int64_t K,
-                                    int64_t row_bytes, void* WdqT, int dt, cudaStream_t s) {
+                                    int64_t row_bytes, void* WdqT, int dt, cudaStream_t s, int fmt) {
   if (N == 0 || K == 0) return cudaSuccess;
   const int nblk = static_cast<int>(ceil_div(K, 64));
   const dim3 grid(static_cast<unsigned>(ceil_div(N, kTn)), static_cast<unsigned>(ceil_div(K, kTk)));
-  const Nf4Tables& c = tables();
+  const Nf4Tables& c = fmt == kFmtFp4 ? fp4_tables() : tables();
   ProfScope ps(K_NF4_DEQUANTIZE, s);
   if (dt == DT_BF16) {
     nf4_dequantize_t_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(packed, absmax, N, K, row_bytes, nblk, c,

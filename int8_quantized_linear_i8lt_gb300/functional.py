@@ -406,53 +406,94 @@ class Int8MLPFunction(torch.autograd.Function):
 
 
 # ---------------------------------------------------------------------------
-# 4-bit NormalFloat weight-only layer (QLoRA fine-tuning: frozen 4-bit base
-# weights, 16-bit compute; see i8lt_nf4_forward in include/i8lt.h)
+# 4-bit weight-only layers (QLoRA fine-tuning: frozen 4-bit base weights,
+# 16-bit compute; NF4 and FP4 share one storage and one set of matmul
+# kernels, see i8lt_nf4_forward / i8lt_fp4_forward in include/i8lt.h)
 # ---------------------------------------------------------------------------
 
-def nf4_levels() -> list[float]:
-    st, lv = _lib.i8lt_nf4_levels()
-    _check(st, "i8lt_nf4_levels")
+FORMATS_4BIT = ("nf4", "fp4")
+
+
+def _fmt4(fmt: str) -> str:
+    if fmt not in FORMATS_4BIT:
+        raise I8LTError(f"unknown 4-bit format {fmt!r} (expected one of {FORMATS_4BIT})")
+    return fmt
+
+
+def _fn4(fmt: str, name: str):
+    return getattr(_lib, f"i8lt_{_fmt4(fmt)}_{name}")
+
+
+def levels_4bit(fmt: str = "nf4") -> list[float]:
+    """The 16 levels of a 4-bit format, by code."""
+    st, lv = _fn4(fmt, "levels")()
+    _check(st, f"i8lt_{fmt}_levels")
     return lv
 
 
-def nf4_quantize(W: torch.Tensor):
+def nf4_levels() -> list[float]:
+    return levels_4bit("nf4")
+
+
+def fp4_levels() -> list[float]:
+    return levels_4bit("fp4")
+
+
+def quantize_4bit(W: torch.Tensor, fmt: str = "nf4"):
     """W [N, K] (f16 / bf16 / f32, CUDA) -> (packed uint8 [N, row_bytes],
-    absmax fp32 [N, ceil(K / 64)])."""
+    absmax fp32 [N, ceil(K / 64)]) in the 4-bit format ``fmt``."""
     _require_cuda(W)
     W = W.contiguous()
     N, K = W.shape
     packed = torch.empty(N, _lib.i8lt_nf4_row_bytes(K), dtype=torch.uint8, device=W.device)
     absmax = torch.empty(N, _lib.i8lt_nf4_blocks(K), dtype=torch.float32, device=W.device)
-    _check(_lib.i8lt_nf4_quantize(W.data_ptr(), _code(W.dtype), N, K, packed.data_ptr(), absmax.data_ptr(),
-                                  _stream(W)), "i8lt_nf4_quantize")
+    _check(_fn4(fmt, "quantize")(W.data_ptr(), _code(W.dtype), N, K, packed.data_ptr(), absmax.data_ptr(),
+                                 _stream(W)), f"i8lt_{fmt}_quantize")
     return packed, absmax
 
 
-def nf4_dequantize(packed: torch.Tensor, absmax: torch.Tensor, K: int, dtype: torch.dtype) -> torch.Tensor:
+def nf4_quantize(W: torch.Tensor):
+    return quantize_4bit(W, "nf4")
+
+
+def fp4_quantize(W: torch.Tensor):
+    return quantize_4bit(W, "fp4")
+
+
+def dequantize_4bit(packed: torch.Tensor, absmax: torch.Tensor, K: int, dtype: torch.dtype,
+                    fmt: str = "nf4") -> torch.Tensor:
     """The dequantized weight [N, K] in ``dtype``."""
     _require_cuda(packed, absmax)
     N = packed.shape[0]
     out = torch.empty(N, K, dtype=dtype, device=packed.device)
-    _check(_lib.i8lt_nf4_dequantize(packed.data_ptr(), absmax.data_ptr(), N, K, out.data_ptr(), _code(dtype),
-                                    _stream(packed)), "i8lt_nf4_dequantize")
+    _check(_fn4(fmt, "dequantize")(packed.data_ptr(), absmax.data_ptr(), N, K, out.data_ptr(), _code(dtype),
+                                   _stream(packed)), f"i8lt_{fmt}_dequantize")
     return out
 
 
-def _nf4_ws(device, ws, K, N, materialized):
-    """Workspace of the 4-bit matmuls: the status word only (the weight is
-    decoded inside the GEMM), or room for the dequantized weight
-    (``materialized``: a prepass writes it, a plain 16-bit GEMM reads it;
-    same bits, faster, N * K * 2 bytes more)."""
+def nf4_dequantize(packed: torch.Tensor, absmax: torch.Tensor, K: int, dtype: torch.dtype) -> torch.Tensor:
+    return dequantize_4bit(packed, absmax, K, dtype, "nf4")
+
+
+def fp4_dequantize(packed: torch.Tensor, absmax: torch.Tensor, K: int, dtype: torch.dtype) -> torch.Tensor:
+    return dequantize_4bit(packed, absmax, K, dtype, "fp4")
+
+
+def _nf4_ws(device, ws, K, N, materialized, extra=0):
+    """Workspace of the 4-bit matmuls: the status word (and ``extra`` bytes
+    of grad_bias partial sums), the weight then decoded inside the GEMM; or
+    room for the dequantized weight after them (``materialized``: a prepass
+    writes it, a plain 16-bit GEMM reads it; same bits, faster, N * K * 2
+    bytes more)."""
     if ws is None:
         n = _lib.i8lt_nf4_workspace_size_dq(K, N) if materialized else _lib.i8lt_nf4_workspace_size()
-        ws = torch.empty(n, dtype=torch.uint8, device=device)
+        ws = torch.empty(n + extra, dtype=torch.uint8, device=device)
     return ws
 
 
-def nf4_forward(A: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: int,
-                bias: torch.Tensor | None = None, out: torch.Tensor | None = None,
-                ws: torch.Tensor | None = None, materialized: bool = False) -> torch.Tensor:
+def forward_4bit(A: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: int,
+                 bias: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                 ws: torch.Tensor | None = None, materialized: bool = False, fmt: str = "nf4") -> torch.Tensor:
     """out [M, N] = A [M, K] @ Wdq^T (+ bias) in A's dtype (f16 or bf16)."""
     _require_cuda(A, packed, absmax, bias)
     A = A.contiguous()
@@ -461,39 +502,63 @@ def nf4_forward(A: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: 
     if out is None:
         out = torch.empty(M, N, dtype=A.dtype, device=A.device)
     ws = _nf4_ws(A.device, ws, K, N, materialized)
-    _check(_lib.i8lt_nf4_forward(A.data_ptr(), _code(A.dtype), M, K, packed.data_ptr(), absmax.data_ptr(), N,
-                                 _ptr(bias), _code(bias.dtype) if bias is not None else 0, out.data_ptr(),
-                                 ws.data_ptr(), ws.numel(), _stream(A)), "i8lt_nf4_forward")
+    _check(_fn4(fmt, "forward")(A.data_ptr(), _code(A.dtype), M, K, packed.data_ptr(), absmax.data_ptr(), N,
+                                _ptr(bias), _code(bias.dtype) if bias is not None else 0, out.data_ptr(),
+                                ws.data_ptr(), ws.numel(), _stream(A)), f"i8lt_{fmt}_forward")
     return out
 
 
-def nf4_backward_input(G: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: int,
-                       out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
-                       materialized: bool = False) -> torch.Tensor:
-    """grad_A [M, K] = G [M, N] @ Wdq in G's dtype (f16 or bf16)."""
+def nf4_forward(A, packed, absmax, K, bias=None, out=None, ws=None, materialized=False) -> torch.Tensor:
+    return forward_4bit(A, packed, absmax, K, bias, out, ws, materialized, "nf4")
+
+
+def fp4_forward(A, packed, absmax, K, bias=None, out=None, ws=None, materialized=False) -> torch.Tensor:
+    return forward_4bit(A, packed, absmax, K, bias, out, ws, materialized, "fp4")
+
+
+def backward_input_4bit(G: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, K: int,
+                        need_grad_A: bool = True, bias_dtype: torch.dtype | None = None,
+                        out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                        materialized: bool = False, fmt: str = "nf4"):
+    """(grad_A [M, K] = G [M, N] @ Wdq in G's dtype (f16 or bf16) or None,
+    grad_bias [N] in ``bias_dtype`` or None).  grad_bias is reduced inside
+    the GEMM (or by a pass of its own when grad_A is not needed)."""
     _require_cuda(G, packed, absmax)
     G = G.contiguous()
     M, N = G.shape
-    if out is None:
+    if need_grad_A and out is None:
         out = torch.empty(M, K, dtype=G.dtype, device=G.device)
-    ws = _nf4_ws(G.device, ws, K, N, materialized)
-    _check(_lib.i8lt_nf4_backward_input(G.data_ptr(), _code(G.dtype), M, N, packed.data_ptr(), absmax.data_ptr(),
-                                        K, out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(G)),
-           "i8lt_nf4_backward_input")
-    return out
+    gb = torch.empty(N, dtype=bias_dtype, device=G.device) if bias_dtype is not None else None
+    extra = _lib.i8lt_nf4_grad_bias_bytes(M, N) if gb is not None else 0
+    ws = _nf4_ws(G.device, ws, K, N, materialized, extra)
+    _check(_fn4(fmt, "backward_input")(G.data_ptr(), _code(G.dtype), M, N, packed.data_ptr(), absmax.data_ptr(), K,
+                                       _ptr(out) if need_grad_A else None, _ptr(gb),
+                                       _code(bias_dtype) if bias_dtype is not None else 0, ws.data_ptr(), ws.numel(),
+                                       _stream(G)), f"i8lt_{fmt}_backward_input")
+    return (out if need_grad_A else None), gb
 
 
-class NF4LinearFunction(torch.autograd.Function):
-    """y = x @ Wdq^T + bias with the frozen 4-bit weight decoded inside the
-    matmuls; gradients to x and to the bias (summed over the tokens)."""
+def nf4_backward_input(G, packed, absmax, K, out=None, ws=None, materialized=False) -> torch.Tensor:
+    """grad_A [M, K] = G [M, N] @ Wdq in G's dtype (f16 or bf16)."""
+    return backward_input_4bit(G, packed, absmax, K, out=out, ws=ws, materialized=materialized, fmt="nf4")[0]
+
+
+def fp4_backward_input(G, packed, absmax, K, out=None, ws=None, materialized=False) -> torch.Tensor:
+    return backward_input_4bit(G, packed, absmax, K, out=out, ws=ws, materialized=materialized, fmt="fp4")[0]
+
+
+class Linear4bitFunction(torch.autograd.Function):
+    """y = x @ Wdq^T + bias with the frozen 4-bit weight (format ``fmt``)
+    decoded inside the matmuls; gradients to x and to the bias (summed over
+    the tokens inside the input-gradient GEMM)."""
 
     @staticmethod
-    def forward(ctx, x, packed, absmax, K, bias, materialized=False):
+    def forward(ctx, x, packed, absmax, K, bias, materialized=False, fmt="nf4"):
         shape = x.shape
         x2 = x.reshape(-1, K)
-        y = nf4_forward(x2, packed, absmax, K, bias, materialized=materialized)
+        y = forward_4bit(x2, packed, absmax, K, bias, materialized=materialized, fmt=fmt)
         ctx.save_for_backward(packed, absmax)
-        ctx.K, ctx.shape, ctx.has_bias, ctx.materialized = K, shape, bias is not None, materialized
+        ctx.K, ctx.shape, ctx.materialized, ctx.fmt = K, shape, materialized, fmt
         ctx.bias_dtype = bias.dtype if bias is not None else None
         return y.reshape(*shape[:-1], packed.shape[0])
 
@@ -501,8 +566,17 @@ class NF4LinearFunction(torch.autograd.Function):
     def backward(ctx, gy):
         packed, absmax = ctx.saved_tensors
         g2 = gy.reshape(-1, packed.shape[0])
-        gx = None
-        if ctx.needs_input_grad[0]:
-            gx = nf4_backward_input(g2, packed, absmax, ctx.K, materialized=ctx.materialized).reshape(ctx.shape)
-        gb = g2.float().sum(0).to(ctx.bias_dtype) if ctx.has_bias and ctx.needs_input_grad[4] else None
-        return gx, None, None, None, gb, None
+        need_x = ctx.needs_input_grad[0]
+        need_b = ctx.bias_dtype is not None and ctx.needs_input_grad[4]
+        if not (need_x or need_b):
+            return None, None, None, None, None, None, None
+        gx, gb = backward_input_4bit(g2, packed, absmax, ctx.K, need_grad_A=need_x,
+                                     bias_dtype=ctx.bias_dtype if need_b else None,
+                                     materialized=ctx.materialized, fmt=ctx.fmt)
+        if gx is not None:
+            gx = gx.reshape(ctx.shape)
+        return gx, None, None, None, gb, None, None
+
+
+# the NF4 layer's function under its own name
+NF4LinearFunction = Linear4bitFunction

@@ -96,20 +96,26 @@ class Int8MLP(torch.nn.Module):
                                        self.fc2.bias, self.fc1.threshold, self.residual, self.fc1.max_outliers)
 
 
-class LinearNF4(torch.nn.Module):
-    """Frozen 4-bit NormalFloat linear layer of QLoRA fine-tuning: the weight
-    is stored as packed 4-bit codes with one fp32 absmax per 64 elements of a
-    row and decoded to the 16-bit compute dtype (the input's: f16 or bf16)
-    inside the tensor-core matmuls of the forward and of the input gradient.
-    The weight takes no gradient; the bias does.  ``materialized``: each
-    matmul first writes the 16-bit weight to a temporary workspace and reads
-    it with a plain GEMM (faster, N * K * 2 bytes of transient memory);
-    the results are the same bits."""
+class Linear4bit(torch.nn.Module):
+    """Frozen 4-bit linear layer of QLoRA fine-tuning: the weight is stored
+    as packed 4-bit codes (``fmt``: "nf4", 4-bit NormalFloat, or "fp4", the
+    E2M1 floating-point format) with one fp32 absmax per 64 elements of a row
+    and decoded to the 16-bit compute dtype (the input's: f16 or bf16) inside
+    the tensor-core matmuls of the forward and of the input gradient.  The
+    weight takes no gradient; the bias does (reduced inside the
+    input-gradient GEMM).  ``materialized``: each matmul first writes the
+    16-bit weight to a temporary workspace and reads it with a plain GEMM
+    (faster, N * K * 2 bytes of transient memory); the results are the same
+    bits."""
+
+    fmt = "nf4"
 
     def __init__(self, in_features: int, out_features: int, bias: bool = True, device=None,
-                 bias_dtype: torch.dtype = torch.bfloat16, materialized: bool = False):
+                 bias_dtype: torch.dtype = torch.bfloat16, materialized: bool = False, fmt: str | None = None):
         super().__init__()
         from . import _lib
+        if fmt is not None:
+            self.fmt = F._fmt4(fmt)
         self.in_features = in_features
         self.out_features = out_features
         self.materialized = bool(materialized)
@@ -124,11 +130,11 @@ class LinearNF4(torch.nn.Module):
 
     @classmethod
     def from_float(cls, weight: torch.Tensor, bias: torch.Tensor | None = None,
-                   materialized: bool = False) -> "LinearNF4":
+                   materialized: bool = False, **kw) -> "Linear4bit":
         N, K = weight.shape
         layer = cls(K, N, bias=bias is not None, device=weight.device,
-                    bias_dtype=bias.dtype if bias is not None else torch.bfloat16, materialized=materialized)
-        packed, absmax = F.nf4_quantize(weight)
+                    bias_dtype=bias.dtype if bias is not None else torch.bfloat16, materialized=materialized, **kw)
+        packed, absmax = F.quantize_4bit(weight, layer.fmt)
         layer.packed.copy_(packed)
         layer.absmax.copy_(absmax)
         if bias is not None:
@@ -137,7 +143,19 @@ class LinearNF4(torch.nn.Module):
         return layer
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
-        return F.NF4LinearFunction.apply(x, self.packed, self.absmax, self.in_features, self.bias, self.materialized)
+        return F.Linear4bitFunction.apply(x, self.packed, self.absmax, self.in_features, self.bias,
+                                          self.materialized, self.fmt)
 
     def extra_repr(self) -> str:
-        return f"in_features={self.in_features}, out_features={self.out_features}, bias={self.bias is not None}"
+        return (f"in_features={self.in_features}, out_features={self.out_features}, bias={self.bias is not None}, "
+                f"fmt={self.fmt}")
+
+
+class LinearNF4(Linear4bit):
+    """The 4-bit NormalFloat layer (bnb.nf4)."""
+    fmt = "nf4"
+
+
+class LinearFP4(Linear4bit):
+    """The 4-bit floating-point (E2M1) layer (bnb.fp4)."""
+    fmt = "fp4"

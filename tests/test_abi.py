@@ -9,6 +9,7 @@ import ctypes
 import math
 import os
 
+import numpy as np
 import pytest
 
 from int8_quantized_linear_i8lt_gb300 import _lib
@@ -30,7 +31,7 @@ def test_exports_every_declared_function(L):
 
 
 def test_version_and_strings(L):
-    assert _lib.i8lt_abi_version() == 2
+    assert _lib.i8lt_abi_version() == 3
     for code in range(10):
         assert _lib.i8lt_status_string(code) != "unknown status"
     assert _lib.i8lt_status_string(42) == "unknown status"
@@ -186,6 +187,14 @@ def test_nf4_sizes_and_levels(L):
     st, lv = _lib.i8lt_nf4_levels()
     assert st == _lib.I8LT_OK and len(lv) == 16 and lv[0] == -1.0 and lv[7] == 0.0 and lv[15] == 1.0
     assert all(a < b for a, b in zip(lv, lv[1:]))
+    # FP4 (E2M1 / 6), by sign-magnitude code; the same host-side computation
+    st, lv = _lib.i8lt_fp4_levels()
+    assert st == _lib.I8LT_OK and lv[0] == 0.0 and lv[7] == 1.0 and lv[6] == np.float32(4.0 / 6.0)
+    assert lv[8:] == [-v for v in lv[:8]] and math.copysign(1.0, lv[8]) == -1.0
+    assert all(a < b for a, b in zip(lv[:8], lv[1:8]))
+    # grad_bias partial sums of the 4-bit input gradient: 128-token chunks x N fp32, 256-byte aligned
+    assert _lib.i8lt_nf4_grad_bias_bytes(300, 64) == 3 * 64 * 4
+    assert _lib.i8lt_nf4_grad_bias_bytes(1, 10) == 256 and _lib.i8lt_nf4_grad_bias_bytes(-1, 10) == 0
 
 
 def nf4(which, **kw):
@@ -196,7 +205,7 @@ def nf4(which, **kw):
         return _lib.i8lt_nf4_forward(a["X"], a["xt"], a["M"], a["K"], a["packed"], a["absmax"], a["N"], a["bias"],
                                      a["bt"], a["out"], a["ws"], a["ws_bytes"])
     return _lib.i8lt_nf4_backward_input(a["X"], a["xt"], a["M"], a["N"], a["packed"], a["absmax"], a["K"], a["out"],
-                                        a["ws"], a["ws_bytes"])
+                                        a.get("gb"), a["bt"], a["ws"], a["ws_bytes"])
 
 
 @pytest.mark.parametrize("which", ["fwd", "bwd"])
@@ -215,6 +224,17 @@ def test_nf4_argument_errors(L, which):
     assert nf4(which, ws_bytes=255) == _lib.I8LT_ERR_WORKSPACE
     if which == "fwd":
         assert nf4(which, bias=FAKE, bt=9) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    else:
+        assert nf4(which, gb=FAKE, bt=9) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+        # grad_bias needs room for its partial sums after the status word
+        assert nf4(which, gb=FAKE, bt=1, ws_bytes=256) == _lib.I8LT_ERR_WORKSPACE
+        assert nf4(which, out=None, gb=None) == _lib.I8LT_ERR_INVALID_ARG   # nothing asked for
+        for fn in (_lib.i8lt_fp4_backward_input,):
+            assert fn(FAKE, 2, 64, 64, FAKE, FAKE, 64, FAKE, None, 0, FAKE, 256) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert _lib.i8lt_fp4_forward(FAKE, 1, 64, 100, FAKE, FAKE, 64, None, 0, FAKE, FAKE, 256) == \
+        _lib.I8LT_ERR_INVALID_ARG
+    assert _lib.i8lt_fp4_quantize(FAKE, 5, 4, 4, FAKE, FAKE) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
+    assert _lib.i8lt_fp4_dequantize(FAKE, FAKE, 4, 4, FAKE, 3) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
     assert _lib.i8lt_nf4_quantize(FAKE, 5, 4, 4, FAKE, FAKE) == _lib.I8LT_ERR_UNSUPPORTED_DTYPE
     assert _lib.i8lt_nf4_quantize(FAKE, 0, 4, 4, FAKE + 4, FAKE) == _lib.I8LT_ERR_MISALIGNED
     assert _lib.i8lt_nf4_quantize(FAKE, 0, 4, 0, FAKE, FAKE) == _lib.I8LT_OK    # nothing to do
