@@ -429,6 +429,149 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+class ShardLayer:
+    """One rank's share of a layer of a token-sharded batch: the weight is the
+    same on every rank (drawn from the layer's seed), the rank holds rows
+    [r0, r0 + M_r) of the batch's activations and grad_output (drawn from the
+    rank's own seed: the same recipe and shapes)."""
+
+    def __init__(self, wl, li, seed, rank, world, device):
+        import dataclasses
+
+        import int8_quantized_linear_i8lt_gb300 as I
+        spec = wl.layers[li]
+        M_r = spec.M // world + (1 if rank < spec.M % world else 0)
+        self.spec = dataclasses.replace(spec, M=M_r)
+        self.full_M = spec.M
+        s = self.spec
+        wdt = wl.w_dtype or spec.dtype
+        torch.manual_seed(seed * 1000 + li)                     # the weight: same on every rank
+        Wf = (torch.randn(s.N, s.K, device=device) * s.w_std).to(wdt)
+        self.CB, self.SCB = I.quantize_weight(Wf)
+        del Wf
+        self.bias = (torch.randn(s.N, device=device) * (s.bias_std or 0.0)).to(wdt)
+        torch.manual_seed(seed * 1000 + li + 7919 * (rank + 1))  # this rank's rows
+        A = torch.randn(M_r, s.K, device=device, dtype=torch.float32)
+        heavy = W.heavy_columns(s.K, s.heavy_frac, seed + li * W.OFF_LAYER2 + W.OFF_HEAVY).to(device)
+        if len(heavy):
+            A[:, heavy] *= s.heavy_factor
+        self.A = A.to(s.dtype)
+        del A
+        self.G = torch.randn(M_r, s.N, device=device).to(s.dtype)
+        self.cap = I.default_max_outliers(s.K)
+        self.out = torch.empty(M_r, s.N, dtype=s.dtype, device=device)
+        self.ws_f = I.functional.forward_workspace(M_r, s.K, s.N, self.cap, device)
+        self.colmax = I.functional.colmax_region(self.ws_f, M_r, s.K, s.N, s.threshold)
+        self.ws_b = I.functional.backward_workspace(M_r, s.N, s.dtype, device)
+        self.grad_A = torch.empty(M_r, s.K, dtype=s.dtype, device=device)
+        self.grad_bias = torch.empty(s.N, dtype=wdt, device=device)
+
+    def ops(self):
+        s = self.spec
+        return 4.0 * s.M * s.N * s.K
+
+
+def _launch_sharded_layer(L, stream, merge, ev=None):
+    """One rank's share of a layer: column maxima of its rows, the exchange
+    (``merge``: an all-reduce MAX of the K maxima, or nothing on one rank),
+    the rest of the forward, then the backward to the input and the bias."""
+    from int8_quantized_linear_i8lt_gb300 import _lib
+    from int8_quantized_linear_i8lt_gb300.functional import DTYPE_CODE
+    s = L.spec
+    dt, bt, sp = DTYPE_CODE[s.dtype], DTYPE_CODE[L.bias.dtype], stream.cuda_stream
+    st = _lib.i8lt_forward_colmax(L.A.data_ptr(), dt, s.M, s.K, s.N, L.ws_f.data_ptr(), L.ws_f.numel(), L.cap,
+                                  stream=sp)
+    assert st == 0, _lib.i8lt_status_string(st)
+    if ev is not None:
+        ev[0].record(stream)
+    merge(L.colmax)
+    if ev is not None:
+        ev[1].record(stream)
+    st = _lib.i8lt_forward_from_colmax(L.A.data_ptr(), dt, s.M, s.K, L.CB.data_ptr(), L.SCB.data_ptr(), s.N,
+                                       L.bias.data_ptr(), bt, s.threshold, None, L.out.data_ptr(), L.ws_f.data_ptr(),
+                                       L.ws_f.numel(), L.cap, stream=sp)
+    assert st == 0, _lib.i8lt_status_string(st)
+    st = _lib.i8lt_backward_input(L.G.data_ptr(), dt, s.M, s.N, L.CB.data_ptr(), L.SCB.data_ptr(), s.K, None,
+                                  L.grad_A.data_ptr(), L.grad_bias.data_ptr(), bt, L.ws_b.data_ptr(), L.ws_b.numel(),
+                                  sp)
+    assert st == 0, _lib.i8lt_status_string(st)
+
+
+def run_sharded(args):
+    """``--shard tokens``: one batch of the workload split over the ranks by
+    tokens (strong scaling).  The outlier columns are a property of the whole
+    batch, so every layer's forward exchanges its K column maxima with one
+    all-reduce MAX between the column-maxima pass and the rest; after that
+    every row is independent.  On one rank the exchange is empty and the
+    output equals the unsharded forward bit for bit (checked here)."""
+    import int8_quantized_linear_i8lt_gb300 as I
+    from int8_quantized_linear_i8lt_gb300 import _lib
+    _lib.load()
+    world, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        merge = I.functional.allreduce_colmax()
+    else:
+        merge = lambda t: None  # noqa: E731  (one rank: its maxima are the batch's)
+    wl = W.WORKLOADS[args.workload]
+    layers = [ShardLayer(wl, li, 1234, rank, world, device) for li in range(len(wl.layers))]
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        for L in layers:
+            _launch_sharded_layer(L, stream, merge)
+    torch.cuda.synchronize()
+    identical = None
+    if world == 1:
+        identical = True
+        for L in layers:
+            ref, _ = I.forward(L.A, L.CB, L.SCB, L.spec.K, L.bias, L.spec.threshold, max_outliers=L.cap)
+            identical = identical and bool(torch.equal(ref.view(torch.uint8), L.out.view(torch.uint8)))
+            del ref
+    barrier()
+    torch.cuda.synchronize()
+    ex_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in layers]
+             for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for k in range(args.steps):
+            for L, ev in zip(layers, ex_ev[k]):
+                _launch_sharded_layer(L, stream, merge, ev)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = reduce_max(ev0.elapsed_time(ev1), device)
+    ex_ms = reduce_max(sum(a.elapsed_time(b) for step in ex_ev for a, b in step), device)
+    units = reduce_sum(sum(L.ops() for L in layers) * args.steps, device)
+    value = units / (ms_total * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None,
+        "dtype": "int8 codes (exact fp16 on tcgen05 kind::f16, int32 sums) + f16",
+        "data": "synthetic (seeded N(0,1) activations with heavy outlier columns, N(0,std) weights)",
+        "config": {"workload": wl.name, "layers": [[s.M, s.K, s.N, str(s.dtype).replace("torch.", "")]
+                                                   for s in wl.layers],
+                   "rows_per_rank": [L.spec.M for L in layers], "threshold": wl.layers[0].threshold,
+                   "l2": "inputs larger than L2 (126 MB); no flush", "parallelism": f"tokens sharded x{world}"},
+        "exchange": {"what": "all-reduce MAX of each layer's K column maxima (int32), between the column-maxima "
+                             "pass and the rest of the forward",
+                     "ms_per_step": round(ex_ms / args.steps, 4), "share": round(ex_ms / ms_total, 5),
+                     "bytes_per_step": sum(4 * L.spec.K for L in layers)},
+        "bit_identical_to_unsharded": identical,
+        "e2e": None,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def measure_int8_peak(device, n=8192, iters=10):
     """The int8 tensor rate of this GPU as the CUDA libraries reach it
     (torch._int_mm, cuBLASLt int8 x int8 -> int32, n^3).  sm_103a offers no
@@ -914,6 +1057,9 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--bwd-schedule", default="fused", choices=["fused", "materialized"],
                     help="backward schedule of the timed steps (the other one is timed beside it)")
+    ap.add_argument("--shard", default="none", choices=["none", "tokens"],
+                    help="tokens: one batch split over the ranks by tokens, with the column-maxima all-reduce "
+                         "(strong scaling); none: every rank runs its own replica (weak scaling)")
     ap.add_argument("--nf4-only", action="store_true",
                     help="time only the NF4 weight-only layers (qlora_mlp_7b_nf4) and print their line")
     args = ap.parse_args(argv)
@@ -923,6 +1069,8 @@ def main(argv=None):
         run_nf4_only(args)
     elif args.impl == "reference":
         run_reference(args)
+    elif args.shard == "tokens":
+        run_sharded(args)
     else:
         run_ours(args)
 

@@ -54,3 +54,16 @@ def test_cuda_arm_line():
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     assert d["per_layer"] and d["per_layer"][0]["fwd_tops"] > 0
     assert d["cuda_graph"]["ms_per_step"] > 0 and d["nf4_weight_only"]["value"] > 0
+
+
+@pytest.mark.gpu
+def test_token_sharded_mode_line():
+    """--shard tokens at one rank: the colmax / all-reduce / from-colmax
+    forward gives the unsharded forward's bits, and the line reports the
+    exchange."""
+    d = _run(["--shard", "tokens", "--workload", "linear_4096", "--steps", "3", "--warmup", "3"], timeout=600)
+    assert {"metric", "value", "unit", "n_gpus", "steps", "ms_per_step", "scaling", "config"} <= set(d)
+    assert d["scaling"] == "strong" and d["n_gpus"] == 1 and d["value"] > 0
+    assert d["bit_identical_to_unsharded"] is True
+    assert d["config"]["rows_per_rank"] == [2048]
+    assert d["exchange"]["bytes_per_step"] == 4 * 4096 and 0 <= d["exchange"]["share"] < 0.05
