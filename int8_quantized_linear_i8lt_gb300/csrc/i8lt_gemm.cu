@@ -266,6 +266,26 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
   tn = local / gm;
 }
 
+// Tile t of the kernels with kTileTokens-token pair tiles (the fused
+// backward and the 4-bit matmuls, 512 tokens).  The grouped raster's tiles
+// [0, full) run whole; the remaining raster tiles, which would leave most
+// pairs idle in the last round, run as two 256-token halves each: tiles
+// full + 2 j and full + 2 j + 1 are the halves of raster tile full + j.
+// Returns the tile's raster coordinates, its first token and its number of
+// 256-token sub-tiles (1 or kTileTokens / 256).
+template <int kTileTokens>
+__device__ __forceinline__ void split_tile(int t, int full, int num_m, int num_k, int group, int& tm, int& tk,
+                                           int& m_base, int& nsub) {
+  int r = t, half = -1;
+  if (t >= full) {
+    r = full + ((t - full) >> 1);
+    half = (t - full) & 1;
+  }
+  tile_coords(r, num_m, num_k, group, tm, tk);
+  m_base = tm * kTileTokens + (half > 0 ? kTileTokens / 2 : 0);
+  nsub = half >= 0 ? 1 : kTileTokens / 256;
+}
+
 __device__ __forceinline__ void init_barriers(Barriers* bars, int epi_warps) {
   for (int s = 0; s < kMaxStages; ++s) {
     mbar_init(&bars->full[s], 1);
@@ -795,7 +815,8 @@ __device__ __forceinline__ void bias_chunk_sums(const T* __restrict__ G, int M, 
 // G16) and the converter, weight-producer and relay warps stay idle.
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
-    bwd_gemm_kernel(const __grid_constant__ BwdGemmArgs g, const BwdEpiArgs e, int num_k, int num_m, int group) {
+    bwd_gemm_kernel(const __grid_constant__ BwdGemmArgs g, const BwdEpiArgs e, int num_k, int num_m, int group,
+                    int split) {
   using Geo = BwdGeom<kMode>;
   constexpr bool kFused = Geo::kFused;
   extern __shared__ uint8_t smem_raw[];
@@ -807,8 +828,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const int cid = static_cast<int>(cluster_id_x()), ncl = static_cast<int>(num_clusters_x());
-  const int num_tiles = num_k * num_m;
+  // `split` raster tiles at the end run as two 256-token halves each
+  // (split_tile): num_tiles counts the tiles as run
+  const int full_tiles = num_k * num_m - split;
+  const int num_tiles = full_tiles + 2 * split;
   const int NB = (e.N + kBK - 1) / kBK;   // reduction blocks over n
+  auto tile_of = [&](int t, int& tm, int& tk, int& m_base, int& nsub) {
+    split_tile<Geo::kTileTokens>(t, full_tiles, num_m, num_k, group, tm, tk, m_base, nsub);
+  };
 
   if (threadIdx.x == 0) init_barriers(bars, kBwdEpiWarps);
   __shared__ float lv_s[16];   // 4-bit modes: the code levels
@@ -835,22 +862,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl) {
-        int tm, tk;
-        tile_coords(t, num_m, num_k, group, tm, tk);
-        const int m_cta = tm * Geo::kTileTokens + static_cast<int>(rank) * kCtaRows;
+        int tm, tk, m_base, nsub;
+        tile_of(t, tm, tk, m_base, nsub);
+        const int m_cta = m_base + static_cast<int>(rank) * kCtaRows;
         const int k_cta = tk * kPairM + static_cast<int>(rank) * kCtaRows;
         for (int b = 0; b < NB; ++b, ++it) {
           const int s = it % Geo::kStages;
           const uint32_t ph = (it / Geo::kStages) & 1;
           if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
           // the even CTA expects both CTAs' bytes of this stage
-          if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], 2 * (kFused ? Geo::kSub : 2) * kOpBytes);
+          if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], 2 * (kFused ? nsub : 2) * kOpBytes);
           const uint32_t full_s = full0 + static_cast<uint32_t>(s) * 8u;
           uint8_t* st_base = smem + s * Geo::kStageBytes;
           if (!kFused) tma_load_2d_pair(st_base, &g.tmWT, b * kBK, k_cta, full_s);   // WdqT[k:+128][n:+64]
 #pragma unroll
           for (int u = 0; u < Geo::kSub; ++u)   // G16[m:+128][n:+64] of token sub-tile u
-            tma_load_2d_pair(st_base + (1 + u) * kOpBytes, &g.tmG, b * kBK, m_cta + u * kPairN, full_s);
+            if (u < nsub) tma_load_2d_pair(st_base + (1 + u) * kOpBytes, &g.tmG, b * kBK, m_cta + u * kPairN, full_s);
         }
       }
       if (rank == 0)
@@ -876,8 +903,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl) {
-        int tm, tk;
-        tile_coords(t, num_m, num_k, group, tm, tk);
+        int tm, tk, m_base, nsub;
+        tile_of(t, tm, tk, m_base, nsub);
         for (int b = 0; b < NB; ++b, ++it) {
           const int j = it % kI8Stages;
           const uint32_t ph = (it / kI8Stages) & 1;
@@ -894,8 +921,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
             tp += ncl;
           }
           if (tp < num_tiles) {
-            int tmp, tkp;
-            tile_coords(tp, num_m, num_k, group, tmp, tkp);
+            int tmp, tkp, mbp, nsp;
+            tile_of(tp, tmp, tkp, mbp, nsp);
             ring_xy(tkp, bp, x, y);
             tma_prefetch_l2_2d(&g.tmW, x, y);
           }
@@ -913,6 +940,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       int it = 0, tl = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl, ++tl) {
+        int tm, tk, m_base, nsub;
+        tile_of(t, tm, tk, m_base, nsub);
         const int buf = tl % Geo::kAccBufs;
         const int use = tl / Geo::kAccBufs;
         if (use > 0 && !mbar_wait_cluster(&bars->acc_empty[buf], (use - 1) & 1, abort_flag, e.st, kWhereMMA)) {
@@ -937,6 +966,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
                                           : make_sdesc(a_base + k * 32, 16, 1024, kSwizzle128B);
 #pragma unroll
             for (int u = 0; u < Geo::kSub; ++u) {   // token sub-tile u -> accumulator columns [256 u, 256 u + 256)
+              if (u >= nsub) break;
               const uint64_t bd = make_sdesc(a_base + (1 + u) * kOpBytes + k * 32, 16, 1024, kSwizzle128B);
               umma_f16_pair(d + static_cast<uint32_t>(u) * 256u, ad, bd, idesc, (b > 0 || k > 0) ? 1u : 0u);
             }
@@ -1052,8 +1082,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       constexpr int kRowBytes = kMode == kModeNf4T ? 64 : 32;
       // first output row of this CTA in tile t
       auto cta_row0 = [&](int t) {
-        int tm, tk;
-        tile_coords(t, num_m, num_k, group, tm, tk);
+        int tm, tk, m_base, nsub;
+        tile_of(t, tm, tk, m_base, nsub);
         return tk * kPairM + static_cast<int>(rank) * kCtaRows;
       };
       // the absmax values of stage b of a tile whose CTA rows start at r_cta
@@ -1139,18 +1169,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ---- epilogue: lanes = this CTA's 128 output features k, columns = the
-    // tile's tokens (column c of the accumulator is token tm * kTileTokens + c).
+    // tile's tokens (column c of the accumulator is token m_base + c).
     // Warps 10-13 take the first half of the columns, warps 18-21 the second.
     const int quad = warp & 3;
-    constexpr int kHalf = Geo::kTileTokens / 2;
-    const int col0 = warp >= kBwdWarpEpi1 ? kHalf : 0;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t acc_empty_pair[2] = {mapa_shared(&bars->acc_empty[0], 0), mapa_shared(&bars->acc_empty[1], 0)};
     const int ew = (warp >= kBwdWarpEpi1 ? 4 : 0) + quad;   // epilogue warp 0..7
     int tl = 0;
     for (int t = cid; t < num_tiles; t += ncl, ++tl) {
-      int tm, tk;
-      tile_coords(t, num_m, num_k, group, tm, tk);
+      int tm, tk, m_base, nsub;
+      tile_of(t, tm, tk, m_base, nsub);
+      const int half_w = nsub * (kPairN / 2);              // this warp's columns
+      const int col0 = warp >= kBwdWarpEpi1 ? half_w : 0;
       const int buf = tl % Geo::kAccBufs;
       if (e.partial != nullptr) {
         // while the tensor cores run this tile: the grad_bias partial sums of
@@ -1159,9 +1189,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
         // tile), one (chunk, block) item per warp in turn
         int item = 0;
         for (int b = tk; b < NB; b += num_k) {
-#pragma unroll
-          for (int u = 0; u < Geo::kSub; ++u, ++item) {
-            const int c = (tm * Geo::kTileTokens + u * kPairN) / kBiasChunkRows + static_cast<int>(rank);
+          for (int u = 0; u < nsub; ++u, ++item) {
+            const int c = (m_base + u * kPairN) / kBiasChunkRows + static_cast<int>(rank);
             if (item % kBwdEpiWarps != ew || c * kBiasChunkRows >= e.M) continue;
             if (e.gsum_dt == DT_BF16)
               bias_chunk_sums(static_cast<const __nv_bfloat16*>(e.gsum), e.M, e.N, c, b * kBK, e.partial, lane);
@@ -1176,7 +1205,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const int64_t kk = static_cast<int64_t>(tk) * kPairM + static_cast<int64_t>(rank) * kCtaRows + quad * 32 + lane;
       const uint32_t d = tmem + static_cast<uint32_t>(buf) * 256u + lane_off + static_cast<uint32_t>(col0);
-      const int m0 = tm * Geo::kTileTokens + col0;
+      const int m0 = m_base + col0;
       auto store = [&](const uint32_t(&x)[16], int gc) {
         if (kk < e.K) {
           switch (e.dt) {
@@ -1191,11 +1220,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       tmem_ld16_nowait(d, xa);
       tmem_ld_wait_tie16(xa, xb);
 #pragma unroll 1
-      for (int gc = 0; gc < kHalf; gc += 32) {
+      for (int gc = 0; gc < half_w; gc += 32) {
         tmem_ld16_nowait(d + gc + 16, xb);
         store(xa, gc);
         tmem_ld_wait_tie16(xa, xb);
-        if (gc + 32 < kHalf) tmem_ld16_nowait(d + gc + 32, xa);
+        if (gc + 32 < half_w) tmem_ld16_nowait(d + gc + 32, xa);
         store(xb, gc + 16);
         tmem_ld_wait_tie16(xa, xb);
         __syncwarp();
@@ -1457,6 +1486,15 @@ cudaError_t launch_fwd_gemm(const FwdGemmArgs& g, const FwdEpiArgs& e, cudaStrea
   return e.act != nullptr ? launch_fwd_variant<true>(g, e, s, prof_id) : launch_fwd_variant<false>(g, e, s, prof_id);
 }
 
+// Raster tiles of the 512-token schedules to run as two 256-token halves:
+// the R = tiles % pairs tiles of an incomplete last round, when their 2 R
+// halves fit in one round (then that round takes half as long); with fewer
+// tiles than pairs, every tile when the halves fit.
+int tail_split(int tiles, int pairs) {
+  const int r = tiles >= pairs ? tiles % pairs : tiles;
+  return (r > 0 && 2 * r <= pairs) ? r : 0;
+}
+
 template <int kMode>
 cudaError_t launch_bwd_schedule(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaStream_t s, int prof_id) {
   using Geo = BwdGeom<kMode>;
@@ -1466,10 +1504,12 @@ cudaError_t launch_bwd_schedule(const BwdGemmArgs& g, const BwdEpiArgs& e, cudaS
   const void* fn = reinterpret_cast<const void*>(bwd_gemm_kernel<kMode>);
   if (!ensure_smem_attr(fn, Geo::kSmemBytes)) return cudaGetLastError();
   const int tiles = num_k * num_m;
-  const int clusters = std::min(tiles, resident_pairs(fn, kBwdThreads, Geo::kSmemBytes, g_pairs_bwd[kMode]));
+  const int pairs = resident_pairs(fn, kBwdThreads, Geo::kSmemBytes, g_pairs_bwd[kMode]);
+  const int split = Geo::kSub == 2 ? tail_split(tiles, pairs) : 0;
+  const int clusters = std::min(tiles + split, pairs);
   const int group = std::min(num_m, 8);
   ProfScope ps(prof_id, s);
-  bwd_gemm_kernel<kMode><<<2 * clusters, kBwdThreads, Geo::kSmemBytes, s>>>(g, e, num_k, num_m, group);
+  bwd_gemm_kernel<kMode><<<2 * clusters, kBwdThreads, Geo::kSmemBytes, s>>>(g, e, num_k, num_m, group, split);
   return cudaGetLastError();
 }
 
