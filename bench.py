@@ -233,6 +233,19 @@ def kernel_flops(L, name):
     return 2.0 * s.M * s.N * s.K if name in ("fwd_gemm", "bwd_gemm") else 0.0
 
 
+def fused_quantize(spec) -> bool:
+    """Whether the forward quantizes the activations in one launch (column
+    maxima, outlier set and row quantization: 16-bit A, K a multiple of 8,
+    rows up to 32768 columns), as the library decides."""
+    kp = (spec.K + 15) // 16 * 16
+    return spec.dtype in (torch.float16, torch.bfloat16) and spec.K % 8 == 0 and kp <= 32768
+
+
+def _threshold_on(spec) -> bool:
+    import math
+    return math.isfinite(spec.threshold) and spec.threshold > 0
+
+
 def kernel_bytes(L, name):
     """Algorithmic HBM bytes of one launch of a memory-bound kernel."""
     s = L.spec
@@ -240,10 +253,13 @@ def kernel_bytes(L, name):
     cnt = getattr(L, "found", 0)
     cap_pad = (min(cnt, s.K) + 63) // 64 * 64
     kp = (s.K + 15) // 16 * 16
+    # the one-launch activation quantization reads A twice (the column maxima
+    # must be complete before any row's scale) when the outliers are on
+    reads = 2 if (fused_quantize(s) and _threshold_on(s)) else 1
     return {
         "colmax": s.M * s.K * a + s.K * 4,
         # the codes count as int8, one byte each, whatever form the kernel stores
-        "row_quantize": s.M * s.K * a + s.M * kp + s.M * 4 + s.M * cap_pad * 2,
+        "row_quantize": reads * s.M * s.K * a + s.M * kp + s.M * 4 + s.M * cap_pad * 2,
         "gradout_prepass": s.M * s.N * a,
         "build_subB": s.N * cap_pad * 3,
         "widen_codes": s.N * kp * 3,
@@ -611,14 +627,20 @@ def _layer_of(i, layers, materialized=False):
 
 
 def launches_per_layer(L, materialized=False) -> int:
-    """Our kernels per layer and step: colmax, outlier index (outliers on),
-    row quantize, subB (outliers on), weight-code widening, accumulation
-    plan, forward GEMM; then (weight dequantization when materialized,) the
+    """Our kernels per layer and step: the activation quantization (one
+    launch for 16-bit rows of a multiple of 8 columns, else colmax and the
+    outlier index (outliers on) and row quantize), subB (outliers on),
+    weight-code widening, accumulation plan, forward GEMM; then (weight
+    dequantization when materialized,) the
     backward GEMM and the grad_bias finalize -- with a grad_output prepass
     first when G is not fp16 with N a multiple of 8 (the GEMM reads fp16 G
     as it is and reduces grad_bias from it itself)."""
-    import math
-    fwd = 7 if (math.isfinite(L.spec.threshold) and L.spec.threshold > 0) else 4
+    if _threshold_on(L.spec):
+        # column maxima + outlier index + row quantization, or the one launch
+        # that does all three; subB; widening; plan; GEMM
+        fwd = 5 if fused_quantize(L.spec) else 7
+    else:
+        fwd = 4
     prepass = 0 if (L.spec.dtype == torch.float16 and L.spec.N % 8 == 0) else 1
     return fwd + 2 + prepass + (1 if materialized else 0)
 

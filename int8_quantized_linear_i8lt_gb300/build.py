@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libi8lt.so")
 
-SOURCES = ("i8lt_api.cu", "i8lt_quant.cu", "i8lt_gemm.cu", "i8lt_noalloc.cu", "i8lt_nf4.cu")
+SOURCES = ("i8lt_api.cu", "i8lt_quant.cu", "i8lt_gemm.cu", "i8lt_noalloc.cu", "i8lt_nf4.cu", "i8lt_actquant.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-Xcompiler", "-ffp-contract=off",   # host arithmetic rounds each operation (same on x86 and Arm)

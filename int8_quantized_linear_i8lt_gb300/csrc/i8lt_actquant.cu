@@ -1,0 +1,405 @@
+// Fused activation quantization of the forward (K2 + K3 in one launch):
+// outlier-column detection and row-wise (vector-wise) absmax int8
+// quantization of a 16-bit activation A [M, K] (bitsandbytes PR #33 "Memory
+// efficient backward": the double_quant of the cast fp16 input with its
+// coo_tensorA of outlier columns, and the "Mixed-precision decomposition
+// matmul" review thread for the outlier rule).
+//
+// One cooperative persistent launch.  Block b owns the contiguous rows
+// [M b / nb, M (b + 1) / nb); thread t owns the 8-column groups t + i NT
+// (i < G) of every row, so that it keeps the same columns through all phases:
+//   phase 1  column maxima of |fp16(A)| over the block's rows, kept in
+//            registers as packed 16-bit magnitudes, then one max reduction per
+//            column into colmax (fp16 magnitudes order as integers);
+//   --       a bounded grid-wide wait (all blocks co-resident by the
+//            cooperative launch) that records ST_TIMEOUT when it runs out;
+//   phase 2  every block reads the finished column maxima of its columns and
+//            derives the outlier mask (max > threshold, strictly) and, by an
+//            ordered block scan over (i, t) -- column order --, the ascending
+//            position of each outlier column in subA; block 0 also writes the
+//            global mask, idx and outlier counts for the later kernels;
+//   phase 3  the block's rows in reverse order (the rows phase 1 read last
+//            are the likeliest to be still in L2): each row is held in
+//            registers (one HBM read), its absmax outside the outlier columns
+//            is reduced over the block, and the codes rint(fp32(A16) * (127 /
+//            absmax)) (IEEE fp32 divide and multiply, round half to even) are
+//            stored as exact fp16 integers with the outlier columns at 0; the
+//            outlier columns' fp16 values go to subA; the per-1024-column sums
+//            of squared codes raise the row tile's asq entries.
+// The same arithmetic as colmax_kernel + outlier_index_kernel +
+// row_quantize_bulk_kernel (i8lt_quant.cu), so the results are bit-identical.
+// Used for 16-bit A with K a multiple of 8 (16-byte rows); the other inputs
+// take the separate kernels.
+#include <algorithm>
+#include <type_traits>
+
+#include "i8lt_internal.h"
+
+namespace i8lt {
+
+namespace {
+
+constexpr int kWhereActQuant = 7;   // status `where` of a timed-out grid-wide wait
+
+struct ActQuantArgs {
+  const void* A;         // [M, K] fp16 or bf16, K % 8 == 0, 16-byte aligned
+  int64_t M;
+  int K, k_pad;          // k_pad = round_up(K, 16): the leading dimension of Aq
+  float thr;             // outlier threshold (used when `enabled`)
+  int enabled;           // outlier decomposition on
+  int do_colmax;         // phase 1: this call's rows' column maxima into colmax (zeroed)
+  int do_quant;          // phases 2 and 3
+  int64_t cap, cap_pad;  // outlier capacity and the leading dimension of subA
+  int nch;               // 1024-column chunks of a code row (asq's second dimension)
+  uint32_t* colmax;      // [K]
+  uint32_t* mask;        // [ceil(K / 32)]
+  int* idx;              // [cap_pad]
+  DevStatus* st;
+  unsigned* arrive;      // grid-wide wait counter (zeroed)
+  float* SCA;            // [M]
+  __half* Aq;            // [M, k_pad]
+  __half* subA;          // [M, cap_pad]
+  uint32_t* asq;         // [ceil(M / 256), nch]
+};
+
+// 8 elements (16 bytes) as fp16 values in a uint4; bf16 cast to fp16 (RNE).
+template <typename T>
+__device__ __forceinline__ uint4 to_half8(uint4 v) {
+  if constexpr (std::is_same<T, __half>::value) {
+    return v;
+  } else {
+    const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&v);
+    uint4 o;
+    __half* h = reinterpret_cast<__half*>(&o);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) h[j] = to_half(b[j]);
+    return o;
+  }
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Every block of the grid arrives once; returns false (after recording
+// ST_TIMEOUT) when the others have not all arrived within the time limit.
+__device__ bool grid_wait(unsigned* arrive, unsigned nblocks, DevStatus* st) {
+  __shared__ int ok_s;
+  __threadfence();   // this thread's column-maxima reductions, before the arrival
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(arrive, 1u);
+    int ok = 1;
+    const unsigned long long t0 = global_ns();
+    while (ld_acquire_gpu(arrive) < nblocks) {
+      __nanosleep(256);
+      if (global_ns() - t0 > kWaitTimeoutNs) {
+        set_status(st, ST_TIMEOUT, kWhereActQuant);
+        ok = 0;
+        break;
+      }
+    }
+    __threadfence();
+    ok_s = ok;
+  }
+  __syncthreads();
+  return ok_s != 0;
+}
+
+// Exclusive prefix sum of v over the block (threads in order) and the total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int& total, int* warp_s) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_s[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int x = lane < nw ? warp_s[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane < nw) warp_s[lane] = x;   // inclusive over warps
+  }
+  __syncthreads();
+  const int before = w > 0 ? warp_s[w - 1] : 0;
+  total = warp_s[nw - 1];
+  __syncthreads();   // warp_s is reused by the next scan
+  return before + incl - v;
+}
+
+template <typename T, int G, int NT>
+__global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs a) {
+  __shared__ float red_s[2][32];
+  __shared__ int chunk_s[2][64];
+  __shared__ int warp_s[32];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  constexpr int kWarps = NT / 32;
+  const int ng = a.K / 8;            // 8-column groups holding data
+  const int ng_pad = a.k_pad / 8;    // groups of a code row (with the zero padding)
+  const int64_t r0 = a.M * blockIdx.x / gridDim.x, r1 = a.M * (blockIdx.x + 1) / gridDim.x;
+  const T* A = static_cast<const T*>(a.A);
+  auto load_row = [&](int64_t r, uint4 (&v)[G]) {
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const int gi = t + i * NT;
+      v[i] = gi < ng ? __ldg(reinterpret_cast<const uint4*>(A + r * a.K) + gi) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+
+  // ---- phase 1: column maxima of this block's rows
+  if (a.do_colmax) {
+    uint32_t cm[G][4];
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cm[i][j] = 0u;
+    uint4 nxt[G];
+    if (r0 < r1) load_row(r0, nxt);
+    for (int64_t r = r0; r < r1; ++r) {
+      uint4 cur[G];
+#pragma unroll
+      for (int i = 0; i < G; ++i) cur[i] = nxt[i];
+      if (r + 1 < r1) load_row(r + 1, nxt);
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const uint4 h = to_half8<T>(cur[i]);
+        cm[i][0] = __vmaxu2(cm[i][0], h.x & 0x7FFF7FFFu);
+        cm[i][1] = __vmaxu2(cm[i][1], h.y & 0x7FFF7FFFu);
+        cm[i][2] = __vmaxu2(cm[i][2], h.z & 0x7FFF7FFFu);
+        cm[i][3] = __vmaxu2(cm[i][3], h.w & 0x7FFF7FFFu);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const int gi = t + i * NT;
+      if (gi >= ng) continue;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t v = (cm[i][j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+        if (v != 0u) atomicMax(a.colmax + 8 * gi + j, v);
+      }
+    }
+    if (!a.do_quant) return;
+    if (!grid_wait(a.arrive, gridDim.x, a.st)) return;
+  }
+
+  // ---- phase 2: the outlier columns among this thread's columns and their
+  // ascending positions in subA (the same in every block)
+  uint32_t mb[G];   // bit j: column 8 gi + j is an outlier
+  int jb[G];        // position in subA of the first outlier column of group i
+  int used = 0;
+#pragma unroll
+  for (int i = 0; i < G; ++i) mb[i] = 0u;
+  if (a.enabled) {
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const int gi = t + i * NT;
+      if (gi < ng) {
+        const uint4 c0 = __ldcg(reinterpret_cast<const uint4*>(a.colmax + 8 * gi));
+        const uint4 c1 = __ldcg(reinterpret_cast<const uint4*>(a.colmax + 8 * gi) + 1);
+        const uint32_t cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (__half2float(__ushort_as_half(static_cast<unsigned short>(cv[j]))) > a.thr) mb[i] |= 1u << j;
+      }
+    }
+    int base = 0;
+#pragma unroll
+    for (int i = 0; i < G; ++i) {   // column order: group i of every thread, then group i + 1
+      int total;
+      jb[i] = base + block_exclusive_scan(__popc(mb[i]), total, warp_s);
+      base += total;
+    }
+    used = static_cast<int>(min(static_cast<int64_t>(base), a.cap));
+    if (blockIdx.x == 0) {
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const int gi = t + i * NT;
+        // four consecutive groups make one 32-bit mask word (NT % 4 == 0)
+        const uint32_t m1 = __shfl_down_sync(0xffffffffu, mb[i], 1);
+        const uint32_t m2 = __shfl_down_sync(0xffffffffu, mb[i], 2);
+        const uint32_t m3 = __shfl_down_sync(0xffffffffu, mb[i], 3);
+        if ((t & 3) == 0 && gi < ng) a.mask[gi >> 2] = mb[i] | (m1 << 8) | (m2 << 16) | (m3 << 24);
+        uint32_t bits = mb[i];
+        int j = jb[i];
+        while (bits) {
+          const int b = __ffs(bits) - 1;
+          bits &= bits - 1;
+          if (j < a.cap) a.idx[j] = 8 * gi + b;
+          ++j;
+        }
+      }
+      if (t == 0) {
+        a.st->found = base;
+        a.st->used = used;
+        if (base > a.cap) set_status(a.st, ST_OUTLIER_CAPACITY, 0);
+      }
+    }
+  }
+  const int used_pad = (used + 63) / 64 * 64;
+
+  // ---- phase 3: the rows, in reverse order, held in registers
+  if (t < 64) {
+    chunk_s[0][t] = 0;
+    chunk_s[1][t] = 0;
+  }
+  __syncthreads();
+  uint4 nxt[G];
+  if (r0 < r1) load_row(r1 - 1, nxt);
+  int par = 0;
+  int64_t prev = -1;
+  for (int64_t r = r1 - 1; r >= r0; --r, par ^= 1) {
+    uint4 h[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) h[i] = to_half8<T>(nxt[i]);
+    if (r > r0) load_row(r - 1, nxt);
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const __half* x = reinterpret_cast<const __half*>(&h[i]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (!((mb[i] >> j) & 1u)) amax = fmaxf(amax, fabsf(__half2float(x[j])));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) red_s[par][w] = amax;
+    __syncthreads();
+    // the previous row's chunk sums are complete: raise its tile's asq entries
+    if (prev >= 0 && t < a.nch) {
+      const int v = chunk_s[par ^ 1][t];
+      if (v != 0) atomicMax(a.asq + (prev >> 8) * a.nch + t, static_cast<uint32_t>(v));
+      chunk_s[par ^ 1][t] = 0;
+    }
+    amax = red_s[par][0];
+#pragma unroll
+    for (int k = 1; k < kWarps; ++k) amax = fmaxf(amax, red_s[par][k]);
+    const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const int gi = t + i * NT;
+      const __half* x = reinterpret_cast<const __half*>(&h[i]);
+      float q[8];
+      float sq = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float rr = __fsub_rn(__fadd_rn(__fmul_rn(__half2float(x[j]), s), 12582912.0f), 12582912.0f);
+        q[j] = ((mb[i] >> j) & 1u) ? 0.f : fminf(127.f, fmaxf(-127.f, rr));
+        sq += q[j] * q[j];
+      }
+      if (gi < ng_pad) {
+        uint4 o;
+        __half2* o2 = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o2[j] = __floats2half2_rn(q[2 * j], q[2 * j + 1]);
+        *reinterpret_cast<uint4*>(a.Aq + r * a.k_pad + 8 * gi) = o;
+      }
+      // the 128 groups of a 1024-column chunk are 4 whole warps (NT % 128 == 0)
+      int v = static_cast<int>(sq);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0 && v != 0) atomicAdd(&chunk_s[par][gi >> 7], v);
+      if (mb[i] != 0u) {   // rare: the outlier columns of the group, in column order
+        int j = jb[i];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if ((mb[i] >> b) & 1u) {
+            if (j < a.cap) a.subA[r * a.cap_pad + j] = x[b];
+            ++j;
+          }
+        }
+      }
+    }
+    for (int j = used + t; j < used_pad; j += NT) a.subA[r * a.cap_pad + j] = __float2half_rn(0.f);
+    if (t == 0) a.SCA[r] = amax;
+    prev = r;
+  }
+  __syncthreads();
+  if (prev >= 0 && t < a.nch) {
+    const int v = chunk_s[par ^ 1][t];
+    if (v != 0) atomicMax(a.asq + (prev >> 8) * a.nch + t, static_cast<uint32_t>(v));
+  }
+}
+
+// Blocks of NT threads, G groups each: the smallest configuration that covers
+// the row (NT 256 up to 16384 columns, else 1024).
+template <typename T, int G, int NT>
+cudaError_t launch_cfg(const ActQuantArgs& a, bool cooperative, int sms, cudaStream_t s) {
+  const void* fn = reinterpret_cast<const void*>(act_quant_fused_kernel<T, G, NT>);
+  const int per_sm = std::min(cached_blocks_per_sm(fn, NT, 0), NT == 256 ? 2 : 1);
+  const int nb = static_cast<int>(std::min<int64_t>(a.M, static_cast<int64_t>(sms) * per_sm));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(nb), 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = cooperative ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, act_quant_fused_kernel<T, G, NT>, a);
+}
+
+template <typename T>
+cudaError_t launch_typed(const ActQuantArgs& a, bool cooperative, int sms, cudaStream_t s) {
+  const int groups = a.k_pad / 8;
+  if (groups <= 256 * 2) return launch_cfg<T, 2, 256>(a, cooperative, sms, s);
+  if (groups <= 256 * 4) return launch_cfg<T, 4, 256>(a, cooperative, sms, s);
+  if (groups <= 256 * 8) return launch_cfg<T, 8, 256>(a, cooperative, sms, s);
+  return launch_cfg<T, 4, 1024>(a, cooperative, sms, s);
+}
+
+}  // namespace
+
+// Rows up to 32768 columns (one block of 1024 threads, 4 groups of 8 each);
+// longer rows take the separate kernels.
+bool act_quant_fused_supported(int at, int64_t K) {
+  return (at == DT_F16 || at == DT_BF16) && K > 0 && K % 8 == 0 && round_up(K, 16) <= 1024 * 4 * 8;
+}
+
+cudaError_t launch_act_quant_fused(const void* A, int at, int64_t M, int64_t K, int64_t k_pad, bool enabled,
+                                   float thr, bool do_colmax, bool do_quant, int64_t cap, int64_t cap_pad,
+                                   uint32_t* colmax, uint32_t* mask, int* idx, DevStatus* st, unsigned* arrive,
+                                   float* SCA, __half* Aq, __half* subA, uint32_t* asq, cudaStream_t s) {
+  if (M == 0 || !(do_colmax || do_quant)) return cudaSuccess;
+  ActQuantArgs a;
+  a.A = A;
+  a.M = M;
+  a.K = static_cast<int>(K);
+  a.k_pad = static_cast<int>(k_pad);
+  a.thr = thr;
+  a.enabled = enabled ? 1 : 0;
+  a.do_colmax = do_colmax ? 1 : 0;
+  a.do_quant = do_quant ? 1 : 0;
+  a.cap = cap;
+  a.cap_pad = cap_pad;
+  a.nch = static_cast<int>(ceil_div(k_pad, 1024));
+  a.colmax = colmax;
+  a.mask = mask;
+  a.idx = idx;
+  a.st = st;
+  a.arrive = arrive;
+  a.SCA = SCA;
+  a.Aq = Aq;
+  a.subA = subA;
+  a.asq = asq;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool cooperative = do_colmax && do_quant;   // the grid-wide wait needs every block resident
+  ProfScope ps(do_quant ? K_ROW_QUANTIZE : K_COLMAX, s);
+  return at == DT_BF16 ? launch_typed<__nv_bfloat16>(a, cooperative, sms, s)
+                       : launch_typed<__half>(a, cooperative, sms, s);
+}
+
+}  // namespace i8lt

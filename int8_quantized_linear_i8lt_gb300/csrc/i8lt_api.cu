@@ -273,22 +273,34 @@ int forward_impl(FwdMode mode, const void* A, int at, int64_t M, int64_t K, cons
   const bool enabled = threshold_enabled(threshold);
   const bool vec = (K % 8) == 0;
 
-  // one memset clears the status word of this call, the chunk maxima of the
-  // accumulation plan and (unless they are given) the column maxima
-  const bool own_colmax = enabled && mode != kFwdFromColmax;
+  // one memset clears the status word of this call (with the grid-wide wait
+  // counter after it), the chunk maxima of the accumulation plan and (unless
+  // they are given) the column maxima
+  const bool own_colmax = (enabled || colmax_only) && mode != kFwdFromColmax;
   const size_t clear = own_colmax ? L.colmax + static_cast<size_t>(K) * 4 : L.colmax;
   if ((cudaMemsetAsync(w, 0, clear, s)) != cudaSuccess) return I8LT_ERR_CUDA;
-  if (own_colmax && M > 0) {
-    if ((launch_colmax(A, at, M, K, vec, colmax, s)) != cudaSuccess) return I8LT_ERR_CUDA;
-  }
-  if (colmax_only) return I8LT_OK;
-  if (enabled) {
-    if ((launch_outlier_index(colmax, K, threshold, max_outliers, idx, mask, st, s)) != cudaSuccess)
+  if (act_quant_fused_supported(at, K)) {
+    // 16-bit A, 16-byte rows: column maxima, outlier set and row quantization
+    // in one launch
+    unsigned* arrive = reinterpret_cast<unsigned*>(w + L.status + 64);
+    if (launch_act_quant_fused(A, at, M, K, L.k_pad, enabled, threshold, own_colmax && M > 0, !colmax_only,
+                               max_outliers, L.cap_pad, colmax, mask, idx, st, arrive, SCA, Aq,
+                               enabled ? subA : nullptr, asq, s) != cudaSuccess)
+      return I8LT_ERR_CUDA;
+    if (colmax_only) return I8LT_OK;
+  } else {
+    if (own_colmax && M > 0) {
+      if ((launch_colmax(A, at, M, K, vec, colmax, s)) != cudaSuccess) return I8LT_ERR_CUDA;
+    }
+    if (colmax_only) return I8LT_OK;
+    if (enabled) {
+      if ((launch_outlier_index(colmax, K, threshold, max_outliers, idx, mask, st, s)) != cudaSuccess)
+        return I8LT_ERR_CUDA;
+    }
+    if ((launch_row_quantize(A, at, M, K, L.k_pad, vec, enabled ? mask : nullptr, idx, st, L.cap_pad, SCA, Aq,
+                             enabled ? subA : nullptr, asq, s)) != cudaSuccess)
       return I8LT_ERR_CUDA;
   }
-  if ((launch_row_quantize(A, at, M, K, L.k_pad, vec, enabled ? mask : nullptr, idx, st, L.cap_pad, SCA, Aq,
-                               enabled ? subA : nullptr, asq, s)) != cudaSuccess)
-    return I8LT_ERR_CUDA;
   const bool with_outliers = enabled && L.cap_pad > 0;
   if (with_outliers) {
     if ((launch_build_subB(CB, L.k_pad, SCB, N, idx, st, L.cap_pad, subB, s)) != cudaSuccess)
