@@ -60,6 +60,7 @@ struct ActQuantArgs {
   __half* Aq;            // [M, k_pad]
   __half* subA;          // [M, cap_pad]
   uint32_t* asq;         // [ceil(M / 256), nch]
+  int nbuf;              // rows in the shared-memory ring
 };
 
 // 8 elements (16 bytes) as fp16 values in a uint4; bf16 cast to fp16 (RNE).
@@ -136,8 +137,13 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int& total, int* warp
   return before + incl - v;
 }
 
+constexpr int kMaxBufs = 8;   // rows in the shared-memory ring
+
 template <typename T, int G, int NT>
 __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs a) {
+  extern __shared__ __align__(128) uint8_t ring[];   // a.nbuf row buffers of K 16-bit elements
+  __shared__ __align__(8) uint64_t full[kMaxBufs];
+  __shared__ int abort_flag;
   __shared__ float red_s[2][32];
   __shared__ int chunk_s[2][64];
   __shared__ int warp_s[32];
@@ -146,14 +152,55 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
   const int ng = a.K / 8;            // 8-column groups holding data
   const int ng_pad = a.k_pad / 8;    // groups of a code row (with the zero padding)
   const int64_t r0 = a.M * blockIdx.x / gridDim.x, r1 = a.M * (blockIdx.x + 1) / gridDim.x;
+  const int64_t nrows = r1 - r0;
   const T* A = static_cast<const T*>(a.A);
-  auto load_row = [&](int64_t r, uint4 (&v)[G]) {
+  const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;
+  const int nbuf = a.nbuf;
+  volatile int* abort_p = &abort_flag;
+  if (t == 0) {
+    for (int b = 0; b < nbuf; ++b) mbar_init(&full[b], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (t < 64) {
+    chunk_s[0][t] = 0;
+    chunk_s[1][t] = 0;
+  }
+  __syncthreads();
+
+  // Rows stream through the ring of shared-memory buffers by bulk copies
+  // (thread 0 issues them, nbuf rows ahead); the u-th row streamed by this
+  // block goes to buffer u % nbuf.  Phase 1 streams rows r0, r0 + 1, ...,
+  // phase 3 rows r1 - 1, r1 - 2, ... (u keeps counting across the phases).
+  auto issue = [&](int64_t u, int64_t r) {
+    const int b = static_cast<int>(u % nbuf);
+    fence_proxy_async_smem();   // the buffer's last readers are past a block barrier
+    mbar_arrive_expect_tx(&full[b], row_bytes);
+    bulk_load(ring + static_cast<size_t>(b) * row_bytes, A + r * a.K, row_bytes, &full[b]);
+  };
+  // wait for stream row u and copy this thread's groups of it into registers
+  auto fetch = [&](int64_t u, uint4 (&v)[G]) -> bool {
+    const int b = static_cast<int>(u % nbuf);
+    const bool ok = mbar_wait(&full[b], static_cast<uint32_t>((u / nbuf) & 1), abort_p, a.st, kWhereActQuant);
+    const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(b) * row_bytes);
 #pragma unroll
     for (int i = 0; i < G; ++i) {
       const int gi = t + i * NT;
-      v[i] = gi < ng ? __ldg(reinterpret_cast<const uint4*>(A + r * a.K) + gi) : make_uint4(0u, 0u, 0u, 0u);
+      v[i] = gi < ng ? to_half8<T>(src[gi]) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    return ok;
+  };
+  // after a timeout at stream row u_fail: let the copies issued and not yet
+  // consumed (rows u_fail .. u_issued - 1) land, each wait bounded, before
+  // the block leaves
+  auto drain = [&](int64_t u_fail, int64_t u_issued) {
+    if (t == 0) {
+      *abort_p = 0;
+      for (int64_t v = u_fail; v < u_issued; ++v)
+        mbar_wait(&full[v % nbuf], static_cast<uint32_t>((v / nbuf) & 1), abort_p, nullptr, 0);
     }
   };
+  int64_t u = 0;   // rows streamed so far
 
   // ---- phase 1: column maxima of this block's rows
   if (a.do_colmax) {
@@ -162,22 +209,25 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
     for (int i = 0; i < G; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) cm[i][j] = 0u;
-    uint4 nxt[G];
-    if (r0 < r1) load_row(r0, nxt);
-    for (int64_t r = r0; r < r1; ++r) {
-      uint4 cur[G];
-#pragma unroll
-      for (int i = 0; i < G; ++i) cur[i] = nxt[i];
-      if (r + 1 < r1) load_row(r + 1, nxt);
+    if (t == 0)
+      for (int64_t k = 0; k < nrows && k < nbuf; ++k) issue(u + k, r0 + k);
+    for (int64_t k = 0; k < nrows; ++k) {
+      uint4 h[G];
+      const bool ok = fetch(u + k, h);
+      if (!__syncthreads_and(ok)) {   // every thread read its groups: the buffer is free
+        drain(u + k, u + std::min<int64_t>(nrows, k + nbuf));
+        return;
+      }
+      if (t == 0 && k + nbuf < nrows) issue(u + k + nbuf, r0 + k + nbuf);
 #pragma unroll
       for (int i = 0; i < G; ++i) {
-        const uint4 h = to_half8<T>(cur[i]);
-        cm[i][0] = __vmaxu2(cm[i][0], h.x & 0x7FFF7FFFu);
-        cm[i][1] = __vmaxu2(cm[i][1], h.y & 0x7FFF7FFFu);
-        cm[i][2] = __vmaxu2(cm[i][2], h.z & 0x7FFF7FFFu);
-        cm[i][3] = __vmaxu2(cm[i][3], h.w & 0x7FFF7FFFu);
+        cm[i][0] = __vmaxu2(cm[i][0], h[i].x & 0x7FFF7FFFu);
+        cm[i][1] = __vmaxu2(cm[i][1], h[i].y & 0x7FFF7FFFu);
+        cm[i][2] = __vmaxu2(cm[i][2], h[i].z & 0x7FFF7FFFu);
+        cm[i][3] = __vmaxu2(cm[i][3], h[i].w & 0x7FFF7FFFu);
       }
     }
+    u += nrows;
 #pragma unroll
     for (int i = 0; i < G; ++i) {
       const int gi = t + i * NT;
@@ -198,7 +248,10 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
   int jb[G];        // position in subA of the first outlier column of group i
   int used = 0;
 #pragma unroll
-  for (int i = 0; i < G; ++i) mb[i] = 0u;
+  for (int i = 0; i < G; ++i) {
+    mb[i] = 0u;
+    jb[i] = 0;
+  }
   if (a.enabled) {
 #pragma unroll
     for (int i = 0; i < G; ++i) {
@@ -229,13 +282,13 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
         const uint32_t m2 = __shfl_down_sync(0xffffffffu, mb[i], 2);
         const uint32_t m3 = __shfl_down_sync(0xffffffffu, mb[i], 3);
         if ((t & 3) == 0 && gi < ng) a.mask[gi >> 2] = mb[i] | (m1 << 8) | (m2 << 16) | (m3 << 24);
-        uint32_t bits = mb[i];
         int j = jb[i];
-        while (bits) {
-          const int b = __ffs(bits) - 1;
-          bits &= bits - 1;
-          if (j < a.cap) a.idx[j] = 8 * gi + b;
-          ++j;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if ((mb[i] >> b) & 1u) {
+            if (j < a.cap) a.idx[j] = 8 * gi + b;
+            ++j;
+          }
         }
       }
       if (t == 0) {
@@ -247,21 +300,15 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
   }
   const int used_pad = (used + 63) / 64 * 64;
 
-  // ---- phase 3: the rows, in reverse order, held in registers
-  if (t < 64) {
-    chunk_s[0][t] = 0;
-    chunk_s[1][t] = 0;
-  }
-  __syncthreads();
-  uint4 nxt[G];
-  if (r0 < r1) load_row(r1 - 1, nxt);
+  // ---- phase 3: the rows in reverse order (those phase 1 read last first)
+  if (t == 0)
+    for (int64_t k = 0; k < nrows && k < nbuf; ++k) issue(u + k, r1 - 1 - k);
   int par = 0;
   int64_t prev = -1;
-  for (int64_t r = r1 - 1; r >= r0; --r, par ^= 1) {
+  for (int64_t k = 0; k < nrows; ++k, par ^= 1) {
+    const int64_t r = r1 - 1 - k;
     uint4 h[G];
-#pragma unroll
-    for (int i = 0; i < G; ++i) h[i] = to_half8<T>(nxt[i]);
-    if (r > r0) load_row(r - 1, nxt);
+    const bool ok = fetch(u + k, h);
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < G; ++i) {
@@ -273,16 +320,21 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if (lane == 0) red_s[par][w] = amax;
-    __syncthreads();
+    // every thread has read its groups of the buffer and published its warp maximum
+    if (!__syncthreads_and(ok)) {
+      drain(u + k, u + std::min<int64_t>(nrows, k + nbuf));
+      return;
+    }
+    if (t == 0 && k + nbuf < nrows) issue(u + k + nbuf, r1 - 1 - (k + nbuf));
     // the previous row's chunk sums are complete: raise its tile's asq entries
     if (prev >= 0 && t < a.nch) {
       const int v = chunk_s[par ^ 1][t];
       if (v != 0) atomicMax(a.asq + (prev >> 8) * a.nch + t, static_cast<uint32_t>(v));
       chunk_s[par ^ 1][t] = 0;
     }
-    amax = red_s[par][0];
+    amax = lane < kWarps ? red_s[par][lane] : 0.f;
 #pragma unroll
-    for (int k = 1; k < kWarps; ++k) amax = fmaxf(amax, red_s[par][k]);
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
 #pragma unroll
     for (int i = 0; i < G; ++i) {
@@ -331,16 +383,25 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
 }
 
 // Blocks of NT threads, G groups each: the smallest configuration that covers
-// the row (NT 256 up to 16384 columns, else 1024).
+// the row (NT 256 up to 16384 columns, else 1024).  Two blocks per SM for the
+// 256-thread configurations, one for 1024; the ring takes what shared memory
+// the blocks of an SM leave, 2 to kMaxBufs rows.
+constexpr int kRingBudget = 200 * 1024;
+
 template <typename T, int G, int NT>
-cudaError_t launch_cfg(const ActQuantArgs& a, bool cooperative, int sms, cudaStream_t s) {
+cudaError_t launch_cfg(ActQuantArgs a, bool cooperative, int sms, cudaStream_t s) {
   const void* fn = reinterpret_cast<const void*>(act_quant_fused_kernel<T, G, NT>);
-  const int per_sm = std::min(cached_blocks_per_sm(fn, NT, 0), NT == 256 ? 2 : 1);
+  const int target = NT == 256 ? 2 : 1;
+  const int64_t row_bytes = static_cast<int64_t>(a.K) * 2;
+  a.nbuf = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(kMaxBufs, kRingBudget / target / row_bytes)));
+  const int smem = static_cast<int>(a.nbuf * row_bytes);
+  if (!ensure_smem_attr(fn, kRingBudget)) return cudaGetLastError();
+  const int per_sm = std::max(1, std::min(cached_blocks_per_sm(fn, NT, smem), target));
   const int nb = static_cast<int>(std::min<int64_t>(a.M, static_cast<int64_t>(sms) * per_sm));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nb), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

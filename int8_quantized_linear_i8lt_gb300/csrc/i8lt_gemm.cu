@@ -1025,7 +1025,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
           const uint8_t* src = i8_ring + j8 * kI8Bytes;
           uint4 v[2];
 #pragma unroll
-          for (int j = 0; j < 2; ++j) v[j] = *reinterpret_cast<const uint4*>(src + (nl0 + 32 * j) * 128 + ((q ^ r) << 4));
+          for (int j = 0; j < 2; ++j) v[j] = ld_shared_v4(src + (nl0 + 32 * j) * 128 + ((q ^ r) << 4));
           // the operand slot is free once the pair's MMAs of its previous use completed
           if (!__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereCvt))) {
             go = false;
@@ -1044,8 +1044,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
             i8x4_scale_to_h4(v[j].z, negc2, f2, o1.x, o1.y);
             i8x4_scale_to_h4(v[j].w, negc2, f2, o1.z, o1.w);
             uint8_t* rowp = sa + i * 2048 + ja * 1024 + r * 128;
-            *reinterpret_cast<uint4*>(rowp + ((c0 ^ r) << 4)) = o0;
-            *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ r) << 4)) = o1;
+            st_shared_v4(rowp + ((c0 ^ r) << 4), o0);
+            st_shared_v4(rowp + (((c0 + 1) ^ r) << 4), o1);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -1130,7 +1130,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
           const uint8_t* src = i8_ring + j8 * Geo::kRingBytes;
           uint2 v[2];
 #pragma unroll
-          for (int j = 0; j < 2; ++j) v[j] = *reinterpret_cast<const uint2*>(src + row[j] * kRowBytes + seg * 8);
+          for (int j = 0; j < 2; ++j) v[j] = ld_shared_v2(src + row[j] * kRowBytes + seg * 8);
           if (!__all_sync(0xffffffffu, mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereCvt))) {
             go = false;
             break;
@@ -1155,8 +1155,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
               rowp = sa + (row[j] >> 3) * 1024 + r * 128;
               c0 = seg * 2;
             }
-            *reinterpret_cast<uint4*>(rowp + ((c0 ^ r) << 4)) = o0;
-            *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ r) << 4)) = o1;
+            st_shared_v4(rowp + ((c0 ^ r) << 4), o0);
+            st_shared_v4(rowp + (((c0 + 1) ^ r) << 4), o1);
           }
           fence_proxy_async_smem();
           __syncwarp();
