@@ -84,9 +84,10 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
-// Every block of the grid arrives once; returns false (after recording
-// ST_TIMEOUT) when the others have not all arrived within the time limit.
-__device__ bool grid_wait(unsigned* arrive, unsigned nblocks, DevStatus* st) {
+// Every block of the grid arrives once per wait; returns false (after
+// recording ST_TIMEOUT) when the counter has not reached `target` (the
+// blocks times the waits so far) within the time limit.
+__device__ bool grid_wait(unsigned* arrive, unsigned target, DevStatus* st) {
   __shared__ int ok_s;
   __threadfence();   // this thread's column-maxima reductions, before the arrival
   __syncthreads();
@@ -95,7 +96,7 @@ __device__ bool grid_wait(unsigned* arrive, unsigned nblocks, DevStatus* st) {
     atomicAdd(arrive, 1u);
     int ok = 1;
     const unsigned long long t0 = global_ns();
-    while (ld_acquire_gpu(arrive) < nblocks) {
+    while (ld_acquire_gpu(arrive) < target) {
       __nanosleep(256);
       if (global_ns() - t0 > kWaitTimeoutNs) {
         set_status(st, ST_TIMEOUT, kWhereActQuant);
@@ -228,18 +229,53 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
       }
     }
     u += nrows;
+    if (!a.do_quant) {
+      // the column maxima of this call's rows only (no grid-wide wait): one
+      // max reduction per column into colmax
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const int gi = t + i * NT;
+        if (gi >= ng) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t v = (cm[i][j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+          if (v != 0u) atomicMax(a.colmax + 8 * gi + j, v);
+        }
+      }
+      return;
+    }
+    // Two-level reduction, with no two blocks reducing into one address at
+    // once: every block stores its partial maxima (8 packed 16-bit values a
+    // group) as row b of a scratch in the Aq region (written only in phase
+    // 3); after the wait, block b reduces the groups [g0, g1) over all the
+    // partial rows in shared memory and stores the final column maxima.
+    uint4* part = reinterpret_cast<uint4*>(a.Aq);   // [gridDim.x, ng]: M * k_pad >= gridDim.x * K
 #pragma unroll
     for (int i = 0; i < G; ++i) {
       const int gi = t + i * NT;
-      if (gi >= ng) continue;
+      if (gi < ng) part[static_cast<int64_t>(blockIdx.x) * ng + gi] = make_uint4(cm[i][0], cm[i][1], cm[i][2], cm[i][3]);
+    }
+    if (!grid_wait(a.arrive, gridDim.x, a.st)) return;
+    const int g0 = static_cast<int>(static_cast<int64_t>(ng) * blockIdx.x / gridDim.x);
+    const int g1 = static_cast<int>(static_cast<int64_t>(ng) * (blockIdx.x + 1) / gridDim.x);
+    const int S = g1 - g0;
+    uint32_t* colm_s = reinterpret_cast<uint32_t*>(ring);   // 8 S values (the ring holds >= 2 K halves)
+    for (int x = t; x < 8 * S; x += NT) colm_s[x] = 0u;
+    __syncthreads();
+    const int nparts = static_cast<int>(gridDim.x);
+    for (int x = t; x < S * nparts; x += NT) {
+      const int p = x / S, gl = x - p * S;
+      const uint4 v = __ldcg(part + static_cast<int64_t>(p) * ng + g0 + gl);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint32_t v = (cm[i][j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-        if (v != 0u) atomicMax(a.colmax + 8 * gi + j, v);
+        const uint32_t m = (w4[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+        if (m != 0u) atomicMax(colm_s + 8 * gl + j, m);
       }
     }
-    if (!a.do_quant) return;
-    if (!grid_wait(a.arrive, gridDim.x, a.st)) return;
+    __syncthreads();
+    for (int x = t; x < 8 * S; x += NT) a.colmax[8 * g0 + x] = colm_s[x];
+    if (!grid_wait(a.arrive, 2 * gridDim.x, a.st)) return;
   }
 
   // ---- phase 2: the outlier columns among this thread's columns and their
@@ -309,14 +345,24 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
     const int64_t r = r1 - 1 - k;
     uint4 h[G];
     const bool ok = fetch(u + k, h);
+    // the row's absmax outside the outlier columns: packed fp16 maxima of
+    // magnitudes (exact) for groups without outlier columns
+    __half2 m2 = __float2half2_rn(0.f);
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < G; ++i) {
-      const __half* x = reinterpret_cast<const __half*>(&h[i]);
+      if (mb[i] == 0u) {
+        const __half2* x2 = reinterpret_cast<const __half2*>(&h[i]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (!((mb[i] >> j) & 1u)) amax = fmaxf(amax, fabsf(__half2float(x[j])));
+        for (int j = 0; j < 4; ++j) m2 = __hmax2(m2, __habs2(x2[j]));
+      } else {
+        const __half* x = reinterpret_cast<const __half*>(&h[i]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (!((mb[i] >> j) & 1u)) amax = fmaxf(amax, fabsf(__half2float(x[j])));
+      }
     }
+    amax = fmaxf(amax, fmaxf(__low2float(m2), __high2float(m2)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if (lane == 0) red_s[par][w] = amax;
@@ -340,13 +386,23 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
     for (int i = 0; i < G; ++i) {
       const int gi = t + i * NT;
       const __half* x = reinterpret_cast<const __half*>(&h[i]);
+      // q = rint(x * s), round half to even by the exact add of 1.5 * 2^23;
+      // |x| <= absmax outside the outlier columns, so |x * s| <= 127 (1 +
+      // 2^-23) and no clamp is needed
       float q[8];
       float sq = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float rr = __fsub_rn(__fadd_rn(__fmul_rn(__half2float(x[j]), s), 12582912.0f), 12582912.0f);
-        q[j] = ((mb[i] >> j) & 1u) ? 0.f : fminf(127.f, fmaxf(-127.f, rr));
-        sq += q[j] * q[j];
+        q[j] = __fsub_rn(__fadd_rn(__fmul_rn(__half2float(x[j]), s), 12582912.0f), 12582912.0f);
+        sq = __fmaf_rn(q[j], q[j], sq);
+      }
+      if (mb[i] != 0u) {
+        sq = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if ((mb[i] >> j) & 1u) q[j] = 0.f;
+          sq = __fmaf_rn(q[j], q[j], sq);
+        }
       }
       if (gi < ng_pad) {
         uint4 o;
