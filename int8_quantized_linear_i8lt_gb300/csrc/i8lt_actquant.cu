@@ -5,31 +5,37 @@
 // coo_tensorA of outlier columns, and the "Mixed-precision decomposition
 // matmul" review thread for the outlier rule).
 //
-// One cooperative persistent launch.  Block b owns the contiguous rows
-// [M b / nb, M (b + 1) / nb); thread t owns the 8-column groups t + i NT
-// (i < G) of every row, so that it keeps the same columns through all phases:
-//   phase 1  column maxima of |fp16(A)| over the block's rows, kept in
-//            registers as packed 16-bit magnitudes, then one max reduction per
-//            column into colmax (fp16 magnitudes order as integers);
-//   --       a bounded grid-wide wait (all blocks co-resident by the
-//            cooperative launch) that records ST_TIMEOUT when it runs out;
-//   phase 2  every block reads the finished column maxima of its columns and
-//            derives the outlier mask (max > threshold, strictly) and, by an
-//            ordered block scan over (i, t) -- column order --, the ascending
-//            position of each outlier column in subA; block 0 also writes the
-//            global mask, idx and outlier counts for the later kernels;
-//   phase 3  the block's rows in reverse order (the rows phase 1 read last
-//            are the likeliest to be still in L2): each row is held in
-//            registers (one HBM read), its absmax outside the outlier columns
-//            is reduced over the block, and the codes rint(fp32(A16) * (127 /
-//            absmax)) (IEEE fp32 divide and multiply, round half to even) are
-//            stored as exact fp16 integers with the outlier columns at 0; the
-//            outlier columns' fp16 values go to subA; the per-1024-column sums
-//            of squared codes raise the row tile's asq entries.
+// One persistent launch (cooperative when it computes the column maxima).
+// Block b owns the contiguous rows [M b / nb, M (b + 1) / nb); thread t owns
+// the 8-column groups t + i NT (i < G) of every row, so that it keeps the same
+// columns through all phases.  Rows stream through a ring of shared-memory
+// buffers filled by bulk copies, several rows ahead, and every thread copies
+// its groups of a row into registers once.
+//   phase 1  column maxima of |fp16(A)| over the block's rows, in registers as
+//            packed 16-bit magnitudes (fp16 magnitudes order as integers);
+//            then a two-level reduction that never has two blocks reducing
+//            into one address at once: each block stores its partial maxima
+//            as one row of a scratch (the code region, written only in phase
+//            3), a bounded grid-wide wait, block b reduces the columns of its
+//            slice over all partial rows in shared memory and stores the final
+//            maxima, a second bounded grid-wide wait (every block resident by
+//            the cooperative launch; a wait that runs out records ST_TIMEOUT);
+//   phase 2  every block reads the column maxima of its columns and derives
+//            the outlier mask (max > threshold, strictly) and, by an ordered
+//            block scan over (i, t) -- column order --, the ascending position
+//            of each outlier column in subA; block 0 also writes the global
+//            mask, idx and outlier counts for the later kernels;
+//   phase 3  the block's rows in reverse order (the rows phase 1 read last are
+//            the likeliest to be still in L2): the absmax outside the outlier
+//            columns reduced over the block, then the codes rint(fp32(A16) *
+//            (127 / absmax)) (IEEE fp32 divide and multiply, round half to
+//            even) stored as exact fp16 integers with the outlier columns at
+//            0; the outlier columns' fp16 values go to subA; the per-1024-column
+//            sums of squared codes raise the row tile's asq entries.
 // The same arithmetic as colmax_kernel + outlier_index_kernel +
 // row_quantize_bulk_kernel (i8lt_quant.cu), so the results are bit-identical.
-// Used for 16-bit A with K a multiple of 8 (16-byte rows); the other inputs
-// take the separate kernels.
+// Used for 16-bit A with K a multiple of 8 up to 32768 (16-byte rows that fit
+// the ring); the other inputs take the separate kernels.
 #include <algorithm>
 #include <type_traits>
 
@@ -47,8 +53,7 @@ struct ActQuantArgs {
   int K, k_pad;          // k_pad = round_up(K, 16): the leading dimension of Aq
   float thr;             // outlier threshold (used when `enabled`)
   int enabled;           // outlier decomposition on
-  int do_colmax;         // phase 1: this call's rows' column maxima into colmax (zeroed)
-  int do_quant;          // phases 2 and 3
+  int do_colmax;         // phase 1: the column maxima of A's rows into colmax (zeroed)
   int64_t cap, cap_pad;  // outlier capacity and the leading dimension of subA
   int nch;               // 1024-column chunks of a code row (asq's second dimension)
   uint32_t* colmax;      // [K]
@@ -229,21 +234,6 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
       }
     }
     u += nrows;
-    if (!a.do_quant) {
-      // the column maxima of this call's rows only (no grid-wide wait): one
-      // max reduction per column into colmax
-#pragma unroll
-      for (int i = 0; i < G; ++i) {
-        const int gi = t + i * NT;
-        if (gi >= ng) continue;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t v = (cm[i][j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-          if (v != 0u) atomicMax(a.colmax + 8 * gi + j, v);
-        }
-      }
-      return;
-    }
     // Two-level reduction, with no two blocks reducing into one address at
     // once: every block stores its partial maxima (8 packed 16-bit values a
     // group) as row b of a scratch in the Aq region (written only in phase
@@ -438,16 +428,17 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
   }
 }
 
-// Blocks of NT threads, G groups each: the smallest configuration that covers
-// the row (NT 256 up to 16384 columns, else 1024).  Two blocks per SM for the
-// 256-thread configurations, one for 1024; the ring takes what shared memory
-// the blocks of an SM leave, 2 to kMaxBufs rows.
+// Blocks of NT threads, G groups each: a configuration that covers the row
+// (256 x 2 groups up to 4096 columns, 512 x 2 up to 8192, 256 x 8 up to
+// 16384, else 1024 x 4).  Two blocks per SM for the 256- and 512-thread
+// configurations, one for 1024; the ring takes what shared memory the blocks
+// of an SM leave, 2 to kMaxBufs rows.
 constexpr int kRingBudget = 200 * 1024;
 
 template <typename T, int G, int NT>
 cudaError_t launch_cfg(ActQuantArgs a, bool cooperative, int sms, cudaStream_t s) {
   const void* fn = reinterpret_cast<const void*>(act_quant_fused_kernel<T, G, NT>);
-  const int target = NT == 256 ? 2 : 1;
+  const int target = NT <= 512 ? 2 : 1;
   const int64_t row_bytes = static_cast<int64_t>(a.K) * 2;
   a.nbuf = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(kMaxBufs, kRingBudget / target / row_bytes)));
   const int smem = static_cast<int>(a.nbuf * row_bytes);
@@ -471,7 +462,7 @@ template <typename T>
 cudaError_t launch_typed(const ActQuantArgs& a, bool cooperative, int sms, cudaStream_t s) {
   const int groups = a.k_pad / 8;
   if (groups <= 256 * 2) return launch_cfg<T, 2, 256>(a, cooperative, sms, s);
-  if (groups <= 256 * 4) return launch_cfg<T, 4, 256>(a, cooperative, sms, s);
+  if (groups <= 512 * 2) return launch_cfg<T, 2, 512>(a, cooperative, sms, s);
   if (groups <= 256 * 8) return launch_cfg<T, 8, 256>(a, cooperative, sms, s);
   return launch_cfg<T, 4, 1024>(a, cooperative, sms, s);
 }
@@ -485,10 +476,10 @@ bool act_quant_fused_supported(int at, int64_t K) {
 }
 
 cudaError_t launch_act_quant_fused(const void* A, int at, int64_t M, int64_t K, int64_t k_pad, bool enabled,
-                                   float thr, bool do_colmax, bool do_quant, int64_t cap, int64_t cap_pad,
-                                   uint32_t* colmax, uint32_t* mask, int* idx, DevStatus* st, unsigned* arrive,
-                                   float* SCA, __half* Aq, __half* subA, uint32_t* asq, cudaStream_t s) {
-  if (M == 0 || !(do_colmax || do_quant)) return cudaSuccess;
+                                   float thr, bool do_colmax, int64_t cap, int64_t cap_pad, uint32_t* colmax,
+                                   uint32_t* mask, int* idx, DevStatus* st, unsigned* arrive, float* SCA,
+                                   __half* Aq, __half* subA, uint32_t* asq, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
   ActQuantArgs a;
   a.A = A;
   a.M = M;
@@ -497,7 +488,6 @@ cudaError_t launch_act_quant_fused(const void* A, int at, int64_t M, int64_t K, 
   a.thr = thr;
   a.enabled = enabled ? 1 : 0;
   a.do_colmax = do_colmax ? 1 : 0;
-  a.do_quant = do_quant ? 1 : 0;
   a.cap = cap;
   a.cap_pad = cap_pad;
   a.nch = static_cast<int>(ceil_div(k_pad, 1024));
@@ -513,8 +503,8 @@ cudaError_t launch_act_quant_fused(const void* A, int at, int64_t M, int64_t K, 
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const bool cooperative = do_colmax && do_quant;   // the grid-wide wait needs every block resident
-  ProfScope ps(do_quant ? K_ROW_QUANTIZE : K_COLMAX, s);
+  const bool cooperative = do_colmax;   // the grid-wide waits need every block resident
+  ProfScope ps(K_ROW_QUANTIZE, s);
   return at == DT_BF16 ? launch_typed<__nv_bfloat16>(a, cooperative, sms, s)
                        : launch_typed<__half>(a, cooperative, sms, s);
 }

@@ -279,15 +279,14 @@ int forward_impl(FwdMode mode, const void* A, int at, int64_t M, int64_t K, cons
   const bool own_colmax = (enabled || colmax_only) && mode != kFwdFromColmax;
   const size_t clear = own_colmax ? L.colmax + static_cast<size_t>(K) * 4 : L.colmax;
   if ((cudaMemsetAsync(w, 0, clear, s)) != cudaSuccess) return I8LT_ERR_CUDA;
-  if (act_quant_fused_supported(at, K)) {
+  if (!colmax_only && act_quant_fused_supported(at, K)) {
     // 16-bit A, 16-byte rows: column maxima, outlier set and row quantization
     // in one launch
     unsigned* arrive = reinterpret_cast<unsigned*>(w + L.status + 64);
-    if (launch_act_quant_fused(A, at, M, K, L.k_pad, enabled, threshold, own_colmax && M > 0, !colmax_only,
-                               max_outliers, L.cap_pad, colmax, mask, idx, st, arrive, SCA, Aq,
-                               enabled ? subA : nullptr, asq, s) != cudaSuccess)
+    if (launch_act_quant_fused(A, at, M, K, L.k_pad, enabled, threshold, own_colmax && M > 0, max_outliers,
+                               L.cap_pad, colmax, mask, idx, st, arrive, SCA, Aq, enabled ? subA : nullptr, asq,
+                               s) != cudaSuccess)
       return I8LT_ERR_CUDA;
-    if (colmax_only) return I8LT_OK;
   } else {
     if (own_colmax && M > 0) {
       if ((launch_colmax(A, at, M, K, vec, colmax, s)) != cudaSuccess) return I8LT_ERR_CUDA;

@@ -46,17 +46,17 @@ cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int
                                 const uint32_t* mask, const int* idx, DevStatus* st, int64_t cap_pad,
                                 float* SCA, __half* Aq, __half* subA, uint32_t* asq, cudaStream_t s);
 
-// K2 + K3 in one cooperative launch (i8lt_actquant.cu), for 16-bit A with K
-// a multiple of 8 (act_quant_fused_supported): do_colmax -- the column maxima
-// of A's rows into colmax (zeroed); do_quant -- the outlier set from colmax
-// (block 0 writes mask, idx and the counts in st), then SCA, Aq, subA and asq
-// as launch_row_quantize.  Both: one launch with a bounded grid-wide wait
-// between the phases (arrive: a zeroed counter).
+// K2 + K3 in one launch (i8lt_actquant.cu), for 16-bit A with K a multiple
+// of 8 up to 32768 (act_quant_fused_supported): with do_colmax, the column
+// maxima of A's rows into colmax (zeroed), by a cooperative launch with
+// bounded grid-wide waits (arrive: a zeroed counter); then (or from the given
+// colmax) the outlier set -- block 0 writes mask, idx and the counts in st --
+// and SCA, Aq, subA and asq as launch_row_quantize.
 bool act_quant_fused_supported(int at, int64_t K);
 cudaError_t launch_act_quant_fused(const void* A, int at, int64_t M, int64_t K, int64_t k_pad, bool enabled,
-                                   float thr, bool do_colmax, bool do_quant, int64_t cap, int64_t cap_pad,
-                                   uint32_t* colmax, uint32_t* mask, int* idx, DevStatus* st, unsigned* arrive,
-                                   float* SCA, __half* Aq, __half* subA, uint32_t* asq, cudaStream_t s);
+                                   float thr, bool do_colmax, int64_t cap, int64_t cap_pad, uint32_t* colmax,
+                                   uint32_t* mask, int* idx, DevStatus* st, unsigned* arrive, float* SCA,
+                                   __half* Aq, __half* subA, uint32_t* asq, cudaStream_t s);
 
 // Blocks of a kernel resident per SM at a given block size and dynamic shared
 // memory, cached per (kernel, device, size): no query while a stream is
