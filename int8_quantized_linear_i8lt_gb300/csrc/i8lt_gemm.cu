@@ -1244,20 +1244,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
 }
 
 // Forward prepass: CB int8 codes -> the same values as fp16 (exact).  One
-// warp per (row, 1024-column chunk): 32 bytes per lane, 16-byte loads and
-// stores; the chunk's sum of squares of the codes (dp4a) raises the row tile's
-// entry of bsq, the weight side of the accumulation plan.
+// warp per (row, 1024-column chunk): four rounds in which lane l converts the
+// 8 codes at 256 u + 8 l, so that every load (256 bytes) and every store (512
+// bytes) of the warp is contiguous; the chunk's sum of squares of the codes
+// (dp4a) raises the row tile's entry of bsq, the weight side of the
+// accumulation plan.  Two work items per iteration, all their loads first.
 __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restrict__ CB, __half* __restrict__ CBh,
                                                           int64_t N, int64_t k_pad, int nchunks,
                                                           uint32_t* __restrict__ bsq) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * 8;
   const int64_t total = N * nchunks;
-  // two work items per iteration, all four 16-byte loads issued first (the
-  // bounds are uniform over the warp, so the shuffles below are safe)
+  // the bounds are uniform over the warp, so the shuffles below are safe
   for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); w0 < total; w0 += 2 * nwarps) {
-    uint4 v[2][2];
-    int64_t n[2], k[2][2];
+    uint2 v[2][4];
+    int64_t n[2];
     int c[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -1265,11 +1266,11 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
       n[i] = w < total ? w / nchunks : 0;
       c[i] = static_cast<int>(w - n[i] * nchunks);
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        k[i][j] = static_cast<int64_t>(c[i]) * 1024 + lane * 32 + j * 16;
-        v[i][j] = (w < total && k[i][j] < k_pad)   // k_pad is a multiple of 16
-                      ? __ldg(reinterpret_cast<const uint4*>(CB + n[i] * k_pad + k[i][j]))
-                      : make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < 4; ++u) {
+        const int64_t k = static_cast<int64_t>(c[i]) * 1024 + u * 256 + lane * 8;
+        v[i][u] = (w < total && k < k_pad)   // k_pad is a multiple of 16: a group of 8 is all in or all out
+                      ? __ldg(reinterpret_cast<const uint2*>(CB + n[i] * k_pad + k))
+                      : make_uint2(0u, 0u);
       }
     }
 #pragma unroll
@@ -1277,21 +1278,16 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t* __restri
       if (w0 + i * nwarps >= total) break;
       int sq = 0;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        if (k[i][j] < k_pad) {
-          const uint4 x = v[i][j];
+      for (int u = 0; u < 4; ++u) {
+        const int64_t k = static_cast<int64_t>(c[i]) * 1024 + u * 256 + lane * 8;
+        if (k < k_pad) {
+          const uint2 x = v[i][u];
           sq = __dp4a(static_cast<int>(x.x), static_cast<int>(x.x), sq);
           sq = __dp4a(static_cast<int>(x.y), static_cast<int>(x.y), sq);
-          sq = __dp4a(static_cast<int>(x.z), static_cast<int>(x.z), sq);
-          sq = __dp4a(static_cast<int>(x.w), static_cast<int>(x.w), sq);
-          uint4 o0, o1;
-          i8x4_to_h4(x.x, o0.x, o0.y);
-          i8x4_to_h4(x.y, o0.z, o0.w);
-          i8x4_to_h4(x.z, o1.x, o1.y);
-          i8x4_to_h4(x.w, o1.z, o1.w);
-          uint4* dst = reinterpret_cast<uint4*>(CBh + n[i] * k_pad + k[i][j]);
-          dst[0] = o0;
-          dst[1] = o1;
+          uint4 o;
+          i8x4_to_h4(x.x, o.x, o.y);
+          i8x4_to_h4(x.y, o.z, o.w);
+          *reinterpret_cast<uint4*>(CBh + n[i] * k_pad + k) = o;
         }
       }
 #pragma unroll
