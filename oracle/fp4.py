@@ -28,7 +28,8 @@ Reading (every point is listed in the design notes):
 * packing, dequantization (fp32(level) * absmax, one fp32 multiply, rounded
   once to the compute dtype) and the matmuls (float64 sums here, one
   rounding of the result) are those of the NF4 option;
-* the ``fp4-dq`` variant (absmax stored in 8 bits) is not modelled.
+* the ``fp4-dq`` variant stores the absmax values in 8 bits; its encoding is
+  oracle/dq8.py, and the matmuls here take the decoded values.
 
 Parity status: pinned by ``tests/test_fp4_oracle.py`` (the levels against the
 E2M1 bit-field definition, brute-force nearest level, constructed half-way

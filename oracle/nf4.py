@@ -35,8 +35,8 @@ every point is listed in the design notes):
   the compute dtype (bf16 or fp16);
 * the matmuls multiply the compute-dtype operands exactly and sum in float64
   here; the result is rounded once to the compute dtype;
-* the ``nf4-dq`` variant (the absmax values themselves stored in 8 bits) is
-  not modelled.
+* the ``nf4-dq`` variant stores the absmax values themselves in 8 bits; its
+  encoding is oracle/dq8.py, and the matmuls here take the decoded values.
 
 Parity status: every function here is pinned by ``tests/test_nf4_oracle.py``
 (equal probability mass between levels evaluated with ``math.erf``,
