@@ -724,9 +724,18 @@ def time_nf4(stream, steps, device, warmup=3, fmt="nf4", materialized_too=True):
     ws_dq = torch.empty(max(_lib.i8lt_nf4_workspace_size_dq(s_.K, s_.N) for s_ in wl.layers), dtype=torch.uint8,
                         device=device) if materialized_too else None
 
-    def step(w):
-        for spec, A, G, packed, absmax, out, gA in lay:
+    # the double-quantized storage of each layer's absmax (the -dq option) and
+    # a buffer its decoded values go to on every step
+    dq = [(I.double_quantize_absmax(absmax), torch.empty_like(absmax)) for (_, _, _, _, absmax, _, _) in lay]
+
+    def step(w, double_quant=False):
+        for li, (spec, A, G, packed, absmax, out, gA) in enumerate(lay):
             dt = DTYPE_CODE[spec.dtype]
+            if double_quant:
+                (q, a2, off), absmax = dq[li]
+                st = _lib.i8lt_absmax8_dequantize(q.data_ptr(), a2.data_ptr(), off.data_ptr(), q.numel(),
+                                                  absmax.data_ptr(), sp)
+                assert st == 0, _lib.i8lt_status_string(st)
             st = fwd_fn(A.data_ptr(), dt, spec.M, spec.K, packed.data_ptr(), absmax.data_ptr(), spec.N,
                         None, 0, out.data_ptr(), w.data_ptr(), w.numel(), sp)
             assert st == 0, _lib.i8lt_status_string(st)
@@ -734,15 +743,15 @@ def time_nf4(stream, steps, device, warmup=3, fmt="nf4", materialized_too=True):
                         spec.K, gA.data_ptr(), None, 0, w.data_ptr(), w.numel(), sp)
             assert st == 0, _lib.i8lt_status_string(st)
 
-    def timed(w):
+    def timed(w, double_quant=False):
         for _ in range(warmup):
-            step(w)
+            step(w, double_quant)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         _lib.i8lt_profile_start(1 << 16)
         e0.record(stream)
         for _ in range(steps):
-            step(w)
+            step(w, double_quant)
         e1.record(stream)
         torch.cuda.synchronize()
         _, r, n = _lib.i8lt_profile_stop(1 << 16)
@@ -774,6 +783,12 @@ def time_nf4(stream, steps, device, warmup=3, fmt="nf4", materialized_too=True):
             if k_ms:
                 tf = half / (k_ms * 1e-3) / 1e12
                 res["materialized"][name] = {"tflops": round(tf, 1), "frac_tensor": round(tf / peak_t, 4)}
+    ms_q, recs_q, _ = timed(ws, double_quant=True)   # fused, absmax stored in 8 bits and decoded per step
+    res["double_quant"] = {"value": round(reduce_sum(flops, device) / (ms_q * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                           "ms_per_step": round(ms_q / steps, 4),
+                           "absmax8_ms_per_step": round(sum(t for n, t in recs_q if n == "absmax8") / steps, 4),
+                           "absmax_bytes_per_layer": [int(q.numel() + 4 * a2.numel() + 4)
+                                                      for ((q, a2, _), _) in dq]}
     res["peak"] = peak_t
     res["peak_source"] = f"{src} bf16 sustained"
     return res

@@ -68,7 +68,8 @@ typedef enum { I8LT_F16 = 0, I8LT_BF16 = 1, I8LT_F32 = 2 } i8lt_dtype;
 #define I8LT_MAX_K 133144
 
 /* Version of this ABI; bumped on any incompatible change (3: the 4-bit
- * input gradients take grad_bias). */
+ * input gradients take grad_bias; 4: the double-quantized absmax entry
+ * points and their kernel id, I8LT_K_COUNT = 21). */
 int i8lt_abi_version(void);
 
 /* Human-readable name of a status code (static storage). */
@@ -425,6 +426,47 @@ int i8lt_fp4_backward_input(const void* G, int gt, int64_t M, int64_t N,
                             int64_t K, void* grad_A, void* grad_bias, int bt,
                             void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Double-quantized absmax: the `bnb.nf4-dq` and `bnb.fp4-dq` options of
+ * "Support QLoRA 4-bit finetuning with bitsandbytes" (lit-gpt PR #275), which
+ * store the fp32 absmax values of the 64-element blocks in 8 bits (QLoRA's
+ * double quantization).  The page names the options without a definition;
+ * the reading:
+ *   offset   = fp32(S / count), S the sum of all `count` absmax values exactly
+ *              rounded to float64, an IEEE float64 division;
+ *   d        = fp32(c - offset) for every value c (row-major order);
+ *   absmax2  = max |d| over each block of 256 consecutive values (fp32);
+ *   q        = the FP8 E4M3 code (1 sign, 4 exponent bits with bias 7, 3
+ *              mantissa bits, subnormals, largest finite 448) nearest to
+ *              fp32(d * fp32(448 / absmax2)) (0 for a block of zeros), ties
+ *              to the even code, saturating at +-448, the sign kept;
+ *   decoded  = fp32(fp32(E4M3(q) * fp32(absmax2 * fp32(1 / 448))) + offset).
+ * The 4-bit codes are those of the plain format; the matmuls take the
+ * decoded absmax (i8lt_absmax8_dequantize writes it, fp32 [N, blocks per
+ * row], e.g. into a buffer reused across layers).  Storage: 1 byte per
+ * 64-element block plus 4 bytes per 256 blocks and 4 bytes, instead of 4
+ * bytes per block.
+ *
+ * i8lt_absmax8_blocks(count): ceil(count / 256), the length of absmax2.
+ * i8lt_absmax8_quantize: absmax [count] fp32 (finite, >= 0, as
+ *   i8lt_nf4_quantize / i8lt_fp4_quantize write them) -> q [count] u8,
+ *   absmax2 [i8lt_absmax8_blocks(count)] fp32, *offset (one fp32, device
+ *   memory); ws of i8lt_absmax8_workspace_size() bytes, 256-byte aligned
+ *   (scratch for the exact sum).  count == 0 writes offset = 0.
+ * i8lt_absmax8_dequantize: q, absmax2, offset (device) -> out [count] fp32.
+ * All pointers are device pointers owned by the caller; asynchronous on
+ * `stream`.  Errors: I8LT_ERR_INVALID_ARG (count < 0 or > 2^40, a NULL
+ * pointer), I8LT_ERR_WORKSPACE, I8LT_ERR_MISALIGNED.
+ */
+int64_t i8lt_absmax8_blocks(int64_t count);
+size_t i8lt_absmax8_workspace_size(void);
+int i8lt_absmax8_quantize(const float* absmax, int64_t count, uint8_t* q,
+                          float* absmax2, float* offset, void* ws,
+                          size_t ws_bytes, void* stream);
+int i8lt_absmax8_dequantize(const uint8_t* q, const float* absmax2,
+                            const float* offset, int64_t count, float* out,
+                            void* stream);
+
 /* SiLU between the two layers of an MLP: out = h * sigmoid(h), and its
  * backward out = g * silu'(h).  n elements of dtype dt. */
 int i8lt_silu_forward(const void* h, int dt, int64_t n, void* out, void* stream);
@@ -445,7 +487,7 @@ typedef enum {
   I8LT_K_BWD_GEMM = 8, I8LT_K_SILU = 9, I8LT_K_SILU_BACKWARD = 10, I8LT_K_WIDEN_CODES = 11,
   I8LT_K_DEQUANT_WEIGHT = 12, I8LT_K_COL_QUANTIZE = 13, I8LT_K_WGRAD_GEMM = 14, I8LT_K_UNIT_PLAN = 15,
   I8LT_K_NF4_QUANTIZE = 16, I8LT_K_NF4_DEQUANTIZE = 17, I8LT_K_NF4_GEMM_FWD = 18, I8LT_K_NF4_GEMM_BWD = 19,
-  I8LT_K_COUNT = 20
+  I8LT_K_ABSMAX8 = 20, I8LT_K_COUNT = 21
 } i8lt_kernel_id;
 typedef struct {
   int kernel;

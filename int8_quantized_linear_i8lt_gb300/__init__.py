@@ -16,7 +16,8 @@ include/i8lt.h); build it with ``python -m int8_quantized_linear_i8lt_gb300.buil
 """
 from .functional import (I8LTError, Int8LinearFunction, Int8LinearTrainableFunction, Int8MLPFunction,
                          Linear4bitFunction, NF4LinearFunction, SiLUFunction, backward_input, backward_input_4bit,
-                         default_max_outliers, dequantize_4bit, device_status, forward, forward_4bit,
+                         default_max_outliers, dequantize_4bit, dequantize_absmax, device_status,
+                         double_quantize_absmax, forward, forward_4bit,
                          fp4_backward_input, fp4_dequantize, fp4_forward, fp4_levels, fp4_quantize, grad_weight,
                          levels_4bit, nf4_backward_input, nf4_dequantize, nf4_forward, nf4_levels, nf4_quantize,
                          quantize_4bit, quantize_weight, silu, silu_backward, weight_ld)
@@ -28,4 +29,5 @@ __all__ = ["Linear8bitLt", "Linear8bitLtTrainable", "Int8MLP", "I8LTError", "Int
            "weight_ld", "Linear4bit", "LinearNF4", "LinearFP4", "Linear4bitFunction", "NF4LinearFunction",
            "levels_4bit", "quantize_4bit", "dequantize_4bit", "forward_4bit", "backward_input_4bit",
            "nf4_levels", "nf4_quantize", "nf4_dequantize", "nf4_forward", "nf4_backward_input",
-           "fp4_levels", "fp4_quantize", "fp4_dequantize", "fp4_forward", "fp4_backward_input"]
+           "fp4_levels", "fp4_quantize", "fp4_dequantize", "fp4_forward", "fp4_backward_input",
+           "double_quantize_absmax", "dequantize_absmax"]

@@ -103,6 +103,11 @@ SIGNATURES = {
                                         c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
     "i8lt_fp4_backward_input": (c_int, [c_void_p, c_int, c_int64, c_int64, c_void_p, c_void_p, c_int64, c_void_p,
                                         c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
+    "i8lt_absmax8_blocks": (c_int64, [c_int64]),
+    "i8lt_absmax8_workspace_size": (c_size_t, []),
+    "i8lt_absmax8_quantize": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                      c_void_p]),
+    "i8lt_absmax8_dequantize": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p]),
     "i8lt_silu_forward": (c_int, [c_void_p, c_int, c_int64, c_void_p, c_void_p]),
     "i8lt_silu_backward": (c_int, [c_void_p, c_void_p, c_int, c_int64, c_void_p, c_void_p]),
     "i8lt_profile_start": (c_int, [c_int]),
@@ -303,6 +308,23 @@ def i8lt_nf4_backward_input(G, gt, M, N, packed, absmax, K, grad_A, grad_bias, b
 def i8lt_fp4_backward_input(G, gt, M, N, packed, absmax, K, grad_A, grad_bias, bt, ws, ws_bytes, stream=None) -> int:
     return load().i8lt_fp4_backward_input(_p(G), gt, M, N, _p(packed), _p(absmax), K, _p(grad_A), _p(grad_bias), bt,
                                           _p(ws), ws_bytes, _p(stream))
+
+
+def i8lt_absmax8_blocks(count) -> int:
+    return load().i8lt_absmax8_blocks(int(count))
+
+
+def i8lt_absmax8_workspace_size() -> int:
+    return load().i8lt_absmax8_workspace_size()
+
+
+def i8lt_absmax8_quantize(absmax, count, q, absmax2, offset, ws, ws_bytes, stream=None) -> int:
+    return load().i8lt_absmax8_quantize(_p(absmax), int(count), _p(q), _p(absmax2), _p(offset), _p(ws), ws_bytes,
+                                        _p(stream))
+
+
+def i8lt_absmax8_dequantize(q, absmax2, offset, count, out, stream=None) -> int:
+    return load().i8lt_absmax8_dequantize(_p(q), _p(absmax2), _p(offset), int(count), _p(out), _p(stream))
 
 
 def i8lt_silu_forward(h, dt, n, out, stream=None) -> int:

@@ -29,9 +29,11 @@
 //            the likeliest to be still in L2): the absmax outside the outlier
 //            columns reduced over the block, then the codes rint(fp32(A16) *
 //            (127 / absmax)) (IEEE fp32 divide and multiply, round half to
-//            even) stored as exact fp16 integers with the outlier columns at
-//            0; the outlier columns' fp16 values go to subA; the per-1024-column
-//            sums of squared codes raise the row tile's asq entries.
+//            even) as exact fp16 integers with the outlier columns at 0,
+//            written over the row's own ring buffer and sent to global memory
+//            by one bulk store per row; the outlier columns' fp16 values go to
+//            subA; the per-1024-column sums of squared codes raise the row
+//            tile's asq entries.
 // The same arithmetic as colmax_kernel + outlier_index_kernel +
 // row_quantize_bulk_kernel (i8lt_quant.cu), so the results are bit-identical.
 // Used for 16-bit A with K a multiple of 8 up to 32768 (16-byte rows that fit
@@ -143,6 +145,29 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int& total, int* warp
   return before + incl - v;
 }
 
+// Sums x[i] over the warp for every i < G (G a power of two, 2..32) with
+// G - 1 + log2(32 / G) shuffles instead of G * 5: each halving step
+// exchanges half of the remaining values with the lane `o` apart, the lane
+// with bit o clear keeping the lower half.  Returns, at lane l, the warp sum
+// of x[l / (32 / G)].
+template <int G>
+__device__ __forceinline__ int warp_transpose_sum(int (&x)[G], int lane) {
+#pragma unroll
+  for (int n = G, o = 16; n > 1; n >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const int send = up ? x[j] : x[j + n / 2];
+      const int keep = up ? x[j + n / 2] : x[j];
+      x[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  int y = x[0];
+#pragma unroll
+  for (int o = 16 / G; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+  return y;
+}
+
 constexpr int kMaxBufs = 8;   // rows in the shared-memory ring
 
 template <typename T, int G, int NT>
@@ -160,7 +185,8 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
   const int64_t r0 = a.M * blockIdx.x / gridDim.x, r1 = a.M * (blockIdx.x + 1) / gridDim.x;
   const int64_t nrows = r1 - r0;
   const T* A = static_cast<const T*>(a.A);
-  const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;
+  const uint32_t row_bytes = static_cast<uint32_t>(a.K) * 2u;     // one input row
+  const uint32_t buf_bytes = static_cast<uint32_t>(a.k_pad) * 2u; // one ring buffer: a row of fp16 codes
   const int nbuf = a.nbuf;
   volatile int* abort_p = &abort_flag;
   if (t == 0) {
@@ -182,13 +208,13 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
     const int b = static_cast<int>(u % nbuf);
     fence_proxy_async_smem();   // the buffer's last readers are past a block barrier
     mbar_arrive_expect_tx(&full[b], row_bytes);
-    bulk_load(ring + static_cast<size_t>(b) * row_bytes, A + r * a.K, row_bytes, &full[b]);
+    bulk_load(ring + static_cast<size_t>(b) * buf_bytes, A + r * a.K, row_bytes, &full[b]);
   };
   // wait for stream row u and copy this thread's groups of it into registers
   auto fetch = [&](int64_t u, uint4 (&v)[G]) -> bool {
     const int b = static_cast<int>(u % nbuf);
     const bool ok = mbar_wait(&full[b], static_cast<uint32_t>((u / nbuf) & 1), abort_p, a.st, kWhereActQuant);
-    const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(b) * row_bytes);
+    const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(b) * buf_bytes);
 #pragma unroll
     for (int i = 0; i < G; ++i) {
       const int gi = t + i * NT;
@@ -197,13 +223,14 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
     return ok;
   };
   // after a timeout at stream row u_fail: let the copies issued and not yet
-  // consumed (rows u_fail .. u_issued - 1) land, each wait bounded, before
-  // the block leaves
+  // consumed (rows u_fail .. u_issued - 1) land, each wait bounded, and the
+  // bulk stores in flight finish, before the block leaves
   auto drain = [&](int64_t u_fail, int64_t u_issued) {
     if (t == 0) {
       *abort_p = 0;
       for (int64_t v = u_fail; v < u_issued; ++v)
         mbar_wait(&full[v % nbuf], static_cast<uint32_t>((v / nbuf) & 1), abort_p, nullptr, 0);
+      bulk_wait_all();   // code rows still being stored from shared memory
     }
   };
   int64_t u = 0;   // rows streamed so far
@@ -249,7 +276,7 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
     const int g0 = static_cast<int>(static_cast<int64_t>(ng) * blockIdx.x / gridDim.x);
     const int g1 = static_cast<int>(static_cast<int64_t>(ng) * (blockIdx.x + 1) / gridDim.x);
     const int S = g1 - g0;
-    uint32_t* colm_s = reinterpret_cast<uint32_t*>(ring);   // 8 S values (the ring holds >= 2 K halves)
+    uint32_t* colm_s = reinterpret_cast<uint32_t*>(ring);   // 8 S values (the ring holds >= 3 K halves)
     for (int x = t; x < 8 * S; x += NT) colm_s[x] = 0u;
     __syncthreads();
     const int nparts = static_cast<int>(gridDim.x);
@@ -326,9 +353,18 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
   }
   const int used_pad = (used + 63) / 64 * 64;
 
-  // ---- phase 3: the rows in reverse order (those phase 1 read last first)
+  // ---- phase 3: the rows in reverse order (those phase 1 read last first).
+  // A row's codes are written over its own ring buffer (each thread over the
+  // groups it read) and leave as one bulk store, issued after the next row's
+  // barrier; the buffer is refilled once that store has read it, so a buffer
+  // goes: loaded -> read -> codes -> stored -> loaded, nbuf - 2 rows ahead.
+  // (Refilling the buffer of row k - 2 instead, with more lookahead for the
+  // store, made the 8192-column rows 30 % slower.)
+  int64_t issued = std::min<int64_t>(nrows, nbuf);   // stream rows issued (uniform over the block)
   if (t == 0)
-    for (int64_t k = 0; k < nrows && k < nbuf; ++k) issue(u + k, r1 - 1 - k);
+    for (int64_t k = 0; k < issued; ++k) issue(u + k, r1 - 1 - k);
+  auto slot = [&](int64_t v) { return ring + static_cast<size_t>(v % nbuf) * buf_bytes; };
+  constexpr int kSpan = 32 / G;   // lanes that end up holding one group's warp sum (warp_transpose_sum)
   int par = 0;
   int64_t prev = -1;
   for (int64_t k = 0; k < nrows; ++k, par ^= 1) {
@@ -356,12 +392,16 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if (lane == 0) red_s[par][w] = amax;
-    // every thread has read its groups of the buffer and published its warp maximum
+    // every thread has read its groups of this row and published its warp
+    // maximum, and has written and fenced its codes of the previous row
     if (!__syncthreads_and(ok)) {
-      drain(u + k, u + std::min<int64_t>(nrows, k + nbuf));
+      drain(u + k, u + issued);
       return;
     }
-    if (t == 0 && k + nbuf < nrows) issue(u + k + nbuf, r1 - 1 - (k + nbuf));
+    if (t == 0 && prev >= 0) {
+      bulk_store(a.Aq + prev * a.k_pad, slot(u + k - 1), buf_bytes);
+      bulk_commit();
+    }
     // the previous row's chunk sums are complete: raise its tile's asq entries
     if (prev >= 0 && t < a.nch) {
       const int v = chunk_s[par ^ 1][t];
@@ -372,6 +412,8 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = (amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
+    uint8_t* cbuf = slot(u + k);
+    int sqi[G];
 #pragma unroll
     for (int i = 0; i < G; ++i) {
       const int gi = t + i * NT;
@@ -399,13 +441,9 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
         __half2* o2 = reinterpret_cast<__half2*>(&o);
 #pragma unroll
         for (int j = 0; j < 4; ++j) o2[j] = __floats2half2_rn(q[2 * j], q[2 * j + 1]);
-        *reinterpret_cast<uint4*>(a.Aq + r * a.k_pad + 8 * gi) = o;
+        st_shared_v4(cbuf + 16 * gi, o);
       }
-      // the 128 groups of a 1024-column chunk are 4 whole warps (NT % 128 == 0)
-      int v = static_cast<int>(sq);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0 && v != 0) atomicAdd(&chunk_s[par][gi >> 7], v);
+      sqi[i] = static_cast<int>(sq);
       if (mb[i] != 0u) {   // rare: the outlier columns of the group, in column order
         int j = jb[i];
 #pragma unroll
@@ -417,11 +455,31 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
         }
       }
     }
+    // the warp's sums of the G groups at once; group i of this warp lies in
+    // the 1024-column chunk (32 w + i NT) / 128 (NT % 128 == 0)
+    const int tot = warp_transpose_sum<G>(sqi, lane);
+    if ((lane & (kSpan - 1)) == 0 && tot != 0) atomicAdd(&chunk_s[par][(32 * w + (lane / kSpan) * NT) >> 7], tot);
     for (int j = used + t; j < used_pad; j += NT) a.subA[r * a.cap_pad + j] = __float2half_rn(0.f);
     if (t == 0) a.SCA[r] = amax;
+    fence_proxy_async_smem();   // this thread's codes, for the bulk store
+    // the buffer of the previous row: refill it once its store has read it
+    if (k >= 1) {
+      if (t == 0 && k - 1 + nbuf < nrows) {
+        bulk_wait_read<0>();
+        issue(u + k - 1 + nbuf, r1 - 1 - (k - 1 + nbuf));
+      }
+      issued = std::min<int64_t>(nrows, k + nbuf);
+    }
     prev = r;
   }
-  __syncthreads();
+  __syncthreads();   // the last row's codes are written and fenced; its chunk sums are complete
+  if (t == 0) {
+    if (prev >= 0) {
+      bulk_store(a.Aq + prev * a.k_pad, slot(u + nrows - 1), buf_bytes);
+      bulk_commit();
+    }
+    bulk_wait_all();
+  }
   if (prev >= 0 && t < a.nch) {
     const int v = chunk_s[par ^ 1][t];
     if (v != 0) atomicMax(a.asq + (prev >> 8) * a.nch + t, static_cast<uint32_t>(v));
@@ -439,9 +497,9 @@ template <typename T, int G, int NT>
 cudaError_t launch_cfg(ActQuantArgs a, bool cooperative, int sms, cudaStream_t s) {
   const void* fn = reinterpret_cast<const void*>(act_quant_fused_kernel<T, G, NT>);
   const int target = NT <= 512 ? 2 : 1;
-  const int64_t row_bytes = static_cast<int64_t>(a.K) * 2;
-  a.nbuf = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(kMaxBufs, kRingBudget / target / row_bytes)));
-  const int smem = static_cast<int>(a.nbuf * row_bytes);
+  const int64_t buf_bytes = static_cast<int64_t>(a.k_pad) * 2;   // a row of fp16 codes
+  a.nbuf = static_cast<int>(std::max<int64_t>(3, std::min<int64_t>(kMaxBufs, kRingBudget / target / buf_bytes)));
+  const int smem = static_cast<int>(a.nbuf * buf_bytes);
   if (!ensure_smem_attr(fn, kRingBudget)) return cudaGetLastError();
   const int per_sm = std::max(1, std::min(cached_blocks_per_sm(fn, NT, smem), target));
   const int nb = static_cast<int>(std::min<int64_t>(a.M, static_cast<int64_t>(sms) * per_sm));

@@ -16,7 +16,7 @@ using namespace i8lt;
 
 namespace {
 
-constexpr int kAbiVersion = 3;
+constexpr int kAbiVersion = 4;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -640,6 +640,32 @@ int i8lt_fp4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, i
   return dequantize_4bit(kFmtFp4, packed, absmax, N, K, out, dt, stream);
 }
 
+int64_t i8lt_absmax8_blocks(int64_t count) { return count < 0 ? -1 : ceil_div(count, 256); }
+
+size_t i8lt_absmax8_workspace_size(void) { return kAlign + 256 * sizeof(unsigned long long); }
+
+int i8lt_absmax8_quantize(const float* absmax, int64_t count, uint8_t* q, float* absmax2, float* offset, void* ws,
+                          size_t ws_bytes, void* stream) {
+  if (count < 0 || count > (int64_t(1) << 40)) return I8LT_ERR_INVALID_ARG;
+  if (offset == nullptr || (count > 0 && (absmax == nullptr || q == nullptr || absmax2 == nullptr)))
+    return I8LT_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < i8lt_absmax8_workspace_size()) return I8LT_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
+  if (int d = check_device()) return d;
+  auto* buckets = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + kAlign);
+  return cuda_status(
+      launch_absmax8_quantize(absmax, count, q, absmax2, offset, buckets, static_cast<cudaStream_t>(stream)));
+}
+
+int i8lt_absmax8_dequantize(const uint8_t* q, const float* absmax2, const float* offset, int64_t count, float* out,
+                            void* stream) {
+  if (count < 0 || count > (int64_t(1) << 40)) return I8LT_ERR_INVALID_ARG;
+  if (count == 0) return I8LT_OK;
+  if (q == nullptr || absmax2 == nullptr || offset == nullptr || out == nullptr) return I8LT_ERR_INVALID_ARG;
+  if (int d = check_device()) return d;
+  return cuda_status(launch_absmax8_dequantize(q, absmax2, offset, count, out, static_cast<cudaStream_t>(stream)));
+}
+
 size_t i8lt_nf4_workspace_size(void) { return kAlign; }
 
 size_t i8lt_nf4_workspace_size_dq(int64_t K, int64_t N) {
@@ -818,7 +844,8 @@ const char* i8lt_kernel_name(int k) {
                                 "build_subB",      "fwd_gemm",        "gradout_prepass",    "grad_bias_finalize",
                                 "bwd_gemm",        "silu",            "silu_backward",      "widen_codes",
                                 "dequant_weight",  "col_quantize",    "wgrad_gemm",         "unit_plan",
-                                "nf4_quantize",    "nf4_dequantize",  "nf4_gemm_fwd",       "nf4_gemm_bwd"};
+                                "nf4_quantize",    "nf4_dequantize",  "nf4_gemm_fwd",       "nf4_gemm_bwd",
+                                "absmax8"};
   return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
 }
 

@@ -273,6 +273,27 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from this CTA's shared memory to global memory, tracked in the
+// issuing thread's bulk-async groups (commit with bulk_commit, wait with
+// bulk_wait_read / bulk_wait_all).  The shared-memory writes it reads must be
+// made visible to the async proxy first (fence_proxy_async_smem by every
+// writer, then a barrier).
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// all but the newest `kPending` committed groups of this thread have finished
+// reading their source
+template <int kPending>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kPending) : "memory");
+}
+// every committed group of this thread has completed (its writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Fetch the box at (x, y) into L2 ahead of a later tiled load of it (a hint:
 // no shared memory, no barrier; boxes outside the tensor fetch nothing).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int x, int y) {

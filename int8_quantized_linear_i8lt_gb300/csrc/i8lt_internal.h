@@ -212,6 +212,13 @@ cudaError_t launch_nf4_dequantize_t(const uint8_t* packed, const float* absmax, 
 // packed + absmax -> out [N, K] (dtype dt): lv[code] * absmax, rounded once.
 cudaError_t launch_nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t N, int64_t K,
                                   int64_t row_bytes, void* out, int dt, cudaStream_t s, int fmt = kFmtNf4);
+// Double-quantized absmax: n fp32 values -> E4M3 codes q [n], absmax2
+// [ceil(n / 256)], offset [1]; `buckets` is 256 u64 of scratch.
+cudaError_t launch_absmax8_quantize(const float* absmax, int64_t n, uint8_t* q, float* absmax2, float* offset,
+                                    unsigned long long* buckets, cudaStream_t s);
+// ... and back to fp32 [n].
+cudaError_t launch_absmax8_dequantize(const uint8_t* q, const float* absmax2, const float* offset, int64_t n,
+                                      float* out, cudaStream_t s);
 
 // Backward prepass of the materialized schedule: WdqT[k, n] =
 // fp16_rn(fp32(CB[n, k]) * (SCB[n] * fp32(1/127))) for k < k_pad, n < N, and
@@ -231,7 +238,7 @@ cudaError_t gemm_launch_shape(int kernel_id, int* ctas, int* threads, int* smem_
 enum KernelId {
   K_QUANTIZE_WEIGHT = 0, K_COLMAX, K_OUTLIER_INDEX, K_ROW_QUANTIZE, K_SUBB, K_FWD_GEMM, K_GRADOUT_PREPASS,
   K_GRAD_BIAS_FINALIZE, K_BWD_GEMM, K_SILU, K_SILU_BACKWARD, K_WIDEN_CODES, K_DEQUANT_WEIGHT, K_COL_QUANTIZE,
-  K_WGRAD_GEMM, K_UNIT_PLAN, K_NF4_QUANTIZE, K_NF4_DEQUANTIZE, K_NF4_GEMM_FWD, K_NF4_GEMM_BWD, K_COUNT
+  K_WGRAD_GEMM, K_UNIT_PLAN, K_NF4_QUANTIZE, K_NF4_DEQUANTIZE, K_NF4_GEMM_FWD, K_NF4_GEMM_BWD, K_ABSMAX8, K_COUNT
 };
 
 // Box sizes of the tensor maps (each CTA of a pair stages 128 rows of each

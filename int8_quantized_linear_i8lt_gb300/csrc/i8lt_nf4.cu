@@ -348,4 +348,194 @@ cudaError_t launch_nf4_dequantize_t(const uint8_t* packed, const float* absmax, 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Double-quantized absmax (the "-dq" options of the 4-bit formats, lit-gpt PR
+// #275 "Support QLoRA 4-bit finetuning with bitsandbytes"; QLoRA's double
+// quantization): the fp32 absmax values c of the 64-element blocks are stored
+// as FP8 E4M3 codes of d = c - offset in blocks of 256 with an fp32 scale
+// each; offset is the mean of all c.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kAbs8Block = 256;
+constexpr float kInv448 = 0x1.24924ap-9f;   // fp32(1 / 448), correctly rounded
+
+// E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, exponent 0
+// subnormal, largest finite 448) from its bit fields.  Codes 0x7F / 0xFF (NaN)
+// are never produced by absmax8_encode.
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const uint32_t e = (code >> 3) & 15u, m = code & 7u;
+  const float mag = e == 0u ? static_cast<float>(m) * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+  return (code & 0x80u) ? -mag : mag;
+}
+
+// The E4M3 code nearest to y, ties to the even code (round half to even on
+// the 3-bit mantissa), |y| >= 448 saturating to 448, the sign of y kept.
+__device__ __forceinline__ uint32_t absmax8_encode(float y) {
+  const uint32_t sign = (__float_as_uint(y) >> 24) & 0x80u;
+  const float a = fabsf(y);
+  if (!(a < 448.f)) return sign | 0x7Eu;
+  if (a < 0x1p-6f) return sign | static_cast<uint32_t>(__float2int_rn(a * 512.f));   // subnormal: steps of 2^-9
+  const int e = static_cast<int>(__float_as_uint(a) >> 23) - 127;                     // -6 .. 8
+  // a * 2^(3 - e) in [8, 16): the mantissa with its leading bit, rounded;
+  // 16 carries into the next exponent through the addition below
+  const float scaled = a * __uint_as_float(static_cast<uint32_t>(127 + 3 - e) << 23);
+  const int m = __float2int_rn(scaled);
+  return sign | static_cast<uint32_t>(((e + 7) << 3) + (m - 8));
+}
+
+// Per-exponent integer sums of the significands (exact): bucket[e] gathers
+// the 24-bit significands of the values with biased exponent e (subnormals
+// in bucket 1), so sum(c) = sum_e bucket[e] * 2^(e - 150).  Lanes with the
+// same exponent are combined first, then one shared atomic per group.
+__global__ void __launch_bounds__(256) absmax8_sum_kernel(const float* __restrict__ c, int64_t n,
+                                                           unsigned long long* __restrict__ buckets) {
+  __shared__ unsigned long long b_s[256];
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) b_s[i] = 0ull;
+  __syncthreads();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // every lane of a warp runs the same number of rounds (the shuffles below)
+  const int64_t rounds = (n + stride - 1) / stride;
+  for (int64_t rd = 0; rd < rounds; ++rd) {
+    const int64_t i = i0 + rd * stride;
+    uint32_t e = 0u, m = 0u;
+    if (i < n) {
+      const uint32_t bits = __float_as_uint(c[i]) & 0x7FFFFFFFu;   // the values are non-negative
+      const uint32_t be = bits >> 23;
+      if (be != 255u && bits != 0u) {
+        e = be == 0u ? 1u : be;
+        m = (bits & 0x7FFFFFu) | (be == 0u ? 0u : 0x800000u);
+      }
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    const unsigned sum = __reduce_add_sync(grp, m);   // <= 32 * 2^24
+    if (m != 0u || e != 0u) {
+      if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(grp) - 1) && sum != 0u)
+        atomicAdd(&b_s[e], static_cast<unsigned long long>(sum));
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    if (b_s[i] != 0ull) atomicAdd(&buckets[i], b_s[i]);
+}
+
+__device__ __forceinline__ double pow2d(int k) {   // 2^k for -1022 <= k <= 1023
+  return __longlong_as_double(static_cast<long long>(1023 + k) << 52);
+}
+
+// offset = fp32(S / n): the exact sum S of the buckets as a 384-bit integer
+// times 2^-149, rounded once to float64 (half to even), an IEEE float64
+// division by n, one rounding to fp32.  One thread.
+__global__ void absmax8_offset_kernel(const unsigned long long* __restrict__ buckets, int64_t n,
+                                      float* __restrict__ offset) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  uint64_t w[6] = {0, 0, 0, 0, 0, 0};   // little-endian words of sum_e bucket[e] * 2^(e - 1)
+  for (int e = 1; e < 255; ++e) {
+    const uint64_t v = buckets[e];
+    if (v == 0) continue;
+    const int sh = e - 1, q = sh >> 6, r = sh & 63;
+    const uint64_t lo = v << r, hi = r ? (v >> (64 - r)) : 0ull;
+    uint64_t s0 = w[q] + lo;
+    uint64_t carry = s0 < lo ? 1ull : 0ull;
+    w[q] = s0;
+    uint64_t s1 = w[q + 1] + hi;
+    uint64_t c1 = s1 < hi ? 1ull : 0ull;
+    s1 += carry;
+    c1 += s1 < carry ? 1ull : 0ull;
+    w[q + 1] = s1;
+    for (int j = q + 2; j < 6 && c1 != 0ull; ++j) {
+      w[j] += c1;
+      c1 = w[j] == 0ull ? 1ull : 0ull;
+    }
+  }
+  int top = -1;
+  for (int j = 5; j >= 0 && top < 0; --j)
+    if (w[j] != 0ull) top = 64 * j + 63 - __clzll(static_cast<long long>(w[j]));
+  auto bit = [&](int b) -> uint64_t { return (w[b >> 6] >> (b & 63)) & 1ull; };
+  double s64 = 0.0;
+  if (top >= 0 && top < 53) {
+    s64 = static_cast<double>(w[0]) * pow2d(-149);   // exact: fewer than 54 bits
+  } else if (top >= 53) {
+    uint64_t mant = 0;
+    for (int b = top; b > top - 53; --b) mant = (mant << 1) | bit(b);
+    const uint64_t rnd = bit(top - 53);
+    bool sticky = false;
+    for (int b = top - 54; b >= 0 && !sticky; --b) sticky = bit(b) != 0ull;
+    int p = top;
+    if (rnd && (sticky || (mant & 1ull))) {
+      ++mant;
+      if (mant == (1ull << 53)) {
+        mant >>= 1;
+        ++p;
+      }
+    }
+    s64 = static_cast<double>(mant) * pow2d(p - 52 - 149);   // exact: 53 bits times a power of two
+  }
+  *offset = n > 0 ? __double2float_rn(__ddiv_rn(s64, static_cast<double>(n))) : 0.f;
+}
+
+// One warp per block of 256 values: d = c - offset, absmax2 = max |d|, codes
+// of d * fp32(448 / absmax2).
+__global__ void __launch_bounds__(256) absmax8_quant_kernel(const float* __restrict__ c, int64_t n,
+                                                             const float* __restrict__ offset,
+                                                             uint8_t* __restrict__ q, float* __restrict__ absmax2) {
+  const int lane = threadIdx.x & 31;
+  const int64_t blk = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (blk >= (n + kAbs8Block - 1) / kAbs8Block) return;   // uniform over the warp
+  const float off = *offset;
+  float d[8];
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t i = blk * kAbs8Block + j * 32 + lane;
+    d[j] = i < n ? __fsub_rn(c[i], off) : 0.f;
+    m = fmaxf(m, fabsf(d[j]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float s2 = m > 0.f ? __fdiv_rn(448.f, m) : 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t i = blk * kAbs8Block + j * 32 + lane;
+    if (i < n) q[i] = static_cast<uint8_t>(absmax8_encode(__fmul_rn(d[j], s2)));
+  }
+  if (lane == 0) absmax2[blk] = m;
+}
+
+__global__ void __launch_bounds__(256) absmax8_dequant_kernel(const uint8_t* __restrict__ q,
+                                                               const float* __restrict__ absmax2,
+                                                               const float* __restrict__ offset, int64_t n,
+                                                               float* __restrict__ out) {
+  const float off = *offset;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float f2 = __fmul_rn(absmax2[i / kAbs8Block], kInv448);
+    out[i] = __fadd_rn(__fmul_rn(e4m3_value(q[i]), f2), off);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_absmax8_quantize(const float* absmax, int64_t n, uint8_t* q, float* absmax2, float* offset,
+                                    unsigned long long* buckets, cudaStream_t s) {
+  ProfScope ps(K_ABSMAX8, s);
+  if (n == 0) return cudaMemsetAsync(offset, 0, sizeof(float), s);
+  cudaError_t err = cudaMemsetAsync(buckets, 0, 256 * sizeof(unsigned long long), s);
+  if (err != cudaSuccess) return err;
+  absmax8_sum_kernel<<<grid_for(n), 256, 0, s>>>(absmax, n, buckets);
+  absmax8_offset_kernel<<<1, 32, 0, s>>>(buckets, n, offset);
+  const int64_t warps = (n + kAbs8Block - 1) / kAbs8Block;
+  absmax8_quant_kernel<<<static_cast<unsigned>(ceil_div(warps, 8)), 256, 0, s>>>(absmax, n, offset, q, absmax2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_absmax8_dequantize(const uint8_t* q, const float* absmax2, const float* offset, int64_t n,
+                                      float* out, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  ProfScope ps(K_ABSMAX8, s);
+  absmax8_dequant_kernel<<<grid_for(n), 256, 0, s>>>(q, absmax2, offset, n, out);
+  return cudaGetLastError();
+}
+
 }  // namespace i8lt

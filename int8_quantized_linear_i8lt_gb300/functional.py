@@ -479,6 +479,35 @@ def fp4_dequantize(packed: torch.Tensor, absmax: torch.Tensor, K: int, dtype: to
     return dequantize_4bit(packed, absmax, K, dtype, "fp4")
 
 
+def double_quantize_absmax(absmax: torch.Tensor):
+    """The 8-bit storage of a 4-bit weight's absmax values (the ``-dq``
+    options): (q uint8 with absmax's shape, absmax2 fp32 [ceil(n / 256)],
+    offset fp32 [1]) -- FP8 E4M3 codes of absmax - offset in blocks of 256
+    with one fp32 scale each, offset the mean of all the values."""
+    _require_cuda(absmax)
+    a = absmax.contiguous()
+    n = a.numel()
+    q = torch.empty(a.shape, dtype=torch.uint8, device=a.device)
+    a2 = torch.empty(_lib.i8lt_absmax8_blocks(n), dtype=torch.float32, device=a.device)
+    off = torch.empty(1, dtype=torch.float32, device=a.device)
+    ws = torch.empty(_lib.i8lt_absmax8_workspace_size(), dtype=torch.uint8, device=a.device)
+    _check(_lib.i8lt_absmax8_quantize(a.data_ptr(), n, q.data_ptr(), a2.data_ptr(), off.data_ptr(), ws.data_ptr(),
+                                      ws.numel(), _stream(a)), "i8lt_absmax8_quantize")
+    return q, a2, off
+
+
+def dequantize_absmax(q: torch.Tensor, absmax2: torch.Tensor, offset: torch.Tensor,
+                      out: torch.Tensor | None = None) -> torch.Tensor:
+    """The fp32 absmax values decoded from double_quantize_absmax's storage."""
+    _require_cuda(q, absmax2, offset)
+    q = q.contiguous()
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _check(_lib.i8lt_absmax8_dequantize(q.data_ptr(), absmax2.data_ptr(), offset.data_ptr(), q.numel(),
+                                        out.data_ptr(), _stream(q)), "i8lt_absmax8_dequantize")
+    return out
+
+
 def _nf4_ws(device, ws, K, N, materialized, extra=0):
     """Workspace of the 4-bit matmuls: the status word (and ``extra`` bytes
     of grad_bias partial sums), the weight then decoded inside the GEMM; or

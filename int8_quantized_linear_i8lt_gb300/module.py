@@ -106,12 +106,16 @@ class Linear4bit(torch.nn.Module):
     input-gradient GEMM).  ``materialized``: each matmul first writes the
     16-bit weight to a temporary workspace and reads it with a plain GEMM
     (faster, N * K * 2 bytes of transient memory); the results are the same
-    bits."""
+    bits.  ``double_quant`` (the ``bnb.nf4-dq`` / ``bnb.fp4-dq`` options): the
+    absmax values are stored in 8 bits (FP8 E4M3 codes in blocks of 256 with
+    an fp32 scale each, around their mean) and decoded by one kernel per
+    call."""
 
     fmt = "nf4"
 
     def __init__(self, in_features: int, out_features: int, bias: bool = True, device=None,
-                 bias_dtype: torch.dtype = torch.bfloat16, materialized: bool = False, fmt: str | None = None):
+                 bias_dtype: torch.dtype = torch.bfloat16, materialized: bool = False, fmt: str | None = None,
+                 double_quant: bool = False):
         super().__init__()
         from . import _lib
         if fmt is not None:
@@ -119,10 +123,17 @@ class Linear4bit(torch.nn.Module):
         self.in_features = in_features
         self.out_features = out_features
         self.materialized = bool(materialized)
+        self.double_quant = bool(double_quant)
+        nblk = _lib.i8lt_nf4_blocks(in_features)
         self.register_buffer("packed", torch.zeros(out_features, _lib.i8lt_nf4_row_bytes(in_features),
                                                    dtype=torch.uint8, device=device))
-        self.register_buffer("absmax", torch.zeros(out_features, _lib.i8lt_nf4_blocks(in_features),
-                                                   dtype=torch.float32, device=device))
+        if self.double_quant:
+            self.register_buffer("absmax_q", torch.zeros(out_features, nblk, dtype=torch.uint8, device=device))
+            self.register_buffer("absmax2", torch.zeros(_lib.i8lt_absmax8_blocks(out_features * nblk),
+                                                        dtype=torch.float32, device=device))
+            self.register_buffer("absmax_offset", torch.zeros(1, dtype=torch.float32, device=device))
+        else:
+            self.register_buffer("absmax", torch.zeros(out_features, nblk, dtype=torch.float32, device=device))
         if bias:
             self.bias = torch.nn.Parameter(torch.zeros(out_features, dtype=bias_dtype, device=device))
         else:
@@ -136,19 +147,31 @@ class Linear4bit(torch.nn.Module):
                     bias_dtype=bias.dtype if bias is not None else torch.bfloat16, materialized=materialized, **kw)
         packed, absmax = F.quantize_4bit(weight, layer.fmt)
         layer.packed.copy_(packed)
-        layer.absmax.copy_(absmax)
+        if layer.double_quant:
+            q, a2, off = F.double_quantize_absmax(absmax)
+            layer.absmax_q.copy_(q)
+            layer.absmax2.copy_(a2)
+            layer.absmax_offset.copy_(off)
+        else:
+            layer.absmax.copy_(absmax)
         if bias is not None:
             with torch.no_grad():
                 layer.bias.copy_(bias)
         return layer
 
+    def decoded_absmax(self) -> torch.Tensor:
+        """The fp32 absmax [N, blocks per row] the matmuls use."""
+        if self.double_quant:
+            return F.dequantize_absmax(self.absmax_q, self.absmax2, self.absmax_offset)
+        return self.absmax
+
     def forward(self, x: torch.Tensor) -> torch.Tensor:
-        return F.Linear4bitFunction.apply(x, self.packed, self.absmax, self.in_features, self.bias,
+        return F.Linear4bitFunction.apply(x, self.packed, self.decoded_absmax(), self.in_features, self.bias,
                                           self.materialized, self.fmt)
 
     def extra_repr(self) -> str:
         return (f"in_features={self.in_features}, out_features={self.out_features}, bias={self.bias is not None}, "
-                f"fmt={self.fmt}")
+                f"fmt={self.fmt}, double_quant={self.double_quant}")
 
 
 class LinearNF4(Linear4bit):

@@ -31,7 +31,7 @@ def test_exports_every_declared_function(L):
 
 
 def test_version_and_strings(L):
-    assert _lib.i8lt_abi_version() == 3
+    assert _lib.i8lt_abi_version() == 4
     for code in range(10):
         assert _lib.i8lt_status_string(code) != "unknown status"
     assert _lib.i8lt_status_string(42) == "unknown status"
@@ -193,6 +193,14 @@ def test_nf4_sizes_and_levels(L):
     assert lv[8:] == [-v for v in lv[:8]] and math.copysign(1.0, lv[8]) == -1.0
     assert all(a < b for a, b in zip(lv[:8], lv[1:8]))
     # grad_bias partial sums of the 4-bit input gradient: 128-token chunks x N fp32, 256-byte aligned
+    assert _lib.i8lt_absmax8_blocks(0) == 0 and _lib.i8lt_absmax8_blocks(256) == 1
+    assert _lib.i8lt_absmax8_blocks(257) == 2 and _lib.i8lt_absmax8_blocks(-1) == -1
+    assert _lib.i8lt_absmax8_workspace_size() == 256 + 256 * 8
+    # argument errors come back before any device work
+    assert _lib.i8lt_absmax8_quantize(None, -1, None, None, None, None, 0, None) == _lib.I8LT_ERR_INVALID_ARG
+    assert _lib.i8lt_absmax8_quantize(None, 0, None, None, 8, None, 0, None) == _lib.I8LT_ERR_WORKSPACE
+    assert _lib.i8lt_absmax8_dequantize(None, None, None, 5, None, None) == _lib.I8LT_ERR_INVALID_ARG
+    assert _lib.i8lt_absmax8_dequantize(None, None, None, 0, None, None) == _lib.I8LT_OK
     assert _lib.i8lt_nf4_grad_bias_bytes(300, 64) == 3 * 64 * 4
     assert _lib.i8lt_nf4_grad_bias_bytes(1, 10) == 256 and _lib.i8lt_nf4_grad_bias_bytes(-1, 10) == 0
 

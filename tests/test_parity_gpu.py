@@ -88,6 +88,10 @@ SMALL = [
     (19, 13, 9, torch.float32, 0.0, 1.0, 6.0),            # K, N not multiples of 8 (scalar paths)
     (140, 200, 300, torch.bfloat16, 0.05, 10.0, 6.0),     # many outliers (4 outlier blocks)
     (600, 16, 4, torch.float32, 0.0, 1.0, math.inf),      # the tiny MLP's second layer shape
+    # more tiles than CTA pairs in every GEMM: several tiles per pair (both
+    # accumulators of the materialized backward, the staggered halves of the
+    # fused one across tile boundaries, its split last round)
+    (2100, 5120, 264, torch.float16, 0.002, 15.0, 6.0),
 ]
 
 
