@@ -714,6 +714,65 @@ __device__ __forceinline__ void bwd_store16(const BwdEpiArgs& e, int64_t kk, int
   }
 }
 
+// The 16 fp32 values x[j] (tokens m_base + j) of this lane's output feature,
+// stored as 8-feature rows: within each group of 8 lanes (8 consecutive
+// features) an 8 x 8 block of tokens x features is transposed in three
+// exchange rounds, after which lane i of the group holds token 8 h + i of
+// block h for the group's 8 features and stores them with one 16-byte store
+// (two for fp32).  kg: the group's first feature; K % 8 == 0 and the output
+// rows are 16-byte aligned, so a group is wholly in or out of range.  The
+// addend, then the bias, are added after the exchange, in the order of the
+// scalar path.  Every lane of the warp calls this (the exchange), whatever
+// its range checks.
+template <typename OutT>
+__device__ __forceinline__ void bwd_store16_rows(const BwdEpiArgs& e, int64_t kg, int m_base, const uint32_t (&x)[16],
+                                                 int lane) {
+  OutT* out = static_cast<OutT*>(e.grad_A);
+  const OutT* add = static_cast<const OutT*>(e.addend);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(x[8 * h + j]);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j & o) continue;
+        const float send = up ? v[j] : v[j + o];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+        if (up)
+          v[j] = recv;
+        else
+          v[j + o] = recv;
+      }
+    }
+    const int64_t mm = m_base + 8 * h + (lane & 7);
+    if (mm >= e.M || kg >= e.K) continue;
+    OutT* dst = out + mm * e.K + kg;
+    if (add != nullptr) {
+      const OutT* src = add + mm * e.K + kg;
+#pragma unroll
+      for (int f = 0; f < 8; ++f) v[f] = __fadd_rn(v[f], to_float(src[f]));
+    }
+    if (e.bias != nullptr) {
+#pragma unroll
+      for (int f = 0; f < 8; ++f) v[f] = __fadd_rn(v[f], load_any(e.bias, e.bias_dt, kg + f));
+    }
+    if constexpr (sizeof(OutT) == 4) {
+      reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+      uint4 o;
+      OutT* q = reinterpret_cast<OutT*>(&o);
+#pragma unroll
+      for (int f = 0; f < 8; ++f) q[f] = from_float<OutT>(v[f]);
+      *reinterpret_cast<uint4*>(dst) = o;
+    }
+  }
+}
+
 // Two fp32 values times the splatted scale (one packed IEEE multiply, the
 // same rounding as two scalar ones), rounded to a 16-bit pair; e0 in the low
 // half.
@@ -1175,6 +1234,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t acc_empty_pair[2] = {mapa_shared(&bars->acc_empty[0], 0), mapa_shared(&bars->acc_empty[1], 0)};
     const int ew = (warp >= kBwdWarpEpi1 ? 4 : 0) + quad;   // epilogue warp 0..7
+    // output rows of whole 16-byte groups of 8 features (and a 16-byte
+    // aligned addend): the transposed 16-byte stores; else one scalar store
+    // per element (2-byte stores scattered over 16 rows cost the epilogue
+    // about 13 us per tile against 1 us for the transposed ones)
+    const bool rows16 = (e.K % 8) == 0 && (reinterpret_cast<uintptr_t>(e.grad_A) & 15u) == 0 &&
+                        (reinterpret_cast<uintptr_t>(e.addend) & 15u) == 0;
     int tl = 0;
     for (int t = cid; t < num_tiles; t += ncl, ++tl) {
       int tm, tk, m_base, nsub;
@@ -1204,10 +1269,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
         break;
       tc_fence_after();
       const int64_t kk = static_cast<int64_t>(tk) * kPairM + static_cast<int64_t>(rank) * kCtaRows + quad * 32 + lane;
+      const int64_t kg = kk - (lane & 7);   // first feature of this lane's group of 8
       const uint32_t d = tmem + static_cast<uint32_t>(buf) * 256u + lane_off + static_cast<uint32_t>(col0);
       const int m0 = m_base + col0;
       auto store = [&](const uint32_t(&x)[16], int gc) {
-        if (kk < e.K) {
+        if (rows16) {   // 16-byte stores of 8 features (every lane takes part in the exchange)
+          switch (e.dt) {
+            case DT_F16: bwd_store16_rows<__half>(e, kg, m0 + gc, x, lane); break;
+            case DT_BF16: bwd_store16_rows<__nv_bfloat16>(e, kg, m0 + gc, x, lane); break;
+            default: bwd_store16_rows<float>(e, kg, m0 + gc, x, lane); break;
+          }
+        } else if (kk < e.K) {
           switch (e.dt) {
             case DT_F16: bwd_store16<__half>(e, kk, m0 + gc, x); break;
             case DT_BF16: bwd_store16<__nv_bfloat16>(e, kk, m0 + gc, x); break;
