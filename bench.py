@@ -44,10 +44,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 MEASURED_TRAFFIC = {
     "workload": "proj_8192x28672",
     "sources": {"int8_quantized_linear_i8lt_gb300/csrc/i8lt_gemm.cu":
-                "6271604b0a8903d5bd76eafba4b1df15f7414a06aa15f583d824f0cf78b733fd",
+                "f08d86f125c1733ef8aa1a4b1b739f755232646eb3e187e673a3127712e8555e",
                 "int8_quantized_linear_i8lt_gb300/csrc/i8lt_common.cuh":
-                "ea330a3319c81e6e3ec691a3ae0f938a9410fc9d74d3a5f1ec638eb4245a4274"},
-    "bytes_per_launch": {"fwd_gemm": 8.10e9, "bwd_gemm": 5.30e9},
+                "cc2fb6fa161ef5430ebd36ed4e9af7f9a5113376b51d4738964ca1dbdcce7d42"},
+    "bytes_per_launch": {"fwd_gemm": 8.76e9, "bwd_gemm": 8.32e9},
 }
 
 
