@@ -170,8 +170,8 @@ __device__ __forceinline__ int warp_transpose_sum(int (&x)[G], int lane) {
 
 constexpr int kMaxBufs = 8;   // rows in the shared-memory ring
 
-template <typename T, int G, int NT>
-__global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs a) {
+template <typename T, int G, int NT, int MINB>
+__global__ void __launch_bounds__(NT, MINB) act_quant_fused_kernel(const ActQuantArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];   // a.nbuf row buffers of K 16-bit elements
   __shared__ __align__(8) uint64_t full[kMaxBufs];
   __shared__ int abort_flag;
@@ -486,17 +486,19 @@ __global__ void __launch_bounds__(NT) act_quant_fused_kernel(const ActQuantArgs 
   }
 }
 
-// Blocks of NT threads, G groups each: a configuration that covers the row
-// (256 x 2 groups up to 4096 columns, 512 x 2 up to 8192, 256 x 8 up to
-// 16384, else 1024 x 4).  Two blocks per SM for the 256- and 512-thread
-// configurations, one for 1024; the ring takes what shared memory the blocks
-// of an SM leave, 2 to kMaxBufs rows.
+// Blocks of NT threads, G groups each, MINB blocks per SM: a configuration
+// that covers the row (256 x 2 groups up to 4096 columns and 256 x 4 up to
+// 8192, four blocks per SM, when there are rows enough -- else 256 x 2 and
+// 512 x 2, two; 256 x 8 up to 16384, two; else 1024 x 4, one).  More
+// resident blocks hide each block's per-row barrier and bulk-copy waits
+// behind the others' work.  The ring takes what shared memory the blocks of
+// an SM leave, 3 to kMaxBufs rows.
 constexpr int kRingBudget = 200 * 1024;
 
-template <typename T, int G, int NT>
+template <typename T, int G, int NT, int MINB>
 cudaError_t launch_cfg(ActQuantArgs a, bool cooperative, int sms, cudaStream_t s) {
-  const void* fn = reinterpret_cast<const void*>(act_quant_fused_kernel<T, G, NT>);
-  const int target = NT <= 512 ? 2 : 1;
+  const void* fn = reinterpret_cast<const void*>(act_quant_fused_kernel<T, G, NT, MINB>);
+  const int target = MINB;
   const int64_t buf_bytes = static_cast<int64_t>(a.k_pad) * 2;   // a row of fp16 codes
   a.nbuf = static_cast<int>(std::max<int64_t>(3, std::min<int64_t>(kMaxBufs, kRingBudget / target / buf_bytes)));
   const int smem = static_cast<int>(a.nbuf * buf_bytes);
@@ -513,16 +515,21 @@ cudaError_t launch_cfg(ActQuantArgs a, bool cooperative, int sms, cudaStream_t s
   attr[0].val.cooperative = cooperative ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, act_quant_fused_kernel<T, G, NT>, a);
+  return cudaLaunchKernelEx(&cfg, act_quant_fused_kernel<T, G, NT, MINB>, a);
 }
 
 template <typename T>
 cudaError_t launch_typed(const ActQuantArgs& a, bool cooperative, int sms, cudaStream_t s) {
   const int groups = a.k_pad / 8;
-  if (groups <= 256 * 2) return launch_cfg<T, 2, 256>(a, cooperative, sms, s);
-  if (groups <= 512 * 2) return launch_cfg<T, 2, 512>(a, cooperative, sms, s);
-  if (groups <= 256 * 8) return launch_cfg<T, 8, 256>(a, cooperative, sms, s);
-  return launch_cfg<T, 4, 1024>(a, cooperative, sms, s);
+  // four blocks per SM only when every block still gets a few dozen rows
+  // (with 2048 rows of 4096 columns they made the launch 24 % slower)
+  const bool many_rows = a.M >= 32LL * sms;
+  if (groups <= 256 * 2)
+    return many_rows ? launch_cfg<T, 2, 256, 4>(a, cooperative, sms, s) : launch_cfg<T, 2, 256, 2>(a, cooperative, sms, s);
+  if (groups <= 512 * 2)
+    return many_rows ? launch_cfg<T, 4, 256, 4>(a, cooperative, sms, s) : launch_cfg<T, 2, 512, 2>(a, cooperative, sms, s);
+  if (groups <= 256 * 8) return launch_cfg<T, 8, 256, 2>(a, cooperative, sms, s);
+  return launch_cfg<T, 4, 1024, 1>(a, cooperative, sms, s);
 }
 
 }  // namespace

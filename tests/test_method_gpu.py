@@ -92,6 +92,30 @@ def test_large_two_layer_net_against_dequantized_weights(dtype):
     page_rule(fc2.bias.grad, grad_proj.float().reshape(-1, 1024).sum(0), k=0.02)
 
 
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_large_two_layer_net_against_float_weights(dtype):
+    """The page's check at 1024 -> 4096 -> 1024 features, 1024 tokens,
+    against the original float weights.  The int8 weight quantization of
+    the method itself (one scale per row, step absmax / 127 ~ 4.5 sigma / 127
+    of these N(0, 0.02) weights) puts an error of about 1 % of the rms
+    gradient on every element, whatever its own size, so elements much
+    smaller than the mean miss isclose(0.01 * scale, rtol 0.1).  Measured on
+    GB300 (printed with -s): max |err| = 0.074 (fp16) / 0.079 (bf16) of the
+    scale, 2.8 % of the elements outside isclose -- above the page's 0.05 and
+    0.5 %, which were set for its own test data; bounded here at 0.1 and
+    5 %.  The page's own bounds hold against the dequantized weights above,
+    which isolates the implementation."""
+    x, o1, grad_proj, w1, w2, fc1, fc2 = _two_layers(1024, 4096, 8, 128, dtype, 0)
+    grad_ref = (grad_proj.flatten(2).float() @ w2.float() @ w1.float()).reshape(x.shape)
+    got = x.grad.float()
+    scale = grad_ref.abs().mean()
+    max_rel = float((got - grad_ref).abs().max() / scale)
+    bad = float((~torch.isclose(got, grad_ref, atol=0.01 * scale, rtol=0.1)).float().mean())
+    print(f"[page rule vs float weights, {dtype}] max |err| / scale = {max_rel:.4f}, "
+          f"outside isclose = {100 * bad:.2f} %")
+    assert max_rel <= 0.1 and bad <= 0.05
+
+
 def test_weight_is_frozen_and_cast_warning():
     w = torch.randn(64, 32, device=DEV, dtype=torch.float16) * 0.02
     fc = I.Linear8bitLt.from_float(w, torch.zeros(64, device=DEV, dtype=torch.float16))
