@@ -503,6 +503,12 @@ int i8lt_profile_start(int max_launches);
  * i8lt_read_device_status.  ws: at least 256 bytes, 256-byte aligned (its
  * status word is cleared first).  No counterpart on the pages. */
 int i8lt_debug_wait_timeout(int64_t limit_ns, void* ws, size_t ws_bytes, void* stream);
+/* The same for the grid-wide wait of the fused activation quantization: two
+ * blocks of a cooperative launch wait, limit_ns long, at a barrier that is
+ * one arrival short of complete (the arrival counter at byte 64 of ws, as in
+ * the forward workspace); each records I8LT_ERR_TIMEOUT (role 7) and
+ * returns.  ws: at least 256 bytes, 256-byte aligned, cleared first. */
+int i8lt_debug_grid_wait_timeout(int64_t limit_ns, void* ws, size_t ws_bytes, void* stream);
 
 /* Launch shape the library uses for the persistent GEMM kernels
  * (kernel = I8LT_K_FWD_GEMM or I8LT_K_BWD_GEMM): CTAs (pairs x 2), threads

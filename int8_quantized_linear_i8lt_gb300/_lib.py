@@ -75,6 +75,7 @@ SIGNATURES = {
                                          c_void_p, c_size_t, c_int64, POINTER(i8lt_fwd_debug), c_void_p]),
     "i8lt_backward_workspace_size": (c_size_t, [c_int64, c_int64, c_int]),
     "i8lt_debug_wait_timeout": (c_int, [c_int64, c_void_p, c_size_t, c_void_p]),
+    "i8lt_debug_grid_wait_timeout": (c_int, [c_int64, c_void_p, c_size_t, c_void_p]),
     "i8lt_grad_weight_workspace_size": (c_size_t, [c_int64, c_int64, c_int64]),
     "i8lt_grad_weight": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int64, c_int64, c_int64, c_void_p, c_int,
                                  c_void_p, c_size_t, c_void_p]),
@@ -214,6 +215,10 @@ def i8lt_grad_weight(G, gt, A, at, M, N, K, grad_W, wt, ws, ws_bytes, stream=Non
 
 def i8lt_debug_wait_timeout(limit_ns, ws, ws_bytes, stream=None) -> int:
     return load().i8lt_debug_wait_timeout(limit_ns, _p(ws), ws_bytes, _p(stream))
+
+
+def i8lt_debug_grid_wait_timeout(limit_ns, ws, ws_bytes, stream=None) -> int:
+    return load().i8lt_debug_grid_wait_timeout(limit_ns, _p(ws), ws_bytes, _p(stream))
 
 
 def i8lt_backward_workspace_size(M, N, gt) -> int:

@@ -94,7 +94,8 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 // Every block of the grid arrives once per wait; returns false (after
 // recording ST_TIMEOUT) when the counter has not reached `target` (the
 // blocks times the waits so far) within the time limit.
-__device__ bool grid_wait(unsigned* arrive, unsigned target, DevStatus* st) {
+__device__ bool grid_wait(unsigned* arrive, unsigned target, DevStatus* st,
+                          unsigned long long limit_ns = kWaitTimeoutNs) {
   __shared__ int ok_s;
   __threadfence();   // this thread's column-maxima reductions, before the arrival
   __syncthreads();
@@ -105,7 +106,7 @@ __device__ bool grid_wait(unsigned* arrive, unsigned target, DevStatus* st) {
     const unsigned long long t0 = global_ns();
     while (ld_acquire_gpu(arrive) < target) {
       __nanosleep(256);
-      if (global_ns() - t0 > kWaitTimeoutNs) {
+      if (global_ns() - t0 > limit_ns) {
         set_status(st, ST_TIMEOUT, kWhereActQuant);
         ok = 0;
         break;
@@ -532,7 +533,27 @@ cudaError_t launch_typed(const ActQuantArgs& a, bool cooperative, int sms, cudaS
   return launch_cfg<T, 4, 1024, 1>(a, cooperative, sms, s);
 }
 
+// The failure path of the grid-wide wait without a fault: every block
+// waits for one arrival more than the grid makes, so each one runs out of
+// time, records ST_TIMEOUT and returns.
+__global__ void grid_wait_probe_kernel(unsigned* arrive, DevStatus* st, unsigned long long limit_ns) {
+  grid_wait(arrive, gridDim.x + 1, st, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_grid_wait_probe(DevStatus* st, unsigned* arrive, unsigned long long limit_ns, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grid_wait_probe_kernel, arrive, st, limit_ns);
+}
 
 // Rows up to 32768 columns (one block of 1024 threads, 4 groups of 8 each);
 // longer rows take the separate kernels.

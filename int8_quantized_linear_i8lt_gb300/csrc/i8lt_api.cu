@@ -859,6 +859,18 @@ int i8lt_debug_wait_timeout(int64_t limit_ns, void* ws, size_t ws_bytes, void* s
   return cuda_status(launch_wait_limit(static_cast<DevStatus*>(ws), static_cast<unsigned long long>(limit_ns), s));
 }
 
+int i8lt_debug_grid_wait_timeout(int64_t limit_ns, void* ws, size_t ws_bytes, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 2000000000LL) return I8LT_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < kAlign) return I8LT_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return I8LT_ERR_MISALIGNED;
+  if (int d = check_device()) return d;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, kAlign, s) != cudaSuccess) return I8LT_ERR_CUDA;
+  unsigned* arrive = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + 64);
+  return cuda_status(launch_grid_wait_probe(static_cast<DevStatus*>(ws), arrive,
+                                            static_cast<unsigned long long>(limit_ns), s));
+}
+
 int i8lt_read_device_status(void* ws, int32_t* status, int32_t* outliers, void* stream) {
   if (ws == nullptr) return I8LT_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -52,6 +52,9 @@ cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int
 // bounded grid-wide waits (arrive: a zeroed counter); then (or from the given
 // colmax) the outlier set -- block 0 writes mask, idx and the counts in st --
 // and SCA, Aq, subA and asq as launch_row_quantize.
+// Two blocks of a cooperative launch wait at a grid-wide barrier that one
+// arrival short of complete, with the given limit (a test of the timeout path).
+cudaError_t launch_grid_wait_probe(DevStatus* st, unsigned* arrive, unsigned long long limit_ns, cudaStream_t s);
 bool act_quant_fused_supported(int at, int64_t K);
 cudaError_t launch_act_quant_fused(const void* A, int at, int64_t M, int64_t K, int64_t k_pad, bool enabled,
                                    float thr, bool do_colmax, int64_t cap, int64_t cap_pad, uint32_t* colmax,
