@@ -39,6 +39,7 @@
 // Used for 16-bit A with K a multiple of 8 up to 32768 (16-byte rows that fit
 // the ring); the other inputs take the separate kernels.
 #include <algorithm>
+#include <cstring>
 #include <type_traits>
 
 #include "i8lt_internal.h"
@@ -64,7 +65,7 @@ struct ActQuantArgs {
   DevStatus* st;
   unsigned* arrive;      // grid-wide wait counter (zeroed)
   float* SCA;            // [M]
-  __half* Aq;            // [M, k_pad]
+  void* Aq;              // [M, k_pad] codes: exact fp16 integers (activations) or int8 (weights)
   __half* subA;          // [M, cap_pad]
   uint32_t* asq;         // [ceil(M / 256), nch]
   int nbuf;              // rows in the shared-memory ring
@@ -171,8 +172,11 @@ __device__ __forceinline__ int warp_transpose_sum(int (&x)[G], int lane) {
 
 constexpr int kMaxBufs = 8;   // rows in the shared-memory ring
 
-template <typename T, int G, int NT, int MINB>
+template <typename T, typename CodeT, int G, int NT, int MINB>
 __global__ void __launch_bounds__(NT, MINB) act_quant_fused_kernel(const ActQuantArgs a) {
+  // int8 codes: the weight quantization (no column maxima, no outliers, no
+  // sums of squared codes); fp16 codes: the activations
+  constexpr bool kI8 = std::is_same<CodeT, int8_t>::value;
   extern __shared__ __align__(128) uint8_t ring[];   // a.nbuf row buffers of K 16-bit elements
   __shared__ __align__(8) uint64_t full[kMaxBufs];
   __shared__ int abort_flag;
@@ -365,6 +369,8 @@ __global__ void __launch_bounds__(NT, MINB) act_quant_fused_kernel(const ActQuan
   if (t == 0)
     for (int64_t k = 0; k < issued; ++k) issue(u + k, r1 - 1 - k);
   auto slot = [&](int64_t v) { return ring + static_cast<size_t>(v % nbuf) * buf_bytes; };
+  const uint32_t code_bytes = static_cast<uint32_t>(a.k_pad) * sizeof(CodeT);   // a row of codes
+  auto code_row = [&](int64_t r) { return static_cast<uint8_t*>(a.Aq) + r * code_bytes; };
   constexpr int kSpan = 32 / G;   // lanes that end up holding one group's warp sum (warp_transpose_sum)
   int par = 0;
   int64_t prev = -1;
@@ -400,11 +406,11 @@ __global__ void __launch_bounds__(NT, MINB) act_quant_fused_kernel(const ActQuan
       return;
     }
     if (t == 0 && prev >= 0) {
-      bulk_store(a.Aq + prev * a.k_pad, slot(u + k - 1), buf_bytes);
+      bulk_store(code_row(prev), slot(u + k - 1), code_bytes);
       bulk_commit();
     }
     // the previous row's chunk sums are complete: raise its tile's asq entries
-    if (prev >= 0 && t < a.nch) {
+    if (!kI8 && prev >= 0 && t < a.nch) {
       const int v = chunk_s[par ^ 1][t];
       if (v != 0) atomicMax(a.asq + (prev >> 8) * a.nch + t, static_cast<uint32_t>(v));
       chunk_s[par ^ 1][t] = 0;
@@ -427,7 +433,7 @@ __global__ void __launch_bounds__(NT, MINB) act_quant_fused_kernel(const ActQuan
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         q[j] = __fsub_rn(__fadd_rn(__fmul_rn(__half2float(x[j]), s), 12582912.0f), 12582912.0f);
-        sq = __fmaf_rn(q[j], q[j], sq);
+        if (!kI8) sq = __fmaf_rn(q[j], q[j], sq);
       }
       if (mb[i] != 0u) {
         sq = 0.f;
@@ -438,11 +444,19 @@ __global__ void __launch_bounds__(NT, MINB) act_quant_fused_kernel(const ActQuan
         }
       }
       if (gi < ng_pad) {
-        uint4 o;
-        __half2* o2 = reinterpret_cast<__half2*>(&o);
+        if constexpr (kI8) {   // 8 bytes: the codes as int8, element j in byte j
+          uint32_t wd[2] = {0u, 0u};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o2[j] = __floats2half2_rn(q[2 * j], q[2 * j + 1]);
-        st_shared_v4(cbuf + 16 * gi, o);
+          for (int j = 0; j < 8; ++j)
+            wd[j >> 2] |= (static_cast<uint32_t>(static_cast<int>(q[j])) & 0xFFu) << (8 * (j & 3));
+          *reinterpret_cast<uint2*>(cbuf + 8 * gi) = make_uint2(wd[0], wd[1]);
+        } else {
+          uint4 o;
+          __half2* o2 = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o2[j] = __floats2half2_rn(q[2 * j], q[2 * j + 1]);
+          st_shared_v4(cbuf + 16 * gi, o);
+        }
       }
       sqi[i] = static_cast<int>(sq);
       if (mb[i] != 0u) {   // rare: the outlier columns of the group, in column order
@@ -458,8 +472,10 @@ __global__ void __launch_bounds__(NT, MINB) act_quant_fused_kernel(const ActQuan
     }
     // the warp's sums of the G groups at once; group i of this warp lies in
     // the 1024-column chunk (32 w + i NT) / 128 (NT % 128 == 0)
-    const int tot = warp_transpose_sum<G>(sqi, lane);
-    if ((lane & (kSpan - 1)) == 0 && tot != 0) atomicAdd(&chunk_s[par][(32 * w + (lane / kSpan) * NT) >> 7], tot);
+    if constexpr (!kI8) {
+      const int tot = warp_transpose_sum<G>(sqi, lane);
+      if ((lane & (kSpan - 1)) == 0 && tot != 0) atomicAdd(&chunk_s[par][(32 * w + (lane / kSpan) * NT) >> 7], tot);
+    }
     for (int j = used + t; j < used_pad; j += NT) a.subA[r * a.cap_pad + j] = __float2half_rn(0.f);
     if (t == 0) a.SCA[r] = amax;
     fence_proxy_async_smem();   // this thread's codes, for the bulk store
@@ -476,12 +492,12 @@ __global__ void __launch_bounds__(NT, MINB) act_quant_fused_kernel(const ActQuan
   __syncthreads();   // the last row's codes are written and fenced; its chunk sums are complete
   if (t == 0) {
     if (prev >= 0) {
-      bulk_store(a.Aq + prev * a.k_pad, slot(u + nrows - 1), buf_bytes);
+      bulk_store(code_row(prev), slot(u + nrows - 1), code_bytes);
       bulk_commit();
     }
     bulk_wait_all();
   }
-  if (prev >= 0 && t < a.nch) {
+  if (!kI8 && prev >= 0 && t < a.nch) {
     const int v = chunk_s[par ^ 1][t];
     if (v != 0) atomicMax(a.asq + (prev >> 8) * a.nch + t, static_cast<uint32_t>(v));
   }
@@ -496,9 +512,9 @@ __global__ void __launch_bounds__(NT, MINB) act_quant_fused_kernel(const ActQuan
 // an SM leave, 3 to kMaxBufs rows.
 constexpr int kRingBudget = 200 * 1024;
 
-template <typename T, int G, int NT, int MINB>
+template <typename T, typename CodeT, int G, int NT, int MINB>
 cudaError_t launch_cfg(ActQuantArgs a, bool cooperative, int sms, cudaStream_t s) {
-  const void* fn = reinterpret_cast<const void*>(act_quant_fused_kernel<T, G, NT, MINB>);
+  const void* fn = reinterpret_cast<const void*>(act_quant_fused_kernel<T, CodeT, G, NT, MINB>);
   const int target = MINB;
   const int64_t buf_bytes = static_cast<int64_t>(a.k_pad) * 2;   // a row of fp16 codes
   a.nbuf = static_cast<int>(std::max<int64_t>(3, std::min<int64_t>(kMaxBufs, kRingBudget / target / buf_bytes)));
@@ -516,21 +532,21 @@ cudaError_t launch_cfg(ActQuantArgs a, bool cooperative, int sms, cudaStream_t s
   attr[0].val.cooperative = cooperative ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, act_quant_fused_kernel<T, G, NT, MINB>, a);
+  return cudaLaunchKernelEx(&cfg, act_quant_fused_kernel<T, CodeT, G, NT, MINB>, a);
 }
 
-template <typename T>
+template <typename T, typename CodeT>
 cudaError_t launch_typed(const ActQuantArgs& a, bool cooperative, int sms, cudaStream_t s) {
   const int groups = a.k_pad / 8;
   // four blocks per SM only when every block still gets a few dozen rows
   // (with 2048 rows of 4096 columns they made the launch 24 % slower)
   const bool many_rows = a.M >= 32LL * sms;
   if (groups <= 256 * 2)
-    return many_rows ? launch_cfg<T, 2, 256, 4>(a, cooperative, sms, s) : launch_cfg<T, 2, 256, 2>(a, cooperative, sms, s);
+    return many_rows ? launch_cfg<T, CodeT, 2, 256, 4>(a, cooperative, sms, s) : launch_cfg<T, CodeT, 2, 256, 2>(a, cooperative, sms, s);
   if (groups <= 512 * 2)
-    return many_rows ? launch_cfg<T, 4, 256, 4>(a, cooperative, sms, s) : launch_cfg<T, 2, 512, 2>(a, cooperative, sms, s);
-  if (groups <= 256 * 8) return launch_cfg<T, 8, 256, 2>(a, cooperative, sms, s);
-  return launch_cfg<T, 4, 1024, 1>(a, cooperative, sms, s);
+    return many_rows ? launch_cfg<T, CodeT, 4, 256, 4>(a, cooperative, sms, s) : launch_cfg<T, CodeT, 2, 512, 2>(a, cooperative, sms, s);
+  if (groups <= 256 * 8) return launch_cfg<T, CodeT, 8, 256, 2>(a, cooperative, sms, s);
+  return launch_cfg<T, CodeT, 4, 1024, 1>(a, cooperative, sms, s);
 }
 
 // The failure path of the grid-wide wait without a fault: every block
@@ -591,8 +607,34 @@ cudaError_t launch_act_quant_fused(const void* A, int at, int64_t M, int64_t K, 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool cooperative = do_colmax;   // the grid-wide waits need every block resident
   ProfScope ps(K_ROW_QUANTIZE, s);
-  return at == DT_BF16 ? launch_typed<__nv_bfloat16>(a, cooperative, sms, s)
-                       : launch_typed<__half>(a, cooperative, sms, s);
+  return at == DT_BF16 ? launch_typed<__nv_bfloat16, __half>(a, cooperative, sms, s)
+                       : launch_typed<__half, __half>(a, cooperative, sms, s);
+}
+
+
+// The weight quantization through the same kernel: W [N, K] (16-bit, K % 8
+// == 0, k_pad <= 32768) -> SCB[n] = max_k |fp16(W[n, k])| and CB [N, k_pad]
+// int8 codes rint(fp32(W16) * (127 / SCB[n])), zero in the padding -- the
+// row pass alone (no column maxima, no outliers), each code row stored in
+// bulk from its ring buffer.
+cudaError_t launch_quantize_weight_fused(const void* W, int wt, int64_t N, int64_t K, int64_t k_pad, int8_t* CB,
+                                         float* SCB, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  ActQuantArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.A = W;
+  a.M = N;
+  a.K = static_cast<int>(K);
+  a.k_pad = static_cast<int>(k_pad);
+  a.nch = static_cast<int>(ceil_div(k_pad, 1024));
+  a.SCA = SCB;
+  a.Aq = CB;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  ProfScope ps(K_QUANTIZE_WEIGHT, s);
+  return wt == DT_BF16 ? launch_typed<__nv_bfloat16, int8_t>(a, false, sms, s)
+                       : launch_typed<__half, int8_t>(a, false, sms, s);
 }
 
 }  // namespace i8lt

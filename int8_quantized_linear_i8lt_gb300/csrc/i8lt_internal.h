@@ -52,6 +52,10 @@ cudaError_t launch_row_quantize(const void* A, int at, int64_t M, int64_t K, int
 // bounded grid-wide waits (arrive: a zeroed counter); then (or from the given
 // colmax) the outlier set -- block 0 writes mask, idx and the counts in st --
 // and SCA, Aq, subA and asq as launch_row_quantize.
+// W [N, K] 16-bit -> CB int8 [N, k_pad], SCB [N] by the fused kernel's row
+// pass (K % 8 == 0, k_pad <= 32768; act_quant_fused_supported).
+cudaError_t launch_quantize_weight_fused(const void* W, int wt, int64_t N, int64_t K, int64_t k_pad, int8_t* CB,
+                                         float* SCB, cudaStream_t s);
 // Two blocks of a cooperative launch wait at a grid-wide barrier that one
 // arrival short of complete, with the given limit (a test of the timeout path).
 cudaError_t launch_grid_wait_probe(DevStatus* st, unsigned* arrive, unsigned long long limit_ns, cudaStream_t s);

@@ -833,6 +833,10 @@ cudaError_t launch_staged(int prof_id, const T* A, int64_t M, int64_t K, int64_t
 cudaError_t launch_quantize_weight(const void* W, int wt, int64_t N, int64_t K, int64_t ld, bool vec, int8_t* CB,
                                    float* SCB, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
+  // 16-bit weights with 16-byte rows that fit the ring: the row pass of the
+  // fused activation quantization, each code row stored in bulk
+  if (act_quant_fused_supported(wt, K) && ld == round_up(K, 16))
+    return launch_quantize_weight_fused(W, wt, N, K, ld, CB, SCB, s);
   return dispatch_dt(wt, [&](auto* tag) {
     using T = std::remove_pointer_t<decltype(tag)>;
     if (vec && K * static_cast<int64_t>(sizeof(T)) <= kBulkMaxRowBytes)
