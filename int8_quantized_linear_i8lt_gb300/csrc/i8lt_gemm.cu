@@ -478,14 +478,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMMA) {
     if (rank == 0 && lane == 0) {
       const uint32_t idesc = make_idesc_f16(kPairM, kPairN, false, false);
-      int it = 0, u = 0;
+      const uint64_t desc0 = make_sdesc(smem_u32(smem), 16, 1024, kSwizzle128B);   // stage 0, A, k = 0
+      int it = 0, u = 0, tl = 0;
       bool ok = true;
-      for (int t = cid; t < num_tiles && ok; t += ncl) {
+      for (int t = cid; t < num_tiles && ok; t += ncl, ++tl) {
         int tm, tn;
         tile_coords(t, num_m, num_n, group, tm, tn);
         int per, n_int;
         bool fast;
-        const int units = tile_units(e.plan[tm * num_n + tn], per, n_int, fast);
+        const int units0 = tile_units(e.plan[tm * num_n + tn], per, n_int, fast);
+        // one int8 unit and outliers: the outlier unit accumulates in R's
+        // columns while the int8 unit stays in X, with no drain between them;
+        // R must first be free of the previous tile's output values
+        const bool r_out = OB > 0 && n_int == 1;
+        const int units = r_out ? 1 : units0;
         for (int uu = 0; uu < units && ok; ++uu, ++u) {
           // the epilogues of both CTAs released the accumulator of unit u-1
           if (u > 0 && !mbar_wait_cluster(&bars->acc_empty[0], (u - 1) & 1, abort_flag, e.st, kWhereMMA)) {
@@ -494,22 +500,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const bool is_int = uu < n_int;
-          const int b0 = is_int ? uu * per * kChunkKB : KB;
-          const int b1 = is_int ? min(KB, b0 + per * kChunkKB) : blocks;
-          for (int b = b0; b < b1; ++b, ++it) {
-            const int s = it % kFwdStages;
-            const uint32_t ph = (it / kFwdStages) & 1;
-            if (!mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t a_base = smem_u32(smem + s * kFwdStageBytes);
-            const uint32_t b_base = a_base + kOpBytes;
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              const uint64_t ad = make_sdesc(a_base + k * 32, 16, 1024, kSwizzle128B);
-              const uint64_t bd = make_sdesc(b_base + k * 32, 16, 1024, kSwizzle128B);
-              umma_f16_pair(tmem_X, ad, bd, idesc, (b > b0 || k > 0) ? 1u : 0u);
+          const int b0 = r_out ? 0 : is_int ? uu * per * kChunkKB : KB;
+          const int b1 = r_out ? KB : is_int ? min(KB, b0 + per * kChunkKB) : blocks;
+          // one run of blocks into one accumulator, or (r_out) the int8 blocks
+          // into X and then the outlier blocks into R; each run's loop is kept
+          // free of per-block branches (the issuing thread's latency per block
+          // shows directly in the tile time)
+          for (int seg = 0; seg < (r_out ? 2 : 1) && ok; ++seg) {
+            const int c0 = seg == 0 ? b0 : KB, c1 = seg == 0 ? b1 : blocks;
+            const uint32_t dst = seg == 0 ? tmem_X : tmem_R;
+            if (seg == 1 && tl > 0 &&
+                !mbar_wait_cluster(&bars->acc_empty[1], (tl - 1) & 1, abort_flag, e.st, kWhereMMA)) {
+              ok = false;
+              break;
             }
-            umma_commit_pair_mc(&bars->empty[s], 0x3);
+            for (int b = c0; b < c1; ++b, ++it) {
+              const int s = it % kFwdStages;
+              const uint32_t ph = (it / kFwdStages) & 1;
+              if (!mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereMMA)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t ad0 = desc0 + static_cast<uint64_t>(s * (kFwdStageBytes >> 4));
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k) {
+                const uint64_t ad = ad0 + 2 * k;
+                const uint64_t bd = ad0 + (kOpBytes >> 4) + 2 * k;
+                umma_f16_pair(dst, ad, bd, idesc, (b > c0 || k > 0) ? 1u : 0u);
+              }
+              umma_commit_pair_mc(&bars->empty[s], 0x3);
+            }
           }
           if (ok) umma_commit_pair_mc(&bars->acc_full[0], 0x3);
         }
@@ -524,6 +542,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int col0 = ((warp - kWarpEpi0) >> 2) * 128;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t acc_empty0 = mapa_shared(&bars->acc_empty[0], 0);
+    const uint32_t acc_empty1 = mapa_shared(&bars->acc_empty[1], 0);   // R free again, once per tile
     const bool vec = (e.N % 8) == 0;
     int u = 0;
     bool ok = true;
@@ -557,7 +576,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool row_ok = m < e.M;
       int per, n_int;
       bool small;   // every partial sum of the tile's units below 2^22: the fast exact conversion
-      const int units = tile_units(e.plan[tm * num_n + tn], per, n_int, small);
+      const int units0 = tile_units(e.plan[tm * num_n + tn], per, n_int, small);
+      const bool r_out = OB > 0 && n_int == 1;   // as the MMA: the int8 unit in X, the outliers in R
+      const int units = r_out ? 1 : units0;
       for (int uu = 0; uu < units; ++uu, ++u) {
         // all 256 epilogue threads agree, so none is left at a named barrier
         if (!named_bar_and(kBarEpi, kEpiThreads,
@@ -588,16 +609,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int gc = 0; gc < 128; gc += 16) {
             uint32_t r[16], x[16];
-            tmem_ld16_nowait(tmem_X + lane_off + col0 + gc, x);
-            if (r_live) tmem_ld16_nowait(tmem_R + lane_off + col0 + gc, r);
-            tmem_ld_wait_tie16(x, r);
-            if (!has_o) {
-              chunk_to_int(x, r, !r_live, small);   // the last int8 chunk is still in X
+            if (r_out) {   // r: the int8 unit from X; x: the outlier unit from R
+              uint32_t xi[16];
+              tmem_ld16_nowait(tmem_X + lane_off + col0 + gc, xi);
+              tmem_ld16_nowait(tmem_R + lane_off + col0 + gc, x);
+              tmem_ld_wait_tie16(xi, x);
+              chunk_to_int(xi, r, true, small);
+            } else {
+              tmem_ld16_nowait(tmem_X + lane_off + col0 + gc, x);
+              if (r_live) tmem_ld16_nowait(tmem_R + lane_off + col0 + gc, r);
+              tmem_ld_wait_tie16(x, r);
+              if (!has_o) {
+                chunk_to_int(x, r, !r_live, small);   // the last int8 chunk is still in X
 #pragma unroll
-              for (int j = 0; j < 16; ++j) x[j] = 0u;   // no outlier term
-            } else if (!r_live) {
+                for (int j = 0; j < 16; ++j) x[j] = 0u;   // no outlier term
+              } else if (!r_live) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) r[j] = 0;
+                for (int j = 0; j < 16; ++j) r[j] = 0;
+              }
             }
             const int nb = n0 + col0 + gc;
             if (e.acc_i32 != nullptr && row_ok && nb < e.N) {
@@ -659,6 +688,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
           }
+          // phase 2 has read R: the next tile's outlier unit may accumulate there
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(acc_empty1);
         }
       }
     }
