@@ -97,9 +97,10 @@ constexpr int kCtaRows = 128;  // rows of A and of B that each CTA stages
 enum { kWhereProducer = 1, kWhereCvt = 2, kWhereMMA = 3, kWhereEpi = 4, kWhereTeardown = 5 };
 
 struct __align__(8) Barriers {
-  uint64_t full[kMaxStages];      // forward: both CTAs' copies of stage s landed (even CTA);
-                                  // backward: this CTA's copies of stage s landed
-  uint64_t ready[kMaxStages];     // backward, even CTA: both CTAs' operands of stage s in place
+  uint64_t full[kMaxStages];      // forward and materialized backward, even CTA: both CTAs' copies of
+                                  // stage s landed
+  uint64_t ready[kMaxStages];     // fused backward, even CTA: both CTAs' operands of stage s in place
+                                  // (the G16 copies and the converted tiles: the MMA's one wait a stage)
   uint64_t cvt_done[kMaxStages];  // backward, odd CTA: its converters finished stage s
   uint64_t empty[kMaxStages];     // the pair's MMAs finished reading stage s
   uint64_t i8_full[kI8Stages];    // backward: this CTA's int8 weight tile j landed
@@ -289,7 +290,9 @@ __device__ __forceinline__ void split_tile(int t, int full, int num_m, int num_k
 __device__ __forceinline__ void init_barriers(Barriers* bars, int epi_warps) {
   for (int s = 0; s < kMaxStages; ++s) {
     mbar_init(&bars->full[s], 1);
-    mbar_init(&bars->ready[s], kCvtWarps + 1);   // the even CTA's converters + one relay arrival
+    // backward, fused: the even CTA's converters, one relay arrival and the
+    // producer's arrival with both CTAs' G16 bytes
+    mbar_init(&bars->ready[s], kCvtWarps + 2);
     mbar_init(&bars->cvt_done[s], kCvtWarps);
     mbar_init(&bars->empty[s], 1);
   }
@@ -950,7 +953,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
     // ---- G16 tiles (and WdqT tiles when materialized): both CTAs' copies
     // complete on the even CTA's barrier
     if (lane == 0) {
-      const uint32_t full0 = mapa_shared(&bars->full[0], 0);
+      // fused: the G16 copies complete on ready[s], the one barrier the MMA
+      // waits on; materialized: on full[s]
+      uint64_t* const land = kFused ? bars->ready : bars->full;
+      const uint32_t full0 = mapa_shared(&land[0], 0);
       int it = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl) {
@@ -963,7 +969,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
           const uint32_t ph = (it / Geo::kStages) & 1;
           if (!mbar_wait(&bars->empty[s], ph ^ 1, abort_flag, e.st, kWhereProducer)) { ok = false; break; }
           // the even CTA expects both CTAs' bytes of this stage
-          if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], 2 * (kFused ? nsub : 2) * kOpBytes);
+          if (rank == 0) mbar_arrive_expect_tx(&land[s], 2 * (kFused ? nsub : 2) * kOpBytes);
           const uint32_t full_s = full0 + static_cast<uint32_t>(s) * 8u;
           uint8_t* st_base = smem + s * Geo::kStageBytes;
           if (!kFused) tma_load_2d_pair(st_base, &g.tmWT, b * kBK, k_cta, full_s);   // WdqT[k:+128][n:+64]
@@ -974,7 +980,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       }
       if (rank == 0)
         for (int j = max(0, it - Geo::kStages); j < it; ++j)
-          mbar_wait_teardown(&bars->full[j % Geo::kStages], (j / Geo::kStages) & 1, e.st);
+          mbar_wait_teardown(&land[j % Geo::kStages], (j / Geo::kStages) & 1, e.st);
     }
   } else if (warp == kWarpI8Producer) {
     // ---- weight tiles, this CTA's own ring: int8 CB[n:+64][k:+128]; 4-bit,
@@ -1029,6 +1035,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
       // (64 k) 1024 B apart, K atoms (8 n) 2048 B apart.  Materialized and
       // 4-bit forward: K-major like B.  ab_fmt: bf16 operands.
       const uint32_t idesc = make_idesc_f16(kPairM, kPairN, Geo::kAmn, false) | e.ab_fmt;
+      // stage 0's descriptors at k = 0 (the start-address field, in 16-byte
+      // units, then takes the offsets within shared memory below 256 KB)
+      const uint32_t base0 = smem_u32(smem);
+      const uint64_t adesc0 = Geo::kAmn ? make_sdesc(base0, 1024, 2048, kSwizzle128B)
+                                        : make_sdesc(base0, 16, 1024, kSwizzle128B);
+      const uint64_t bdesc0 = make_sdesc(base0 + kOpBytes, 16, 1024, kSwizzle128B);
       int it = 0, tl = 0;
       bool ok = true;
       for (int t = cid; t < num_tiles && ok; t += ncl, ++tl) {
@@ -1045,21 +1057,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kBwdThreads, 1)
         for (int b = 0; b < NB; ++b, ++it) {
           const int s = it % Geo::kStages;
           const uint32_t ph = (it / Geo::kStages) & 1;
-          if (!mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereMMA) ||
-              (kFused && !mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA))) {
+          if (kFused ? !mbar_wait_cluster(&bars->ready[s], ph, abort_flag, e.st, kWhereMMA)
+                     : !mbar_wait(&bars->full[s], ph, abort_flag, e.st, kWhereMMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + s * Geo::kStageBytes);
+          const uint64_t st16 = static_cast<uint64_t>(s * (Geo::kStageBytes >> 4));   // the stage, 16-byte units
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = Geo::kAmn ? make_sdesc(a_base + k * 4096, 1024, 2048, kSwizzle128B)
-                                          : make_sdesc(a_base + k * 32, 16, 1024, kSwizzle128B);
+            const uint64_t ad = adesc0 + st16 + (Geo::kAmn ? k * (4096 >> 4) : 2 * k);
 #pragma unroll
             for (int u = 0; u < Geo::kSub; ++u) {   // token sub-tile u -> accumulator columns [256 u, 256 u + 256)
               if (u >= nsub) break;
-              const uint64_t bd = make_sdesc(a_base + (1 + u) * kOpBytes + k * 32, 16, 1024, kSwizzle128B);
+              const uint64_t bd = bdesc0 + st16 + u * (kOpBytes >> 4) + 2 * k;
               umma_f16_pair(d + static_cast<uint32_t>(u) * 256u, ad, bd, idesc, (b > 0 || k > 0) ? 1u : 0u);
             }
           }
