@@ -604,8 +604,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_st_wait();
         } else {
           // last unit of the tile, phase 1: the fp32 output values before the
-          // residual, written over the running sum in R, so that X can be
-          // handed back to the MMA before the slower stores of phase 2
+          // residual, written into R (over the running sum, or over the
+          // outlier unit's sums), so that X can be handed back to the MMA
+          // before the slower stores of phase 2
           const bool has_o = OB > 0;
           const bool r_live = has_o ? (n_int > 0) : (n_int > 1);
           const float rs = row_ok ? __fmul_rn(e.SCA[m], 1.0f / 16129.0f) : 0.f;
