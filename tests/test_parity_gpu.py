@@ -191,6 +191,36 @@ def test_accumulation_plan():
     assert fast.any() and (fast == 0).any()
 
 
+def test_accumulation_plan_with_outliers():
+    """The same mix of accumulation plans with outlier columns.  A tile whose
+    int8 reduction is one unit keeps it in the fp32 columns while the outlier
+    unit accumulates in the running-sum columns; the other tiles drain between
+    their units.  Both kinds run in one launch, with the running-sum columns
+    handed between them tile after tile: the int32 accumulator stays exact and
+    the output within tolerance."""
+    M, K, N = 700, 5000, 600
+    g = torch.Generator().manual_seed(31)
+    A = torch.randn(M, K, generator=g)
+    A[:256] = 1.0                                   # tile 0: every code 127
+    A[512:] = (torch.rand(M - 512, K, generator=g) < 0.01) * torch.randn(M - 512, K, generator=g)
+    heavy = torch.randperm(K, generator=g)[:6]
+    A[:, heavy] *= 20.0                             # outlier columns in every row tile
+    A = A.half()
+    Wf = (torch.randn(N, K, generator=g) * 0.02).half()
+    Wf[:256] = 0.25                                 # weight tile 0: every code 127
+    Wf[512:] = Wf[512:] * (torch.rand(N - 512, K, generator=g) < 0.02).half()
+    CB, SCB = I.quantize_weight(Wf.to(DEV))
+    CB_ref, SCB_ref = check_weight(CB, SCB, Wf, K)
+    res = gpu_forward(A.to(DEV), CB, SCB, K, None, 6.0)
+    ref = O.forward(to_np(A), O.F16, CB_ref, SCB_ref, threshold=6.0)
+    check_forward_stages(res, ref)
+    assert len(ref["idx"]) >= 6
+    plan = to_np(res["plan"]).astype(np.int64)
+    L = plan & 0xFFFF
+    nch = (res["k_pad"] + 1023) // 1024
+    assert (L >= nch).any() and (L < nch).any()
+
+
 def test_max_k_accumulator():
     """K at the int32 bound: every product +127^2, |Cacc| = 2147479576."""
     M, K, N = 128, _lib.I8LT_MAX_K, 256
