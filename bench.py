@@ -44,10 +44,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 MEASURED_TRAFFIC = {
     "workload": "proj_8192x28672",
     "sources": {"int8_quantized_linear_i8lt_gb300/csrc/i8lt_gemm.cu":
-                "932f7bb889d3f8fc6499698870a38469acf5750a7afb530a6916e65fc05a9e03",
+                "db72aec6e1193a23043428cf17ce2e294e8fb2466bc09ac14163773552107a15",
                 "int8_quantized_linear_i8lt_gb300/csrc/i8lt_common.cuh":
                 "cc2fb6fa161ef5430ebd36ed4e9af7f9a5113376b51d4738964ca1dbdcce7d42"},
-    "bytes_per_launch": {"fwd_gemm": 8.16e9, "bwd_gemm": 5.74e9},
+    "bytes_per_launch": {"fwd_gemm": 8.07e9, "bwd_gemm": 5.64e9},
 }
 
 
