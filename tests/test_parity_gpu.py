@@ -89,9 +89,14 @@ SMALL = [
     (140, 200, 300, torch.bfloat16, 0.05, 10.0, 6.0),     # many outliers (4 outlier blocks)
     (600, 16, 4, torch.float32, 0.0, 1.0, math.inf),      # the tiny MLP's second layer shape
     # more tiles than CTA pairs in every GEMM: several tiles per pair (both
-    # accumulators of the materialized backward, the staggered halves of the
-    # fused one across tile boundaries, its split last round)
+    # accumulators of the materialized backward, the fused one's single
+    # accumulator handed from tile to tile, its split last round)
     (2100, 5120, 264, torch.float16, 0.002, 15.0, 6.0),
+    # the longest rows of the one-launch quantization (1024 threads x 4
+    # groups of 8) and one group longer, which takes the separate kernels;
+    # the weight quantization meets the same boundary
+    (200, 32768, 264, torch.float16, 0.001, 15.0, 6.0),
+    (200, 32776, 264, torch.bfloat16, 0.001, 15.0, 6.0),
 ]
 
 
