@@ -260,7 +260,8 @@ def kernel_bytes(L, name):
         "colmax": s.M * s.K * a + s.K * 4,
         # the codes count as int8, one byte each, whatever form the kernel stores
         "row_quantize": reads * s.M * s.K * a + s.M * kp + s.M * 4 + s.M * cap_pad * 2,
-        "gradout_prepass": s.M * s.N * a,
+        # it runs where the GEMM needs an fp16 copy of G: reads G, writes the copy
+        "gradout_prepass": s.M * s.N * a + s.M * ((s.N + 7) // 8 * 8) * 2,
         "build_subB": s.N * cap_pad * 3,
         "widen_codes": s.N * kp * 3,
         "dequant_weight": s.N * kp + kp * ((s.N + 7) // 8 * 8) * 2 + s.N * 4,
