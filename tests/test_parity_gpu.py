@@ -305,20 +305,21 @@ def test_repeat_calls_identical():
     assert torch.equal(b1.view(torch.int16), b2.view(torch.int16))
 
 
-@pytest.mark.parametrize("M,N,K", [(4096, 11008, 4096), (8192, 4096, 11008)])
-def test_fused_backward_repeats_bit_identical(M, N, K):
+@pytest.mark.parametrize("M,N,K,runs", [(4096, 11008, 4096, 12), (8192, 4096, 11008, 12), (16384, 28672, 8192, 20)])
+def test_fused_backward_repeats_bit_identical(M, N, K, runs):
     """The odd CTA of a pair hands its converted weight tiles to the even
     CTA's MMA through a cluster-scope release, on the same barrier that the G
     copies complete on.  A hand-over that ordered less would let a stage be
     read before its tile is complete, which shows as runs that differ.
-    Twelve runs over several rounds of pair tiles must give the same bytes."""
+    Repeated runs over several rounds of pair tiles, up to the projection
+    workload's first layer, must give the same bytes."""
     g = torch.Generator().manual_seed(7)
     G = torch.randn(M, N, generator=g).half().to(DEV)
     Wf = (torch.randn(N, K, generator=g) * 0.02).half().to(DEV)
     CB, SCB = I.quantize_weight(Wf)
     ref, ref_b = I.backward_input(G, CB, SCB, K, bias_dtype=torch.float16, fused=True)
     ref, ref_b = ref.clone(), ref_b.clone()
-    for _ in range(11):
+    for _ in range(runs - 1):
         gA, gb = I.backward_input(G, CB, SCB, K, bias_dtype=torch.float16, fused=True)
         assert torch.equal(gA.view(torch.int16), ref.view(torch.int16))
         assert torch.equal(gb.view(torch.int16), ref_b.view(torch.int16))
