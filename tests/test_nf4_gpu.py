@@ -115,6 +115,22 @@ def test_repeat_calls_identical_and_empty_batch():
     assert I.nf4_backward_input(torch.empty(0, N, dtype=torch.bfloat16, device=DEV), packed, absmax, K).shape == (0, K)
 
 
+def test_fused_matmuls_repeat_bit_identical():
+    """The 4-bit matmuls hand the odd CTA's decoded weight tiles to the even
+    CTA's MMA the same way as the int8 backward: repeated runs at the 7B MLP's
+    first layer (several rounds of pair tiles) must give the same bytes."""
+    M, K, N = 8192, 4096, 11008
+    Wf = _weight(N, K, torch.bfloat16, 21)
+    packed, absmax = I.nf4_quantize(Wf.to(DEV))
+    A = W.normal((M, K), 1.0, 22, torch.bfloat16, DEV)
+    G = W.normal((M, N), 1.0, 23, torch.bfloat16, DEV)
+    y0 = I.nf4_forward(A, packed, absmax, K).clone()
+    g0 = I.nf4_backward_input(G, packed, absmax, K).clone()
+    for _ in range(7):
+        assert torch.equal(I.nf4_forward(A, packed, absmax, K), y0)
+        assert torch.equal(I.nf4_backward_input(G, packed, absmax, K), g0)
+
+
 def test_argument_errors():
     K, N = 100, 64                               # K not a multiple of 8
     Wf = _weight(N, K, torch.bfloat16, 11)
