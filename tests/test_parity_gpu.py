@@ -325,6 +325,24 @@ def test_fused_backward_repeats_bit_identical(M, N, K, runs):
         assert torch.equal(gb.view(torch.int16), ref_b.view(torch.int16))
 
 
+def test_forward_repeats_bit_identical():
+    """The forward hands the running-sum columns from one tile's stores to the
+    next tile's outlier unit through a barrier of its own.  Repeated forwards
+    of the projection workload's first layer (one-unit tiles with outlier
+    columns, many tiles per pair) must give the same bytes."""
+    spec = W.WORKLOADS["proj_8192x28672"].layers[0]
+    wl = W.Workload("case", "", (spec,), w_dtype=spec.dtype)
+    A = W.activation(spec, 3).to(DEV)
+    Wf, b, _ = W.layer_tensors(wl, 0, 3)
+    CB, SCB = I.quantize_weight(Wf.to(DEV))
+    b = b.to(DEV)
+    o0, ws = I.forward(A, CB, SCB, spec.K, b, spec.threshold)
+    o0 = o0.clone()
+    for _ in range(9):
+        o, _ = I.forward(A, CB, SCB, spec.K, b, spec.threshold, ws=ws)
+        assert torch.equal(o.view(torch.int16), o0.view(torch.int16))
+
+
 # ---------------------------------------------------------------------------
 # the workloads
 # ---------------------------------------------------------------------------
