@@ -1073,6 +1073,118 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_aux_kernels(args):
+    """The library's kernels that the bench step does not launch, each on an
+    input larger than L2 (where it streams one): the quantization paths for
+    fp32 activations and for rows longer than the one-launch kernel takes, the
+    16-bit copy of a bf16 grad_output, the materialized schedules' prepasses,
+    the SiLU of the MLP block, the 4-bit quantize and dequantize kernels, the
+    absmax double quantization, the weight gradient's column passes and the
+    fallback weight quantization.  Each case builds its inputs, runs once
+    untimed and once with the library's CUDA-event records, and frees them
+    (so that an ncu capture holds at most about a GB on the device): one JSON
+    line of milliseconds per kernel and case."""
+    import int8_quantized_linear_i8lt_gb300 as I
+    from int8_quantized_linear_i8lt_gb300 import _lib
+    _lib.load()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    F = I.functional
+    g = torch.Generator(device=device).manual_seed(11)
+
+    def rnd(shape, dtype, std=1.0):
+        return (torch.randn(shape, generator=g, device=device) * std).to(dtype)
+
+    def weight(N, K):
+        return I.quantize_weight(rnd((N, K), torch.float16, 0.02))
+
+    def fwd(M, K, N, dt):
+        A = rnd((M, K), dt)
+        A[:, :16] *= 20.0                                 # outlier columns
+        CB, SCB = weight(N, K)
+        return lambda: F.forward(A, CB, SCB, K, None, 6.0)
+
+    def bwd_bf16():
+        G = rnd((16384, 8192), torch.bfloat16)
+        CB, SCB = weight(8192, 1024)
+        return lambda: F.backward_input(G, CB, SCB, 1024, bias_dtype=torch.bfloat16)
+
+    def bwd_materialized():
+        G = rnd((256, 16384), torch.float16)
+        CB, SCB = weight(16384, 8192)
+        ws = F.backward_workspace(256, 16384, torch.float16, device, K=8192)
+        return lambda: F.backward_input(G, CB, SCB, 8192, ws=ws, fused=False)
+
+    def silu_fwd():
+        H = rnd((16384, 8192), torch.float16)
+        return lambda: F.silu(H)
+
+    def silu_bwd():
+        H = rnd((16384, 8192), torch.float16)
+        Gs = rnd((16384, 8192), torch.float16)
+        return lambda: F.silu_backward(Gs, H)
+
+    def nf4(kind):
+        W4 = rnd((8192, 16384), torch.bfloat16, 0.02)
+        if kind == "quantize":
+            return lambda: I.nf4_quantize(W4)
+        packed, absmax = I.nf4_quantize(W4)
+        del W4
+        if kind == "forward":
+            A4 = rnd((256, 16384), torch.bfloat16)
+            return lambda: F.nf4_forward(A4, packed, absmax, 16384, materialized=True)
+        if kind == "input_grad":
+            G4 = rnd((256, 8192), torch.bfloat16)
+            return lambda: F.nf4_backward_input(G4, packed, absmax, 16384, materialized=True)
+        if kind == "dq":
+            return lambda: F.double_quantize_absmax(absmax)
+        dq = F.double_quantize_absmax(absmax)
+        return lambda: F.dequantize_absmax(*dq)
+
+    def wgrad():
+        Gw = rnd((8192, 8192), torch.float16)
+        Aw = rnd((8192, 8192), torch.float16)
+        return lambda: F.grad_weight(Gw, Aw)
+
+    def wq32():
+        W32 = rnd((8192, 8192), torch.float32, 0.02)
+        return lambda: I.quantize_weight(W32)
+
+    cases = [
+        ("fp32 activations 8192 x 8192 (separate quantization kernels, bulk rows)",
+         lambda: fwd(8192, 8192, 256, torch.float32)),
+        ("fp32 activations 2048 x 32768 (staged rows)", lambda: fwd(2048, 32768, 256, torch.float32)),
+        ("fp16 activations 2048 x 57344 (rows past the staged kernel)", lambda: fwd(2048, 57344, 256, torch.float16)),
+        ("bf16 grad_output 16384 x 8192 (fp16 copy and grad_bias sums)", bwd_bf16),
+        ("materialized backward, weight 16384 x 8192 (dequantized weight prepass)", bwd_materialized),
+        ("SiLU forward 16384 x 8192", silu_fwd),
+        ("SiLU backward 16384 x 8192", silu_bwd),
+        ("NF4 quantize 8192 x 16384", lambda: nf4("quantize")),
+        ("NF4 forward, materialized (dequantize 8192 x 16384)", lambda: nf4("forward")),
+        ("NF4 input gradient, materialized (transposed dequantize 8192 x 16384)", lambda: nf4("input_grad")),
+        ("absmax double quantization (8192 x 256 values)", lambda: nf4("dq")),
+        ("absmax decode (8192 x 256 values)", lambda: nf4("decode")),
+        ("weight gradient 8192 x 8192 x 8192 (column maxima, column quantization, tile maxima)", wgrad),
+        ("fp32 weight quantization 8192 x 8192 (bulk rows)", wq32),
+    ]
+    out = []
+    for name, make in cases:
+        fn = make()
+        fn()
+        torch.cuda.synchronize()
+        _lib.i8lt_profile_start(1 << 12)
+        fn()
+        torch.cuda.synchronize()
+        _, recs, _ = _lib.i8lt_profile_stop(1 << 12)
+        ms = {}
+        for n, t in recs:
+            ms[n] = round(ms.get(n, 0.0) + t, 4)
+        out.append({"case": name, "ms": ms})
+        del fn
+        torch.cuda.empty_cache()
+    print(json.dumps({"aux_kernels": out, "device": torch.cuda.get_device_name(device)}), flush=True)
+
+
 def run_nf4_only(args):
     """The NF4 section of the bench line on its own (profiling runs of the
     4-bit matmuls): W warm-up steps, then K timed steps."""
@@ -1102,10 +1214,14 @@ def main(argv=None):
                          "(strong scaling); none: every rank runs its own replica (weak scaling)")
     ap.add_argument("--nf4-only", action="store_true",
                     help="time only the NF4 weight-only layers (qlora_mlp_7b_nf4) and print their line")
+    ap.add_argument("--aux-kernels", action="store_true",
+                    help="run each kernel outside the bench step once, on inputs larger than L2 (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.nf4_only:
+    if args.aux_kernels:
+        run_aux_kernels(args)
+    elif args.nf4_only:
         run_nf4_only(args)
     elif args.impl == "reference":
         run_reference(args)
