@@ -121,6 +121,11 @@ __global__ void __launch_bounds__(256) nf4_quantize_kernel(const T* __restrict__
                                                            uint8_t* __restrict__ packed,
                                                            float* __restrict__ absmax) {
   constexpr uint32_t kZero = kFp4 ? 0u : 7u;   // the code of the zero level
+  // NF4: the 15 level midpoints in shared memory for a binary search (each
+  // lane indexes its own midpoints)
+  __shared__ float mid_s[16];
+  if (threadIdx.x < 15) mid_s[threadIdx.x] = c.mid[threadIdx.x];
+  __syncthreads();
   const int64_t gpr = row_bytes / 4;   // groups of 8 per row (a multiple of 8)
   const int64_t total = N * gpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -155,8 +160,12 @@ __global__ void __launch_bounds__(256) nf4_quantize_kernel(const T* __restrict__
           for (int j = 0; j < 7; ++j) code += (a > c.mid[j] || (a == c.mid[j] && ((c.tie_up >> j) & 1u))) ? 1u : 0u;
           if (xn < 0.f && code != 0u) code |= 8u;
         } else {
-#pragma unroll
-          for (int j = 0; j < 15; ++j) code += xn > c.mid[j] ? 1u : 0u;
+          // the number of midpoints below xn (they ascend), by halving: the
+          // same count as comparing with all fifteen
+          code = xn > mid_s[7] ? 8u : 0u;
+          code += xn > mid_s[code + 3] ? 4u : 0u;
+          code += xn > mid_s[code + 1] ? 2u : 0u;
+          code += xn > mid_s[code] ? 1u : 0u;
         }
       }
       // byte i / 2 holds elements (2j, 2j + 1) as (high, low) nibbles
@@ -171,6 +180,11 @@ __global__ void __launch_bounds__(256) nf4_dequantize_kernel(const uint8_t* __re
                                                              const float* __restrict__ absmax, int64_t N, int64_t K,
                                                              int64_t row_bytes, int nblk, Nf4Tables c,
                                                              bool vec, OutT* __restrict__ out) {
+  // the levels in shared memory: indexed by each lane's own code (a
+  // parameter-space table indexed per lane would serialize the warp)
+  __shared__ float lv_s[16];
+  if (threadIdx.x < 16) lv_s[threadIdx.x] = c.lv[threadIdx.x];
+  __syncthreads();
   const int64_t gpr = row_bytes / 4;
   const int64_t total = N * gpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -185,7 +199,7 @@ __global__ void __launch_bounds__(256) nf4_dequantize_kernel(const uint8_t* __re
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t code = (word >> (8 * (i >> 1) + ((i & 1) ? 0 : 4))) & 15u;
-      o[i] = from_float<OutT>(__fmul_rn(c.lv[code], am));
+      o[i] = from_float<OutT>(__fmul_rn(lv_s[code], am));
     }
     OutT* dst = out + n * K + k0;
     if (vec && k0 + 8 <= K) {   // 16 or 32 bytes at an aligned address
