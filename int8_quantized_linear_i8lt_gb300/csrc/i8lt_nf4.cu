@@ -29,6 +29,8 @@
 #include <cmath>
 #include <mutex>
 
+#include <type_traits>
+
 #include "i8lt_internal.h"
 
 namespace i8lt {
@@ -175,6 +177,26 @@ __global__ void __launch_bounds__(256) nf4_quantize_kernel(const T* __restrict__
   }
 }
 
+// Two fp32 levels times the block's absmax (one packed IEEE multiply: the
+// same rounding as two scalar ones), rounded to a 16-bit pair, e0 in the low
+// half.
+template <bool kBf16>
+__device__ __forceinline__ uint32_t levels_times_absmax(float e0, float e1, float am) {
+  uint32_t out;
+  if (kBf16) {
+    asm("{\n .reg .b64 x, a, p;\n .reg .b32 lo, hi;\n mov.b64 x, {%1, %2};\n mov.b64 a, {%3, %3};\n"
+        " mul.rn.f32x2 p, x, a;\n mov.b64 {lo, hi}, p;\n cvt.rn.bf16x2.f32 %0, hi, lo;\n}"
+        : "=r"(out)
+        : "f"(e0), "f"(e1), "f"(am));
+  } else {
+    asm("{\n .reg .b64 x, a, p;\n .reg .b32 lo, hi;\n mov.b64 x, {%1, %2};\n mov.b64 a, {%3, %3};\n"
+        " mul.rn.f32x2 p, x, a;\n mov.b64 {lo, hi}, p;\n cvt.rn.f16x2.f32 %0, hi, lo;\n}"
+        : "=r"(out)
+        : "f"(e0), "f"(e1), "f"(am));
+  }
+  return out;
+}
+
 template <typename OutT>
 __global__ void __launch_bounds__(256) nf4_dequantize_kernel(const uint8_t* __restrict__ packed,
                                                              const float* __restrict__ absmax, int64_t N, int64_t K,
@@ -196,10 +218,19 @@ __global__ void __launch_bounds__(256) nf4_dequantize_kernel(const uint8_t* __re
     const uint32_t word = *reinterpret_cast<const uint32_t*>(packed + n * row_bytes + kg * 4);
     const float am = absmax[n * nblk + (kg >> 3)];
     OutT o[8];
+    if constexpr (sizeof(OutT) == 2) {   // byte j: element 2j in the high nibble, 2j + 1 in the low
+      uint32_t* w = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t code = (word >> (8 * (i >> 1) + ((i & 1) ? 0 : 4))) & 15u;
-      o[i] = from_float<OutT>(__fmul_rn(lv_s[code], am));
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t byte = (word >> (8 * j)) & 0xFFu;
+        w[j] = levels_times_absmax<std::is_same<OutT, __nv_bfloat16>::value>(lv_s[byte >> 4], lv_s[byte & 15u], am);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t code = (word >> (8 * (i >> 1) + ((i & 1) ? 0 : 4))) & 15u;
+        o[i] = from_float<OutT>(__fmul_rn(lv_s[code], am));
+      }
     }
     OutT* dst = out + n * K + k0;
     if (vec && k0 + 8 <= K) {   // 16 or 32 bytes at an aligned address
